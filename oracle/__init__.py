@@ -1,0 +1,31 @@
+"""CPU oracle for fused operator-group execution and tensor-fusion packing.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports this package:
+only the tests, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` call it.  It shares no code, table
+or constant with the CUDA library; the only module both sides use is
+``workloads`` (seeded input generators, no arithmetic of the method).
+
+It is deliberately plain and slow: every operator runs on its own, in
+float64, and rounds its result to float32; the pattern-kind table, the
+post-dominator tree, the fusion rules and the pack layout are each written
+out from the passages they cite:
+
+* ``kinds``     -- OpPatternKind values and the operator table
+                   (TVM "Operator Fusion", Operator Pattern Classification).
+* ``postdom``   -- immediate post-dominators by LCA on the DAG and the path
+                   pattern (TVM, FuseOps > Algorithm, steps 1-2).
+* ``partition`` -- CheckPath / CommitFuse with union-find, phases 0 and 1,
+                   and the constraints (TVM, FuseOps > Algorithm step 3,
+                   Fusion rules).
+* ``execute``   -- unfused op-by-op execution (the semantics fusion must keep:
+                   DisCo, Introduction, on what op fusion changes).
+* ``pack``      -- tensor-fusion layout, bf16 round-to-nearest-even, pack and
+                   unpack (DisCo, Introduction, on tensor fusion).
+
+Parity status: every function here is pinned by tests under ``tests/``
+(``-m "not gpu"``) against brute force, closed forms, worked examples from the
+pages or library routines, except the long random-DAG numerics, which only the
+oracle itself defines ("parity unpinned" beyond per-op pins).
+"""
+from . import kinds, postdom, partition, execute, pack  # noqa: F401
