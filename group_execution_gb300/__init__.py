@@ -1,0 +1,193 @@
+"""Fused operator-group execution and tensor-fusion packing on one GB300.
+
+A thin Python layer over libgroupexec.so (C ABI in include/groupexec.h):
+
+* ``Graph``  -- build a dataflow graph of operators (node i = i-th operator);
+* ``Plan``   -- FuseOps-style grouping of a graph, one CUDA kernel per group
+                (``launch_group``) or per operator (``launch_unfused``);
+* ``TensorFusion`` -- pack many float32 gradients into one bf16 fusion buffer
+                and unpack them again, one kernel each.
+
+PyTorch supplies device memory and streams only; every step runs in the
+library's kernels.  There is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+from . import _lib
+from ._lib import FgError, OPCODES, EXEC_KINDS, FG_F32, FG_BF16  # noqa: F401
+
+__all__ = ["Graph", "Plan", "TensorFusion", "FgError", "OPCODES", "graph_from_spec"]
+
+
+def _i32a(xs):
+    return (C.c_int32 * max(1, len(xs)))(*xs)
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return C.c_void_p(stream)
+    return C.c_void_p(stream.cuda_stream)
+
+
+class Graph:
+    def __init__(self):
+        self.lib = _lib.load()
+        self.h = C.c_void_p()
+        _lib.check(self.lib.fg_graph_create(C.byref(self.h)))
+        self.shapes = []
+        self.dtypes = []
+
+    def __del__(self):
+        h = getattr(self, "h", None)
+        if h:
+            self.lib.fg_graph_destroy(h)
+            self.h = None
+
+    def input(self, shape, dtype="f32") -> int:
+        dt = FG_BF16 if dtype == "bf16" else FG_F32
+        shp = (C.c_int64 * len(shape))(*shape)
+        vid = C.c_int32()
+        _lib.check(self.lib.fg_graph_add_input(self.h, dt, len(shape), shp, C.byref(vid)))
+        self.shapes.append(tuple(shape))
+        self.dtypes.append(dtype)
+        return vid.value
+
+    def op(self, name, args, attrs=()) -> int:
+        vid = C.c_int32()
+        at = (C.c_float * max(1, len(attrs)))(*attrs)
+        _lib.check(self.lib.fg_graph_add_op(self.h, OPCODES[name], len(args), _i32a(args), len(attrs), at,
+                                            C.byref(vid)))
+        dt, nd, shp = C.c_int32(), C.c_int32(), (C.c_int64 * 2)()
+        _lib.check(self.lib.fg_graph_value_info(self.h, vid.value, C.byref(dt), C.byref(nd), shp))
+        self.shapes.append((shp[0],) if nd.value == 1 else (shp[0], shp[1]))
+        self.dtypes.append("f32")
+        return vid.value
+
+    def mark_output(self, vid):
+        _lib.check(self.lib.fg_graph_mark_output(self.h, vid))
+
+    def build(self, max_fused_ops=256, max_args=64, allow_reduce_epilogue=False, wait_limit_ns=2_000_000_000):
+        return Plan(self, max_fused_ops, max_args, allow_reduce_epilogue, wait_limit_ns)
+
+
+def graph_from_spec(spec) -> Graph:
+    """A Graph with the same values, in the same order, as a workloads.GraphSpec."""
+    g = Graph()
+    for v in spec.values:
+        if v.is_input:
+            g.input(v.shape, v.dtype)
+        else:
+            g.op(v.op, v.args, v.attrs)
+    for o in spec.outputs:
+        g.mark_output(o)
+    return g
+
+
+class GroupInfo:
+    def __init__(self, nodes, leaves, out, kind, alg_bytes, alg_flops, status):
+        self.nodes, self.leaves, self.out = nodes, leaves, out
+        self.kind, self.alg_bytes, self.alg_flops, self.status = kind, alg_bytes, alg_flops, status
+
+    def __repr__(self):
+        return (f"GroupInfo(nodes={self.nodes}, leaves={self.leaves}, out={self.out}, kind={self.kind}, "
+                f"alg_bytes={self.alg_bytes})")
+
+
+class Plan:
+    def __init__(self, graph: Graph, max_fused_ops=256, max_args=64, allow_reduce_epilogue=False,
+                 wait_limit_ns=2_000_000_000):
+        self.lib = graph.lib
+        self.graph = graph
+        o = _lib.BuildOpts()
+        self.lib.fg_build_opts_default(C.byref(o))
+        o.max_fused_ops, o.max_args = max_fused_ops, max_args
+        o.allow_reduce_epilogue = int(bool(allow_reduce_epilogue))
+        o.wait_limit_ns = wait_limit_ns
+        self.h = C.c_void_p()
+        _lib.check(self.lib.fg_build_groups(graph.h, C.byref(o), C.byref(self.h)))
+        nn, ng = C.c_int32(), C.c_int32()
+        _lib.check(self.lib.fg_plan_query(self.h, C.byref(nn), C.byref(ng), None, None))
+        self.n_nodes, self.n_groups = nn.value, ng.value
+        gof, ipd = (C.c_int32 * nn.value)(), (C.c_int32 * nn.value)()
+        _lib.check(self.lib.fg_plan_query(self.h, None, None, gof, ipd))
+        self.group_of, self.ipdom = list(gof), list(ipd)
+        self.groups = [self._info(g) for g in range(self.n_groups)]
+
+    def __del__(self):
+        h = getattr(self, "h", None)
+        if h:
+            self.lib.fg_plan_destroy(h)
+            self.h = None
+
+    def _info(self, gid):
+        nn, nl = C.c_int32(), C.c_int32()
+        self.lib.fg_plan_group_info(self.h, gid, C.byref(nn), None, C.byref(nl), None, None, None, None, None)
+        nodes, leaves = (C.c_int32 * max(1, nn.value))(), (C.c_int32 * max(1, nl.value))()
+        out, kind, ab, af = C.c_int32(), C.c_int32(), C.c_int64(), C.c_int64()
+        st = self.lib.fg_plan_group_info(self.h, gid, C.byref(nn), nodes, C.byref(nl), leaves, C.byref(out),
+                                         C.byref(kind), C.byref(ab), C.byref(af))
+        return GroupInfo(list(nodes)[:nn.value], list(leaves)[:nl.value], out.value, EXEC_KINDS[kind.value],
+                         ab.value, af.value, st)
+
+    def exec_info(self, gid):
+        v = [C.c_int32() for _ in range(6)]
+        _lib.check(self.lib.fg_plan_group_exec_info(self.h, gid, *[C.byref(x) for x in v]))
+        return dict(zip(("tile_rows", "tile_cols", "stages", "n_staged", "n_gathered", "prog_len"),
+                        [x.value for x in v]))
+
+    def _ptrs(self, tensors):
+        n = len(self.graph.shapes)
+        arr = (C.c_void_p * n)()
+        for vid, t in tensors.items():
+            arr[vid] = t if isinstance(t, int) else t.data_ptr()
+        return arr
+
+    def launch_group(self, gid, tensors, stream=None):
+        """tensors: {value id: device tensor or pointer} for the group's leaves and output."""
+        _lib.check(self.lib.fg_launch_group(self.h, gid, self._ptrs(tensors), _stream_handle(stream)))
+
+    def launch_unfused(self, node, tensors, stream=None):
+        _lib.check(self.lib.fg_launch_unfused(self.h, node, self._ptrs(tensors), _stream_handle(stream)))
+
+    def launch_group_ptrs(self, gid, ptr_array, stream_handle):
+        """Pre-marshalled launch (ctypes pointer array indexed by value id)."""
+        return self.lib.fg_launch_group(self.h, gid, ptr_array, stream_handle)
+
+    def sync(self, stream=None):
+        _lib.check(self.lib.fg_sync_status(self.h, _stream_handle(stream)))
+
+
+class TensorFusion:
+    """Layout of float32 gradient tensors inside one fusion buffer."""
+
+    def __init__(self, grads, buf_dtype="bf16", align=256):
+        self.lib = _lib.load()
+        n = len(grads)
+        numel = (C.c_int64 * n)(*[g.numel() for g in grads])
+        ptrs = (C.c_void_p * n)(*[g.data_ptr() for g in grads])
+        offs = (C.c_int64 * n)()
+        total = C.c_int64()
+        self.h = C.c_void_p()
+        _lib.check(self.lib.tf_layout_create(n, numel, ptrs, FG_BF16 if buf_dtype == "bf16" else FG_F32, align,
+                                             C.byref(self.h), offs, C.byref(total)))
+        self.grads = grads
+        self.offsets = list(offs)
+        self.total_bytes = total.value
+
+    def __del__(self):
+        h = getattr(self, "h", None)
+        if h:
+            self.lib.tf_layout_destroy(h)
+            self.h = None
+
+    def pack(self, scale, buf, stream=None):
+        _lib.check(self.lib.tf_pack(self.h, C.c_float(scale), C.c_void_p(buf.data_ptr()), _stream_handle(stream)))
+
+    def unpack(self, uscale, buf, stream=None):
+        _lib.check(self.lib.tf_unpack(self.h, C.c_float(uscale), C.c_void_p(buf.data_ptr()),
+                                      _stream_handle(stream)))

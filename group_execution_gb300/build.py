@@ -1,0 +1,86 @@
+"""Builds libgroupexec.so in-tree for sm_103a (GB300).
+
+Every translation unit compiles in parallel with nvcc (CUDA) or g++ (host
+C++); the CUDA runtime is linked statically, and the driver API is reached at
+run time through the runtime's entry-point lookup, so the library loads on a
+machine without a GPU driver (graph building and grouping then still work).
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import os
+import shutil
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(HERE, "csrc")
+BUILD = os.path.join(HERE, "_build")
+LIB = os.path.join(HERE, "libgroupexec.so")
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def _cuda_home():
+    for c in (os.environ.get("CUDA_HOME"), "/usr/local/cuda"):
+        if c and os.path.exists(os.path.join(c, "bin", "nvcc")):
+            return c
+    nvcc = shutil.which("nvcc")
+    if nvcc:
+        return os.path.dirname(os.path.dirname(nvcc))
+    raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libgroupexec.so")
+
+
+def sources():
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cpp")))
+
+
+def headers():
+    hs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
+    return hs + [os.path.join(ROOT, "include", "groupexec.h"), __file__]
+
+
+def _cmd(src, obj, cuda):
+    inc = ["-I", os.path.join(cuda, "include"), "-I", CSRC]
+    if src.endswith(".cu"):
+        return [os.path.join(cuda, "bin", "nvcc"), *ARCH, "-O3", "-lineinfo", "-std=c++17",
+                "-Xcompiler", "-fPIC", "-Xptxas", "-warn-spills", *inc, "-c", src, "-o", obj]
+    return ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", *inc, "-c", src, "-o", obj]
+
+
+def stale():
+    if not os.path.exists(LIB):
+        return True
+    t = os.path.getmtime(LIB)
+    return any(os.path.getmtime(f) > t for f in sources() + headers())
+
+
+def build(force=False, verbose=False, jobs=None):
+    """Compile (if stale) and return the path of libgroupexec.so."""
+    if not force and not stale():
+        return LIB
+    cuda = _cuda_home()
+    os.makedirs(BUILD, exist_ok=True)
+    srcs = sources()
+    objs = [os.path.join(BUILD, os.path.basename(s) + ".o") for s in srcs]
+
+    def run(cmd):
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if verbose or r.returncode:
+            sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
+        if r.returncode:
+            raise RuntimeError(f"compilation failed: {cmd[-3]}")
+        return r.stderr
+
+    with cf.ThreadPoolExecutor(max_workers=jobs or min(8, len(srcs))) as ex:
+        list(ex.map(run, [_cmd(s, o, cuda) for s, o in zip(srcs, objs)]))
+    tmp = LIB + ".tmp"
+    run([os.path.join(cuda, "bin", "nvcc"), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs,
+         "-lpthread", "-ldl", "-lrt"])
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    build(force="--force" in sys.argv, verbose=True)
+    print(LIB)

@@ -1,0 +1,694 @@
+// The C ABI (include/groupexec.h): graph construction, grouping, plan
+// queries, group launches and tensor-fusion layouts.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <memory>
+#include <mutex>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "host.h"
+#include "launch.h"
+
+using namespace fg;
+
+// ---------------------------------------------------------------------------
+// errors
+namespace {
+thread_local std::string g_last_error;
+
+fg_status err(fg_status st, const std::string& msg) {
+  g_last_error = msg;
+  return st;
+}
+fg_status cuda_err(cudaError_t e, const char* what) {
+  return err(FG_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point, so the
+// library loads on machines without a driver.
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  });
+  return fn;
+}
+
+bool device_present(int* nsm) {
+  int n = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess || n == 0) {
+    cudaGetLastError();
+    return false;
+  }
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (nsm) cudaDeviceGetAttribute(nsm, cudaDevAttrMultiProcessorCount, dev);
+  return true;
+}
+
+int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// opaque handles
+struct fg_graph {
+  Graph g;
+};
+
+namespace {
+struct GroupExec {
+  CompiledGroup cg;
+  std::unique_ptr<GroupParams> gp;   // K1 / K2
+  std::unique_ptr<GemmParams> mp;    // K3
+  bool big = false;
+  int grid = 1, smem = 0;
+  float* scratch = nullptr;
+  int32_t* counters = nullptr;
+  std::string compile_error;          // non-empty: cannot launch
+  fg_status compile_status = FG_OK;
+  std::vector<const void*> last_ptrs; // tensor-map cache key
+};
+}  // namespace
+
+struct fg_plan {
+  Graph g;
+  BuildOpts opts;
+  std::vector<int32_t> group_of, ipdom;
+  std::vector<GroupExec> groups;     // by gid (ascending sink)
+  std::vector<GroupExec> singles;    // per node, for fg_launch_unfused
+  bool has_device = false;
+  int nsm = 148;
+  int32_t* d_err = nullptr;
+};
+
+struct tf_layout {
+  int32_t n = 0;
+  int buf_bf16 = 1;
+  int64_t total = 0;
+  std::vector<int64_t> numel, offsets;
+  std::vector<float*> grads;
+  TfChunk* d_chunks = nullptr;
+  int nchunks = 0;
+};
+
+// ---------------------------------------------------------------------------
+extern "C" {
+
+const char* fg_last_error(void) { return g_last_error.c_str(); }
+
+void fg_build_opts_default(fg_build_opts* o) {
+  if (!o) return;
+  o->max_fused_ops = 256;
+  o->max_args = 64;
+  o->allow_reduce_epilogue = 0;
+  o->reserved = 0;
+  o->wait_limit_ns = 2000000000LL;
+}
+
+fg_status fg_graph_create(fg_graph** g) {
+  if (!g) return err(FG_EINVAL, "null output pointer");
+  *g = new (std::nothrow) fg_graph();
+  return *g ? FG_OK : err(FG_ENOMEM, "out of host memory");
+}
+
+void fg_graph_destroy(fg_graph* g) { delete g; }
+
+fg_status fg_graph_add_input(fg_graph* gh, fg_dtype dtype, int32_t ndim, const int64_t* shape, int32_t* vid) {
+  if (!gh || !shape || !vid) return err(FG_EINVAL, "null argument");
+  if (dtype != FG_F32 && dtype != FG_BF16) return err(FG_EINVAL, "unknown dtype");
+  if (ndim != 1 && ndim != 2) return err(FG_ESHAPE, "inputs have rank 1 or 2");
+  Value v;
+  v.dtype = dtype;
+  v.ndim = ndim;
+  v.rows = ndim == 2 ? shape[0] : 1;
+  v.cols = ndim == 2 ? shape[1] : shape[0];
+  if (v.rows <= 0 || v.cols <= 0) return err(FG_ESHAPE, "empty or negative extent");
+  if (v.rows > (int64_t(1) << 31) - 64 || v.cols > (int64_t(1) << 31) - 64) return err(FG_ESHAPE, "extent too large");
+  v.is_input = true;
+  gh->g.values.push_back(v);
+  gh->g.is_output.push_back(0);
+  *vid = (int32_t)gh->g.values.size() - 1;
+  return FG_OK;
+}
+
+fg_status fg_graph_add_op(fg_graph* gh, int32_t op, int32_t n_in, const int32_t* in_ids, int32_t n_attr,
+                          const float* attrs, int32_t* vid) {
+  if (!gh || !vid || (n_in > 0 && !in_ids) || (n_attr > 0 && !attrs)) return err(FG_EINVAL, "null argument");
+  if (op < 0 || op >= FG_OP_COUNT) return err(FG_EINVAL, "unknown opcode");
+  Graph& g = gh->g;
+  for (int i = 0; i < n_in; ++i)
+    if (in_ids[i] < 0 || in_ids[i] >= (int32_t)g.values.size()) return err(FG_EINVAL, "unknown operand value id");
+  auto need = [&](int lo, int hi, int na) -> fg_status {
+    if (n_in < lo || n_in > hi) return err(FG_EINVAL, "wrong number of operands");
+    if (n_attr < na) return err(FG_EINVAL, "missing attribute");
+    return FG_OK;
+  };
+  auto V = [&](int i) -> const Value& { return g.values[in_ids[i]]; };
+  Value out;
+  out.is_input = false;
+  fg_status st = FG_OK;
+  switch (op) {
+    case FG_OP_ADD:
+      if ((st = need(2, 3, 0))) return st;
+      for (int i = 1; i < n_in; ++i) if (!V(i).same_shape(V(0))) return err(FG_ESHAPE, "add operands differ in shape");
+      out = V(0);
+      break;
+    case FG_OP_SUB: case FG_OP_MUL: case FG_OP_DIV:
+      if ((st = need(2, 2, 0))) return st;
+      if (!V(1).same_shape(V(0))) return err(FG_ESHAPE, "operands differ in shape");
+      out = V(0);
+      break;
+    case FG_OP_SCALE: case FG_OP_ADDC:
+      if ((st = need(1, 1, 1))) return st;
+      out = V(0);
+      break;
+    case FG_OP_RELU: case FG_OP_EXP: case FG_OP_SIGMOID: case FG_OP_TANH: case FG_OP_NEG: case FG_OP_OPAQUE_COPY:
+      if ((st = need(1, 1, 0))) return st;
+      out = V(0);
+      break;
+    case FG_OP_BADD_COL: case FG_OP_BMUL_COL: case FG_OP_BADD_ROW: case FG_OP_BMUL_ROW: {
+      if ((st = need(2, 2, 0))) return st;
+      bool col = op == FG_OP_BADD_COL || op == FG_OP_BMUL_COL;
+      if (V(0).ndim != 2 || V(1).ndim != 1 || V(1).cols != (col ? V(0).cols : V(0).rows))
+        return err(FG_ESHAPE, "broadcast needs x[R,C] and a vector of length C (col) or R (row)");
+      out = V(0);
+      break;
+    }
+    case FG_OP_TRANSPOSE:
+      if ((st = need(1, 1, 0))) return st;
+      if (V(0).ndim != 2) return err(FG_ESHAPE, "transpose needs rank 2");
+      out = V(0);
+      std::swap(out.rows, out.cols);
+      break;
+    case FG_OP_RESHAPE: {
+      if ((st = need(1, 1, 2))) return st;
+      int64_t r = (int64_t)attrs[0], c = (int64_t)attrs[1];
+      if (r <= 0 || c <= 0 || r * c != V(0).numel()) return err(FG_ESHAPE, "reshape must keep the element count");
+      out = V(0);
+      out.ndim = 2;
+      out.rows = r;
+      out.cols = c;
+      break;
+    }
+    case FG_OP_ROWSUM: case FG_OP_ROWMAX:
+      if ((st = need(1, 1, 0))) return st;
+      if (V(0).ndim != 2) return err(FG_ESHAPE, "row reduction needs rank 2");
+      out = V(0);
+      out.ndim = 1;
+      out.cols = V(0).rows;
+      out.rows = 1;
+      break;
+    case FG_OP_MATMUL_BF16: {
+      if ((st = need(2, 2, 0))) return st;
+      int ta = n_attr > 0 ? (int)attrs[0] : 0, tb = n_attr > 1 ? (int)attrs[1] : 0;
+      const Value &A = V(0), &B = V(1);
+      if (A.dtype != FG_BF16 || B.dtype != FG_BF16) return err(FG_EINVAL, "matmul operands must be bf16");
+      if (A.ndim != 2 || B.ndim != 2) return err(FG_ESHAPE, "matmul needs rank-2 operands");
+      int64_t M = ta ? A.cols : A.rows, KA = ta ? A.rows : A.cols;
+      int64_t KB = tb ? B.cols : B.rows, N = tb ? B.rows : B.cols;
+      if (KA != KB) return err(FG_ESHAPE, "matmul inner extents differ");
+      out.ndim = 2;
+      out.rows = M;
+      out.cols = N;
+      break;
+    }
+    default:
+      return err(FG_EINVAL, "unknown opcode");
+  }
+  if (op != FG_OP_MATMUL_BF16) {
+    for (int i = 0; i < n_in; ++i)
+      if (V(i).dtype != FG_F32) return err(FG_EUNSUPPORTED, "bf16 values can only feed MATMUL_BF16");
+  }
+  out.dtype = FG_F32;
+  out.is_input = false;
+  Node n;
+  n.op = op;
+  n.args.assign(in_ids, in_ids + n_in);
+  if (n_attr > 0) n.attrs.assign(attrs, attrs + n_attr);
+  out.node = (int32_t)g.nodes.size();
+  n.value = (int32_t)g.values.size();
+  g.values.push_back(out);
+  g.is_output.push_back(0);
+  g.nodes.push_back(n);
+  *vid = n.value;
+  return FG_OK;
+}
+
+fg_status fg_graph_mark_output(fg_graph* gh, int32_t vid) {
+  if (!gh) return err(FG_EINVAL, "null graph");
+  if (vid < 0 || vid >= (int32_t)gh->g.values.size()) return err(FG_EINVAL, "unknown value id");
+  gh->g.is_output[vid] = 1;
+  return FG_OK;
+}
+
+fg_status fg_graph_value_info(const fg_graph* gh, int32_t vid, int32_t* dtype, int32_t* ndim, int64_t* shape2) {
+  if (!gh) return err(FG_EINVAL, "null graph");
+  if (vid < 0 || vid >= (int32_t)gh->g.values.size()) return err(FG_EINVAL, "unknown value id");
+  const Value& v = gh->g.values[vid];
+  if (dtype) *dtype = v.dtype;
+  if (ndim) *ndim = v.ndim;
+  if (shape2) {
+    shape2[0] = v.ndim == 2 ? v.rows : v.cols;
+    shape2[1] = v.ndim == 2 ? v.cols : 1;
+  }
+  return FG_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// plan construction
+namespace {
+
+void fill_leaf_desc(LeafDesc& d, const LeafUse& l, int stage_off, int map_idx) {
+  std::memset(&d, 0, sizeof(d));
+  d.cls = l.cls;
+  d.stage_off = stage_off;
+  d.map_idx = map_idx;
+  d.nterms = l.map.n;
+  for (int k = 0; k < l.map.n; ++k) {
+    d.d[k] = l.map.d[k];
+    d.m[k] = l.map.m[k];
+    d.s[k] = l.map.s[k];
+  }
+}
+
+int box_tx_bytes(int cls) {
+  switch (cls) {
+    case LEAF_IDENT: case LEAF_TRANS: return kTileR * kTileC * 4;
+    case LEAF_COL: return kTileC * 4;
+    case LEAF_ROW: return kTileR * 4;
+    default: return 0;
+  }
+}
+
+// Static part of the kernel parameters of a K1/K2 group.
+void prepare_group(GroupExec& ge, const BuildOpts& o, int nsm) {
+  CompiledGroup& cg = ge.cg;
+  ge.gp.reset(new GroupParams());
+  GroupParams& p = *ge.gp;
+  std::memset(&p, 0, sizeof(p));
+  if (cg.prog.size() > (size_t)kMaxProg) throw CompileError{FG_EUNSUPPORTED, "group program too long"};
+  std::copy(cg.prog.begin(), cg.prog.end(), p.prog);
+  p.nprog = (int)cg.prog.size();
+  p.nleaves = (int)cg.leaves.size();
+  int mi = 0, tx = 0;
+  for (size_t i = 0; i < cg.leaves.size(); ++i) {
+    bool staged = cg.leaves[i].cls != LEAF_GATHER;
+    fill_leaf_desc(p.leaves[i], cg.leaves[i], staged ? cg.leaf_stage_off[i] : -1, staged ? mi : -1);
+    if (staged) {
+      ++mi;
+      tx += box_tx_bytes(cg.leaves[i].cls);
+    }
+  }
+  p.nstaged = mi;
+  std::copy(cg.epi.begin(), cg.epi.end(), p.epi);
+  p.nepi = (int)cg.epi.size();
+  p.FR = (int32_t)cg.FR;
+  p.FC = (int32_t)cg.FC;
+  p.ntr = (int32_t)((cg.FR + kTileR - 1) / kTileR);
+  p.ntc = (int32_t)((cg.FC + kTileC - 1) / kTileC);
+  p.ntiles = p.ntr * p.ntc;
+  p.stage_bytes = cg.stage_bytes;
+  p.nstages = cg.nstages;
+  p.tx_bytes = tx;
+  p.out_tma = cg.out_tma ? 1 : 0;
+  p.wait_limit_ns = o.wait_limit_ns;
+  ge.big = std::max(cg.depth, cg.epi_depth) > 4 || std::max(cg.slots, cg.epi_slots) > 4;
+  const int ctas = std::min(cg.ctas_per_sm, ge.big ? 1 : 2);
+  ge.smem = cg.smem_bytes;
+  if (cg.exec == FG_EXEC_REDUCE) {
+    p.red_op = cg.red_op;
+    const int want = 2 * ctas * nsm;
+    int nsplit = (want + p.ntr - 1) / p.ntr;
+    nsplit = std::max(1, std::min(nsplit, std::max(1, p.ntc / 4)));
+    int tps = (p.ntc + nsplit - 1) / nsplit;
+    nsplit = (p.ntc + tps - 1) / tps;
+    p.nsplit = nsplit;
+    p.tiles_per_split = tps;
+    p.nunits = p.ntr * nsplit;
+    cg.nsplit = nsplit;
+    cg.tiles_per_split = tps;
+    ge.grid = std::max(1, std::min(p.nunits, ctas * nsm));
+  } else {
+    ge.grid = std::max(1, std::min(p.ntiles, ctas * nsm));
+  }
+}
+
+GroupExec make_exec(const Graph& g, const std::vector<int32_t>& nodes, const BuildOpts& o, int nsm) {
+  GroupExec ge;
+  try {
+    ge.cg = compile_group(g, nodes);
+    plan_staging(g, ge.cg);
+    if (ge.cg.exec == FG_EXEC_GEMM) {
+      ge.compile_status = FG_EUNSUPPORTED;
+      ge.compile_error = "GEMM groups are not available in this build";
+    } else {
+      prepare_group(ge, o, nsm);
+    }
+  } catch (const CompileError& e) {
+    ge.compile_status = e.st;
+    ge.compile_error = e.msg;
+    ge.cg.nodes = nodes;
+    std::sort(ge.cg.nodes.begin(), ge.cg.nodes.end());
+    ge.cg.sink = ge.cg.nodes.back();
+    ge.cg.out_value = g.nodes[ge.cg.sink].value;
+  }
+  return ge;
+}
+
+fg_status alloc_device(fg_plan* p, GroupExec& ge) {
+  if (ge.compile_status != FG_OK || !ge.gp) return FG_OK;
+  GroupParams& gp = *ge.gp;
+  gp.err = p->d_err;
+  if (ge.cg.exec == FG_EXEC_REDUCE && gp.nsplit > 1) {
+    cudaError_t e = cudaMalloc(&ge.scratch, sizeof(float) * (size_t)gp.nsplit * gp.FR);
+    if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(reduce scratch)");
+    e = cudaMalloc(&ge.counters, sizeof(int32_t) * (size_t)gp.ntr);
+    if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(reduce counters)");
+    e = cudaMemset(ge.counters, 0, sizeof(int32_t) * (size_t)gp.ntr);
+    if (e != cudaSuccess) return cuda_err(e, "cudaMemset(reduce counters)");
+    gp.scratch = ge.scratch;
+    gp.counters = ge.counters;
+  }
+  return FG_OK;
+}
+
+void free_exec(GroupExec& ge) {
+  if (ge.scratch) cudaFree(ge.scratch);
+  if (ge.counters) cudaFree(ge.counters);
+  ge.scratch = nullptr;
+  ge.counters = nullptr;
+}
+
+// ---- tensor maps -----------------------------------------------------------
+fg_status encode(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, const uint64_t* strides,
+                 const uint32_t* box, bool swizzle, CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT32) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return err(FG_ECUDA, "cuTensorMapEncodeTiled is not available");
+  cuuint64_t d[5], s[5];
+  cuuint32_t b[5], e[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+  }
+  for (int i = 0; i + 1 < rank; ++i) s[i] = strides[i];
+  CUresult r = fn(m, dt, rank, const_cast<void*>(ptr), d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return err(FG_ECUDA, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+  return FG_OK;
+}
+
+// Tensor map of a leaf (or the output, cls = LEAF_IDENT) for a frame
+// [FR, FC] and a tile of TR x TC.
+fg_status leaf_map(CUtensorMap* m, const void* ptr, int cls, int64_t FR, int64_t FC, int TR, int TC) {
+  uint64_t dims[2], strides[1];
+  uint32_t box[2];
+  switch (cls) {
+    case LEAF_IDENT:
+      dims[0] = FC; dims[1] = FR;
+      strides[0] = FR == 1 ? round_up(FC * 4, 16) : FC * 4;
+      box[0] = 32; box[1] = TR;
+      return encode(m, ptr, 2, dims, strides, box, true);
+    case LEAF_TRANS:
+      dims[0] = FR; dims[1] = FC;
+      strides[0] = FC == 1 ? round_up(FR * 4, 16) : FR * 4;
+      box[0] = 32; box[1] = TC;
+      return encode(m, ptr, 2, dims, strides, box, true);
+    case LEAF_COL:
+      dims[0] = FC; box[0] = TC;
+      return encode(m, ptr, 1, dims, strides, box, false);
+    case LEAF_ROW:
+      dims[0] = FR; box[0] = TR;
+      return encode(m, ptr, 1, dims, strides, box, false);
+    default:
+      return err(FG_EINVAL, "internal: map for a gathered leaf");
+  }
+}
+
+fg_status check_ptr(const void* p, int32_t vid) {
+  if (!p) return err(FG_EINVAL, "null device pointer for value " + std::to_string(vid));
+  if (reinterpret_cast<uintptr_t>(p) % 16) return err(FG_EINVAL, "value " + std::to_string(vid) + " is not 16-byte aligned");
+  return FG_OK;
+}
+
+fg_status launch_exec(fg_plan* p, GroupExec& ge, void* const* ptrs, void* stream) {
+  if (ge.compile_status != FG_OK) return err(ge.compile_status, ge.compile_error);
+  if (!p->has_device) return err(FG_ECUDA, "no CUDA device: the plan is host-only");
+  if (!ptrs) return err(FG_EINVAL, "null value_ptrs");
+  const CompiledGroup& cg = ge.cg;
+  GroupParams& gp = *ge.gp;
+  // cache key: the pointers this group reads and writes
+  std::vector<const void*> key;
+  for (int32_t v : cg.leaf_values) key.push_back(ptrs[v]);
+  for (int32_t v : cg.epi_leaf_values) key.push_back(ptrs[v]);
+  key.push_back(ptrs[cg.out_value]);
+  if (key != ge.last_ptrs) {
+    for (int32_t v : cg.leaf_values) if (fg_status st = check_ptr(ptrs[v], v)) return st;
+    for (int32_t v : cg.epi_leaf_values) if (fg_status st = check_ptr(ptrs[v], v)) return st;
+    if (fg_status st = check_ptr(ptrs[cg.out_value], cg.out_value)) return st;
+    for (size_t i = 0; i < cg.leaves.size(); ++i) {
+      const LeafUse& l = cg.leaves[i];
+      LeafDesc& d = gp.leaves[i];
+      d.ptr = static_cast<const float*>(ptrs[l.value]);
+      if (l.cls != LEAF_GATHER)
+        if (fg_status st = leaf_map(&gp.maps[d.map_idx], ptrs[l.value], l.cls, cg.FR, cg.FC, kTileR, kTileC)) return st;
+    }
+    for (size_t i = 0; i < cg.epi_leaf_values.size(); ++i)
+      gp.epi_leaf[i] = static_cast<const float*>(ptrs[cg.epi_leaf_values[i]]);
+    gp.out = static_cast<float*>(ptrs[cg.out_value]);
+    if (cg.exec == FG_EXEC_ELEMWISE && cg.out_tma)
+      if (fg_status st = leaf_map(&gp.maps[kMaxStaged], ptrs[cg.out_value], LEAF_IDENT, cg.FR, cg.FC, kTileR, kTileC))
+        return st;
+    ge.last_ptrs = key;
+  }
+  cudaError_t e = launch_group_kernel(gp, cg.exec == FG_EXEC_REDUCE ? 1 : 0, ge.big ? 1 : 0, ge.grid, ge.smem,
+                                      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    ge.last_ptrs.clear();
+    return cuda_err(e, "group kernel launch");
+  }
+  return FG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fg_status fg_build_groups(const fg_graph* gh, const fg_build_opts* opts, fg_plan** out) {
+  if (!gh || !out) return err(FG_EINVAL, "null argument");
+  *out = nullptr;
+  fg_build_opts o;
+  fg_build_opts_default(&o);
+  if (opts) o = *opts;
+  if (o.max_fused_ops < 1 || o.max_args < 2) return err(FG_EINVAL, "max_fused_ops >= 1 and max_args >= 2 required");
+  if (gh->g.nodes.empty()) return err(FG_EINVAL, "graph has no operators");
+  std::unique_ptr<fg_plan> p(new (std::nothrow) fg_plan());
+  if (!p) return err(FG_ENOMEM, "out of host memory");
+  p->g = gh->g;
+  p->opts.max_fused_ops = o.max_fused_ops;
+  p->opts.max_args = o.max_args;
+  p->opts.allow_reduce_epilogue = o.allow_reduce_epilogue;
+  p->opts.wait_limit_ns = o.wait_limit_ns > 0 ? o.wait_limit_ns : 2000000000LL;
+  p->has_device = device_present(&p->nsm);
+  partition(p->g, p->opts, p->group_of, p->ipdom);
+  std::vector<int32_t> sinks;
+  for (size_t i = 0; i < p->group_of.size(); ++i)
+    if (p->group_of[i] == (int32_t)i) sinks.push_back((int32_t)i);
+  for (int32_t s : sinks) {
+    std::vector<int32_t> nodes;
+    for (size_t i = 0; i < p->group_of.size(); ++i)
+      if (p->group_of[i] == s) nodes.push_back((int32_t)i);
+    p->groups.push_back(make_exec(p->g, nodes, p->opts, p->nsm));
+  }
+  for (size_t i = 0; i < p->g.nodes.size(); ++i)
+    p->singles.push_back(make_exec(p->g, {(int32_t)i}, p->opts, p->nsm));
+  if (p->has_device) {
+    cudaError_t e = cudaMalloc(&p->d_err, sizeof(int32_t));
+    if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(error flag)");
+    e = cudaMemset(p->d_err, 0, sizeof(int32_t));
+    if (e != cudaSuccess) return cuda_err(e, "cudaMemset(error flag)");
+    for (auto& ge : p->groups) if (fg_status st = alloc_device(p.get(), ge)) return st;
+    for (auto& ge : p->singles) if (fg_status st = alloc_device(p.get(), ge)) return st;
+  }
+  *out = p.release();
+  return FG_OK;
+}
+
+void fg_plan_destroy(fg_plan* p) {
+  if (!p) return;
+  for (auto& ge : p->groups) free_exec(ge);
+  for (auto& ge : p->singles) free_exec(ge);
+  if (p->d_err) cudaFree(p->d_err);
+  delete p;
+}
+
+fg_status fg_plan_query(const fg_plan* p, int32_t* n_nodes, int32_t* n_groups, int32_t* group_of, int32_t* ipdom) {
+  if (!p) return err(FG_EINVAL, "null plan");
+  if (n_nodes) *n_nodes = (int32_t)p->group_of.size();
+  if (n_groups) *n_groups = (int32_t)p->groups.size();
+  if (group_of) std::copy(p->group_of.begin(), p->group_of.end(), group_of);
+  if (ipdom) std::copy(p->ipdom.begin(), p->ipdom.end(), ipdom);
+  return FG_OK;
+}
+
+fg_status fg_plan_group_info(const fg_plan* p, int32_t gid, int32_t* n_nodes, int32_t* nodes, int32_t* n_leaves,
+                             int32_t* leaves, int32_t* out_value, int32_t* kind, int64_t* alg_bytes,
+                             int64_t* alg_flops) {
+  if (!p) return err(FG_EINVAL, "null plan");
+  if (gid < 0 || gid >= (int32_t)p->groups.size()) return err(FG_EINVAL, "unknown group id");
+  const GroupExec& ge = p->groups[gid];
+  const CompiledGroup& cg = ge.cg;
+  if (n_nodes) *n_nodes = (int32_t)cg.nodes.size();
+  if (nodes) std::copy(cg.nodes.begin(), cg.nodes.end(), nodes);
+  if (n_leaves) *n_leaves = (int32_t)cg.leaf_values.size();
+  if (leaves) std::copy(cg.leaf_values.begin(), cg.leaf_values.end(), leaves);
+  if (out_value) *out_value = cg.out_value;
+  if (kind) *kind = cg.exec;
+  if (alg_bytes) *alg_bytes = cg.alg_bytes;
+  if (alg_flops) *alg_flops = cg.alg_flops;
+  if (ge.compile_status != FG_OK) return err(ge.compile_status, ge.compile_error);
+  return FG_OK;
+}
+
+fg_status fg_plan_group_exec_info(const fg_plan* p, int32_t gid, int32_t* tile_rows, int32_t* tile_cols,
+                                  int32_t* stages, int32_t* n_staged, int32_t* n_gathered, int32_t* prog_len) {
+  if (!p) return err(FG_EINVAL, "null plan");
+  if (gid < 0 || gid >= (int32_t)p->groups.size()) return err(FG_EINVAL, "unknown group id");
+  const CompiledGroup& cg = p->groups[gid].cg;
+  bool gemm = cg.exec == FG_EXEC_GEMM;
+  if (tile_rows) *tile_rows = gemm ? 128 : kTileR;
+  if (tile_cols) *tile_cols = gemm ? 256 : kTileC;
+  if (stages) *stages = cg.nstages;
+  if (n_staged) *n_staged = cg.nstaged;
+  if (n_gathered) *n_gathered = cg.ngathered;
+  if (prog_len) *prog_len = (int32_t)cg.prog.size();
+  return FG_OK;
+}
+
+fg_status fg_launch_group(fg_plan* p, int32_t gid, void* const* value_ptrs, void* stream) {
+  if (!p) return err(FG_EINVAL, "null plan");
+  if (gid < 0 || gid >= (int32_t)p->groups.size()) return err(FG_EINVAL, "unknown group id");
+  return launch_exec(p, p->groups[gid], value_ptrs, stream);
+}
+
+fg_status fg_launch_unfused(fg_plan* p, int32_t node, void* const* value_ptrs, void* stream) {
+  if (!p) return err(FG_EINVAL, "null plan");
+  if (node < 0 || node >= (int32_t)p->singles.size()) return err(FG_EINVAL, "unknown node id");
+  return launch_exec(p, p->singles[node], value_ptrs, stream);
+}
+
+fg_status fg_sync_status(fg_plan* p, void* stream) {
+  if (!p) return err(FG_EINVAL, "null plan");
+  if (!p->has_device) return err(FG_ECUDA, "no CUDA device: the plan is host-only");
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_err(e, "cudaStreamSynchronize");
+  int32_t flag = 0;
+  e = cudaMemcpy(&flag, p->d_err, sizeof(flag), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_err(e, "reading the device error flag");
+  if (flag == 0) return FG_OK;
+  cudaMemset(p->d_err, 0, sizeof(int32_t));
+  if (flag == DEVERR_TIMEOUT) return err(FG_ETIMEOUT, "a device-side wait exceeded wait_limit_ns");
+  return err(FG_EDEVICE, "device error flag " + std::to_string(flag));
+}
+
+// ---------------------------------------------------------------------------
+// tensor fusion
+fg_status tf_layout_create(int32_t n, const int64_t* numel, float* const* grads, fg_dtype buf_dtype,
+                           int64_t align, tf_layout** out, int64_t* offsets_out, int64_t* total_out) {
+  if (!out || (n > 0 && (!numel || !grads))) return err(FG_EINVAL, "null argument");
+  *out = nullptr;
+  if (n <= 0) return err(FG_EINVAL, "no tensors");
+  if (buf_dtype != FG_BF16 && buf_dtype != FG_F32) return err(FG_EINVAL, "unknown buffer dtype");
+  if (align < 16 || (align & (align - 1))) return err(FG_EINVAL, "align_bytes must be a power of two >= 16");
+  std::unique_ptr<tf_layout> l(new (std::nothrow) tf_layout());
+  if (!l) return err(FG_ENOMEM, "out of host memory");
+  l->n = n;
+  l->buf_bf16 = buf_dtype == FG_BF16;
+  const int64_t eb = l->buf_bf16 ? 2 : 4;
+  int64_t cur = 0;
+  for (int i = 0; i < n; ++i) {
+    if (numel[i] < 0) return err(FG_ESHAPE, "negative element count");
+    if (numel[i] > 0) if (fg_status st = check_ptr(grads[i], i)) return st;
+    l->numel.push_back(numel[i]);
+    l->grads.push_back(grads[i]);
+    l->offsets.push_back(cur);
+    cur = round_up(cur + numel[i] * eb, align);
+  }
+  l->total = cur;
+  std::vector<TfChunk> ch;
+  for (int i = 0; i < n; ++i) {
+    const int64_t end_bytes = l->offsets[i] + numel[i] * eb;
+    const int64_t next = i + 1 < n ? l->offsets[i + 1] : l->total;
+    int64_t s = 0;
+    do {
+      TfChunk c;
+      c.tensor = grads[i];
+      c.start = s;
+      c.count = (int32_t)std::min<int64_t>(kTfChunk, numel[i] - s);
+      c.buf_off = l->offsets[i] + s * eb;
+      s += c.count;
+      c.pad_bytes = s >= numel[i] ? (int32_t)(next - end_bytes) : 0;
+      ch.push_back(c);
+    } while (s < numel[i]);
+  }
+  l->nchunks = (int)ch.size();
+  if (!device_present(nullptr)) return err(FG_ECUDA, "no CUDA device");
+  cudaError_t e = cudaMalloc(&l->d_chunks, sizeof(TfChunk) * ch.size());
+  if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(chunk table)");
+  e = cudaMemcpy(l->d_chunks, ch.data(), sizeof(TfChunk) * ch.size(), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(l->d_chunks);
+    return cuda_err(e, "cudaMemcpy(chunk table)");
+  }
+  if (offsets_out) std::copy(l->offsets.begin(), l->offsets.end(), offsets_out);
+  if (total_out) *total_out = l->total;
+  *out = l.release();
+  return FG_OK;
+}
+
+static int tf_grid(const tf_layout* l) {
+  int nsm = 148;
+  device_present(&nsm);
+  return std::max(1, std::min(l->nchunks, nsm * 8));
+}
+
+fg_status tf_pack(const tf_layout* l, float scale, void* buf, void* stream) {
+  if (!l || !buf) return err(FG_EINVAL, "null argument");
+  if (reinterpret_cast<uintptr_t>(buf) % 256) return err(FG_EINVAL, "fusion buffer must be 256-byte aligned");
+  cudaError_t e = launch_tf_pack(l->d_chunks, l->nchunks, l->buf_bf16, scale, buf, tf_grid(l),
+                                 static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FG_OK : cuda_err(e, "tf_pack launch");
+}
+
+fg_status tf_unpack(const tf_layout* l, float uscale, const void* buf, void* stream) {
+  if (!l || !buf) return err(FG_EINVAL, "null argument");
+  if (reinterpret_cast<uintptr_t>(buf) % 256) return err(FG_EINVAL, "fusion buffer must be 256-byte aligned");
+  cudaError_t e = launch_tf_unpack(l->d_chunks, l->nchunks, l->buf_bf16, uscale, buf, tf_grid(l),
+                                   static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FG_OK : cuda_err(e, "tf_unpack launch");
+}
+
+void tf_layout_destroy(tf_layout* l) {
+  if (!l) return;
+  if (l->d_chunks) cudaFree(l->d_chunks);
+  delete l;
+}
+
+}  // extern "C"

@@ -1,0 +1,262 @@
+// Device helpers for sm_103a: mbarriers with bounded waits, TMA tile copies,
+// bulk-group bookkeeping, and the register-stack interpreter that runs a
+// group's operator program on eight values per thread.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+
+#include "fg_abi.h"
+
+namespace fg {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---- mbarrier ------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase with the given parity to complete, at most limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if ((int64_t)(global_ns() - t0) > limit_ns) return false;
+  }
+  return true;
+}
+
+// ---- TMA -------------------------------------------------------------------------
+__device__ __forceinline__ void tma_prefetch(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+__device__ __forceinline__ void tma_load_1d(uint32_t dst, const CUtensorMap* m, int32_t x, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.1d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2}], [%3];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, int32_t x, int32_t y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, int32_t x, int32_t y, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
+               ::"l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void set_error(int32_t* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// ---- operator semantics (float32, one rounding per operator) -------------------
+// Products and sums use the _rn intrinsics so the compiler never contracts
+// two operators into one fused multiply-add: fusion must not change the
+// per-operator rounding of the unfused program.
+__device__ __forceinline__ float op_relu(float x) { return x > 0.f ? x : 0.f; }
+__device__ __forceinline__ float op_sigmoid(float x) { return __frcp_rn(__fadd_rn(1.f, expf(-x))); }
+
+// ---- the register-stack machine -------------------------------------------------
+// V values per thread.  The top of the stack lives in TOP; the entries below
+// it in R[0..D-2]; S save slots hold values a group reuses.  Unary operators
+// act on TOP whatever the depth, so their code exists once; only moves
+// between TOP, R and the slots depend on the depth, and those use
+// compile-time register indices.  `Env` provides load_leaf(arg, float(&)[V])
+// and load_acc(float(&)[V]).
+template <int D, int S, int V>
+struct Machine {
+  float TOP[V];
+  float R[D > 1 ? D - 1 : 1][V];
+  float SL[S > 0 ? S : 1][V];
+
+  // push: the old top (stack depth d before the push, d >= 1) moves to R[d-1]
+  template <int d>
+  __device__ __forceinline__ void push(const float (&t)[V]) {
+    if constexpr (d < D) {
+      if constexpr (d >= 1) {
+#pragma unroll
+        for (int i = 0; i < V; ++i) R[d - 1][i] = TOP[i];
+      }
+#pragma unroll
+      for (int i = 0; i < V; ++i) TOP[i] = t[i];
+    }
+  }
+  // binary op at depth d: TOP = R[d-2] op TOP
+  template <int op, int d>
+  __device__ __forceinline__ void bin() {
+    if constexpr (d >= 2 && d <= D) {
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const float a = R[d - 2][i], b = TOP[i];
+        if constexpr (op == VM_ADD) TOP[i] = __fadd_rn(a, b);
+        else if constexpr (op == VM_SUB) TOP[i] = __fsub_rn(a, b);
+        else TOP[i] = __fmul_rn(a, b);
+      }
+    }
+  }
+  template <int d>
+  __device__ __forceinline__ void second(float (&t)[V]) {
+    if constexpr (d >= 2 && d <= D) {
+#pragma unroll
+      for (int i = 0; i < V; ++i) t[i] = R[d - 2][i];
+    }
+  }
+  // The empty asm statements keep the compiler from merging the per-(slot,
+  // depth) cases into one indexed access, which would move the slots to
+  // local memory.
+  template <int s, int d>
+  __device__ __forceinline__ void push_slot() {
+    if constexpr (s < S && d < D) {
+      asm volatile("");
+      if constexpr (d >= 1) {
+#pragma unroll
+        for (int i = 0; i < V; ++i) R[d - 1][i] = TOP[i];
+      }
+#pragma unroll
+      for (int i = 0; i < V; ++i) TOP[i] = SL[s][i];
+    }
+  }
+  template <int s, int d>
+  __device__ __forceinline__ void tee() {
+    if constexpr (s < S && d >= 1) {
+      asm volatile("");
+#pragma unroll
+      for (int i = 0; i < V; ++i) SL[s][i] = TOP[i];
+    }
+  }
+  // store: copy the top into slot s and pop (the entry below becomes TOP)
+  template <int s, int d>
+  __device__ __forceinline__ void store() {
+    if constexpr (s < S && d >= 1 && d <= D) {
+      asm volatile("");
+#pragma unroll
+      for (int i = 0; i < V; ++i) SL[s][i] = TOP[i];
+      if constexpr (d >= 2) {
+#pragma unroll
+        for (int i = 0; i < V; ++i) TOP[i] = R[d - 2][i];
+      }
+    }
+  }
+
+  // Runs `n` instructions; the result is TOP.
+  template <class Env>
+  __device__ __forceinline__ void run(const VmInstr* prog, int n, Env& env) {
+    for (int pc = 0; pc < n; ++pc) {
+      const VmInstr ins = prog[pc];
+      const int key = ins.key;
+      float t[V];
+      if (key < kKeyStride) env.load_leaf(ins.arg, t);        // VM_PUSH_LEAF at any depth
+      else if (key < 2 * kKeyStride) env.load_acc(t);         // VM_PUSH_ACC at any depth
+      bool div = false;
+      switch (key) {
+#define FG_ALL_D(op)                                                                    \
+  case vm_key(op, 0): case vm_key(op, 1): case vm_key(op, 2): case vm_key(op, 3):      \
+  case vm_key(op, 4): case vm_key(op, 5): case vm_key(op, 6): case vm_key(op, 7):      \
+  case vm_key(op, 8):
+        FG_ALL_D(VM_SCALE)
+#pragma unroll
+          for (int i = 0; i < V; ++i) TOP[i] = __fmul_rn(ins.imm, TOP[i]);
+          break;
+        FG_ALL_D(VM_ADDC)
+#pragma unroll
+          for (int i = 0; i < V; ++i) TOP[i] = __fadd_rn(TOP[i], ins.imm);
+          break;
+        FG_ALL_D(VM_RELU)
+#pragma unroll
+          for (int i = 0; i < V; ++i) TOP[i] = op_relu(TOP[i]);
+          break;
+        FG_ALL_D(VM_EXP)
+#pragma unroll
+          for (int i = 0; i < V; ++i) TOP[i] = expf(TOP[i]);
+          break;
+        FG_ALL_D(VM_SIGMOID)
+#pragma unroll
+          for (int i = 0; i < V; ++i) TOP[i] = op_sigmoid(TOP[i]);
+          break;
+        FG_ALL_D(VM_TANH)
+#pragma unroll
+          for (int i = 0; i < V; ++i) TOP[i] = tanhf(TOP[i]);
+          break;
+        FG_ALL_D(VM_NEG)
+#pragma unroll
+          for (int i = 0; i < V; ++i) TOP[i] = -TOP[i];
+          break;
+#undef FG_ALL_D
+#define FG_CASES_D(d)                                                         \
+  case vm_key(VM_PUSH_LEAF, d): push<d>(t); break;                            \
+  case vm_key(VM_PUSH_ACC, d): push<d>(t); break;                             \
+  case vm_key(VM_ADD, d): bin<VM_ADD, d>(); break;                            \
+  case vm_key(VM_SUB, d): bin<VM_SUB, d>(); break;                            \
+  case vm_key(VM_MUL, d): bin<VM_MUL, d>(); break;                            \
+  case vm_key(VM_DIV, d): second<d>(t); div = true; break;
+#define FG_CASES_SD(s, d)                                                     \
+  case vm_slot_key(VM_PUSH_SLOT, s, d): push_slot<s, d>(); break;             \
+  case vm_slot_key(VM_TEE, s, d): tee<s, d>(); break;                         \
+  case vm_slot_key(VM_STORE, s, d): store<s, d>(); break;
+#define FG_CASES_S(s) \
+  FG_CASES_SD(s, 0) FG_CASES_SD(s, 1) FG_CASES_SD(s, 2) FG_CASES_SD(s, 3) \
+  FG_CASES_SD(s, 4) FG_CASES_SD(s, 5) FG_CASES_SD(s, 6) FG_CASES_SD(s, 7) FG_CASES_SD(s, 8)
+        FG_CASES_D(0) FG_CASES_D(1) FG_CASES_D(2) FG_CASES_D(3)
+        FG_CASES_D(4) FG_CASES_D(5) FG_CASES_D(6) FG_CASES_D(7) FG_CASES_D(8)
+        FG_CASES_S(0) FG_CASES_S(1) FG_CASES_S(2) FG_CASES_S(3)
+        FG_CASES_S(4) FG_CASES_S(5) FG_CASES_S(6) FG_CASES_S(7)
+#undef FG_CASES_S
+#undef FG_CASES_SD
+#undef FG_CASES_D
+        default: break;
+      }
+      if (div) {
+#pragma unroll
+        for (int i = 0; i < V; ++i) TOP[i] = __fdiv_rn(t[i], TOP[i]);
+      }
+    }
+  }
+};
+
+}  // namespace fg

@@ -1,0 +1,568 @@
+// Group compilation: one operator program per group, evaluated in the frame
+// of the group's output (TVM "Operator Fusion", FuseTIR: the operators of a
+// group merge into one function whose intermediates never reach global
+// memory).  Every operator is evaluated at the frame point; injective
+// operators turn into index maps on the leaves they read (a transpose or
+// reshape moves no data inside a group), broadcasts read their vector at the
+// mapped row or column.
+#include <algorithm>
+#include <map>
+#include <tuple>
+
+#include "host.h"
+
+namespace fg {
+
+bool Map::operator==(const Map& o) const {
+  if (n != o.n) return false;
+  for (int k = 0; k < n; ++k)
+    if (d[k] != o.d[k] || m[k] != o.m[k] || s[k] != o.s[k]) return false;
+  return true;
+}
+
+namespace {
+
+[[noreturn]] void fail(fg_status st, const std::string& msg) { throw CompileError{st, msg}; }
+
+struct Term { int64_t d, m, s; };
+
+Map make_map(std::vector<Term> t) {
+  // drop unit digits, order by place value, merge digits that continue
+  // each other both in the frame index and in the value index
+  t.erase(std::remove_if(t.begin(), t.end(), [](const Term& x) { return x.m == 1; }), t.end());
+  std::sort(t.begin(), t.end(), [](const Term& a, const Term& b) { return a.s < b.s; });
+  std::vector<Term> out;
+  for (const Term& x : t) {
+    if (!out.empty() && out.back().s * out.back().m == x.s && out.back().d * out.back().m == x.d) {
+      out.back().m *= x.m;
+    } else {
+      out.push_back(x);
+    }
+  }
+  if ((int)out.size() > kMaxTerms) fail(FG_EUNSUPPORTED, "index map needs more than 4 digits");
+  Map mp;
+  mp.n = (int)out.size();
+  for (int k = 0; k < mp.n; ++k) {
+    mp.d[k] = out[k].d;
+    mp.m[k] = out[k].m;
+    mp.s[k] = out[k].s;
+  }
+  return mp;
+}
+
+std::vector<Term> terms(const Map& mp) {
+  std::vector<Term> t;
+  for (int k = 0; k < mp.n; ++k) t.push_back({mp.d[k], mp.m[k], mp.s[k]});
+  return t;
+}
+
+Map ident(int64_t rows, int64_t cols) { return make_map({{1, rows * cols, 1}}); }
+
+// f % Q and f / Q as maps; Q must fall on a digit boundary (a digit may be
+// split when its radix divides accordingly).
+void split(const Map& mp, int64_t Q, Map& lo, Map& hi) {
+  std::vector<Term> L, H;
+  for (Term t : terms(mp)) {
+    if (t.s * t.m <= Q) {
+      L.push_back(t);
+    } else if (t.s >= Q) {
+      if (t.s % Q) fail(FG_EUNSUPPORTED, "index map does not split at the row boundary");
+      H.push_back({t.d, t.m, t.s / Q});
+    } else {
+      int64_t q = Q / t.s;
+      if (Q % t.s || t.m % q) fail(FG_EUNSUPPORTED, "index map does not split at the row boundary");
+      L.push_back({t.d, q, t.s});
+      H.push_back({t.d * q, t.m / q, 1});
+    }
+  }
+  int64_t prod = 1;
+  for (const Term& t : L) prod *= t.m;
+  if (!H.empty() && prod != Q) fail(FG_EUNSUPPORTED, "index map does not split at the row boundary");
+  lo = make_map(L);
+  hi = make_map(H);
+}
+
+// The map of x = y^T's index, given y's map; x is [A, B], y is [B, A]:
+// f_x = (f_y % A) * B + f_y / A.
+Map transpose_map(const Map& fy, int64_t A, int64_t B) {
+  Map lo, hi;
+  split(fy, A, lo, hi);
+  std::vector<Term> t;
+  for (Term x : terms(lo)) t.push_back({x.d, x.m, x.s * B});
+  for (Term x : terms(hi)) t.push_back(x);
+  return make_map(t);
+}
+
+int classify(const Map& mp, int64_t FR, int64_t FC) {
+  if (mp == ident(FR, FC)) return LEAF_IDENT;
+  if (mp == make_map({{FC, FR, 1}, {1, FC, FR}})) return LEAF_TRANS;
+  if (mp == make_map({{1, FC, 1}})) return LEAF_COL;
+  if (mp == make_map({{FC, FR, 1}})) return LEAF_ROW;
+  return LEAF_GATHER;
+}
+
+// ---- expression DAG --------------------------------------------------------
+
+enum ExprKind { E_LEAF, E_ACC, E_UN, E_BIN };
+
+struct Expr {
+  ExprKind kind;
+  int vm;                // VmOp for E_UN / E_BIN
+  float imm = 0.f;
+  int a = -1, b = -1;    // children
+  int leaf = -1;         // index into leaves (E_LEAF)
+  int uses = 0;
+  int need = 1;          // registers to evaluate (Sethi-Ullman, no caching)
+};
+
+struct Builder {
+  const Graph& g;
+  std::vector<char> in_group;     // per node
+  int anchor = -1;                // node read as the accumulator (matmul / reduce)
+  Map anchor_map;
+  int64_t FR, FC;
+  std::vector<Expr> ex;
+  std::vector<LeafUse> leaves;
+  std::map<std::tuple<int, int, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t,
+                      int64_t, int64_t, int64_t, int64_t, int64_t>, int> memo;
+
+  Builder(const Graph& gg, const std::vector<int32_t>& nodes, int64_t fr, int64_t fc)
+      : g(gg), in_group(gg.nodes.size(), 0), FR(fr), FC(fc) {
+    for (int x : nodes) in_group[x] = 1;
+  }
+
+  int mk(Expr e) {
+    ex.push_back(e);
+    return (int)ex.size() - 1;
+  }
+
+  int leaf(int value, const Map& mp) {
+    for (size_t i = 0; i < leaves.size(); ++i)
+      if (leaves[i].value == value && leaves[i].map == mp) return (int)i;
+    leaves.push_back({value, mp, classify(mp, FR, FC)});
+    return (int)leaves.size() - 1;
+  }
+
+  int build(int value, const Map& mp) {
+    auto key = std::make_tuple(value, mp.n, mp.d[0], mp.m[0], mp.s[0], mp.d[1], mp.m[1], mp.s[1],
+                               mp.d[2], mp.m[2], mp.s[2], mp.d[3], mp.m[3], mp.s[3]);
+    auto it = memo.find(key);
+    if (it != memo.end()) {
+      ex[it->second].uses++;
+      return it->second;
+    }
+    int id = build_new(value, mp);
+    ex[id].uses++;
+    memo[key] = id;
+    return id;
+  }
+
+  int build_new(int value, const Map& mp) {
+    const Value& v = g.values[value];
+    int nd = v.node;
+    if (nd < 0 || !in_group[nd]) {
+      Expr e{E_LEAF, 0};
+      e.leaf = leaf(value, mp);
+      return mk(e);
+    }
+    if (nd == anchor) {
+      if (!(mp == anchor_map)) fail(FG_EUNSUPPORTED, "accumulator read at a moved index");
+      return mk(Expr{E_ACC, VM_PUSH_ACC});
+    }
+    const Node& n = g.nodes[nd];
+    auto un = [&](int vm, int a, float imm) {
+      Expr e{E_UN, vm};
+      e.a = a;
+      e.imm = imm;
+      return mk(e);
+    };
+    auto bin = [&](int vm, int a, int b) {
+      Expr e{E_BIN, vm};
+      e.a = a;
+      e.b = b;
+      return mk(e);
+    };
+    auto arg = [&](int i) { return n.args[i]; };
+    const Value& x0 = g.values[arg(0)];
+    switch (n.op) {
+      case FG_OP_TRANSPOSE:
+        return build_alias(arg(0), transpose_map(mp, x0.rows, x0.cols));
+      case FG_OP_RESHAPE:
+      case FG_OP_OPAQUE_COPY:
+        return build_alias(arg(0), mp);
+      case FG_OP_ADD: {
+        int acc = bin(VM_ADD, build(arg(0), mp), build(arg(1), mp));
+        for (size_t i = 2; i < n.args.size(); ++i) {
+          ex[acc].uses++;
+          acc = bin(VM_ADD, acc, build(arg((int)i), mp));
+        }
+        return acc;
+      }
+      case FG_OP_SUB: return bin(VM_SUB, build(arg(0), mp), build(arg(1), mp));
+      case FG_OP_MUL: return bin(VM_MUL, build(arg(0), mp), build(arg(1), mp));
+      case FG_OP_DIV: return bin(VM_DIV, build(arg(0), mp), build(arg(1), mp));
+      case FG_OP_SCALE: return un(VM_SCALE, build(arg(0), mp), n.attrs[0]);
+      case FG_OP_ADDC: return un(VM_ADDC, build(arg(0), mp), n.attrs[0]);
+      case FG_OP_RELU: return un(VM_RELU, build(arg(0), mp), 0.f);
+      case FG_OP_EXP: return un(VM_EXP, build(arg(0), mp), 0.f);
+      case FG_OP_SIGMOID: return un(VM_SIGMOID, build(arg(0), mp), 0.f);
+      case FG_OP_TANH: return un(VM_TANH, build(arg(0), mp), 0.f);
+      case FG_OP_NEG: return un(VM_NEG, build(arg(0), mp), 0.f);
+      case FG_OP_BADD_COL:
+      case FG_OP_BMUL_COL:
+      case FG_OP_BADD_ROW:
+      case FG_OP_BMUL_ROW: {
+        bool col = n.op == FG_OP_BADD_COL || n.op == FG_OP_BMUL_COL;
+        Map lo, hi;
+        split(mp, x0.cols, lo, hi);
+        int xa = build(arg(0), mp);
+        int va = build(arg(1), col ? lo : hi);
+        bool add = n.op == FG_OP_BADD_COL || n.op == FG_OP_BADD_ROW;
+        return bin(add ? VM_ADD : VM_MUL, xa, va);
+      }
+      default:
+        fail(FG_EUNSUPPORTED, "operator cannot sit inside a group program");
+    }
+  }
+
+  // Injective operators add no instruction: the operand's expression is the
+  // result.  Its use count is bumped by the caller's `build`.
+  int build_alias(int value, const Map& mp) {
+    int id = build(value, mp);
+    ex[id].uses--;
+    return id;
+  }
+};
+
+// ---- postfix emission --------------------------------------------------------
+
+struct Emitter {
+  std::vector<Expr>& ex;
+  std::vector<VmInstr> code;
+  int depth = 0, max_depth = 0, max_slot = 0;
+  std::vector<int> slot_of;     // expr -> slot or -1
+  std::vector<int> remaining;   // references still to emit
+  std::vector<char> slot_busy;
+
+  explicit Emitter(std::vector<Expr>& e)
+      : ex(e), slot_of(e.size(), -1), remaining(e.size(), 0), slot_busy(kMaxSlots, 0) {
+    for (size_t i = 0; i < e.size(); ++i) remaining[i] = e[i].uses;
+    for (size_t i = 0; i < e.size(); ++i) need(i);
+  }
+
+  int need(size_t i) {
+    Expr& e = ex[i];
+    if (e.kind == E_UN) e.need = ex[e.a].need;
+    if (e.kind == E_BIN) {
+      int la = ex[e.a].need, lb = ex[e.b].need;
+      e.need = la == lb ? la + 1 : std::max(la, lb);
+    }
+    return e.need;
+  }
+
+  void put(int key, int arg = 0, float imm = 0.f) {
+    if ((int)code.size() >= kMaxProg) fail(FG_EUNSUPPORTED, "group program too long");
+    code.push_back(VmInstr{(uint16_t)key, (uint16_t)arg, imm});
+  }
+  void push_depth() {
+    ++depth;
+    if (depth > kMaxDepth) fail(FG_EUNSUPPORTED, "group program needs more than 8 stack registers");
+    max_depth = std::max(max_depth, depth);
+  }
+  int alloc_slot() {
+    for (int s = 0; s < kMaxSlots; ++s)
+      if (!slot_busy[s]) {
+        slot_busy[s] = 1;
+        max_slot = std::max(max_slot, s + 1);
+        return s;
+      }
+    return -1;
+  }
+
+  // Emit code that leaves expr i on top of the stack.
+  void emit(int i) {
+    Expr& e = ex[i];
+    if (slot_of[i] >= 0) {
+      int s = slot_of[i];
+      put(vm_slot_key(VM_PUSH_SLOT, s, depth));
+      push_depth();
+      if (--remaining[i] == 0) slot_busy[s] = 0;
+      return;
+    }
+    switch (e.kind) {
+      case E_LEAF:
+        put(vm_key(VM_PUSH_LEAF, depth), e.leaf);
+        push_depth();
+        break;
+      case E_ACC:
+        put(vm_key(VM_PUSH_ACC, depth));
+        push_depth();
+        break;
+      case E_UN:
+        emit(e.a);
+        put(vm_key(e.vm, depth), 0, e.imm);
+        break;
+      case E_BIN: {
+        int a = e.a, b = e.b;
+        bool comm = e.vm == VM_ADD || e.vm == VM_MUL;
+        if (comm && ex[b].need > ex[a].need) std::swap(a, b);
+        // evaluate a deep right operand into a slot first if the stack
+        // would overflow otherwise
+        int spill = -1;
+        if (slot_of[b] < 0 && depth + std::max(ex[a].need, ex[b].need + 1) > kMaxDepth) {
+          spill = alloc_slot();
+          if (spill >= 0) {
+            emit(b);
+            put(vm_slot_key(VM_STORE, spill, depth));
+            --depth;
+          }
+        }
+        emit(a);
+        if (spill >= 0) {
+          put(vm_slot_key(VM_PUSH_SLOT, spill, depth));
+          push_depth();
+          slot_busy[spill] = 0;
+        } else {
+          emit(b);
+        }
+        put(vm_key(e.vm, depth));
+        --depth;
+        break;
+      }
+    }
+    // a value needed again later is kept in a save slot until its last use
+    if (--remaining[i] > 0) {
+      int s = alloc_slot();
+      if (s < 0) fail(FG_EUNSUPPORTED, "group program keeps more than 8 values live");
+      slot_of[i] = s;
+      put(vm_slot_key(VM_TEE, s, depth));
+    }
+  }
+};
+
+struct Program {
+  std::vector<VmInstr> code;
+  std::vector<LeafUse> leaves;
+  int depth = 0, slots = 0;
+};
+
+Program emit_program(Builder& b, int root) {
+  Emitter em(b.ex);
+  em.emit(root);
+  if (em.depth != 1) fail(FG_EUNSUPPORTED, "internal: unbalanced program");
+  Program p;
+  p.code = em.code;
+  p.leaves = b.leaves;
+  p.depth = em.max_depth;
+  p.slots = em.max_slot;
+  if ((int)p.leaves.size() > kMaxLeaves) fail(FG_EUNSUPPORTED, "group reads more than 24 leaf views");
+  return p;
+}
+
+}  // namespace
+
+CompiledGroup compile_group(const Graph& g, const std::vector<int32_t>& nodes_in) {
+  CompiledGroup cg;
+  cg.nodes = nodes_in;
+  std::sort(cg.nodes.begin(), cg.nodes.end());
+  cg.sink = cg.nodes.back();
+  cg.out_value = g.nodes[cg.sink].value;
+  int mm = -1, red = -1;
+  for (int x : cg.nodes) {
+    int op = g.nodes[x].op;
+    if (op == FG_OP_MATMUL_BF16) {
+      if (mm >= 0) fail(FG_EUNSUPPORTED, "two matmuls in one group");
+      mm = x;
+    }
+    if (op == FG_OP_ROWSUM || op == FG_OP_ROWMAX) {
+      if (red >= 0) fail(FG_EUNSUPPORTED, "two reductions in one group");
+      red = x;
+    }
+  }
+  if (mm >= 0 && red >= 0) fail(FG_EUNSUPPORTED, "matmul and reduction in one group");
+
+  // distinct outside values, first-use order
+  std::vector<char> in(g.nodes.size(), 0);
+  for (int x : cg.nodes) in[x] = 1;
+  for (int x : cg.nodes)
+    for (int32_t a : g.nodes[x].args) {
+      int prod = g.values[a].node;
+      if (prod >= 0 && in[prod]) continue;
+      if (std::find(cg.leaf_values.begin(), cg.leaf_values.end(), a) == cg.leaf_values.end())
+        cg.leaf_values.push_back(a);
+    }
+  for (int32_t a : cg.leaf_values) {
+    if (g.values[a].dtype != FG_F32 && !(mm >= 0 && (a == g.nodes[mm].args[0] || a == g.nodes[mm].args[1])))
+      fail(FG_EUNSUPPORTED, "bf16 value read outside a matmul operand");
+    cg.alg_bytes += g.values[a].bytes();
+  }
+  const Value& out = g.values[cg.out_value];
+  cg.alg_bytes += out.bytes();
+
+  if (mm >= 0) {
+    const Node& n = g.nodes[mm];
+    cg.exec = FG_EXEC_GEMM;
+    cg.mm_a = n.args[0];
+    cg.mm_b = n.args[1];
+    cg.mm_ta = n.attrs.size() > 0 ? (int)n.attrs[0] : 0;
+    cg.mm_tb = n.attrs.size() > 1 ? (int)n.attrs[1] : 0;
+    const Value& mv = g.values[n.value];
+    cg.M = mv.rows;
+    cg.N = mv.cols;
+    const Value& A = g.values[cg.mm_a];
+    cg.K = cg.mm_ta ? A.rows : A.cols;
+    cg.alg_flops = 2 * cg.M * cg.N * cg.K;
+    cg.FR = cg.M;
+    cg.FC = cg.N;
+    // the epilogue runs on the accumulator tile; operands are not leaves of it
+    Builder b(g, cg.nodes, cg.FR, cg.FC);
+    b.anchor = mm;
+    b.anchor_map = ident(cg.FR, cg.FC);
+    Program p = emit_program(b, b.build(cg.out_value, ident(cg.FR, cg.FC)));
+    cg.prog = p.code;
+    cg.leaves = p.leaves;
+    cg.depth = p.depth;
+    cg.slots = p.slots;
+    for (auto& l : cg.leaves)
+      if (l.value == cg.mm_a || l.value == cg.mm_b) fail(FG_EUNSUPPORTED, "matmul operand read by the epilogue");
+    return cg;
+  }
+  if (red >= 0) {
+    const Node& n = g.nodes[red];
+    cg.exec = FG_EXEC_REDUCE;
+    cg.red_op = n.op == FG_OP_ROWSUM ? RED_SUM : RED_MAX;
+    const Value& x = g.values[n.args[0]];
+    if (x.ndim != 2) fail(FG_ESHAPE, "row reduction of a rank-1 value");
+    cg.FR = x.rows;
+    cg.FC = x.cols;
+    Builder b(g, cg.nodes, cg.FR, cg.FC);
+    b.anchor = red;   // never reached from the prologue root
+    b.anchor_map = ident(1, cg.FR);
+    Program p = emit_program(b, b.build(n.args[0], ident(cg.FR, cg.FC)));
+    cg.prog = p.code;
+    cg.leaves = p.leaves;
+    cg.depth = p.depth;
+    cg.slots = p.slots;
+    if (cg.sink != red) {
+      // epilogue on the reduced vector (allow_reduce_epilogue)
+      Builder be(g, cg.nodes, 1, cg.FR);
+      be.anchor = red;
+      be.anchor_map = ident(1, cg.FR);
+      Program pe = emit_program(be, be.build(cg.out_value, ident(1, cg.FR)));
+      if ((int)pe.code.size() > kMaxEpi) fail(FG_EUNSUPPORTED, "reduce epilogue too long");
+      if ((int)pe.leaves.size() > kMaxEpiLeaves) fail(FG_EUNSUPPORTED, "reduce epilogue reads too many values");
+      for (auto& l : pe.leaves)
+        if (l.cls != LEAF_IDENT) fail(FG_EUNSUPPORTED, "reduce epilogue reads a moved vector");
+      cg.epi = pe.code;
+      for (auto& l : pe.leaves) cg.epi_leaf_values.push_back(l.value);
+      cg.epi_depth = pe.depth;
+      cg.epi_slots = pe.slots;
+    }
+    return cg;
+  }
+  cg.exec = FG_EXEC_ELEMWISE;
+  cg.FR = out.rows;
+  cg.FC = out.cols;
+  Builder b(g, cg.nodes, cg.FR, cg.FC);
+  Program p = emit_program(b, b.build(cg.out_value, ident(cg.FR, cg.FC)));
+  cg.prog = p.code;
+  cg.leaves = p.leaves;
+  cg.depth = p.depth;
+  cg.slots = p.slots;
+  return cg;
+}
+
+// Which leaves are staged through shared memory by TMA, and the pipeline
+// depth.  A TMA tensor needs 16-byte row strides, so IDENT leaves need a
+// frame width that is a multiple of 4 floats and TRANS leaves a frame height
+// that is.  Everything else is gathered from global memory.
+void plan_staging(const Graph& g, CompiledGroup& cg) {
+  (void)g;
+  const bool gemm = cg.exec == FG_EXEC_GEMM;
+  const int TR = gemm ? 128 : kTileR, TC = gemm ? 32 : kTileC;
+  auto box_bytes = [&](int cls) -> int {
+    switch (cls) {
+      case LEAF_IDENT: case LEAF_TRANS: return TR * TC * 4;
+      case LEAF_COL: return TC * 4;
+      case LEAF_ROW: return TR * 4;
+      default: return 0;
+    }
+  };
+  const bool rows_ok = cg.FC % 4 == 0 || cg.FR == 1;
+  const bool cols_ok = cg.FR % 4 == 0 || cg.FC == 1;
+  cg.out_tma = rows_ok;
+  std::vector<char> stage(cg.leaves.size(), 0);
+  int want = 0;
+  for (size_t i = 0; i < cg.leaves.size(); ++i) {
+    int c = cg.leaves[i].cls;
+    bool ok = (c == LEAF_IDENT && rows_ok) || (c == LEAF_TRANS && cols_ok) || c == LEAF_COL || c == LEAF_ROW;
+    if (ok && want < kMaxStaged) {
+      stage[i] = 1;
+      ++want;
+    }
+  }
+  // big boxes first (1024-byte aligned for the 128-byte swizzle), then vectors
+  auto layout = [&](std::vector<int>* offs) {
+    int off = 0;
+    for (size_t i = 0; i < cg.leaves.size(); ++i)
+      if (stage[i] && box_bytes(cg.leaves[i].cls) >= 1024) {
+        if (offs) (*offs)[i] = off;
+        off += box_bytes(cg.leaves[i].cls);
+      }
+    for (size_t i = 0; i < cg.leaves.size(); ++i)
+      if (stage[i] && box_bytes(cg.leaves[i].cls) < 1024) {
+        if (offs) (*offs)[i] = off;
+        off += (box_bytes(cg.leaves[i].cls) + 127) / 128 * 128;
+      }
+    return (off + 1023) / 1024 * 1024;
+  };
+  int fixed = 2048;   // barriers + alignment slack
+  if (!gemm) {
+    if (cg.out_tma) fixed += 3 * TR * TC * 4;               // three output buffers
+    if (cg.exec == FG_EXEC_REDUCE) fixed += 2 * kConsumerWarps * 32 * 4;   // double-buffered row partials
+  }
+  const int budget_two = 112 * 1024, budget_one = 224 * 1024;
+  int sb = layout(nullptr);
+  int budget = budget_two;
+  if (!gemm) {
+    while (true) {
+      if (sb == 0 || (budget_two - fixed) / sb >= 3) { budget = budget_two; break; }
+      if ((budget_one - fixed) / sb >= 2) { budget = budget_one; break; }
+      int last = -1;   // demote the last staged leaf to a gather
+      for (size_t i = 0; i < cg.leaves.size(); ++i) if (stage[i]) last = (int)i;
+      stage[last] = 0;
+      sb = layout(nullptr);
+    }
+  } else {
+    // GEMM epilogue: two buffers of staged leaves must fit beside the
+    // operand pipeline; demote leaves beyond 64 KB
+    while (sb > 64 * 1024) {
+      int last = -1;
+      for (size_t i = 0; i < cg.leaves.size(); ++i) if (stage[i]) last = (int)i;
+      stage[last] = 0;
+      sb = layout(nullptr);
+    }
+  }
+  if (cg.FR * cg.FC >= (int64_t(1) << 31))
+    for (size_t i = 0; i < cg.leaves.size(); ++i)
+      if (!stage[i]) throw CompileError{FG_EUNSUPPORTED, "gathered leaf in a frame of 2^31 or more elements"};
+  cg.leaf_stage_off.assign(cg.leaves.size(), -1);
+  cg.stage_bytes = layout(&cg.leaf_stage_off);
+  cg.nstaged = cg.ngathered = 0;
+  for (size_t i = 0; i < cg.leaves.size(); ++i) {
+    if (stage[i]) {
+      cg.nstaged++;
+    } else {
+      cg.leaves[i].cls = LEAF_GATHER;
+      cg.ngathered++;
+    }
+  }
+  if (!gemm) {
+    int ns = cg.stage_bytes ? (budget - fixed) / cg.stage_bytes : 4;
+    cg.nstages = std::max(2, std::min(ns, 6));
+    cg.smem_bytes = fixed + cg.nstages * cg.stage_bytes;
+    cg.ctas_per_sm = budget == budget_two ? 2 : 1;
+  }
+}
+
+}  // namespace fg

@@ -1,0 +1,32 @@
+// Host-callable kernel launchers (defined in the .cu files).
+#pragma once
+#include <cuda_runtime.h>
+
+#include "fg_abi.h"
+
+namespace fg {
+
+// exec: 0 = elementwise group (K1), 1 = reduce group (K2).  big selects the
+// 8-register / 8-slot machine (one CTA per SM) over the 4/4 one.
+cudaError_t launch_group_kernel(const GroupParams& p, int exec, int big, int grid, int smem, cudaStream_t st);
+int group_kernel_threads();
+
+cudaError_t launch_gemm_kernel(const GemmParams& p, int big, int grid, int smem, cudaStream_t st);
+int gemm_smem_bytes(const GemmParams& p);
+
+// Tensor fusion.  One chunk = up to kTfChunk consecutive elements of one
+// tensor; the tensor's last chunk also zeroes the padding after it.
+constexpr int kTfChunk = 4096;
+struct TfChunk {
+  float* tensor;        // fp32 tensor base
+  int64_t start;        // first element of the chunk
+  int64_t buf_off;      // byte offset of element `start` in the fusion buffer
+  int32_t count;        // elements in the chunk
+  int32_t pad_bytes;    // bytes to zero after the chunk (last chunk of a tensor)
+};
+cudaError_t launch_tf_pack(const TfChunk* chunks, int nchunks, int buf_bf16, float scale, void* buf, int grid,
+                           cudaStream_t st);
+cudaError_t launch_tf_unpack(const TfChunk* chunks, int nchunks, int buf_bf16, float uscale, const void* buf,
+                             int grid, cudaStream_t st);
+
+}  // namespace fg

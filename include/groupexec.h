@@ -1,0 +1,213 @@
+/*
+ * groupexec.h -- C ABI of libgroupexec.so: fused operator-group execution and
+ * tensor-fusion pack/unpack on one GB300 (sm_103a).
+ *
+ * What is computed.
+ *   A dataflow graph of operators is annotated with pattern kinds, a
+ *   post-dominator tree is built on it, and operators are grouped by
+ *   CheckPath/CommitFuse (TVM "Operator Fusion", Operator Pattern
+ *   Classification; FuseOps > Algorithm, steps 1-4; Fusion rules).  Each
+ *   group then runs as ONE kernel whose intermediates never reach device
+ *   memory (DisCo, Introduction, on op fusion; TVM, FuseTIR: the merged
+ *   function drops the intermediate buffers).  Separately, many small float32
+ *   gradient tensors are scaled, cast and packed into one contiguous fusion
+ *   buffer and unpacked again (DisCo, Introduction, on tensor fusion: the
+ *   fused tensor's size is the sum of the parts).
+ *
+ * Conventions (all entry points).
+ *   - Every function returns fg_status; FG_OK == 0.  On any other status a
+ *     thread-local message is available from fg_last_error().
+ *   - Ownership: the caller owns every tensor and the fusion buffer and passes
+ *     raw DEVICE pointers (float32 or bfloat16, row-major, contiguous) and a
+ *     CUDA stream as `void*` (NULL = legacy default stream).  The library owns
+ *     graphs, plans and layouts and the small device tables they hold; it
+ *     allocates device memory only in fg_build_groups / tf_layout_create,
+ *     never in a launch, and frees it in the matching *_destroy.
+ *   - Launches are asynchronous on the given stream.  Argument, shape and
+ *     alignment errors are returned synchronously (tensors 16-byte aligned,
+ *     fusion buffer 256-byte aligned).  CUDA launch errors map to FG_ECUDA.
+ *     Errors found on the device (a bounded wait that expired) are latched in
+ *     the plan's device flag and reported by fg_sync_status.
+ *   - A plan is immutable after build.  Launches of one plan must be ordered
+ *     on one stream (reduce groups use plan-owned scratch); use one plan per
+ *     stream for concurrency.
+ *   - No CPU fallback exists: without a CUDA device every launch returns
+ *     FG_ECUDA.  Graph building and grouping are host-only and work without a
+ *     device.
+ */
+#ifndef GROUPEXEC_H
+#define GROUPEXEC_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FG_OK = 0,
+  FG_EINVAL = 1,        /* bad argument: null pointer, unknown id, bad opcode */
+  FG_ESHAPE = 2,        /* operand shapes do not fit the operator */
+  FG_EUNSUPPORTED = 3,  /* valid graph this build cannot execute (reason in fg_last_error) */
+  FG_ENOMEM = 4,        /* host or device allocation failed */
+  FG_ECUDA = 5,         /* CUDA runtime/driver error, or no CUDA device */
+  FG_ETIMEOUT = 6,      /* a device-side bounded wait expired */
+  FG_EDEVICE = 7        /* other device-side error flag */
+} fg_status;
+
+typedef enum { FG_F32 = 0, FG_BF16 = 1 } fg_dtype;
+
+/* Operators.  Kinds follow TVM's OpPatternKind (Operator Pattern
+ * Classification): elementwise 0, broadcast 1, injective 2, commutative
+ * reduce 3, out-elementwise-fusable 4, opaque 8.  All compute in float32 and
+ * round after every operator; immediates are float32 attributes.
+ *   ADD (2 or 3 operands, (a+b)+c), SUB, MUL, DIV         elementwise
+ *   SCALE(imm) = imm*x, ADDC(imm) = x+imm, RELU (x>0?x:0),
+ *   EXP, SIGMOID = 1/(1+exp(-x)), TANH, NEG               elementwise
+ *   BADD_COL/BMUL_COL: x[R,C] (+|*) v[C]                   broadcast
+ *   BADD_ROW/BMUL_ROW: x[R,C] (+|*) v[R]                   broadcast
+ *   TRANSPOSE [R,C]->[C,R]; RESHAPE(rows, cols) row-major  injective
+ *   ROWSUM, ROWMAX: [R,C] -> [R] over the last axis        commutative reduce
+ *   MATMUL_BF16(transA, transB): bf16 x bf16 -> f32 [M,N]  out-elementwise-fusable
+ *       A is [M,K] (or [K,M] when transA), B is [K,N] (or [N,K] when transB)
+ *   OPAQUE_COPY: identity that never fuses                 opaque
+ */
+typedef enum {
+  FG_OP_ADD = 0, FG_OP_SUB, FG_OP_MUL, FG_OP_DIV, FG_OP_SCALE, FG_OP_ADDC,
+  FG_OP_RELU, FG_OP_EXP, FG_OP_SIGMOID, FG_OP_TANH, FG_OP_NEG,
+  FG_OP_BADD_COL, FG_OP_BMUL_COL, FG_OP_BADD_ROW, FG_OP_BMUL_ROW,
+  FG_OP_TRANSPOSE, FG_OP_RESHAPE, FG_OP_ROWSUM, FG_OP_ROWMAX,
+  FG_OP_MATMUL_BF16, FG_OP_OPAQUE_COPY, FG_OP_COUNT
+} fg_opcode;
+
+/* Which kernel executes a group. */
+typedef enum { FG_EXEC_ELEMWISE = 0, FG_EXEC_REDUCE = 1, FG_EXEC_GEMM = 2 } fg_exec_kind;
+
+typedef struct fg_graph fg_graph;
+typedef struct fg_plan fg_plan;
+typedef struct tf_layout tf_layout;
+
+/* Grouping options.  max_fused_ops: kMaxFusedOps (TVM, Fusion rules, the
+ * constraints: 256).  max_args: the function-argument limit the page names
+ * without a value; counts distinct outside values read plus one output.
+ * allow_reduce_epilogue: let a reduce group absorb an elementwise tail on the
+ * reduced vector (off = the page's rule that a reduction never fuses forward).
+ * wait_limit_ns: bound on every device-side wait before it sets the error
+ * flag and the kernel returns. */
+typedef struct {
+  int32_t max_fused_ops;
+  int32_t max_args;
+  int32_t allow_reduce_epilogue;
+  int32_t reserved;
+  int64_t wait_limit_ns;
+} fg_build_opts;
+
+/* Fills the defaults: 256, 64, 0, 0, 2e9 ns. */
+void fg_build_opts_default(fg_build_opts* opts);
+
+/* ---- graph construction (host only) ------------------------------------ */
+
+/* New empty graph.  Value ids are assigned in creation order to inputs and
+ * operator outputs alike; the i-th operator added is node i. */
+fg_status fg_graph_create(fg_graph** g);
+
+/* Graph input of rank 1 or 2.  bf16 inputs may only feed MATMUL_BF16. */
+fg_status fg_graph_add_input(fg_graph* g, fg_dtype dtype, int32_t ndim,
+                             const int64_t* shape, int32_t* value_id);
+
+/* Operator over existing values (so the graph is topological by
+ * construction).  attrs: SCALE/ADDC {imm}; RESHAPE {rows, cols};
+ * MATMUL_BF16 {transA, transB}; others none.  Shapes are checked here
+ * (FG_ESHAPE). */
+fg_status fg_graph_add_op(fg_graph* g, int32_t opcode, int32_t n_in,
+                          const int32_t* in_ids, int32_t n_attr,
+                          const float* attrs, int32_t* value_id);
+
+/* Marks a value as a graph output: it is always materialised. */
+fg_status fg_graph_mark_output(fg_graph* g, int32_t value_id);
+
+/* dtype, rank and shape (shape[1] = 1 for rank 1) of a value. */
+fg_status fg_graph_value_info(const fg_graph* g, int32_t value_id, int32_t* dtype,
+                              int32_t* ndim, int64_t* shape2);
+
+void fg_graph_destroy(fg_graph* g);
+
+/* ---- grouping and execution ---------------------------------------------- */
+
+/* Annotate kinds, build the post-dominator tree, group (phases 0 and 1) and
+ * compile each group into an operator program for its kernel.  Also compiles a
+ * one-operator program per node for fg_launch_unfused.  Allocates the plan's
+ * device error flag and reduce scratch when a CUDA device is present; without
+ * one the plan is host-only (queries work, launches fail).  opts may be NULL
+ * for the defaults. */
+fg_status fg_build_groups(const fg_graph* g, const fg_build_opts* opts, fg_plan** plan);
+
+/* Node and group counts; group_of[node] = the node id of its group's sink
+ * (largest node id in the group); ipdom[node] = immediate post-dominator
+ * node or -1.  Either array may be NULL. */
+fg_status fg_plan_query(const fg_plan* p, int32_t* n_nodes, int32_t* n_groups,
+                        int32_t* group_of, int32_t* ipdom);
+
+/* Group gid (0..n_groups-1, in order of sink node id).  Array outputs may be
+ * NULL; `nodes` needs n_nodes entries and `leaves` n_leaves entries (call
+ * once with NULL arrays to get the counts).  leaves are the value ids the
+ * group reads from outside in first-use order; out_value is its one output;
+ * kind is the fg_exec_kind; alg_bytes counts each leaf once plus the output;
+ * alg_flops is 2*M*N*K for a GEMM group and 0 otherwise. */
+fg_status fg_plan_group_info(const fg_plan* p, int32_t gid, int32_t* n_nodes,
+                             int32_t* nodes, int32_t* n_leaves, int32_t* leaves,
+                             int32_t* out_value, int32_t* kind,
+                             int64_t* alg_bytes, int64_t* alg_flops);
+
+/* Runs group gid as one kernel on `cuda_stream`.  value_ptrs is indexed by
+ * value id and must hold device pointers for the group's leaves and output
+ * (other entries are ignored and may be NULL). */
+fg_status fg_launch_group(fg_plan* p, int32_t gid, void* const* value_ptrs, void* cuda_stream);
+
+/* Runs one node on its own (the unfused baseline: its output is written to
+ * device memory).  value_ptrs as above for that node's operands and output. */
+fg_status fg_launch_unfused(fg_plan* p, int32_t node, void* const* value_ptrs, void* cuda_stream);
+
+/* Synchronises the stream, then reads and clears the plan's device error flag:
+ * FG_ETIMEOUT when a bounded wait expired, FG_EDEVICE for other flags. */
+fg_status fg_sync_status(fg_plan* p, void* cuda_stream);
+
+/* Diagnostics for benchmarks: number of kernel launches fg_launch_group
+ * issues for gid (always 1), the tile shape, pipeline depth and number of
+ * TMA-staged leaves chosen for it. */
+fg_status fg_plan_group_exec_info(const fg_plan* p, int32_t gid, int32_t* tile_rows,
+                                  int32_t* tile_cols, int32_t* stages, int32_t* n_staged,
+                                  int32_t* n_gathered, int32_t* prog_len);
+
+void fg_plan_destroy(fg_plan* p);
+
+/* Message for the last non-OK status on this thread ("" if none). */
+const char* fg_last_error(void);
+
+/* ---- tensor fusion ------------------------------------------------------- */
+
+/* Layout of n float32 gradient tensors (device pointers grads[i], numel[i]
+ * elements, 16-byte aligned) in one fusion buffer of buf_dtype (FG_BF16 or
+ * FG_F32): tensor i starts at byte offset offsets_out[i], a multiple of
+ * align_bytes (a power of two >= 16; 256 recommended); tensors are in index
+ * order; total_bytes_out is the end of the last tensor rounded up to
+ * align_bytes.  Uploads a chunk table to the device (requires a device). */
+fg_status tf_layout_create(int32_t n, const int64_t* numel, float* const* grads,
+                           fg_dtype buf_dtype, int64_t align_bytes, tf_layout** out,
+                           int64_t* offsets_out, int64_t* total_bytes_out);
+
+/* One kernel: buf[offset_i + k] = cast(fp32(grads[i][k] * scale)) with
+ * round-to-nearest-even for bf16, and every padding byte set to 0.
+ * fusion_buf: device, 256-byte aligned, at least total_bytes. */
+fg_status tf_pack(const tf_layout* l, float scale, void* fusion_buf, void* cuda_stream);
+
+/* One kernel: grads[i][k] = fp32(widen(buf[offset_i + k]) * uscale). */
+fg_status tf_unpack(const tf_layout* l, float uscale, const void* fusion_buf, void* cuda_stream);
+
+void tf_layout_destroy(tf_layout* l);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GROUPEXEC_H */

@@ -1,0 +1,152 @@
+"""GPU parity of the fused-group kernels (elementwise and reduce groups)
+against the CPU oracle, element by element, through the C ABI."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import workloads as W
+from oracle import execute as OE
+from tests._helpers import rel_err, TOL_F32
+from tests._gpu import prepare, run_fused, run_unfused
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(spec, seed=0, unfused=True, **kw):
+    g, plan, inputs, dev = prepare(spec, seed, **kw)
+    for info in plan.groups:
+        assert info.status == 0, info
+    outs = [info.out for info in plan.groups]
+    ref = OE.run_unfused(spec, inputs, keep=outs)
+    env = run_fused(plan, spec, dev)
+    plan.sync()
+    worst = 0.0
+    for vid in outs:
+        e = rel_err(env[vid].cpu().numpy(), ref[vid])
+        assert e <= TOL_F32, (vid, spec.values[vid].op, e)
+        worst = max(worst, e)
+    if unfused:
+        envu = run_unfused(plan, spec, dev)
+        plan.sync()
+        for vid in spec.outputs:
+            e = rel_err(envu[vid].cpu().numpy(), ref[vid])
+            assert e <= TOL_F32, ("unfused", vid, e)
+    return plan, env, ref, worst
+
+
+@pytest.mark.parametrize("shape", [(200, 132), (64, 64), (33, 96), (1, 256), (96, 4), (4, 8)])
+def test_diamond_small_shapes(shape):
+    plan, env, ref, _ = _check(W.diamond(*shape))
+    assert plan.n_groups == 1
+
+
+def test_diamond_full_size():
+    spec = W.diamond(8192, 4096)
+    g, plan, inputs, dev = prepare(spec)
+    env = run_fused(plan, spec, dev)
+    plan.sync()
+    out = env[spec.outputs[0]].cpu().numpy()
+    ref = OE.run_unfused(spec, inputs)[spec.outputs[0]]
+    assert rel_err(out, ref) <= TOL_F32
+
+
+def test_diamond_odd_width_uses_direct_paths():
+    """A frame width that is not a multiple of 4 floats cannot use TMA: the
+    plan gathers those leaves and stores directly."""
+    spec = W.diamond(37, 30)
+    plan, *_ = _check(spec)
+    assert plan.exec_info(0)["n_gathered"] >= 1
+
+
+@pytest.mark.parametrize("epi", [False, True])
+def test_rnnlm_chain(epi):
+    plan, env, ref, _ = _check(W.rnnlm_chain(), allow_reduce_epilogue=epi)
+    assert plan.n_groups == (1 if epi else 2)
+
+
+@pytest.mark.parametrize("shape", [(64, 1024), (100, 200), (8192, 4096), (4096, 8192), (3, 2052)])
+def test_row_reductions(shape):
+    R, C = shape
+    for op in ("rowsum", "rowmax"):
+        spec = W.GraphSpec()
+        x = spec.input((R, C))
+        y = spec.input((R, C))
+        v = spec.input((C,))
+        a = spec.op("mul", (x, y))
+        b = spec.op("badd_col", (a, v))
+        s = spec.op(op, (b,))
+        spec.mark_output(s)
+        _check(spec, unfused=(R * C <= 1 << 20))
+
+
+def test_reduce_of_transposed_operand():
+    spec = W.GraphSpec()
+    x = spec.input((96, 160))
+    t = spec.op("transpose", (x,))
+    r = spec.op("tanh", (t,))
+    y = spec.input((160, 96))
+    a = spec.op("add", (r, y))
+    s = spec.op("rowsum", (a,))
+    spec.mark_output(s)
+    _check(spec)
+
+
+def test_all_elementwise_ops():
+    spec = W.GraphSpec()
+    x = spec.input((64, 96))
+    y = spec.input((64, 96), init=("uniform", 0.5, 2.0))
+    vr = spec.input((64,))
+    vc = spec.input((96,))
+    a = spec.op("sub", (x, y))
+    b = spec.op("div", (a, y))
+    c = spec.op("addc", (b,), (0.25,))
+    d = spec.op("neg", (c,))
+    e = spec.op("sigmoid", (d,))
+    f = spec.op("bmul_row", (e, vr))
+    h = spec.op("badd_row", (f, vr))
+    i = spec.op("bmul_col", (h, vc))
+    j = spec.op("tanh", (i,))
+    k = spec.op("exp", (j,))
+    spec.mark_output(k)
+    plan, *_ = _check(spec)
+    assert plan.n_groups == 1
+
+
+def test_transpose_reshape_chains():
+    """Leaves read through composed transposes and reshapes (digit maps)."""
+    spec = W.GraphSpec()
+    x = spec.input((64, 32))
+    t = spec.op("transpose", (x,))            # [32, 64]
+    r = spec.op("reshape", (t,), (64, 32))    # reinterpret
+    y = spec.input((64, 32))
+    a = spec.op("add", (r, y))
+    u = spec.op("transpose", (a,))            # [32, 64]
+    w = spec.op("relu", (u,))
+    spec.mark_output(w)
+    plan, *_ = _check(spec)
+    assert plan.n_groups == 1
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_dag_small(seed):
+    spec = W.random_dag(seed, **W.CONFIGS["random_dag"]["small"])
+    _check(spec, seed=seed)
+
+
+def test_launch_rejects_bad_pointers():
+    from group_execution_gb300 import FgError
+    spec = W.diamond(64, 32)
+    g, plan, inputs, dev = prepare(spec)
+    info = plan.groups[0]
+    out = torch.empty((32, 64), device="cuda")
+    ptrs = {v: dev[v] for v in info.leaves}
+    ptrs[info.out] = out
+    ptrs[info.leaves[0]] = dev[info.leaves[0]].data_ptr() + 4      # misaligned
+    with pytest.raises(FgError):
+        plan.launch_group(0, ptrs)
+    ptrs[info.leaves[0]] = 0
+    with pytest.raises(FgError):
+        plan.launch_group(0, ptrs)
+    plan.launch_group(0, {v: dev[v] for v in info.leaves} | {info.out: out})
+    plan.sync()

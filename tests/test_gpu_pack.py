@@ -1,0 +1,66 @@
+"""GPU parity of tensor-fusion pack/unpack against the oracle: bit-exact
+buffer bytes (data and zero padding) and bit-exact unpacked tensors."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import workloads as W
+from oracle import pack as PK
+from group_execution_gb300 import TensorFusion
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(sizes, scale=0.125, uscale=1.0, buf_dtype="bf16", seed=0):
+    xs = W.tensor_fusion_inputs(sizes, seed)
+    dev = [torch.from_numpy(x).cuda() for x in xs]
+    tf = TensorFusion(dev, buf_dtype)
+    offs, total = PK.layout(sizes, 2 if buf_dtype == "bf16" else 4)
+    assert tf.offsets == offs and tf.total_bytes == total
+    buf = torch.full((total,), 0xAB, dtype=torch.uint8, device="cuda")   # poison padding
+    tf.pack(scale, buf)
+    torch.cuda.synchronize()
+    ref = PK.pack(xs, scale, buf_dtype)
+    np.testing.assert_array_equal(buf.cpu().numpy(), ref)
+    for d in dev:
+        d.fill_(float("nan"))
+    tf.unpack(uscale, buf)
+    torch.cuda.synchronize()
+    back = PK.unpack(ref, sizes, uscale, buf_dtype)
+    for d, r in zip(dev, back):
+        np.testing.assert_array_equal(d.cpu().numpy(), r)
+    return tf
+
+
+def test_pack_small_ragged():
+    _run([1, 3, 4, 5, 127, 128, 129, 1000, 4095, 4096, 4097, 8192 + 7])
+
+
+def test_pack_config_full():
+    _run(W.tensor_fusion_sizes(0))
+
+
+def test_pack_fp32_buffer_identity():
+    sizes = [7, 64, 5000, 4096 * 3]
+    xs = W.tensor_fusion_inputs(sizes, 3)
+    dev = [torch.from_numpy(x).cuda() for x in xs]
+    tf = TensorFusion(dev, "f32")
+    buf = torch.zeros((tf.total_bytes,), dtype=torch.uint8, device="cuda")
+    tf.pack(1.0, buf)
+    for d in dev:
+        d.zero_()
+    tf.unpack(1.0, buf)
+    torch.cuda.synchronize()
+    for d, x in zip(dev, xs):
+        np.testing.assert_array_equal(d.cpu().numpy(), x)
+
+
+def test_pack_special_values():
+    x = np.array([0.0, -0.0, np.inf, -np.inf, 3.4e38, 1e-45, -1e-40, 1.0 + 2 ** -8, 65504.0], np.float32)
+    dev = [torch.from_numpy(x).cuda()]
+    tf = TensorFusion(dev)
+    buf = torch.zeros((tf.total_bytes,), dtype=torch.uint8, device="cuda")
+    tf.pack(1.0, buf)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(buf.cpu().numpy(), PK.pack([x], 1.0))
