@@ -71,8 +71,9 @@ class Graph:
     def mark_output(self, vid):
         _lib.check(self.lib.fg_graph_mark_output(self.h, vid))
 
-    def build(self, max_fused_ops=256, max_args=64, allow_reduce_epilogue=False, wait_limit_ns=2_000_000_000):
-        return Plan(self, max_fused_ops, max_args, allow_reduce_epilogue, wait_limit_ns)
+    def build(self, max_fused_ops=256, max_args=64, allow_reduce_epilogue=False, wait_limit_ns=2_000_000_000,
+              flags=0):
+        return Plan(self, max_fused_ops, max_args, allow_reduce_epilogue, wait_limit_ns, flags)
 
 
 def graph_from_spec(spec) -> Graph:
@@ -100,7 +101,7 @@ class GroupInfo:
 
 class Plan:
     def __init__(self, graph: Graph, max_fused_ops=256, max_args=64, allow_reduce_epilogue=False,
-                 wait_limit_ns=2_000_000_000):
+                 wait_limit_ns=2_000_000_000, flags=0):
         self.lib = graph.lib
         self.graph = graph
         o = _lib.BuildOpts()
@@ -108,6 +109,7 @@ class Plan:
         o.max_fused_ops, o.max_args = max_fused_ops, max_args
         o.allow_reduce_epilogue = int(bool(allow_reduce_epilogue))
         o.wait_limit_ns = wait_limit_ns
+        o.flags = flags
         self.h = C.c_void_p()
         _lib.check(self.lib.fg_build_groups(graph.h, C.byref(o), C.byref(self.h)))
         nn, ng = C.c_int32(), C.c_int32()

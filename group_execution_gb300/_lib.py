@@ -30,7 +30,7 @@ EXEC_KINDS = ("elementwise", "reduce", "gemm")
 
 class BuildOpts(C.Structure):
     _fields_ = [("max_fused_ops", C.c_int32), ("max_args", C.c_int32),
-                ("allow_reduce_epilogue", C.c_int32), ("reserved", C.c_int32),
+                ("allow_reduce_epilogue", C.c_int32), ("flags", C.c_int32),
                 ("wait_limit_ns", C.c_int64)]
 
 

@@ -41,7 +41,7 @@ def headers():
 
 
 def _cmd(src, obj, cuda):
-    inc = ["-I", os.path.join(cuda, "include"), "-I", CSRC]
+    inc = ["-I", os.path.join(cuda, "include"), "-I", CSRC, "-I", os.path.join(ROOT, "include")]
     if src.endswith(".cu"):
         return [os.path.join(cuda, "bin", "nvcc"), *ARCH, "-O3", "-lineinfo", "-std=c++17",
                 "-Xcompiler", "-fPIC", "-Xptxas", "-warn-spills", *inc, "-c", src, "-o", obj]

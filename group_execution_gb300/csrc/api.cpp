@@ -115,7 +115,7 @@ void fg_build_opts_default(fg_build_opts* o) {
   o->max_fused_ops = 256;
   o->max_args = 64;
   o->allow_reduce_epilogue = 0;
-  o->reserved = 0;
+  o->flags = 0;
   o->wait_limit_ns = 2000000000LL;
 }
 
@@ -326,17 +326,27 @@ void prepare_group(GroupExec& ge, const BuildOpts& o, int nsm) {
   p.stage_bytes = cg.stage_bytes;
   p.nstages = cg.nstages;
   p.tx_bytes = tx;
-  p.out_tma = cg.out_tma ? 1 : 0;
+  p.out_tma = cg.out_tma;
+  p.band = (o.flags >> 8) & 0xff;
   p.wait_limit_ns = o.wait_limit_ns;
   ge.big = std::max(cg.depth, cg.epi_depth) > 4 || std::max(cg.slots, cg.epi_slots) > 4;
   const int ctas = std::min(cg.ctas_per_sm, ge.big ? 1 : 2);
   ge.smem = cg.smem_bytes;
   if (cg.exec == FG_EXEC_REDUCE) {
     p.red_op = cg.red_op;
-    const int want = 2 * ctas * nsm;
-    int nsplit = (want + p.ntr - 1) / p.ntr;
-    nsplit = std::max(1, std::min(nsplit, std::max(1, p.ntc / 4)));
-    int tps = (p.ntc + nsplit - 1) / nsplit;
+    // units are (32-row strip, run of column tiles), walked in row-major
+    // order
+    const int unit = (o.flags >> 16) & 0xff;
+    int tps, nsplit;
+    if (unit > 0) {
+      tps = std::min(p.ntc, unit);
+    } else {
+      // enough units for two waves of CTAs, each unit long enough to
+      // amortise its combine step
+      const int want = 2 * ctas * nsm;
+      nsplit = std::max(1, std::min((want + p.ntr - 1) / p.ntr, std::max(1, p.ntc / 16)));
+      tps = (p.ntc + nsplit - 1) / nsplit;
+    }
     nsplit = (p.ntc + tps - 1) / tps;
     p.nsplit = nsplit;
     p.tiles_per_split = tps;
@@ -353,7 +363,7 @@ GroupExec make_exec(const Graph& g, const std::vector<int32_t>& nodes, const Bui
   GroupExec ge;
   try {
     ge.cg = compile_group(g, nodes);
-    plan_staging(g, ge.cg);
+    plan_staging(g, ge.cg, o);
     if (ge.cg.exec == FG_EXEC_GEMM) {
       ge.compile_status = FG_EUNSUPPORTED;
       ge.compile_error = "GEMM groups are not available in this build";
@@ -473,9 +483,16 @@ fg_status launch_exec(fg_plan* p, GroupExec& ge, void* const* ptrs, void* stream
     for (size_t i = 0; i < cg.epi_leaf_values.size(); ++i)
       gp.epi_leaf[i] = static_cast<const float*>(ptrs[cg.epi_leaf_values[i]]);
     gp.out = static_cast<float*>(ptrs[cg.out_value]);
-    if (cg.exec == FG_EXEC_ELEMWISE && cg.out_tma)
+    if (cg.exec == FG_EXEC_ELEMWISE && cg.out_tma == 1)
       if (fg_status st = leaf_map(&gp.maps[kMaxStaged], ptrs[cg.out_value], LEAF_IDENT, cg.FR, cg.FC, kTileR, kTileC))
         return st;
+    if (cg.exec == FG_EXEC_ELEMWISE && cg.out_tma == 2) {
+      // one warp's 32 x 8 slice per store
+      uint64_t dims[2] = {(uint64_t)cg.FC, (uint64_t)cg.FR};
+      uint64_t strides[1] = {(uint64_t)(cg.FR == 1 ? round_up(cg.FC * 4, 16) : cg.FC * 4)};
+      uint32_t box[2] = {8, (uint32_t)kTileR};
+      if (fg_status st = encode(&gp.maps[kMaxStaged], ptrs[cg.out_value], 2, dims, strides, box, false)) return st;
+    }
     ge.last_ptrs = key;
   }
   cudaError_t e = launch_group_kernel(gp, cg.exec == FG_EXEC_REDUCE ? 1 : 0, ge.big ? 1 : 0, ge.grid, ge.smem,
@@ -506,6 +523,7 @@ fg_status fg_build_groups(const fg_graph* gh, const fg_build_opts* opts, fg_plan
   p->opts.max_args = o.max_args;
   p->opts.allow_reduce_epilogue = o.allow_reduce_epilogue;
   p->opts.wait_limit_ns = o.wait_limit_ns > 0 ? o.wait_limit_ns : 2000000000LL;
+  p->opts.flags = o.flags;
   p->has_device = device_present(&p->nsm);
   partition(p->g, p->opts, p->group_of, p->ipdom);
   std::vector<int32_t> sinks;

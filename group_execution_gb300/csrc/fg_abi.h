@@ -16,34 +16,53 @@ namespace fg {
 // ---- operator program --------------------------------------------------------
 // A group compiles to a postfix program over a small register stack.  The
 // host knows the stack depth before every instruction, so each instruction
-// carries a dispatch key that already names (operation, depth[, slot]); the
-// device switches on it and every register index is a compile-time constant.
+// carries a dense case number that already names (operation, depth[, slot]);
+// the device switches on it and every register index is a compile-time
+// constant.  Binary operators also come in forms whose right operand is a
+// leaf or a save slot, which saves a push.
 constexpr int kMaxDepth = 8;   // stack registers in the largest machine
 constexpr int kMaxSlots = 8;   // save slots (values reused inside a group)
 
 enum VmOp : int {
   VM_PUSH_LEAF = 0,  // push leaf `arg` read at this thread's frame points
   VM_PUSH_ACC,       // push the accumulator (GEMM tile value / reduced row value)
-  VM_ADD, VM_SUB, VM_MUL, VM_DIV,           // s[d-2] = s[d-2] op s[d-1]; pop
-  VM_SCALE, VM_ADDC,                         // s[d-1] = imm*s / s+imm
+  VM_ADD, VM_SUB, VM_MUL, VM_DIV,           // TOP = below op TOP; pop
+  VM_SCALE, VM_ADDC,                         // TOP = imm*TOP / TOP+imm
   VM_RELU, VM_EXP, VM_SIGMOID, VM_TANH, VM_NEG,
-  VM_NUM_STACK_OPS,
-  // slot ops: PUSH_SLOT pushes slot `arg`; TEE copies the top into slot `arg`;
-  // STORE copies the top into slot `arg` and pops.
-  VM_PUSH_SLOT = 16, VM_TEE = 17, VM_STORE = 18,
+  VM_ADD_L, VM_SUB_L, VM_MUL_L, VM_DIV_L,    // TOP = TOP op leaf[arg]
+  VM_ADD_S, VM_SUB_S, VM_MUL_S, VM_DIV_S,    // TOP = TOP op slot
+  VM_PUSH_SLOT,      // push slot
+  VM_TEE,            // copy TOP into slot
+  VM_STORE,          // copy TOP into slot and pop
 };
 
-// depth before an instruction is 0..kMaxDepth, so keys step by 16
-constexpr int kKeyStride = 16;
-constexpr int kSlotKeyBase = 256;
-FG_HD constexpr int vm_key(int op, int depth) { return op * kKeyStride + depth; }
-FG_HD constexpr int vm_slot_key(int op, int slot, int depth) {
-  return kSlotKeyBase + (((op - VM_PUSH_SLOT) * kMaxSlots + slot) * kKeyStride + depth);
+// Dense case numbers (no holes, so the device switch is one jump table).
+constexpr int kCaseLeaf = 0;                                // + d, d in [0, 8)
+constexpr int kCaseAcc = kCaseLeaf + kMaxDepth;             // + d
+constexpr int kCaseBin = kCaseAcc + kMaxDepth;              // + (op-ADD)*(8-1) + (d-2), d in [2, 8]
+constexpr int kCaseUn = kCaseBin + 4 * (kMaxDepth - 1);     // + (op-SCALE)
+constexpr int kCaseBinL = kCaseUn + 7;                      // + (op-ADD_L)
+constexpr int kCaseBinS = kCaseBinL + 4;                    // + (op-ADD_S)*8 + s
+constexpr int kCasePushS = kCaseBinS + 4 * kMaxSlots;       // + s*8 + d, d in [0, 8)
+constexpr int kCaseTee = kCasePushS + kMaxSlots * kMaxDepth;  // + s
+constexpr int kCaseStore = kCaseTee + kMaxSlots;            // + s*8 + (d-1), d in [1, 8]
+constexpr int kNumCases = kCaseStore + kMaxSlots * kMaxDepth;
+
+FG_HD constexpr int vm_case(int op, int depth, int slot) {
+  return op == VM_PUSH_LEAF ? kCaseLeaf + depth
+       : op == VM_PUSH_ACC ? kCaseAcc + depth
+       : op <= VM_DIV ? kCaseBin + (op - VM_ADD) * (kMaxDepth - 1) + (depth - 2)
+       : op <= VM_NEG ? kCaseUn + (op - VM_SCALE)
+       : op <= VM_DIV_L ? kCaseBinL + (op - VM_ADD_L)
+       : op <= VM_DIV_S ? kCaseBinS + (op - VM_ADD_S) * kMaxSlots + slot
+       : op == VM_PUSH_SLOT ? kCasePushS + slot * kMaxDepth + depth
+       : op == VM_TEE ? kCaseTee + slot
+       : kCaseStore + slot * kMaxDepth + (depth - 1);
 }
 
 struct VmInstr {
-  uint16_t key;   // dispatch key (vm_key / vm_slot_key)
-  uint16_t arg;   // leaf index for PUSH_LEAF (slot ops encode the slot in the key)
+  uint16_t key;   // dense case number (vm_case)
+  uint16_t arg;   // leaf index for PUSH_LEAF and the *_L forms
   float imm;      // SCALE / ADDC immediate
 };
 
@@ -81,6 +100,7 @@ constexpr int kMaxEpiLeaves = 8;
 constexpr int kTileR = 32;
 constexpr int kTileC = 64;
 constexpr int kConsumerWarps = 8;
+constexpr int kMaxStages = 16;
 
 enum RedOp : int { RED_NONE = 0, RED_SUM = 1, RED_MAX = 2 };
 
@@ -99,7 +119,8 @@ struct GroupParams {
   int32_t FR, FC;                      // frame
   int32_t ntr, ntc, ntiles;            // tile grid
   int32_t stage_bytes, nstages, tx_bytes;   // stage stride, depth, bytes TMA writes per stage
-  int32_t out_tma;                     // 1: output via TMA store, 0: direct stores
+  int32_t out_tma;                     // 1: CTA tile via smem + TMA store, 2: per-warp TMA slices, 0: direct stores
+  int32_t band;                        // tile order: 0 row-major, else bands of `band` tile rows
   int32_t red_op, nsplit, tiles_per_split, nunits;
 };
 

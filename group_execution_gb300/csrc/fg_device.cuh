@@ -105,10 +105,10 @@ __device__ __forceinline__ float op_sigmoid(float x) { return __frcp_rn(__fadd_r
 // ---- the register-stack machine -------------------------------------------------
 // V values per thread.  The top of the stack lives in TOP; the entries below
 // it in R[0..D-2]; S save slots hold values a group reuses.  Unary operators
-// act on TOP whatever the depth, so their code exists once; only moves
-// between TOP, R and the slots depend on the depth, and those use
-// compile-time register indices.  `Env` provides load_leaf(arg, float(&)[V])
-// and load_acc(float(&)[V]).
+// and the leaf-operand forms act on TOP whatever the depth, so their code
+// exists once; only moves between TOP, R and the slots depend on the depth,
+// and those use compile-time register indices.  `Env` provides
+// load_leaf(arg, float(&)[V]) and load_acc(float(&)[V]).
 template <int D, int S, int V>
 struct Machine {
   float TOP[V];
@@ -147,9 +147,23 @@ struct Machine {
       for (int i = 0; i < V; ++i) t[i] = R[d - 2][i];
     }
   }
-  // The empty asm statements keep the compiler from merging the per-(slot,
-  // depth) cases into one indexed access, which would move the slots to
-  // local memory.
+  // The empty asm statements keep the compiler from merging the per-slot
+  // cases into one indexed access, which would move the slots to local
+  // memory.
+  template <int op, int s>
+  __device__ __forceinline__ void slot_bin(float (&t)[V]) {
+    if constexpr (s < S) {
+      asm volatile("");
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const float b = SL[s][i];
+        if constexpr (op == VM_ADD_S) TOP[i] = __fadd_rn(TOP[i], b);
+        else if constexpr (op == VM_SUB_S) TOP[i] = __fsub_rn(TOP[i], b);
+        else if constexpr (op == VM_MUL_S) TOP[i] = __fmul_rn(TOP[i], b);
+        else t[i] = b;
+      }
+    }
+  }
   template <int s, int d>
   __device__ __forceinline__ void push_slot() {
     if constexpr (s < S && d < D) {
@@ -162,9 +176,9 @@ struct Machine {
       for (int i = 0; i < V; ++i) TOP[i] = SL[s][i];
     }
   }
-  template <int s, int d>
+  template <int s>
   __device__ __forceinline__ void tee() {
-    if constexpr (s < S && d >= 1) {
+    if constexpr (s < S) {
       asm volatile("");
 #pragma unroll
       for (int i = 0; i < V; ++i) SL[s][i] = TOP[i];
@@ -187,73 +201,92 @@ struct Machine {
   // Runs `n` instructions; the result is TOP.
   template <class Env>
   __device__ __forceinline__ void run(const VmInstr* prog, int n, Env& env) {
+#pragma unroll 1
     for (int pc = 0; pc < n; ++pc) {
       const VmInstr ins = prog[pc];
       const int key = ins.key;
       float t[V];
-      if (key < kKeyStride) env.load_leaf(ins.arg, t);        // VM_PUSH_LEAF at any depth
-      else if (key < 2 * kKeyStride) env.load_acc(t);         // VM_PUSH_ACC at any depth
-      bool div = false;
+      if (key < kCaseAcc || (key >= kCaseBinL && key < kCaseBinS)) env.load_leaf(ins.arg, t);
+      else if (key < kCaseBin) env.load_acc(t);
+      int dv = 0;   // 1: TOP = t / TOP, 2: TOP = TOP / t
       switch (key) {
-#define FG_ALL_D(op)                                                                    \
-  case vm_key(op, 0): case vm_key(op, 1): case vm_key(op, 2): case vm_key(op, 3):      \
-  case vm_key(op, 4): case vm_key(op, 5): case vm_key(op, 6): case vm_key(op, 7):      \
-  case vm_key(op, 8):
-        FG_ALL_D(VM_SCALE)
+#define FG_PUSH(d) \
+  case kCaseLeaf + d: push<d>(t); break; \
+  case kCaseAcc + d: push<d>(t); break;
+#define FG_BIN(d) \
+  case vm_case(VM_ADD, d, 0): bin<VM_ADD, d>(); break; \
+  case vm_case(VM_SUB, d, 0): bin<VM_SUB, d>(); break; \
+  case vm_case(VM_MUL, d, 0): bin<VM_MUL, d>(); break; \
+  case vm_case(VM_DIV, d, 0): second<d>(t); dv = 1; break;
+#define FG_SLOT_D(s, d) case vm_case(VM_PUSH_SLOT, d, s): push_slot<s, d>(); break;
+#define FG_STORE_D(s, d) case vm_case(VM_STORE, d, s): store<s, d>(); break;
+#define FG_SLOT(s) \
+  case vm_case(VM_ADD_S, 0, s): slot_bin<VM_ADD_S, s>(t); break; \
+  case vm_case(VM_SUB_S, 0, s): slot_bin<VM_SUB_S, s>(t); break; \
+  case vm_case(VM_MUL_S, 0, s): slot_bin<VM_MUL_S, s>(t); break; \
+  case vm_case(VM_DIV_S, 0, s): slot_bin<VM_DIV_S, s>(t); dv = 2; break; \
+  case vm_case(VM_TEE, 0, s): tee<s>(); break; \
+  FG_SLOT_D(s, 0) FG_SLOT_D(s, 1) FG_SLOT_D(s, 2) FG_SLOT_D(s, 3) \
+  FG_SLOT_D(s, 4) FG_SLOT_D(s, 5) FG_SLOT_D(s, 6) FG_SLOT_D(s, 7) \
+  FG_STORE_D(s, 1) FG_STORE_D(s, 2) FG_STORE_D(s, 3) FG_STORE_D(s, 4) \
+  FG_STORE_D(s, 5) FG_STORE_D(s, 6) FG_STORE_D(s, 7) FG_STORE_D(s, 8)
+        FG_PUSH(0) FG_PUSH(1) FG_PUSH(2) FG_PUSH(3) FG_PUSH(4) FG_PUSH(5) FG_PUSH(6) FG_PUSH(7)
+        FG_BIN(2) FG_BIN(3) FG_BIN(4) FG_BIN(5) FG_BIN(6) FG_BIN(7) FG_BIN(8)
+        case kCaseUn + (VM_SCALE - VM_SCALE):
 #pragma unroll
           for (int i = 0; i < V; ++i) TOP[i] = __fmul_rn(ins.imm, TOP[i]);
           break;
-        FG_ALL_D(VM_ADDC)
+        case kCaseUn + (VM_ADDC - VM_SCALE):
 #pragma unroll
           for (int i = 0; i < V; ++i) TOP[i] = __fadd_rn(TOP[i], ins.imm);
           break;
-        FG_ALL_D(VM_RELU)
+        case kCaseUn + (VM_RELU - VM_SCALE):
 #pragma unroll
           for (int i = 0; i < V; ++i) TOP[i] = op_relu(TOP[i]);
           break;
-        FG_ALL_D(VM_EXP)
+        case kCaseUn + (VM_EXP - VM_SCALE):
 #pragma unroll
           for (int i = 0; i < V; ++i) TOP[i] = expf(TOP[i]);
           break;
-        FG_ALL_D(VM_SIGMOID)
+        case kCaseUn + (VM_SIGMOID - VM_SCALE):
 #pragma unroll
           for (int i = 0; i < V; ++i) TOP[i] = op_sigmoid(TOP[i]);
           break;
-        FG_ALL_D(VM_TANH)
+        case kCaseUn + (VM_TANH - VM_SCALE):
 #pragma unroll
           for (int i = 0; i < V; ++i) TOP[i] = tanhf(TOP[i]);
           break;
-        FG_ALL_D(VM_NEG)
+        case kCaseUn + (VM_NEG - VM_SCALE):
 #pragma unroll
           for (int i = 0; i < V; ++i) TOP[i] = -TOP[i];
           break;
-#undef FG_ALL_D
-#define FG_CASES_D(d)                                                         \
-  case vm_key(VM_PUSH_LEAF, d): push<d>(t); break;                            \
-  case vm_key(VM_PUSH_ACC, d): push<d>(t); break;                             \
-  case vm_key(VM_ADD, d): bin<VM_ADD, d>(); break;                            \
-  case vm_key(VM_SUB, d): bin<VM_SUB, d>(); break;                            \
-  case vm_key(VM_MUL, d): bin<VM_MUL, d>(); break;                            \
-  case vm_key(VM_DIV, d): second<d>(t); div = true; break;
-#define FG_CASES_SD(s, d)                                                     \
-  case vm_slot_key(VM_PUSH_SLOT, s, d): push_slot<s, d>(); break;             \
-  case vm_slot_key(VM_TEE, s, d): tee<s, d>(); break;                         \
-  case vm_slot_key(VM_STORE, s, d): store<s, d>(); break;
-#define FG_CASES_S(s) \
-  FG_CASES_SD(s, 0) FG_CASES_SD(s, 1) FG_CASES_SD(s, 2) FG_CASES_SD(s, 3) \
-  FG_CASES_SD(s, 4) FG_CASES_SD(s, 5) FG_CASES_SD(s, 6) FG_CASES_SD(s, 7) FG_CASES_SD(s, 8)
-        FG_CASES_D(0) FG_CASES_D(1) FG_CASES_D(2) FG_CASES_D(3)
-        FG_CASES_D(4) FG_CASES_D(5) FG_CASES_D(6) FG_CASES_D(7) FG_CASES_D(8)
-        FG_CASES_S(0) FG_CASES_S(1) FG_CASES_S(2) FG_CASES_S(3)
-        FG_CASES_S(4) FG_CASES_S(5) FG_CASES_S(6) FG_CASES_S(7)
-#undef FG_CASES_S
-#undef FG_CASES_SD
-#undef FG_CASES_D
+        case kCaseBinL + 0:
+#pragma unroll
+          for (int i = 0; i < V; ++i) TOP[i] = __fadd_rn(TOP[i], t[i]);
+          break;
+        case kCaseBinL + 1:
+#pragma unroll
+          for (int i = 0; i < V; ++i) TOP[i] = __fsub_rn(TOP[i], t[i]);
+          break;
+        case kCaseBinL + 2:
+#pragma unroll
+          for (int i = 0; i < V; ++i) TOP[i] = __fmul_rn(TOP[i], t[i]);
+          break;
+        case kCaseBinL + 3: dv = 2; break;
+        FG_SLOT(0) FG_SLOT(1) FG_SLOT(2) FG_SLOT(3) FG_SLOT(4) FG_SLOT(5) FG_SLOT(6) FG_SLOT(7)
+#undef FG_SLOT
+#undef FG_STORE_D
+#undef FG_SLOT_D
+#undef FG_BIN
+#undef FG_PUSH
         default: break;
       }
-      if (div) {
+      if (dv) {
 #pragma unroll
-        for (int i = 0; i < V; ++i) TOP[i] = __fdiv_rn(t[i], TOP[i]);
+        for (int i = 0; i < V; ++i) {
+          const float a = dv == 1 ? t[i] : TOP[i], b = dv == 1 ? TOP[i] : t[i];
+          TOP[i] = __fdiv_rn(a, b);
+        }
       }
     }
   }

@@ -4,7 +4,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/groupexec.h"
+#include "groupexec.h"
 #include "fg_abi.h"
 
 namespace fg {
@@ -80,13 +80,14 @@ struct CompiledGroup {
   // staging decisions (filled by plan_staging)
   int nstaged = 0, ngathered = 0, stage_bytes = 0, nstages = 0, nsplit = 1;
   int tiles_per_split = 0;
-  bool out_tma = true;
+  int out_tma = 1;
   std::vector<int> leaf_stage_off;    // byte offset inside a stage, -1 = gathered
   int smem_bytes = 0, ctas_per_sm = 2;
 };
 
 struct BuildOpts {
   int max_fused_ops = 256, max_args = 64, allow_reduce_epilogue = 0;
+  int flags = 0;   // bit 0: stage the output in smem and store it with TMA; bits 8-15: tile band
   int64_t wait_limit_ns = 2000000000LL;
 };
 
@@ -100,6 +101,6 @@ struct CompileError {
   std::string msg;
 };
 CompiledGroup compile_group(const Graph& g, const std::vector<int32_t>& nodes);
-void plan_staging(const Graph& g, CompiledGroup& cg);
+void plan_staging(const Graph& g, CompiledGroup& cg, const BuildOpts& o);
 
 }  // namespace fg

@@ -260,9 +260,9 @@ struct Emitter {
     return e.need;
   }
 
-  void put(int key, int arg = 0, float imm = 0.f) {
+  void put(int op, int slot = 0, int arg = 0, float imm = 0.f) {
     if ((int)code.size() >= kMaxProg) fail(FG_EUNSUPPORTED, "group program too long");
-    code.push_back(VmInstr{(uint16_t)key, (uint16_t)arg, imm});
+    code.push_back(VmInstr{(uint16_t)vm_case(op, depth, slot), (uint16_t)arg, imm});
   }
   void push_depth() {
     ++depth;
@@ -278,54 +278,67 @@ struct Emitter {
       }
     return -1;
   }
+  // a value that can be the right operand of a binary op without a push
+  bool direct(int i) const { return ex[i].kind == E_LEAF || slot_of[i] >= 0; }
+  void use_slot(int i) {
+    if (--remaining[i] == 0) slot_busy[slot_of[i]] = 0;
+  }
 
   // Emit code that leaves expr i on top of the stack.
   void emit(int i) {
     Expr& e = ex[i];
     if (slot_of[i] >= 0) {
-      int s = slot_of[i];
-      put(vm_slot_key(VM_PUSH_SLOT, s, depth));
+      put(VM_PUSH_SLOT, slot_of[i]);
       push_depth();
-      if (--remaining[i] == 0) slot_busy[s] = 0;
+      use_slot(i);
       return;
     }
     switch (e.kind) {
       case E_LEAF:
-        put(vm_key(VM_PUSH_LEAF, depth), e.leaf);
+        put(VM_PUSH_LEAF, 0, e.leaf);
         push_depth();
-        break;
+        return;   // leaves are re-read from shared memory, never kept in slots
       case E_ACC:
-        put(vm_key(VM_PUSH_ACC, depth));
+        put(VM_PUSH_ACC);
         push_depth();
         break;
       case E_UN:
         emit(e.a);
-        put(vm_key(e.vm, depth), 0, e.imm);
+        put(e.vm, 0, 0, e.imm);
         break;
       case E_BIN: {
         int a = e.a, b = e.b;
-        bool comm = e.vm == VM_ADD || e.vm == VM_MUL;
-        if (comm && ex[b].need > ex[a].need) std::swap(a, b);
+        const bool comm = e.vm == VM_ADD || e.vm == VM_MUL;
+        if (comm && (direct(a) && !direct(b))) std::swap(a, b);
+        else if (comm && !direct(b) && ex[b].need > ex[a].need) std::swap(a, b);
+        const int off = e.vm - VM_ADD;
+        if (direct(b)) {
+          emit(a);
+          if (ex[b].kind == E_LEAF) {
+            put(VM_ADD_L + off, 0, ex[b].leaf);
+          } else {
+            put(VM_ADD_S + off, slot_of[b]);
+            use_slot(b);
+          }
+          break;
+        }
         // evaluate a deep right operand into a slot first if the stack
         // would overflow otherwise
-        int spill = -1;
-        if (slot_of[b] < 0 && depth + std::max(ex[a].need, ex[b].need + 1) > kMaxDepth) {
-          spill = alloc_slot();
+        if (depth + std::max(ex[a].need, ex[b].need + 1) > kMaxDepth) {
+          int spill = alloc_slot();
           if (spill >= 0) {
             emit(b);
-            put(vm_slot_key(VM_STORE, spill, depth));
+            put(VM_STORE, spill);
             --depth;
+            emit(a);
+            put(VM_ADD_S + off, spill);
+            slot_busy[spill] = 0;
+            break;
           }
         }
         emit(a);
-        if (spill >= 0) {
-          put(vm_slot_key(VM_PUSH_SLOT, spill, depth));
-          push_depth();
-          slot_busy[spill] = 0;
-        } else {
-          emit(b);
-        }
-        put(vm_key(e.vm, depth));
+        emit(b);
+        put(e.vm);
         --depth;
         break;
       }
@@ -335,7 +348,7 @@ struct Emitter {
       int s = alloc_slot();
       if (s < 0) fail(FG_EUNSUPPORTED, "group program keeps more than 8 values live");
       slot_of[i] = s;
-      put(vm_slot_key(VM_TEE, s, depth));
+      put(VM_TEE, s);
     }
   }
 };
@@ -476,7 +489,7 @@ CompiledGroup compile_group(const Graph& g, const std::vector<int32_t>& nodes_in
 // depth.  A TMA tensor needs 16-byte row strides, so IDENT leaves need a
 // frame width that is a multiple of 4 floats and TRANS leaves a frame height
 // that is.  Everything else is gathered from global memory.
-void plan_staging(const Graph& g, CompiledGroup& cg) {
+void plan_staging(const Graph& g, CompiledGroup& cg, const BuildOpts& o) {
   (void)g;
   const bool gemm = cg.exec == FG_EXEC_GEMM;
   const int TR = gemm ? 128 : kTileR, TC = gemm ? 32 : kTileC;
@@ -490,7 +503,10 @@ void plan_staging(const Graph& g, CompiledGroup& cg) {
   };
   const bool rows_ok = cg.FC % 4 == 0 || cg.FR == 1;
   const bool cols_ok = cg.FR % 4 == 0 || cg.FC == 1;
-  cg.out_tma = rows_ok;
+  // output: 1 = CTA tile staged in smem + TMA store, 2 = per-warp slices
+  // stored by TMA, 0 = direct stores
+  const int omode = (o.flags >> 24) & 3;
+  cg.out_tma = (rows_ok && cg.exec == FG_EXEC_ELEMWISE) ? (omode == 0 ? 2 : omode == 3 ? 0 : omode) : 0;
   std::vector<char> stage(cg.leaves.size(), 0);
   int want = 0;
   for (size_t i = 0; i < cg.leaves.size(); ++i) {
@@ -518,10 +534,11 @@ void plan_staging(const Graph& g, CompiledGroup& cg) {
   };
   int fixed = 2048;   // barriers + alignment slack
   if (!gemm) {
-    if (cg.out_tma) fixed += 3 * TR * TC * 4;               // three output buffers
+    if (cg.out_tma) fixed += 3 * TR * TC * 4;               // three output buffers (per CTA or per warp)
     if (cg.exec == FG_EXEC_REDUCE) fixed += 2 * kConsumerWarps * 32 * 4;   // double-buffered row partials
   }
-  const int budget_two = 112 * 1024, budget_one = 224 * 1024;
+  // dynamic shared memory per CTA; about 5 KB of static tables come on top
+  const int budget_two = 106 * 1024, budget_one = 218 * 1024;
   int sb = layout(nullptr);
   int budget = budget_two;
   if (!gemm) {
@@ -559,7 +576,7 @@ void plan_staging(const Graph& g, CompiledGroup& cg) {
   }
   if (!gemm) {
     int ns = cg.stage_bytes ? (budget - fixed) / cg.stage_bytes : 4;
-    cg.nstages = std::max(2, std::min(ns, 6));
+    cg.nstages = std::max(2, std::min(ns, kMaxStages));
     cg.smem_bytes = fixed + cg.nstages * cg.stage_bytes;
     cg.ctas_per_sm = budget == budget_two ? 2 : 1;
   }

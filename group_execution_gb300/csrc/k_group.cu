@@ -51,14 +51,34 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int
 // are 128 bytes long.
 __device__ __forceinline__ int swz(int row, int chunk) { return row * 128 + ((chunk ^ (row & 7)) << 4); }
 
+// The program and the leaf table are copied to shared memory once per CTA:
+// every thread reads them at every instruction.
+struct LeafInfo {
+  int32_t cls, stage_off, map_idx, pad;
+};
+
+struct SmemTables {
+  VmInstr prog[kMaxProg];
+  VmInstr epi[kMaxEpi];
+  LeafInfo leaf[kMaxLeaves];
+};
+
+__device__ __forceinline__ void load_tables(SmemTables& T, const GroupParams& P) {
+  for (int i = threadIdx.x; i < P.nprog; i += blockDim.x) T.prog[i] = P.prog[i];
+  for (int i = threadIdx.x; i < P.nepi; i += blockDim.x) T.epi[i] = P.epi[i];
+  for (int i = threadIdx.x; i < P.nleaves; i += blockDim.x)
+    T.leaf[i] = LeafInfo{P.leaves[i].cls, P.leaves[i].stage_off, P.leaves[i].map_idx, 0};
+}
+
 // Leaf reads for one thread: 8 frame points (r0+lr, c0+lc0 .. c0+lc0+7).
 struct TileEnv {
   const GroupParams& P;
+  const LeafInfo* leaf;
   const uint8_t* stage;
   int lr, lc0, r0, c0;
 
   __device__ __forceinline__ void load_leaf(int arg, float (&t)[8]) const {
-    const LeafDesc& L = P.leaves[arg];
+    const LeafInfo L = leaf[arg];
     const int cls = L.cls;
     if (cls == LEAF_IDENT) {
       const uint8_t* b = stage + L.stage_off + (lc0 >> 5) * (kTileR * 128);
@@ -85,6 +105,7 @@ struct TileEnv {
     } else {
       // gather: f = sum_k ((g / d_k) % m_k) * s_k over g = r*FC + c
       // (frames with gathered leaves hold fewer than 2^31 elements)
+      const LeafDesc& G = P.leaves[arg];
       const int r = r0 + lr;
 #pragma unroll 1
       for (int k = 0; k < 8; ++k) {
@@ -93,9 +114,9 @@ struct TileEnv {
         if (r < P.FR && c < P.FC) {
           const uint32_t g = (uint32_t)r * (uint32_t)P.FC + (uint32_t)c;
           uint32_t f = 0;
-          for (int q = 0; q < L.nterms; ++q)
-            f += ((g / (uint32_t)L.d[q]) % (uint32_t)L.m[q]) * (uint32_t)L.s[q];
-          v = __ldg(L.ptr + f);
+          for (int q = 0; q < G.nterms; ++q)
+            f += ((g / (uint32_t)G.d[q]) % (uint32_t)G.m[q]) * (uint32_t)G.s[q];
+          v = __ldg(G.ptr + f);
         }
         t[k] = v;
       }
@@ -109,11 +130,12 @@ struct TileEnv {
 
 // The producer: one elected thread issues the TMA loads of every staged leaf
 // for tile (tr, tc) into stage `st`.
-__device__ __forceinline__ void issue_tile(const GroupParams& P, uint32_t st, uint32_t bar, int tr, int tc) {
+__device__ __forceinline__ void issue_tile(const GroupParams& P, const LeafInfo* leaf, uint32_t st, uint32_t bar,
+                                           int tr, int tc) {
   const int r0 = tr * kTileR, c0 = tc * kTileC;
   mbar_expect_tx(bar, P.tx_bytes);
   for (int j = 0; j < P.nleaves; ++j) {
-    const LeafDesc& L = P.leaves[j];
+    const LeafInfo L = leaf[j];
     if (L.cls == LEAF_GATHER) continue;
     const CUtensorMap* m = &P.maps[L.map_idx];
     const uint32_t dst = st + L.stage_off;
@@ -148,10 +170,10 @@ __device__ __forceinline__ void drain_producer(const GroupParams& P, const Ring&
 }
 
 template <class Tiles>
-__device__ __forceinline__ void producer_loop(const GroupParams& P, const Ring& R, Tiles tiles,
+__device__ __forceinline__ void producer_loop(const GroupParams& P, const LeafInfo* leaf, const Ring& R, Tiles tiles,
                                               volatile int* abort_flag) {
   for (int j = 0; j < P.nleaves; ++j)
-    if (P.leaves[j].cls != LEAF_GATHER) tma_prefetch(&P.maps[P.leaves[j].map_idx]);
+    if (leaf[j].cls != LEAF_GATHER) tma_prefetch(&P.maps[leaf[j].map_idx]);
   const int NS = P.nstages;
   int i = 0;
   int tr, tc;
@@ -162,7 +184,7 @@ __device__ __forceinline__ void producer_loop(const GroupParams& P, const Ring& 
       ok = false;
       break;
     }
-    issue_tile(P, R.base_s + s * P.stage_bytes, R.full_s + 8 * s, tr, tc);
+    issue_tile(P, leaf, R.base_s + s * P.stage_bytes, R.full_s + 8 * s, tr, tc);
     ++i;
   }
   if (!ok) {
@@ -173,12 +195,27 @@ __device__ __forceinline__ void producer_loop(const GroupParams& P, const Ring& 
 }
 
 // Tile sequences --------------------------------------------------------------------
-struct EwTiles {
-  int t, step, ntiles, ntc;
-  __device__ __forceinline__ bool next(int& tr, int& tc) {
-    if (t >= ntiles) return false;
+// Linear tile index -> (tile row, tile col): row-major, or column-major inside
+// bands of `band` tile rows so that the tiles in flight at once form a
+// compact block of both the frame and a transposed leaf.
+__device__ __forceinline__ void tile_coords(int t, int ntr, int ntc, int band, int& tr, int& tc) {
+  if (band <= 0) {
     tr = t / ntc;
     tc = t % ntc;
+    return;
+  }
+  const int per = band * ntc;
+  const int b = t / per, local = t - b * per;
+  const int rows = min(band, ntr - b * band);
+  tr = b * band + local % rows;
+  tc = local / rows;
+}
+
+struct EwTiles {
+  int t, step, ntiles, ntr, ntc, band;
+  __device__ __forceinline__ bool next(int& tr, int& tc) {
+    if (t >= ntiles) return false;
+    tile_coords(t, ntr, ntc, band, tr, tc);
     t += step;
     return true;
   }
@@ -206,7 +243,7 @@ struct RedTiles {   // units (row strip, column split), then the split's tiles
 __device__ __forceinline__ Ring setup_ring(uint8_t* smem, const GroupParams& P) {
   Ring R;
   R.full_s = smem_u32(smem);
-  R.empty_s = R.full_s + 64;
+  R.empty_s = R.full_s + 8 * kMaxStages;
   R.base = smem + 1024;
   R.base_s = smem_u32(R.base);
   return R;
@@ -239,10 +276,12 @@ template <int D, int S>
 __global__ void __launch_bounds__(kThreads, D <= 4 ? 2 : 1) fg_ew_group_kernel(const __grid_constant__ GroupParams P) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int abort_flag;
+  __shared__ SmemTables T;
   uint8_t* smem = align1024(smem_raw);
   const Ring R = setup_ring(smem, P);
   uint8_t* outbuf = R.base + P.nstages * P.stage_bytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  load_tables(T, P);
   if (threadIdx.x == 0) {
     abort_flag = 0;
     init_barriers(R, P.nstages);
@@ -251,53 +290,89 @@ __global__ void __launch_bounds__(kThreads, D <= 4 ? 2 : 1) fg_ew_group_kernel(c
   __syncthreads();
 
   if (warp == kConsumerWarps) {
-    if (lane == 0) producer_loop(P, R, EwTiles{(int)blockIdx.x, (int)gridDim.x, P.ntiles, P.ntc}, &abort_flag);
+    if (lane == 0)
+      producer_loop(P, T.leaf, R, EwTiles{(int)blockIdx.x, (int)gridDim.x, P.ntiles, P.ntr, P.ntc, P.band},
+                    &abort_flag);
     return;
   }
 
   const int NS = P.nstages;
   const int lr = lane, lc0 = warp * 8;
   Machine<D, S, 8> M;
+  const bool vec_store = (P.FC & 3) == 0 && (reinterpret_cast<uintptr_t>(P.out) & 15) == 0;
   int i = 0;
   for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x, ++i) {
     const int s = i % NS;
-    const int tr = t / P.ntc, tc = t % P.ntc;
+    int tr, tc;
+    tile_coords(t, P.ntr, P.ntc, P.band, tr, tc);
     const int r0 = tr * kTileR, c0 = tc * kTileC;
     const bool got = wait_or_abort(R.full_s + 8 * s, (i / NS) & 1, P.wait_limit_ns, &abort_flag);
     uint8_t* ob = outbuf + (i % 3) * kOutBufBytes;
     if (got) {
-      TileEnv env{P, R.base + s * P.stage_bytes, lr, lc0, r0, c0};
-      M.run(P.prog, P.nprog, env);
-      if (P.out_tma) {
+      TileEnv env{P, T.leaf, R.base + s * P.stage_bytes, lr, lc0, r0, c0};
+      M.run(T.prog, P.nprog, env);
+      if (P.out_tma == 1) {
         uint8_t* b = ob + (lc0 >> 5) * (kTileR * 128);
         const int j0 = (lc0 & 31) >> 2;
         *reinterpret_cast<float4*>(b + swz(lr, j0)) = make_float4(M.TOP[0], M.TOP[1], M.TOP[2], M.TOP[3]);
         *reinterpret_cast<float4*>(b + swz(lr, j0 + 1)) = make_float4(M.TOP[4], M.TOP[5], M.TOP[6], M.TOP[7]);
+      } else if (P.out_tma == 2) {
+        // this warp's 32 x 8 slice, row-major, stored by its own lane 0
+        float4* b = reinterpret_cast<float4*>(ob + warp * (kTileR * 32) + lr * 32);
+        b[0] = make_float4(M.TOP[0], M.TOP[1], M.TOP[2], M.TOP[3]);
+        b[1] = make_float4(M.TOP[4], M.TOP[5], M.TOP[6], M.TOP[7]);
       } else {
-        const int64_t r = r0 + lr;
+        // each lane writes 32 contiguous bytes of its row: whole sectors
+        const int r = r0 + lr, c = c0 + lc0;
+        if (r < P.FR) {
+          float* o = P.out + (int64_t)r * P.FC + c;
+          if (vec_store && c + 8 <= P.FC) {
+            reinterpret_cast<float4*>(o)[0] = make_float4(M.TOP[0], M.TOP[1], M.TOP[2], M.TOP[3]);
+            reinterpret_cast<float4*>(o)[1] = make_float4(M.TOP[4], M.TOP[5], M.TOP[6], M.TOP[7]);
+          } else {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int64_t c = c0 + lc0 + k;
-          if (r < P.FR && c < P.FC) P.out[r * P.FC + c] = M.TOP[k];
+            for (int k = 0; k < 8; ++k)
+              if (c + k < P.FC) o[k] = M.TOP[k];
+          }
         }
       }
     } else {
       abort_flag = 1;
       set_error(P.err, DEVERR_TIMEOUT);
     }
+    if (P.out_tma == 2) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(R.empty_s + 8 * s);
+        if (got && c0 + lc0 < P.FC) {
+          tma_store_2d(&P.maps[kMaxStaged], c0 + lc0, r0, smem_u32(ob + warp * (kTileR * 32)));
+          bulk_commit();
+          bulk_wait_read<1>();
+        }
+      }
+      __syncwarp();
+      if (!got) break;
+      continue;
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(R.empty_s + 8 * s);
-    if (P.out_tma) fence_proxy_async_smem();
-    if (consumer_bar_or(!got)) break;
-    if (P.out_tma && threadIdx.x == 0) {
-      const uint32_t src = smem_u32(ob);
-      tma_store_2d(&P.maps[kMaxStaged], c0, r0, src);
-      if (c0 + 32 < P.FC) tma_store_2d(&P.maps[kMaxStaged], c0 + 32, r0, src + kTileR * 128);
-      bulk_commit();
-      bulk_wait_read<1>();
+    if (P.out_tma) {
+      fence_proxy_async_smem();
+      if (consumer_bar_or(!got)) break;
+      if (threadIdx.x == 0) {
+        const uint32_t src = smem_u32(ob);
+        tma_store_2d(&P.maps[kMaxStaged], c0, r0, src);
+        if (c0 + 32 < P.FC) tma_store_2d(&P.maps[kMaxStaged], c0 + 32, r0, src + kTileR * 128);
+        bulk_commit();
+        bulk_wait_read<1>();
+      }
+    } else if (!got) {
+      break;
     }
   }
-  if (P.out_tma && threadIdx.x == 0) bulk_wait<0>();
+  if (P.out_tma == 1 && threadIdx.x == 0) bulk_wait<0>();
+  if (P.out_tma == 2 && lane == 0) bulk_wait<0>();
 }
 
 // ---------------------------------------------------------------------------------
@@ -310,10 +385,12 @@ template <int D, int S>
 __global__ void __launch_bounds__(kThreads, D <= 4 ? 2 : 1) fg_reduce_group_kernel(const __grid_constant__ GroupParams P) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int abort_flag;
+  __shared__ SmemTables T;
   uint8_t* smem = align1024(smem_raw);
   const Ring R = setup_ring(smem, P);
   float* red = reinterpret_cast<float*>(R.base + P.nstages * P.stage_bytes);   // [2][8 warps][32]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  load_tables(T, P);
   if (threadIdx.x == 0) {
     abort_flag = 0;
     init_barriers(R, P.nstages);
@@ -322,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, D <= 4 ? 2 : 1) fg_reduce_group_kern
 
   if (warp == kConsumerWarps) {
     if (lane == 0)
-      producer_loop(P, R, RedTiles{(int)blockIdx.x, (int)gridDim.x, P.nunits, P.nsplit, P.tiles_per_split, P.ntc, 0, 0, 0},
+      producer_loop(P, T.leaf, R, RedTiles{(int)blockIdx.x, (int)gridDim.x, P.nunits, P.nsplit, P.tiles_per_split, P.ntc, 0, 0, 0},
                     &abort_flag);
     return;
   }
@@ -344,8 +421,8 @@ __global__ void __launch_bounds__(kThreads, D <= 4 ? 2 : 1) fg_reduce_group_kern
       const int c0 = tc * kTileC;
       const bool got = !dead && wait_or_abort(R.full_s + 8 * s, (i / NS) & 1, P.wait_limit_ns, &abort_flag);
       if (got) {
-        TileEnv env{P, R.base + s * P.stage_bytes, lr, lc0, r0, c0};
-        M.run(P.prog, P.nprog, env);
+        TileEnv env{P, T.leaf, R.base + s * P.stage_bytes, lr, lc0, r0, c0};
+        M.run(T.prog, P.nprog, env);
         float v[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -405,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, D <= 4 ? 2 : 1) fg_reduce_group_kern
             __device__ __forceinline__ void load_acc(float (&t)[1]) const { t[0] = a; }
           } env{P, r, p};
           Machine<D, S, 1> E;
-          E.run(P.epi, P.nepi, env);
+          E.run(T.epi, P.nepi, env);
           outv = E.TOP[0];
         }
         P.out[r] = outv;

@@ -93,12 +93,18 @@ typedef struct tf_layout tf_layout;
  * allow_reduce_epilogue: let a reduce group absorb an elementwise tail on the
  * reduced vector (off = the page's rule that a reduction never fuses forward).
  * wait_limit_ns: bound on every device-side wait before it sets the error
- * flag and the kernel returns. */
+ * flag and the kernel returns.  flags tune the kernels without changing
+ * results: bits 8-15 = height in tiles of the bands the tile walk sweeps
+ * column by column (0 = row-major walk); bits 16-23 = tiles per reduce work
+ * unit (0 = chosen from the frame and the SM count); bits 24-25 = how an
+ * elementwise group writes its output: 0 default (= 2), 1 the CTA's tile
+ * staged in shared memory and stored by one TMA store, 2 each warp's slice
+ * stored by its own TMA store, 3 direct 16-byte stores from registers. */
 typedef struct {
   int32_t max_fused_ops;
   int32_t max_args;
   int32_t allow_reduce_epilogue;
-  int32_t reserved;
+  int32_t flags;
   int64_t wait_limit_ns;
 } fg_build_opts;
 
