@@ -1,0 +1,377 @@
+"""Benchmark of the fused-group hot path on GB300.
+
+One step = one execution of the diamond workload's plan (X, Z [8192, 4096]
+float32, bias [4096]; P = X + bias, relu(P) + exp(0.01 P) + P*Z, transposed
+to [4096, 8192]): the post-dominator pass fuses all seven operators into one
+group, so a step is one kernel launch.  The headline is that group's HBM
+throughput counted in algorithmic bytes (each leaf read once, the output
+written once) per second, whole job over all ranks.
+
+Printed as one JSON line (rank 0).  Beside the headline the line carries:
+the roofline of the dominant kernel, the end-to-end number through the C ABI
+with host buffers, the CPU oracle's throughput on a bounded sample, the
+unfused one-kernel-per-operator time of the same plan, and the other hot-path
+rows measured in the same process (the RNNLM chain, tensor-fusion pack and
+unpack, the random DAG, and the GEMM-epilogue group when it is available).
+
+Inputs (256 MiB) and the output (128 MiB) together exceed the 129 MB L2, so
+the timed loop needs no L2 flush; the smaller rows flush L2 between reps.
+
+Multi-GPU: replicas only -- every rank runs the same plan on its own data
+(data-parallel replicas, weak scaling); there is no collective in the path.
+`--impl reference` times the CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+R, C = 8192, 4096
+METRIC = "fused-group HBM GB/s (diamond group, algorithmic bytes)"
+WORKLOAD = {"workload": "diamond DAG X,Z[8192,4096] fp32 + bias[4096] -> transpose [4096,8192]",
+            "group": "1 fused group of 7 operators", "l2": "inputs+output 384 MiB > L2 (129 MB), no flush"}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return d["hbm_gbs"], d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+class Clocks:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.rows, self.proc = index, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            self.proc.wait()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["not sampled"]}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in self.rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ---------------------------------------------------------------------------
+def setup_dist(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "native" else "gloo"
+        dist.init_process_group(backend)
+        return dist, rank, ws, local
+    return None, rank, ws, local
+
+
+def cpu_sample(rows=1024, reps=3):
+    """The oracle, as it stands, on a slab of the diamond workload: `rows` rows
+    of X and Z (the same columns), op by op in float64 rounded to float32."""
+    import workloads as W
+    from oracle import execute as OE
+    spec = W.diamond(rows, C)
+    ins = W.make_inputs(spec, 0)
+    alg = (2 * rows * C + C + rows * C) * 4
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        OE.run_unfused(spec, ins)
+        times.append(time.perf_counter() - t0)
+    t = min(times)
+    return {"value": alg / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"diamond slab X,Z[{rows},{C}] op by op in float64, best of {reps} ({t:.2f} s each)"}
+
+
+def run_reference(args):
+    dist, rank, ws, _ = setup_dist(args)
+    if rank != 0:
+        return
+    rows = 512
+    for _ in range(args.warmup):
+        cpu_sample(rows, 1)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        s = cpu_sample(rows, 1)
+    t = time.perf_counter() - t0
+    alg = (3 * rows * C + C) * 4
+    v = alg * args.steps / t / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": dict(WORKLOAD, sample=f"CPU oracle on a [{rows},{C}] slab per step"),
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"diamond slab X,Z[{rows},{C}] per step"},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--no-rows", action="store_true", help="skip the secondary rows")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import workloads as W
+    from group_execution_gb300 import graph_from_spec, _lib
+
+    dist, rank, ws, local = setup_dist(args)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    hbm, bf16, bf16s, peak_kind = peaks()
+
+    spec = W.diamond(R, C)
+    plan = graph_from_spec(spec).build()
+    assert plan.n_groups == 1
+    info = plan.groups[0]
+    ins = W.make_inputs(spec, seed=rank)
+    dv = {k: torch.from_numpy(v).to(dev) for k, v in ins.items()}
+    out = torch.empty((C, R), device=dev)
+    tensors = {v: dv[v] for v in info.leaves} | {info.out: out}
+    ptrs = plan._ptrs(tensors)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+
+    def step():
+        st = plan.launch_group_ptrs(0, ptrs, sh)
+        if st:
+            _lib.check(st)
+
+    def barrier():
+        if dist:
+            dist.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    barrier()
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    plan.sync()
+    ms_step = ms / args.steps
+    value = ws * info.alg_bytes * args.steps / (ms * 1e-3) / 1e9
+    achieved = info.alg_bytes / (ms_step * 1e-3) / 1e9
+
+    # end to end through the C ABI: pinned host inputs in, result out, per step
+    hin = {v: dv[v].cpu().pin_memory() for v in info.leaves}
+    hout = torch.empty((C, R), pin_memory=True)
+    e2e_steps = max(3, min(args.steps, 8))
+
+    def e2e_step():
+        for v in info.leaves:
+            dv[v].copy_(hin[v], non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1) / e2e_steps
+    h2d = sum(hin[v].numel() * 4 for v in info.leaves)
+    e2e = {"value": ws * info.alg_bytes / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hout.numel() * 4, "ms_per_step": ms_e2e}
+
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": dict(WORKLOAD, parallelism=f"replicas x{ws}", plan=plan.exec_info(0)),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": traffic_for("fg_ew_group_kernel", "diamond"),
+                         "kernel": "fg_ew_group_kernel", "peak_source": peak_kind,
+                         "alg_bytes_per_launch": info.alg_bytes},
+            "e2e": e2e, "gpu_launches": args.steps, "clocks": clk.summary()}
+    if rank == 0 and not args.no_rows:
+        line["rows"] = secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf16s)
+        line["cpu_baseline"] = cpu_sample()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def traffic_for(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(p))[workload]
+    except Exception:
+        return None
+    if d.get("kernel") != kernel or d.get("sources") != sources_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def sources_hash():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "group_execution_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+# ---------------------------------------------------------------------------
+def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf16s):
+    """Other hot-path rows, measured outside the headline's timed region."""
+    rows = {}
+    l2 = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def timed(fn, reps=10, flush=True):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            if flush:
+                l2.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts), min(ts)
+
+    def run_plan(p, sp, env, fused=True):
+        def f():
+            if fused:
+                for gid, gi in enumerate(p.groups):
+                    p.launch_group(gid, {v: env[v] for v in gi.leaves + [gi.out]})
+            else:
+                node = 0
+                for v in sp.values:
+                    if not v.is_input:
+                        p.launch_unfused(node, {a: env[a] for a in v.args} | {v.vid: env[v.vid]})
+                        node += 1
+        return f
+
+    # diamond, unfused: seven kernels, intermediates in HBM
+    env = dict(dv)
+    for v in spec.ops:
+        env[v.vid] = torch.empty(v.shape, device="cuda")
+    env[spec.outputs[0]] = out
+    med_f, _ = timed(run_plan(plan, spec, env, True), flush=False)
+    med_u, _ = timed(run_plan(plan, spec, env, False), flush=False)
+    rows["diamond"] = {"fused_us": med_f * 1e3, "unfused_us": med_u * 1e3, "speedup_vs_unfused": med_u / med_f,
+                       "fused_launches": 1, "unfused_launches": len(spec.ops),
+                       "unfused_bytes": W.algorithmic_bytes_unfused(spec)}
+
+    # RNNLM chain, both partitions (launch-bound by construction)
+    for epi in (False, True):
+        sp = W.rnnlm_chain()
+        p = graph_from_spec(sp).build(allow_reduce_epilogue=epi)
+        e = {k: torch.from_numpy(v).cuda() for k, v in W.make_inputs(sp).items()}
+        for gi in p.groups:
+            e[gi.out] = torch.empty(sp.values[gi.out].shape, device="cuda")
+        for v in sp.ops:
+            e.setdefault(v.vid, torch.empty(v.shape, device="cuda"))
+        med, mn = timed(run_plan(p, sp, e, True))
+        medu, _ = timed(run_plan(p, sp, e, False))
+        alg = sum(gi.alg_bytes for gi in p.groups)
+        rows["rnnlm_chain" + ("_1group" if epi else "_2groups")] = {
+            "fused_us": med * 1e3, "fused_min_us": mn * 1e3, "groups": p.n_groups, "unfused_us": medu * 1e3,
+            "GBps": alg / (med * 1e-3) / 1e9, "note": "launch-latency bound (0.53 MB); L2 flushed"}
+
+    # tensor-fusion pack / unpack
+    from group_execution_gb300 import TensorFusion
+    sizes = W.tensor_fusion_sizes(0)
+    xs = [torch.from_numpy(x).cuda() for x in W.tensor_fusion_inputs(sizes)]
+    tf = TensorFusion(xs)
+    buf = torch.empty((tf.total_bytes,), dtype=torch.uint8, device="cuda")
+    nbytes = int(sizes.sum()) * 6
+    mp, _ = timed(lambda: tf.pack(0.125, buf))
+    mu, _ = timed(lambda: tf.unpack(1.0, buf))
+    rows["tensor_fusion"] = {"tensors": len(sizes), "elements": int(sizes.sum()),
+                             "pack_us": mp * 1e3, "pack_GBps": nbytes / (mp * 1e-3) / 1e9,
+                             "pack_frac": nbytes / (mp * 1e-3) / 1e9 / hbm,
+                             "unpack_us": mu * 1e3, "unpack_GBps": nbytes / (mu * 1e-3) / 1e9,
+                             "unpack_frac": nbytes / (mu * 1e-3) / 1e9 / hbm, "launches_each": 1,
+                             "per_tensor_unfused_launches": 2 * len(sizes)}
+
+    # random DAG (seed 0), every group in order vs one kernel per operator
+    sp = W.random_dag(0)
+    p = graph_from_spec(sp).build()
+    e = {k: torch.from_numpy(v).cuda() for k, v in W.make_inputs(sp).items()}
+    for v in sp.ops:
+        e[v.vid] = torch.empty(v.shape, device="cuda")
+    medf, _ = timed(run_plan(p, sp, e, True), reps=3, flush=False)
+    medu, _ = timed(run_plan(p, sp, e, False), reps=3, flush=False)
+    alg = sum(gi.alg_bytes for gi in p.groups)
+    rows["random_dag_seed0"] = {"ops": len(sp.ops), "groups": p.n_groups, "fused_ms": medf,
+                                "unfused_ms": medu, "speedup_vs_unfused": medu / medf,
+                                "fused_alg_GBps": alg / (medf * 1e-3) / 1e9,
+                                "fused_alg_bytes": alg, "unfused_bytes": W.algorithmic_bytes_unfused(sp)}
+    del e
+    torch.cuda.empty_cache()
+    return rows
+
+
+if __name__ == "__main__":
+    main()
