@@ -142,6 +142,14 @@ class Plan:
         return dict(zip(("tile_rows", "tile_cols", "stages", "n_staged", "n_gathered", "prog_len"),
                         [x.value for x in v]))
 
+    def source(self, gid):
+        """CUDA source the plan compiles for group gid."""
+        n = C.c_int64()
+        _lib.check(self.lib.fg_plan_group_source(self.h, gid, None, 0, C.byref(n)))
+        buf = C.create_string_buffer(n.value + 1)
+        _lib.check(self.lib.fg_plan_group_source(self.h, gid, buf, n.value + 1, C.byref(n)))
+        return buf.value.decode()
+
     def _ptrs(self, tensors):
         n = len(self.graph.shapes)
         arr = (C.c_void_p * n)()

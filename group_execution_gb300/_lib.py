@@ -18,6 +18,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "groupexec.h")
 
 FG_OK, FG_EINVAL, FG_ESHAPE, FG_EUNSUPPORTED, FG_ENOMEM, FG_ECUDA, FG_ETIMEOUT, FG_EDEVICE = range(8)
 FG_F32, FG_BF16 = 0, 1
+FG_FLAG_INTERPRET = 1 << 26
 STATUS_NAMES = ["FG_OK", "FG_EINVAL", "FG_ESHAPE", "FG_EUNSUPPORTED", "FG_ENOMEM", "FG_ECUDA",
                 "FG_ETIMEOUT", "FG_EDEVICE"]
 
@@ -59,6 +60,7 @@ SIGNATURES = {
     "fg_launch_unfused": (_I32, [_P, _I32, C.POINTER(_P), _P]),
     "fg_sync_status": (_I32, [_P, _P]),
     "fg_plan_group_exec_info": (_I32, [_P, _I32, _PI32, _PI32, _PI32, _PI32, _PI32, _PI32]),
+    "fg_plan_group_source": (_I32, [_P, _I32, C.c_char_p, _I64, _PI64]),
     "fg_plan_destroy": (None, [_P]),
     "fg_last_error": (C.c_char_p, []),
     "tf_layout_create": (_I32, [_I32, _PI64, C.POINTER(_P), _I32, _I64, C.POINTER(_P), _PI64, _PI64]),

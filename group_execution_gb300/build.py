@@ -40,8 +40,28 @@ def headers():
     return hs + [os.path.join(ROOT, "include", "groupexec.h"), __file__]
 
 
+EMBED = ("fg_abi.h", "fg_device.cuh", "group_kernels.cuh")
+EMBED_NAMES = ("kEmbedAbi", "kEmbedDevice", "kEmbedKernels")
+
+
+def write_embed():
+    """Raw-string copies of the device headers for run-time compilation of
+    group programs (their local #include lines dropped: the texts are
+    concatenated in dependency order)."""
+    os.makedirs(BUILD, exist_ok=True)
+    out = []
+    for f, name in zip(EMBED, EMBED_NAMES):
+        text = "".join(ln for ln in open(os.path.join(CSRC, f)) if not ln.lstrip().startswith('#include "'))
+        assert ")FGSRC" not in text
+        out.append(f'static const char* {name} = R"FGSRC(\n{text})FGSRC";\n')
+    path = os.path.join(BUILD, "jit_embed.inc")
+    new = "".join(out)
+    if not os.path.exists(path) or open(path).read() != new:
+        open(path, "w").write(new)
+
+
 def _cmd(src, obj, cuda):
-    inc = ["-I", os.path.join(cuda, "include"), "-I", CSRC, "-I", os.path.join(ROOT, "include")]
+    inc = ["-I", os.path.join(cuda, "include"), "-I", CSRC, "-I", os.path.join(ROOT, "include"), "-I", BUILD]
     if src.endswith(".cu"):
         return [os.path.join(cuda, "bin", "nvcc"), *ARCH, "-O3", "-lineinfo", "-std=c++17",
                 "-Xcompiler", "-fPIC", "-Xptxas", "-warn-spills", *inc, "-c", src, "-o", obj]
@@ -61,6 +81,7 @@ def build(force=False, verbose=False, jobs=None):
         return LIB
     cuda = _cuda_home()
     os.makedirs(BUILD, exist_ok=True)
+    write_embed()
     srcs = sources()
     objs = [os.path.join(BUILD, os.path.basename(s) + ".o") for s in srcs]
 

@@ -12,6 +12,7 @@
 #include <vector>
 
 #include "host.h"
+#include "jit.h"
 #include "launch.h"
 
 using namespace fg;
@@ -80,6 +81,9 @@ struct GroupExec {
   int32_t* counters = nullptr;
   std::string compile_error;          // non-empty: cannot launch
   fg_status compile_status = FG_OK;
+  bool compiled = false;              // run the compiled program (else the interpreter)
+  int min_blocks = 2;                 // CTAs per SM the kernel is built for
+  void* fn = nullptr;                 // compiled kernel
   std::vector<const void*> last_ptrs; // tensor-map cache key
 };
 }  // namespace
@@ -330,7 +334,12 @@ void prepare_group(GroupExec& ge, const BuildOpts& o, int nsm) {
   p.band = (o.flags >> 8) & 0xff;
   p.wait_limit_ns = o.wait_limit_ns;
   ge.big = std::max(cg.depth, cg.epi_depth) > 4 || std::max(cg.slots, cg.epi_slots) > 4;
-  const int ctas = std::min(cg.ctas_per_sm, ge.big ? 1 : 2);
+  // compiled programs keep every operator's values in registers: large
+  // groups get the whole register file of the SM
+  ge.compiled = !(o.flags & FG_FLAG_INTERPRET);
+  ge.min_blocks = ge.compiled ? (cg.dag.size() + cg.epi_dag.size() <= 48 ? 2 : 1) : (ge.big ? 1 : 2);
+  const int ctas = std::min(cg.ctas_per_sm, ge.min_blocks);
+  ge.min_blocks = ctas;
   ge.smem = cg.smem_bytes;
   if (cg.exec == FG_EXEC_REDUCE) {
     p.red_op = cg.red_op;
@@ -495,8 +504,9 @@ fg_status launch_exec(fg_plan* p, GroupExec& ge, void* const* ptrs, void* stream
     }
     ge.last_ptrs = key;
   }
-  cudaError_t e = launch_group_kernel(gp, cg.exec == FG_EXEC_REDUCE ? 1 : 0, ge.big ? 1 : 0, ge.grid, ge.smem,
-                                      static_cast<cudaStream_t>(stream));
+  cudaError_t e = ge.fn ? jit_launch(ge.fn, gp, ge.grid, ge.smem, static_cast<cudaStream_t>(stream))
+                        : launch_group_kernel(gp, cg.exec == FG_EXEC_REDUCE ? 1 : 0, ge.big ? 1 : 0, ge.grid,
+                                              ge.smem, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
     ge.last_ptrs.clear();
     return cuda_err(e, "group kernel launch");
@@ -544,6 +554,21 @@ fg_status fg_build_groups(const fg_graph* gh, const fg_build_opts* opts, fg_plan
     if (e != cudaSuccess) return cuda_err(e, "cudaMemset(error flag)");
     for (auto& ge : p->groups) if (fg_status st = alloc_device(p.get(), ge)) return st;
     for (auto& ge : p->singles) if (fg_status st = alloc_device(p.get(), ge)) return st;
+    // compile every group program (and every single-operator program) once
+    std::vector<GroupExec*> todo;
+    std::vector<std::string> srcs;
+    for (auto* v : {&p->groups, &p->singles})
+      for (auto& ge : *v)
+        if (ge.compile_status == FG_OK && ge.gp && ge.compiled) {
+          todo.push_back(&ge);
+          srcs.push_back(jit_source(ge.cg, ge.min_blocks));
+        }
+    if (!todo.empty()) {
+      std::vector<void*> fns;
+      std::string msg = jit_compile(srcs, fns);
+      if (!msg.empty()) return err(FG_ECUDA, msg);
+      for (size_t i = 0; i < todo.size(); ++i) todo[i]->fn = fns[i];
+    }
   }
   *out = p.release();
   return FG_OK;
@@ -597,6 +622,22 @@ fg_status fg_plan_group_exec_info(const fg_plan* p, int32_t gid, int32_t* tile_r
   if (n_staged) *n_staged = cg.nstaged;
   if (n_gathered) *n_gathered = cg.ngathered;
   if (prog_len) *prog_len = (int32_t)cg.prog.size();
+  return FG_OK;
+}
+
+fg_status fg_plan_group_source(const fg_plan* p, int32_t gid, char* buf, int64_t cap, int64_t* len_out) {
+  if (!p) return err(FG_EINVAL, "null plan");
+  if (gid < 0 || gid >= (int32_t)p->groups.size()) return err(FG_EINVAL, "unknown group id");
+  const GroupExec& ge = p->groups[gid];
+  if (ge.compile_status != FG_OK) return err(ge.compile_status, ge.compile_error);
+  if (!ge.gp) return err(FG_EUNSUPPORTED, "no compiled program for this group kind");
+  const std::string src = jit_source(ge.cg, ge.min_blocks);
+  if (len_out) *len_out = (int64_t)src.size();
+  if (buf && cap > 0) {
+    const size_t n = std::min<size_t>(src.size(), (size_t)cap - 1);
+    std::memcpy(buf, src.data(), n);
+    buf[n] = 0;
+  }
   return FG_OK;
 }
 

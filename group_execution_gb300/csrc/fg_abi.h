@@ -2,8 +2,22 @@
 // program format, leaf descriptors and kernel parameter blocks.  Plain data
 // only; no std types.
 #pragma once
+#ifdef __CUDACC_RTC__
+// compiled at run time by NVRTC: no system headers
+typedef unsigned char uint8_t;
+typedef unsigned short uint16_t;
+typedef unsigned int uint32_t;
+typedef unsigned long long uint64_t;
+typedef int int32_t;
+typedef long long int64_t;
+typedef unsigned long long uintptr_t;
+struct alignas(128) CUtensorMap {
+  unsigned long long opaque[16];
+};
+#else
 #include <cstdint>
 #include <cuda.h>
+#endif
 
 #ifdef __CUDACC__
 #define FG_HD __host__ __device__

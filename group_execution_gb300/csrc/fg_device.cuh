@@ -2,8 +2,10 @@
 // bulk-group bookkeeping, and the register-stack interpreter that runs a
 // group's operator program on eight values per thread.
 #pragma once
+#ifndef __CUDACC_RTC__
 #include <cstdint>
 #include <cuda.h>
+#endif
 
 #include "fg_abi.h"
 

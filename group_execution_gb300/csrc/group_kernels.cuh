@@ -1,0 +1,506 @@
+// Fused-group kernels for elementwise/broadcast/injective groups (K1) and
+// groups ending in a row reduction (K2), templated on how the group's
+// operator program is evaluated: `Prog` is either the register-stack
+// interpreter (InterpProg) or a straight-line program generated from the
+// group and compiled at plan-build time.
+//
+// One persistent CTA per SM slot walks 32x64 tiles of the group's frame.  A
+// producer warp streams every staged leaf's tile into a ring of shared-memory
+// stages with TMA (transposed leaves arrive as transposed boxes, so the
+// transposition costs no extra global traffic); eight consumer warps evaluate
+// the program on the tile from shared memory, eight values per thread, in
+// registers.  K1 writes the result with TMA stores; K2 folds it into per-row
+// partial sums or maxima.  No intermediate of the group ever reaches global
+// memory (TVM "Operator Fusion", FuseTIR; DisCo, Introduction, on op fusion).
+//
+// Thread layout inside a tile: lane = tile row (0..31), consumer warp w owns
+// tile columns 8w..8w+7.  Staged 2-D boxes are 128-byte swizzled so that the
+// row-per-lane reads (and the column-per-lane reads of transposed boxes) hit
+// 32 distinct banks.
+#pragma once
+#include "fg_device.cuh"
+
+namespace fg {
+
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kOutBufBytes = kTileR * kTileC * 4;   // 8 KB
+
+__device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return reinterpret_cast<uint8_t*>((a + 1023) & ~uintptr_t(1023));
+}
+
+// Bounded wait that also gives up as soon as another thread of the CTA has
+// recorded a timeout.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int64_t limit,
+                                              volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if ((int64_t)(global_ns() - t0) > limit) return false;
+  }
+  return true;
+}
+
+// 128-byte swizzled address of (row, 16-byte chunk) inside a box whose rows
+// are 128 bytes long.
+__device__ __forceinline__ int swz(int row, int chunk) { return row * 128 + ((chunk ^ (row & 7)) << 4); }
+
+// ---- leaf reads for one thread: 8 frame points (r0+lr, c0+lc0 .. c0+lc0+7) ----
+struct TileEnv {
+  const GroupParams& P;
+  const uint8_t* stage;
+  int lr, lc0, r0, c0;
+
+  __device__ __forceinline__ void ident(int off, float (&t)[8]) const {
+    const uint8_t* b = stage + off + (lc0 >> 5) * (kTileR * 128);
+    const int j0 = (lc0 & 31) >> 2;
+    const float4 a = *reinterpret_cast<const float4*>(b + swz(lr, j0));
+    const float4 c = *reinterpret_cast<const float4*>(b + swz(lr, j0 + 1));
+    t[0] = a.x; t[1] = a.y; t[2] = a.z; t[3] = a.w;
+    t[4] = c.x; t[5] = c.y; t[6] = c.z; t[7] = c.w;
+  }
+  // box rows are frame columns, 32 frame rows per 128-byte box row
+  __device__ __forceinline__ void trans(int off, float (&t)[8]) const {
+    const uint8_t* b = stage + off + (lr >> 5) * (kTileC * 128) + (lr & 3) * 4;
+    const int ch = (lr & 31) >> 2;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t[k] = *reinterpret_cast<const float*>(b + swz(lc0 + k, ch));
+  }
+  __device__ __forceinline__ void col(int off, float (&t)[8]) const {
+    const float4* p = reinterpret_cast<const float4*>(stage + off + lc0 * 4);
+    const float4 a = p[0], c = p[1];
+    t[0] = a.x; t[1] = a.y; t[2] = a.z; t[3] = a.w;
+    t[4] = c.x; t[5] = c.y; t[6] = c.z; t[7] = c.w;
+  }
+  __device__ __forceinline__ void row(int off, float (&t)[8]) const {
+    const float v = *reinterpret_cast<const float*>(stage + off + lr * 4);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t[k] = v;
+  }
+  // f = sum_k ((g / d_k) % m_k) * s_k over g = r*FC + c (frames with gathered
+  // leaves hold fewer than 2^31 elements)
+  __device__ __forceinline__ void gather(int leaf, float (&t)[8]) const {
+    const LeafDesc& G = P.leaves[leaf];
+    const int r = r0 + lr;
+#pragma unroll 1
+    for (int k = 0; k < 8; ++k) {
+      const int c = c0 + lc0 + k;
+      float v = 0.f;
+      if (r < P.FR && c < P.FC) {
+        const uint32_t g = (uint32_t)r * (uint32_t)P.FC + (uint32_t)c;
+        uint32_t f = 0;
+        for (int q = 0; q < G.nterms; ++q) f += ((g / (uint32_t)G.d[q]) % (uint32_t)G.m[q]) * (uint32_t)G.s[q];
+        v = __ldg(G.ptr + f);
+      }
+      t[k] = v;
+    }
+  }
+};
+
+// Issues the TMA loads of one staged leaf for the tile at (r0, c0).
+__device__ __forceinline__ void issue_leaf(const CUtensorMap* m, int cls, uint32_t dst, uint32_t bar, int r0, int c0) {
+  if (cls == LEAF_IDENT) {
+    tma_load_2d(dst, m, c0, r0, bar);
+    tma_load_2d(dst + kTileR * 128, m, c0 + 32, r0, bar);
+  } else if (cls == LEAF_TRANS) {
+    tma_load_2d(dst, m, r0, c0, bar);
+  } else if (cls == LEAF_COL) {
+    tma_load_1d(dst, m, c0, bar);
+  } else if (cls == LEAF_ROW) {
+    tma_load_1d(dst, m, r0, bar);
+  }
+}
+
+// ---- the interpreter as a program policy ---------------------------------------
+struct LeafInfo {
+  int32_t cls, stage_off, map_idx, pad;
+};
+
+// The program and the leaf table are copied to shared memory once per CTA:
+// every thread reads them at every instruction.
+struct SmemTables {
+  VmInstr prog[kMaxProg];
+  VmInstr epi[kMaxEpi];
+  LeafInfo leaf[kMaxLeaves];
+};
+
+template <int D, int S>
+struct InterpProg {
+  using Tables = SmemTables;
+  static constexpr int kMinBlocks = D <= 4 ? 2 : 1;
+
+  __device__ static void load_tables(Tables& T, const GroupParams& P) {
+    for (int i = threadIdx.x; i < P.nprog; i += blockDim.x) T.prog[i] = P.prog[i];
+    for (int i = threadIdx.x; i < P.nepi; i += blockDim.x) T.epi[i] = P.epi[i];
+    for (int i = threadIdx.x; i < P.nleaves; i += blockDim.x)
+      T.leaf[i] = LeafInfo{P.leaves[i].cls, P.leaves[i].stage_off, P.leaves[i].map_idx, 0};
+  }
+  __device__ static void prefetch(const GroupParams& P, const Tables& T) {
+    for (int j = 0; j < P.nleaves; ++j)
+      if (T.leaf[j].cls != LEAF_GATHER) tma_prefetch(&P.maps[T.leaf[j].map_idx]);
+  }
+  __device__ static void issue(const GroupParams& P, const Tables& T, uint32_t st, uint32_t bar, int r0, int c0) {
+    for (int j = 0; j < P.nleaves; ++j) {
+      const LeafInfo L = T.leaf[j];
+      if (L.cls != LEAF_GATHER) issue_leaf(&P.maps[L.map_idx], L.cls, st + L.stage_off, bar, r0, c0);
+    }
+  }
+  struct Env {
+    const TileEnv& te;
+    const LeafInfo* leaf;
+    __device__ __forceinline__ void load_leaf(int arg, float (&t)[8]) const {
+      const LeafInfo L = leaf[arg];
+      if (L.cls == LEAF_IDENT) te.ident(L.stage_off, t);
+      else if (L.cls == LEAF_TRANS) te.trans(L.stage_off, t);
+      else if (L.cls == LEAF_COL) te.col(L.stage_off, t);
+      else if (L.cls == LEAF_ROW) te.row(L.stage_off, t);
+      else te.gather(arg, t);
+    }
+    __device__ __forceinline__ void load_acc(float (&t)[8]) const {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) t[k] = 0.f;
+    }
+  };
+  __device__ __forceinline__ static void run(const TileEnv& te, const Tables& T, const GroupParams& P, float (&o)[8]) {
+    Machine<D, S, 8> M;
+    Env env{te, T.leaf};
+    M.run(T.prog, P.nprog, env);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) o[k] = M.TOP[k];
+  }
+  // reduce epilogue on the reduced value of row r
+  __device__ static float epi(const GroupParams& P, const Tables& T, int r, float acc) {
+    if (P.nepi == 0) return acc;
+    struct EpiEnv {
+      const GroupParams& P;
+      int r;
+      float a;
+      __device__ __forceinline__ void load_leaf(int arg, float (&t)[1]) const { t[0] = __ldg(P.epi_leaf[arg] + r); }
+      __device__ __forceinline__ void load_acc(float (&t)[1]) const { t[0] = a; }
+    } env{P, r, acc};
+    Machine<D, S, 1> E;
+    E.run(T.epi, P.nepi, env);
+    return E.TOP[0];
+  }
+};
+
+// ---- pipeline pieces ----------------------------------------------------------------
+struct Ring {
+  uint8_t* base;        // generic pointer to stage 0
+  uint32_t base_s;      // shared address of stage 0
+  uint32_t full_s, empty_s;
+};
+
+__device__ __forceinline__ Ring setup_ring(uint8_t* smem) {
+  Ring R;
+  R.full_s = smem_u32(smem);
+  R.empty_s = R.full_s + 8 * kMaxStages;
+  R.base = smem + 1024;
+  R.base_s = smem_u32(R.base);
+  return R;
+}
+
+__device__ __forceinline__ void init_barriers(const Ring& R, int NS) {
+  for (int s = 0; s < NS; ++s) {
+    mbar_init(R.full_s + 8 * s, 1);
+    mbar_init(R.empty_s + 8 * s, kConsumerWarps);
+  }
+  fence_mbar_init();
+}
+
+// Named barrier 1 over the consumer warps, returning the OR of `pred`.
+__device__ __forceinline__ bool consumer_bar_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "n"(kConsumers)
+      : "memory");
+  return r != 0;
+}
+
+// Linear tile index -> (tile row, tile col): row-major, or column-major inside
+// bands of `band` tile rows.
+__device__ __forceinline__ void tile_coords(int t, int ntr, int ntc, int band, int& tr, int& tc) {
+  if (band <= 0) {
+    tr = t / ntc;
+    tc = t % ntc;
+    return;
+  }
+  const int per = band * ntc;
+  const int b = t / per, local = t - b * per;
+  const int rows = min(band, ntr - b * band);
+  tr = b * band + local % rows;
+  tc = local / rows;
+}
+
+struct EwTiles {
+  int t, step, ntiles, ntr, ntc, band;
+  __device__ __forceinline__ bool next(int& tr, int& tc) {
+    if (t >= ntiles) return false;
+    tile_coords(t, ntr, ntc, band, tr, tc);
+    t += step;
+    return true;
+  }
+};
+
+struct RedTiles {   // units (row strip, column split), then the split's tiles
+  int u, step, nunits, nsplit, tps, ntc;
+  int tc, tc_end, strip;
+  bool started;
+  __device__ __forceinline__ bool next(int& tr, int& tcol) {
+    while (!started || tc >= tc_end) {
+      if (started) u += step;
+      started = true;
+      if (u >= nunits) return false;
+      strip = u / nsplit;
+      tc = (u % nsplit) * tps;
+      tc_end = min(ntc, tc + tps);
+    }
+    tr = strip;
+    tcol = tc++;
+    return true;
+  }
+};
+
+// The producer: one thread issues the TMA loads of every staged leaf for each
+// tile into the ring; on a timeout it waits for its loads still in flight.
+template <class Prog, class Tiles>
+__device__ __forceinline__ void producer_loop(const GroupParams& P, const typename Prog::Tables& T, const Ring& R,
+                                              Tiles tiles, volatile int* abort_flag) {
+  Prog::prefetch(P, T);
+  const int NS = P.nstages;
+  int i = 0, tr, tc;
+  bool ok = true;
+  while (tiles.next(tr, tc)) {
+    const int s = i % NS;
+    if (i >= NS && !wait_or_abort(R.empty_s + 8 * s, ((i / NS) & 1) ^ 1, P.wait_limit_ns, abort_flag)) {
+      ok = false;
+      break;
+    }
+    const uint32_t bar = R.full_s + 8 * s;
+    mbar_expect_tx(bar, P.tx_bytes);
+    Prog::issue(P, T, R.base_s + s * P.stage_bytes, bar, tr * kTileR, tc * kTileC);
+    ++i;
+  }
+  if (!ok) {
+    *abort_flag = 1;
+    set_error(P.err, DEVERR_TIMEOUT);
+    for (int k = i - NS < 0 ? 0 : i - NS; k < i; ++k) mbar_wait(R.full_s + 8 * (k % NS), (k / NS) & 1, P.wait_limit_ns);
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// K1 body: elementwise / broadcast / injective group.
+template <class Prog>
+__device__ __forceinline__ void ew_body(const GroupParams& P) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int abort_flag;
+  __shared__ typename Prog::Tables T;
+  uint8_t* smem = align1024(smem_raw);
+  const Ring R = setup_ring(smem);
+  uint8_t* outbuf = R.base + P.nstages * P.stage_bytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  Prog::load_tables(T, P);
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    init_barriers(R, P.nstages);
+    if (P.out_tma) tma_prefetch(&P.maps[kMaxStaged]);
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    if (lane == 0)
+      producer_loop<Prog>(P, T, R, EwTiles{(int)blockIdx.x, (int)gridDim.x, P.ntiles, P.ntr, P.ntc, P.band},
+                          &abort_flag);
+    return;
+  }
+
+  const int NS = P.nstages;
+  const int lr = lane, lc0 = warp * 8;
+  const bool vec_store = (P.FC & 3) == 0 && (reinterpret_cast<uintptr_t>(P.out) & 15) == 0;
+  float o[8];
+  int i = 0;
+  for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x, ++i) {
+    const int s = i % NS;
+    int tr, tc;
+    tile_coords(t, P.ntr, P.ntc, P.band, tr, tc);
+    const int r0 = tr * kTileR, c0 = tc * kTileC;
+    const bool got = wait_or_abort(R.full_s + 8 * s, (i / NS) & 1, P.wait_limit_ns, &abort_flag);
+    uint8_t* ob = outbuf + (i % 3) * kOutBufBytes;
+    if (got) {
+      const TileEnv te{P, R.base + s * P.stage_bytes, lr, lc0, r0, c0};
+      Prog::run(te, T, P, o);
+      if (P.out_tma == 1) {
+        uint8_t* b = ob + (lc0 >> 5) * (kTileR * 128);
+        const int j0 = (lc0 & 31) >> 2;
+        *reinterpret_cast<float4*>(b + swz(lr, j0)) = make_float4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<float4*>(b + swz(lr, j0 + 1)) = make_float4(o[4], o[5], o[6], o[7]);
+      } else if (P.out_tma == 2) {
+        // this warp's 32 x 8 slice, row-major, stored by its own lane 0
+        float4* b = reinterpret_cast<float4*>(ob + warp * (kTileR * 32) + lr * 32);
+        b[0] = make_float4(o[0], o[1], o[2], o[3]);
+        b[1] = make_float4(o[4], o[5], o[6], o[7]);
+      } else {
+        // each lane writes 32 contiguous bytes of its row: whole sectors
+        const int r = r0 + lr, c = c0 + lc0;
+        if (r < P.FR) {
+          float* op = P.out + (int64_t)r * P.FC + c;
+          if (vec_store && c + 8 <= P.FC) {
+            reinterpret_cast<float4*>(op)[0] = make_float4(o[0], o[1], o[2], o[3]);
+            reinterpret_cast<float4*>(op)[1] = make_float4(o[4], o[5], o[6], o[7]);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              if (c + k < P.FC) op[k] = o[k];
+          }
+        }
+      }
+    } else {
+      abort_flag = 1;
+      set_error(P.err, DEVERR_TIMEOUT);
+    }
+    if (P.out_tma == 2) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(R.empty_s + 8 * s);
+        if (got && c0 + lc0 < P.FC) {
+          tma_store_2d(&P.maps[kMaxStaged], c0 + lc0, r0, smem_u32(ob + warp * (kTileR * 32)));
+          bulk_commit();
+          bulk_wait_read<1>();
+        }
+      }
+      __syncwarp();
+      if (!got) break;
+      continue;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(R.empty_s + 8 * s);
+    if (P.out_tma == 1) {
+      fence_proxy_async_smem();
+      if (consumer_bar_or(!got)) break;
+      if (threadIdx.x == 0) {
+        const uint32_t src = smem_u32(ob);
+        tma_store_2d(&P.maps[kMaxStaged], c0, r0, src);
+        if (c0 + 32 < P.FC) tma_store_2d(&P.maps[kMaxStaged], c0 + 32, r0, src + kTileR * 128);
+        bulk_commit();
+        bulk_wait_read<1>();
+      }
+    } else if (!got) {
+      break;
+    }
+  }
+  if (P.out_tma == 1 && threadIdx.x == 0) bulk_wait<0>();
+  if (P.out_tma == 2 && lane == 0) bulk_wait<0>();
+}
+
+// ---------------------------------------------------------------------------------
+// K2 body: group ending in a row reduction over the frame's last axis, with an
+// optional elementwise epilogue on the reduced vector.  Work units are
+// (32-row strip, run of column tiles); a unit writes its partial row values
+// to scratch and the last unit of a strip to arrive combines them in split
+// order, so the result does not depend on scheduling.
+template <class Prog>
+__device__ __forceinline__ void reduce_body(const GroupParams& P) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int abort_flag;
+  __shared__ typename Prog::Tables T;
+  uint8_t* smem = align1024(smem_raw);
+  const Ring R = setup_ring(smem);
+  float* red = reinterpret_cast<float*>(R.base + P.nstages * P.stage_bytes);   // [2][8 warps][32]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  Prog::load_tables(T, P);
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    init_barriers(R, P.nstages);
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    if (lane == 0)
+      producer_loop<Prog>(P, T, R,
+                          RedTiles{(int)blockIdx.x, (int)gridDim.x, P.nunits, P.nsplit, P.tiles_per_split, P.ntc, 0, 0,
+                                   0, false},
+                          &abort_flag);
+    return;
+  }
+
+  const int NS = P.nstages;
+  const int lr = lane, lc0 = warp * 8;
+  const bool is_sum = P.red_op == RED_SUM;
+  float o[8];
+  int i = 0, k_unit = 0;
+  bool dead = false;
+  for (int u = blockIdx.x; u < P.nunits; u += gridDim.x, ++k_unit) {
+    const int strip = u / P.nsplit, sp = u % P.nsplit;
+    const int tcb = sp * P.tiles_per_split;
+    const int tce = min(P.ntc, tcb + P.tiles_per_split);
+    const int r0 = strip * kTileR;
+    float acc = is_sum ? 0.f : neg_inf();
+    for (int tc = tcb; tc < tce; ++tc, ++i) {
+      const int s = i % NS;
+      const int c0 = tc * kTileC;
+      const bool got = !dead && wait_or_abort(R.full_s + 8 * s, (i / NS) & 1, P.wait_limit_ns, &abort_flag);
+      if (got) {
+        const TileEnv te{P, R.base + s * P.stage_bytes, lr, lc0, r0, c0};
+        Prog::run(te, T, P, o);
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const bool in = c0 + lc0 + k < P.FC;
+          v[k] = in ? o[k] : (is_sum ? 0.f : neg_inf());
+        }
+        if (is_sum) {
+          acc = __fadd_rn(acc, __fadd_rn(__fadd_rn(__fadd_rn(v[0], v[1]), __fadd_rn(v[2], v[3])),
+                                         __fadd_rn(__fadd_rn(v[4], v[5]), __fadd_rn(v[6], v[7]))));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) acc = fmaxf(acc, v[k]);
+        }
+      } else if (!dead) {
+        dead = true;
+        abort_flag = 1;
+        set_error(P.err, DEVERR_TIMEOUT);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(R.empty_s + 8 * s);
+    }
+    float* rb = red + (k_unit & 1) * (kConsumerWarps * 32);
+    rb[warp * 32 + lane] = acc;
+    if (consumer_bar_or(dead)) break;
+    if (warp == 0) {
+      float p = rb[lane];
+      for (int w = 1; w < kConsumerWarps; ++w) p = is_sum ? __fadd_rn(p, rb[w * 32 + lane]) : fmaxf(p, rb[w * 32 + lane]);
+      const int r = r0 + lane;
+      bool finish = true;
+      if (P.nsplit > 1) {
+        if (r < P.FR) P.scratch[(int64_t)sp * P.FR + r] = p;
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(&P.counters[strip], 1) == P.nsplit - 1;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        finish = last != 0;
+        if (finish) {
+          __threadfence();
+          p = is_sum ? 0.f : neg_inf();
+          if (r < P.FR)
+            for (int q = 0; q < P.nsplit; ++q) {
+              const float x = __ldcg(P.scratch + (int64_t)q * P.FR + r);
+              p = is_sum ? __fadd_rn(p, x) : fmaxf(p, x);
+            }
+          if (lane == 0) P.counters[strip] = 0;
+        }
+      }
+      if (finish && r < P.FR) P.out[r] = Prog::epi(P, T, r, p);
+    }
+  }
+}
+
+}  // namespace fg

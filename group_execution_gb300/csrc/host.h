@@ -57,6 +57,15 @@ struct LeafUse {            // one (value, map) read by a program
   int32_t cls;              // LeafClass
 };
 
+// One node of a group's expression DAG (children before parents).
+struct JExpr {
+  int kind;          // 0 leaf, 1 accumulator, 2 unary, 3 binary
+  int vm;            // VmOp of the operation
+  float imm;
+  int a, b;          // children
+  int leaf;          // leaf index (kind 0)
+};
+
 struct CompiledGroup {
   int32_t exec = FG_EXEC_ELEMWISE;   // fg_exec_kind
   std::vector<int32_t> nodes;         // ascending node ids
@@ -68,6 +77,10 @@ struct CompiledGroup {
   // main program (K1: whole group; K2: prologue; K3: epilogue)
   std::vector<VmInstr> prog;
   std::vector<LeafUse> leaves;
+  std::vector<JExpr> dag;             // expression DAG of the main program
+  int dag_root = -1;
+  std::vector<JExpr> epi_dag;         // reduce epilogue DAG (leaves index epi_leaf_values)
+  int epi_root = -1;
   int depth = 0, slots = 0;
   // reduce
   int32_t red_op = RED_NONE;
@@ -84,6 +97,8 @@ struct CompiledGroup {
   std::vector<int> leaf_stage_off;    // byte offset inside a stage, -1 = gathered
   int smem_bytes = 0, ctas_per_sm = 2;
 };
+
+constexpr int FG_FLAG_INTERPRET = 1 << 26;   // run group programs on the interpreter
 
 struct BuildOpts {
   int max_fused_ops = 256, max_args = 64, allow_reduce_epilogue = 0;

@@ -357,13 +357,17 @@ struct Program {
   std::vector<VmInstr> code;
   std::vector<LeafUse> leaves;
   int depth = 0, slots = 0;
+  std::vector<JExpr> dag;
+  int root = -1;
 };
 
 Program emit_program(Builder& b, int root) {
+  Program p;
+  for (const Expr& e : b.ex) p.dag.push_back(JExpr{(int)e.kind, e.vm, e.imm, e.a, e.b, e.leaf});
+  p.root = root;
   Emitter em(b.ex);
   em.emit(root);
   if (em.depth != 1) fail(FG_EUNSUPPORTED, "internal: unbalanced program");
-  Program p;
   p.code = em.code;
   p.leaves = b.leaves;
   p.depth = em.max_depth;
@@ -436,6 +440,8 @@ CompiledGroup compile_group(const Graph& g, const std::vector<int32_t>& nodes_in
     cg.leaves = p.leaves;
     cg.depth = p.depth;
     cg.slots = p.slots;
+    cg.dag = p.dag;
+    cg.dag_root = p.root;
     for (auto& l : cg.leaves)
       if (l.value == cg.mm_a || l.value == cg.mm_b) fail(FG_EUNSUPPORTED, "matmul operand read by the epilogue");
     return cg;
@@ -456,6 +462,8 @@ CompiledGroup compile_group(const Graph& g, const std::vector<int32_t>& nodes_in
     cg.leaves = p.leaves;
     cg.depth = p.depth;
     cg.slots = p.slots;
+    cg.dag = p.dag;
+    cg.dag_root = p.root;
     if (cg.sink != red) {
       // epilogue on the reduced vector (allow_reduce_epilogue)
       Builder be(g, cg.nodes, 1, cg.FR);
@@ -467,6 +475,8 @@ CompiledGroup compile_group(const Graph& g, const std::vector<int32_t>& nodes_in
       for (auto& l : pe.leaves)
         if (l.cls != LEAF_IDENT) fail(FG_EUNSUPPORTED, "reduce epilogue reads a moved vector");
       cg.epi = pe.code;
+      cg.epi_dag = pe.dag;
+      cg.epi_root = pe.root;
       for (auto& l : pe.leaves) cg.epi_leaf_values.push_back(l.value);
       cg.epi_depth = pe.depth;
       cg.epi_slots = pe.slots;
@@ -482,6 +492,8 @@ CompiledGroup compile_group(const Graph& g, const std::vector<int32_t>& nodes_in
   cg.leaves = p.leaves;
   cg.depth = p.depth;
   cg.slots = p.slots;
+  cg.dag = p.dag;
+  cg.dag_root = p.root;
   return cg;
 }
 

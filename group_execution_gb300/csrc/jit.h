@@ -1,0 +1,21 @@
+// Plan-build-time compilation of group programs (see jit.cpp).
+#pragma once
+#include <cuda_runtime.h>
+
+#include <functional>
+#include <string>
+#include <vector>
+
+#include "host.h"
+
+namespace fg {
+
+bool jit_available();
+// CUDA source of a group's kernel; min_blocks is the kernel's CTAs-per-SM bound.
+std::string jit_source(const CompiledGroup& cg, int min_blocks);
+// Compiles (once per process per distinct source) and loads; returns "" or an
+// error message.  funcs[i] is the loaded kernel of sources[i].
+std::string jit_compile(const std::vector<std::string>& sources, std::vector<void*>& funcs);
+cudaError_t jit_launch(void* func, const GroupParams& p, int grid, int smem, cudaStream_t st);
+
+}  // namespace fg

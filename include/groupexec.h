@@ -99,7 +99,10 @@ typedef struct tf_layout tf_layout;
  * unit (0 = chosen from the frame and the SM count); bits 24-25 = how an
  * elementwise group writes its output: 0 default (= 2), 1 the CTA's tile
  * staged in shared memory and stored by one TMA store, 2 each warp's slice
- * stored by its own TMA store, 3 direct 16-byte stores from registers. */
+ * stored by its own TMA store, 3 direct 16-byte stores from registers;
+ * bit 26 runs the groups' operator programs on the register-stack
+ * interpreter instead of compiling each program to straight-line code when
+ * the plan is built (default; needs NVRTC, loaded at run time). */
 typedef struct {
   int32_t max_fused_ops;
   int32_t max_args;
@@ -184,6 +187,12 @@ fg_status fg_sync_status(fg_plan* p, void* cuda_stream);
 fg_status fg_plan_group_exec_info(const fg_plan* p, int32_t gid, int32_t* tile_rows,
                                   int32_t* tile_cols, int32_t* stages, int32_t* n_staged,
                                   int32_t* n_gathered, int32_t* prog_len);
+
+/* The CUDA source the plan compiles for group gid (the group's operator
+ * program written out as straight-line code inside the shared pipeline).
+ * Writes at most cap bytes including the terminating NUL to buf (buf may be
+ * NULL) and the full length without the NUL to *len_out. */
+fg_status fg_plan_group_source(const fg_plan* p, int32_t gid, char* buf, int64_t cap, int64_t* len_out);
 
 void fg_plan_destroy(fg_plan* p);
 

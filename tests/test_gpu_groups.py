@@ -9,11 +9,19 @@ import workloads as W
 from oracle import execute as OE
 from tests._helpers import rel_err, TOL_F32
 from tests._gpu import prepare, run_fused, run_unfused
+from group_execution_gb300 import _lib
 
 pytestmark = pytest.mark.gpu
 
 
+MODES = [0, _lib.FG_FLAG_INTERPRET]
+
+
 def _check(spec, seed=0, unfused=True, **kw):
+    if "flags" not in kw:
+        for fl in MODES:
+            r = _check(spec, seed, unfused, flags=fl, **kw)
+        return r
     g, plan, inputs, dev = prepare(spec, seed, **kw)
     for info in plan.groups:
         assert info.status == 0, info
