@@ -243,8 +243,8 @@ def main():
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": dict(WORKLOAD, parallelism=f"replicas x{ws}", plan=plan.exec_info(0)),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                         "frac": achieved / hbm, "traffic": traffic_for("fg_ew_group_kernel", "diamond"),
-                         "kernel": "fg_ew_group_kernel", "peak_source": peak_kind,
+                         "frac": achieved / hbm, "traffic": traffic_for("fg_jit_ew_group", "diamond"),
+                         "kernel": "fg_jit_ew_group (compiled group program)", "peak_source": peak_kind,
                          "alg_bytes_per_launch": info.alg_bytes},
             "e2e": e2e, "gpu_launches": args.steps, "clocks": clk.summary()}
     if rank == 0 and not args.no_rows:
