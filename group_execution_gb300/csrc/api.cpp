@@ -64,6 +64,10 @@ bool device_present(int* nsm) {
 int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 }  // namespace
 
+namespace fg {
+int set_last_error(int status, const char* msg) { return err(static_cast<fg_status>(status), msg); }
+}  // namespace fg
+
 // ---------------------------------------------------------------------------
 // opaque handles
 struct fg_graph {

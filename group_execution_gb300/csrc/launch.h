@@ -10,6 +10,8 @@ namespace fg {
 // 8-register / 8-slot machine (one CTA per SM) over the 4/4 one.
 cudaError_t launch_group_kernel(const GroupParams& p, int exec, int big, int grid, int smem, cudaStream_t st);
 int group_kernel_threads();
+// Records the message fg_last_error() returns on this thread; returns status.
+int set_last_error(int status, const char* msg);
 
 cudaError_t launch_gemm_kernel(const GemmParams& p, int big, int grid, int smem, cudaStream_t st);
 int gemm_smem_bytes(const GemmParams& p);

@@ -199,6 +199,26 @@ void fg_plan_destroy(fg_plan* p);
 /* Message for the last non-OK status on this thread ("" if none). */
 const char* fg_last_error(void);
 
+/* Row reduction without device allocation: y[r] = sum over c of x[r, c]
+ * (opcode FG_OP_ROWSUM) or the maximum over c (FG_OP_ROWMAX) of a row-major
+ * float32 matrix x[rows, cols], for callers that cannot call cudaMalloc -- a
+ * host framework that owns every device allocation through its own pool, or
+ * a step that cannot accept the device-wide synchronisation an allocation
+ * may imply -- and so cannot build a plan either.  The pages have no
+ * counterpart of this entry point.  It runs the reduce-group kernel on a
+ * one-operator program with its scratch (per-split partial row values and
+ * arrival counters) in a 4 MiB + 8 KiB file-scope device array that every
+ * GPU which loads the library holds until the process exits.
+ * Limits: rows <= 65536 (else FG_EINVAL) and rows*cols < 2^31 (else
+ * FG_ESHAPE).  x (16-byte aligned) and y (4-byte aligned) are device
+ * pointers owned by the caller.  Asynchronous on cuda_stream.  The first
+ * call on a device looks up the array's device address; make that call
+ * before any stream capture.  All calls share the array, so calls that
+ * overlap on the GPU (other streams, or host threads without ordering) race.
+ * Device-side timeouts are not reported by this entry point. */
+fg_status fg_row_reduce_noalloc(int32_t opcode, const float* x, int64_t rows, int64_t cols, float* y,
+                                void* cuda_stream);
+
 /* ---- tensor fusion ------------------------------------------------------- */
 
 /* Layout of n float32 gradient tensors (device pointers grads[i], numel[i]
