@@ -40,8 +40,8 @@ def headers():
     return hs + [os.path.join(ROOT, "include", "groupexec.h"), __file__]
 
 
-EMBED = ("fg_abi.h", "fg_device.cuh", "group_kernels.cuh")
-EMBED_NAMES = ("kEmbedAbi", "kEmbedDevice", "kEmbedKernels")
+EMBED = ("fg_abi.h", "fg_device.cuh", "group_kernels.cuh", "gemm_kernel.cuh")
+EMBED_NAMES = ("kEmbedAbi", "kEmbedDevice", "kEmbedKernels", "kEmbedGemm")
 
 
 def write_embed():

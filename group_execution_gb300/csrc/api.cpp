@@ -372,14 +372,83 @@ void prepare_group(GroupExec& ge, const BuildOpts& o, int nsm) {
   }
 }
 
+int gemm_box_bytes(int cls) {
+  switch (cls) {
+    case LEAF_IDENT: case LEAF_TRANS: return kGemmM * kGemmChunk * 4;
+    case LEAF_COL: return kGemmChunk * 4;
+    case LEAF_ROW: return kGemmM * 4;
+    default: return 0;
+  }
+}
+
+// Static part of the kernel parameters of a GEMM-epilogue group.
+void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
+  CompiledGroup& cg = ge.cg;
+  const int a_mn = cg.mm_ta ? 1 : 0, b_mn = cg.mm_tb ? 0 : 1;
+  // TMA rows must be 16-byte multiples: the contiguous extent of each operand
+  const int64_t a_inner = a_mn ? cg.M : cg.K, b_inner = b_mn ? cg.N : cg.K;
+  if (a_inner % 8 || b_inner % 8)
+    throw CompileError{FG_EUNSUPPORTED, "matmul operands need a contiguous extent that is a multiple of 8"};
+  if (cg.N % 4) throw CompileError{FG_EUNSUPPORTED, "matmul output width must be a multiple of 4"};
+  if (cg.M >= (1LL << 31) || cg.N >= (1LL << 31) || cg.K >= (1LL << 31))
+    throw CompileError{FG_EUNSUPPORTED, "matmul extent too large"};
+  (void)g;
+  ge.mp.reset(new GemmParams());
+  GemmParams& p = *ge.mp;
+  std::memset(&p, 0, sizeof(p));
+  if (cg.prog.size() > (size_t)kMaxProg) throw CompileError{FG_EUNSUPPORTED, "epilogue program too long"};
+  std::copy(cg.prog.begin(), cg.prog.end(), p.prog);
+  p.nprog = (int)cg.prog.size();
+  p.nleaves = (int)cg.leaves.size();
+  int mi = 0, tx = 0;
+  for (size_t i = 0; i < cg.leaves.size(); ++i) {
+    bool staged = cg.leaves[i].cls != LEAF_GATHER;
+    fill_leaf_desc(p.leaves[i], cg.leaves[i], staged ? cg.leaf_stage_off[i] : -1, staged ? mi : -1);
+    if (staged) {
+      ++mi;
+      tx += gemm_box_bytes(cg.leaves[i].cls);
+    }
+  }
+  p.nstaged = mi;
+  p.M = (int32_t)cg.M;
+  p.N = (int32_t)cg.N;
+  p.K = (int32_t)cg.K;
+  p.ntm = (int32_t)((cg.M + kGemmM - 1) / kGemmM);
+  p.ntn = (int32_t)((cg.N + kGemmN - 1) / kGemmN);
+  p.ntiles = p.ntm * p.ntn;
+  p.nkb = (int32_t)((cg.K + kGemmK - 1) / kGemmK);
+  p.a_mn = a_mn;
+  p.b_mn = b_mn;
+  p.wait_limit_ns = o.wait_limit_ns;
+  p.epi_stage_bytes = cg.stage_bytes;
+  p.epi_tx_bytes = tx;
+  // operand ring and epilogue-leaf ring depths that fit 227 KB
+  const int limit = 227 * 1024, fixed = 2048 + 2 * kGemmM * kGemmChunk * 4;
+  int ns = 0, ne = 0;
+  const int prefs[][2] = {{3, 4}, {3, 3}, {2, 4}, {2, 3}, {3, 2}, {2, 2}};
+  for (const auto& pr : prefs)
+    if (!ns && fixed + pr[0] * (kGemmM + kGemmN) * kGemmK * 2 + pr[1] * cg.stage_bytes <= limit) {
+      ns = pr[0];
+      ne = pr[1];
+    }
+  if (!ns) throw CompileError{FG_EUNSUPPORTED, "GEMM epilogue stages do not fit in shared memory"};
+  p.nstages = ns;
+  p.n_epi_bufs = ne;
+  ge.smem = fixed + ns * (kGemmM + kGemmN) * kGemmK * 2 + ne * cg.stage_bytes;
+  cg.nstages = ns;
+  ge.big = cg.depth > 4 || cg.slots > 4;
+  ge.compiled = !(o.flags & FG_FLAG_INTERPRET);
+  ge.min_blocks = 1;
+  ge.grid = std::max(1, std::min(p.ntiles, nsm));
+}
+
 GroupExec make_exec(const Graph& g, const std::vector<int32_t>& nodes, const BuildOpts& o, int nsm) {
   GroupExec ge;
   try {
     ge.cg = compile_group(g, nodes);
     plan_staging(g, ge.cg, o);
     if (ge.cg.exec == FG_EXEC_GEMM) {
-      ge.compile_status = FG_EUNSUPPORTED;
-      ge.compile_error = "GEMM groups are not available in this build";
+      prepare_gemm(ge, o, nsm, g);
     } else {
       prepare_group(ge, o, nsm);
     }
@@ -395,6 +464,7 @@ GroupExec make_exec(const Graph& g, const std::vector<int32_t>& nodes, const Bui
 }
 
 fg_status alloc_device(fg_plan* p, GroupExec& ge) {
+  if (ge.compile_status == FG_OK && ge.mp) ge.mp->err = p->d_err;
   if (ge.compile_status != FG_OK || !ge.gp) return FG_OK;
   GroupParams& gp = *ge.gp;
   gp.err = p->d_err;
@@ -471,10 +541,66 @@ fg_status check_ptr(const void* p, int32_t vid) {
   return FG_OK;
 }
 
+fg_status launch_gemm(GroupExec& ge, void* const* ptrs, void* stream) {
+  const CompiledGroup& cg = ge.cg;
+  GemmParams& gp = *ge.mp;
+  std::vector<const void*> key{ptrs[cg.mm_a], ptrs[cg.mm_b], ptrs[cg.out_value]};
+  for (int32_t v : cg.leaf_values) key.push_back(ptrs[v]);
+  if (key != ge.last_ptrs) {
+    for (int32_t v : cg.leaf_values) if (fg_status st = check_ptr(ptrs[v], v)) return st;
+    if (fg_status st = check_ptr(ptrs[cg.out_value], cg.out_value)) return st;
+    {
+      // A: [K, M] (M contiguous) when transposed, else [M, K]
+      uint64_t dims[2], strides[1];
+      uint32_t box[2];
+      if (gp.a_mn) {
+        dims[0] = cg.M; dims[1] = cg.K; strides[0] = cg.M * 2; box[0] = 64; box[1] = 64;
+      } else {
+        dims[0] = cg.K; dims[1] = cg.M; strides[0] = cg.K * 2; box[0] = 64; box[1] = kGemmM;
+      }
+      if (fg_status st = encode(&gp.mapA, ptrs[cg.mm_a], 2, dims, strides, box, true, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+        return st;
+      // B: [K, N] (N contiguous), or [N, K] when transposed
+      if (gp.b_mn) {
+        dims[0] = cg.N; dims[1] = cg.K; strides[0] = cg.N * 2; box[0] = 64; box[1] = 64;
+      } else {
+        dims[0] = cg.K; dims[1] = cg.N; strides[0] = cg.K * 2; box[0] = 64; box[1] = kGemmN;
+      }
+      if (fg_status st = encode(&gp.mapB, ptrs[cg.mm_b], 2, dims, strides, box, true, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+        return st;
+    }
+    for (size_t i = 0; i < cg.leaves.size(); ++i) {
+      const LeafUse& l = cg.leaves[i];
+      LeafDesc& d = gp.leaves[i];
+      d.ptr = static_cast<const float*>(ptrs[l.value]);
+      if (l.cls != LEAF_GATHER)
+        if (fg_status st = leaf_map(&gp.maps[d.map_idx], ptrs[l.value], l.cls, cg.FR, cg.FC, kGemmM, kGemmChunk))
+          return st;
+    }
+    gp.out = static_cast<float*>(ptrs[cg.out_value]);
+    if (fg_status st = leaf_map(&gp.maps[kMaxStaged], ptrs[cg.out_value], LEAF_IDENT, cg.FR, cg.FC, kGemmM, kGemmChunk))
+      return st;
+    ge.last_ptrs = key;
+  }
+  cudaError_t e = ge.fn ? jit_launch_gemm(ge.fn, gp, ge.grid, ge.smem, static_cast<cudaStream_t>(stream))
+                        : launch_gemm_kernel(gp, ge.big ? 1 : 0, ge.grid, ge.smem, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    ge.last_ptrs.clear();
+    return cuda_err(e, "GEMM kernel launch");
+  }
+  return FG_OK;
+}
+
 fg_status launch_exec(fg_plan* p, GroupExec& ge, void* const* ptrs, void* stream) {
   if (ge.compile_status != FG_OK) return err(ge.compile_status, ge.compile_error);
   if (!p->has_device) return err(FG_ECUDA, "no CUDA device: the plan is host-only");
   if (!ptrs) return err(FG_EINVAL, "null value_ptrs");
+  if (ge.cg.exec == FG_EXEC_GEMM) {
+    if (!ptrs[ge.cg.mm_a] || !ptrs[ge.cg.mm_b]) return err(FG_EINVAL, "null matmul operand");
+    if (reinterpret_cast<uintptr_t>(ptrs[ge.cg.mm_a]) % 16 || reinterpret_cast<uintptr_t>(ptrs[ge.cg.mm_b]) % 16)
+      return err(FG_EINVAL, "matmul operands must be 16-byte aligned");
+    return launch_gemm(ge, ptrs, stream);
+  }
   const CompiledGroup& cg = ge.cg;
   GroupParams& gp = *ge.gp;
   // cache key: the pointers this group reads and writes
@@ -563,7 +689,7 @@ fg_status fg_build_groups(const fg_graph* gh, const fg_build_opts* opts, fg_plan
     std::vector<std::string> srcs;
     for (auto* v : {&p->groups, &p->singles})
       for (auto& ge : *v)
-        if (ge.compile_status == FG_OK && ge.gp && ge.compiled) {
+        if (ge.compile_status == FG_OK && (ge.gp || ge.mp) && ge.compiled) {
           todo.push_back(&ge);
           srcs.push_back(jit_source(ge.cg, ge.min_blocks));
         }
@@ -634,7 +760,7 @@ fg_status fg_plan_group_source(const fg_plan* p, int32_t gid, char* buf, int64_t
   if (gid < 0 || gid >= (int32_t)p->groups.size()) return err(FG_EINVAL, "unknown group id");
   const GroupExec& ge = p->groups[gid];
   if (ge.compile_status != FG_OK) return err(ge.compile_status, ge.compile_error);
-  if (!ge.gp) return err(FG_EUNSUPPORTED, "no compiled program for this group kind");
+  if (!ge.gp && !ge.mp) return err(FG_EUNSUPPORTED, "no compiled program for this group kind");
   const std::string src = jit_source(ge.cg, ge.min_blocks);
   if (len_out) *len_out = (int64_t)src.size();
   if (buf && cap > 0) {

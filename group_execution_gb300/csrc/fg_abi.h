@@ -138,18 +138,25 @@ struct GroupParams {
   int32_t red_op, nsplit, tiles_per_split, nunits;
 };
 
-// GEMM + epilogue kernel.
+// GEMM + epilogue kernel: 128 x 256 accumulator tiles in TMEM, K in blocks
+// of 64, the epilogue in 128 x 32 column chunks.
+constexpr int kGemmM = 128, kGemmN = 256, kGemmK = 64, kGemmChunk = 32;
+constexpr int kGemmWarps = 7;          // TMA, MMA, epilogue loads, 4 epilogue warps
+
 struct GemmParams {
-  CUtensorMap mapA, mapB;              // bf16 operands, MN-major (transA=1 / transB=0)
+  CUtensorMap mapA, mapB;              // bf16 operands (boxes per major-ness)
   CUtensorMap maps[kMaxStaged + 1];    // epilogue leaves, [kMaxStaged] = output
-  VmInstr prog[kMaxProg];
+  VmInstr prog[kMaxProg];              // epilogue program (interpreted variant)
   LeafDesc leaves[kMaxLeaves];
+  float* out;
   int32_t* err;
   int64_t wait_limit_ns;
   int32_t nprog, nleaves, nstaged;
   int32_t M, N, K;
-  int32_t ntm, ntn, ntiles;
-  int32_t epi_stage_bytes;
+  int32_t ntm, ntn, ntiles, nkb;
+  int32_t a_mn, b_mn;                  // 1: operand stored MN-major (M or N contiguous)
+  int32_t nstages;                     // operand ring depth
+  int32_t epi_stage_bytes, epi_tx_bytes, n_epi_bufs;
 };
 
 // Device error codes written to the flag.

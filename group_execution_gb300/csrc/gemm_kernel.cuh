@@ -1,0 +1,369 @@
+// GEMM-epilogue group kernel (K3): D = A * B on the 5th-generation tensor
+// cores with the group's elementwise tail applied to the accumulator before
+// it ever reaches global memory (TVM "Operator Fusion", Fusion rules, phase
+// 0: an out-elementwise-fusable operator such as matmul fuses with its
+// elementwise successors; TAG's sufficient-factor gradient G = U^T V is the
+// workload).
+//
+// Persistent: one CTA per SM walks 128 x 256 output tiles.  Warp roles:
+//   warp 0  TMA producer of the bf16 operand tiles (64-deep K blocks),
+//   warp 1  allocates TMEM (2 x 256 columns: double-buffered accumulator)
+//           and issues tcgen05.mma from one thread,
+//   warp 2  TMA producer of the epilogue leaves, 128 x 32 chunk by chunk,
+//   warps 3-6 epilogue: each thread owns one accumulator row (TMEM lane),
+//           reads 32 columns per chunk with tcgen05.ld, evaluates the
+//           epilogue program eight values at a time and stages the result
+//           for a TMA store.
+// The epilogue of tile i overlaps the MMAs of tile i+1.  Every wait is
+// bounded; on expiry the CTA records the error, drains its copies, frees its
+// TMEM and returns.
+#pragma once
+#include "fg_device.cuh"
+
+namespace fg {
+
+constexpr int kGemmThreads = kGemmWarps * 32;
+constexpr int kGemmABytes = kGemmM * kGemmK * 2;    // 16 KB
+constexpr int kGemmBBytes = kGemmN * kGemmK * 2;    // 32 KB
+constexpr int kGemmOutBytes = kGemmM * kGemmChunk * 4;   // 16 KB
+constexpr int kGemmChunks = kGemmN / kGemmChunk;    // 8
+
+// Leaf reads for one epilogue thread: accumulator row rr of the tile, eight
+// columns starting at q8 inside the current 32-column chunk.
+struct GemmEnv {
+  const GemmParams& P;
+  const uint8_t* stage;
+  int rr, r0, cc0, q8;
+
+  __device__ __forceinline__ static int swz(int row, int chunk) { return row * 128 + ((chunk ^ (row & 7)) << 4); }
+  __device__ __forceinline__ void ident(int off, float (&t)[8]) const {
+    const uint8_t* b = stage + off;
+    const float4 a = *reinterpret_cast<const float4*>(b + swz(rr, q8 >> 2));
+    const float4 c = *reinterpret_cast<const float4*>(b + swz(rr, (q8 >> 2) + 1));
+    t[0] = a.x; t[1] = a.y; t[2] = a.z; t[3] = a.w;
+    t[4] = c.x; t[5] = c.y; t[6] = c.z; t[7] = c.w;
+  }
+  // four 32 x 32 boxes, box b holding tile rows 32b..32b+31 transposed
+  __device__ __forceinline__ void trans(int off, float (&t)[8]) const {
+    const uint8_t* b = stage + off + (rr >> 5) * 4096 + (rr & 3) * 4;
+    const int ch = (rr & 31) >> 2;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t[k] = *reinterpret_cast<const float*>(b + swz(q8 + k, ch));
+  }
+  __device__ __forceinline__ void col(int off, float (&t)[8]) const {
+    const float4* p = reinterpret_cast<const float4*>(stage + off + q8 * 4);
+    const float4 a = p[0], c = p[1];
+    t[0] = a.x; t[1] = a.y; t[2] = a.z; t[3] = a.w;
+    t[4] = c.x; t[5] = c.y; t[6] = c.z; t[7] = c.w;
+  }
+  __device__ __forceinline__ void row(int off, float (&t)[8]) const {
+    const float v = *reinterpret_cast<const float*>(stage + off + rr * 4);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t[k] = v;
+  }
+  __device__ __forceinline__ void gather(int leaf, float (&t)[8]) const {
+    const LeafDesc& G = P.leaves[leaf];
+    const int r = r0 + rr;
+#pragma unroll 1
+    for (int k = 0; k < 8; ++k) {
+      const int c = cc0 + q8 + k;
+      float v = 0.f;
+      if (r < P.M && c < P.N) {
+        const uint32_t g = (uint32_t)r * (uint32_t)P.N + (uint32_t)c;
+        uint32_t f = 0;
+        for (int q = 0; q < G.nterms; ++q) f += ((g / (uint32_t)G.d[q]) % (uint32_t)G.m[q]) * (uint32_t)G.s[q];
+        v = __ldg(G.ptr + f);
+      }
+      t[k] = v;
+    }
+  }
+};
+
+// TMA loads of one staged epilogue leaf for rows r0..r0+127, columns
+// cc0..cc0+31.
+__device__ __forceinline__ void gemm_issue_leaf(const CUtensorMap* m, int cls, uint32_t dst, uint32_t bar, int r0,
+                                                int cc0) {
+  if (cls == LEAF_IDENT) {
+    tma_load_2d(dst, m, cc0, r0, bar);
+  } else if (cls == LEAF_TRANS) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) tma_load_2d(dst + b * 4096, m, r0 + 32 * b, cc0, bar);
+  } else if (cls == LEAF_COL) {
+    tma_load_1d(dst, m, cc0, bar);
+  } else if (cls == LEAF_ROW) {
+    tma_load_1d(dst, m, r0, bar);
+  }
+}
+
+// The interpreted epilogue.
+template <int D, int S>
+struct InterpGemmEpi {
+  __device__ static void prefetch(const GemmParams& P) {
+    for (int j = 0; j < P.nleaves; ++j)
+      if (P.leaves[j].cls != LEAF_GATHER) tma_prefetch(&P.maps[P.leaves[j].map_idx]);
+  }
+  __device__ static void issue(const GemmParams& P, uint32_t st, uint32_t bar, int r0, int cc0) {
+    for (int j = 0; j < P.nleaves; ++j) {
+      const LeafDesc& L = P.leaves[j];
+      if (L.cls != LEAF_GATHER) gemm_issue_leaf(&P.maps[L.map_idx], L.cls, st + L.stage_off, bar, r0, cc0);
+    }
+  }
+  struct Env {
+    const GemmEnv& ge;
+    const float (&acc)[8];
+    __device__ __forceinline__ void load_leaf(int arg, float (&t)[8]) const {
+      const LeafDesc& L = ge.P.leaves[arg];
+      if (L.cls == LEAF_IDENT) ge.ident(L.stage_off, t);
+      else if (L.cls == LEAF_TRANS) ge.trans(L.stage_off, t);
+      else if (L.cls == LEAF_COL) ge.col(L.stage_off, t);
+      else if (L.cls == LEAF_ROW) ge.row(L.stage_off, t);
+      else ge.gather(arg, t);
+    }
+    __device__ __forceinline__ void load_acc(float (&t)[8]) const {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) t[k] = acc[k];
+    }
+  };
+  __device__ __forceinline__ static void run(const GemmEnv& ge, const float (&acc)[8], float (&o)[8]) {
+    Machine<D, S, 8> M;
+    Env env{ge, acc};
+    M.run(ge.P.prog, ge.P.nprog, env);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) o[k] = M.TOP[k];
+  }
+};
+
+__device__ __forceinline__ bool gemm_wait(uint32_t bar, uint32_t parity, int64_t limit, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if ((int64_t)(global_ns() - t0) > limit) return false;
+  }
+  return true;
+}
+
+template <class Epi>
+__device__ __forceinline__ void gemm_body(const GemmParams& P) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int abort_flag;
+  __shared__ uint32_t tmem_slot;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // barriers: full[4] empty[4] tfull[2] tempty[2] efull[4] eempty[4] done
+  const uint32_t bars = smem_u32(smem);
+  const uint32_t full0 = bars, empty0 = bars + 32, tfull0 = bars + 64, tempty0 = bars + 80;
+  const uint32_t efull0 = bars + 96, eempty0 = bars + 128, done_bar = bars + 160;
+  uint8_t* opnd = smem + 1024;
+  const int NS = P.nstages, NE = P.n_epi_bufs;
+  uint8_t* ebuf = opnd + NS * (kGemmABytes + kGemmBBytes);
+  uint8_t* obuf = ebuf + NE * P.epi_stage_bytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool staged = P.epi_tx_bytes > 0;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull0 + 8 * b, 1);
+      mbar_init(tempty0 + 8 * b, 4);
+    }
+    for (int e = 0; e < NE; ++e) {
+      mbar_init(efull0 + 8 * e, 1);
+      mbar_init(eempty0 + 8 * e, 4);
+    }
+    mbar_init(done_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const int64_t limit = P.wait_limit_ns;
+
+  if (warp == 0) {
+    // ---- operand producer ----
+    if (lane == 0) {
+      tma_prefetch(&P.mapA);
+      tma_prefetch(&P.mapB);
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < P.ntiles && ok; t += gridDim.x) {
+        const int m0 = (t / P.ntn) * kGemmM, n0 = (t % P.ntn) * kGemmN;
+        for (int kb = 0; kb < P.nkb; ++kb, ++it) {
+          const int s = it % NS;
+          if (it >= NS && !gemm_wait(empty0 + 8 * s, ((it / NS) & 1) ^ 1, limit, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = full0 + 8 * s;
+          const uint32_t a = smem_u32(opnd + s * (kGemmABytes + kGemmBBytes)), b = a + kGemmABytes;
+          const int k0 = kb * kGemmK;
+          mbar_expect_tx(bar, kGemmABytes + kGemmBBytes);
+          if (P.a_mn) {
+            tma_load_2d(a, &P.mapA, m0, k0, bar);
+            tma_load_2d(a + 8192, &P.mapA, m0 + 64, k0, bar);
+          } else {
+            tma_load_2d(a, &P.mapA, k0, m0, bar);
+          }
+          if (P.b_mn) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) tma_load_2d(b + 8192 * i, &P.mapB, n0 + 64 * i, k0, bar);
+          } else {
+            tma_load_2d(b, &P.mapB, k0, n0, bar);
+          }
+        }
+      }
+      if (!ok) {
+        abort_flag = 1;
+        set_error(P.err, DEVERR_TIMEOUT);
+        for (int k = it - NS < 0 ? 0 : it - NS; k < it; ++k) mbar_wait(full0 + 8 * (k % NS), (k / NS) & 1, limit);
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer ----
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kGemmM, kGemmN, P.a_mn, P.b_mn);
+      const uint32_t a_lbo = P.a_mn ? 8192 : 16, b_lbo = P.b_mn ? 8192 : 16;
+      const uint32_t a_step = P.a_mn ? 2048 : 32, b_step = P.b_mn ? 2048 : 32;
+      int it = 0, i = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < P.ntiles && ok; t += gridDim.x, ++i) {
+        const int b = i & 1;
+        if (i >= 2 && !gemm_wait(tempty0 + 8 * b, ((i >> 1) & 1) ^ 1, limit, &abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + b * kGemmN;
+        for (int kb = 0; kb < P.nkb; ++kb, ++it) {
+          const int s = it % NS;
+          if (!gemm_wait(full0 + 8 * s, (it / NS) & 1, limit, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a = smem_u32(opnd + s * (kGemmABytes + kGemmBBytes)), bb = a + kGemmABytes;
+#pragma unroll
+          for (int kk = 0; kk < kGemmK / 16; ++kk) {
+            const uint64_t ad = smem_desc_sw128(a + kk * a_step, a_lbo, 1024);
+            const uint64_t bd = smem_desc_sw128(bb + kk * b_step, b_lbo, 1024);
+            tc_mma_bf16(d, ad, bd, idesc, (kb | kk) != 0);
+          }
+          tc_commit(empty0 + 8 * s);
+        }
+        if (!ok) break;
+        tc_commit(tfull0 + 8 * b);
+      }
+      if (!ok) {
+        abort_flag = 1;
+        set_error(P.err, DEVERR_TIMEOUT);
+      }
+      // every MMA issued has completed before the CTA may free TMEM
+      tc_commit(done_bar);
+      mbar_wait(done_bar, 0, limit);
+    }
+  } else if (warp == 2) {
+    // ---- epilogue leaf producer ----
+    if (lane == 0 && staged) {
+      Epi::prefetch(P);
+      int g = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < P.ntiles && ok; t += gridDim.x) {
+        const int m0 = (t / P.ntn) * kGemmM, n0 = (t % P.ntn) * kGemmN;
+        for (int j = 0; j < kGemmChunks; ++j, ++g) {
+          const int e = g % NE;
+          if (g >= NE && !gemm_wait(eempty0 + 8 * e, ((g / NE) & 1) ^ 1, limit, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(efull0 + 8 * e, P.epi_tx_bytes);
+          Epi::issue(P, smem_u32(ebuf + e * P.epi_stage_bytes), efull0 + 8 * e, m0, n0 + j * kGemmChunk);
+        }
+      }
+      if (!ok) {
+        abort_flag = 1;
+        set_error(P.err, DEVERR_TIMEOUT);
+        for (int k = g - NE < 0 ? 0 : g - NE; k < g; ++k) mbar_wait(efull0 + 8 * (k % NE), (k / NE) & 1, limit);
+      }
+    }
+  } else {
+    // ---- epilogue ----
+    const int q = warp & 3;              // TMEM lane quarter this warp may access
+    const int rr = q * 32 + lane;        // accumulator row of this thread
+    const bool leader = warp == 3 && lane == 0;
+    int g = 0, i = 0;
+    bool dead = false;
+    for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x, ++i) {
+      const int m0 = (t / P.ntn) * kGemmM, n0 = (t % P.ntn) * kGemmN;
+      const int b = i & 1;
+      bool got = gemm_wait(tfull0 + 8 * b, (i >> 1) & 1, limit, &abort_flag);
+      tc_fence_after();
+      for (int j = 0; j < kGemmChunks; ++j, ++g) {
+        const int e = g % NE;
+        if (got && staged) got = gemm_wait(efull0 + 8 * e, (g / NE) & 1, limit, &abort_flag);
+        // tcgen05.ld is warp-collective: decide per warp
+        got = __all_sync(0xffffffffu, got);
+        float acc[32], o[32];
+        if (got) {
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + b * kGemmN + j * kGemmChunk, acc);
+          const uint8_t* st = ebuf + e * P.epi_stage_bytes;
+#pragma unroll
+          for (int s8 = 0; s8 < 4; ++s8) {
+            const GemmEnv env{P, st, rr, m0, n0 + j * kGemmChunk, s8 * 8};
+            float a8[8], o8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) a8[k] = acc[s8 * 8 + k];
+            Epi::run(env, a8, o8);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) o[s8 * 8 + k] = o8[k];
+          }
+        }
+        // the output buffer of chunk j-2 must have been read by its store
+        if (leader) bulk_wait_read<1>();
+        uint32_t any;
+        asm volatile(
+            "{\n .reg .pred p, r;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred r, 2, 128, p;\n selp.u32 %0, 1, 0, r;\n}\n"
+            : "=r"(any)
+            : "r"((uint32_t)!got)
+            : "memory");
+        if (any) {
+          dead = true;
+          break;
+        }
+        uint8_t* ob = obuf + (j & 1) * kGemmOutBytes;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<float4*>(ob + GemmEnv::swz(rr, c)) =
+              make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (staged && lane == 0) mbar_arrive(eempty0 + 8 * e);
+        named_bar_sync(2, 128);
+        if (leader && n0 + j * kGemmChunk < P.N) {
+          tma_store_2d(&P.maps[kMaxStaged], n0 + j * kGemmChunk, m0, smem_u32(ob));
+          bulk_commit();
+        }
+      }
+      if (dead) break;
+      // this accumulator buffer may be overwritten by the next tile's MMAs
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * b);
+    }
+    if (dead) {
+      abort_flag = 1;
+      set_error(P.err, DEVERR_TIMEOUT);
+    }
+    if (leader) bulk_wait<0>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace fg

@@ -563,9 +563,9 @@ void plan_staging(const Graph& g, CompiledGroup& cg, const BuildOpts& o) {
       sb = layout(nullptr);
     }
   } else {
-    // GEMM epilogue: two buffers of staged leaves must fit beside the
-    // operand pipeline; demote leaves beyond 64 KB
-    while (sb > 64 * 1024) {
+    // GEMM epilogue: several buffers of staged leaves must fit beside the
+    // operand pipeline; demote leaves beyond 40 KB per chunk
+    while (sb > 40 * 1024) {
       int last = -1;
       for (size_t i = 0; i < cg.leaves.size(); ++i) if (stage[i]) last = (int)i;
       stage[last] = 0;

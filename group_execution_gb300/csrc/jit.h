@@ -17,5 +17,6 @@ std::string jit_source(const CompiledGroup& cg, int min_blocks);
 // error message.  funcs[i] is the loaded kernel of sources[i].
 std::string jit_compile(const std::vector<std::string>& sources, std::vector<void*>& funcs);
 cudaError_t jit_launch(void* func, const GroupParams& p, int grid, int smem, cudaStream_t st);
+cudaError_t jit_launch_gemm(void* func, const GemmParams& p, int grid, int smem, cudaStream_t st);
 
 }  // namespace fg

@@ -40,7 +40,9 @@ def run_unfused(plan, spec, dev_inputs):
     return env
 
 
-def prepare(spec, seed=0, **build_kw):
+def prepare(spec, seed=0, flags=None, **build_kw):
+    if flags is not None:
+        build_kw["flags"] = flags
     import workloads as W
     inputs = W.make_inputs(spec, seed)
     g = graph_from_spec(spec)

@@ -21,7 +21,7 @@ def _compile(src):
 
 
 @pytest.mark.parametrize("name,kw", [("diamond", {}), ("rnnlm_chain", {"allow_reduce_epilogue": True}),
-                                     ("rnnlm_chain", {})])
+                                     ("rnnlm_chain", {}), ("sf_update", {})])
 def test_config_programs_compile(name, kw):
     spec = getattr(W, name)(**W.CONFIGS[name]["small"])
     plan = graph_from_spec(spec).build(**kw)

@@ -1,0 +1,96 @@
+"""GPU parity of the GEMM-epilogue kernel (tcgen05 MMA into TMEM, fused
+elementwise tail) against the oracle's float64 matmul, through the C ABI."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import workloads as W
+from oracle import execute as OE
+from tests._helpers import rel_err, TOL_F32, TOL_BF16
+from tests._gpu import prepare, run_fused, run_unfused
+from group_execution_gb300 import _lib
+
+pytestmark = pytest.mark.gpu
+MODES = [0, _lib.FG_FLAG_INTERPRET]
+
+
+def _matmul_graph(K, M, N, ta, tb, epi=None):
+    g = W.GraphSpec("mm")
+    a = g.input((K, M) if ta else (M, K), "bf16", ("normal", 0.0, 1.0))
+    b = g.input((N, K) if tb else (K, N), "bf16", ("normal", 0.0, 1.0))
+    m = g.op("matmul_bf16", (a, b), (ta, tb))
+    out = m
+    if epi == "bias_relu":
+        v = g.input((N,))
+        out = g.op("relu", (g.op("badd_col", (m, v)),))
+    elif epi == "trans_leaf":
+        y = g.input((N, M))
+        r = g.input((M,))
+        out = g.op("badd_row", (g.op("add", (m, g.op("transpose", (y,)))), r))
+    g.mark_output(out)
+    return g
+
+
+def _check_matmul_bound(got, A, B):
+    """|G - exact| <= K * 2^-22 * sum_k |a_k b_k| elementwise (f32 accumulation
+    of exact bf16 products, with slack for the tensor core's adder)."""
+    A64, B64 = A.astype(np.float64), B.astype(np.float64)
+    exact = A64 @ B64
+    bound = A64.shape[1] * 2.0 ** -22 * (np.abs(A64) @ np.abs(B64)) + 1e-30
+    assert np.all(np.abs(got.astype(np.float64) - exact) <= bound), np.max(np.abs(got - exact) / bound)
+
+
+@pytest.mark.parametrize("ta,tb", [(1, 0), (0, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("kmn", [(128, 256, 512), (72, 200, 264), (512, 128, 256), (64, 384, 768)])
+@pytest.mark.parametrize("mode", MODES)
+def test_matmul_layouts(ta, tb, kmn, mode):
+    K, M, N = kmn
+    spec = _matmul_graph(K, M, N, ta, tb)
+    g, plan, inputs, dev = prepare(spec, flags=mode)
+    assert plan.groups[0].kind == "gemm"
+    env = run_fused(plan, spec, dev)
+    plan.sync()
+    got = env[spec.outputs[0]].cpu().numpy()
+    A = inputs[0].T if ta else inputs[0]
+    B = inputs[1].T if tb else inputs[1]
+    _check_matmul_bound(got, A, B)
+
+
+@pytest.mark.parametrize("epi", ["bias_relu", "trans_leaf"])
+@pytest.mark.parametrize("mode", MODES)
+def test_matmul_epilogues(epi, mode):
+    spec = _matmul_graph(96, 256, 512, 1, 0, epi)
+    g, plan, inputs, dev = prepare(spec, flags=mode)
+    assert plan.n_groups == 1 and plan.groups[0].kind == "gemm"
+    env = run_fused(plan, spec, dev)
+    plan.sync()
+    ref = OE.run_unfused(spec, inputs)[spec.outputs[0]]
+    assert rel_err(env[spec.outputs[0]].cpu().numpy(), ref) <= 1e-4
+
+
+def _sf_update(B, M, N, mode):
+    spec = W.sf_update(B, M, N)
+    g, plan, inputs, dev = prepare(spec, flags=mode)
+    assert plan.n_groups == 1 and plan.groups[0].kind == "gemm"
+    env = run_fused(plan, spec, dev)
+    plan.sync()
+    ref = OE.run_unfused(spec, inputs)[spec.outputs[0]]
+    got = env[spec.outputs[0]].cpu().numpy()
+    w = inputs[2]
+    assert rel_err(got, ref) <= TOL_F32
+    # the update itself, W - W_new, on its own (W_new ~ W hides G errors)
+    assert rel_err(w - got, w - ref) <= TOL_BF16
+    return plan, spec, dev, env, ref
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_sf_update_small(mode):
+    plan, spec, dev, env, ref = _sf_update(128, 256, 512, mode)
+    envu = run_unfused(plan, spec, dev)
+    plan.sync()
+    assert rel_err(envu[spec.outputs[0]].cpu().numpy(), ref) <= TOL_F32
+
+
+def test_sf_update_full():
+    _sf_update(512, 4096, 4096, 0)
