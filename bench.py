@@ -355,6 +355,32 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
                              "unpack_frac": nbytes / (mu * 1e-3) / 1e9 / hbm, "launches_each": 1,
                              "per_tensor_unfused_launches": 2 * len(sizes)}
 
+    # sufficient-factor gradient + update: one tcgen05 GEMM-epilogue group
+    for B, label in ((512, "sf_update_K512"), (4096, "sf_update_K4096_compute_bound_variant")):
+        sp = W.sf_update(B, 4096, 4096)
+        p = graph_from_spec(sp).build()
+        e = {}
+        for k, v in W.make_inputs(sp).items():
+            t = torch.from_numpy(v).cuda()
+            e[k] = t.to(torch.bfloat16) if sp.values[k].dtype == "bf16" else t
+        for v in sp.ops:
+            e[v.vid] = torch.empty(v.shape, device="cuda")
+        gi = p.groups[0]
+        med, mn = timed(run_plan(p, sp, e, True))
+        medu, _ = timed(run_plan(p, sp, e, False))
+        tflops = gi.alg_flops / (med * 1e-3) / 1e12
+        gbps = gi.alg_bytes / (med * 1e-3) / 1e9
+        t_mem = gi.alg_bytes / (hbm * 1e9)
+        t_mma = gi.alg_flops / (bf16 * 1e12)
+        rows[label] = {"fused_us": med * 1e3, "unfused_us": medu * 1e3, "speedup_vs_unfused": medu / med,
+                       "TFLOPs": tflops, "frac_of_bf16_peak": tflops / bf16, "GBps": gbps, "frac_of_hbm": gbps / hbm,
+                       "roofline_floor_us": max(t_mem, t_mma) * 1e6,
+                       "frac_of_roofline": max(t_mem, t_mma) / (med * 1e-3),
+                       "bound": "hbm" if t_mem > t_mma else "tensor", "alg_flops": gi.alg_flops,
+                       "alg_bytes": gi.alg_bytes, "kernel": "fg_jit_gemm_group (tcgen05, 128x256 TMEM tiles)"}
+        del e
+    torch.cuda.empty_cache()
+
     # random DAG (seed 0), every group in order vs one kernel per operator
     sp = W.random_dag(0)
     p = graph_from_spec(sp).build()

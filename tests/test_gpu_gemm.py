@@ -25,9 +25,15 @@ def _matmul_graph(K, M, N, ta, tb, epi=None):
         v = g.input((N,))
         out = g.op("relu", (g.op("badd_col", (m, v)),))
     elif epi == "trans_leaf":
+        # y2 has two transposed paths into the epilogue, so its post-dominator
+        # is the add inside the matmul group and it fuses there (an injective
+        # group alone never joins a matmul group)
         y = g.input((N, M))
+        y2 = g.op("relu", (y,))
+        t1 = g.op("transpose", (y2,))
+        t2 = g.op("transpose", (g.op("exp", (y2,)),))
         r = g.input((M,))
-        out = g.op("badd_row", (g.op("add", (m, g.op("transpose", (y,)))), r))
+        out = g.op("badd_row", (g.op("add", (m, t1, t2)), r))
     g.mark_output(out)
     return g
 
