@@ -19,6 +19,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "groupexec.h")
 FG_OK, FG_EINVAL, FG_ESHAPE, FG_EUNSUPPORTED, FG_ENOMEM, FG_ECUDA, FG_ETIMEOUT, FG_EDEVICE = range(8)
 FG_F32, FG_BF16 = 0, 1
 FG_FLAG_INTERPRET = 1 << 26
+FG_FLAG_INJECT_NO_LOADS = 1 << 27
 STATUS_NAMES = ["FG_OK", "FG_EINVAL", "FG_ESHAPE", "FG_EUNSUPPORTED", "FG_ENOMEM", "FG_ECUDA",
                 "FG_ETIMEOUT", "FG_EDEVICE"]
 

@@ -336,6 +336,7 @@ void prepare_group(GroupExec& ge, const BuildOpts& o, int nsm) {
   p.tx_bytes = tx;
   p.out_tma = cg.out_tma;
   p.band = (o.flags >> 8) & 0xff;
+  p.inject = (o.flags & FG_FLAG_INJECT_NO_LOADS) ? 1 : 0;
   p.wait_limit_ns = o.wait_limit_ns;
   ge.big = std::max(cg.depth, cg.epi_depth) > 4 || std::max(cg.slots, cg.epi_slots) > 4;
   // compiled programs keep every operator's values in registers: large
@@ -422,6 +423,7 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
   p.wait_limit_ns = o.wait_limit_ns;
   p.epi_stage_bytes = cg.stage_bytes;
   p.epi_tx_bytes = tx;
+  p.inject = (o.flags & FG_FLAG_INJECT_NO_LOADS) ? 1 : 0;
   // operand ring and epilogue-leaf ring depths that fit 227 KB
   const int limit = 227 * 1024, fixed = 2048 + 2 * kGemmM * kGemmChunk * 4;
   int ns = 0, ne = 0;

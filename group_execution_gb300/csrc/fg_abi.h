@@ -136,6 +136,7 @@ struct GroupParams {
   int32_t out_tma;                     // 1: CTA tile via smem + TMA store, 2: per-warp TMA slices, 0: direct stores
   int32_t band;                        // tile order: 0 row-major, else bands of `band` tile rows
   int32_t red_op, nsplit, tiles_per_split, nunits;
+  int32_t inject;                      // failure injection: 1 = the producer issues no loads
 };
 
 // GEMM + epilogue kernel: 128 x 256 accumulator tiles in TMEM, K in blocks
@@ -157,7 +158,12 @@ struct GemmParams {
   int32_t a_mn, b_mn;                  // 1: operand stored MN-major (M or N contiguous)
   int32_t nstages;                     // operand ring depth
   int32_t epi_stage_bytes, epi_tx_bytes, n_epi_bufs;
+  int32_t inject;                      // failure injection: 1 = the producers issue no loads
 };
+
+// Loads already issued always land; waiting for them before a CTA exits uses
+// at least this bound, whatever the user's wait limit.
+constexpr int64_t kDrainLimitNs = 100000000LL;
 
 // Device error codes written to the flag.
 enum DevErr : int { DEVERR_NONE = 0, DEVERR_TIMEOUT = 1, DEVERR_PROGRAM = 2 };

@@ -183,10 +183,11 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   const int64_t limit = P.wait_limit_ns;
+  const int64_t drain = limit > kDrainLimitNs ? limit : kDrainLimitNs;
 
   if (warp == 0) {
     // ---- operand producer ----
-    if (lane == 0) {
+    if (lane == 0 && !P.inject) {
       tma_prefetch(&P.mapA);
       tma_prefetch(&P.mapB);
       int it = 0;
@@ -220,7 +221,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       if (!ok) {
         abort_flag = 1;
         set_error(P.err, DEVERR_TIMEOUT);
-        for (int k = it - NS < 0 ? 0 : it - NS; k < it; ++k) mbar_wait(full0 + 8 * (k % NS), (k / NS) & 1, limit);
+        for (int k = it - NS < 0 ? 0 : it - NS; k < it; ++k) mbar_wait(full0 + 8 * (k % NS), (k / NS) & 1, drain);
       }
     }
   } else if (warp == 1) {
@@ -264,11 +265,11 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       }
       // every MMA issued has completed before the CTA may free TMEM
       tc_commit(done_bar);
-      mbar_wait(done_bar, 0, limit);
+      mbar_wait(done_bar, 0, drain);
     }
   } else if (warp == 2) {
     // ---- epilogue leaf producer ----
-    if (lane == 0 && staged) {
+    if (lane == 0 && staged && !P.inject) {
       Epi::prefetch(P);
       int g = 0;
       bool ok = true;
@@ -287,7 +288,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       if (!ok) {
         abort_flag = 1;
         set_error(P.err, DEVERR_TIMEOUT);
-        for (int k = g - NE < 0 ? 0 : g - NE; k < g; ++k) mbar_wait(efull0 + 8 * (k % NE), (k / NE) & 1, limit);
+        for (int k = g - NE < 0 ? 0 : g - NE; k < g; ++k) mbar_wait(efull0 + 8 * (k % NE), (k / NE) & 1, drain);
       }
     }
   } else {

@@ -273,6 +273,7 @@ struct RedTiles {   // units (row strip, column split), then the split's tiles
 template <class Prog, class Tiles>
 __device__ __forceinline__ void producer_loop(const GroupParams& P, const typename Prog::Tables& T, const Ring& R,
                                               Tiles tiles, volatile int* abort_flag) {
+  if (P.inject) return;   // failure injection: consumers wait for loads that never come
   Prog::prefetch(P, T);
   const int NS = P.nstages;
   int i = 0, tr, tc;
@@ -291,7 +292,8 @@ __device__ __forceinline__ void producer_loop(const GroupParams& P, const typena
   if (!ok) {
     *abort_flag = 1;
     set_error(P.err, DEVERR_TIMEOUT);
-    for (int k = i - NS < 0 ? 0 : i - NS; k < i; ++k) mbar_wait(R.full_s + 8 * (k % NS), (k / NS) & 1, P.wait_limit_ns);
+    const int64_t drain = P.wait_limit_ns > kDrainLimitNs ? P.wait_limit_ns : kDrainLimitNs;
+    for (int k = i - NS < 0 ? 0 : i - NS; k < i; ++k) mbar_wait(R.full_s + 8 * (k % NS), (k / NS) & 1, drain);
   }
 }
 

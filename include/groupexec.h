@@ -102,7 +102,10 @@ typedef struct tf_layout tf_layout;
  * stored by its own TMA store, 3 direct 16-byte stores from registers;
  * bit 26 runs the groups' operator programs on the register-stack
  * interpreter instead of compiling each program to straight-line code when
- * the plan is built (default; needs NVRTC, loaded at run time). */
+ * the plan is built (default; needs NVRTC, loaded at run time); bit 27 is a
+ * failure-injection hook for tests: the kernels' load producers issue
+ * nothing, so every consumer's bounded wait expires and fg_sync_status
+ * reports FG_ETIMEOUT with the context still usable. */
 typedef struct {
   int32_t max_fused_ops;
   int32_t max_args;
