@@ -157,9 +157,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-rows", action="store_true", help="skip the secondary rows")
+    ap.add_argument("--workload", default="diamond",
+                    choices=["diamond", "sf_update", "sf_update_k4096", "pack", "unpack", "rowsum", "rnnlm"],
+                    help="diamond is the headline; the others time one kernel of another row "
+                         "(used for profiling), with the same JSON fields")
+    ap.add_argument("--flags", type=lambda x: int(x, 0), default=0,
+                    help="plan tuning flags (fg_build_opts.flags) for --workload runs")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload != "diamond":
+        return run_single(args)
 
     import torch
     import workloads as W
@@ -256,6 +264,72 @@ def main():
         dist.destroy_process_group()
 
 
+def run_single(args):
+    """One other hot-path row on one GPU: warm-up, then K timed launches."""
+    import torch
+    import workloads as W
+    from group_execution_gb300 import graph_from_spec, TensorFusion
+    torch.cuda.set_device(0)
+    hbm, bf16, _, peak_kind = peaks()
+    flops = 0
+    if args.workload in ("pack", "unpack"):
+        sizes = W.tensor_fusion_sizes(0)
+        xs = [torch.from_numpy(x).cuda() for x in W.tensor_fusion_inputs(sizes)]
+        tf = TensorFusion(xs)
+        buf = torch.empty((tf.total_bytes,), dtype=torch.uint8, device="cuda")
+        tf.pack(0.125, buf)
+        fn = (lambda: tf.pack(0.125, buf)) if args.workload == "pack" else (lambda: tf.unpack(1.0, buf))
+        alg, kernel, wl = int(sizes.sum()) * 6, "tf_" + args.workload + "_kernel", "161 gradient tensors, 25.6M elements"
+    else:
+        if args.workload == "rowsum":
+            spec = W.GraphSpec("rowsum")
+            x = spec.input((R, C))
+            spec.mark_output(spec.op("rowsum", (x,)))
+        elif args.workload == "rnnlm":
+            spec = W.rnnlm_chain()
+        else:
+            spec = W.sf_update(4096 if args.workload == "sf_update_k4096" else 512, 4096, 4096)
+        plan = graph_from_spec(spec).build(allow_reduce_epilogue=args.workload == "rnnlm", flags=args.flags)
+        env = {}
+        for k, v in W.make_inputs(spec).items():
+            t = torch.from_numpy(v).cuda()
+            env[k] = t.to(torch.bfloat16) if spec.values[k].dtype == "bf16" else t
+        for gi in plan.groups:
+            env[gi.out] = torch.empty(spec.values[gi.out].shape, device="cuda")
+
+        def fn():
+            for gid, gi in enumerate(plan.groups):
+                plan.launch_group(gid, {v: env[v] for v in gi.leaves + [gi.out]})
+        alg = sum(gi.alg_bytes for gi in plan.groups)
+        flops = sum(gi.alg_flops for gi in plan.groups)
+        kernel = {"elementwise": "fg_jit_ew_group", "reduce": "fg_jit_reduce_group",
+                  "gemm": "fg_jit_gemm_group"}[plan.groups[-1].kind]
+        wl = spec.name
+    for _ in range(max(3, args.warmup)):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(0) as clk:
+        a.record()
+        for _ in range(args.steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    gbps = alg / (ms * 1e-3) / 1e9
+    line = {"metric": f"{args.workload} HBM GB/s (algorithmic bytes)", "value": gbps, "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": wl}, "gpu_launches": args.steps,
+            "roofline": {"bound": "hbm", "achieved": gbps, "peak": hbm, "unit": "GB/s", "frac": gbps / hbm,
+                         "traffic": None, "kernel": kernel, "peak_source": peak_kind},
+            "clocks": clk.summary()}
+    if flops:
+        line["TFLOPs"] = flops / (ms * 1e-3) / 1e12
+        line["frac_of_bf16_peak"] = line["TFLOPs"] / bf16
+    print(json.dumps(line), flush=True)
+
+
 def traffic_for(kernel, workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current sources."""
@@ -284,7 +358,9 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
     rows = {}
     l2 = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
 
-    def timed(fn, reps=10, flush=True):
+    def timed(fn, reps=10, flush=True, inner=1):
+        """Median and min ms of `inner` back-to-back calls (L2 flushed first
+        when asked), over `reps` repetitions."""
         fn()
         torch.cuda.synchronize()
         ts = []
@@ -293,11 +369,26 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
                 l2.fill_(1)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
-            fn()
+            for _ in range(inner):
+                fn()
             b.record()
             torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
+            ts.append(a.elapsed_time(b) / inner)
         return statistics.median(ts), min(ts)
+
+    def graphed(fn):
+        """The launches of fn captured once into a CUDA graph and replayed:
+        device time without per-launch host work."""
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g.replay
 
     def run_plan(p, sp, env, fused=True):
         def f():
@@ -334,10 +425,14 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
             e.setdefault(v.vid, torch.empty(v.shape, device="cuda"))
         med, mn = timed(run_plan(p, sp, e, True))
         medu, _ = timed(run_plan(p, sp, e, False))
+        gmed, gmn = timed(graphed(run_plan(p, sp, e, True)))
+        gmedu, _ = timed(graphed(run_plan(p, sp, e, False)))
         alg = sum(gi.alg_bytes for gi in p.groups)
         rows["rnnlm_chain" + ("_1group" if epi else "_2groups")] = {
             "fused_us": med * 1e3, "fused_min_us": mn * 1e3, "groups": p.n_groups, "unfused_us": medu * 1e3,
-            "GBps": alg / (med * 1e-3) / 1e9, "note": "launch-latency bound (0.53 MB); L2 flushed"}
+            "graph_fused_us": gmed * 1e3, "graph_fused_min_us": gmn * 1e3, "graph_unfused_us": gmedu * 1e3,
+            "GBps": alg / (gmed * 1e-3) / 1e9,
+            "note": "launch-latency bound (0.53 MB); L2 flushed; graph_* = CUDA-graph replay"}
 
     # tensor-fusion pack / unpack
     from group_execution_gb300 import TensorFusion
@@ -346,8 +441,9 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
     tf = TensorFusion(xs)
     buf = torch.empty((tf.total_bytes,), dtype=torch.uint8, device="cuda")
     nbytes = int(sizes.sum()) * 6
-    mp, _ = timed(lambda: tf.pack(0.125, buf))
-    mu, _ = timed(lambda: tf.unpack(1.0, buf))
+    # 153.6 MB per call exceeds L2: back-to-back calls, no flush
+    mp, _ = timed(lambda: tf.pack(0.125, buf), flush=False, inner=10)
+    mu, _ = timed(lambda: tf.unpack(1.0, buf), flush=False, inner=10)
     rows["tensor_fusion"] = {"tensors": len(sizes), "elements": int(sizes.sum()),
                              "pack_us": mp * 1e3, "pack_GBps": nbytes / (mp * 1e-3) / 1e9,
                              "pack_frac": nbytes / (mp * 1e-3) / 1e9 / hbm,

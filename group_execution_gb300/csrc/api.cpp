@@ -355,10 +355,10 @@ void prepare_group(GroupExec& ge, const BuildOpts& o, int nsm) {
     if (unit > 0) {
       tps = std::min(p.ntc, unit);
     } else {
-      // enough units for two waves of CTAs, each unit long enough to
-      // amortise its combine step
-      const int want = 2 * ctas * nsm;
-      nsplit = std::max(1, std::min((want + p.ntr - 1) / p.ntr, std::max(1, p.ntc / 16)));
+      // whole rows per unit when there is a strip for every SM (no combine
+      // across CTAs); otherwise split the columns just enough to occupy
+      // every SM, each unit long enough to amortise its combine step
+      nsplit = p.ntr >= nsm ? 1 : std::max(1, std::min((nsm + p.ntr - 1) / p.ntr, std::max(1, p.ntc / 16)));
       tps = (p.ntc + nsplit - 1) / nsplit;
     }
     nsplit = (p.ntc + tps - 1) / tps;
@@ -424,15 +424,29 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
   p.epi_stage_bytes = cg.stage_bytes;
   p.epi_tx_bytes = tx;
   p.inject = (o.flags & FG_FLAG_INJECT_NO_LOADS) ? 1 : 0;
-  // operand ring and epilogue-leaf ring depths that fit 227 KB
-  const int limit = 227 * 1024, fixed = 2048 + 2 * kGemmM * kGemmChunk * 4;
+  // an IDENT leaf's chunk buffer receives the result in place, so no
+  // separate output buffers are needed
+  p.inplace_off = -1;
+  for (size_t i = 0; i < cg.leaves.size(); ++i)
+    if (cg.leaves[i].cls == LEAF_IDENT) {
+      p.inplace_off = cg.leaf_stage_off[i];
+      break;
+    }
+  // operand ring and epilogue-leaf ring depths that fit 227 KB, in order of
+  // preference: long K needs a deep operand ring (its feed is latency bound),
+  // short K a deep leaf ring (the epilogue streams the leaves from HBM)
+  const int limit = 227 * 1024, fixed = 2048 + (p.inplace_off >= 0 ? 0 : 2 * kGemmM * kGemmChunk * 4);
   int ns = 0, ne = 0;
-  const int prefs[][2] = {{3, 4}, {3, 3}, {2, 4}, {2, 3}, {3, 2}, {2, 2}};
-  for (const auto& pr : prefs)
+  static const std::vector<std::pair<int, int>> prefs_short = {{3, 5}, {3, 4}, {3, 3}, {2, 4}, {2, 3}, {3, 2}, {2, 2}};
+  static const std::vector<std::pair<int, int>> prefs_long = {{4, 2}, {3, 3}, {3, 2}, {2, 4}, {2, 3}, {2, 2}};
+  const bool short_k = p.nkb <= 16 && cg.stage_bytes > 0;
+  for (const auto& q : short_k ? prefs_short : prefs_long) {
+    const int pr[2] = {q.first, q.second};
     if (!ns && fixed + pr[0] * (kGemmM + kGemmN) * kGemmK * 2 + pr[1] * cg.stage_bytes <= limit) {
       ns = pr[0];
       ne = pr[1];
     }
+  }
   if (!ns) throw CompileError{FG_EUNSUPPORTED, "GEMM epilogue stages do not fit in shared memory"};
   p.nstages = ns;
   p.n_epi_bufs = ne;
@@ -441,7 +455,9 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
   ge.big = cg.depth > 4 || cg.slots > 4;
   ge.compiled = !(o.flags & FG_FLAG_INTERPRET);
   ge.min_blocks = 1;
-  ge.grid = std::max(1, std::min(p.ntiles, nsm));
+  // clusters of kGemmCluster CTAs walk tile groups; one CTA per SM
+  const int units = ((p.ntm + kGemmCluster - 1) / kGemmCluster) * p.ntn;
+  ge.grid = kGemmCluster * std::max(1, std::min(units, nsm / kGemmCluster));
 }
 
 GroupExec make_exec(const Graph& g, const std::vector<int32_t>& nodes, const BuildOpts& o, int nsm) {
@@ -566,7 +582,8 @@ fg_status launch_gemm(GroupExec& ge, void* const* ptrs, void* stream) {
       if (gp.b_mn) {
         dims[0] = cg.N; dims[1] = cg.K; strides[0] = cg.N * 2; box[0] = 64; box[1] = 64;
       } else {
-        dims[0] = cg.K; dims[1] = cg.N; strides[0] = cg.K * 2; box[0] = 64; box[1] = kGemmN;
+        // each CTA of a cluster loads its share of the B tile's rows
+        dims[0] = cg.K; dims[1] = cg.N; strides[0] = cg.K * 2; box[0] = 64; box[1] = kGemmN / kGemmCluster;
       }
       if (fg_status st = encode(&gp.mapB, ptrs[cg.mm_b], 2, dims, strides, box, true, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
         return st;
@@ -580,7 +597,8 @@ fg_status launch_gemm(GroupExec& ge, void* const* ptrs, void* stream) {
           return st;
     }
     gp.out = static_cast<float*>(ptrs[cg.out_value]);
-    if (fg_status st = leaf_map(&gp.maps[kMaxStaged], ptrs[cg.out_value], LEAF_IDENT, cg.FR, cg.FC, kGemmM, kGemmChunk))
+    // each epilogue warp stores its own 32 x 32 box
+    if (fg_status st = leaf_map(&gp.maps[kMaxStaged], ptrs[cg.out_value], LEAF_IDENT, cg.FR, cg.FC, 32, kGemmChunk))
       return st;
     ge.last_ptrs = key;
   }

@@ -5,7 +5,11 @@
 // elementwise successors; TAG's sufficient-factor gradient G = U^T V is the
 // workload).
 //
-// Persistent: one CTA per SM walks 128 x 256 output tiles.  Warp roles:
+// Persistent: one CTA per SM walks 128 x 256 output tiles.  With CL = 2 the
+// CTAs run in pairs (a 2-CTA cluster) on vertically adjacent tiles that share
+// their 256 columns: each CTA loads half of the shared B tile and multicasts
+// it to both, so a K block costs each CTA 32 KB of L2 reads instead of 48 KB.
+// Warp roles:
 //   warp 0  TMA producer of the bf16 operand tiles (64-deep K blocks),
 //   warp 1  allocates TMEM (2 x 256 columns: double-buffered accumulator)
 //           and issues tcgen05.mma from one thread,
@@ -143,16 +147,16 @@ __device__ __forceinline__ bool gemm_wait(uint32_t bar, uint32_t parity, int64_t
   return true;
 }
 
-template <class Epi>
+template <class Epi, int CL>
 __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int abort_flag;
   __shared__ uint32_t tmem_slot;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  // barriers: full[4] empty[4] tfull[2] tempty[2] efull[4] eempty[4] done
+  // barriers: full[4] empty[4] tfull[2] tempty[2] efull[8] eempty[8] done
   const uint32_t bars = smem_u32(smem);
   const uint32_t full0 = bars, empty0 = bars + 32, tfull0 = bars + 64, tempty0 = bars + 80;
-  const uint32_t efull0 = bars + 96, eempty0 = bars + 128, done_bar = bars + 160;
+  const uint32_t efull0 = bars + 96, eempty0 = bars + 160, done_bar = bars + 224;
   uint8_t* opnd = smem + 1024;
   const int NS = P.nstages, NE = P.n_epi_bufs;
   uint8_t* ebuf = opnd + NS * (kGemmABytes + kGemmBBytes);
@@ -160,11 +164,20 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool staged = P.epi_tx_bytes > 0;
 
+  const uint32_t rank = CL > 1 ? cluster_ctarank() : 0;
+  const uint16_t all_ctas = (uint16_t)((1u << CL) - 1);
+  // tile sequence: pairs of vertically adjacent tiles per cluster
+  const int ncl = gridDim.x / CL, cl = blockIdx.x / CL;
+  const int npm = (P.ntm + CL - 1) / CL, nunits = npm * P.ntn;
+  auto tile_of = [&](int u, int& m0, int& n0) {
+    m0 = ((u / P.ntn) * CL + (int)rank) * kGemmM;
+    n0 = (u % P.ntn) * kGemmN;
+  };
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int s = 0; s < NS; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, CL);   // every CTA's MMAs must release a stage
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull0 + 8 * b, 1);
@@ -180,6 +193,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) cluster_sync();   // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   const int64_t limit = P.wait_limit_ns;
@@ -192,8 +206,9 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       tma_prefetch(&P.mapB);
       int it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < P.ntiles && ok; t += gridDim.x) {
-        const int m0 = (t / P.ntn) * kGemmM, n0 = (t % P.ntn) * kGemmN;
+      for (int u = cl; u < nunits && ok; u += ncl) {
+        int m0, n0;
+        tile_of(u, m0, n0);
         for (int kb = 0; kb < P.nkb; ++kb, ++it) {
           const int s = it % NS;
           if (it >= NS && !gemm_wait(empty0 + 8 * s, ((it / NS) & 1) ^ 1, limit, &abort_flag)) {
@@ -203,6 +218,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
           const uint32_t bar = full0 + 8 * s;
           const uint32_t a = smem_u32(opnd + s * (kGemmABytes + kGemmBBytes)), b = a + kGemmABytes;
           const int k0 = kb * kGemmK;
+          // the whole B tile lands in every CTA: its own part plus the peers'
           mbar_expect_tx(bar, kGemmABytes + kGemmBBytes);
           if (P.a_mn) {
             tma_load_2d(a, &P.mapA, m0, k0, bar);
@@ -210,11 +226,24 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
           } else {
             tma_load_2d(a, &P.mapA, k0, m0, bar);
           }
-          if (P.b_mn) {
+          if (CL == 1) {
+            if (P.b_mn) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) tma_load_2d(b + 8192 * i, &P.mapB, n0 + 64 * i, k0, bar);
+              for (int i = 0; i < 4; ++i) tma_load_2d(b + 8192 * i, &P.mapB, n0 + 64 * i, k0, bar);
+            } else {
+              tma_load_2d(b, &P.mapB, k0, n0, bar);
+            }
           } else {
-            tma_load_2d(b, &P.mapB, k0, n0, bar);
+            // this CTA's 1/CL of the B tile, written to every CTA of the pair
+            constexpr int part = kGemmN / CL;   // columns of N per CTA
+            const int nb = n0 + (int)rank * part;
+            if (P.b_mn) {
+#pragma unroll
+              for (int i = 0; i < part / 64; ++i)
+                tma_load_2d_mc(b + 8192 * ((int)rank * (part / 64) + i), &P.mapB, nb + 64 * i, k0, bar, all_ctas);
+            } else {
+              tma_load_2d_mc(b + (int)rank * part * 128, &P.mapB, k0, nb, bar, all_ctas);
+            }
           }
         }
       }
@@ -232,7 +261,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       const uint32_t a_step = P.a_mn ? 2048 : 32, b_step = P.b_mn ? 2048 : 32;
       int it = 0, i = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < P.ntiles && ok; t += gridDim.x, ++i) {
+      for (int u = cl; u < nunits && ok; u += ncl, ++i) {
         const int b = i & 1;
         if (i >= 2 && !gemm_wait(tempty0 + 8 * b, ((i >> 1) & 1) ^ 1, limit, &abort_flag)) {
           ok = false;
@@ -254,7 +283,8 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
             const uint64_t bd = smem_desc_sw128(bb + kk * b_step, b_lbo, 1024);
             tc_mma_bf16(d, ad, bd, idesc, (kb | kk) != 0);
           }
-          tc_commit(empty0 + 8 * s);
+          if (CL == 1) tc_commit(empty0 + 8 * s);
+          else tc_commit_mc(empty0 + 8 * s, all_ctas);   // every CTA may refill the stage
         }
         if (!ok) break;
         tc_commit(tfull0 + 8 * b);
@@ -273,8 +303,9 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       Epi::prefetch(P);
       int g = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < P.ntiles && ok; t += gridDim.x) {
-        const int m0 = (t / P.ntn) * kGemmM, n0 = (t % P.ntn) * kGemmN;
+      for (int u = cl; u < nunits && ok; u += ncl) {
+        int m0, n0;
+        tile_of(u, m0, n0);
         for (int j = 0; j < kGemmChunks; ++j, ++g) {
           const int e = g % NE;
           if (g >= NE && !gemm_wait(eempty0 + 8 * e, ((g / NE) & 1) ^ 1, limit, &abort_flag)) {
@@ -295,11 +326,14 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
     // ---- epilogue ----
     const int q = warp & 3;              // TMEM lane quarter this warp may access
     const int rr = q * 32 + lane;        // accumulator row of this thread
-    const bool leader = warp == 3 && lane == 0;
+    const bool inplace = P.inplace_off >= 0;
+    int prev_e = -1;                     // buffer whose release waits for its store (lane 0)
+
     int g = 0, i = 0;
     bool dead = false;
-    for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x, ++i) {
-      const int m0 = (t / P.ntn) * kGemmM, n0 = (t % P.ntn) * kGemmN;
+    for (int u = cl; u < nunits; u += ncl, ++i) {
+      int m0, n0;
+      tile_of(u, m0, n0);
       const int b = i & 1;
       bool got = gemm_wait(tfull0 + 8 * b, (i >> 1) & 1, limit, &abort_flag);
       tc_fence_after();
@@ -323,30 +357,36 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
             for (int k = 0; k < 8; ++k) o[s8 * 8 + k] = o8[k];
           }
         }
-        // the output buffer of chunk j-2 must have been read by its store
-        if (leader) bulk_wait_read<1>();
-        uint32_t any;
-        asm volatile(
-            "{\n .reg .pred p, r;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred r, 2, 128, p;\n selp.u32 %0, 1, 0, r;\n}\n"
-            : "=r"(any)
-            : "r"((uint32_t)!got)
-            : "memory");
-        if (any) {
+        // this warp's 32 rows x 32 columns go out through its own TMA store:
+        // no barrier across the epilogue warps
+        if (!got) {
           dead = true;
           break;
         }
-        uint8_t* ob = obuf + (j & 1) * kGemmOutBytes;
+        // the result goes to this warp's rows of the IDENT leaf's chunk (read
+        // above, no longer needed) or to a separate double buffer
+        uint8_t* ob = inplace ? ebuf + e * P.epi_stage_bytes + P.inplace_off + q * (32 * 128)
+                              : obuf + (j & 1) * kGemmOutBytes + q * (32 * 128);
+        if (!inplace && lane == 0) bulk_wait_read<1>();   // this buffer's previous store has read it
+        __syncwarp();
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<float4*>(ob + GemmEnv::swz(rr, c)) =
+          *reinterpret_cast<float4*>(ob + GemmEnv::swz(lane, c)) =
               make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
         fence_proxy_async_smem();
         __syncwarp();
-        if (staged && lane == 0) mbar_arrive(eempty0 + 8 * e);
-        named_bar_sync(2, 128);
-        if (leader && n0 + j * kGemmChunk < P.N) {
-          tma_store_2d(&P.maps[kMaxStaged], n0 + j * kGemmChunk, m0, smem_u32(ob));
+        if (lane == 0) {
+          if (staged && !inplace) mbar_arrive(eempty0 + 8 * e);
+          if (n0 + j * kGemmChunk < P.N && m0 + q * 32 < P.M) {
+            tma_store_2d(&P.maps[kMaxStaged], n0 + j * kGemmChunk, m0 + q * 32, smem_u32(ob));
+          }
           bulk_commit();
+          if (inplace) {
+            // the previous chunk's buffer is free once its store has read it
+            bulk_wait_read<1>();
+            if (prev_e >= 0) mbar_arrive(eempty0 + 8 * prev_e);
+            prev_e = e;
+          }
         }
       }
       if (dead) break;
@@ -359,10 +399,12 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       abort_flag = 1;
       set_error(P.err, DEVERR_TIMEOUT);
     }
-    if (leader) bulk_wait<0>();
+    if (lane == 0) bulk_wait<0>();
   }
   tc_fence_before();
   __syncthreads();
+  // no CTA leaves while a peer may still write to its shared memory
+  if (CL > 1) cluster_sync();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
 }

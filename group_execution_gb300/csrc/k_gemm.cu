@@ -8,8 +8,9 @@
 namespace fg {
 
 template <int D, int S>
-__global__ void __launch_bounds__(kGemmThreads, 1) fg_gemm_epi_kernel(const __grid_constant__ GemmParams P) {
-  gemm_body<InterpGemmEpi<D, S>>(P);
+__global__ void __cluster_dims__(kGemmCluster, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    fg_gemm_epi_kernel(const __grid_constant__ GemmParams P) {
+  gemm_body<InterpGemmEpi<D, S>, kGemmCluster>(P);
 }
 
 cudaError_t launch_gemm_kernel(const GemmParams& p, int big, int grid, int smem, cudaStream_t st) {

@@ -18,7 +18,7 @@ int gemm_smem_bytes(const GemmParams& p);
 
 // Tensor fusion.  One chunk = up to kTfChunk consecutive elements of one
 // tensor; the tensor's last chunk also zeroes the padding after it.
-constexpr int kTfChunk = 4096;
+constexpr int kTfChunk = 8192;
 struct TfChunk {
   float* tensor;        // fp32 tensor base
   int64_t start;        // first element of the chunk
