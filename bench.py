@@ -473,7 +473,7 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
                        "roofline_floor_us": max(t_mem, t_mma) * 1e6,
                        "frac_of_roofline": max(t_mem, t_mma) / (med * 1e-3),
                        "bound": "hbm" if t_mem > t_mma else "tensor", "alg_flops": gi.alg_flops,
-                       "alg_bytes": gi.alg_bytes, "kernel": "fg_jit_gemm_group (tcgen05, 128x256 TMEM tiles)"}
+                       "alg_bytes": gi.alg_bytes, "kernel": "fg_jit_gemm_group (tcgen05 cta_group::2, 256x256 tiles per CTA pair)"}
         del e
     torch.cuda.empty_cache()
 

@@ -201,3 +201,8 @@ class TensorFusion:
     def unpack(self, uscale, buf, stream=None):
         _lib.check(self.lib.tf_unpack(self.h, C.c_float(uscale), C.c_void_p(buf.data_ptr()),
                                       _stream_handle(stream)))
+
+    def sync(self, stream=None):
+        """Waits for the stream; raises FgError (FG_ETIMEOUT) if an unpack
+        recorded an expired wait."""
+        _lib.check(self.lib.tf_sync_status(self.h, _stream_handle(stream)))

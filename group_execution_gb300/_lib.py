@@ -68,6 +68,7 @@ SIGNATURES = {
     "tf_layout_create": (_I32, [_I32, _PI64, C.POINTER(_P), _I32, _I64, C.POINTER(_P), _PI64, _PI64]),
     "tf_pack": (_I32, [_P, _F, _P, _P]),
     "tf_unpack": (_I32, [_P, _F, _P, _P]),
+    "tf_sync_status": (_I32, [_P, _P]),
     "tf_layout_destroy": (None, [_P]),
 }
 

@@ -109,7 +109,8 @@ struct tf_layout {
   int64_t total = 0;
   std::vector<int64_t> numel, offsets;
   std::vector<float*> grads;
-  TfChunk* d_chunks = nullptr;
+  TfChunk* d_chunks = nullptr;       // chunk table, followed by the device error word
+  int32_t* d_err = nullptr;
   int nchunks = 0;
 };
 
@@ -420,6 +421,10 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
   p.nkb = (int32_t)((cg.K + kGemmK - 1) / kGemmK);
   p.a_mn = a_mn;
   p.b_mn = b_mn;
+  // two 64-wide column groups per copy when the contiguous extent splits
+  // into whole groups (a 3-D view would otherwise wrap into the next row)
+  p.a_3d = a_mn && cg.M % 64 == 0;
+  p.b_3d = b_mn && cg.N % 64 == 0;
   p.wait_limit_ns = o.wait_limit_ns;
   p.epi_stage_bytes = cg.stage_bytes;
   p.epi_tx_bytes = tx;
@@ -434,28 +439,34 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
     }
   // operand ring and epilogue-leaf ring depths that fit 227 KB, in order of
   // preference: long K needs a deep operand ring (its feed is latency bound),
-  // short K a deep leaf ring (the epilogue streams the leaves from HBM)
-  const int limit = 227 * 1024, fixed = 2048 + (p.inplace_off >= 0 ? 0 : 2 * kGemmM * kGemmChunk * 4);
+  // short K a deep leaf ring (the epilogue streams the leaves from HBM).  A
+  // CTA stages its 128 rows of A and its half of B's columns per K block.
+  const int limit = 227 * 1024 - 256, fixed = 2048 + (p.inplace_off >= 0 ? 0 : 2 * kGemmM * kGemmChunk * 4);
+  const int stage = (kGemmM + kGemmN / kGemmCluster) * kGemmK * 2;
   int ns = 0, ne = 0;
-  static const std::vector<std::pair<int, int>> prefs_short = {{3, 5}, {3, 4}, {3, 3}, {2, 4}, {2, 3}, {3, 2}, {2, 2}};
-  static const std::vector<std::pair<int, int>> prefs_long = {{4, 2}, {3, 3}, {3, 2}, {2, 4}, {2, 3}, {2, 2}};
+  static const std::vector<std::pair<int, int>> prefs_short = {{4, 6}, {4, 5}, {4, 4}, {3, 4}, {3, 3},
+                                                               {2, 4}, {2, 3}, {3, 2}, {2, 2}};
+  static const std::vector<std::pair<int, int>> prefs_long = {{6, 2}, {5, 3}, {5, 2}, {4, 3}, {4, 2},
+                                                              {3, 3}, {3, 2}, {2, 4}, {2, 3}, {2, 2}};
   const bool short_k = p.nkb <= 16 && cg.stage_bytes > 0;
   for (const auto& q : short_k ? prefs_short : prefs_long) {
-    const int pr[2] = {q.first, q.second};
-    if (!ns && fixed + pr[0] * (kGemmM + kGemmN) * kGemmK * 2 + pr[1] * cg.stage_bytes <= limit) {
-      ns = pr[0];
-      ne = pr[1];
+    if (!ns && fixed + q.first * stage + q.second * cg.stage_bytes <= limit) {
+      ns = q.first;
+      ne = q.second;
     }
   }
   if (!ns) throw CompileError{FG_EUNSUPPORTED, "GEMM epilogue stages do not fit in shared memory"};
   p.nstages = ns;
   p.n_epi_bufs = ne;
-  ge.smem = fixed + ns * (kGemmM + kGemmN) * kGemmK * 2 + ne * cg.stage_bytes;
+  ge.smem = fixed + ns * stage + ne * cg.stage_bytes;
+  // more than half of an SM's shared memory: one CTA per SM, so no two CTAs
+  // ever compete for the SM's TMEM
+  ge.smem = std::max(ge.smem, 120 * 1024);
   cg.nstages = ns;
   ge.big = cg.depth > 4 || cg.slots > 4;
   ge.compiled = !(o.flags & FG_FLAG_INTERPRET);
   ge.min_blocks = 1;
-  // clusters of kGemmCluster CTAs walk tile groups; one CTA per SM
+  // CTA pairs walk 256-row tile units; one CTA per SM
   const int units = ((p.ntm + kGemmCluster - 1) / kGemmCluster) * p.ntn;
   ge.grid = kGemmCluster * std::max(1, std::min(units, nsm / kGemmCluster));
 }
@@ -569,23 +580,35 @@ fg_status launch_gemm(GroupExec& ge, void* const* ptrs, void* stream) {
     if (fg_status st = check_ptr(ptrs[cg.out_value], cg.out_value)) return st;
     {
       // A: [K, M] (M contiguous) when transposed, else [M, K]
-      uint64_t dims[2], strides[1];
-      uint32_t box[2];
-      if (gp.a_mn) {
+      // (MN-major with whole 64-wide groups: [M/64, K, 64], one box of two
+      // groups per copy)
+      uint64_t dims[3], strides[2];
+      uint32_t box[3];
+      int rank = 2;
+      if (gp.a_3d) {
+        dims[0] = 64; dims[1] = cg.K; dims[2] = cg.M / 64; strides[0] = cg.M * 2; strides[1] = 128;
+        box[0] = 64; box[1] = 64; box[2] = 2; rank = 3;
+      } else if (gp.a_mn) {
         dims[0] = cg.M; dims[1] = cg.K; strides[0] = cg.M * 2; box[0] = 64; box[1] = 64;
       } else {
         dims[0] = cg.K; dims[1] = cg.M; strides[0] = cg.K * 2; box[0] = 64; box[1] = kGemmM;
       }
-      if (fg_status st = encode(&gp.mapA, ptrs[cg.mm_a], 2, dims, strides, box, true, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+      if (fg_status st = encode(&gp.mapA, ptrs[cg.mm_a], rank, dims, strides, box, true,
+                                CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
         return st;
       // B: [K, N] (N contiguous), or [N, K] when transposed
-      if (gp.b_mn) {
+      rank = 2;
+      if (gp.b_3d) {
+        dims[0] = 64; dims[1] = cg.K; dims[2] = cg.N / 64; strides[0] = cg.N * 2; strides[1] = 128;
+        box[0] = 64; box[1] = 64; box[2] = 2; rank = 3;
+      } else if (gp.b_mn) {
         dims[0] = cg.N; dims[1] = cg.K; strides[0] = cg.N * 2; box[0] = 64; box[1] = 64;
       } else {
-        // each CTA of a cluster loads its share of the B tile's rows
+        // each CTA of a pair stages its half of the B tile's columns
         dims[0] = cg.K; dims[1] = cg.N; strides[0] = cg.K * 2; box[0] = 64; box[1] = kGemmN / kGemmCluster;
       }
-      if (fg_status st = encode(&gp.mapB, ptrs[cg.mm_b], 2, dims, strides, box, true, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+      if (fg_status st = encode(&gp.mapB, ptrs[cg.mm_b], rank, dims, strides, box, true,
+                                CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
         return st;
     }
     for (size_t i = 0; i < cg.leaves.size(); ++i) {
@@ -859,9 +882,12 @@ fg_status tf_layout_create(int32_t n, const int64_t* numel, float* const* grads,
   }
   l->nchunks = (int)ch.size();
   if (!device_present(nullptr)) return err(FG_ECUDA, "no CUDA device");
-  cudaError_t e = cudaMalloc(&l->d_chunks, sizeof(TfChunk) * ch.size());
+  const size_t table = round_up((int64_t)(sizeof(TfChunk) * ch.size()), 256);
+  cudaError_t e = cudaMalloc(&l->d_chunks, table + 256);
   if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(chunk table)");
+  l->d_err = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(l->d_chunks) + table);
   e = cudaMemcpy(l->d_chunks, ch.data(), sizeof(TfChunk) * ch.size(), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemset(l->d_err, 0, sizeof(int32_t));
   if (e != cudaSuccess) {
     cudaFree(l->d_chunks);
     return cuda_err(e, "cudaMemcpy(chunk table)");
@@ -889,9 +915,25 @@ fg_status tf_pack(const tf_layout* l, float scale, void* buf, void* stream) {
 fg_status tf_unpack(const tf_layout* l, float uscale, const void* buf, void* stream) {
   if (!l || !buf) return err(FG_EINVAL, "null argument");
   if (reinterpret_cast<uintptr_t>(buf) % 256) return err(FG_EINVAL, "fusion buffer must be 256-byte aligned");
-  cudaError_t e = launch_tf_unpack(l->d_chunks, l->nchunks, l->buf_bf16, uscale, buf, tf_grid(l),
+  int nsm = 148;
+  device_present(&nsm);
+  cudaError_t e = launch_tf_unpack(l->d_chunks, l->nchunks, l->buf_bf16, uscale, buf,
+                                   std::max(1, std::min(l->nchunks, nsm)), l->d_err,
                                    static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FG_OK : cuda_err(e, "tf_unpack launch");
+}
+
+fg_status tf_sync_status(tf_layout* l, void* stream) {
+  if (!l) return err(FG_EINVAL, "null layout");
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_err(e, "cudaStreamSynchronize");
+  int32_t flag = 0;
+  e = cudaMemcpy(&flag, l->d_err, sizeof(flag), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_err(e, "reading the device error flag");
+  if (flag == 0) return FG_OK;
+  cudaMemset(l->d_err, 0, sizeof(int32_t));
+  if (flag == DEVERR_TIMEOUT) return err(FG_ETIMEOUT, "a device-side wait for a chunk load expired");
+  return err(FG_EDEVICE, "device error flag " + std::to_string(flag));
 }
 
 void tf_layout_destroy(tf_layout* l) {

@@ -5,14 +5,17 @@
 // elementwise successors; TAG's sufficient-factor gradient G = U^T V is the
 // workload).
 //
-// Persistent: one CTA per SM walks 128 x 256 output tiles.  With CL = 2 the
-// CTAs run in pairs (a 2-CTA cluster) on vertically adjacent tiles that share
-// their 256 columns: each CTA loads half of the shared B tile and multicasts
-// it to both, so a K block costs each CTA 32 KB of L2 reads instead of 48 KB.
-// Warp roles:
-//   warp 0  TMA producer of the bf16 operand tiles (64-deep K blocks),
-//   warp 1  allocates TMEM (2 x 256 columns: double-buffered accumulator)
-//           and issues tcgen05.mma from one thread,
+// Persistent: CTAs run in pairs (a 2-CTA cluster) on the SMs of one TPC, and
+// a pair walks 256 x 256 output tiles.  Each CTA stages half of the tile's A
+// rows and half of its B columns (32 KB per 64-deep K block); the even CTA
+// issues 2-SM tcgen05.mma instructions (cta_group::2) that read both CTAs'
+// halves and leave each CTA's 128 accumulator rows in its own TMEM.  Warp
+// roles, in each CTA:
+//   warp 0  TMA producer of the bf16 operand halves; every load completes on
+//           the even CTA's stage barrier,
+//   warp 1  allocates TMEM (2 x 256 columns: double-buffered accumulator,
+//           jointly with the peer) and, in the even CTA, issues the MMAs from
+//           one thread,
 //   warp 2  TMA producer of the epilogue leaves, 128 x 32 chunk by chunk,
 //   warps 3-6 epilogue: each thread owns one accumulator row (TMEM lane),
 //           reads 32 columns per chunk with tcgen05.ld, evaluates the
@@ -27,8 +30,8 @@
 namespace fg {
 
 constexpr int kGemmThreads = kGemmWarps * 32;
-constexpr int kGemmABytes = kGemmM * kGemmK * 2;    // 16 KB
-constexpr int kGemmBBytes = kGemmN * kGemmK * 2;    // 32 KB
+constexpr int kGemmABytes = kGemmM * kGemmK * 2;    // 16 KB: this CTA's 128 rows of A
+constexpr int kGemmBBytes = kGemmN * kGemmK * 2;    // 32 KB: the whole B block of a tile
 constexpr int kGemmOutBytes = kGemmM * kGemmChunk * 4;   // 16 KB
 constexpr int kGemmChunks = kGemmN / kGemmChunk;    // 8
 
@@ -147,26 +150,31 @@ __device__ __forceinline__ bool gemm_wait(uint32_t bar, uint32_t parity, int64_t
   return true;
 }
 
+// CL = 1: one CTA per 128 x 256 tile (cta_group::1).  CL = 2: a CTA pair per
+// 256 x 256 tile (cta_group::2), each CTA holding half of B.
 template <class Epi, int CL>
 __device__ __forceinline__ void gemm_body(const GemmParams& P) {
+  static_assert(CL == 1 || CL == 2, "CTA group of one or two");
+  constexpr int kStageBytes = kGemmABytes + kGemmBBytes / CL;   // per CTA
+  constexpr int kBCols = kGemmN / CL;                            // B columns staged per CTA
   extern __shared__ uint8_t smem_raw[];
   __shared__ int abort_flag;
   __shared__ uint32_t tmem_slot;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  // barriers: full[4] empty[4] tfull[2] tempty[2] efull[8] eempty[8] done
+  // barriers: full[16] empty[16] tfull[2] tempty[2] efull[8] eempty[8] done
   const uint32_t bars = smem_u32(smem);
-  const uint32_t full0 = bars, empty0 = bars + 32, tfull0 = bars + 64, tempty0 = bars + 80;
-  const uint32_t efull0 = bars + 96, eempty0 = bars + 160, done_bar = bars + 224;
+  const uint32_t full0 = bars, empty0 = bars + 128, tfull0 = bars + 256, tempty0 = bars + 272;
+  const uint32_t efull0 = bars + 288, eempty0 = bars + 352, done_bar = bars + 416;
   uint8_t* opnd = smem + 1024;
   const int NS = P.nstages, NE = P.n_epi_bufs;
-  uint8_t* ebuf = opnd + NS * (kGemmABytes + kGemmBBytes);
+  uint8_t* ebuf = opnd + NS * kStageBytes;
   uint8_t* obuf = ebuf + NE * P.epi_stage_bytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool staged = P.epi_tx_bytes > 0;
 
   const uint32_t rank = CL > 1 ? cluster_ctarank() : 0;
-  const uint16_t all_ctas = (uint16_t)((1u << CL) - 1);
-  // tile sequence: pairs of vertically adjacent tiles per cluster
+  const bool leader = rank == 0;
+  // tile sequence: units of CL vertically adjacent 128-row tiles
   const int ncl = gridDim.x / CL, cl = blockIdx.x / CL;
   const int npm = (P.ntm + CL - 1) / CL, nunits = npm * P.ntn;
   auto tile_of = [&](int u, int& m0, int& n0) {
@@ -177,11 +185,11 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
     abort_flag = 0;
     for (int s = 0; s < NS; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, CL);   // every CTA's MMAs must release a stage
+      mbar_init(empty0 + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull0 + 8 * b, 1);
-      mbar_init(tempty0 + 8 * b, 4);
+      mbar_init(tempty0 + 8 * b, 4 * CL);   // every epilogue warp of the pair
     }
     for (int e = 0; e < NE; ++e) {
       mbar_init(efull0 + 8 * e, 1);
@@ -190,10 +198,10 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
     mbar_init(done_bar, 1);
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), 512);
+  if (warp == 1) tmem_alloc<CL>(smem_u32(&tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
-  if (CL > 1) cluster_sync();   // peers' barriers are initialised before any multicast
+  if (CL > 1) cluster_sync();   // the peer's barriers are initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   const int64_t limit = P.wait_limit_ns;
@@ -215,34 +223,50 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
             ok = false;
             break;
           }
-          const uint32_t bar = full0 + 8 * s;
-          const uint32_t a = smem_u32(opnd + s * (kGemmABytes + kGemmBBytes)), b = a + kGemmABytes;
+          const uint32_t a = smem_u32(opnd + s * kStageBytes), b = a + kGemmABytes;
           const int k0 = kb * kGemmK;
-          // the whole B tile lands in every CTA: its own part plus the peers'
-          mbar_expect_tx(bar, kGemmABytes + kGemmBBytes);
-          if (P.a_mn) {
-            tma_load_2d(a, &P.mapA, m0, k0, bar);
-            tma_load_2d(a + 8192, &P.mapA, m0 + 64, k0, bar);
-          } else {
-            tma_load_2d(a, &P.mapA, k0, m0, bar);
-          }
+          const int nb = n0 + (int)rank * kBCols;
           if (CL == 1) {
-            if (P.b_mn) {
-#pragma unroll
-              for (int i = 0; i < 4; ++i) tma_load_2d(b + 8192 * i, &P.mapB, n0 + 64 * i, k0, bar);
+            const uint32_t bar = full0 + 8 * s;
+            mbar_expect_tx(bar, kStageBytes);
+            if (P.a_3d) {
+              tma_load_3d(a, &P.mapA, 0, k0, m0 / 64, bar);
+            } else if (P.a_mn) {
+              tma_load_2d(a, &P.mapA, m0, k0, bar);
+              tma_load_2d(a + 8192, &P.mapA, m0 + 64, k0, bar);
             } else {
-              tma_load_2d(b, &P.mapB, k0, n0, bar);
+              tma_load_2d(a, &P.mapA, k0, m0, bar);
+            }
+            if (P.b_3d) {
+#pragma unroll
+              for (int i = 0; i < kBCols / 128; ++i) tma_load_3d(b + 16384 * i, &P.mapB, 0, k0, nb / 64 + 2 * i, bar);
+            } else if (P.b_mn) {
+#pragma unroll
+              for (int i = 0; i < kBCols / 64; ++i) tma_load_2d(b + 8192 * i, &P.mapB, nb + 64 * i, k0, bar);
+            } else {
+#pragma unroll
+              for (int i = 0; i < kBCols / 128; ++i) tma_load_2d(b + 16384 * i, &P.mapB, k0, nb + 128 * i, bar);
             }
           } else {
-            // this CTA's 1/CL of the B tile, written to every CTA of the pair
-            constexpr int part = kGemmN / CL;   // columns of N per CTA
-            const int nb = n0 + (int)rank * part;
-            if (P.b_mn) {
-#pragma unroll
-              for (int i = 0; i < part / 64; ++i)
-                tma_load_2d_mc(b + 8192 * ((int)rank * (part / 64) + i), &P.mapB, nb + 64 * i, k0, bar, all_ctas);
+            // both CTAs' halves are counted on the even CTA's barrier, which
+            // the even CTA alone arms with the whole block's bytes
+            const uint32_t cbar = cluster_addr(full0 + 8 * s, 0);
+            if (leader) mbar_expect_tx(full0 + 8 * s, CL * kStageBytes);
+            if (P.a_3d) {
+              tma_load_3d_pair(a, &P.mapA, 0, k0, m0 / 64, cbar);
+            } else if (P.a_mn) {
+              tma_load_2d_pair(a, &P.mapA, m0, k0, cbar);
+              tma_load_2d_pair(a + 8192, &P.mapA, m0 + 64, k0, cbar);
             } else {
-              tma_load_2d_mc(b + (int)rank * part * 128, &P.mapB, k0, nb, bar, all_ctas);
+              tma_load_2d_pair(a, &P.mapA, k0, m0, cbar);
+            }
+            if (P.b_3d) {
+              tma_load_3d_pair(b, &P.mapB, 0, k0, nb / 64, cbar);
+            } else if (P.b_mn) {
+#pragma unroll
+              for (int i = 0; i < kBCols / 64; ++i) tma_load_2d_pair(b + 8192 * i, &P.mapB, nb + 64 * i, k0, cbar);
+            } else {
+              tma_load_2d_pair(b, &P.mapB, k0, nb, cbar);
             }
           }
         }
@@ -250,22 +274,35 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       if (!ok) {
         abort_flag = 1;
         set_error(P.err, DEVERR_TIMEOUT);
-        for (int k = it - NS < 0 ? 0 : it - NS; k < it; ++k) mbar_wait(full0 + 8 * (k % NS), (k / NS) & 1, drain);
+        // loads in flight complete on the even CTA's barriers: that CTA
+        // drains them (the odd CTA stays resident until then, at the final
+        // cluster barrier)
+        if (leader)
+          for (int k = it - NS < 0 ? 0 : it - NS; k < it; ++k) mbar_wait(full0 + 8 * (k % NS), (k / NS) & 1, drain);
       }
     }
   } else if (warp == 1) {
-    // ---- MMA issuer ----
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kGemmM, kGemmN, P.a_mn, P.b_mn);
+    // ---- MMA issuer (the even CTA of a pair) ----
+    if (lane == 0 && leader) {
+      const uint32_t idesc = idesc_bf16_f32(CL * kGemmM, kGemmN, P.a_mn, P.b_mn);
       const uint32_t a_lbo = P.a_mn ? 8192 : 16, b_lbo = P.b_mn ? 8192 : 16;
       const uint32_t a_step = P.a_mn ? 2048 : 32, b_step = P.b_mn ? 2048 : 32;
       int it = 0, i = 0;
       bool ok = true;
       for (int u = cl; u < nunits && ok; u += ncl, ++i) {
         const int b = i & 1;
-        if (i >= 2 && !gemm_wait(tempty0 + 8 * b, ((i >> 1) & 1) ^ 1, limit, &abort_flag)) {
-          ok = false;
-          break;
+        if (i >= 2) {
+          // both CTAs' epilogues have drained this accumulator buffer
+          bool got = mbar_try_wait_cluster(tempty0 + 8 * b, ((i >> 1) & 1) ^ 1);
+          if (!got) {
+            const uint64_t t0 = global_ns();
+            while (!(got = mbar_try_wait_cluster(tempty0 + 8 * b, ((i >> 1) & 1) ^ 1)))
+              if (abort_flag || (int64_t)(global_ns() - t0) > limit) break;
+          }
+          if (!got) {
+            ok = false;
+            break;
+          }
         }
         tc_fence_after();
         const uint32_t d = tmem + b * kGemmN;
@@ -276,25 +313,24 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
             break;
           }
           tc_fence_after();
-          const uint32_t a = smem_u32(opnd + s * (kGemmABytes + kGemmBBytes)), bb = a + kGemmABytes;
+          const uint32_t a = smem_u32(opnd + s * kStageBytes), bb = a + kGemmABytes;
 #pragma unroll
           for (int kk = 0; kk < kGemmK / 16; ++kk) {
             const uint64_t ad = smem_desc_sw128(a + kk * a_step, a_lbo, 1024);
             const uint64_t bd = smem_desc_sw128(bb + kk * b_step, b_lbo, 1024);
-            tc_mma_bf16(d, ad, bd, idesc, (kb | kk) != 0);
+            tc_mma_bf16<CL>(d, ad, bd, idesc, (kb | kk) != 0);
           }
-          if (CL == 1) tc_commit(empty0 + 8 * s);
-          else tc_commit_mc(empty0 + 8 * s, all_ctas);   // every CTA may refill the stage
+          tc_commit<CL>(empty0 + 8 * s);   // both CTAs may refill the stage
         }
         if (!ok) break;
-        tc_commit(tfull0 + 8 * b);
+        tc_commit<CL>(tfull0 + 8 * b);
       }
       if (!ok) {
         abort_flag = 1;
         set_error(P.err, DEVERR_TIMEOUT);
       }
-      // every MMA issued has completed before the CTA may free TMEM
-      tc_commit(done_bar);
+      // every MMA issued has completed before either CTA may free TMEM
+      tc_commit<CL>(done_bar);
       mbar_wait(done_bar, 0, drain);
     }
   } else if (warp == 2) {
@@ -393,7 +429,10 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       // this accumulator buffer may be overwritten by the next tile's MMAs
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty0 + 8 * b);
+      if (lane == 0) {
+        if (CL == 1) mbar_arrive(tempty0 + 8 * b);
+        else mbar_arrive_cluster(cluster_addr(tempty0 + 8 * b, 0));
+      }
     }
     if (dead) {
       abort_flag = 1;
@@ -403,10 +442,11 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   }
   tc_fence_before();
   __syncthreads();
-  // no CTA leaves while a peer may still write to its shared memory
+  // no CTA leaves while its peer may still write to its shared memory or
+  // issue MMAs into its TMEM
   if (CL > 1) cluster_sync();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (warp == 1) tmem_dealloc<CL>(tmem, 512);
 }
 
 }  // namespace fg

@@ -4,14 +4,20 @@
 // size is the sum of theirs).
 //
 // The host splits every tensor into chunks of up to 8192 elements and uploads
-// the chunk table once; CTAs stride over chunks.  Each thread issues all of
-// its loads for a full chunk (32 elements: 128 bytes when packing, 64 bytes
-// when unpacking bf16) before any conversion, and the next chunk's
-// descriptor is fetched while the current chunk is in flight.  A tensor's last chunk also zeroes the padding
-// up to the next aligned offset, so the buffer is fully defined.
+// the chunk table once.  Pack: CTAs stride over chunks; each thread issues all
+// of its loads for a full chunk (32 elements, 128 bytes) before any
+// conversion, and the next chunk's descriptor is fetched while the current
+// chunk is in flight.  A tensor's last chunk also zeroes the padding up to the
+// next aligned offset, so the buffer is fully defined.  Unpack: one CTA per SM;
+// a producer warp brings chunks of the buffer into a shared-memory ring with
+// bulk copies (rounded up to 16 bytes, which stays inside the tensor's
+// padding), four warps widen and scale them into a staging buffer, and each
+// chunk leaves as one bulk store of its 16-byte multiple plus at most three
+// plain stores.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "fg_device.cuh"
 #include "launch.h"
 
 namespace fg {
@@ -19,8 +25,7 @@ namespace fg {
 namespace {
 
 constexpr int kPackThreads = 256;     // pack: 32 elements (128 bytes of loads) per thread
-constexpr int kUnpackThreads = 256;   // unpack: 32 bf16 elements (64 bytes of loads) per thread
-static_assert(kTfChunk == 32 * kPackThreads && kTfChunk == 32 * kUnpackThreads, "chunk geometry");
+static_assert(kTfChunk == 32 * kPackThreads, "chunk geometry");
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -74,62 +79,121 @@ __global__ void __launch_bounds__(kPackThreads) tf_pack_kernel(const TfChunk* __
   }
 }
 
-__global__ void __launch_bounds__(kUnpackThreads) tf_unpack_kernel(const TfChunk* __restrict__ chunks, int nchunks,
-                                                                 int bf16, float uscale,
-                                                                 const uint8_t* __restrict__ buf) {
-  int ci = blockIdx.x;
-  if (ci >= nchunks) return;
-  TfChunk c = chunks[ci];
-  for (; ci < nchunks; ci += gridDim.x) {
-    const int nx = ci + gridDim.x;
-    TfChunk cn;
-    if (nx < nchunks) cn = chunks[nx];
-    float* dst = c.tensor + c.start;
-    const uint8_t* src = buf + c.buf_off;
-    if (c.count == kTfChunk && bf16) {
-      // 8 bf16 (16 bytes) per load, four loads per thread
-      uint4 h[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) h[k] = __ldcs(reinterpret_cast<const uint4*>(src) + threadIdx.x + k * kUnpackThreads);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int e = 8 * (threadIdx.x + k * kUnpackThreads);
-        const uint32_t w[4] = {h[k].x, h[k].y, h[k].z, h[k].w};
-        float f[8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          f[2 * j] = __fmul_rn(__uint_as_float(w[j] << 16), uscale);
-          f[2 * j + 1] = __fmul_rn(__uint_as_float(w[j] & 0xffff0000u), uscale);
+constexpr int kUnpackConsumers = 128;                  // four warps
+constexpr int kUnpackThreadsTma = 32 + kUnpackConsumers;  // + the producer warp
+constexpr int kUnpackOutBufs = 4;
+constexpr int kUnpackOutBytes = kTfChunk * 4;
+constexpr int64_t kUnpackWaitNs = 100000000LL;          // 100 ms: a chunk load never takes this long
+
+// Stages of the load ring: bf16 chunks are 16 KB, f32 chunks 32 KB.
+__host__ __device__ constexpr int unpack_stages(int bf16) { return bf16 ? 4 : 3; }
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+               "r"(src), "r"(bytes)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kUnpackThreadsTma, 1)
+    tf_unpack_kernel(const TfChunk* __restrict__ chunks, int nchunks, int bf16, float uscale,
+                     const uint8_t* __restrict__ buf, int32_t* err) {
+  extern __shared__ uint8_t sm_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 127) & ~uintptr_t(127));
+  const int NS = unpack_stages(bf16);
+  const int stage_bytes = kTfChunk * (bf16 ? 2 : 4);
+  const uint32_t full0 = smem_u32(sm), empty0 = full0 + 64;
+  uint8_t* stage0 = sm + 128;
+  uint8_t* out0 = stage0 + NS * stage_bytes;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5;
+
+  if (warp == 0) {
+    // ---- producer: one bulk copy per chunk ----
+    if (threadIdx.x == 0) {
+      int k = 0;
+      bool ok = true;
+      for (int ci = blockIdx.x; ci < nchunks; ci += gridDim.x, ++k) {
+        const int s = k % NS;
+        if (k >= NS && !mbar_wait(empty0 + 8 * s, ((k / NS) & 1) ^ 1, kUnpackWaitNs)) {
+          ok = false;
+          break;
         }
-        __stcs(reinterpret_cast<float4*>(dst + e), make_float4(f[0], f[1], f[2], f[3]));
-        __stcs(reinterpret_cast<float4*>(dst + e) + 1, make_float4(f[4], f[5], f[6], f[7]));
-      }
-    } else if (c.count == kTfChunk) {
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float4 v[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          v[k] = __ldcs(reinterpret_cast<const float4*>(src) + threadIdx.x + (half * 4 + k) * kUnpackThreads);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          __stcs(reinterpret_cast<float4*>(dst) + threadIdx.x + (half * 4 + k) * kUnpackThreads,
-                 make_float4(__fmul_rn(v[k].x, uscale), __fmul_rn(v[k].y, uscale), __fmul_rn(v[k].z, uscale),
-                             __fmul_rn(v[k].w, uscale)));
-      }
-    } else {
-      for (int e = threadIdx.x; e < c.count; e += kUnpackThreads) {
-        float a;
-        if (bf16) {
-          const uint16_t hh = *reinterpret_cast<const uint16_t*>(src + (size_t)e * 2);
-          a = __uint_as_float((uint32_t)hh << 16);
+        const TfChunk c = chunks[ci];
+        // a partial chunk's bytes rounded up to 16 end inside its padding
+        const uint32_t bytes = ((uint32_t)c.count * (bf16 ? 2u : 4u) + 15u) & ~15u;
+        if (bytes) {
+          mbar_expect_tx(full0 + 8 * s, bytes);
+          bulk_load(smem_u32(stage0 + s * stage_bytes), buf + c.buf_off, bytes, full0 + 8 * s);
         } else {
-          a = *reinterpret_cast<const float*>(src + (size_t)e * 4);
+          mbar_arrive(full0 + 8 * s);   // an empty tensor
         }
-        dst[e] = __fmul_rn(a, uscale);
+      }
+      if (!ok) {
+        // the consumers' own bounded waits end their loop
+        set_error(err, DEVERR_TIMEOUT);
+        for (int j = k - NS < 0 ? 0 : k - NS; j < k; ++j) mbar_wait(full0 + 8 * (j % NS), (j / NS) & 1, kUnpackWaitNs);
       }
     }
-    c = cn;
+  } else {
+    // ---- consumers ----
+    const int t = threadIdx.x - 32;
+    int k = 0;
+    bool failed = false;
+    for (int ci = blockIdx.x; ci < nchunks; ci += gridDim.x, ++k) {
+      const int s = k % NS;
+      const TfChunk c = chunks[ci];
+      const bool got = mbar_wait(full0 + 8 * s, (k / NS) & 1, kUnpackWaitNs);
+      uint8_t* ob = out0 + (k % kUnpackOutBufs) * kUnpackOutBytes;
+      if (got) {
+        const uint8_t* st = stage0 + s * stage_bytes;
+        const int ngroups = (c.count + 3) >> 2;   // groups of 4 elements (the last may be partial)
+        // consecutive threads take consecutive groups (conflict-free
+        // shared-memory accesses)
+#pragma unroll 4
+        for (int g = t; g < ngroups; g += kUnpackConsumers) {
+          float4 f;
+          if (bf16) {
+            const uint2 h = *reinterpret_cast<const uint2*>(st + g * 8);
+            f = make_float4(__uint_as_float(h.x << 16), __uint_as_float(h.x & 0xffff0000u),
+                            __uint_as_float(h.y << 16), __uint_as_float(h.y & 0xffff0000u));
+          } else {
+            f = *reinterpret_cast<const float4*>(st + g * 16);
+          }
+          *reinterpret_cast<float4*>(ob + g * 16) =
+              make_float4(__fmul_rn(f.x, uscale), __fmul_rn(f.y, uscale), __fmul_rn(f.z, uscale),
+                          __fmul_rn(f.w, uscale));
+        }
+        fence_proxy_async_smem();
+      }
+      // the staging buffer the next chunk writes was last stored kUnpackOutBufs
+      // chunks ago: at most kUnpackOutBufs - 2 newer stores may still read
+      if (t == 0) bulk_wait_read<kUnpackOutBufs - 2>();
+      // every consumer takes the same decision: stop if any wait expired
+      failed = named_bar_or(1, kUnpackConsumers, !got);
+      if (failed) break;
+      if (t == 0) {
+        float* dst = c.tensor + c.start;
+        const int body = c.count & ~3;
+        if (body > 0) bulk_store(dst, smem_u32(ob), (uint32_t)body * 4u);
+        bulk_commit();
+        for (int e = body; e < c.count; ++e) dst[e] = reinterpret_cast<const float*>(ob)[e];
+        mbar_arrive(empty0 + 8 * s);
+      }
+    }
+    if (failed && t == 0) set_error(err, DEVERR_TIMEOUT);
+    if (t == 0) bulk_wait<0>();
   }
 }
 
@@ -141,10 +205,17 @@ cudaError_t launch_tf_pack(const TfChunk* chunks, int nchunks, int buf_bf16, flo
   return cudaGetLastError();
 }
 
+int tf_unpack_smem(int buf_bf16) {
+  return 128 + 128 + unpack_stages(buf_bf16) * kTfChunk * (buf_bf16 ? 2 : 4) + kUnpackOutBufs * kUnpackOutBytes;
+}
+
 cudaError_t launch_tf_unpack(const TfChunk* chunks, int nchunks, int buf_bf16, float uscale, const void* buf,
-                             int grid, cudaStream_t st) {
-  tf_unpack_kernel<<<grid, kUnpackThreads, 0, st>>>(chunks, nchunks, buf_bf16, uscale,
-                                                  static_cast<const uint8_t*>(buf));
+                             int grid, int32_t* err, cudaStream_t st) {
+  const int smem = tf_unpack_smem(buf_bf16);
+  cudaError_t e = cudaFuncSetAttribute(tf_unpack_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  tf_unpack_kernel<<<grid, kUnpackThreadsTma, smem, st>>>(chunks, nchunks, buf_bf16, uscale,
+                                                          static_cast<const uint8_t*>(buf), err);
   return cudaGetLastError();
 }
 

@@ -28,7 +28,9 @@ struct TfChunk {
 };
 cudaError_t launch_tf_pack(const TfChunk* chunks, int nchunks, int buf_bf16, float scale, void* buf, int grid,
                            cudaStream_t st);
+// Unpack runs one CTA per SM (grid = SM count); err receives DEVERR_TIMEOUT
+// if a wait for a chunk load expires.
 cudaError_t launch_tf_unpack(const TfChunk* chunks, int nchunks, int buf_bf16, float uscale, const void* buf,
-                             int grid, cudaStream_t st);
+                             int grid, int32_t* err, cudaStream_t st);
 
 }  // namespace fg

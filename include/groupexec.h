@@ -239,8 +239,15 @@ fg_status tf_layout_create(int32_t n, const int64_t* numel, float* const* grads,
  * fusion_buf: device, 256-byte aligned, at least total_bytes. */
 fg_status tf_pack(const tf_layout* l, float scale, void* fusion_buf, void* cuda_stream);
 
-/* One kernel: grads[i][k] = fp32(widen(buf[offset_i + k]) * uscale). */
+/* One kernel: grads[i][k] = fp32(widen(buf[offset_i + k]) * uscale).
+ * fusion_buf: device, 256-byte aligned.  The kernel waits (at most 100 ms
+ * each) for its own chunk loads; an expired wait is recorded on the device
+ * and reported by tf_sync_status. */
 fg_status tf_unpack(const tf_layout* l, float uscale, const void* fusion_buf, void* cuda_stream);
+
+/* Synchronises cuda_stream and returns FG_ETIMEOUT (clearing the record) if a
+ * tf_unpack since the last call recorded an expired wait, else FG_OK. */
+fg_status tf_sync_status(tf_layout* l, void* cuda_stream);
 
 void tf_layout_destroy(tf_layout* l);
 

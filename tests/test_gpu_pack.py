@@ -26,7 +26,7 @@ def _run(sizes, scale=0.125, uscale=1.0, buf_dtype="bf16", seed=0):
     for d in dev:
         d.fill_(float("nan"))
     tf.unpack(uscale, buf)
-    torch.cuda.synchronize()
+    tf.sync()
     back = PK.unpack(ref, sizes, uscale, buf_dtype)
     for d, r in zip(dev, back):
         np.testing.assert_array_equal(d.cpu().numpy(), r)
@@ -37,8 +37,21 @@ def test_pack_small_ragged():
     _run([1, 3, 4, 5, 127, 128, 129, 1000, 4095, 4096, 4097, 8192 + 7])
 
 
+def test_pack_empty_tensors():
+    _run([5, 0, 8192, 0, 3, 8192 * 2 + 1])
+    _run([0, 9, 0], buf_dtype="f32")
+
+
 def test_pack_config_full():
     _run(W.tensor_fusion_sizes(0))
+
+
+def test_unpack_scaled_both_buffers():
+    # whole chunks (bulk-copied) and partial ones (through registers), with a
+    # non-trivial unscale, for both buffer types
+    sizes = [8192 * 5, 8192 * 2 + 3, 17, 8192 * 40 + 8]
+    _run(sizes, scale=0.25, uscale=0.375, buf_dtype="bf16", seed=5)
+    _run(sizes, scale=0.25, uscale=0.375, buf_dtype="f32", seed=6)
 
 
 def test_pack_fp32_buffer_identity():
@@ -51,7 +64,7 @@ def test_pack_fp32_buffer_identity():
     for d in dev:
         d.zero_()
     tf.unpack(1.0, buf)
-    torch.cuda.synchronize()
+    tf.sync()
     for d, x in zip(dev, xs):
         np.testing.assert_array_equal(d.cpu().numpy(), x)
 
