@@ -421,10 +421,11 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
   p.nkb = (int32_t)((cg.K + kGemmK - 1) / kGemmK);
   p.a_mn = a_mn;
   p.b_mn = b_mn;
-  // two 64-wide column groups per copy when the contiguous extent splits
-  // into whole groups (a 3-D view would otherwise wrap into the next row)
-  p.a_3d = a_mn && cg.M % 64 == 0;
-  p.b_3d = b_mn && cg.N % 64 == 0;
+  // one copy per operand half and ring slot through a 3-D view when the
+  // contiguous extent splits into whole 64-element groups (the view would
+  // otherwise wrap into the next row instead of reading zeros)
+  p.a_3d = (a_mn ? cg.M : cg.K) % 64 == 0;
+  p.b_3d = (b_mn ? cg.N : cg.K) % 64 == 0;
   p.wait_limit_ns = o.wait_limit_ns;
   p.epi_stage_bytes = cg.stage_bytes;
   p.epi_tx_bytes = tx;
@@ -440,14 +441,13 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
   // operand ring and epilogue-leaf ring depths that fit 227 KB, in order of
   // preference: long K needs a deep operand ring (its feed is latency bound),
   // short K a deep leaf ring (the epilogue streams the leaves from HBM).  A
-  // CTA stages its 128 rows of A and its half of B's columns per K block.
+  // ring slot holds two K blocks of the CTA's 128 rows of A and of its half of
+  // B's columns.
   const int limit = 227 * 1024 - 256, fixed = 2048 + (p.inplace_off >= 0 ? 0 : 2 * kGemmM * kGemmChunk * 4);
-  const int stage = (kGemmM + kGemmN / kGemmCluster) * kGemmK * 2;
+  const int stage = kGemmKB * (kGemmM + kGemmN / kGemmCluster) * kGemmK * 2;
   int ns = 0, ne = 0;
-  static const std::vector<std::pair<int, int>> prefs_short = {{4, 6}, {4, 5}, {4, 4}, {3, 4}, {3, 3},
-                                                               {2, 4}, {2, 3}, {3, 2}, {2, 2}};
-  static const std::vector<std::pair<int, int>> prefs_long = {{6, 2}, {5, 3}, {5, 2}, {4, 3}, {4, 2},
-                                                              {3, 3}, {3, 2}, {2, 4}, {2, 3}, {2, 2}};
+  static const std::vector<std::pair<int, int>> prefs_short = {{2, 6}, {2, 5}, {2, 4}, {2, 3}, {2, 2}};
+  static const std::vector<std::pair<int, int>> prefs_long = {{3, 2}, {2, 4}, {2, 3}, {2, 2}};
   const bool short_k = p.nkb <= 16 && cg.stage_bytes > 0;
   for (const auto& q : short_k ? prefs_short : prefs_long) {
     if (!ns && fixed + q.first * stage + q.second * cg.stage_bytes <= limit) {
@@ -580,33 +580,29 @@ fg_status launch_gemm(GroupExec& ge, void* const* ptrs, void* stream) {
     if (fg_status st = check_ptr(ptrs[cg.out_value], cg.out_value)) return st;
     {
       // A: [K, M] (M contiguous) when transposed, else [M, K]
-      // (MN-major with whole 64-wide groups: [M/64, K, 64], one box of two
-      // groups per copy)
+      // 3-D views (one copy per operand half and ring slot):
+      //   MN-major [extent/64][K][64], box 64 x 128 K rows x 2 groups;
+      //   K-major  [K/64][rows][64],   box 64 x 128 rows x 2 K blocks.
+      // Otherwise 2-D boxes: MN-major 64 x 64, K-major 64 x 128 rows.
       uint64_t dims[3], strides[2];
       uint32_t box[3];
-      int rank = 2;
-      if (gp.a_3d) {
-        dims[0] = 64; dims[1] = cg.K; dims[2] = cg.M / 64; strides[0] = cg.M * 2; strides[1] = 128;
-        box[0] = 64; box[1] = 64; box[2] = 2; rank = 3;
-      } else if (gp.a_mn) {
-        dims[0] = cg.M; dims[1] = cg.K; strides[0] = cg.M * 2; box[0] = 64; box[1] = 64;
-      } else {
-        dims[0] = cg.K; dims[1] = cg.M; strides[0] = cg.K * 2; box[0] = 64; box[1] = kGemmM;
-      }
+      auto view = [&](bool mn, bool v3, int64_t rows) {
+        const int64_t inner = mn ? rows : cg.K, outer = mn ? cg.K : rows;
+        if (v3) {
+          dims[0] = 64; dims[1] = outer; dims[2] = inner / 64; strides[0] = inner * 2; strides[1] = 128;
+          box[0] = 64; box[1] = 128; box[2] = 2;
+          return 3;
+        }
+        dims[0] = inner; dims[1] = outer; strides[0] = inner * 2; box[0] = 64; box[1] = mn ? 64 : 128;
+        return 2;
+      };
+      int rank = view(gp.a_mn, gp.a_3d, cg.M);
       if (fg_status st = encode(&gp.mapA, ptrs[cg.mm_a], rank, dims, strides, box, true,
                                 CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
         return st;
-      // B: [K, N] (N contiguous), or [N, K] when transposed
-      rank = 2;
-      if (gp.b_3d) {
-        dims[0] = 64; dims[1] = cg.K; dims[2] = cg.N / 64; strides[0] = cg.N * 2; strides[1] = 128;
-        box[0] = 64; box[1] = 64; box[2] = 2; rank = 3;
-      } else if (gp.b_mn) {
-        dims[0] = cg.N; dims[1] = cg.K; strides[0] = cg.N * 2; box[0] = 64; box[1] = 64;
-      } else {
-        // each CTA of a pair stages its half of the B tile's columns
-        dims[0] = cg.K; dims[1] = cg.N; strides[0] = cg.K * 2; box[0] = 64; box[1] = kGemmN / kGemmCluster;
-      }
+      // B: [K, N] (N contiguous), or [N, K] when transposed; each CTA of a
+      // pair stages its half of the tile's columns
+      rank = view(gp.b_mn, gp.b_3d, cg.N);
       if (fg_status st = encode(&gp.mapB, ptrs[cg.mm_b], rank, dims, strides, box, true,
                                 CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
         return st;

@@ -142,6 +142,7 @@ struct GroupParams {
 // GEMM + epilogue kernel: 128 x 256 accumulator tiles in TMEM, K in blocks
 // of 64, the epilogue in 128 x 32 column chunks.
 constexpr int kGemmM = 128, kGemmN = 256, kGemmK = 64, kGemmChunk = 32;
+constexpr int kGemmKB = 2;             // K blocks per operand ring slot
 constexpr int kGemmWarps = 7;          // TMA, MMA, epilogue loads, 4 epilogue warps
 constexpr int kGemmCluster = 2;        // CTAs of a pair issuing 2-SM MMAs on one 256-row tile
 
@@ -157,8 +158,9 @@ struct GemmParams {
   int32_t M, N, K;
   int32_t ntm, ntn, ntiles, nkb;
   int32_t a_mn, b_mn;                  // 1: operand stored MN-major (M or N contiguous)
-  int32_t a_3d, b_3d;                  // 1: an MN-major operand's 64-wide column groups come
-                                       //    two at a time through a 3-D map (one copy per half tile)
+  int32_t a_3d, b_3d;                  // 1: the operand's half tile of a ring slot comes in one
+                                       //    copy through a 3-D map (MN-major: [groups][K][64],
+                                       //    K-major: [K blocks][rows][64])
   int32_t nstages;                     // operand ring depth
   int32_t epi_stage_bytes, epi_tx_bytes, n_epi_bufs;
   int32_t inplace_off;                 // >= 0: the result overwrites this IDENT leaf's chunk (no out buffers)

@@ -7,7 +7,8 @@
 //
 // Persistent: CTAs run in pairs (a 2-CTA cluster) on the SMs of one TPC, and
 // a pair walks 256 x 256 output tiles.  Each CTA stages half of the tile's A
-// rows and half of its B columns (32 KB per 64-deep K block); the even CTA
+// rows and half of its B columns, two 64-deep K blocks (64 KB) per ring slot,
+// each operand half in one TMA copy where the layout allows; the even CTA
 // issues 2-SM tcgen05.mma instructions (cta_group::2) that read both CTAs'
 // halves and leave each CTA's 128 accumulator rows in its own TMEM.  Warp
 // roles, in each CTA:
@@ -30,8 +31,7 @@
 namespace fg {
 
 constexpr int kGemmThreads = kGemmWarps * 32;
-constexpr int kGemmABytes = kGemmM * kGemmK * 2;    // 16 KB: this CTA's 128 rows of A
-constexpr int kGemmBBytes = kGemmN * kGemmK * 2;    // 32 KB: the whole B block of a tile
+constexpr int kGemmABytes = kGemmM * kGemmK * 2;    // 16 KB: this CTA's 128 rows of one A block
 constexpr int kGemmOutBytes = kGemmM * kGemmChunk * 4;   // 16 KB
 constexpr int kGemmChunks = kGemmN / kGemmChunk;    // 8
 
@@ -150,13 +150,14 @@ __device__ __forceinline__ bool gemm_wait(uint32_t bar, uint32_t parity, int64_t
   return true;
 }
 
-// CL = 1: one CTA per 128 x 256 tile (cta_group::1).  CL = 2: a CTA pair per
-// 256 x 256 tile (cta_group::2), each CTA holding half of B.
+// CL = 2: a CTA pair per 256 x 256 tile (cta_group::2), each CTA holding
+// half of A's rows and half of B's columns.
 template <class Epi, int CL>
 __device__ __forceinline__ void gemm_body(const GemmParams& P) {
-  static_assert(CL == 1 || CL == 2, "CTA group of one or two");
-  constexpr int kStageBytes = kGemmABytes + kGemmBBytes / CL;   // per CTA
-  constexpr int kBCols = kGemmN / CL;                            // B columns staged per CTA
+  static_assert(CL == 2, "the kernel runs CTA pairs");
+  constexpr int kBCols = kGemmN / CL;                              // B columns staged per CTA
+  constexpr int kHalfA = kGemmKB * kGemmABytes;                    // 32 KB: 128 rows x 2 K blocks
+  constexpr int kStageBytes = kHalfA + kGemmKB * kBCols * kGemmK * 2;   // 64 KB per CTA
   extern __shared__ uint8_t smem_raw[];
   __shared__ int abort_flag;
   __shared__ uint32_t tmem_slot;
@@ -171,8 +172,9 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   uint8_t* obuf = ebuf + NE * P.epi_stage_bytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool staged = P.epi_tx_bytes > 0;
+  const int nslots = (P.nkb + kGemmKB - 1) / kGemmKB;             // ring slots per tile
 
-  const uint32_t rank = CL > 1 ? cluster_ctarank() : 0;
+  const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
   // tile sequence: units of CL vertically adjacent 128-row tiles
   const int ncl = gridDim.x / CL, cl = blockIdx.x / CL;
@@ -201,7 +203,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   if (warp == 1) tmem_alloc<CL>(smem_u32(&tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
-  if (CL > 1) cluster_sync();   // the peer's barriers are initialised before any remote arrival
+  cluster_sync();   // the peer's barriers are initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   const int64_t limit = P.wait_limit_ns;
@@ -209,6 +211,9 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
 
   if (warp == 0) {
     // ---- operand producer ----
+    // Ring slot layouts (per CTA), each 128-byte row 128B-swizzled:
+    //   K-major operand:  [K block][128 rows][64 K]        (16 KB per K block)
+    //   MN-major operand: [64-wide group][128 K rows][64]  (16 KB per group)
     if (lane == 0 && !P.inject) {
       tma_prefetch(&P.mapA);
       tma_prefetch(&P.mapB);
@@ -217,57 +222,51 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       for (int u = cl; u < nunits && ok; u += ncl) {
         int m0, n0;
         tile_of(u, m0, n0);
-        for (int kb = 0; kb < P.nkb; ++kb, ++it) {
+        const int nb = n0 + (int)rank * kBCols;
+        for (int sl = 0; sl < nslots; ++sl, ++it) {
           const int s = it % NS;
           if (it >= NS && !gemm_wait(empty0 + 8 * s, ((it / NS) & 1) ^ 1, limit, &abort_flag)) {
             ok = false;
             break;
           }
-          const uint32_t a = smem_u32(opnd + s * kStageBytes), b = a + kGemmABytes;
-          const int k0 = kb * kGemmK;
-          const int nb = n0 + (int)rank * kBCols;
-          if (CL == 1) {
-            const uint32_t bar = full0 + 8 * s;
-            mbar_expect_tx(bar, kStageBytes);
-            if (P.a_3d) {
-              tma_load_3d(a, &P.mapA, 0, k0, m0 / 64, bar);
-            } else if (P.a_mn) {
-              tma_load_2d(a, &P.mapA, m0, k0, bar);
-              tma_load_2d(a + 8192, &P.mapA, m0 + 64, k0, bar);
-            } else {
-              tma_load_2d(a, &P.mapA, k0, m0, bar);
-            }
-            if (P.b_3d) {
-#pragma unroll
-              for (int i = 0; i < kBCols / 128; ++i) tma_load_3d(b + 16384 * i, &P.mapB, 0, k0, nb / 64 + 2 * i, bar);
-            } else if (P.b_mn) {
-#pragma unroll
-              for (int i = 0; i < kBCols / 64; ++i) tma_load_2d(b + 8192 * i, &P.mapB, nb + 64 * i, k0, bar);
-            } else {
-#pragma unroll
-              for (int i = 0; i < kBCols / 128; ++i) tma_load_2d(b + 16384 * i, &P.mapB, k0, nb + 128 * i, bar);
-            }
-          } else {
-            // both CTAs' halves are counted on the even CTA's barrier, which
-            // the even CTA alone arms with the whole block's bytes
-            const uint32_t cbar = cluster_addr(full0 + 8 * s, 0);
-            if (leader) mbar_expect_tx(full0 + 8 * s, CL * kStageBytes);
+          const uint32_t a = smem_u32(opnd + s * kStageBytes), b = a + kHalfA;
+          const int k0 = sl * kGemmKB * kGemmK;
+          // both CTAs' halves are counted on the even CTA's barrier, which
+          // the even CTA alone arms with the whole slot's bytes (blocks past
+          // K arrive zero-filled and count in full)
+          const uint32_t cbar = cluster_addr(full0 + 8 * s, 0);
+          if (leader) mbar_expect_tx(full0 + 8 * s, CL * kStageBytes);
+          if (P.a_mn) {
             if (P.a_3d) {
               tma_load_3d_pair(a, &P.mapA, 0, k0, m0 / 64, cbar);
-            } else if (P.a_mn) {
-              tma_load_2d_pair(a, &P.mapA, m0, k0, cbar);
-              tma_load_2d_pair(a + 8192, &P.mapA, m0 + 64, k0, cbar);
             } else {
-              tma_load_2d_pair(a, &P.mapA, k0, m0, cbar);
+#pragma unroll
+              for (int g = 0; g < 2; ++g)
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                  tma_load_2d_pair(a + g * 16384 + j * 8192, &P.mapA, m0 + 64 * g, k0 + 64 * j, cbar);
             }
+          } else if (P.a_3d) {
+            tma_load_3d_pair(a, &P.mapA, 0, m0, k0 / 64, cbar);
+          } else {
+#pragma unroll
+            for (int j = 0; j < kGemmKB; ++j) tma_load_2d_pair(a + j * 16384, &P.mapA, k0 + 64 * j, m0, cbar);
+          }
+          if (P.b_mn) {
             if (P.b_3d) {
               tma_load_3d_pair(b, &P.mapB, 0, k0, nb / 64, cbar);
-            } else if (P.b_mn) {
-#pragma unroll
-              for (int i = 0; i < kBCols / 64; ++i) tma_load_2d_pair(b + 8192 * i, &P.mapB, nb + 64 * i, k0, cbar);
             } else {
-              tma_load_2d_pair(b, &P.mapB, k0, nb, cbar);
+#pragma unroll
+              for (int g = 0; g < 2; ++g)
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                  tma_load_2d_pair(b + g * 16384 + j * 8192, &P.mapB, nb + 64 * g, k0 + 64 * j, cbar);
             }
+          } else if (P.b_3d) {
+            tma_load_3d_pair(b, &P.mapB, 0, nb, k0 / 64, cbar);
+          } else {
+#pragma unroll
+            for (int j = 0; j < kGemmKB; ++j) tma_load_2d_pair(b + j * 16384, &P.mapB, k0 + 64 * j, nb, cbar);
           }
         }
       }
@@ -285,8 +284,11 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
     // ---- MMA issuer (the even CTA of a pair) ----
     if (lane == 0 && leader) {
       const uint32_t idesc = idesc_bf16_f32(CL * kGemmM, kGemmN, P.a_mn, P.b_mn);
-      const uint32_t a_lbo = P.a_mn ? 8192 : 16, b_lbo = P.b_mn ? 8192 : 16;
-      const uint32_t a_step = P.a_mn ? 2048 : 32, b_step = P.b_mn ? 2048 : 32;
+      // MN-major: atoms of 64 (M or N) x 8 K rows, 64-wide groups 16 KB
+      // apart; K-major: atoms of 8 rows x 64 K, K blocks 16 KB apart
+      const uint32_t a_lbo = P.a_mn ? 16384 : 16, b_lbo = P.b_mn ? 16384 : 16;
+      const uint32_t a_blk = P.a_mn ? 8192 : 16384, b_blk = P.b_mn ? 8192 : 16384;   // next K block
+      const uint32_t a_step = P.a_mn ? 2048 : 32, b_step = P.b_mn ? 2048 : 32;         // next 16 of K
       int it = 0, i = 0;
       bool ok = true;
       for (int u = cl; u < nunits && ok; u += ncl, ++i) {
@@ -306,21 +308,26 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         }
         tc_fence_after();
         const uint32_t d = tmem + b * kGemmN;
-        for (int kb = 0; kb < P.nkb; ++kb, ++it) {
+        for (int sl = 0; sl < nslots; ++sl, ++it) {
           const int s = it % NS;
           if (!gemm_wait(full0 + 8 * s, (it / NS) & 1, limit, &abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a = smem_u32(opnd + s * kStageBytes), bb = a + kGemmABytes;
+          const uint32_t a = smem_u32(opnd + s * kStageBytes), bb = a + kHalfA;
 #pragma unroll
-          for (int kk = 0; kk < kGemmK / 16; ++kk) {
-            const uint64_t ad = smem_desc_sw128(a + kk * a_step, a_lbo, 1024);
-            const uint64_t bd = smem_desc_sw128(bb + kk * b_step, b_lbo, 1024);
-            tc_mma_bf16<CL>(d, ad, bd, idesc, (kb | kk) != 0);
+          for (int j = 0; j < kGemmKB; ++j) {
+            const int kb = sl * kGemmKB + j;
+            if (kb >= P.nkb) break;
+#pragma unroll
+            for (int kk = 0; kk < kGemmK / 16; ++kk) {
+              const uint64_t ad = smem_desc_sw128(a + j * a_blk + kk * a_step, a_lbo, 1024);
+              const uint64_t bd = smem_desc_sw128(bb + j * b_blk + kk * b_step, b_lbo, 1024);
+              tc_mma_bf16<CL>(d, ad, bd, idesc, (kb | kk) != 0);
+            }
           }
-          tc_commit<CL>(empty0 + 8 * s);   // both CTAs may refill the stage
+          tc_commit<CL>(empty0 + 8 * s);   // both CTAs may refill the slot
         }
         if (!ok) break;
         tc_commit<CL>(tfull0 + 8 * b);
@@ -430,8 +437,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if (CL == 1) mbar_arrive(tempty0 + 8 * b);
-        else mbar_arrive_cluster(cluster_addr(tempty0 + 8 * b, 0));
+        mbar_arrive_cluster(cluster_addr(tempty0 + 8 * b, 0));
       }
     }
     if (dead) {
@@ -444,7 +450,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   __syncthreads();
   // no CTA leaves while its peer may still write to its shared memory or
   // issue MMAs into its TMEM
-  if (CL > 1) cluster_sync();
+  cluster_sync();
   tc_fence_after();
   if (warp == 1) tmem_dealloc<CL>(tmem, 512);
 }
