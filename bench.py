@@ -434,6 +434,25 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
             "GBps": alg / (gmed * 1e-3) / 1e9,
             "note": "launch-latency bound (0.53 MB); L2 flushed; graph_* = CUDA-graph replay"}
 
+    # the same chain scaled to X, Y [65536, 1024] (512 MiB): bandwidth-bound,
+    # so its roofline fraction means something; inputs exceed L2, no flush
+    for epi in (False, True):
+        sp = W.rnnlm_chain(65536, 1024)
+        p = graph_from_spec(sp).build(allow_reduce_epilogue=epi)
+        gen = torch.Generator(device="cuda").manual_seed(0)
+        e = {v.vid: torch.empty(v.shape, device="cuda").uniform_(-1.0, 1.0, generator=gen)
+             for v in sp.values if v.is_input}
+        for v in sp.ops:
+            e[v.vid] = torch.empty(v.shape, device="cuda")
+        med, mn = timed(run_plan(p, sp, e, True), flush=False)
+        medu, _ = timed(run_plan(p, sp, e, False), flush=False)
+        alg = sum(gi.alg_bytes for gi in p.groups)
+        rows["rnnlm_chain_65536x1024" + ("_1group" if epi else "_2groups")] = {
+            "fused_us": med * 1e3, "fused_min_us": mn * 1e3, "groups": p.n_groups, "unfused_us": medu * 1e3,
+            "speedup_vs_unfused": medu / med, "alg_bytes": alg, "GBps": alg / (med * 1e-3) / 1e9,
+            "frac_of_hbm": alg / (med * 1e-3) / 1e9 / hbm}
+        del e
+
     # tensor-fusion pack / unpack
     from group_execution_gb300 import TensorFusion
     sizes = W.tensor_fusion_sizes(0)

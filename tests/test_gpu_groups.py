@@ -73,6 +73,13 @@ def test_rnnlm_chain(epi):
     assert plan.n_groups == (1 if epi else 2)
 
 
+@pytest.mark.parametrize("epi", [False, True])
+def test_rnnlm_chain_scaled(epi):
+    # the bandwidth-bound variant of the chain: X, Y [65536, 1024] (512 MiB)
+    plan, env, ref, _ = _check(W.rnnlm_chain(65536, 1024), unfused=False, allow_reduce_epilogue=epi, flags=0)
+    assert plan.n_groups == (1 if epi else 2)
+
+
 @pytest.mark.parametrize("shape", [(64, 1024), (100, 200), (8192, 4096), (4096, 8192), (3, 2052)])
 def test_row_reductions(shape):
     R, C = shape
