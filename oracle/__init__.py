@@ -22,10 +22,13 @@ out from the passages they cite:
                    DisCo, Introduction, on what op fusion changes).
 * ``pack``      -- tensor-fusion layout, bf16 round-to-nearest-even, pack and
                    unpack (DisCo, Introduction, on tensor fusion).
+* ``buckets``   -- AllReduce buckets: threshold fusion (DisCo, Related Work,
+                   on Horovod and XLA) and neighbour combination (DisCo,
+                   Strategy Maker, method (iii)).
 
 Parity status: every function here is pinned by tests under ``tests/``
 (``-m "not gpu"``) against brute force, closed forms, worked examples from the
 pages or library routines, except the long random-DAG numerics, which only the
 oracle itself defines ("parity unpinned" beyond per-op pins).
 """
-from . import kinds, postdom, partition, execute, pack  # noqa: F401
+from . import kinds, postdom, partition, execute, pack, buckets  # noqa: F401
