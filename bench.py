@@ -470,6 +470,28 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
                              "unpack_frac": nbytes / (mu * 1e-3) / 1e9 / hbm, "launches_each": 1,
                              "per_tensor_unfused_launches": 2 * len(sizes)}
 
+    # the same gradients cut into AllReduce buckets by an 8 MiB fusion
+    # threshold, packed and unpacked one launch per bucket (what an overlapped
+    # exchange issues as each bucket's gradients become ready)
+    from group_execution_gb300 import plan_threshold
+    bounds = plan_threshold(list(sizes), 8 << 20)
+    nb = len(bounds) - 1
+
+    def each_bucket(fn, s):
+        return lambda: [fn(bounds[k], bounds[k + 1] - bounds[k], s, buf) for k in range(nb)]
+
+    bp, _ = timed(each_bucket(tf.pack_range, 0.125), flush=False, inner=10)
+    bu, _ = timed(each_bucket(tf.unpack_range, 1.0), flush=False, inner=10)
+    gp, _ = timed(graphed(each_bucket(tf.pack_range, 0.125)), flush=False, inner=10)
+    gu, _ = timed(graphed(each_bucket(tf.unpack_range, 1.0)), flush=False, inner=10)
+    rows["tensor_fusion_buckets_8MiB"] = {
+        "buckets": nb, "launches_each": nb, "pack_us": bp * 1e3, "unpack_us": bu * 1e3,
+        "graph_pack_us": gp * 1e3, "graph_pack_GBps": nbytes / (gp * 1e-3) / 1e9,
+        "graph_pack_frac": nbytes / (gp * 1e-3) / 1e9 / hbm, "graph_unpack_us": gu * 1e3,
+        "graph_unpack_GBps": nbytes / (gu * 1e-3) / 1e9, "graph_unpack_frac": nbytes / (gu * 1e-3) / 1e9 / hbm,
+        "bucket_bytes": [e - s for s, e in tf.bucket_ranges(bounds)],
+        "note": "pack_us/unpack_us: one host launch per bucket; graph_*: the launches replayed from a CUDA graph"}
+
     # sufficient-factor gradient + update: one tcgen05 GEMM-epilogue group
     for B, label in ((512, "sf_update_K512"), (4096, "sf_update_K4096_compute_bound_variant")):
         sp = W.sf_update(B, 4096, 4096)

@@ -18,7 +18,7 @@ import ctypes as C
 from . import _lib
 from ._lib import FgError, OPCODES, EXEC_KINDS, FG_F32, FG_BF16  # noqa: F401
 
-__all__ = ["Graph", "Plan", "TensorFusion", "FgError", "OPCODES", "graph_from_spec"]
+__all__ = ["Graph", "Plan", "TensorFusion", "FgError", "OPCODES", "graph_from_spec", "plan_threshold", "merge_buckets"]
 
 
 def _i32a(xs):
@@ -206,3 +206,40 @@ class TensorFusion:
         """Waits for the stream; raises FgError (FG_ETIMEOUT) if an unpack
         recorded an expired wait."""
         _lib.check(self.lib.tf_sync_status(self.h, _stream_handle(stream)))
+
+    def pack_range(self, first, count, scale, buf, stream=None):
+        """Pack tensors first .. first+count-1 only (e.g. one bucket)."""
+        _lib.check(self.lib.tf_pack_range(self.h, first, count, C.c_float(scale), C.c_void_p(buf.data_ptr()),
+                                          _stream_handle(stream)))
+
+    def unpack_range(self, first, count, uscale, buf, stream=None):
+        _lib.check(self.lib.tf_unpack_range(self.h, first, count, C.c_float(uscale), C.c_void_p(buf.data_ptr()),
+                                            _stream_handle(stream)))
+
+    def bucket_ranges(self, bounds):
+        """Byte range [start, end) of every bucket in the fusion buffer."""
+        starts = [self.offsets[b] if b < len(self.offsets) else self.total_bytes for b in bounds]
+        return [(starts[k], starts[k + 1]) for k in range(len(bounds) - 1)]
+
+
+def plan_threshold(numels, threshold_bytes, buf_dtype="bf16", align=256):
+    """Threshold fusion of gradient tensors (in production order) into
+    AllReduce buckets; returns the boundaries: bucket b holds tensors
+    bounds[b] .. bounds[b+1]-1.  Host only."""
+    lib = _lib.load()
+    n = len(numels)
+    arr = (C.c_int64 * max(n, 1))(*[int(x) for x in numels])
+    bounds = (C.c_int32 * (n + 1))()
+    nb = C.c_int32()
+    _lib.check(lib.tf_plan_threshold(n, arr, FG_BF16 if buf_dtype == "bf16" else FG_F32, align, threshold_bytes,
+                                     bounds, C.byref(nb)))
+    return list(bounds[:nb.value + 1])
+
+
+def merge_buckets(bounds, j):
+    """Bucket j combined with its neighbour j+1."""
+    lib = _lib.load()
+    arr = (C.c_int32 * len(bounds))(*bounds)
+    nb = C.c_int32(len(bounds) - 1)
+    _lib.check(lib.tf_buckets_merge(arr, C.byref(nb), j))
+    return list(arr[:nb.value + 1])

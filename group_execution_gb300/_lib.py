@@ -69,6 +69,10 @@ SIGNATURES = {
     "tf_pack": (_I32, [_P, _F, _P, _P]),
     "tf_unpack": (_I32, [_P, _F, _P, _P]),
     "tf_sync_status": (_I32, [_P, _P]),
+    "tf_plan_threshold": (_I32, [_I32, _P, _I32, _I64, _I64, _P, _P]),
+    "tf_buckets_merge": (_I32, [_P, _P, _I32]),
+    "tf_pack_range": (_I32, [_P, _I32, _I32, _F, _P, _P]),
+    "tf_unpack_range": (_I32, [_P, _I32, _I32, _F, _P, _P]),
     "tf_layout_destroy": (None, [_P]),
 }
 

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <memory>
 #include <mutex>
@@ -112,6 +113,7 @@ struct tf_layout {
   TfChunk* d_chunks = nullptr;       // chunk table, followed by the device error word
   int32_t* d_err = nullptr;
   int nchunks = 0;
+  std::vector<int32_t> chunk_begin;  // first chunk of every tensor, [n + 1]
 };
 
 // ---------------------------------------------------------------------------
@@ -357,10 +359,24 @@ void prepare_group(GroupExec& ge, const BuildOpts& o, int nsm) {
       tps = std::min(p.ntc, unit);
     } else {
       // whole rows per unit when there is a strip for every SM (no combine
-      // across CTAs); otherwise split the columns just enough to occupy
-      // every SM, each unit long enough to amortise its combine step
-      nsplit = p.ntr >= nsm ? 1 : std::max(1, std::min((nsm + p.ntr - 1) / p.ntr, std::max(1, p.ntc / 16)));
-      tps = (p.ntc + nsplit - 1) / nsplit;
+      // across CTAs: measured faster than any split there); otherwise the
+      // fewest column splits per strip that spread the units evenly over the
+      // SMs (an SM's share within 5 % of the busiest one's), each unit at
+      // least 4 tiles long to amortise its combine step
+      tps = p.ntc;
+      double best = p.ntr >= nsm ? 2.0 : 0.0;
+      for (int sp = 1; sp <= 64 && best < 1.5; ++sp) {
+        const int t = (p.ntc + sp - 1) / sp;
+        if (t < 4 && sp > 1) break;
+        const int64_t units = (int64_t)p.ntr * ((p.ntc + t - 1) / t);
+        const double per_sm = (double)units / nsm;
+        const double balance = per_sm / std::ceil(per_sm);
+        if (balance > best + 1e-9) {
+          best = balance;
+          tps = t;
+        }
+        if (balance >= 0.95) break;
+      }
     }
     nsplit = (p.ntc + tps - 1) / tps;
     p.nsplit = nsplit;
@@ -862,6 +878,7 @@ fg_status tf_layout_create(int32_t n, const int64_t* numel, float* const* grads,
   l->total = cur;
   std::vector<TfChunk> ch;
   for (int i = 0; i < n; ++i) {
+    l->chunk_begin.push_back((int32_t)ch.size());
     const int64_t end_bytes = l->offsets[i] + numel[i] * eb;
     const int64_t next = i + 1 < n ? l->offsets[i + 1] : l->total;
     int64_t s = 0;
@@ -877,6 +894,7 @@ fg_status tf_layout_create(int32_t n, const int64_t* numel, float* const* grads,
     } while (s < numel[i]);
   }
   l->nchunks = (int)ch.size();
+  l->chunk_begin.push_back(l->nchunks);
   if (!device_present(nullptr)) return err(FG_ECUDA, "no CUDA device");
   const size_t table = round_up((int64_t)(sizeof(TfChunk) * ch.size()), 256);
   cudaError_t e = cudaMalloc(&l->d_chunks, table + 256);
@@ -894,29 +912,84 @@ fg_status tf_layout_create(int32_t n, const int64_t* numel, float* const* grads,
   return FG_OK;
 }
 
-static int tf_grid(const tf_layout* l) {
-  int nsm = 148;
-  device_present(&nsm);
-  return std::max(1, std::min(l->nchunks, nsm * 8));
+// Chunks [c0, c1) of the layout's table: tensors first .. first+count-1.
+static fg_status tf_chunk_range(const tf_layout* l, int32_t first, int32_t count, int* c0, int* c1) {
+  if (first < 0 || count < 0 || first > l->n || count > l->n - first) return err(FG_EINVAL, "tensor range out of bounds");
+  *c0 = l->chunk_begin[first];
+  *c1 = l->chunk_begin[first + count];
+  return FG_OK;
 }
 
-fg_status tf_pack(const tf_layout* l, float scale, void* buf, void* stream) {
+fg_status tf_pack_range(const tf_layout* l, int32_t first, int32_t count, float scale, void* buf, void* stream) {
   if (!l || !buf) return err(FG_EINVAL, "null argument");
   if (reinterpret_cast<uintptr_t>(buf) % 256) return err(FG_EINVAL, "fusion buffer must be 256-byte aligned");
-  cudaError_t e = launch_tf_pack(l->d_chunks, l->nchunks, l->buf_bf16, scale, buf, tf_grid(l),
+  int c0, c1;
+  if (fg_status st = tf_chunk_range(l, first, count, &c0, &c1)) return st;
+  if (c1 == c0) return FG_OK;
+  int nsm = 148;
+  device_present(&nsm);
+  cudaError_t e = launch_tf_pack(l->d_chunks + c0, c1 - c0, l->buf_bf16, scale, buf, std::min(c1 - c0, nsm * 8),
                                  static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FG_OK : cuda_err(e, "tf_pack launch");
 }
 
-fg_status tf_unpack(const tf_layout* l, float uscale, const void* buf, void* stream) {
+fg_status tf_unpack_range(const tf_layout* l, int32_t first, int32_t count, float uscale, const void* buf,
+                          void* stream) {
   if (!l || !buf) return err(FG_EINVAL, "null argument");
   if (reinterpret_cast<uintptr_t>(buf) % 256) return err(FG_EINVAL, "fusion buffer must be 256-byte aligned");
+  int c0, c1;
+  if (fg_status st = tf_chunk_range(l, first, count, &c0, &c1)) return st;
+  if (c1 == c0) return FG_OK;
   int nsm = 148;
   device_present(&nsm);
-  cudaError_t e = launch_tf_unpack(l->d_chunks, l->nchunks, l->buf_bf16, uscale, buf,
-                                   std::max(1, std::min(l->nchunks, nsm)), l->d_err,
-                                   static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_tf_unpack(l->d_chunks + c0, c1 - c0, l->buf_bf16, uscale, buf, std::min(c1 - c0, nsm),
+                                   l->d_err, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FG_OK : cuda_err(e, "tf_unpack launch");
+}
+
+fg_status tf_pack(const tf_layout* l, float scale, void* buf, void* stream) {
+  if (!l) return err(FG_EINVAL, "null argument");
+  return tf_pack_range(l, 0, l->n, scale, buf, stream);
+}
+
+fg_status tf_unpack(const tf_layout* l, float uscale, const void* buf, void* stream) {
+  if (!l) return err(FG_EINVAL, "null argument");
+  return tf_unpack_range(l, 0, l->n, uscale, buf, stream);
+}
+
+// Threshold fusion in production order: a tensor joins the open bucket while
+// the bucket's padded bytes stay within the threshold, otherwise it opens
+// the next one (a tensor above the threshold sits alone).
+fg_status tf_plan_threshold(int32_t n, const int64_t* numel, fg_dtype buf_dtype, int64_t align,
+                            int64_t threshold, int32_t* bounds, int32_t* n_buckets) {
+  if (n < 0 || (n > 0 && !numel) || !bounds || !n_buckets) return err(FG_EINVAL, "null argument");
+  if (buf_dtype != FG_BF16 && buf_dtype != FG_F32) return err(FG_EINVAL, "unknown buffer dtype");
+  if (align < 16 || (align & (align - 1))) return err(FG_EINVAL, "align_bytes must be a power of two >= 16");
+  if (threshold < 0) return err(FG_EINVAL, "negative threshold");
+  const int64_t eb = buf_dtype == FG_BF16 ? 2 : 4;
+  int32_t nb = 0;
+  bounds[0] = 0;
+  int64_t cur = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    if (numel[i] < 0) return err(FG_ESHAPE, "negative element count");
+    const int64_t sz = round_up(numel[i] * eb, align);
+    if (i > bounds[nb] && cur + sz > threshold) {
+      bounds[++nb] = i;
+      cur = 0;
+    }
+    cur += sz;
+  }
+  if (n > 0) bounds[++nb] = n;
+  *n_buckets = nb;
+  return FG_OK;
+}
+
+fg_status tf_buckets_merge(int32_t* bounds, int32_t* n_buckets, int32_t j) {
+  if (!bounds || !n_buckets) return err(FG_EINVAL, "null argument");
+  if (j < 0 || j + 1 >= *n_buckets) return err(FG_EINVAL, "bucket has no successor");
+  for (int32_t k = j + 1; k < *n_buckets; ++k) bounds[k] = bounds[k + 1];
+  --*n_buckets;
+  return FG_OK;
 }
 
 fg_status tf_sync_status(tf_layout* l, void* stream) {

@@ -15,6 +15,9 @@
 // chunk leaves as one bulk store of its 16-byte multiple plus at most three
 // plain stores.
 #include <cuda_bf16.h>
+
+#include <algorithm>
+#include <atomic>
 #include <cuda_runtime.h>
 
 #include "fg_device.cuh"
@@ -212,8 +215,19 @@ int tf_unpack_smem(int buf_bf16) {
 cudaError_t launch_tf_unpack(const TfChunk* chunks, int nchunks, int buf_bf16, float uscale, const void* buf,
                              int grid, int32_t* err, cudaStream_t st) {
   const int smem = tf_unpack_smem(buf_bf16);
-  cudaError_t e = cudaFuncSetAttribute(tf_unpack_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // the shared-memory opt-in is set once per device (the largest size either
+  // buffer type needs), not on every launch
+  static std::atomic<uint64_t> opted{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
+  if (!bit || !(opted.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(tf_unpack_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             std::max(tf_unpack_smem(0), tf_unpack_smem(1)));
+    if (e != cudaSuccess) return e;
+    opted.fetch_or(bit, std::memory_order_release);
+  }
   tf_unpack_kernel<<<grid, kUnpackThreadsTma, smem, st>>>(chunks, nchunks, buf_bf16, uscale,
                                                           static_cast<const uint8_t*>(buf), err);
   return cudaGetLastError();

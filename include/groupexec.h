@@ -249,6 +249,37 @@ fg_status tf_unpack(const tf_layout* l, float uscale, const void* fusion_buf, vo
  * tf_unpack since the last call recorded an expired wait, else FG_OK. */
 fg_status tf_sync_status(tf_layout* l, void* cuda_stream);
 
+/* ---- AllReduce buckets ----------------------------------------------------
+ * A bucket is a contiguous run of tensors (production order) whose bytes in
+ * the fusion buffer form one fused AllReduce tensor: bucket b holds tensors
+ * bounds[b] .. bounds[b+1]-1 and spans bytes offsets[bounds[b]] up to the
+ * next bucket's start (or total_bytes).  DisCo, Related Work (Horovod's
+ * fusion threshold, like XLA's AllReduce combiner) and Strategy Maker,
+ * optimisation method (iii) (combining an AllReduce with a neighbour). */
+
+/* Threshold fusion: greedy in tensor order, a tensor joins the open bucket
+ * while the bucket's bytes (each tensor's numel * elem bytes rounded up to
+ * align_bytes) stay <= threshold_bytes, else it opens the next bucket, so a
+ * tensor above the threshold sits alone.  bounds: host, n + 1 entries
+ * (caller-owned); *n_buckets receives the bucket count (0 when n == 0).
+ * Host only: needs no device. */
+fg_status tf_plan_threshold(int32_t n, const int64_t* numel, fg_dtype buf_dtype,
+                            int64_t align_bytes, int64_t threshold_bytes,
+                            int32_t* bounds, int32_t* n_buckets);
+
+/* Neighbour combination: bucket j absorbs bucket j+1 (bounds and *n_buckets
+ * updated in place).  FG_EINVAL if j has no successor.  Host only. */
+fg_status tf_buckets_merge(int32_t* bounds, int32_t* n_buckets, int32_t j);
+
+/* tf_pack / tf_unpack restricted to tensors first .. first+count-1 (one
+ * launch; e.g. one bucket, as soon as its gradients exist).  Bytes outside
+ * those tensors' ranges (data and padding) are not touched.  FG_EINVAL if
+ * the range exceeds the layout. */
+fg_status tf_pack_range(const tf_layout* l, int32_t first, int32_t count, float scale,
+                        void* fusion_buf, void* cuda_stream);
+fg_status tf_unpack_range(const tf_layout* l, int32_t first, int32_t count, float uscale,
+                          const void* fusion_buf, void* cuda_stream);
+
 void tf_layout_destroy(tf_layout* l);
 
 #ifdef __cplusplus

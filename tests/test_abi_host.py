@@ -140,3 +140,40 @@ def test_exec_info_of_the_diamond():
     assert info["n_staged"] == 3 and info["n_gathered"] == 0
     assert info["stages"] >= 3
     assert plan.groups[0].alg_bytes == 2 * 8192 * 4096 * 4 + 4096 * 4 + 8192 * 4096 * 4
+
+
+# ---- AllReduce bucket planning (host side of the C ABI) ----------------------
+def test_plan_threshold_matches_oracle():
+    import numpy as np
+    from oracle import buckets as OB
+    from group_execution_gb300 import plan_threshold
+    r = np.random.default_rng(11)
+    cases = [(W.tensor_fusion_sizes(0), T) for T in (0, 1 << 20, 4 << 20, 16 << 20, 1 << 40)]
+    for _ in range(200):
+        n = int(r.integers(0, 40))
+        cases.append((r.integers(0, 50_000, size=n), int(r.integers(0, 300_000))))
+    for sizes, T in cases:
+        for dt, eb in (("bf16", 2), ("f32", 4)):
+            for align in (16, 256, 4096):
+                got = plan_threshold(list(sizes), T, dt, align)
+                assert got == OB.threshold_buckets(list(sizes), T, eb, align), (len(sizes), T, dt, align)
+
+
+def test_buckets_merge_matches_oracle():
+    from oracle import buckets as OB
+    from group_execution_gb300 import merge_buckets
+    b = [0, 2, 7, 8, 20]
+    for j in range(len(b) - 2):
+        assert merge_buckets(b, j) == OB.merge_neighbours(b, j)
+    with pytest.raises(FgError):
+        merge_buckets(b, len(b) - 2)
+
+
+def test_plan_threshold_rejects_bad_arguments():
+    from group_execution_gb300 import plan_threshold
+    with pytest.raises(FgError):
+        plan_threshold([1, 2], 100, align=24)
+    with pytest.raises(FgError):
+        plan_threshold([1, -2], 100)
+    with pytest.raises(FgError):
+        plan_threshold([1, 2], -1)

@@ -77,3 +77,64 @@ def test_pack_special_values():
     tf.pack(1.0, buf)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(buf.cpu().numpy(), PK.pack([x], 1.0))
+
+
+def test_bucketed_pack_unpack_ranges():
+    """Threshold buckets packed and unpacked one launch per bucket: each launch
+    writes exactly its bucket's bytes (bit-exact against the oracle) and
+    leaves every other byte and tensor alone."""
+    from oracle import buckets as OB
+    from group_execution_gb300 import plan_threshold
+    sizes = W.tensor_fusion_sizes(0)
+    xs = W.tensor_fusion_inputs(sizes, 1)
+    dev = [torch.from_numpy(x).cuda() for x in xs]
+    tf = TensorFusion(dev)
+    bounds = plan_threshold(list(sizes), 8 << 20)
+    assert bounds == OB.threshold_buckets(list(sizes), 8 << 20)
+    nb = len(bounds) - 1
+    assert nb >= 4
+    rng = tf.bucket_ranges(bounds)
+    assert rng == OB.bucket_ranges(list(sizes), bounds)
+    ref = PK.pack(xs, 0.125)
+    buf = torch.full((tf.total_bytes,), 0xAB, dtype=torch.uint8, device="cuda")
+    for k in reversed(range(nb)):                      # last bucket first
+        tf.pack_range(bounds[k], bounds[k + 1] - bounds[k], 0.125, buf)
+        torch.cuda.synchronize()
+        got = buf.cpu().numpy()
+        s, e = rng[k]
+        np.testing.assert_array_equal(got[s:e], ref[s:e])
+        assert (got[:s] == 0xAB).all()                 # earlier buckets untouched so far
+    np.testing.assert_array_equal(buf.cpu().numpy(), ref)
+    back = PK.unpack(ref, sizes, 2.0, "bf16")
+    for d in dev:
+        d.fill_(float("nan"))
+    for k in range(nb):
+        tf.unpack_range(bounds[k], bounds[k + 1] - bounds[k], 2.0, buf)
+        tf.sync()
+        for i in range(bounds[k], bounds[k + 1]):
+            np.testing.assert_array_equal(dev[i].cpu().numpy(), back[i])
+        if bounds[k + 1] < len(dev):
+            assert torch.isnan(dev[bounds[k + 1]]).all()   # the next bucket is not written yet
+
+
+def test_range_edge_cases():
+    from group_execution_gb300 import FgError
+    sizes = [5, 8192 * 2 + 3, 17]
+    xs = W.tensor_fusion_inputs(sizes, 2)
+    dev = [torch.from_numpy(x).cuda() for x in xs]
+    tf = TensorFusion(dev)
+    buf = torch.full((tf.total_bytes,), 0xAB, dtype=torch.uint8, device="cuda")
+    tf.pack_range(1, 0, 1.0, buf)                      # an empty range launches nothing
+    torch.cuda.synchronize()
+    assert (buf.cpu().numpy() == 0xAB).all()
+    with pytest.raises(FgError):
+        tf.pack_range(2, 2, 1.0, buf)
+    with pytest.raises(FgError):
+        tf.unpack_range(-1, 1, 1.0, buf)
+    tf.pack_range(1, 1, 1.0, buf)                      # the middle tensor, padding included
+    torch.cuda.synchronize()
+    ref = PK.pack(xs, 1.0)
+    s, e = tf.offsets[1], tf.offsets[2]
+    got = buf.cpu().numpy()
+    np.testing.assert_array_equal(got[s:e], ref[s:e])
+    assert (got[:s] == 0xAB).all() and (got[e:] == 0xAB).all()
