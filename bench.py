@@ -453,6 +453,37 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
             "frac_of_hbm": alg / (med * 1e-3) / 1e9 / hbm}
         del e
 
+    # explicit fusion moves on the diamond when P = X + bias is also a result
+    # the caller keeps: FuseOps ends a group at P (2 groups, P written and
+    # read back); non-duplicate fusion of relu with P gives one group with P
+    # as an extra output; duplicate fusion copies P into each of its readers'
+    # group (P recomputed there; the two groups no longer depend on each other)
+    sp = W.diamond(R, C)
+    sp.mark_output(sp.ops[0].vid)
+    gsp = graph_from_spec(sp)
+    e = dict(dv)
+    for v in sp.ops:
+        e[v.vid] = torch.empty(v.shape, device="cuda")
+    plans = {"fuseops": gsp.build()}
+    pn = gsp.partition(from_fuseops=True)
+    pn.fuse(1, 0, False)
+    plans["non_duplicate"] = pn.build()
+    pd = gsp.partition(from_fuseops=True)
+    for reader in (1, 2, 4):
+        pd.fuse(reader, 0, True)
+    plans["duplicate"] = pd.build()
+    row = {}
+    for k, pl in plans.items():
+        def f(pl=pl):
+            for gid, gi in enumerate(pl.groups):
+                pl.launch_group(gid, {v: e[v] for v in gi.leaves + gi.outs})
+        med, _ = timed(f, flush=False)
+        alg = sum(gi.alg_bytes for gi in pl.groups)
+        row[k] = {"groups": pl.n_groups, "us": med * 1e3, "alg_bytes": alg, "GBps": alg / (med * 1e-3) / 1e9,
+                  "frac_of_hbm": alg / (med * 1e-3) / 1e9 / hbm}
+    rows["diamond_with_P_output"] = row
+    del e
+
     # tensor-fusion pack / unpack
     from group_execution_gb300 import TensorFusion
     sizes = W.tensor_fusion_sizes(0)

@@ -18,7 +18,8 @@ import ctypes as C
 from . import _lib
 from ._lib import FgError, OPCODES, EXEC_KINDS, FG_F32, FG_BF16  # noqa: F401
 
-__all__ = ["Graph", "Plan", "TensorFusion", "FgError", "OPCODES", "graph_from_spec", "plan_threshold", "merge_buckets"]
+__all__ = ["Graph", "Plan", "Partition", "TensorFusion", "FgError", "OPCODES", "graph_from_spec", "plan_threshold",
+           "merge_buckets"]
 
 
 def _i32a(xs):
@@ -75,6 +76,59 @@ class Graph:
               flags=0):
         return Plan(self, max_fused_ops, max_args, allow_reduce_epilogue, wait_limit_ns, flags)
 
+    def partition(self, from_fuseops=True, max_fused_ops=256, max_args=64, allow_reduce_epilogue=False,
+                  wait_limit_ns=2_000_000_000, flags=0):
+        """An explicit partition to change with fusion moves (Partition.fuse)."""
+        return Partition(self, from_fuseops, max_fused_ops, max_args, allow_reduce_epilogue, wait_limit_ns, flags)
+
+
+def _opts(lib, max_fused_ops, max_args, allow_reduce_epilogue, wait_limit_ns, flags):
+    o = _lib.BuildOpts()
+    lib.fg_build_opts_default(C.byref(o))
+    o.max_fused_ops, o.max_args = max_fused_ops, max_args
+    o.allow_reduce_epilogue = int(bool(allow_reduce_epilogue))
+    o.wait_limit_ns = wait_limit_ns
+    o.flags = flags
+    return o
+
+
+class Partition:
+    """Explicit fusion moves (DisCo: an operator fused with one of its
+    predecessors, by duplicate or non-duplicate fusion)."""
+
+    def __init__(self, graph, from_fuseops=True, max_fused_ops=256, max_args=64, allow_reduce_epilogue=False,
+                 wait_limit_ns=2_000_000_000, flags=0):
+        self.lib = graph.lib
+        self.graph = graph
+        o = _opts(self.lib, max_fused_ops, max_args, allow_reduce_epilogue, wait_limit_ns, flags)
+        self.h = C.c_void_p()
+        _lib.check(self.lib.fg_partition_create(graph.h, C.byref(o), int(bool(from_fuseops)), C.byref(self.h)))
+
+    def __del__(self):
+        h = getattr(self, "h", None)
+        if h:
+            self.lib.fg_partition_destroy(h)
+            self.h = None
+
+    def fuse(self, node, pred, duplicate=False):
+        _lib.check(self.lib.fg_partition_fuse(self.h, node, pred, int(bool(duplicate))))
+
+    def query(self):
+        """(group_of, clone_of) per operator, copies included."""
+        n = C.c_int32()
+        _lib.check(self.lib.fg_partition_query(self.h, C.byref(n), None, None))
+        g, c = (C.c_int32 * n.value)(), (C.c_int32 * n.value)()
+        _lib.check(self.lib.fg_partition_query(self.h, None, g, c))
+        return list(g), list(c)
+
+    def build(self):
+        return Plan(self.graph, _handle=self._build_handle())
+
+    def _build_handle(self):
+        h = C.c_void_p()
+        _lib.check(self.lib.fg_build_from_partition(self.h, C.byref(h)))
+        return h
+
 
 def graph_from_spec(spec) -> Graph:
     """A Graph with the same values, in the same order, as a workloads.GraphSpec."""
@@ -90,9 +144,10 @@ def graph_from_spec(spec) -> Graph:
 
 
 class GroupInfo:
-    def __init__(self, nodes, leaves, out, kind, alg_bytes, alg_flops, status):
+    def __init__(self, nodes, leaves, out, kind, alg_bytes, alg_flops, status, outs=None):
         self.nodes, self.leaves, self.out = nodes, leaves, out
         self.kind, self.alg_bytes, self.alg_flops, self.status = kind, alg_bytes, alg_flops, status
+        self.outs = outs if outs is not None else [out]   # sink output first, then extra outputs
 
     def __repr__(self):
         return (f"GroupInfo(nodes={self.nodes}, leaves={self.leaves}, out={self.out}, kind={self.kind}, "
@@ -101,17 +156,15 @@ class GroupInfo:
 
 class Plan:
     def __init__(self, graph: Graph, max_fused_ops=256, max_args=64, allow_reduce_epilogue=False,
-                 wait_limit_ns=2_000_000_000, flags=0):
+                 wait_limit_ns=2_000_000_000, flags=0, _handle=None):
         self.lib = graph.lib
         self.graph = graph
-        o = _lib.BuildOpts()
-        self.lib.fg_build_opts_default(C.byref(o))
-        o.max_fused_ops, o.max_args = max_fused_ops, max_args
-        o.allow_reduce_epilogue = int(bool(allow_reduce_epilogue))
-        o.wait_limit_ns = wait_limit_ns
-        o.flags = flags
-        self.h = C.c_void_p()
-        _lib.check(self.lib.fg_build_groups(graph.h, C.byref(o), C.byref(self.h)))
+        if _handle is not None:
+            self.h = _handle
+        else:
+            o = _opts(self.lib, max_fused_ops, max_args, allow_reduce_epilogue, wait_limit_ns, flags)
+            self.h = C.c_void_p()
+            _lib.check(self.lib.fg_build_groups(graph.h, C.byref(o), C.byref(self.h)))
         nn, ng = C.c_int32(), C.c_int32()
         _lib.check(self.lib.fg_plan_query(self.h, C.byref(nn), C.byref(ng), None, None))
         self.n_nodes, self.n_groups = nn.value, ng.value
@@ -133,8 +186,12 @@ class Plan:
         out, kind, ab, af = C.c_int32(), C.c_int32(), C.c_int64(), C.c_int64()
         st = self.lib.fg_plan_group_info(self.h, gid, C.byref(nn), nodes, C.byref(nl), leaves, C.byref(out),
                                          C.byref(kind), C.byref(ab), C.byref(af))
+        no = C.c_int32()
+        self.lib.fg_plan_group_outputs(self.h, gid, C.byref(no), None)
+        outs = (C.c_int32 * no.value)()
+        self.lib.fg_plan_group_outputs(self.h, gid, None, outs)
         return GroupInfo(list(nodes)[:nn.value], list(leaves)[:nl.value], out.value, EXEC_KINDS[kind.value],
-                         ab.value, af.value, st)
+                         ab.value, af.value, st, list(outs))
 
     def exec_info(self, gid):
         v = [C.c_int32() for _ in range(6)]

@@ -69,6 +69,12 @@ SIGNATURES = {
     "tf_pack": (_I32, [_P, _F, _P, _P]),
     "tf_unpack": (_I32, [_P, _F, _P, _P]),
     "tf_sync_status": (_I32, [_P, _P]),
+    "fg_plan_group_outputs": (_I32, [_P, _I32, _P, _P]),
+    "fg_partition_create": (_I32, [_P, _P, _I32, _P]),
+    "fg_partition_fuse": (_I32, [_P, _I32, _I32, _I32]),
+    "fg_partition_query": (_I32, [_P, _P, _P, _P]),
+    "fg_build_from_partition": (_I32, [_P, _P]),
+    "fg_partition_destroy": (None, [_P]),
     "tf_plan_threshold": (_I32, [_I32, _P, _I32, _I64, _I64, _P, _P]),
     "tf_buckets_merge": (_I32, [_P, _P, _I32]),
     "tf_pack_range": (_I32, [_P, _I32, _I32, _F, _P, _P]),

@@ -104,6 +104,11 @@ struct fg_plan {
   int32_t* d_err = nullptr;
 };
 
+struct fg_partition {
+  Partition P;
+  BuildOpts opts;
+};
+
 struct tf_layout {
   int32_t n = 0;
   int buf_bf16 = 1;
@@ -327,6 +332,18 @@ void prepare_group(GroupExec& ge, const BuildOpts& o, int nsm) {
     }
   }
   p.nstaged = mi;
+  p.nxout = (int32_t)cg.xout_values.size();
+  for (int j = 0; j < p.nxout; ++j) {
+    const Map& mp = cg.xout_maps[j];
+    XOutDesc& x = p.xout[j];
+    x.cls = cg.xout_cls[j];
+    x.nterms = mp.n;
+    for (int k = 0; k < mp.n; ++k) {
+      x.d[k] = mp.d[k];
+      x.m[k] = mp.m[k];
+      x.s[k] = mp.s[k];
+    }
+  }
   std::copy(cg.epi.begin(), cg.epi.end(), p.epi);
   p.nepi = (int)cg.epi.size();
   p.FR = (int32_t)cg.FR;
@@ -491,6 +508,8 @@ GroupExec make_exec(const Graph& g, const std::vector<int32_t>& nodes, const Bui
   GroupExec ge;
   try {
     ge.cg = compile_group(g, nodes);
+    if (!ge.cg.xout_values.empty() && (o.flags & FG_FLAG_INTERPRET))
+      throw CompileError{FG_EUNSUPPORTED, "groups with extra outputs run compiled programs only"};
     plan_staging(g, ge.cg, o);
     if (ge.cg.exec == FG_EXEC_GEMM) {
       prepare_gemm(ge, o, nsm, g);
@@ -663,7 +682,10 @@ fg_status launch_exec(fg_plan* p, GroupExec& ge, void* const* ptrs, void* stream
   for (int32_t v : cg.leaf_values) key.push_back(ptrs[v]);
   for (int32_t v : cg.epi_leaf_values) key.push_back(ptrs[v]);
   key.push_back(ptrs[cg.out_value]);
+  for (int32_t v : cg.xout_values) key.push_back(ptrs[v]);
   if (key != ge.last_ptrs) {
+    for (int32_t v : cg.xout_values) if (fg_status st = check_ptr(ptrs[v], v)) return st;
+    for (size_t j = 0; j < cg.xout_values.size(); ++j) gp.xout[j].ptr = static_cast<float*>(ptrs[cg.xout_values[j]]);
     for (int32_t v : cg.leaf_values) if (fg_status st = check_ptr(ptrs[v], v)) return st;
     for (int32_t v : cg.epi_leaf_values) if (fg_status st = check_ptr(ptrs[v], v)) return st;
     if (fg_status st = check_ptr(ptrs[cg.out_value], cg.out_value)) return st;
@@ -699,37 +721,31 @@ fg_status launch_exec(fg_plan* p, GroupExec& ge, void* const* ptrs, void* stream
   return FG_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-fg_status fg_build_groups(const fg_graph* gh, const fg_build_opts* opts, fg_plan** out) {
-  if (!gh || !out) return err(FG_EINVAL, "null argument");
-  *out = nullptr;
+fg_status build_opts_from(const fg_build_opts* opts, BuildOpts& b) {
   fg_build_opts o;
   fg_build_opts_default(&o);
   if (opts) o = *opts;
   if (o.max_fused_ops < 1 || o.max_args < 2) return err(FG_EINVAL, "max_fused_ops >= 1 and max_args >= 2 required");
-  if (gh->g.nodes.empty()) return err(FG_EINVAL, "graph has no operators");
+  b.max_fused_ops = o.max_fused_ops;
+  b.max_args = o.max_args;
+  b.allow_reduce_epilogue = o.allow_reduce_epilogue;
+  b.wait_limit_ns = o.wait_limit_ns > 0 ? o.wait_limit_ns : 2000000000LL;
+  b.flags = o.flags;
+  return FG_OK;
+}
+
+// A plan for the given groups (in launch order): compiled programs, device
+// tables and the unfused single-operator programs.
+fg_status build_plan(const Graph& g, const BuildOpts& o, const std::vector<std::vector<int32_t>>& groups,
+                     const std::vector<int32_t>& group_of, const std::vector<int32_t>& ipdom, fg_plan** out) {
   std::unique_ptr<fg_plan> p(new (std::nothrow) fg_plan());
   if (!p) return err(FG_ENOMEM, "out of host memory");
-  p->g = gh->g;
-  p->opts.max_fused_ops = o.max_fused_ops;
-  p->opts.max_args = o.max_args;
-  p->opts.allow_reduce_epilogue = o.allow_reduce_epilogue;
-  p->opts.wait_limit_ns = o.wait_limit_ns > 0 ? o.wait_limit_ns : 2000000000LL;
-  p->opts.flags = o.flags;
+  p->g = g;
+  p->opts = o;
+  p->group_of = group_of;
+  p->ipdom = ipdom;
   p->has_device = device_present(&p->nsm);
-  partition(p->g, p->opts, p->group_of, p->ipdom);
-  std::vector<int32_t> sinks;
-  for (size_t i = 0; i < p->group_of.size(); ++i)
-    if (p->group_of[i] == (int32_t)i) sinks.push_back((int32_t)i);
-  for (int32_t s : sinks) {
-    std::vector<int32_t> nodes;
-    for (size_t i = 0; i < p->group_of.size(); ++i)
-      if (p->group_of[i] == s) nodes.push_back((int32_t)i);
-    p->groups.push_back(make_exec(p->g, nodes, p->opts, p->nsm));
-  }
+  for (const auto& nodes : groups) p->groups.push_back(make_exec(p->g, nodes, p->opts, p->nsm));
   for (size_t i = 0; i < p->g.nodes.size(); ++i)
     p->singles.push_back(make_exec(p->g, {(int32_t)i}, p->opts, p->nsm));
   if (p->has_device) {
@@ -758,6 +774,98 @@ fg_status fg_build_groups(const fg_graph* gh, const fg_build_opts* opts, fg_plan
   *out = p.release();
   return FG_OK;
 }
+
+}  // namespace
+
+extern "C" {
+
+fg_status fg_build_groups(const fg_graph* gh, const fg_build_opts* opts, fg_plan** out) {
+  if (!gh || !out) return err(FG_EINVAL, "null argument");
+  *out = nullptr;
+  BuildOpts o;
+  if (fg_status st = build_opts_from(opts, o)) return st;
+  if (gh->g.nodes.empty()) return err(FG_EINVAL, "graph has no operators");
+  std::vector<int32_t> group_of, ipdom;
+  partition(gh->g, o, group_of, ipdom);
+  std::vector<std::vector<int32_t>> groups;
+  for (size_t s = 0; s < group_of.size(); ++s)
+    if (group_of[s] == (int32_t)s) {
+      groups.emplace_back();
+      for (size_t i = 0; i < group_of.size(); ++i)
+        if (group_of[i] == (int32_t)s) groups.back().push_back((int32_t)i);
+    }
+  return build_plan(gh->g, o, groups, group_of, ipdom, out);
+}
+
+// ---- explicit fusion ---------------------------------------------------------
+fg_status fg_partition_create(const fg_graph* gh, const fg_build_opts* opts, int32_t from_fuseops,
+                              fg_partition** out) {
+  if (!gh || !out) return err(FG_EINVAL, "null argument");
+  *out = nullptr;
+  BuildOpts o;
+  if (fg_status st = build_opts_from(opts, o)) return st;
+  if (gh->g.nodes.empty()) return err(FG_EINVAL, "graph has no operators");
+  std::unique_ptr<fg_partition> p(new (std::nothrow) fg_partition());
+  if (!p) return err(FG_ENOMEM, "out of host memory");
+  p->opts = o;
+  p->P = singleton_partition(gh->g, o);
+  if (from_fuseops) {
+    std::vector<int32_t> group_of, ipdom;
+    partition(gh->g, o, group_of, ipdom);
+    // label = the group's smallest node id
+    std::vector<int32_t> first(group_of.size(), -1);
+    for (size_t i = 0; i < group_of.size(); ++i)
+      if (first[group_of[i]] < 0) first[group_of[i]] = (int32_t)i;
+    for (size_t i = 0; i < group_of.size(); ++i) p->P.label[i] = first[group_of[i]];
+  }
+  *out = p.release();
+  return FG_OK;
+}
+
+fg_status fg_partition_fuse(fg_partition* p, int32_t node, int32_t pred, int32_t duplicate) {
+  if (!p) return err(FG_EINVAL, "null partition");
+  const BuildOpts o = p->opts;
+  const GroupCheck check = [&o](const Graph& g, const std::vector<int32_t>& nodes) {
+    // an opaque operator stays alone (TVM "Operator Fusion", Operator Pattern
+    // Classification: opaque operators are not fused)
+    if (nodes.size() > 1)
+      for (int32_t x : nodes)
+        if (op_kind(g.nodes[x].op) == K_OPAQUE) throw CompileError{FG_EUNSUPPORTED, "an opaque operator stays alone"};
+    GroupExec ge = make_exec(g, nodes, o, 148);
+    if (ge.compile_status != FG_OK) throw CompileError{ge.compile_status, ge.compile_error};
+    const int args = (int)(ge.cg.leaf_values.size() + ge.cg.epi_leaf_values.size() + 1 + ge.cg.xout_values.size());
+    if (args > o.max_args) throw CompileError{FG_EUNSUPPORTED, "the fused group exceeds max_args"};
+  };
+  try {
+    fuse_move(p->P, node, pred, duplicate != 0, check);
+  } catch (const CompileError& e) {
+    return err(e.st, e.msg);
+  }
+  return FG_OK;
+}
+
+fg_status fg_partition_query(const fg_partition* p, int32_t* n_nodes, int32_t* group_of, int32_t* clone_of) {
+  if (!p) return err(FG_EINVAL, "null partition");
+  if (n_nodes) *n_nodes = (int32_t)p->P.label.size();
+  if (group_of) std::copy(p->P.label.begin(), p->P.label.end(), group_of);
+  if (clone_of) std::copy(p->P.clone_of.begin(), p->P.clone_of.end(), clone_of);
+  return FG_OK;
+}
+
+fg_status fg_build_from_partition(const fg_partition* p, fg_plan** out) {
+  if (!p || !out) return err(FG_EINVAL, "null argument");
+  *out = nullptr;
+  std::vector<std::vector<int32_t>> groups;
+  try {
+    groups = partition_groups(p->P);
+  } catch (const CompileError& e) {
+    return err(e.st, e.msg);
+  }
+  std::vector<int32_t> ipdom(p->P.label.size(), -1);
+  return build_plan(p->P.g, p->opts, groups, p->P.label, ipdom, out);
+}
+
+void fg_partition_destroy(fg_partition* p) { delete p; }
 
 void fg_plan_destroy(fg_plan* p) {
   if (!p) return;
@@ -792,6 +900,18 @@ fg_status fg_plan_group_info(const fg_plan* p, int32_t gid, int32_t* n_nodes, in
   if (alg_bytes) *alg_bytes = cg.alg_bytes;
   if (alg_flops) *alg_flops = cg.alg_flops;
   if (ge.compile_status != FG_OK) return err(ge.compile_status, ge.compile_error);
+  return FG_OK;
+}
+
+fg_status fg_plan_group_outputs(const fg_plan* p, int32_t gid, int32_t* n_out, int32_t* out_values) {
+  if (!p) return err(FG_EINVAL, "null plan");
+  if (gid < 0 || gid >= (int32_t)p->groups.size()) return err(FG_EINVAL, "unknown group id");
+  const CompiledGroup& cg = p->groups[gid].cg;
+  if (n_out) *n_out = (int32_t)(1 + cg.xout_values.size());
+  if (out_values) {
+    out_values[0] = cg.out_value;
+    std::copy(cg.xout_values.begin(), cg.xout_values.end(), out_values + 1);
+  }
   return FG_OK;
 }
 

@@ -103,6 +103,17 @@ struct LeafDesc {
   int64_t d[kMaxTerms], m[kMaxTerms], s[kMaxTerms];
 };
 
+// An extra output of a multi-output group (a value computed inside the group
+// that is also needed outside it): written at frame point g to
+// f = sum_k ((g / d_k) % m_k) * s_k, a permutation of its elements; cls is
+// LEAF_IDENT (f = g), LEAF_TRANS (f = c*FR + r) or LEAF_GATHER (the digits).
+constexpr int kMaxXOut = 4;
+struct XOutDesc {
+  float* ptr;            // filled at launch
+  int32_t cls, nterms;
+  int64_t d[kMaxTerms], m[kMaxTerms], s[kMaxTerms];
+};
+
 // ---- kernel parameter blocks -------------------------------------------------
 constexpr int kMaxStaged = 16;    // TMA-staged leaves per group
 constexpr int kMaxLeaves = 24;    // all leaf reads (staged + gathered)
@@ -137,6 +148,8 @@ struct GroupParams {
   int32_t band;                        // tile order: 0 row-major, else bands of `band` tile rows
   int32_t red_op, nsplit, tiles_per_split, nunits;
   int32_t inject;                      // failure injection: 1 = the producer issues no loads
+  int32_t nxout;                       // extra outputs (compiled programs only)
+  XOutDesc xout[kMaxXOut];
 };
 
 // GEMM + epilogue kernel: 128 x 256 accumulator tiles in TMEM, K in blocks

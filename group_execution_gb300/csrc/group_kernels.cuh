@@ -100,6 +100,40 @@ struct TileEnv {
       t[k] = v;
     }
   }
+  // Extra output j: this thread's eight frame points, written where the
+  // output's map sends them: rows of 32 contiguous bytes for the identity; a
+  // transposed output gets 128-byte runs across the warp (lane = frame row);
+  // any other permutation is evaluated digit by digit (frames with such
+  // outputs hold fewer than 2^31 elements).
+  __device__ __forceinline__ void xstore(int j, const float (&v)[8]) const {
+    const XOutDesc& X = P.xout[j];
+    const int r = r0 + lr, c = c0 + lc0;
+    if (r >= P.FR) return;
+    if (X.cls == LEAF_IDENT) {
+      float* op = X.ptr + (int64_t)r * P.FC + c;
+      if ((P.FC & 3) == 0 && c + 8 <= P.FC) {
+        reinterpret_cast<float4*>(op)[0] = make_float4(v[0], v[1], v[2], v[3]);
+        reinterpret_cast<float4*>(op)[1] = make_float4(v[4], v[5], v[6], v[7]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (c + k < P.FC) op[k] = v[k];
+      }
+    } else if (X.cls == LEAF_TRANS) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (c + k < P.FC) X.ptr[(int64_t)(c + k) * P.FR + r] = v[k];
+    } else {
+#pragma unroll 1
+      for (int k = 0; k < 8; ++k) {
+        if (c + k >= P.FC) break;
+        const uint32_t g = (uint32_t)r * (uint32_t)P.FC + (uint32_t)(c + k);
+        uint32_t f = 0;
+        for (int q = 0; q < X.nterms; ++q) f += ((g / (uint32_t)X.d[q]) % (uint32_t)X.m[q]) * (uint32_t)X.s[q];
+        X.ptr[f] = v[k];
+      }
+    }
+  }
 };
 
 // Issues the TMA loads of one staged leaf for the tile at (r0, c0).

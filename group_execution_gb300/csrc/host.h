@@ -1,6 +1,7 @@
 // Host-side graph IR, grouping and group compilation (internal header).
 #pragma once
 #include <cstdint>
+#include <functional>
 #include <string>
 #include <vector>
 
@@ -71,6 +72,12 @@ struct CompiledGroup {
   std::vector<int32_t> nodes;         // ascending node ids
   int32_t sink = -1;                  // sink node
   int32_t out_value = -1;
+  // extra outputs (values of the group also read outside it): value, map
+  // from the frame, and the expression that computes it
+  std::vector<int32_t> xout_values;
+  std::vector<Map> xout_maps;
+  std::vector<int> xout_cls;          // LEAF_IDENT, LEAF_TRANS or LEAF_GATHER (any other permutation)
+  std::vector<int> xout_expr;
   std::vector<int32_t> leaf_values;   // distinct outside values, first-use order
   int64_t alg_bytes = 0, alg_flops = 0;
   int64_t FR = 1, FC = 1;             // frame
@@ -118,5 +125,23 @@ struct CompileError {
 };
 CompiledGroup compile_group(const Graph& g, const std::vector<int32_t>& nodes);
 void plan_staging(const Graph& g, CompiledGroup& cg, const BuildOpts& o);
+
+// Explicit fusion (host_explicit.cpp).  The partition owns a copy of the
+// graph, which duplicate fusion extends with copies of operators (appended
+// after the original nodes; their values are read only inside their group).
+struct Partition {
+  Graph g;
+  std::vector<int32_t> label;      // per node: group label (the group's smallest node id)
+  std::vector<int32_t> clone_of;   // per node: the copied operator, -1 for originals
+  int max_fused_ops = 256;
+};
+// Throws CompileError when a group cannot run as one kernel.
+using GroupCheck = std::function<void(const Graph&, const std::vector<int32_t>&)>;
+Partition singleton_partition(const Graph& g, const BuildOpts& o);
+// Fuses `node` with its predecessor `pred`; throws CompileError (FG_EINVAL,
+// FG_EUNSUPPORTED) and leaves the partition unchanged when refused.
+void fuse_move(Partition& P, int32_t node, int32_t pred, bool duplicate, const GroupCheck& check);
+// Node lists of the groups in an order that respects their dependencies.
+std::vector<std::vector<int32_t>> partition_groups(const Partition& P);
 
 }  // namespace fg

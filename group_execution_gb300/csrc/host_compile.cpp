@@ -154,7 +154,46 @@ struct Builder {
     int id = build_new(value, mp);
     ex[id].uses++;
     memo[key] = id;
+    built.push_back({value, mp, id});
     return id;
+  }
+
+  struct Built {
+    int value;
+    Map map;
+    int expr;
+  };
+  std::vector<Built> built;   // every (value, map) evaluated, in build order
+
+  // Expressions for the group's extra outputs, appended to the DAG: each at a
+  // map the main program already evaluates it at when that map covers all its
+  // elements, else at the frame's flat index (any one-to-one map will do for
+  // a value nothing else in the group reads).
+  void add_xouts(CompiledGroup& cg) {
+    for (int32_t v : cg.xout_values) {
+      const Value& xv = g.values[v];
+      if (xv.numel() != FR * FC) fail(FG_EUNSUPPORTED, "an extra output must have as many elements as the frame");
+      int expr = -1;
+      Map mp;
+      for (const Built& b : built)
+        if (b.value == v) {
+          expr = b.expr;
+          mp = b.map;
+          break;
+        }
+      if (expr < 0) {
+        mp = ident(FR, FC);
+        expr = build(v, mp);
+      }
+      int cls = classify(mp, FR, FC);
+      if (cls != LEAF_IDENT && cls != LEAF_TRANS) {
+        cls = LEAF_GATHER;
+        if (FR * FC >= (int64_t)1 << 31) fail(FG_EUNSUPPORTED, "a permuted extra output of a frame of 2^31 or more elements");
+      }
+      cg.xout_maps.push_back(mp);
+      cg.xout_cls.push_back(cls);
+      cg.xout_expr.push_back(expr);
+    }
   }
 
   int build_new(int value, const Map& mp) {
@@ -382,7 +421,18 @@ CompiledGroup compile_group(const Graph& g, const std::vector<int32_t>& nodes_in
   CompiledGroup cg;
   cg.nodes = nodes_in;
   std::sort(cg.nodes.begin(), cg.nodes.end());
-  cg.sink = cg.nodes.back();
+  // the sink: the last member whose value no other member reads (for
+  // FuseOps groups, the last member; a copied operator made by duplicate
+  // fusion sits after its reader and is never the sink)
+  {
+    std::vector<char> read_in(g.values.size(), 0);
+    for (int x : cg.nodes)
+      for (int32_t a : g.nodes[x].args) read_in[a] = 1;
+    cg.sink = -1;
+    for (int x : cg.nodes)
+      if (!read_in[g.nodes[x].value]) cg.sink = x;
+    if (cg.sink < 0) fail(FG_EUNSUPPORTED, "internal: group without a sink");
+  }
   cg.out_value = g.nodes[cg.sink].value;
   int mm = -1, red = -1;
   for (int x : cg.nodes) {
@@ -401,6 +451,35 @@ CompiledGroup compile_group(const Graph& g, const std::vector<int32_t>& nodes_in
   // distinct outside values, first-use order
   std::vector<char> in(g.nodes.size(), 0);
   for (int x : cg.nodes) in[x] = 1;
+  // values of the group read outside it (non-duplicate fusion of an operator
+  // whose output other operators still need) or marked as graph outputs
+  {
+    std::vector<char> read_out(g.values.size(), 0);
+    for (size_t x = 0; x < g.nodes.size(); ++x)
+      if (!in[x])
+        for (int32_t a : g.nodes[x].args) read_out[a] = 1;
+    std::vector<char> read_in(g.values.size(), 0);
+    for (int x : cg.nodes)
+      for (int32_t a : g.nodes[x].args) read_in[a] = 1;
+    for (int x : cg.nodes) {
+      const int32_t v = g.nodes[x].value;
+      if (v != cg.out_value && (read_out[v] || g.is_output[v] || !read_in[v])) cg.xout_values.push_back(v);
+    }
+    if ((int)cg.xout_values.size() > kMaxXOut) fail(FG_EUNSUPPORTED, "more than 4 extra outputs in one group");
+    if (!cg.xout_values.empty() && mm >= 0) fail(FG_EUNSUPPORTED, "extra outputs of a matmul group");
+    if (!cg.xout_values.empty() && red >= 0) {
+      // only values of the prologue (frame-shaped, before the reduction)
+      std::vector<char> after(g.nodes.size(), 0);
+      after[red] = 1;
+      for (int x : cg.nodes)
+        for (int32_t a : g.nodes[x].args) {
+          const int prod = g.values[a].node;
+          if (prod >= 0 && in[prod] && after[prod]) after[x] = 1;
+        }
+      for (int32_t v : cg.xout_values)
+        if (after[g.values[v].node]) fail(FG_EUNSUPPORTED, "an extra output after the reduction");
+    }
+  }
   for (int x : cg.nodes)
     for (int32_t a : g.nodes[x].args) {
       int prod = g.values[a].node;
@@ -415,6 +494,7 @@ CompiledGroup compile_group(const Graph& g, const std::vector<int32_t>& nodes_in
   }
   const Value& out = g.values[cg.out_value];
   cg.alg_bytes += out.bytes();
+  for (int32_t v : cg.xout_values) cg.alg_bytes += g.values[v].bytes();
 
   if (mm >= 0) {
     const Node& n = g.nodes[mm];
@@ -457,7 +537,9 @@ CompiledGroup compile_group(const Graph& g, const std::vector<int32_t>& nodes_in
     Builder b(g, cg.nodes, cg.FR, cg.FC);
     b.anchor = red;   // never reached from the prologue root
     b.anchor_map = ident(1, cg.FR);
-    Program p = emit_program(b, b.build(n.args[0], ident(cg.FR, cg.FC)));
+    const int root = b.build(n.args[0], ident(cg.FR, cg.FC));
+    b.add_xouts(cg);
+    Program p = emit_program(b, root);
     cg.prog = p.code;
     cg.leaves = p.leaves;
     cg.depth = p.depth;
@@ -487,7 +569,9 @@ CompiledGroup compile_group(const Graph& g, const std::vector<int32_t>& nodes_in
   cg.FR = out.rows;
   cg.FC = out.cols;
   Builder b(g, cg.nodes, cg.FR, cg.FC);
-  Program p = emit_program(b, b.build(cg.out_value, ident(cg.FR, cg.FC)));
+  const int root = b.build(cg.out_value, ident(cg.FR, cg.FC));
+  b.add_xouts(cg);
+  Program p = emit_program(b, root);
   cg.prog = p.code;
   cg.leaves = p.leaves;
   cg.depth = p.depth;

@@ -184,6 +184,14 @@ fg_status fg_launch_unfused(fg_plan* p, int32_t node, void* const* value_ptrs, v
  * FG_ETIMEOUT when a bounded wait expired, FG_EDEVICE for other flags. */
 fg_status fg_sync_status(fg_plan* p, void* cuda_stream);
 
+/* Every value group gid writes: out_values[0] is the group's sink output
+ * (the out_value of fg_plan_group_info), then its extra outputs: values
+ * computed inside the group that operators outside it, or the caller, still
+ * read (only explicit partitions make these; see fg_partition_fuse).
+ * out_values: host, caller-owned, room for *n_out entries (query with NULL
+ * first; at most 5). */
+fg_status fg_plan_group_outputs(const fg_plan* p, int32_t gid, int32_t* n_out, int32_t* out_values);
+
 /* Diagnostics for benchmarks: number of kernel launches fg_launch_group
  * issues for gid (always 1), the tile shape, pipeline depth and number of
  * TMA-staged leaves chosen for it. */
@@ -221,6 +229,51 @@ const char* fg_last_error(void);
  * Device-side timeouts are not reported by this entry point. */
 fg_status fg_row_reduce_noalloc(int32_t opcode, const float* x, int64_t rows, int64_t cols, float* y,
                                 void* cuda_stream);
+
+/* ---- explicit fusion --------------------------------------------------------
+ * DisCo, Introduction and Strategy Maker, optimisation methods (i) and (ii):
+ * an operator is fused with one of the predecessors whose output it reads.
+ * When that predecessor has other readers, non-duplicate fusion folds it into
+ * the fused group, whose output then also serves those readers (the group
+ * gains an extra output), while duplicate fusion puts a copy of it into the
+ * group and keeps the original for its other readers.  The search that
+ * chooses the moves is the caller's. */
+typedef struct fg_partition fg_partition;
+
+/* A partition of g's operators: every operator alone (from_fuseops = 0) or the
+ * FuseOps grouping of fg_build_groups (from_fuseops = 1).  The partition keeps
+ * its own copy of the graph; opts as for fg_build_groups (max_fused_ops and
+ * max_args bound every fused group). */
+fg_status fg_partition_create(const fg_graph* g, const fg_build_opts* opts, int32_t from_fuseops,
+                              fg_partition** out);
+
+/* Fuses operator `node` with operator `pred`, whose output must be an
+ * operand of `node`; duplicate = 1 for duplicate fusion (a predecessor that
+ * nothing else reads is simply merged either way).  Duplicate fusion appends
+ * a copy of `pred` to the partition's graph (node id = the old node count,
+ * its value id = the old value count; its value is never materialised).
+ * Returns FG_EINVAL (not a predecessor, already one group, bad id) or
+ * FG_EUNSUPPORTED (the merged group would not be convex, or would not run as
+ * one kernel: two reductions, a matmul with extra outputs, more than 4 extra
+ * outputs, an extra output after a reduction or without the frame's element
+ * count, or the max_fused_ops / max_args bounds); the partition is then
+ * unchanged. */
+fg_status fg_partition_fuse(fg_partition* p, int32_t node, int32_t pred, int32_t duplicate);
+
+/* n_nodes: operators including copies; group_of[i]: the group's smallest node
+ * id; clone_of[i]: the operator node i copies, -1 for originals.  Arrays are
+ * host, caller-owned, n_nodes entries, or NULL. */
+fg_status fg_partition_query(const fg_partition* p, int32_t* n_nodes, int32_t* group_of, int32_t* clone_of);
+
+/* A plan for the partition's groups (same queries and launches as a
+ * fg_build_groups plan).  Group ids follow a dependency order: launching
+ * groups 0, 1, ... computes every output.  fg_plan_query reports the
+ * partition's labels as group_of and -1 as ipdom.  Extra outputs need a
+ * pointer in value_ptrs like any output; groups with extra outputs run
+ * compiled programs only. */
+fg_status fg_build_from_partition(const fg_partition* p, fg_plan** plan);
+
+void fg_partition_destroy(fg_partition* p);
 
 /* ---- tensor fusion ------------------------------------------------------- */
 

@@ -23,8 +23,9 @@ def run_fused(plan, spec, dev_inputs, keep_all=True):
     """Launch every group in order; returns {vid: tensor} of group outputs."""
     env = dict(dev_inputs)
     for gid, info in enumerate(plan.groups):
-        env[info.out] = empty_for(spec, info.out)
-        plan.launch_group(gid, {v: env[v] for v in info.leaves + [info.out]})
+        for o in info.outs:                  # the sink output and any extra outputs
+            env[o] = empty_for(spec, o)
+        plan.launch_group(gid, {v: env[v] for v in info.leaves + info.outs})
     return env
 
 

@@ -177,3 +177,102 @@ def test_plan_threshold_rejects_bad_arguments():
         plan_threshold([1, -2], 100)
     with pytest.raises(FgError):
         plan_threshold([1, 2], -1)
+
+
+# ---- explicit fusion moves (host side of the C ABI) --------------------------
+def _lib_moves_match_oracle(spec, seed, from_fuseops):
+    import numpy as np
+    from oracle import explicit as OX
+    from group_execution_gb300 import _lib as L
+    r = np.random.default_rng(seed)
+    part = graph_from_spec(spec).partition(from_fuseops=from_fuseops)
+    st = OX.initial(spec, from_fuseops=from_fuseops)
+    assert part.query() == (st.label, st.clone_of)
+    accepted = 0
+    for _ in range(16):
+        node = int(r.integers(0, len(st.ops)))
+        prod = {o[3]: i for i, o in enumerate(st.ops)}
+        cands = [prod[a] for a in st.ops[node][1] if a in prod]
+        pred = cands[int(r.integers(0, len(cands)))] if cands and r.random() < 0.9 else int(r.integers(0, len(st.ops)))
+        dup = bool(r.integers(0, 2))
+        try:
+            nxt, why = OX.fuse(st, node, pred, dup), None
+        except ValueError:
+            nxt, why = None, L.FG_EINVAL
+        except OX.NotConvex:
+            nxt, why = None, L.FG_EUNSUPPORTED
+        try:
+            part.fuse(node, pred, dup)
+            ok = True
+        except FgError as e:
+            ok, status, msg = False, e.status, str(e)
+        if nxt is None:
+            assert not ok and status == why, (node, pred, dup)
+            continue
+        if not ok:
+            # the library may refuse a convex move its kernels cannot run
+            assert status == L.FG_EUNSUPPORTED and "convex" not in msg, msg
+            continue
+        st = nxt
+        accepted += 1
+        assert part.query() == (st.label, st.clone_of), (node, pred, dup)
+    return accepted
+
+
+def test_partition_moves_match_oracle():
+    from tests._helpers import small_dags, dag_to_spec
+    import numpy as np
+    total = 0
+    for k, (n, preds) in enumerate(small_dags(8, seed=77, count=120)):
+        r = np.random.default_rng(k)
+        # relu / transpose, add / mul: every operator of the random DAGs is legal in the library
+        spec = dag_to_spec(n, preds, op_choice=[int(x) for x in r.integers(0, 2, size=n)], outputs=[n - 1])
+        total += _lib_moves_match_oracle(spec, k, from_fuseops=bool(k % 2))
+    assert total > 100
+
+
+def test_partition_moves_on_the_workloads():
+    for spec in (W.rnnlm_chain(), W.diamond(64, 32), W.sf_update(64, 128, 256)):
+        _lib_moves_match_oracle(spec, 1, False)
+        _lib_moves_match_oracle(spec, 2, True)
+
+
+def test_partition_plan_groups_follow_dependencies():
+    from oracle import explicit as OX
+    spec = W.diamond(64, 32)
+    g = graph_from_spec(spec)
+    part = g.partition(from_fuseops=False)
+    st = OX.initial(spec, from_fuseops=False)
+    # relu, the scale and the multiply all read P = X + bias: fold P into
+    # relu's group without copying (P becomes an extra output), copy it into
+    # the scale's group
+    for node, pred, dup in ((1, 0, False), (2, 0, True)):
+        part.fuse(node, pred, dup)
+        st = OX.fuse(st, node, pred, dup)
+    assert part.query() == (st.label, st.clone_of)
+    plan = part.build()
+    order = OX.groups(st)
+    assert [sorted(gi.nodes) for gi in plan.groups] == [sorted(x) for x in order]
+    for gi, nodes in zip(plan.groups, order):
+        assert gi.outs == OX.group_outputs(st, nodes)
+
+
+def test_interpreter_refuses_extra_outputs():
+    from group_execution_gb300 import _lib as L
+    spec = W.diamond(64, 32)
+    part = graph_from_spec(spec).partition(from_fuseops=False, flags=L.FG_FLAG_INTERPRET)
+    with pytest.raises(FgError) as e:
+        part.fuse(1, 0, False)     # P keeps other readers: an extra output
+    assert e.value.status == L.FG_EUNSUPPORTED
+    part.fuse(2, 0, True)          # a copy needs no extra output
+
+
+def test_opaque_operators_stay_alone():
+    g = W.GraphSpec()
+    x = g.input((8, 8))
+    a = g.op("opaque_copy", (x,))
+    b = g.op("relu", (a,))
+    g.mark_output(b)
+    part = graph_from_spec(g).partition(from_fuseops=False)
+    with pytest.raises(FgError):
+        part.fuse(1, 0, False)
