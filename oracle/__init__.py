@@ -25,10 +25,15 @@ out from the passages they cite:
 * ``buckets``   -- AllReduce buckets: threshold fusion (DisCo, Related Work,
                    on Horovod and XLA) and neighbour combination (DisCo,
                    Strategy Maker, method (iii)).
+* ``explicit``  -- explicit fusion moves: non-duplicate and duplicate fusion
+                   of an operator with a predecessor (DisCo, Introduction).
+* ``simulate``  -- the training-step simulator: ready queue, in-order
+                   AllReduce channel, linear AllReduce time (DisCo,
+                   Simulator and Profiler).
 
 Parity status: every function here is pinned by tests under ``tests/``
 (``-m "not gpu"``) against brute force, closed forms, worked examples from the
 pages or library routines, except the long random-DAG numerics, which only the
 oracle itself defines ("parity unpinned" beyond per-op pins).
 """
-from . import kinds, postdom, partition, execute, pack, buckets  # noqa: F401
+from . import kinds, postdom, partition, execute, pack, buckets, explicit, simulate  # noqa: F401
