@@ -19,7 +19,7 @@ from . import _lib
 from ._lib import FgError, OPCODES, EXEC_KINDS, FG_F32, FG_BF16  # noqa: F401
 
 __all__ = ["Graph", "Plan", "Partition", "TensorFusion", "FgError", "OPCODES", "graph_from_spec", "plan_threshold",
-           "merge_buckets"]
+           "merge_buckets", "simulate"]
 
 
 def _i32a(xs):
@@ -300,3 +300,35 @@ def merge_buckets(bounds, j):
     nb = C.c_int32(len(bounds) - 1)
     _lib.check(lib.tf_buckets_merge(arr, C.byref(nb), j))
     return list(arr[:nb.value + 1])
+
+
+def simulate(op_time, edges, tensor_producer, tensor_bytes, buckets, c, d, ar_edges=()):
+    """Training-step time from the library's simulator (fg_simulate): op_time
+    per operator, edges (src, dst), gradient tensors (producer, bytes),
+    buckets (lists of tensor ids, one AllReduce each), AllReduce time
+    c * bytes + d, ar_edges (bucket, operator).  Returns (total, op_finish,
+    ar_start, ar_finish)."""
+    lib = _lib.load()
+    n, nt, nb = len(op_time), len(tensor_producer), len(buckets)
+
+    def arr(ctype, xs):
+        return (ctype * max(1, len(xs)))(*xs)
+
+    keep = [arr(C.c_double, [float(x) for x in op_time]), arr(C.c_int32, [int(a) for a, _ in edges]),
+            arr(C.c_int32, [int(b) for _, b in edges]), arr(C.c_int32, [int(x) for x in tensor_producer]),
+            arr(C.c_double, [float(x) for x in tensor_bytes])]
+    bounds = [0]
+    flat = []
+    for bk in buckets:
+        flat += [int(x) for x in bk]
+        bounds.append(len(flat))
+    keep += [arr(C.c_int32, bounds), arr(C.c_int32, flat), arr(C.c_int32, [int(b) for b, _ in ar_edges]),
+             arr(C.c_int32, [int(t) for _, t in ar_edges])]
+    pr = _lib.SimProblem(n, C.cast(keep[0], C.c_void_p), len(edges), C.cast(keep[1], C.c_void_p),
+                         C.cast(keep[2], C.c_void_p), nt, C.cast(keep[3], C.c_void_p), C.cast(keep[4], C.c_void_p),
+                         nb, C.cast(keep[5], C.c_void_p), C.cast(keep[6], C.c_void_p), float(c), float(d),
+                         len(ar_edges), C.cast(keep[7], C.c_void_p), C.cast(keep[8], C.c_void_p))
+    total = C.c_double()
+    fin, s0, f0 = (C.c_double * max(1, n))(), (C.c_double * max(1, nb))(), (C.c_double * max(1, nb))()
+    _lib.check(lib.fg_simulate(C.byref(pr), C.byref(total), fin, s0, f0))
+    return total.value, list(fin)[:n], list(s0)[:nb], list(f0)[:nb]

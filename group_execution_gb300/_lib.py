@@ -75,6 +75,7 @@ SIGNATURES = {
     "fg_partition_query": (_I32, [_P, _P, _P, _P]),
     "fg_build_from_partition": (_I32, [_P, _P]),
     "fg_partition_destroy": (None, [_P]),
+    "fg_simulate": (_I32, [_P, _P, _P, _P, _P]),
     "tf_plan_threshold": (_I32, [_I32, _P, _I32, _I64, _I64, _P, _P]),
     "tf_buckets_merge": (_I32, [_P, _P, _I32]),
     "tf_pack_range": (_I32, [_P, _I32, _I32, _F, _P, _P]),
@@ -111,6 +112,16 @@ def load(build_if_needed=True):
             fn.argtypes = args
         _handle = lib
         return lib
+
+
+class SimProblem(C.Structure):
+    """fg_sim_problem of groupexec.h."""
+    _fields_ = [("n_ops", C.c_int32), ("op_time", C.c_void_p), ("n_edges", C.c_int32),
+                ("edge_src", C.c_void_p), ("edge_dst", C.c_void_p), ("n_tensors", C.c_int32),
+                ("tensor_producer", C.c_void_p), ("tensor_bytes", C.c_void_p), ("n_buckets", C.c_int32),
+                ("bucket_bounds", C.c_void_p), ("bucket_tensors", C.c_void_p), ("ar_c", C.c_double),
+                ("ar_d", C.c_double), ("n_ar_edges", C.c_int32), ("ar_edge_bucket", C.c_void_p),
+                ("ar_edge_op", C.c_void_p)]
 
 
 def check(status):

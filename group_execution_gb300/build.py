@@ -65,7 +65,7 @@ def _cmd(src, obj, cuda):
     if src.endswith(".cu"):
         return [os.path.join(cuda, "bin", "nvcc"), *ARCH, "-O3", "-lineinfo", "-std=c++17",
                 "-Xcompiler", "-fPIC", "-Xptxas", "-warn-spills", *inc, "-c", src, "-o", obj]
-    return ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", *inc, "-c", src, "-o", obj]
+    return ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-ffp-contract=off", *inc, "-c", src, "-o", obj]
 
 
 def stale():

@@ -275,6 +275,45 @@ fg_status fg_build_from_partition(const fg_partition* p, fg_plan** plan);
 
 void fg_partition_destroy(fg_partition* p);
 
+/* ---- training-step simulator ----------------------------------------------
+ * DisCo, Simulator: computation operators (e.g. the groups of a plan, with
+ * measured times) run one at a time from a FIFO ready queue: the queue
+ * starts with the operators without dependencies in index order, and an
+ * operator joins its tail when its last dependency clears (successors in
+ * index order).  AllReduce instructions (one per bucket of gradient tensors)
+ * run on one channel in the order their buckets are complete (ties in bucket
+ * order), each once every tensor it carries is produced and the channel is
+ * free, overlapping with computation; one of x bytes takes ar_c * x + ar_d
+ * (DisCo, Profiler; a ring over N devices with narrowest link bandwidth B has
+ * ar_c = 2(N-1)/(B*N)).  An operator may wait for AllReduces (ar edges): it
+ * joins the queue once they are scheduled and starts at their completion at
+ * the earliest.  All arrays are host and caller-owned; times and bytes in the
+ * caller's units. */
+typedef struct {
+  int32_t n_ops;
+  const double* op_time;            /* [n_ops] */
+  int32_t n_edges;
+  const int32_t* edge_src;          /* [n_edges] operator edge_src[e] before edge_dst[e] */
+  const int32_t* edge_dst;
+  int32_t n_tensors;
+  const int32_t* tensor_producer;   /* [n_tensors] operator that produces each gradient tensor */
+  const double* tensor_bytes;       /* [n_tensors] */
+  int32_t n_buckets;
+  const int32_t* bucket_bounds;     /* [n_buckets + 1] ranges of bucket_tensors */
+  const int32_t* bucket_tensors;    /* tensor ids, bucket after bucket */
+  double ar_c, ar_d;
+  int32_t n_ar_edges;
+  const int32_t* ar_edge_bucket;    /* [n_ar_edges] operator ar_edge_op[e] waits for bucket ar_edge_bucket[e] */
+  const int32_t* ar_edge_op;
+} fg_sim_problem;
+
+/* *total: the time the last operator or AllReduce completes; op_finish
+ * [n_ops], ar_start / ar_finish [n_buckets]: optional outputs (NULL to skip).
+ * FG_EINVAL on out-of-range ids, bad bounds or a dependency cycle.  Host
+ * only. */
+fg_status fg_simulate(const fg_sim_problem* p, double* total, double* op_finish, double* ar_start,
+                      double* ar_finish);
+
 /* ---- tensor fusion ------------------------------------------------------- */
 
 /* Layout of n float32 gradient tensors (device pointers grads[i], numel[i]

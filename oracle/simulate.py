@@ -21,6 +21,8 @@ operator may also wait for AllReduces (a parameter update reading the
 aggregated gradient): it joins the queue once those AllReduces are
 scheduled and starts no earlier than their completion;
 AllReduces whose tensors are complete at the same time go in bucket order;
+a bucket's bytes are its tensors' bytes added in bucket order and its time
+is (start + C*bytes) + D in double precision, one rounding per operation;
 the iteration ends when the last operator or AllReduce completes.
 """
 from __future__ import annotations
@@ -75,7 +77,10 @@ def simulate(op_time, edges, tensor_producer, tensor_bytes, buckets, c, d, ar_ed
         while complete_buckets and complete_buckets[0][0] <= upto:
             t, b = complete_buckets.pop(0)
             ar_start[b] = max(t, channel)
-            ar_finish[b] = ar_start[b] + c * sum(tensor_bytes[x] for x in buckets[b]) + d
+            x = 0.0
+            for t_ in buckets[b]:              # the bucket's bytes, added in bucket order
+                x += tensor_bytes[t_]
+            ar_finish[b] = ar_start[b] + c * x + d
             channel = ar_finish[b]
             for r in sorted(readers[b]):
                 pending[r] -= 1

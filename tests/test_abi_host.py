@@ -276,3 +276,38 @@ def test_opaque_operators_stay_alone():
     part = graph_from_spec(g).partition(from_fuseops=False)
     with pytest.raises(FgError):
         part.fuse(1, 0, False)
+
+
+# ---- training-step simulator (host side of the C ABI) ------------------------
+def test_simulate_matches_oracle():
+    import numpy as np
+    from oracle import simulate as OS
+    from group_execution_gb300 import simulate
+    for seed in range(300):
+        r = np.random.default_rng(seed)
+        n = int(r.integers(1, 40))
+        edges = sorted({(int(a), int(b)) for a, b in r.integers(0, n, size=(2 * n, 2)) if a < b})
+        times = r.uniform(0.1, 3.0, size=n).tolist()
+        nt = int(r.integers(0, 20))
+        prod = r.integers(0, n, size=nt).tolist()
+        by = r.uniform(1, 1e6, size=nt).tolist()
+        order = r.permutation(nt).tolist()
+        cuts = sorted(set(r.integers(0, nt + 1, size=4).tolist()) | {0, nt})
+        buckets = [order[a:b] for a, b in zip(cuts, cuts[1:]) if b > a]
+        ar_edges = [(int(b), int(t)) for b, t in zip(r.integers(0, max(1, len(buckets)), size=3),
+                                                       r.integers(0, n, size=3))
+                    if len(buckets) and all(prod[x] < t for x in buckets[int(b)])]
+        c, d = float(r.uniform(1e-7, 1e-5)), float(r.uniform(0, 1))
+        got = simulate(times, edges, prod, by, buckets, c, d, ar_edges)
+        ref = OS.simulate(times, edges, prod, by, buckets, c, d, ar_edges)
+        assert got[0] == ref[0] and got[1] == ref[1] and got[2] == ref[2] and got[3] == ref[3], seed
+
+
+def test_simulate_rejects_cycles_and_bad_ids():
+    from group_execution_gb300 import simulate
+    with pytest.raises(FgError):
+        simulate([1, 1], [(0, 1), (1, 0)], [], [], [], 0.0, 0.0)
+    with pytest.raises(FgError):
+        simulate([1], [(0, 3)], [], [], [], 0.0, 0.0)
+    with pytest.raises(FgError):
+        simulate([1], [], [2], [1.0], [[0]], 0.0, 0.0)
