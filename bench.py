@@ -523,6 +523,53 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
         "bucket_bytes": [e - s for s, e in tf.bucket_ranges(bounds)],
         "note": "pack_us/unpack_us: one host launch per bucket; graph_*: the launches replayed from a CUDA graph"}
 
+    # training-step simulator fed by measured group times: a backward pass of
+    # 161 gradient computations (g_i = 0.5 * relu(x_i) over the gradient set's
+    # sizes, one group each, run in production order), every group timed on
+    # this GPU, then the step simulated with AllReduce buckets of the bf16
+    # gradients for several fusion thresholds on an 8-GPU ring (900 GB/s per
+    # link direction; 20 us of per-AllReduce overhead: assumed, the pages
+    # give none)
+    from group_execution_gb300 import simulate
+    bsp = W.GraphSpec("backward")
+    grads = []
+    for n_i in sizes:
+        x_i = bsp.input((int(n_i),))
+        grads.append(bsp.op("scale", (bsp.op("relu", (x_i,)),), (0.5,)))
+        bsp.mark_output(grads[-1])
+    bplan = graph_from_spec(bsp).build()
+    be = {}
+    for v in bsp.values:
+        be[v.vid] = torch.empty(v.shape, device="cuda").uniform_(-1, 1) if v.is_input else torch.empty(v.shape, device="cuda")
+    op_time = []
+    for gid, gi in enumerate(bplan.groups):
+        # device time per launch: 20 launches of the group replayed from one
+        # CUDA graph (no host work between them)
+        ptrs = {v: be[v] for v in gi.leaves + gi.outs}
+        rep = graphed(lambda gid=gid, ptrs=ptrs: [bplan.launch_group(gid, ptrs) for _ in range(20)])
+        med, _ = timed(rep, reps=3, flush=False)
+        op_time.append(med * 1e-3 / 20)
+    edges = [(k, k + 1) for k in range(len(op_time) - 1)]
+    gbytes = [int(n_i) * 2 for n_i in sizes]
+    c_ring = 2.0 * 7 / (900e9 * 8)
+    sim = {}
+    t0 = time.perf_counter()
+    nsim = 0
+    for thr in (0, 1 << 20, 4 << 20, 16 << 20, 1 << 40):
+        bb = plan_threshold(list(sizes), thr)
+        buckets = [list(range(bb[k], bb[k + 1])) for k in range(len(bb) - 1)]
+        tot, *_ = simulate(op_time, edges, list(range(len(sizes))), gbytes, buckets, c_ring, 20e-6)
+        nsim += 1
+        sim["threshold_" + ("inf" if thr >= 1 << 40 else str(thr))] = {"buckets": len(buckets), "step_us": tot * 1e6}
+    host_us = (time.perf_counter() - t0) / nsim * 1e6
+    rows["simulated_step_backward161"] = {
+        "compute_us": sum(op_time) * 1e6, "groups": len(op_time), "strategies": sim,
+        "best": min(sim, key=lambda k: sim[k]["step_us"]), "host_us_per_simulation": host_us,
+        "note": "op times: device time per launch of each group on this GPU (CUDA graph of 20 launches, CUDA "
+                "events); AllReduce model T = 2(N-1)x/(B N) + D, "
+                "N = 8, B = 900 GB/s, D = 20 us (assumed)"}
+    del be
+
     # sufficient-factor gradient + update: one tcgen05 GEMM-epilogue group
     for B, label in ((512, "sf_update_K512"), (4096, "sf_update_K4096_compute_bound_variant")):
         sp = W.sf_update(B, 4096, 4096)
