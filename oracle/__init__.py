@@ -27,6 +27,8 @@ out from the passages they cite:
                    Strategy Maker, method (iii)).
 * ``explicit``  -- explicit fusion moves: non-duplicate and duplicate fusion
                    of an operator with a predecessor (DisCo, Introduction).
+* ``patterns``  -- pattern-based grouping: priority-ordered operator chains
+                   with a private-intermediate check (TVM, FuseOpsByPattern).
 * ``simulate``  -- the training-step simulator: ready queue, in-order
                    AllReduce channel, linear AllReduce time (DisCo,
                    Simulator and Profiler).
@@ -36,4 +38,4 @@ Parity status: every function here is pinned by tests under ``tests/``
 pages or library routines, except the long random-DAG numerics, which only the
 oracle itself defines ("parity unpinned" beyond per-op pins).
 """
-from . import kinds, postdom, partition, execute, pack, buckets, explicit, simulate  # noqa: F401
+from . import kinds, postdom, partition, execute, pack, buckets, explicit, patterns, simulate  # noqa: F401
