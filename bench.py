@@ -484,6 +484,30 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
     rows["diamond_with_P_output"] = row
     del e
 
+    # an MLP layer grouped by pattern (FuseOpsByPattern with the page's matmul +
+    # bias pattern extended by relu): Y = relu(X W + b), X [4096, 4096],
+    # W [4096, 4096] bf16, one GEMM-epilogue group
+    msp = W.GraphSpec("mlp")
+    mx = msp.input((4096, 4096), "bf16")
+    mw = msp.input((4096, 4096), "bf16")
+    mb = msp.input((4096,))
+    my = msp.op("relu", (msp.op("badd_col", (msp.op("matmul_bf16", (mx, mw), (0, 0)), mb)),))
+    msp.mark_output(my)
+    mpart = graph_from_spec(msp).partition(patterns=[("matmul_bias_relu", ["matmul_bf16", "badd_col", "relu"], True)])
+    mplan = mpart.build()
+    gen = torch.Generator(device="cuda").manual_seed(1)
+    me = {mx: torch.empty((4096, 4096), device="cuda").normal_(generator=gen).to(torch.bfloat16),
+          mw: torch.empty((4096, 4096), device="cuda").normal_(generator=gen).to(torch.bfloat16),
+          mb: torch.empty((4096,), device="cuda").uniform_(-1, 1, generator=gen),
+          my: torch.empty((4096, 4096), device="cuda")}
+    mgi = mplan.groups[0]
+    med, _ = timed(lambda: mplan.launch_group(0, {v: me[v] for v in mgi.leaves + mgi.outs}))
+    rows["mlp_layer_pattern_4096"] = {
+        "groups": mplan.n_groups, "match_of": mpart.match_of, "us": med * 1e3,
+        "TFLOPs": mgi.alg_flops / (med * 1e-3) / 1e12, "frac_of_bf16_peak": mgi.alg_flops / (med * 1e-3) / 1e12 / bf16,
+        "note": "L2 flushed between runs"}
+    del me
+
     # tensor-fusion pack / unpack
     from group_execution_gb300 import TensorFusion
     sizes = W.tensor_fusion_sizes(0)

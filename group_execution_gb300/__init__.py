@@ -77,9 +77,11 @@ class Graph:
         return Plan(self, max_fused_ops, max_args, allow_reduce_epilogue, wait_limit_ns, flags)
 
     def partition(self, from_fuseops=True, max_fused_ops=256, max_args=64, allow_reduce_epilogue=False,
-                  wait_limit_ns=2_000_000_000, flags=0):
-        """An explicit partition to change with fusion moves (Partition.fuse)."""
-        return Partition(self, from_fuseops, max_fused_ops, max_args, allow_reduce_epilogue, wait_limit_ns, flags)
+                  wait_limit_ns=2_000_000_000, flags=0, patterns=None):
+        """An explicit partition to change with fusion moves (Partition.fuse),
+        from the FuseOps grouping, singletons, or operator-chain patterns."""
+        return Partition(self, from_fuseops, max_fused_ops, max_args, allow_reduce_epilogue, wait_limit_ns, flags,
+                         patterns)
 
 
 def _opts(lib, max_fused_ops, max_args, allow_reduce_epilogue, wait_limit_ns, flags):
@@ -97,12 +99,26 @@ class Partition:
     predecessors, by duplicate or non-duplicate fusion)."""
 
     def __init__(self, graph, from_fuseops=True, max_fused_ops=256, max_args=64, allow_reduce_epilogue=False,
-                 wait_limit_ns=2_000_000_000, flags=0):
+                 wait_limit_ns=2_000_000_000, flags=0, patterns=None):
+        """patterns: list of (name, [op names], private) in priority order
+        (FuseOpsByPattern); then from_fuseops is ignored and match_of lists
+        the pattern index per operator."""
         self.lib = graph.lib
         self.graph = graph
         o = _opts(self.lib, max_fused_ops, max_args, allow_reduce_epilogue, wait_limit_ns, flags)
         self.h = C.c_void_p()
-        _lib.check(self.lib.fg_partition_create(graph.h, C.byref(o), int(bool(from_fuseops)), C.byref(self.h)))
+        self.match_of = None
+        if patterns is None:
+            _lib.check(self.lib.fg_partition_create(graph.h, C.byref(o), int(bool(from_fuseops)), C.byref(self.h)))
+        else:
+            codes = [(C.c_int32 * len(ch))(*[OPCODES[x] for x in ch]) for _, ch, _ in patterns]
+            arr = (_lib.Pattern * max(1, len(patterns)))(
+                *[_lib.Pattern(len(ch), C.cast(cd, C.c_void_p), int(bool(pv))) for (_, ch, pv), cd in zip(patterns, codes)])
+            mo = (C.c_int32 * max(1, len(graph.shapes)))()
+            _lib.check(self.lib.fg_partition_from_patterns(graph.h, C.byref(o), len(patterns), arr, C.byref(self.h), mo))
+            n = C.c_int32()
+            _lib.check(self.lib.fg_partition_query(self.h, C.byref(n), None, None))
+            self.match_of = list(mo)[:n.value]
 
     def __del__(self):
         h = getattr(self, "h", None)

@@ -72,6 +72,7 @@ SIGNATURES = {
     "fg_plan_group_outputs": (_I32, [_P, _I32, _P, _P]),
     "fg_partition_create": (_I32, [_P, _P, _I32, _P]),
     "fg_partition_fuse": (_I32, [_P, _I32, _I32, _I32]),
+    "fg_partition_from_patterns": (_I32, [_P, _P, _I32, _P, _P, _P]),
     "fg_partition_query": (_I32, [_P, _P, _P, _P]),
     "fg_build_from_partition": (_I32, [_P, _P]),
     "fg_partition_destroy": (None, [_P]),
@@ -112,6 +113,11 @@ def load(build_if_needed=True):
             fn.argtypes = args
         _handle = lib
         return lib
+
+
+class Pattern(C.Structure):
+    """fg_pattern of groupexec.h."""
+    _fields_ = [("n_ops", C.c_int32), ("opcodes", C.c_void_p), ("private_intermediates", C.c_int32)]
 
 
 class SimProblem(C.Structure):

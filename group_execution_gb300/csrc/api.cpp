@@ -822,10 +822,10 @@ fg_status fg_partition_create(const fg_graph* gh, const fg_build_opts* opts, int
   return FG_OK;
 }
 
-fg_status fg_partition_fuse(fg_partition* p, int32_t node, int32_t pred, int32_t duplicate) {
-  if (!p) return err(FG_EINVAL, "null partition");
-  const BuildOpts o = p->opts;
-  const GroupCheck check = [&o](const Graph& g, const std::vector<int32_t>& nodes) {
+namespace {
+// A fused group must run as one kernel within the build options' bounds.
+GroupCheck executable(const BuildOpts& o) {
+  return [o](const Graph& g, const std::vector<int32_t>& nodes) {
     // an opaque operator stays alone (TVM "Operator Fusion", Operator Pattern
     // Classification: opaque operators are not fused)
     if (nodes.size() > 1)
@@ -835,12 +835,41 @@ fg_status fg_partition_fuse(fg_partition* p, int32_t node, int32_t pred, int32_t
     if (ge.compile_status != FG_OK) throw CompileError{ge.compile_status, ge.compile_error};
     const int args = (int)(ge.cg.leaf_values.size() + ge.cg.epi_leaf_values.size() + 1 + ge.cg.xout_values.size());
     if (args > o.max_args) throw CompileError{FG_EUNSUPPORTED, "the fused group exceeds max_args"};
+    if ((int)nodes.size() > o.max_fused_ops) throw CompileError{FG_EUNSUPPORTED, "the fused group exceeds max_fused_ops"};
   };
+}
+}  // namespace
+
+fg_status fg_partition_fuse(fg_partition* p, int32_t node, int32_t pred, int32_t duplicate) {
+  if (!p) return err(FG_EINVAL, "null partition");
   try {
-    fuse_move(p->P, node, pred, duplicate != 0, check);
+    fuse_move(p->P, node, pred, duplicate != 0, executable(p->opts));
   } catch (const CompileError& e) {
     return err(e.st, e.msg);
   }
+  return FG_OK;
+}
+
+fg_status fg_partition_from_patterns(const fg_graph* gh, const fg_build_opts* opts, int32_t n_patterns,
+                                     const fg_pattern* patterns, fg_partition** out, int32_t* match_of) {
+  if (!gh || !out || (n_patterns > 0 && !patterns) || n_patterns < 0) return err(FG_EINVAL, "null argument");
+  *out = nullptr;
+  BuildOpts o;
+  if (fg_status st = build_opts_from(opts, o)) return st;
+  if (gh->g.nodes.empty()) return err(FG_EINVAL, "graph has no operators");
+  std::vector<ChainPattern> pats(n_patterns);
+  for (int k = 0; k < n_patterns; ++k) {
+    if (patterns[k].n_ops < 1 || !patterns[k].opcodes) return err(FG_EINVAL, "a pattern needs at least one operator");
+    pats[k].ops.assign(patterns[k].opcodes, patterns[k].opcodes + patterns[k].n_ops);
+    pats[k].private_intermediates = patterns[k].private_intermediates != 0;
+  }
+  std::unique_ptr<fg_partition> p(new (std::nothrow) fg_partition());
+  if (!p) return err(FG_ENOMEM, "out of host memory");
+  p->opts = o;
+  std::vector<int32_t> mo;
+  p->P = pattern_partition(gh->g, o, pats, executable(o), mo);
+  if (match_of) std::copy(mo.begin(), mo.end(), match_of);
+  *out = p.release();
   return FG_OK;
 }
 

@@ -143,5 +143,12 @@ Partition singleton_partition(const Graph& g, const BuildOpts& o);
 void fuse_move(Partition& P, int32_t node, int32_t pred, bool duplicate, const GroupCheck& check);
 // Node lists of the groups in an order that respects their dependencies.
 std::vector<std::vector<int32_t>> partition_groups(const Partition& P);
+// Pattern-based grouping: chains of operators in priority order.
+struct ChainPattern {
+  std::vector<int32_t> ops;        // opcodes; ops[k+1] reads ops[k]'s output
+  bool private_intermediates = false;
+};
+Partition pattern_partition(const Graph& g, const BuildOpts& o, const std::vector<ChainPattern>& pats,
+                            const GroupCheck& check, std::vector<int32_t>& match_of);
 
 }  // namespace fg

@@ -166,4 +166,66 @@ std::vector<std::vector<int32_t>> partition_groups(const Partition& P) {
   return out;
 }
 
+// Pattern-based grouping (TVM "Operator Fusion", FuseOpsByPattern): anchors
+// in node order, patterns in priority order at each anchor; a chain's next
+// operator is the smallest-numbered untaken reader of the previous output
+// with the pattern's operator; a match must be convex, pass the private
+// check when asked (no intermediate result read outside it or returned) and
+// run as one kernel; everything else stays alone.
+Partition pattern_partition(const Graph& g, const BuildOpts& o, const std::vector<ChainPattern>& pats,
+                            const GroupCheck& check, std::vector<int32_t>& match_of) {
+  Partition P = singleton_partition(g, o);
+  const int n = (int)g.nodes.size();
+  const auto cons = consumers_of(g);
+  std::vector<char> taken(n, 0);
+  match_of.assign(n, -1);
+  for (int anchor = 0; anchor < n; ++anchor) {
+    if (taken[anchor]) continue;
+    for (size_t k = 0; k < pats.size(); ++k) {
+      const ChainPattern& pt = pats[k];
+      if (pt.ops.empty() || g.nodes[anchor].op != pt.ops[0]) continue;
+      std::vector<int32_t> chain{anchor};
+      for (size_t j = 1; j < pt.ops.size() && !chain.empty(); ++j) {
+        int next = -1;
+        for (int32_t r : cons[g.nodes[chain.back()].value])   // readers in node order
+          if (!taken[r] && g.nodes[r].op == pt.ops[j] && std::find(chain.begin(), chain.end(), r) == chain.end()) {
+            next = r;
+            break;
+          }
+        if (next < 0) chain.clear();
+        else chain.push_back(next);
+      }
+      if (chain.empty()) continue;
+      std::vector<char> in(n, 0);
+      for (int32_t x : chain) in[x] = 1;
+      if (!convex(g, in)) continue;
+      if (pt.private_intermediates) {
+        bool ok = true;
+        for (size_t j = 0; j + 1 < chain.size() && ok; ++j) {
+          const int32_t v = g.nodes[chain[j]].value;
+          if (g.is_output[v]) ok = false;
+          for (int32_t r : cons[v])
+            if (!in[r]) ok = false;
+        }
+        if (!ok) continue;
+      }
+      if (chain.size() > 1) {
+        try {
+          check(g, chain);
+        } catch (const CompileError&) {
+          continue;
+        }
+      }
+      const int32_t lab = *std::min_element(chain.begin(), chain.end());
+      for (int32_t x : chain) {
+        taken[x] = 1;
+        match_of[x] = (int32_t)k;
+        P.label[x] = lab;
+      }
+      break;
+    }
+  }
+  return P;
+}
+
 }  // namespace fg

@@ -260,6 +260,27 @@ fg_status fg_partition_create(const fg_graph* g, const fg_build_opts* opts, int3
  * unchanged. */
 fg_status fg_partition_fuse(fg_partition* p, int32_t node, int32_t pred, int32_t duplicate);
 
+/* Pattern-based grouping (TVM "Operator Fusion", FuseOpsByPattern): the
+ * caller names which operator combinations form groups.  A pattern is a chain
+ * of operators, each reading the previous one's output (as any operand; other
+ * operands are wildcards).  Anchors are tried in node order and, at each, the
+ * patterns in the given (priority) order; the chain's next operator is the
+ * smallest-numbered reader of the previous output with the pattern's opcode
+ * that no earlier match took.  A match is kept only if it is convex, passes
+ * the private check when private_intermediates = 1 (no intermediate result
+ * read outside the match or marked as a graph output) and runs as one kernel
+ * (as fg_partition_fuse checks); every other operator stays alone.  The
+ * partition can then be changed with fg_partition_fuse and built with
+ * fg_build_from_partition.  match_of: host, caller-owned, one entry per
+ * operator (the pattern index, or -1), or NULL. */
+typedef struct {
+  int32_t n_ops;
+  const int32_t* opcodes;           /* fg_opcode values, chain order */
+  int32_t private_intermediates;
+} fg_pattern;
+fg_status fg_partition_from_patterns(const fg_graph* g, const fg_build_opts* opts, int32_t n_patterns,
+                                     const fg_pattern* patterns, fg_partition** out, int32_t* match_of);
+
 /* n_nodes: operators including copies; group_of[i]: the group's smallest node
  * id; clone_of[i]: the operator node i copies, -1 for originals.  Arrays are
  * host, caller-owned, n_nodes entries, or NULL. */

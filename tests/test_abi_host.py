@@ -311,3 +311,47 @@ def test_simulate_rejects_cycles_and_bad_ids():
         simulate([1], [(0, 3)], [], [], [], 0.0, 0.0)
     with pytest.raises(FgError):
         simulate([1], [], [2], [1.0], [[0]], 0.0, 0.0)
+
+
+# ---- pattern-based grouping (host side of the C ABI) -------------------------
+def _labels(groups, n):
+    lab = [0] * n
+    for g in groups:
+        for x in g:
+            lab[x] = min(g)
+    return lab
+
+
+def test_patterns_match_oracle():
+    import numpy as np
+    from oracle import patterns as PT
+    from tests._helpers import small_dags, dag_to_spec
+    pats = [("a", ["relu", "add"], True), ("b", ["add", "mul"], False), ("c", ["transpose", "relu"], True),
+            ("d", ["relu", "relu"], False), ("e", ["mul", "relu", "add"], False)]
+    for k, (n, preds) in enumerate(small_dags(9, seed=31, count=200)):
+        r = np.random.default_rng(k)
+        spec = dag_to_spec(n, preds, op_choice=[int(x) for x in r.integers(0, 2, size=n)], outputs=[n - 1])
+        order = r.permutation(len(pats)).tolist()
+        use = [pats[i] for i in order[:int(r.integers(1, len(pats) + 1))]]
+        groups, mo = PT.match(spec, use)
+        part = graph_from_spec(spec).partition(patterns=use)
+        assert part.match_of == mo, k
+        assert part.query()[0] == _labels(groups, n), k
+
+
+def test_page_pattern_matmul_bias():
+    from oracle import patterns as PT
+    g = W.GraphSpec()
+    x = g.input((256, 128), "bf16")
+    w = g.input((128, 512), "bf16")
+    b = g.input((512,))
+    m = g.op("matmul_bf16", (x, w), (0, 0))
+    a = g.op("badd_col", (m, b))
+    rl = g.op("relu", (a,))
+    g.mark_output(rl)
+    pats = [("cutlass.matmul_bias", ["matmul_bf16", "badd_col"], True)]
+    part = graph_from_spec(g).partition(patterns=pats)
+    assert part.match_of == PT.match(g, pats)[1] == [0, 0, -1]
+    plan = part.build()
+    assert [sorted(gi.nodes) for gi in plan.groups] == [[0, 1], [2]]
+    assert plan.groups[0].kind == "gemm"

@@ -123,3 +123,37 @@ def test_random_moves(seed):
         st = nxt
         moves.append(mv)
     _run_moves(spec, moves, from_fuseops=bool(seed % 2), seed=seed)
+
+
+def _mlp_spec(M, K, N):
+    g = W.GraphSpec()
+    x = g.input((M, K), "bf16")
+    w = g.input((K, N), "bf16")
+    b = g.input((N,))
+    m = g.op("matmul_bf16", (x, w), (0, 0))
+    a = g.op("badd_col", (m, b))
+    r = g.op("relu", (a,))
+    s = g.op("scale", (r,), (0.5,))
+    g.mark_output(s)
+    return g
+
+
+@pytest.mark.parametrize("shape", [(256, 128, 512), (200, 72, 264)])
+def test_pattern_plan_matmul_bias_relu(shape):
+    """FuseOpsByPattern with the page's matmul + bias pattern extended by relu:
+    the match runs as one GEMM-epilogue group, the scale alone."""
+    from oracle import patterns as PT
+    spec = _mlp_spec(*shape)
+    pats = [("matmul_bias_relu", ["matmul_bf16", "badd_col", "relu"], True)]
+    part = graph_from_spec(spec).partition(patterns=pats)
+    assert part.match_of == PT.match(spec, pats)[1] == [0, 0, 0, -1]
+    plan = part.build()
+    assert [sorted(gi.nodes) for gi in plan.groups] == [[0, 1, 2], [3]]
+    ins = W.make_inputs(spec, 0)
+    dev = {vid: to_dev(spec, vid, a) for vid, a in ins.items()}
+    env = run_fused(plan, spec, dev)
+    plan.sync()
+    ref = OE.run_unfused(spec, ins, keep=[v.vid for v in spec.ops])
+    for gi in plan.groups:
+        for o in gi.outs:
+            assert rel_err(env[o].cpu().numpy(), ref[o]) <= 1e-4
