@@ -499,9 +499,24 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
   ge.big = cg.depth > 4 || cg.slots > 4;
   ge.compiled = !(o.flags & FG_FLAG_INTERPRET);
   ge.min_blocks = 1;
-  // CTA pairs walk 256-row tile units; one CTA per SM
+  // CTA pairs walk 256-row tile units; one CTA per SM (flag bits 8-15, when
+  // set, cap the number of pairs: a test hook for the split tail)
   const int units = ((p.ntm + kGemmCluster - 1) / kGemmCluster) * p.ntn;
-  ge.grid = kGemmCluster * std::max(1, std::min(units, nsm / kGemmCluster));
+  int pairs = std::max(1, std::min(units, nsm / kGemmCluster));
+  const int cap = (o.flags >> 8) & 0xff;
+  if (cap > 0) pairs = std::min(pairs, cap);
+  ge.grid = kGemmCluster * pairs;
+  // split the last round's units along K into halves over the pairs it would
+  // leave idle, when K is long enough for the halves to outweigh the partial
+  // sums' traffic (two pieces: their sum does not depend on which ends last)
+  const int nslots = (p.nkb + kGemmKB - 1) / kGemmKB;
+  const int tail = units % pairs;
+  p.nfull = units;
+  p.split = 1;
+  if (units > pairs && tail > 0 && 2 * tail <= pairs && nslots >= 8) {
+    p.nfull = units - tail;
+    p.split = 2;
+  }
 }
 
 GroupExec make_exec(const Graph& g, const std::vector<int32_t>& nodes, const BuildOpts& o, int nsm) {
@@ -528,7 +543,22 @@ GroupExec make_exec(const Graph& g, const std::vector<int32_t>& nodes, const Bui
 }
 
 fg_status alloc_device(fg_plan* p, GroupExec& ge) {
-  if (ge.compile_status == FG_OK && ge.mp) ge.mp->err = p->d_err;
+  if (ge.compile_status == FG_OK && ge.mp) {
+    GemmParams& mp = *ge.mp;
+    mp.err = p->d_err;
+    if (mp.split > 1) {
+      const int units = ((mp.ntm + kGemmCluster - 1) / kGemmCluster) * mp.ntn;
+      const size_t tail = (size_t)(units - mp.nfull);
+      cudaError_t e = cudaMalloc(&ge.scratch, sizeof(float) * tail * mp.split * kGemmCluster * kGemmM * kGemmN);
+      if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(split-tail workspace)");
+      e = cudaMalloc(&ge.counters, sizeof(int32_t) * tail * kGemmCluster * 4);
+      if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(split-tail counters)");
+      e = cudaMemset(ge.counters, 0, sizeof(int32_t) * tail * kGemmCluster * 4);
+      if (e != cudaSuccess) return cuda_err(e, "cudaMemset(split-tail counters)");
+      mp.ws = ge.scratch;
+      mp.ws_cnt = ge.counters;
+    }
+  }
   if (ge.compile_status != FG_OK || !ge.gp) return FG_OK;
   GroupParams& gp = *ge.gp;
   gp.err = p->d_err;

@@ -178,6 +178,13 @@ struct GemmParams {
   int32_t epi_stage_bytes, epi_tx_bytes, n_epi_bufs;
   int32_t inplace_off;                 // >= 0: the result overwrites this IDENT leaf's chunk (no out buffers)
   int32_t inject;                      // failure injection: 1 = the producers issue no loads
+  // the last round's tiles split along K: tile units [0, nfull) run whole;
+  // each later unit runs as split = 2 pieces (pieces 2u, 2u+1) whose partial
+  // accumulators meet in the workspace, where the piece that finishes second
+  // adds the other's and runs the epilogue
+  int32_t nfull, split;
+  float* ws;                           // [pieces][2 CTAs][64 column quads][128 rows][4] partial accumulators
+  int32_t* ws_cnt;                     // [split units][2 CTAs][4 warps] arrival counters (reset by the last)
 };
 
 // Loads already issued always land; waiting for them before a CTA exits uses

@@ -150,6 +150,29 @@ __device__ __forceinline__ bool gemm_wait(uint32_t bar, uint32_t parity, int64_t
   return true;
 }
 
+// One item of a pair's work list: a whole tile unit, or one K piece (ring
+// slots [sl0, sl1)) of a unit of the split last round.
+struct GemmItem {
+  int unit, piece, sl0, sl1, q;   // piece = -1 for a whole unit; q = index among all pieces
+};
+__device__ __forceinline__ GemmItem gemm_item(const GemmParams& P, int idx, int nslots) {
+  GemmItem w;
+  if (idx < P.nfull) {
+    w.unit = idx;
+    w.piece = -1;
+    w.sl0 = 0;
+    w.sl1 = nslots;
+    w.q = -1;
+  } else {
+    w.q = idx - P.nfull;
+    w.unit = P.nfull + w.q / P.split;
+    w.piece = w.q % P.split;
+    w.sl0 = w.piece * nslots / P.split;
+    w.sl1 = (w.piece + 1) * nslots / P.split;
+  }
+  return w;
+}
+
 // CL = 2: a CTA pair per 256 x 256 tile (cta_group::2), each CTA holding
 // half of A's rows and half of B's columns.
 template <class Epi, int CL>
@@ -179,6 +202,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   // tile sequence: units of CL vertically adjacent 128-row tiles
   const int ncl = gridDim.x / CL, cl = blockIdx.x / CL;
   const int npm = (P.ntm + CL - 1) / CL, nunits = npm * P.ntn;
+  const int nitems = P.nfull + (nunits - P.nfull) * P.split;
   auto tile_of = [&](int u, int& m0, int& n0) {
     m0 = ((u / P.ntn) * CL + (int)rank) * kGemmM;
     n0 = (u % P.ntn) * kGemmN;
@@ -219,11 +243,12 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       tma_prefetch(&P.mapB);
       int it = 0;
       bool ok = true;
-      for (int u = cl; u < nunits && ok; u += ncl) {
+      for (int x = cl; x < nitems && ok; x += ncl) {
+        const GemmItem w = gemm_item(P, x, nslots);
         int m0, n0;
-        tile_of(u, m0, n0);
+        tile_of(w.unit, m0, n0);
         const int nb = n0 + (int)rank * kBCols;
-        for (int sl = 0; sl < nslots; ++sl, ++it) {
+        for (int sl = w.sl0; sl < w.sl1; ++sl, ++it) {
           const int s = it % NS;
           if (it >= NS && !gemm_wait(empty0 + 8 * s, ((it / NS) & 1) ^ 1, limit, &abort_flag)) {
             ok = false;
@@ -291,7 +316,8 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       const uint32_t a_step = P.a_mn ? 2048 : 32, b_step = P.b_mn ? 2048 : 32;         // next 16 of K
       int it = 0, i = 0;
       bool ok = true;
-      for (int u = cl; u < nunits && ok; u += ncl, ++i) {
+      for (int x = cl; x < nitems && ok; x += ncl, ++i) {
+        const GemmItem w = gemm_item(P, x, nslots);
         const int b = i & 1;
         if (i >= 2) {
           // both CTAs' epilogues have drained this accumulator buffer
@@ -308,7 +334,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         }
         tc_fence_after();
         const uint32_t d = tmem + b * kGemmN;
-        for (int sl = 0; sl < nslots; ++sl, ++it) {
+        for (int sl = w.sl0; sl < w.sl1; ++sl, ++it) {
           const int s = it % NS;
           if (!gemm_wait(full0 + 8 * s, (it / NS) & 1, limit, &abort_flag)) {
             ok = false;
@@ -324,7 +350,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
             for (int kk = 0; kk < kGemmK / 16; ++kk) {
               const uint64_t ad = smem_desc_sw128(a + j * a_blk + kk * a_step, a_lbo, 1024);
               const uint64_t bd = smem_desc_sw128(bb + j * b_blk + kk * b_step, b_lbo, 1024);
-              tc_mma_bf16<CL>(d, ad, bd, idesc, (kb | kk) != 0);
+              tc_mma_bf16<CL>(d, ad, bd, idesc, (kb != w.sl0 * kGemmKB) || kk != 0);
             }
           }
           tc_commit<CL>(empty0 + 8 * s);   // both CTAs may refill the slot
@@ -346,9 +372,9 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       Epi::prefetch(P);
       int g = 0;
       bool ok = true;
-      for (int u = cl; u < nunits && ok; u += ncl) {
+      for (int x = cl; x < nitems && ok; x += ncl) {
         int m0, n0;
-        tile_of(u, m0, n0);
+        tile_of(gemm_item(P, x, nslots).unit, m0, n0);
         for (int j = 0; j < kGemmChunks; ++j, ++g) {
           const int e = g % NE;
           if (g >= NE && !gemm_wait(eempty0 + 8 * e, ((g / NE) & 1) ^ 1, limit, &abort_flag)) {
@@ -374,38 +400,92 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
 
     int g = 0, i = 0;
     bool dead = false;
-    for (int u = cl; u < nunits; u += ncl, ++i) {
+    for (int x = cl; x < nitems; x += ncl, ++i) {
+      const GemmItem w = gemm_item(P, x, nslots);
       int m0, n0;
-      tile_of(u, m0, n0);
+      tile_of(w.unit, m0, n0);
       const int b = i & 1;
       bool got = gemm_wait(tfull0 + 8 * b, (i >> 1) & 1, limit, &abort_flag);
       tc_fence_after();
+      got = __all_sync(0xffffffffu, got);
+      const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + b * kGemmN;
+      // a piece: its partial accumulator goes to the workspace; the warp that
+      // completes a row block's second piece adds the other and finishes it
+      bool finish = true;
+      if (w.piece >= 0 && got) {
+        // layout [64 column quads][128 rows][4]: a warp's 16-byte accesses
+        // cover 512 contiguous bytes
+        float4* wq = reinterpret_cast<float4*>(P.ws) + (size_t)(w.q * CL + rank) * (kGemmM * kGemmN / 4) + rr;
+#pragma unroll 1
+        for (int j = 0; j < kGemmChunks; ++j) {
+          float acc[32];
+          tmem_ld32(tacc + j * kGemmChunk, acc);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            wq[(size_t)(j * 8 + c) * kGemmM] = make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+        }
+        __threadfence();
+        __syncwarp();
+        int32_t* cnt = P.ws_cnt + ((w.unit - P.nfull) * CL + rank) * 4 + q;
+        int last = 0;
+        if (lane == 0) last = atomicAdd(cnt, 1) == P.split - 1;
+        finish = __shfl_sync(0xffffffffu, last, 0) != 0;
+        if (finish) {
+          __threadfence();
+          if (lane == 0) *cnt = 0;   // every piece has arrived: ready for the next launch
+        }
+      }
       for (int j = 0; j < kGemmChunks; ++j, ++g) {
         const int e = g % NE;
         if (got && staged) got = gemm_wait(efull0 + 8 * e, (g / NE) & 1, limit, &abort_flag);
         // tcgen05.ld is warp-collective: decide per warp
         got = __all_sync(0xffffffffu, got);
-        float acc[32], o[32];
-        if (got) {
-          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + b * kGemmN + j * kGemmChunk, acc);
-          const uint8_t* st = ebuf + e * P.epi_stage_bytes;
-#pragma unroll
-          for (int s8 = 0; s8 < 4; ++s8) {
-            const GemmEnv env{P, st, rr, m0, n0 + j * kGemmChunk, s8 * 8};
-            float a8[8], o8[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) a8[k] = acc[s8 * 8 + k];
-            Epi::run(env, a8, o8);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) o[s8 * 8 + k] = o8[k];
-          }
-        }
-        // this warp's 32 rows x 32 columns go out through its own TMA store:
-        // no barrier across the epilogue warps
         if (!got) {
           dead = true;
           break;
         }
+        if (!finish) {
+          // another piece finishes this row block: only release the leaves
+          if (lane == 0 && staged) {
+            if (inplace) {
+              bulk_wait_read<0>();
+              if (prev_e >= 0) mbar_arrive(eempty0 + 8 * prev_e);
+              prev_e = -1;
+            }
+            mbar_arrive(eempty0 + 8 * e);
+          }
+          __syncwarp();
+          continue;
+        }
+        float acc[32], o[32];
+        tmem_ld32(tacc + j * kGemmChunk, acc);
+        if (w.piece >= 0) {
+          // the other piece's partial: two pieces, one addition, the same
+          // result whichever finished last
+          const float4* oq = reinterpret_cast<const float4*>(P.ws) +
+                             (size_t)((w.q ^ 1) * CL + rank) * (kGemmM * kGemmN / 4) + rr;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float4 t = __ldcg(oq + (size_t)(j * 8 + c) * kGemmM);
+            acc[4 * c] = __fadd_rn(acc[4 * c], t.x);
+            acc[4 * c + 1] = __fadd_rn(acc[4 * c + 1], t.y);
+            acc[4 * c + 2] = __fadd_rn(acc[4 * c + 2], t.z);
+            acc[4 * c + 3] = __fadd_rn(acc[4 * c + 3], t.w);
+          }
+        }
+        const uint8_t* st = ebuf + e * P.epi_stage_bytes;
+#pragma unroll
+        for (int s8 = 0; s8 < 4; ++s8) {
+          const GemmEnv env{P, st, rr, m0, n0 + j * kGemmChunk, s8 * 8};
+          float a8[8], o8[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) a8[k] = acc[s8 * 8 + k];
+          Epi::run(env, a8, o8);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) o[s8 * 8 + k] = o8[k];
+        }
+        // this warp's 32 rows x 32 columns go out through its own TMA store:
+        // no barrier across the epilogue warps
         // the result goes to this warp's rows of the IDENT leaf's chunk (read
         // above, no longer needed) or to a separate double buffer
         uint8_t* ob = inplace ? ebuf + e * P.epi_stage_bytes + P.inplace_off + q * (32 * 128)

@@ -110,7 +110,7 @@ constexpr int FG_FLAG_INJECT_NO_LOADS = 1 << 27;   // failure injection for test
 
 struct BuildOpts {
   int max_fused_ops = 256, max_args = 64, allow_reduce_epilogue = 0;
-  int flags = 0;   // bit 0: stage the output in smem and store it with TMA; bits 8-15: tile band
+  int flags = 0;   // bits 8-15: tile band (GEMM: CTA-pair cap); see fg_build_opts in groupexec.h
   int64_t wait_limit_ns = 2000000000LL;
 };
 

@@ -95,7 +95,8 @@ typedef struct tf_layout tf_layout;
  * wait_limit_ns: bound on every device-side wait before it sets the error
  * flag and the kernel returns.  flags tune the kernels without changing
  * results: bits 8-15 = height in tiles of the bands the tile walk sweeps
- * column by column (0 = row-major walk); bits 16-23 = tiles per reduce work
+ * column by column (0 = row-major walk), and for GEMM-epilogue groups the
+ * most CTA pairs to launch (0 = one pair per two SMs); bits 16-23 = tiles per reduce work
  * unit (0 = chosen from the frame and the SM count); bits 24-25 = how an
  * elementwise group writes its output: 0 default (= 2), 1 the CTA's tile
  * staged in shared memory and stored by one TMA store, 2 each warp's slice

@@ -100,3 +100,39 @@ def test_sf_update_small(mode):
 
 def test_sf_update_full():
     _sf_update(512, 4096, 4096, 0)
+
+
+@pytest.mark.parametrize("K,M,N,cap", [(1024, 1024, 1024, 5), (1024, 1024, 1024, 7), (2048, 1024, 1024, 5),
+                                       (1088, 768, 1280, 7)])
+def test_split_tail(K, M, N, cap):
+    """The last round's tiles split along K (CTA pairs capped so that a tail
+    exists): the partial accumulators meet in the workspace and the last
+    piece finishes the epilogue; run twice, so the arrival counters are seen
+    to reset."""
+    spec = W.sf_update(K, M, N)
+    g, plan, inputs, dev = prepare(spec, flags=cap << 8)
+    ref = OE.run_unfused(spec, inputs)[spec.outputs[0]]
+    w = inputs[2]
+    for _ in range(2):
+        env = run_fused(plan, spec, dev)
+        plan.sync()
+        got = env[spec.outputs[0]].cpu().numpy()
+        assert rel_err(got, ref) <= TOL_F32
+        assert rel_err(w - got, w - ref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("ta,tb", [(1, 0), (0, 1)])
+def test_split_tail_plain_layouts(ta, tb):
+    K, M, N = 1024, 1024, 768
+    spec = _matmul_graph(K, M, N, ta, tb)
+    g, plan, inputs, dev = prepare(spec, flags=5 << 8)
+    env = run_fused(plan, spec, dev)
+    plan.sync()
+    A = inputs[0].T if ta else inputs[0]
+    B = inputs[1].T if tb else inputs[1]
+    _check_matmul_bound(env[spec.outputs[0]].cpu().numpy(), A, B)
+
+
+def test_split_tail_full_size():
+    # 256 pair tiles on 76 pairs: the last 28 run as K halves
+    _sf_update(1024, 4096, 4096, 0)
