@@ -333,6 +333,7 @@ void prepare_group(GroupExec& ge, const BuildOpts& o, int nsm) {
   }
   p.nstaged = mi;
   p.nxout = (int32_t)cg.xout_values.size();
+  p.xout_tma = cg.xout_tma;
   for (int j = 0; j < p.nxout; ++j) {
     const Map& mp = cg.xout_maps[j];
     XOutDesc& x = p.xout[j];
@@ -732,6 +733,16 @@ fg_status launch_exec(fg_plan* p, GroupExec& ge, void* const* ptrs, void* stream
     if (cg.exec == FG_EXEC_ELEMWISE && cg.out_tma == 1)
       if (fg_status st = leaf_map(&gp.maps[kMaxStaged], ptrs[cg.out_value], LEAF_IDENT, cg.FR, cg.FC, kTileR, kTileC))
         return st;
+    if (cg.xout_tma)
+      for (size_t j = 0; j < cg.xout_values.size(); ++j) {
+        // a warp's slice: 32 frame rows x 8 frame columns, or its transpose
+        const bool id = cg.xout_cls[j] == LEAF_IDENT;
+        uint64_t dims[2] = {(uint64_t)(id ? cg.FC : cg.FR), (uint64_t)(id ? cg.FR : cg.FC)};
+        const int64_t inner = id ? cg.FC : cg.FR, outer = id ? cg.FR : cg.FC;
+        uint64_t strides[1] = {(uint64_t)(outer == 1 ? round_up(inner * 4, 16) : inner * 4)};
+        uint32_t box[2] = {id ? 8u : (uint32_t)kTileR, id ? (uint32_t)kTileR : 8u};
+        if (fg_status st = encode(&gp.xmaps[j], ptrs[cg.xout_values[j]], 2, dims, strides, box, false)) return st;
+      }
     if (cg.exec == FG_EXEC_ELEMWISE && cg.out_tma == 2) {
       // one warp's 32 x 8 slice per store
       uint64_t dims[2] = {(uint64_t)cg.FC, (uint64_t)cg.FR};

@@ -149,7 +149,10 @@ struct GroupParams {
   int32_t red_op, nsplit, tiles_per_split, nunits;
   int32_t inject;                      // failure injection: 1 = the producer issues no loads
   int32_t nxout;                       // extra outputs (compiled programs only)
+  int32_t xout_tma;                    // 1: each warp stages its slice of every extra output
+                                       //    in shared memory and stores it with TMA (xmaps)
   XOutDesc xout[kMaxXOut];
+  CUtensorMap xmaps[kMaxXOut];
 };
 
 // GEMM + epilogue kernel: 128 x 256 accumulator tiles in TMEM, K in blocks

@@ -25,6 +25,7 @@ namespace fg {
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kOutBufBytes = kTileR * kTileC * 4;   // 8 KB
+constexpr int kXOutSliceBytes = kOutBufBytes;        // per extra output: 8 warps x 32 x 8 floats
 
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7f800000); }
 
@@ -55,6 +56,7 @@ struct TileEnv {
   const GroupParams& P;
   const uint8_t* stage;
   int lr, lc0, r0, c0;
+  uint8_t* xb = nullptr;   // this warp's staging slices of the extra outputs (TMA stores), or none
 
   __device__ __forceinline__ void ident(int off, float (&t)[8]) const {
     const uint8_t* b = stage + off + (lc0 >> 5) * (kTileR * 128);
@@ -107,6 +109,20 @@ struct TileEnv {
   // outputs hold fewer than 2^31 elements).
   __device__ __forceinline__ void xstore(int j, const float (&v)[8]) const {
     const XOutDesc& X = P.xout[j];
+    if (xb) {
+      // staged for the warp's TMA store: identity slices as [32 rows][8],
+      // transposed ones as [8 rows][32] (lane = column of the output)
+      uint8_t* b = xb + j * kXOutSliceBytes;
+      if (X.cls == LEAF_IDENT) {
+        float4* p = reinterpret_cast<float4*>(b + lr * 32);
+        p[0] = make_float4(v[0], v[1], v[2], v[3]);
+        p[1] = make_float4(v[4], v[5], v[6], v[7]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) reinterpret_cast<float*>(b)[k * 32 + lr] = v[k];
+      }
+      return;
+    }
     const int r = r0 + lr, c = c0 + lc0;
     if (r >= P.FR) return;
     if (X.cls == LEAF_IDENT) {
@@ -341,6 +357,7 @@ __device__ __forceinline__ void ew_body(const GroupParams& P) {
   uint8_t* smem = align1024(smem_raw);
   const Ring R = setup_ring(smem);
   uint8_t* outbuf = R.base + P.nstages * P.stage_bytes;
+  uint8_t* xbuf = outbuf + 3 * kOutBufBytes;   // [3][nxout][8 warps][32 x 8 floats]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Prog::load_tables(T, P);
   if (threadIdx.x == 0) {
@@ -370,7 +387,8 @@ __device__ __forceinline__ void ew_body(const GroupParams& P) {
     const bool got = wait_or_abort(R.full_s + 8 * s, (i / NS) & 1, P.wait_limit_ns, &abort_flag);
     uint8_t* ob = outbuf + (i % 3) * kOutBufBytes;
     if (got) {
-      const TileEnv te{P, R.base + s * P.stage_bytes, lr, lc0, r0, c0};
+      const TileEnv te{P, R.base + s * P.stage_bytes, lr, lc0, r0, c0,
+                       P.xout_tma ? xbuf + ((i % 3) * P.nxout * 8 + warp) * (kTileR * 32) : nullptr};
       Prog::run(te, T, P, o);
       if (P.out_tma == 1) {
         uint8_t* b = ob + (lc0 >> 5) * (kTileR * 128);
@@ -408,6 +426,15 @@ __device__ __forceinline__ void ew_body(const GroupParams& P) {
         mbar_arrive(R.empty_s + 8 * s);
         if (got && c0 + lc0 < P.FC) {
           tma_store_2d(&P.maps[kMaxStaged], c0 + lc0, r0, smem_u32(ob + warp * (kTileR * 32)));
+          if (P.xout_tma) {
+            const uint8_t* xw = xbuf + ((i % 3) * P.nxout * 8 + warp) * (kTileR * 32);
+            for (int j = 0; j < P.nxout; ++j) {
+              if (P.xout[j].cls == LEAF_IDENT)
+                tma_store_2d(&P.xmaps[j], c0 + lc0, r0, smem_u32(xw + j * kXOutSliceBytes));
+              else
+                tma_store_2d(&P.xmaps[j], r0, c0 + lc0, smem_u32(xw + j * kXOutSliceBytes));
+            }
+          }
           bulk_commit();
           bulk_wait_read<1>();
         }

@@ -77,6 +77,7 @@ struct CompiledGroup {
   std::vector<int32_t> xout_values;
   std::vector<Map> xout_maps;
   std::vector<int> xout_cls;          // LEAF_IDENT, LEAF_TRANS or LEAF_GATHER (any other permutation)
+  int xout_tma = 0;                   // extra outputs staged per warp and stored by TMA (plan_staging)
   std::vector<int> xout_expr;
   std::vector<int32_t> leaf_values;   // distinct outside values, first-use order
   int64_t alg_bytes = 0, alg_flops = 0;

@@ -629,8 +629,17 @@ void plan_staging(const Graph& g, CompiledGroup& cg, const BuildOpts& o) {
     return (off + 1023) / 1024 * 1024;
   };
   int fixed = 2048;   // barriers + alignment slack
+  // extra outputs with identity or transposed maps go out like the sink
+  // output: per-warp slices in shared memory, one TMA store each
+  cg.xout_tma = 0;
+  if (cg.exec == FG_EXEC_ELEMWISE && cg.out_tma == 2 && !cg.xout_values.empty()) {
+    cg.xout_tma = 1;
+    for (int c : cg.xout_cls)
+      if (!((c == LEAF_IDENT && rows_ok) || (c == LEAF_TRANS && cols_ok && cg.FR % 4 == 0))) cg.xout_tma = 0;
+  }
   if (!gemm) {
     if (cg.out_tma) fixed += 3 * TR * TC * 4;               // three output buffers (per CTA or per warp)
+    if (cg.xout_tma) fixed += 3 * (int)cg.xout_values.size() * TR * TC * 4;   // and per extra output
     if (cg.exec == FG_EXEC_REDUCE) fixed += 2 * kConsumerWarps * 32 * 4;   // double-buffered row partials
   }
   // dynamic shared memory per CTA; about 5 KB of static tables come on top
