@@ -83,7 +83,8 @@ struct GroupExec {
   bool big = false;
   int grid = 1, smem = 0;
   float* scratch = nullptr;
-  int32_t* counters = nullptr;
+  int32_t* counters = nullptr;        // split arrival counters (zero between launches)
+  size_t counter_bytes = 0;
   std::string compile_error;          // non-empty: cannot launch
   fg_status compile_status = FG_OK;
   bool compiled = false;              // run the compiled program (else the interpreter)
@@ -552,9 +553,10 @@ fg_status alloc_device(fg_plan* p, GroupExec& ge) {
       const size_t tail = (size_t)(units - mp.nfull);
       cudaError_t e = cudaMalloc(&ge.scratch, sizeof(float) * tail * mp.split * kGemmCluster * kGemmM * kGemmN);
       if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(split-tail workspace)");
-      e = cudaMalloc(&ge.counters, sizeof(int32_t) * tail * kGemmCluster * 4);
+      ge.counter_bytes = sizeof(int32_t) * tail * kGemmCluster * 4;
+      e = cudaMalloc(&ge.counters, ge.counter_bytes);
       if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(split-tail counters)");
-      e = cudaMemset(ge.counters, 0, sizeof(int32_t) * tail * kGemmCluster * 4);
+      e = cudaMemset(ge.counters, 0, ge.counter_bytes);
       if (e != cudaSuccess) return cuda_err(e, "cudaMemset(split-tail counters)");
       mp.ws = ge.scratch;
       mp.ws_cnt = ge.counters;
@@ -566,9 +568,10 @@ fg_status alloc_device(fg_plan* p, GroupExec& ge) {
   if (ge.cg.exec == FG_EXEC_REDUCE && gp.nsplit > 1) {
     cudaError_t e = cudaMalloc(&ge.scratch, sizeof(float) * (size_t)gp.nsplit * gp.FR);
     if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(reduce scratch)");
-    e = cudaMalloc(&ge.counters, sizeof(int32_t) * (size_t)gp.ntr);
+    ge.counter_bytes = sizeof(int32_t) * (size_t)gp.ntr;
+    e = cudaMalloc(&ge.counters, ge.counter_bytes);
     if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(reduce counters)");
-    e = cudaMemset(ge.counters, 0, sizeof(int32_t) * (size_t)gp.ntr);
+    e = cudaMemset(ge.counters, 0, ge.counter_bytes);
     if (e != cudaSuccess) return cuda_err(e, "cudaMemset(reduce counters)");
     gp.scratch = ge.scratch;
     gp.counters = ge.counters;
@@ -1038,6 +1041,10 @@ fg_status fg_sync_status(fg_plan* p, void* stream) {
   if (e != cudaSuccess) return cuda_err(e, "reading the device error flag");
   if (flag == 0) return FG_OK;
   cudaMemset(p->d_err, 0, sizeof(int32_t));
+  // a kernel that gave up may have left split arrival counters mid-count
+  for (auto* v : {&p->groups, &p->singles})
+    for (auto& ge : *v)
+      if (ge.counters) cudaMemset(ge.counters, 0, ge.counter_bytes);
   if (flag == DEVERR_TIMEOUT) return err(FG_ETIMEOUT, "a device-side wait exceeded wait_limit_ns");
   return err(FG_EDEVICE, "device error flag " + std::to_string(flag));
 }

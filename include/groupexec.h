@@ -182,7 +182,10 @@ fg_status fg_launch_group(fg_plan* p, int32_t gid, void* const* value_ptrs, void
 fg_status fg_launch_unfused(fg_plan* p, int32_t node, void* const* value_ptrs, void* cuda_stream);
 
 /* Synchronises the stream, then reads and clears the plan's device error flag:
- * FG_ETIMEOUT when a bounded wait expired, FG_EDEVICE for other flags. */
+ * FG_ETIMEOUT when a bounded wait expired, FG_EDEVICE for other flags.  On an
+ * error it also zeroes the plan's split arrival counters, which a kernel that
+ * gave up may have left mid-count, so the plan's next launches are correct;
+ * results of the launches since the last FG_OK are undefined. */
 fg_status fg_sync_status(fg_plan* p, void* cuda_stream);
 
 /* Every value group gid writes: out_values[0] is the group's sink output

@@ -42,3 +42,4 @@ def test_injected_timeout_is_reported_and_recoverable(case, mode):
     ref = OE.run_unfused(spec, inputs2)
     for o in spec.outputs:
         assert rel_err(env[o].cpu().numpy(), ref[o]) <= TOL_F32
+
