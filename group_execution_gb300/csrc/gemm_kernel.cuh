@@ -90,11 +90,13 @@ struct GemmEnv {
 // cc0..cc0+31.
 __device__ __forceinline__ void gemm_issue_leaf(const CUtensorMap* m, int cls, uint32_t dst, uint32_t bar, int r0,
                                                 int cc0) {
+  // a tile's leaf boxes are read once: they leave L2 first
+  const uint64_t once = l2_evict_first();
   if (cls == LEAF_IDENT) {
-    tma_load_2d(dst, m, cc0, r0, bar);
+    tma_load_2d_hint(dst, m, cc0, r0, bar, once);
   } else if (cls == LEAF_TRANS) {
 #pragma unroll
-    for (int b = 0; b < 4; ++b) tma_load_2d(dst + b * 4096, m, r0 + 32 * b, cc0, bar);
+    for (int b = 0; b < 4; ++b) tma_load_2d_hint(dst + b * 4096, m, r0 + 32 * b, cc0, bar, once);
   } else if (cls == LEAF_COL) {
     tma_load_1d(dst, m, cc0, bar);
   } else if (cls == LEAF_ROW) {
@@ -241,6 +243,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
     if (lane == 0 && !P.inject) {
       tma_prefetch(&P.mapA);
       tma_prefetch(&P.mapB);
+      const uint64_t keep = l2_evict_last();   // every operand tile is read by several tiles
       int it = 0;
       bool ok = true;
       for (int x = cl; x < nitems && ok; x += ncl) {
@@ -263,35 +266,35 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
           if (leader) mbar_expect_tx(full0 + 8 * s, CL * kStageBytes);
           if (P.a_mn) {
             if (P.a_3d) {
-              tma_load_3d_pair(a, &P.mapA, 0, k0, m0 / 64, cbar);
+              tma_load_3d_pair(a, &P.mapA, 0, k0, m0 / 64, cbar, keep);
             } else {
 #pragma unroll
               for (int g = 0; g < 2; ++g)
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
-                  tma_load_2d_pair(a + g * 16384 + j * 8192, &P.mapA, m0 + 64 * g, k0 + 64 * j, cbar);
+                  tma_load_2d_pair(a + g * 16384 + j * 8192, &P.mapA, m0 + 64 * g, k0 + 64 * j, cbar, keep);
             }
           } else if (P.a_3d) {
-            tma_load_3d_pair(a, &P.mapA, 0, m0, k0 / 64, cbar);
+            tma_load_3d_pair(a, &P.mapA, 0, m0, k0 / 64, cbar, keep);
           } else {
 #pragma unroll
-            for (int j = 0; j < kGemmKB; ++j) tma_load_2d_pair(a + j * 16384, &P.mapA, k0 + 64 * j, m0, cbar);
+            for (int j = 0; j < kGemmKB; ++j) tma_load_2d_pair(a + j * 16384, &P.mapA, k0 + 64 * j, m0, cbar, keep);
           }
           if (P.b_mn) {
             if (P.b_3d) {
-              tma_load_3d_pair(b, &P.mapB, 0, k0, nb / 64, cbar);
+              tma_load_3d_pair(b, &P.mapB, 0, k0, nb / 64, cbar, keep);
             } else {
 #pragma unroll
               for (int g = 0; g < 2; ++g)
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
-                  tma_load_2d_pair(b + g * 16384 + j * 8192, &P.mapB, nb + 64 * g, k0 + 64 * j, cbar);
+                  tma_load_2d_pair(b + g * 16384 + j * 8192, &P.mapB, nb + 64 * g, k0 + 64 * j, cbar, keep);
             }
           } else if (P.b_3d) {
-            tma_load_3d_pair(b, &P.mapB, 0, nb, k0 / 64, cbar);
+            tma_load_3d_pair(b, &P.mapB, 0, nb, k0 / 64, cbar, keep);
           } else {
 #pragma unroll
-            for (int j = 0; j < kGemmKB; ++j) tma_load_2d_pair(b + j * 16384, &P.mapB, k0 + 64 * j, nb, cbar);
+            for (int j = 0; j < kGemmKB; ++j) tma_load_2d_pair(b + j * 16384, &P.mapB, k0 + 64 * j, nb, cbar, keep);
           }
         }
       }
@@ -501,7 +504,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         if (lane == 0) {
           if (staged && !inplace) mbar_arrive(eempty0 + 8 * e);
           if (n0 + j * kGemmChunk < P.N && m0 + q * 32 < P.M) {
-            tma_store_2d(&P.maps[kMaxStaged], n0 + j * kGemmChunk, m0 + q * 32, smem_u32(ob));
+            tma_store_2d_hint(&P.maps[kMaxStaged], n0 + j * kGemmChunk, m0 + q * 32, smem_u32(ob), l2_evict_first());
           }
           bulk_commit();
           if (inplace) {
