@@ -548,6 +548,26 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
     rows["diamond_with_P_output"] = row
     del e
 
+    # two branches joined by a tuple and a concatenation (FuseOps phases 1 and
+    # 2): relu(X1), exp(X2) [4096, 4096] each -> concat [8192, 4096] -> scale,
+    # one group, against one kernel per operator
+    tsp = W.GraphSpec("inception")
+    t1 = tsp.op("relu", (tsp.input((4096, 4096)),))
+    t2 = tsp.op("exp", (tsp.input((4096, 4096)),))
+    tsp.mark_output(tsp.op("scale", (tsp.op("concat", (tsp.op("tuple", (t1, t2)),)),), (0.5,)))
+    tplan = graph_from_spec(tsp).build()
+    gen = torch.Generator(device="cuda").manual_seed(2)
+    te = {v.vid: torch.empty(v.shape, device="cuda").uniform_(-1, 1, generator=gen) for v in tsp.values if v.is_input}
+    for v in tsp.ops:
+        te[v.vid] = torch.empty(v.shape, device="cuda")
+    med, _ = timed(run_plan(tplan, tsp, te, True), flush=False)
+    medu, _ = timed(run_plan(tplan, tsp, te, False), flush=False)
+    alg = sum(gi.alg_bytes for gi in tplan.groups)
+    rows["tuple_concat_2x4096x4096"] = {
+        "groups": tplan.n_groups, "fused_us": med * 1e3, "unfused_us": medu * 1e3, "speedup_vs_unfused": medu / med,
+        "alg_bytes": alg, "GBps": alg / (med * 1e-3) / 1e9, "frac_of_hbm": alg / (med * 1e-3) / 1e9 / hbm}
+    del te
+
     # an MLP layer grouped by pattern (FuseOpsByPattern with the page's matmul +
     # bias pattern extended by relu): Y = relu(X W + b), X [4096, 4096],
     # W [4096, 4096] bf16, one GEMM-epilogue group

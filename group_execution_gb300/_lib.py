@@ -26,7 +26,7 @@ STATUS_NAMES = ["FG_OK", "FG_EINVAL", "FG_ESHAPE", "FG_EUNSUPPORTED", "FG_ENOMEM
 OPCODES = {name: i for i, name in enumerate((
     "add", "sub", "mul", "div", "scale", "addc", "relu", "exp", "sigmoid", "tanh", "neg",
     "badd_col", "bmul_col", "badd_row", "bmul_row", "transpose", "reshape", "rowsum", "rowmax",
-    "matmul_bf16", "opaque_copy"))}
+    "matmul_bf16", "opaque_copy", "tuple", "concat"))}
 EXEC_KINDS = ("elementwise", "reduce", "gemm")
 
 

@@ -229,6 +229,28 @@ fg_status fg_graph_add_op(fg_graph* gh, int32_t op, int32_t n_in, const int32_t*
       out.cols = V(0).rows;
       out.rows = 1;
       break;
+    case FG_OP_TUPLE: {
+      if ((st = need(2, 4, 0))) return st;
+      int64_t rows = 0;
+      for (int i = 0; i < n_in; ++i) {
+        if (V(i).ndim != 2) return err(FG_ESHAPE, "tuple fields must be rank-2");
+        if (V(i).cols != V(0).cols) return err(FG_ESHAPE, "tuple fields must have one width");
+        if (V(i).node >= 0 && g.nodes[V(i).node].op == FG_OP_TUPLE) return err(FG_EUNSUPPORTED, "a tuple of tuples");
+        rows += V(i).rows;
+      }
+      out.ndim = 2;
+      out.rows = rows;
+      out.cols = V(0).cols;
+      break;
+    }
+    case FG_OP_CONCAT:
+      if ((st = need(1, 1, 0))) return st;
+      if (V(0).node < 0 || g.nodes[V(0).node].op != FG_OP_TUPLE)
+        return err(FG_EINVAL, "concat reads the value of a tuple");
+      out.ndim = 2;
+      out.rows = V(0).rows;
+      out.cols = V(0).cols;
+      break;
     case FG_OP_MATMUL_BF16: {
       if ((st = need(2, 2, 0))) return st;
       int ta = n_attr > 0 ? (int)attrs[0] : 0, tb = n_attr > 1 ? (int)attrs[1] : 0;
@@ -291,11 +313,15 @@ fg_status fg_graph_value_info(const fg_graph* gh, int32_t vid, int32_t* dtype, i
 // plan construction
 namespace {
 
-void fill_leaf_desc(LeafDesc& d, const LeafUse& l, int stage_off, int map_idx) {
+void fill_leaf_desc(LeafDesc& d, const LeafUse& l, int stage_off, int map_idx, int64_t FC) {
   std::memset(&d, 0, sizeof(d));
   d.cls = l.cls;
   d.stage_off = stage_off;
   d.map_idx = map_idx;
+  d.shift = l.map.shift;
+  d.numel = l.numel;
+  d.shift_r = (int32_t)(l.map.shift / FC);
+  d.shift_c = (int32_t)(l.map.shift % FC);
   d.nterms = l.map.n;
   for (int k = 0; k < l.map.n; ++k) {
     d.d[k] = l.map.d[k];
@@ -326,7 +352,7 @@ void prepare_group(GroupExec& ge, const BuildOpts& o, int nsm) {
   int mi = 0, tx = 0;
   for (size_t i = 0; i < cg.leaves.size(); ++i) {
     bool staged = cg.leaves[i].cls != LEAF_GATHER;
-    fill_leaf_desc(p.leaves[i], cg.leaves[i], staged ? cg.leaf_stage_off[i] : -1, staged ? mi : -1);
+    fill_leaf_desc(p.leaves[i], cg.leaves[i], staged ? cg.leaf_stage_off[i] : -1, staged ? mi : -1, cg.FC);
     if (staged) {
       ++mi;
       tx += box_tx_bytes(cg.leaves[i].cls);
@@ -440,7 +466,7 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
   int mi = 0, tx = 0;
   for (size_t i = 0; i < cg.leaves.size(); ++i) {
     bool staged = cg.leaves[i].cls != LEAF_GATHER;
-    fill_leaf_desc(p.leaves[i], cg.leaves[i], staged ? cg.leaf_stage_off[i] : -1, staged ? mi : -1);
+    fill_leaf_desc(p.leaves[i], cg.leaves[i], staged ? cg.leaf_stage_off[i] : -1, staged ? mi : -1, cg.FC);
     if (staged) {
       ++mi;
       tx += gemm_box_bytes(cg.leaves[i].cls);
@@ -527,6 +553,8 @@ GroupExec make_exec(const Graph& g, const std::vector<int32_t>& nodes, const Bui
     ge.cg = compile_group(g, nodes);
     if (!ge.cg.xout_values.empty() && (o.flags & FG_FLAG_INTERPRET))
       throw CompileError{FG_EUNSUPPORTED, "groups with extra outputs run compiled programs only"};
+    if (ge.cg.needs_jit && (o.flags & FG_FLAG_INTERPRET))
+      throw CompileError{FG_EUNSUPPORTED, "groups with tuples run compiled programs only"};
     plan_staging(g, ge.cg, o);
     if (ge.cg.exec == FG_EXEC_GEMM) {
       prepare_gemm(ge, o, nsm, g);

@@ -101,6 +101,10 @@ struct LeafDesc {
   int32_t nterms;        // gather
   const float* ptr;      // gather base pointer (filled at launch)
   int64_t d[kMaxTerms], m[kMaxTerms], s[kMaxTerms];
+  // a tuple's field is read at g - shift (staged boxes move by shift_r rows
+  // and shift_c columns); gathers skip indices outside [0, numel)
+  int64_t shift, numel;
+  int32_t shift_r, shift_c;
 };
 
 // An extra output of a multi-output group (a value computed inside the group

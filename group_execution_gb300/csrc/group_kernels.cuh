@@ -94,10 +94,16 @@ struct TileEnv {
       const int c = c0 + lc0 + k;
       float v = 0.f;
       if (r < P.FR && c < P.FC) {
-        const uint32_t g = (uint32_t)r * (uint32_t)P.FC + (uint32_t)c;
+        uint32_t g = (uint32_t)r * (uint32_t)P.FC + (uint32_t)c;
+        bool in = true;
+        if (G.shift) {
+          // a tuple's field: other fields' points map outside it
+          in = (int64_t)g >= G.shift;
+          g = (uint32_t)((int64_t)g - G.shift);
+        }
         uint32_t f = 0;
         for (int q = 0; q < G.nterms; ++q) f += ((g / (uint32_t)G.d[q]) % (uint32_t)G.m[q]) * (uint32_t)G.s[q];
-        v = __ldg(G.ptr + f);
+        if (in && (!G.shift || (int64_t)f < G.numel)) v = __ldg(G.ptr + f);
       }
       t[k] = v;
     }

@@ -46,9 +46,12 @@ struct Graph {
 
 // Maps: f = sum_k ((g / d_k) % m_k) * s_k over the frame flat index g, with
 // the terms tiling the value's index range (s_0 = 1, s_{k+1} = s_k * m_k).
+// A map may also carry a shift: it is evaluated at g - shift (a field of a
+// tuple read at the tuple's frame point).
 struct Map {
   int n = 0;
   int64_t d[kMaxTerms] = {0}, m[kMaxTerms] = {0}, s[kMaxTerms] = {0};
+  int64_t shift = 0;
   bool operator==(const Map& o) const;
 };
 
@@ -56,15 +59,16 @@ struct LeafUse {            // one (value, map) read by a program
   int32_t value;
   Map map;
   int32_t cls;              // LeafClass
+  int64_t numel;            // elements of the value (bounds of shifted gathers)
 };
 
 // One node of a group's expression DAG (children before parents).
 struct JExpr {
-  int kind;          // 0 leaf, 1 accumulator, 2 unary, 3 binary
-  int vm;            // VmOp of the operation
+  int kind;          // 0 leaf, 1 accumulator, 2 unary, 3 binary, 4 select
+  int vm;            // VmOp of the operation (select: 0 = by frame row, 1 = by frame column)
   float imm;
-  int a, b;          // children
-  int leaf;          // leaf index (kind 0)
+  int a, b;          // children (select: a where the row / column is below `leaf`, else b)
+  int leaf;          // leaf index (kind 0), bound (kind 4)
 };
 
 struct CompiledGroup {
@@ -90,6 +94,7 @@ struct CompiledGroup {
   std::vector<JExpr> epi_dag;         // reduce epilogue DAG (leaves index epi_leaf_values)
   int epi_root = -1;
   int depth = 0, slots = 0;
+  bool needs_jit = false;             // selects (tuples): no interpreter program
   // reduce
   int32_t red_op = RED_NONE;
   std::vector<VmInstr> epi;

@@ -14,7 +14,7 @@
 namespace fg {
 
 bool Map::operator==(const Map& o) const {
-  if (n != o.n) return false;
+  if (n != o.n || shift != o.shift) return false;
   for (int k = 0; k < n; ++k)
     if (d[k] != o.d[k] || m[k] != o.m[k] || s[k] != o.s[k]) return false;
   return true;
@@ -80,6 +80,7 @@ void split(const Map& mp, int64_t Q, Map& lo, Map& hi) {
   if (!H.empty() && prod != Q) fail(FG_EUNSUPPORTED, "index map does not split at the row boundary");
   lo = make_map(L);
   hi = make_map(H);
+  lo.shift = hi.shift = mp.shift;
 }
 
 // The map of x = y^T's index, given y's map; x is [A, B], y is [B, A]:
@@ -90,10 +91,15 @@ Map transpose_map(const Map& fy, int64_t A, int64_t B) {
   std::vector<Term> t;
   for (Term x : terms(lo)) t.push_back({x.d, x.m, x.s * B});
   for (Term x : terms(hi)) t.push_back(x);
-  return make_map(t);
+  Map r = make_map(t);
+  r.shift = fy.shift;
+  return r;
 }
 
-int classify(const Map& mp, int64_t FR, int64_t FC) {
+// The class of a map's digits (its shift aside).
+int classify(const Map& shifted, int64_t FR, int64_t FC) {
+  Map mp = shifted;
+  mp.shift = 0;
   if (mp == ident(FR, FC)) return LEAF_IDENT;
   if (mp == make_map({{FC, FR, 1}, {1, FC, FR}})) return LEAF_TRANS;
   if (mp == make_map({{1, FC, 1}})) return LEAF_COL;
@@ -103,7 +109,7 @@ int classify(const Map& mp, int64_t FR, int64_t FC) {
 
 // ---- expression DAG --------------------------------------------------------
 
-enum ExprKind { E_LEAF, E_ACC, E_UN, E_BIN };
+enum ExprKind { E_LEAF, E_ACC, E_UN, E_BIN, E_SEL };
 
 struct Expr {
   ExprKind kind;
@@ -124,7 +130,8 @@ struct Builder {
   std::vector<Expr> ex;
   std::vector<LeafUse> leaves;
   std::map<std::tuple<int, int, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t,
-                      int64_t, int64_t, int64_t, int64_t, int64_t>, int> memo;
+                      int64_t, int64_t, int64_t, int64_t, int64_t, int64_t>, int> memo;
+  bool tuples_ok = true;          // the epilogue of a reduce or matmul group has no tuples
 
   Builder(const Graph& gg, const std::vector<int32_t>& nodes, int64_t fr, int64_t fc)
       : g(gg), in_group(gg.nodes.size(), 0), FR(fr), FC(fc) {
@@ -139,13 +146,13 @@ struct Builder {
   int leaf(int value, const Map& mp) {
     for (size_t i = 0; i < leaves.size(); ++i)
       if (leaves[i].value == value && leaves[i].map == mp) return (int)i;
-    leaves.push_back({value, mp, classify(mp, FR, FC)});
+    leaves.push_back({value, mp, classify(mp, FR, FC), g.values[value].numel()});
     return (int)leaves.size() - 1;
   }
 
   int build(int value, const Map& mp) {
     auto key = std::make_tuple(value, mp.n, mp.d[0], mp.m[0], mp.s[0], mp.d[1], mp.m[1], mp.s[1],
-                               mp.d[2], mp.m[2], mp.s[2], mp.d[3], mp.m[3], mp.s[3]);
+                               mp.d[2], mp.m[2], mp.s[2], mp.d[3], mp.m[3], mp.s[3], mp.shift);
     auto it = memo.find(key);
     if (it != memo.end()) {
       ex[it->second].uses++;
@@ -224,6 +231,40 @@ struct Builder {
     auto arg = [&](int i) { return n.args[i]; };
     const Value& x0 = g.values[arg(0)];
     switch (n.op) {
+      case FG_OP_CONCAT:
+        return build_alias(arg(0), mp);   // a tuple's value is already its fields stacked
+      case FG_OP_TUPLE: {
+        // the tuple's row for the frame point: the frame row when the tuple
+        // is in the frame's layout, the frame column when it is transposed
+        if (!tuples_ok) fail(FG_EUNSUPPORTED, "a tuple in a reduce or matmul epilogue");
+        if (mp.shift) fail(FG_EUNSUPPORTED, "a tuple read through another tuple's field");
+        const Value& tv = g.values[n.value];
+        const int cls = classify(mp, FR, FC);
+        int axis;
+        if (cls == LEAF_IDENT && tv.cols == FC) axis = 0;
+        else if (cls == LEAF_TRANS && tv.cols == FR) axis = 1;
+        else fail(FG_EUNSUPPORTED, "a tuple read through a map other than the frame's layout or its transpose");
+        std::vector<int> fields;
+        std::vector<int64_t> bounds;
+        int64_t off = 0;
+        for (int32_t f : n.args) {
+          Map fm = mp;
+          fm.shift = axis == 0 ? off * tv.cols : off;   // the field's rows start `off` rows down
+          fields.push_back(build(f, fm));
+          off += g.values[f].rows;
+          bounds.push_back(off);
+        }
+        if (off >= (int64_t)1 << 31) fail(FG_EUNSUPPORTED, "tuple too tall");
+        int acc = fields.back();
+        for (int k = (int)fields.size() - 2; k >= 0; --k) {
+          Expr e{E_SEL, axis};
+          e.a = fields[k];
+          e.b = acc;
+          e.leaf = (int)bounds[k];
+          acc = mk(e);
+        }
+        return acc;
+      }
       case FG_OP_TRANSPOSE:
         return build_alias(arg(0), transpose_map(mp, x0.rows, x0.cols));
       case FG_OP_RESHAPE:
@@ -398,11 +439,21 @@ struct Program {
   int depth = 0, slots = 0;
   std::vector<JExpr> dag;
   int root = -1;
+  bool needs_jit = false;
 };
 
 Program emit_program(Builder& b, int root) {
   Program p;
   for (const Expr& e : b.ex) p.dag.push_back(JExpr{(int)e.kind, e.vm, e.imm, e.a, e.b, e.leaf});
+  p.root = root;
+  p.leaves = b.leaves;
+  for (const Expr& e : b.ex)
+    if (e.kind == E_SEL) {
+      // selects run in compiled programs only: no interpreter program
+      p.needs_jit = true;
+      if ((int)p.leaves.size() > kMaxLeaves) fail(FG_EUNSUPPORTED, "group reads more than 24 leaf views");
+      return p;
+    }
   p.root = root;
   Emitter em(b.ex);
   em.emit(root);
@@ -515,6 +566,7 @@ CompiledGroup compile_group(const Graph& g, const std::vector<int32_t>& nodes_in
     Builder b(g, cg.nodes, cg.FR, cg.FC);
     b.anchor = mm;
     b.anchor_map = ident(cg.FR, cg.FC);
+    b.tuples_ok = false;
     Program p = emit_program(b, b.build(cg.out_value, ident(cg.FR, cg.FC)));
     cg.prog = p.code;
     cg.leaves = p.leaves;
@@ -546,11 +598,13 @@ CompiledGroup compile_group(const Graph& g, const std::vector<int32_t>& nodes_in
     cg.slots = p.slots;
     cg.dag = p.dag;
     cg.dag_root = p.root;
+    cg.needs_jit = p.needs_jit;
     if (cg.sink != red) {
       // epilogue on the reduced vector (allow_reduce_epilogue)
       Builder be(g, cg.nodes, 1, cg.FR);
       be.anchor = red;
       be.anchor_map = ident(1, cg.FR);
+      be.tuples_ok = false;
       Program pe = emit_program(be, be.build(cg.out_value, ident(1, cg.FR)));
       if ((int)pe.code.size() > kMaxEpi) fail(FG_EUNSUPPORTED, "reduce epilogue too long");
       if ((int)pe.leaves.size() > kMaxEpiLeaves) fail(FG_EUNSUPPORTED, "reduce epilogue reads too many values");
@@ -578,6 +632,7 @@ CompiledGroup compile_group(const Graph& g, const std::vector<int32_t>& nodes_in
   cg.slots = p.slots;
   cg.dag = p.dag;
   cg.dag_root = p.root;
+  cg.needs_jit = p.needs_jit;
   return cg;
 }
 
@@ -608,6 +663,14 @@ void plan_staging(const Graph& g, CompiledGroup& cg, const BuildOpts& o) {
   for (size_t i = 0; i < cg.leaves.size(); ++i) {
     int c = cg.leaves[i].cls;
     bool ok = (c == LEAF_IDENT && rows_ok) || (c == LEAF_TRANS && cols_ok) || c == LEAF_COL || c == LEAF_ROW;
+    // a shifted leaf (a tuple's field) moves its boxes by whole rows and
+    // columns; a copy's innermost coordinate must stay 16-byte aligned
+    const int64_t sh = cg.leaves[i].map.shift;
+    if (sh) {
+      const int64_t sr = sh / cg.FC, sc = sh % cg.FC;
+      const int64_t inner = (c == LEAF_IDENT || c == LEAF_COL) ? sc : sr;
+      if (gemm || inner % 4) ok = false;
+    }
     if (ok && want < kMaxStaged) {
       stage[i] = 1;
       ++want;

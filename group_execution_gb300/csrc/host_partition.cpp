@@ -3,8 +3,11 @@
 // TVM "Operator Fusion": Operator Pattern Classification (kinds and their
 // order, CombinePattern = max); FuseOps > Algorithm steps 1-3 (forward graph,
 // post-dominator tree by LCA on the DAG, CheckPath + CommitFuse with
-// union-find); Fusion rules (phases 0 and 1, reduce only as a sink, opaque
-// barrier, kMaxFusedOps and the argument limit).
+// union-find); Fusion rules (phases 0, 1 and 2, reduce only as a sink,
+// opaque barrier, kMaxFusedOps and the argument limit).  A tuple fuses like an
+// injective operator in phase 1 and, once merged with other operators, counts
+// as injective in its group's pattern; phase 2 fuses injective-or-simpler
+// producers into a tuple that a later group has absorbed.
 #include <algorithm>
 
 #include "host.h"
@@ -25,6 +28,10 @@ Kind op_kind(int op) {
       return K_COMM_REDUCE;
     case FG_OP_MATMUL_BF16:
       return K_OUT_EWISE_FUSABLE;
+    case FG_OP_TUPLE:
+      return K_TUPLE;
+    case FG_OP_CONCAT:
+      return K_INJECTIVE;
     default:
       return K_OPAQUE;
   }
@@ -156,7 +163,7 @@ void partition(const Graph& g, const BuildOpts& o, std::vector<int32_t>& group_o
     return (bool)cond(uf.pattern[uf.find(sink)], true);
   };
 
-  for (int phase = 0; phase < 2; ++phase) {
+  for (int phase = 0; phase < 3; ++phase) {
     for (int i = 0; i < n; ++i) {
       int grp = uf.find(i);
       int gk = uf.pattern[grp];
@@ -187,9 +194,15 @@ void partition(const Graph& g, const BuildOpts& o, std::vector<int32_t>& group_o
             if (!is_sink) return k <= K_INJECTIVE;
             return k <= K_INJECTIVE || k == K_COMM_REDUCE || k == K_OUT_EWISE_FUSABLE;
           });
-      } else if (gk == K_INJECTIVE) {
+      } else if (gk == K_INJECTIVE || gk == K_TUPLE) {
         // Phase 1: only along injective-or-simpler paths.
         if (phase == 1 && ppat[i] <= K_INJECTIVE)
+          ok = check_path(i, p, [](int k, bool) { return k <= K_INJECTIVE; });
+      }
+      if (!ok && phase == 2) {
+        // Phase 2: into an intermediate tuple that a later group absorbed.
+        const int tg = uf.find(p);
+        if (gk <= K_INJECTIVE && kinds[p] == K_TUPLE && uf.size[tg] > 1 && uf.pattern[tg] <= K_INJECTIVE)
           ok = check_path(i, p, [](int k, bool) { return k <= K_INJECTIVE; });
       }
       if (!ok) continue;
@@ -224,7 +237,10 @@ void partition(const Graph& g, const BuildOpts& o, std::vector<int32_t>& group_o
       for (int r : roots) {
         if (r == target) continue;
         uf.parent[r] = target;
-        uf.pattern[target] = std::max(uf.pattern[target], uf.pattern[r]);
+        // an absorbed tuple counts as injective in the merged group
+        const int a = uf.pattern[target] == K_TUPLE ? K_INJECTIVE : uf.pattern[target];
+        const int b = uf.pattern[r] == K_TUPLE ? K_INJECTIVE : uf.pattern[r];
+        uf.pattern[target] = std::max(a, b);
         uf.size[target] += uf.size[r];
       }
     }

@@ -71,13 +71,21 @@ typedef enum { FG_F32 = 0, FG_BF16 = 1 } fg_dtype;
  *   MATMUL_BF16(transA, transB): bf16 x bf16 -> f32 [M,N]  out-elementwise-fusable
  *       A is [M,K] (or [K,M] when transA), B is [K,N] (or [N,K] when transB)
  *   OPAQUE_COPY: identity that never fuses                 opaque
+ *   TUPLE(a, b[, c[, d]]): 2-D f32 fields of one width C; its value is the
+ *       fields' rows stacked in order, [sum of rows, C]     tuple (7)
+ *   CONCAT(t): joins the fields of tuple t (its only operand must be a
+ *       TUPLE's value): [sum of rows, C]                     injective
+ * A tuple fuses like an injective operator into its post-dominator (FuseOps
+ * phase 1); phase 2 then fuses injective-or-simpler producers of its fields
+ * into the group that absorbed it (TVM "Operator Fusion", Fusion rules).
+ * Groups holding a tuple run compiled programs only.
  */
 typedef enum {
   FG_OP_ADD = 0, FG_OP_SUB, FG_OP_MUL, FG_OP_DIV, FG_OP_SCALE, FG_OP_ADDC,
   FG_OP_RELU, FG_OP_EXP, FG_OP_SIGMOID, FG_OP_TANH, FG_OP_NEG,
   FG_OP_BADD_COL, FG_OP_BMUL_COL, FG_OP_BADD_ROW, FG_OP_BMUL_ROW,
   FG_OP_TRANSPOSE, FG_OP_RESHAPE, FG_OP_ROWSUM, FG_OP_ROWMAX,
-  FG_OP_MATMUL_BF16, FG_OP_OPAQUE_COPY, FG_OP_COUNT
+  FG_OP_MATMUL_BF16, FG_OP_OPAQUE_COPY, FG_OP_TUPLE, FG_OP_CONCAT, FG_OP_COUNT
 } fg_opcode;
 
 /* Which kernel executes a group. */

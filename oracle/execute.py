@@ -68,6 +68,10 @@ def apply_op(op, args, attrs):
         return _r(a[0] + a[1][:, None])
     if op == "bmul_row":
         return _r(a[0] * a[1][:, None])
+    if op == "tuple":
+        return np.ascontiguousarray(np.concatenate([np.asarray(x, dtype=F32) for x in args], axis=0))
+    if op == "concat":
+        return np.ascontiguousarray(np.asarray(args[0], dtype=F32))
     if op == "transpose":
         return np.ascontiguousarray(args[0].T)
     if op == "reshape":

@@ -38,6 +38,10 @@ OP_TABLE = {
     "rowmax": (K_COMM_REDUCE, (1,)),
     "matmul_bf16": (K_OUT_EWISE_FUSABLE, (2,)),
     "opaque_copy": (K_OPAQUE, (1,)),
+    # a tuple groups 2-D values of one width (laid out as their rows stacked
+    # in order); concat joins a tuple's fields, an injective op
+    "tuple": (K_TUPLE, (2, 3, 4)),
+    "concat": (K_INJECTIVE, (1,)),
 }
 
 

@@ -1,4 +1,4 @@
-"""FuseOps grouping: CheckPath / CommitFuse with union-find, phases 0 and 1.
+"""FuseOps grouping: CheckPath / CommitFuse with union-find, phases 0, 1 and 2.
 
 TVM "Operator Fusion", FuseOps > Algorithm (step 3) and Fusion rules:
 
@@ -23,7 +23,14 @@ Readings where the page is silent (each mirrored by the C++ partitioner):
   read from outside the merged group plus its one output;
 * an elementwise producer never joins a matmul group through the matmul's own
   operand: that edge has the matmul's kind, which the path test rejects;
-* phase 2 (tuples) is not run: the operator set has no tuple;
+* a tuple fuses like an injective op in phase 1 (every path to its
+  post-dominator injective or simpler); once merged into a group with other
+  operators it counts as injective in that group's pattern, so absorbing a
+  tuple does not make a concatenation's group more complex;
+* phase 2: an operator whose group is injective or simpler and whose
+  immediate post-dominator is a tuple already absorbed by a later group (the
+  tuple's group holds more than the tuple and is injective or simpler) fuses
+  into that group when every node between them is injective or simpler;
 * ``allow_reduce_epilogue`` (off by default) lets a reduce group absorb its
   post-dominator when every node on the way is elementwise on the reduced
   shape, a DisCo-style fusion of an op with its predecessor (DisCo Sec. 3.2,
@@ -34,7 +41,7 @@ from __future__ import annotations
 from dataclasses import dataclass
 
 from .kinds import (K_ELEMWISE, K_BROADCAST, K_INJECTIVE, K_COMM_REDUCE,
-                    K_OUT_EWISE_FUSABLE, K_OPAQUE, combine)
+                    K_OUT_EWISE_FUSABLE, K_TUPLE, K_OPAQUE, combine)
 from .postdom import postdom_tree, nodes_between, NONE
 
 
@@ -60,7 +67,11 @@ class UnionFind:
         if child_root == root:
             return
         self.parent[child_root] = root
-        self.pattern[root] = combine(self.pattern[root], self.pattern[child_root])
+        # an absorbed tuple counts as injective in the merged group
+        a, b = self.pattern[root], self.pattern[child_root]
+        a = K_INJECTIVE if a == K_TUPLE else a
+        b = K_INJECTIVE if b == K_TUPLE else b
+        self.pattern[root] = combine(a, b)
         self.size[root] += self.size[child_root]
 
 
@@ -96,7 +107,7 @@ def partition(spec, opts: Options | None = None):
                 return False
         return cond(uf.pattern[uf.find(sink)], True)
 
-    for phase in (0, 1):
+    for phase in (0, 1, 2):
         for i in range(n):
             g = uf.find(i)
             gk = uf.pattern[g]
@@ -122,8 +133,14 @@ def partition(spec, opts: Options | None = None):
                             return k <= K_INJECTIVE
                         return k <= K_INJECTIVE or k in (K_COMM_REDUCE, K_OUT_EWISE_FUSABLE)
                     ok = check_path(i, p, cond)
-            elif gk == K_INJECTIVE:
+            elif gk in (K_INJECTIVE, K_TUPLE):
                 if phase == 1 and pk[i] <= K_INJECTIVE:
+                    ok = check_path(i, p, lambda k, s: k <= K_INJECTIVE)
+            if not ok and phase == 2:
+                # into an intermediate tuple that a later group has absorbed
+                tg = uf.find(p)
+                if (gk <= K_INJECTIVE and kinds[p] == K_TUPLE and uf.size[tg] > 1
+                        and uf.pattern[tg] <= K_INJECTIVE):
                     ok = check_path(i, p, lambda k, s: k <= K_INJECTIVE)
             if not ok:
                 continue

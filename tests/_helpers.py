@@ -159,3 +159,39 @@ def dag_to_spec(n, preds, op_choice=None, outputs=()):
     for o in outputs:
         g.mark_output(vid_of[o])
     return g
+
+
+def tuple_dag(seed):
+    """Random branches (elementwise, with inputs of their own, or opaque
+    copies) joined by a tuple, usually concatenated, then a short tail."""
+    r = np.random.default_rng(seed)
+    g = GraphSpec("tuples")
+    C = int(r.choice([8, 12, 16]))
+    fields = []
+    for _ in range(int(r.integers(2, 5))):
+        rows = int(r.choice([4, 8, 12, 16]))
+        v = g.input((rows, C))
+        for _ in range(int(r.integers(0, 3))):
+            k = int(r.integers(0, 4))
+            if k == 0:
+                v = g.op("relu", (v,))
+            elif k == 1:
+                v = g.op("scale", (v,), (0.5,))
+            elif k == 2:
+                v = g.op("add", (v, g.input((rows, C))))
+            else:
+                v = g.op("opaque_copy", (v,))
+        fields.append(v)
+    t = g.op("tuple", tuple(fields))
+    if r.random() < 0.8:
+        t = g.op("concat", (t,))
+    tail = int(r.integers(0, 4))
+    for _ in range(tail):
+        k = int(r.integers(0, 3))
+        t = g.op("exp", (t,)) if k == 0 else g.op("transpose", (t,)) if k == 1 else g.op("rowsum", (t,))
+        if len(g.values[t].shape) == 1:
+            break
+    g.mark_output(t)
+    if r.random() < 0.3:
+        g.mark_output(fields[0]) if not g.values[fields[0]].is_input else None
+    return g

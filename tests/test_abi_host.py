@@ -355,3 +355,9 @@ def test_page_pattern_matmul_bias():
     plan = part.build()
     assert [sorted(gi.nodes) for gi in plan.groups] == [[0, 1], [2]]
     assert plan.groups[0].kind == "gemm"
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_partition_with_tuples_matches_oracle(seed):
+    from tests._helpers import tuple_dag
+    _parity(tuple_dag(seed))

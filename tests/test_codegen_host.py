@@ -37,3 +37,19 @@ def test_random_dag_programs_compile():
     srcs = sorted({plan.source(g) for g in range(plan.n_groups)}, key=len)
     for s in srcs[-3:] + srcs[:1]:     # the largest programs and one small one
         _compile(s)
+
+
+def test_tuple_programs_compile():
+    """Groups holding a tuple: row selects (the frame's layout) and column
+    selects (a transposed concatenation), fields at shifted boxes."""
+    for transpose in (False, True):
+        g = W.GraphSpec()
+        a = g.op("relu", (g.input((40, 32)),))
+        b = g.op("exp", (g.input((24, 32)),))
+        c = g.op("concat", (g.op("tuple", (a, b)),))
+        if transpose:
+            c = g.op("transpose", (c,))
+        g.mark_output(g.op("scale", (c,), (0.5,)))
+        plan = graph_from_spec(g).build()
+        assert plan.n_groups == 1
+        _compile(plan.source(0))

@@ -183,3 +183,72 @@ def test_invariants_random_dag_workload(seed):
     # same topology at full size -> same partition
     full = W.random_dag(seed)
     assert P.groups(full)[0] == gs
+
+
+# ---- tuples and phase 2 (TVM "Operator Fusion", Fusion rules) ---------------
+def _inception():
+    """Two branches joined by a tuple and a concatenation, then a tail."""
+    g = W.GraphSpec()
+    x1 = g.input((64, 32))
+    x2 = g.input((32, 32))
+    a = g.op("relu", (x1,))
+    b = g.op("exp", (x2,))
+    t = g.op("tuple", (a, b))
+    c = g.op("concat", (t,))
+    s = g.op("scale", (c,), (0.5,))
+    g.mark_output(s)
+    return g
+
+
+def test_phase1_absorbs_the_tuple_phase2_its_fields():
+    from oracle import partition as OP
+    spec = _inception()
+    group_of, ipdom = OP.partition(spec)
+    # the tuple fuses into the concat and its tail (phase 1); the branches,
+    # blocked by the tuple edge in phases 0 and 1, join in phase 2
+    assert ipdom[:2] == [2, 2]
+    assert group_of == [4, 4, 4, 4, 4]
+
+
+def test_phase2_only_after_absorption():
+    from oracle import partition as OP
+    g = W.GraphSpec()
+    x1 = g.input((16, 8))
+    x2 = g.input((16, 8))
+    a = g.op("relu", (x1,))
+    b = g.op("neg", (x2,))
+    t = g.op("tuple", (a, b))
+    r = g.op("rowsum", (t,))          # a tuple does not fuse into a reduction
+    g.mark_output(r)
+    group_of, _ = OP.partition(g)
+    assert group_of == [0, 1, 2, 3]
+
+
+def test_phase2_path_must_be_injective_or_simpler():
+    from oracle import partition as OP
+    g = W.GraphSpec()
+    x1 = g.input((16, 8))
+    x2 = g.input((8, 16))
+    a = g.op("exp", (x1,))
+    tr = g.op("transpose", (x2,))    # injective: joins through phase 2
+    t = g.op("tuple", (a, tr))
+    c = g.op("concat", (t,))
+    o = g.op("relu", (c,))
+    g.mark_output(o)
+    group_of, _ = OP.partition(g)
+    assert group_of == [4, 4, 4, 4, 4]
+
+
+def test_phase2_skips_a_matmul_field():
+    from oracle import partition as OP
+    g = W.GraphSpec()
+    x = g.input((16, 8), "bf16")
+    w = g.input((8, 8), "bf16")
+    y = g.input((16, 8))
+    m = g.op("matmul_bf16", (x, w), (0, 0))   # out-elementwise-fusable: never phase 2
+    r = g.op("relu", (y,))
+    t = g.op("tuple", (m, r))
+    c = g.op("concat", (t,))
+    g.mark_output(c)
+    group_of, _ = OP.partition(g)
+    assert group_of == [0, 3, 3, 3]

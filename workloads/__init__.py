@@ -27,6 +27,7 @@ OPS = (
     "add", "sub", "mul", "div", "scale", "addc", "relu", "exp", "sigmoid",
     "tanh", "neg", "badd_col", "bmul_col", "badd_row", "bmul_row",
     "transpose", "reshape", "rowsum", "rowmax", "matmul_bf16", "opaque_copy",
+    "tuple", "concat",
 )
 
 
@@ -82,6 +83,8 @@ class GraphSpec:
             return (int(attrs[0]), int(attrs[1]))
         if name in ("rowsum", "rowmax"):
             return (s[0][0],)
+        if name == "tuple":            # its fields stacked by rows
+            return (sum(x[0] for x in s), s[0][1])
         if name == "matmul_bf16":
             ta, tb = int(attrs[0]), int(attrs[1])
             m = s[0][1] if ta else s[0][0]
