@@ -15,7 +15,7 @@ out from the passages they cite:
                    (TVM "Operator Fusion", Operator Pattern Classification).
 * ``postdom``   -- immediate post-dominators by LCA on the DAG and the path
                    pattern (TVM, FuseOps > Algorithm, steps 1-2).
-* ``partition`` -- CheckPath / CommitFuse with union-find, phases 0 and 1,
+* ``partition`` -- CheckPath / CommitFuse with union-find, phases 0, 1 and 2,
                    and the constraints (TVM, FuseOps > Algorithm step 3,
                    Fusion rules).
 * ``execute``   -- unfused op-by-op execution (the semantics fusion must keep:

@@ -15,7 +15,8 @@ from tests import test_oracle_execute as TE
 
 
 def _fails(fn):
-    with pytest.raises(AssertionError):
+    # an assertion fails, or an expected error is no longer raised
+    with pytest.raises((AssertionError, pytest.fail.Exception)):
         fn()
 
 
@@ -85,3 +86,66 @@ def test_mutation_matmul_ignores_transpose_flag(monkeypatch):
     monkeypatch.setattr(E, "apply_op", bad)
     with pytest.raises((AssertionError, ValueError)):
         TE.test_matmul_equals_sum_of_outer_products()
+
+
+def test_mutation_no_phase2(monkeypatch):
+    # tuples never recognised: no phase 2, no absorbed-tuple pattern
+    monkeypatch.setattr(P, "K_TUPLE", -99)
+    _fails(TP.test_phase1_absorbs_the_tuple_phase2_its_fields)
+
+
+def test_mutation_absorbed_tuple_keeps_its_pattern(monkeypatch):
+    def union_into(self, child_root, root):
+        if child_root == root:
+            return
+        self.parent[child_root] = root
+        self.pattern[root] = max(self.pattern[root], self.pattern[child_root])
+        self.size[root] += self.size[child_root]
+    monkeypatch.setattr(P.UnionFind, "union_into", union_into)
+    _fails(TP.test_phase1_absorbs_the_tuple_phase2_its_fields)
+
+
+def test_mutation_threshold_inclusive_of_the_next_tensor(monkeypatch):
+    import oracle.buckets as B
+    from tests import test_oracle_buckets as TB
+    orig = B.threshold_buckets
+
+    def bad(numels, threshold, elem_bytes=2, align=256):
+        return orig(numels, threshold + 256, elem_bytes, align)   # lets one more tensor in
+    monkeypatch.setattr(B, "threshold_buckets", bad)
+    _fails(lambda: TB.test_threshold_closed_form_equal_sizes())
+
+
+def test_mutation_groups_never_checked_for_convexity(monkeypatch):
+    import oracle.explicit as X
+    from tests import test_oracle_explicit as TX
+    monkeypatch.setattr(X, "is_convex", lambda st, nodes: True)
+    _fails(TX.test_refused_moves)
+
+
+def test_mutation_last_pattern_wins(monkeypatch):
+    import oracle.patterns as PT
+    from tests import test_oracle_patterns as TPT
+    orig = PT.match
+    monkeypatch.setattr(PT, "match", lambda spec, patterns: orig(spec, list(reversed(patterns))))
+    _fails(TPT.test_first_pattern_wins)
+
+
+def test_mutation_allreduce_ignores_the_channel(monkeypatch):
+    import oracle.simulate as S
+    from tests import test_oracle_simulate as TS
+    orig = S.simulate
+
+    def bad(op_time, edges, tensor_producer, tensor_bytes, buckets, c, d, ar_edges=()):
+        # every bucket alone on its own channel: reduce them one at a time
+        tot, fin, st, fi = 0.0, None, [], []
+        for b in buckets:
+            t, fin, s1, f1 = orig(op_time, edges, tensor_producer, tensor_bytes, [b], c, d)
+            st += s1
+            fi += f1
+            tot = max(tot, t)
+        if not buckets:
+            return orig(op_time, edges, tensor_producer, tensor_bytes, buckets, c, d, ar_edges)
+        return tot, fin, st, fi
+    monkeypatch.setattr(S, "simulate", bad)
+    _fails(TS.test_channel_is_used_in_production_order)
