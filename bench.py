@@ -55,7 +55,8 @@ def peaks():
 
 # ---------------------------------------------------------------------------
 class Clocks:
-    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    """nvidia-smi sampled every 20 ms while the timed region runs (the timed
+    region starts once the first sample has arrived)."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -66,10 +67,14 @@ class Clocks:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            t0 = time.time()
+            while not self.rows and time.time() - t0 < 5.0 and self.proc.poll() is None:
+                time.sleep(0.005)
+            self.rows.clear()           # keep the samples taken during the timed region
         except Exception:
             self.proc = None
         return self
@@ -80,7 +85,7 @@ class Clocks:
 
     def __exit__(self, *a):
         if self.proc:
-            time.sleep(0.25)
+            time.sleep(0.03)
             self.proc.terminate()
             self.proc.wait()
 
@@ -148,7 +153,10 @@ def run_reference(args):
     dist, rank, ws, _ = setup_dist(args)
     if rank != 0:
         return
-    rows = 512
+    # each step a slab of the workload (256 rows, fewer when many steps are
+    # asked for) so that the whole run stays within a minute and a half of CPU
+    # time; the oracle takes about 1.1 ms per 4096-wide row
+    rows = max(8, min(256, int(90.0 / (args.steps + args.warmup) / 1.1e-3) // 8 * 8))
     for _ in range(args.warmup):
         cpu_sample(rows, 1)
     t0 = time.perf_counter()
@@ -171,7 +179,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-rows", action="store_true", help="skip the secondary rows")
