@@ -8,6 +8,7 @@ machine without a GPU driver (graph building and grouping then still work).
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import os
 import shutil
 import subprocess
@@ -76,11 +77,24 @@ def stale():
 
 
 def build(force=False, verbose=False, jobs=None):
-    """Compile (if stale) and return the path of libgroupexec.so."""
+    """Compile (if stale) and return the path of libgroupexec.so.  Processes
+    building at once (parallel test workers) take turns on a lock file; the
+    others then find the library fresh."""
     if not force and not stale():
         return LIB
-    cuda = _cuda_home()
     os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, ".lock"), "w") as lk:
+        fcntl.flock(lk, fcntl.LOCK_EX)
+        try:
+            if not force and not stale():
+                return LIB
+            return _build_locked(verbose, jobs)
+        finally:
+            fcntl.flock(lk, fcntl.LOCK_UN)
+
+
+def _build_locked(verbose, jobs):
+    cuda = _cuda_home()
     write_embed()
     srcs = sources()
     objs = [os.path.join(BUILD, os.path.basename(s) + ".o") for s in srcs]

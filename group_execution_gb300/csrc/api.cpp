@@ -499,20 +499,35 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
       p.inplace_off = cg.leaf_stage_off[i];
       break;
     }
+  // Cluster shape and ring granularity.  Two pairs on side-by-side tiles may
+  // share their A rows (4-CTA clusters), and a ring slot holds one or two K
+  // blocks; the interpreter keeps pairs and two-block slots.  Flag bits
+  // 16-17: 1 = pairs only, 2 = 4-CTA clusters whenever the output has two
+  // tile columns; bits 18-19: 1 or 2 K blocks per slot (0 = chosen).
+  ge.compiled = !(o.flags & FG_FLAG_INTERPRET);
+  const int shape = (o.flags >> 16) & 3, kbf = (o.flags >> 18) & 3, sched = (o.flags >> 20) & 3;
+  const bool c4 = ge.compiled && p.ntn >= 2 && shape == 2;
+  const int KB = ge.compiled && kbf == 1 ? 1 : 2;
+  const int CL = c4 ? kGemmCluster4 : kGemmCluster, PR = CL / 2;
+  if (c4) p.a_3d = 0;   // each CTA fetches half of an A half: 2-D boxes
+  cg.gemm_cl = CL;
+  cg.gemm_kb = KB;
   // operand ring and epilogue-leaf ring depths that fit 227 KB, in order of
   // preference: long K needs a deep operand ring (its feed is latency bound),
   // short K a deep leaf ring (the epilogue streams the leaves from HBM).  A
-  // ring slot holds two K blocks of the CTA's 128 rows of A and of its half of
+  // ring slot holds KB K blocks of the CTA's 128 rows of A and of its half of
   // B's columns.
   const int limit = 227 * 1024 - 256, fixed = 2048 + (p.inplace_off >= 0 ? 0 : 2 * kGemmM * kGemmChunk * 4);
-  const int stage = kGemmKB * (kGemmM + kGemmN / kGemmCluster) * kGemmK * 2;
+  const int stage = KB * (kGemmM + kGemmN / 2) * kGemmK * 2;
   int ns = 0, ne = 0;
   static const std::vector<std::pair<int, int>> prefs_short = {{2, 6}, {2, 5}, {2, 4}, {2, 3}, {2, 2}};
   static const std::vector<std::pair<int, int>> prefs_long = {{3, 2}, {2, 4}, {2, 3}, {2, 2}};
   const bool short_k = p.nkb <= 16 && cg.stage_bytes > 0;
   for (const auto& q : short_k ? prefs_short : prefs_long) {
-    if (!ns && fixed + q.first * stage + q.second * cg.stage_bytes <= limit) {
-      ns = q.first;
+    // the same bytes in flight with one-block slots: twice as many
+    const int qs = q.first * (2 / KB);
+    if (!ns && fixed + qs * stage + q.second * cg.stage_bytes <= limit) {
+      ns = qs;
       ne = q.second;
     }
   }
@@ -525,25 +540,41 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
   ge.smem = std::max(ge.smem, 120 * 1024);
   cg.nstages = ns;
   ge.big = cg.depth > 4 || cg.slots > 4;
-  ge.compiled = !(o.flags & FG_FLAG_INTERPRET);
   ge.min_blocks = 1;
-  // CTA pairs walk 256-row tile units; one CTA per SM (flag bits 8-15, when
-  // set, cap the number of pairs: a test hook for the split tail)
-  const int units = ((p.ntm + kGemmCluster - 1) / kGemmCluster) * p.ntn;
-  int pairs = std::max(1, std::min(units, nsm / kGemmCluster));
+  // units of the cluster's 256 rows x PR 256-column tiles; one CTA per SM,
+  // as many clusters as run at once (flag bits 8-15, when set, cap them: a
+  // test hook for the split schedules)
+  const int nslots = (p.nkb + KB - 1) / KB;
+  const int units = ((p.ntm + 1) / 2) * ((p.ntn + PR - 1) / PR);
+  p.nunits = units;
+  int avail = gemm_max_clusters(CL, ge.smem);
+  if (avail <= 0) avail = nsm / CL;
+  int ncl = std::max(1, std::min(units, avail));
   const int cap = (o.flags >> 8) & 0xff;
-  if (cap > 0) pairs = std::min(pairs, cap);
-  ge.grid = kGemmCluster * pairs;
-  // split the last round's units along K into halves over the pairs it would
-  // leave idle, when K is long enough for the halves to outweigh the partial
-  // sums' traffic (two pieces: their sum does not depend on which ends last)
-  const int nslots = (p.nkb + kGemmKB - 1) / kGemmKB;
-  const int tail = units % pairs;
+  if (cap > 0) ncl = std::min(ncl, cap);
+  ge.grid = CL * ncl;
   p.nfull = units;
   p.split = 1;
-  if (units > pairs && tail > 0 && 2 * tail <= pairs && nslots >= 8) {
+  p.sk = 0;
+  const int tail = units % ncl;
+  if (sched == 2 || (sched == 0 && c4)) {
+    // every cluster takes an equal share of all units' ring slots; a share
+    // spans at least one unit, so a unit is cut at most once
+    if (units > ncl && tail > 0) {
+      p.sk = 1;
+      p.split = 2;
+    }
+  } else if (units > ncl && tail > 0 && 2 * tail <= ncl && p.nkb >= 16) {
+    // split the last round's units along K into halves over the pairs it
+    // would leave idle, when K is long enough for the halves to outweigh the
+    // partial sums' traffic (two pieces: their sum does not depend on which
+    // ends last)
     p.nfull = units - tail;
     p.split = 2;
+    // the first piece also writes its partial (about ten K blocks' worth of
+    // MMA time): it takes that much less of K, so that its partial is ready
+    // when the second piece's MMAs end
+    p.split_at = std::max(1, std::min(nslots / 2, (nslots - 10 / KB) / 2));
   }
 }
 
@@ -577,11 +608,13 @@ fg_status alloc_device(fg_plan* p, GroupExec& ge) {
     GemmParams& mp = *ge.mp;
     mp.err = p->d_err;
     if (mp.split > 1) {
-      const int units = ((mp.ntm + kGemmCluster - 1) / kGemmCluster) * mp.ntn;
-      const size_t tail = (size_t)(units - mp.nfull);
-      cudaError_t e = cudaMalloc(&ge.scratch, sizeof(float) * tail * mp.split * kGemmCluster * kGemmM * kGemmN);
+      // split units: the last round's (round robin), or one per share
+      // boundary (stream-K); two pieces each
+      const int CL = ge.cg.gemm_cl;
+      const size_t keys = mp.sk ? (size_t)(ge.grid / CL - 1) : (size_t)(mp.nunits - mp.nfull);
+      cudaError_t e = cudaMalloc(&ge.scratch, sizeof(float) * keys * 2 * CL * kGemmM * kGemmN);
       if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(split-tail workspace)");
-      ge.counter_bytes = sizeof(int32_t) * tail * kGemmCluster * 4;
+      ge.counter_bytes = sizeof(int32_t) * keys * CL * 4;
       e = cudaMalloc(&ge.counters, ge.counter_bytes);
       if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(split-tail counters)");
       e = cudaMemset(ge.counters, 0, ge.counter_bytes);
@@ -681,25 +714,30 @@ fg_status launch_gemm(GroupExec& ge, void* const* ptrs, void* stream) {
       //   MN-major [extent/64][K][64], box 64 x 128 K rows x 2 groups;
       //   K-major  [K/64][rows][64],   box 64 x 128 rows x 2 K blocks.
       // Otherwise 2-D boxes: MN-major 64 x 64, K-major 64 x 128 rows.
+      // With KB K blocks per ring slot the 3-D boxes cover KB * 64 K rows
+      // (MN-major) or KB K blocks (K-major).  In 4-CTA clusters with one K
+      // block per slot each CTA fetches 64 of its 128 A rows (K-major box
+      // 64 x 64).
       uint64_t dims[3], strides[2];
       uint32_t box[3];
-      auto view = [&](bool mn, bool v3, int64_t rows) {
+      const int KB = cg.gemm_kb;
+      auto view = [&](bool mn, bool v3, int64_t rows, bool half_rows) {
         const int64_t inner = mn ? rows : cg.K, outer = mn ? cg.K : rows;
         if (v3) {
           dims[0] = 64; dims[1] = outer; dims[2] = inner / 64; strides[0] = inner * 2; strides[1] = 128;
-          box[0] = 64; box[1] = 128; box[2] = 2;
+          box[0] = 64; box[1] = mn ? 64 * KB : 128; box[2] = mn ? 2 : KB;
           return 3;
         }
-        dims[0] = inner; dims[1] = outer; strides[0] = inner * 2; box[0] = 64; box[1] = mn ? 64 : 128;
+        dims[0] = inner; dims[1] = outer; strides[0] = inner * 2; box[0] = 64; box[1] = mn || half_rows ? 64 : 128;
         return 2;
       };
-      int rank = view(gp.a_mn, gp.a_3d, cg.M);
+      int rank = view(gp.a_mn, gp.a_3d, cg.M, cg.gemm_cl == kGemmCluster4 && KB == 1);
       if (fg_status st = encode(&gp.mapA, ptrs[cg.mm_a], rank, dims, strides, box, true,
                                 CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
         return st;
       // B: [K, N] (N contiguous), or [N, K] when transposed; each CTA of a
       // pair stages its half of the tile's columns
-      rank = view(gp.b_mn, gp.b_3d, cg.N);
+      rank = view(gp.b_mn, gp.b_3d, cg.N, false);
       if (fg_status st = encode(&gp.mapB, ptrs[cg.mm_b], rank, dims, strides, box, true,
                                 CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
         return st;

@@ -162,9 +162,10 @@ struct GroupParams {
 // GEMM + epilogue kernel: 128 x 256 accumulator tiles in TMEM, K in blocks
 // of 64, the epilogue in 128 x 32 column chunks.
 constexpr int kGemmM = 128, kGemmN = 256, kGemmK = 64, kGemmChunk = 32;
-constexpr int kGemmKB = 2;             // K blocks per operand ring slot
-constexpr int kGemmWarps = 7;          // TMA, MMA, epilogue loads, 4 epilogue warps
+constexpr int kGemmKB = 2;             // K blocks per operand ring slot (interpreted kernel; compiled: 1 or 2)
+constexpr int kGemmWarps = 8;          // A loads, MMA, epilogue loads, 4 epilogue warps, B loads
 constexpr int kGemmCluster = 2;        // CTAs of a pair issuing 2-SM MMAs on one 256-row tile
+constexpr int kGemmCluster4 = 4;       // two pairs on adjacent 256-column tiles sharing their A rows
 
 struct GemmParams {
   CUtensorMap mapA, mapB;              // bf16 operands (boxes per major-ness)
@@ -185,13 +186,20 @@ struct GemmParams {
   int32_t epi_stage_bytes, epi_tx_bytes, n_epi_bufs;
   int32_t inplace_off;                 // >= 0: the result overwrites this IDENT leaf's chunk (no out buffers)
   int32_t inject;                      // failure injection: 1 = the producers issue no loads
-  // the last round's tiles split along K: tile units [0, nfull) run whole;
-  // each later unit runs as split = 2 pieces (pieces 2u, 2u+1) whose partial
-  // accumulators meet in the workspace, where the piece that finishes second
-  // adds the other's and runs the epilogue
-  int32_t nfull, split;
-  float* ws;                           // [pieces][2 CTAs][64 column quads][128 rows][4] partial accumulators
-  int32_t* ws_cnt;                     // [split units][2 CTAs][4 warps] arrival counters (reset by the last)
+  // work units: a cluster's tiles (the pair's 256 x 256 tile, or the two
+  // pairs' 256 x 512) in row-major order
+  int32_t nunits;
+  // round-robin schedule: units [0, nfull) run whole; each later unit runs
+  // as split = 2 pieces along K, ring slots [0, split_at) and
+  // [split_at, nslots); the first publishes its partial accumulator in the
+  // workspace, the second adds it and runs the epilogue
+  int32_t nfull, split, split_at;
+  // sk = 1: each cluster runs a contiguous 1/ncl share of all units' ring
+  // slots instead (at least one whole unit, so a unit is cut at most once,
+  // into the two pieces on either side of a share boundary)
+  int32_t sk;
+  float* ws;                           // [pieces][cluster CTAs][64 column quads][128 rows][4] partial accumulators
+  int32_t* ws_cnt;                     // [split units][cluster CTAs][4 warps] partial-ready flags (cleared by the reader)
 };
 
 // Loads already issued always land; waiting for them before a CTA exits uses

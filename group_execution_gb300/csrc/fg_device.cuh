@@ -77,6 +77,13 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, int32_t x, in
                ::"l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(src)
                : "memory");
 }
+// Contiguous copy global -> shared (both 16-byte aligned, bytes a multiple
+// of 16), counted on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
@@ -383,19 +390,16 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uin
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
-// Arrives once on the mbarrier at `bar` when every MMA issued so far by this
-// thread has completed; with CG = 2 on that offset in both CTAs of the pair.
-template <int CG>
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  if constexpr (CG == 1)
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-  else
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            bar),
-        "h"((uint16_t)3)
-        : "memory");
+// Arrives once on the mbarrier at `bar` in every CTA of the cluster whose bit
+// is set in `mask` when every 2-SM MMA issued so far by this thread has
+// completed (the pair's two CTAs; a 4-CTA cluster also releases a ring slot
+// to the other pair's producers this way).
+__device__ __forceinline__ void tc_commit_mask(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          bar),
+      "h"(mask)
+      : "memory");
 }
 // 32 consecutive f32 columns of this warp's 32 TMEM lanes (one lane per thread).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
@@ -446,6 +450,16 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
       : "memory");
   return ok != 0;
 }
+// Flags between CTAs: a release store after the data it publishes, an
+// acquire load before the data it guards is read.
+__device__ __forceinline__ void st_release_gpu(int32_t* p, int32_t v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 // L2 eviction policies for TMA copies: operand tiles that other tiles will
 // read again stay (evict_last); data streamed once goes first (evict_first).
 __device__ __forceinline__ uint64_t l2_evict_last() {
@@ -476,6 +490,17 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(cbar), "l"(policy)
+      : "memory");
+}
+// The same tile delivered to the same offset in every CTA of `mask`; each
+// destination's bytes are counted on the barrier at cbar's offset in the CTA
+// of the destination's pair that cbar names (cbar's peer bit).
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* m, int32_t x, int32_t y,
+                                                    uint32_t cbar, uint16_t mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(cbar), "h"(mask), "l"(policy)
       : "memory");
 }
 // Hinted single-CTA loads and stores (GEMM epilogue streams).

@@ -5,15 +5,22 @@
 // elementwise successors; TAG's sufficient-factor gradient G = U^T V is the
 // workload).
 //
-// Persistent: CTAs run in pairs (a 2-CTA cluster) on the SMs of one TPC, and
-// a pair walks 256 x 256 output tiles.  Each CTA stages half of the tile's A
-// rows and half of its B columns, two 64-deep K blocks (64 KB) per ring slot,
-// each operand half in one TMA copy where the layout allows; the even CTA
-// issues 2-SM tcgen05.mma instructions (cta_group::2) that read both CTAs'
-// halves and leave each CTA's 128 accumulator rows in its own TMEM.  Warp
-// roles, in each CTA:
-//   warp 0  TMA producer of the bf16 operand halves; every load completes on
-//           the even CTA's stage barrier,
+// Persistent: CTAs run in pairs on the SMs of one TPC, and a pair walks
+// 256 x 256 output tiles.  Each CTA stages half of the tile's A rows and half
+// of its B columns, two 64-deep K blocks (64 KB) per ring slot, each operand
+// half in one TMA copy where the layout allows; the even CTA issues 2-SM
+// tcgen05.mma instructions (cta_group::2) that read both CTAs' halves and
+// leave each CTA's 128 accumulator rows in its own TMEM.  In a 4-CTA cluster
+// two pairs take side-by-side tiles of the same 256 rows: each A half is
+// fetched once, by the two CTAs that need it taking one K block each and
+// multicasting it to both, so the cluster reads 3/4 of the operand bytes
+// two independent pairs would.  Warp roles, in each CTA:
+//   warp 0  TMA producer of the bf16 A halves, arming the even CTA's slot
+//           barrier; every operand load completes on the even CTA's slot
+//           barrier of each destination's pair,
+//   warp 7  TMA producer of the B halves (a slot's copies issue at a few
+//           hundred ns each from one thread: two producers halve the time
+//           from a slot's release to its refill),
 //   warp 1  allocates TMEM (2 x 256 columns: double-buffered accumulator,
 //           jointly with the peer) and, in the even CTA, issues the MMAs from
 //           one thread,
@@ -152,81 +159,166 @@ __device__ __forceinline__ bool gemm_wait(uint32_t bar, uint32_t parity, int64_t
   return true;
 }
 
-// One item of a pair's work list: a whole tile unit, or one K piece (ring
-// slots [sl0, sl1)) of a unit of the split last round.
-struct GemmItem {
-  int unit, piece, sl0, sl1, q;   // piece = -1 for a whole unit; q = index among all pieces
+// A cluster's work list: item indices [x0, end) in steps of `step`.  Round
+// robin: items are whole units, then the pieces of the split last round.
+// Stream-K (P.sk): the cluster owns ring slots [b0, b1) of the sequence of
+// all units' slots, and its items are the units that range touches.
+struct GemmSched {
+  int x0, end, step;
+  int64_t b0, b1;
 };
-__device__ __forceinline__ GemmItem gemm_item(const GemmParams& P, int idx, int nslots) {
+__device__ __forceinline__ GemmSched gemm_sched(const GemmParams& P, int cl, int ncl, int nslots) {
+  GemmSched S;
+  if (P.sk) {
+    const int64_t W = (int64_t)P.nunits * nslots;
+    S.b0 = W * cl / ncl;
+    S.b1 = W * (cl + 1) / ncl;
+    S.x0 = (int)(S.b0 / nslots);
+    S.end = S.b1 > S.b0 ? (int)((S.b1 - 1) / nslots) + 1 : S.x0;
+    S.step = 1;
+  } else {
+    S.b0 = S.b1 = 0;
+    S.x0 = cl;
+    S.end = P.nfull + (P.nunits - P.nfull) * P.split;
+    S.step = ncl;
+  }
+  return S;
+}
+
+// One item: a whole unit, or one K piece (ring slots [sl0, sl1)) of a unit
+// cut in two.  q indexes the piece's workspace (q ^ 1 is the other piece of
+// the same unit) and key its ready flags.  The piece that runs later
+// finishes the unit (fin): the other publishes its partial accumulator.
+struct GemmItem {
+  int unit, piece, sl0, sl1, q, key;   // piece = -1 for a whole unit
+  bool fin;
+};
+__device__ __forceinline__ GemmItem gemm_item(const GemmParams& P, const GemmSched& S, int cl, int idx,
+                                              int nslots) {
   GemmItem w;
-  if (idx < P.nfull) {
+  w.piece = w.q = w.key = -1;
+  w.fin = true;
+  if (P.sk) {
     w.unit = idx;
-    w.piece = -1;
+    const int64_t base = (int64_t)idx * nslots;
+    w.sl0 = (int)(S.b0 > base ? S.b0 - base : 0);
+    w.sl1 = (int)(S.b1 - base < nslots ? S.b1 - base : nslots);
+    if (w.sl0 > 0 || w.sl1 < nslots) {
+      // a share boundary cuts this unit: piece 0 ends cluster cl's share
+      // (boundary cl + 1), piece 1 starts it (boundary cl)
+      w.piece = w.sl0 == 0 ? 0 : 1;
+      w.key = (w.piece == 0 ? cl + 1 : cl) - 1;
+      w.q = 2 * w.key + w.piece;
+      w.fin = w.piece == 0;   // ends the share: its other piece ran first in the next share
+    }
+  } else if (idx < P.nfull) {
+    w.unit = idx;
     w.sl0 = 0;
     w.sl1 = nslots;
-    w.q = -1;
   } else {
     w.q = idx - P.nfull;
     w.unit = P.nfull + w.q / P.split;
-    w.piece = w.q % P.split;
-    w.sl0 = w.piece * nslots / P.split;
-    w.sl1 = (w.piece + 1) * nslots / P.split;
+    w.key = w.unit - P.nfull;
+    w.piece = w.q & 1;
+    // the first piece is the shorter: it also writes its partial, and is
+    // done when the second's MMAs end
+    w.sl0 = w.piece ? P.split_at : 0;
+    w.sl1 = w.piece ? nslots : P.split_at;
+    w.fin = w.piece == 1;
   }
   return w;
 }
 
+// One operand half of a ring slot (this CTA's 128 rows of A or columns of
+// B, KB K blocks from k0) into this CTA's shared memory, counted on the pair
+// barrier cbar: one copy through a 3-D view, or 2-D boxes.
+template <int KB>
+__device__ __forceinline__ void gemm_load_half(uint32_t dst, const CUtensorMap* m, int mn, int v3, int r0, int k0,
+                                               uint32_t cbar, uint64_t keep) {
+  if (mn) {
+    if (v3) {
+      tma_load_3d_pair(dst, m, 0, k0, r0 / 64, cbar, keep);
+    } else {
+#pragma unroll
+      for (int g = 0; g < 2; ++g)
+#pragma unroll
+        for (int j = 0; j < KB; ++j)
+          tma_load_2d_pair(dst + g * (KB * 8192) + j * 8192, m, r0 + 64 * g, k0 + 64 * j, cbar, keep);
+    }
+  } else if (v3) {
+    tma_load_3d_pair(dst, m, 0, r0, k0 / 64, cbar, keep);
+  } else {
+#pragma unroll
+    for (int j = 0; j < KB; ++j) tma_load_2d_pair(dst + j * 16384, m, k0 + 64 * j, r0, cbar, keep);
+  }
+}
+
 // CL = 2: a CTA pair per 256 x 256 tile (cta_group::2), each CTA holding
-// half of A's rows and half of B's columns.
-template <class Epi, int CL>
+// half of A's rows and half of B's columns.  CL = 4: two such pairs on the
+// two 256-column halves of a 256 x 512 unit, sharing their A halves.  KB: K
+// blocks of 64 per operand ring slot (1: 32 KB slots, 2: 64 KB).
+template <class Epi, int CL, int KB>
 __device__ __forceinline__ void gemm_body(const GemmParams& P) {
-  static_assert(CL == 2, "the kernel runs CTA pairs");
-  constexpr int kBCols = kGemmN / CL;                              // B columns staged per CTA
-  constexpr int kHalfA = kGemmKB * kGemmABytes;                    // 32 KB: 128 rows x 2 K blocks
-  constexpr int kStageBytes = kHalfA + kGemmKB * kBCols * kGemmK * 2;   // 64 KB per CTA
+  static_assert(CL == 2 || CL == 4, "the kernel runs CTA pairs, alone or two by two");
+  static_assert(KB == 1 || KB == 2, "one or two K blocks per ring slot");
+  constexpr int PR = CL / 2;                                       // pairs per cluster
+  constexpr int kBCols = kGemmN / 2;                               // B columns staged per CTA
+  constexpr int kHalfA = KB * kGemmABytes;                         // 128 rows x KB K blocks
+  constexpr int kStageBytes = kHalfA + KB * kBCols * kGemmK * 2;   // 32 KB per K block and CTA
   extern __shared__ uint8_t smem_raw[];
   __shared__ int abort_flag;
+  __shared__ int issued[2];            // operand slots issued by the A and B producers
   __shared__ uint32_t tmem_slot;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // barriers: full[16] empty[16] tfull[2] tempty[2] efull[8] eempty[8] done
+  // last[4] (one per epilogue warp)
   const uint32_t bars = smem_u32(smem);
   const uint32_t full0 = bars, empty0 = bars + 128, tfull0 = bars + 256, tempty0 = bars + 272;
-  const uint32_t efull0 = bars + 288, eempty0 = bars + 352, done_bar = bars + 416;
+  const uint32_t efull0 = bars + 288, eempty0 = bars + 352, done_bar = bars + 416, last0 = bars + 424;
   uint8_t* opnd = smem + 1024;
   const int NS = P.nstages, NE = P.n_epi_bufs;
   uint8_t* ebuf = opnd + NS * kStageBytes;
   uint8_t* obuf = ebuf + NE * P.epi_stage_bytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool staged = P.epi_tx_bytes > 0;
-  const int nslots = (P.nkb + kGemmKB - 1) / kGemmKB;             // ring slots per tile
+  const int nslots = (P.nkb + KB - 1) / KB;                       // ring slots per tile
 
   const uint32_t rank = cluster_ctarank();
-  const bool leader = rank == 0;
-  // tile sequence: units of CL vertically adjacent 128-row tiles
+  const int h = (int)(rank & 1), pr = (int)(rank >> 1);   // CTA within its pair, pair within the cluster
+  const bool leader = h == 0;
+  const uint32_t even = rank & ~1u;                       // the pair's MMA-issuing CTA
+  const uint16_t pair_mask = (uint16_t)(3u << (2 * pr));
+  // ring slots are released to every producer that writes into them: the
+  // pair's own, and with CL = 4 the other pair's (A multicast)
+  const uint16_t slot_mask = (uint16_t)((1u << CL) - 1);
+  // unit u: 256 rows of block u / nsn and PR tiles of 256 columns; this CTA
+  // works on rows h, pair pr's columns
   const int ncl = gridDim.x / CL, cl = blockIdx.x / CL;
-  const int npm = (P.ntm + CL - 1) / CL, nunits = npm * P.ntn;
-  const int nitems = P.nfull + (nunits - P.nfull) * P.split;
+  const int nsn = (P.ntn + PR - 1) / PR;
   auto tile_of = [&](int u, int& m0, int& n0) {
-    m0 = ((u / P.ntn) * CL + (int)rank) * kGemmM;
-    n0 = (u % P.ntn) * kGemmN;
+    m0 = ((u / nsn) * 2 + h) * kGemmM;
+    n0 = ((u % nsn) * PR + pr) * kGemmN;
   };
   if (threadIdx.x == 0) {
     abort_flag = 0;
+    issued[0] = issued[1] = 0;
     for (int s = 0; s < NS; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, PR);   // one commit from each pair's MMA issuer
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull0 + 8 * b, 1);
-      mbar_init(tempty0 + 8 * b, 4 * CL);   // every epilogue warp of the pair
+      mbar_init(tempty0 + 8 * b, 4 * 2);   // every epilogue warp of the pair
     }
     for (int e = 0; e < NE; ++e) {
       mbar_init(efull0 + 8 * e, 1);
       mbar_init(eempty0 + 8 * e, 4);
     }
     mbar_init(done_bar, 1);
+    for (int k = 0; k < 4; ++k) mbar_init(last0 + 8 * k, 1);
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc<CL>(smem_u32(&tmem_slot), 512);
+  if (warp == 1) tmem_alloc<2>(smem_u32(&tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
   cluster_sync();   // the peer's barriers are initialised before any remote arrival
@@ -234,93 +326,102 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   const uint32_t tmem = tmem_slot;
   const int64_t limit = P.wait_limit_ns;
   const int64_t drain = limit > kDrainLimitNs ? limit : kDrainLimitNs;
+  const GemmSched S = gemm_sched(P, cl, ncl, nslots);
 
-  if (warp == 0) {
-    // ---- operand producer ----
+  if (warp == 0 || warp == 7) {
+    // ---- operand producers: warp 0 the A halves, warp 7 the B halves ----
     // Ring slot layouts (per CTA), each 128-byte row 128B-swizzled:
-    //   K-major operand:  [K block][128 rows][64 K]        (16 KB per K block)
-    //   MN-major operand: [64-wide group][128 K rows][64]  (16 KB per group)
+    //   K-major operand:  [K block][128 rows][64 K]           (16 KB per K block)
+    //   MN-major operand: [64-wide group][KB * 64 K rows][64]  (KB * 8 KB per group)
+    const bool isA = warp == 0;
     if (lane == 0 && !P.inject) {
-      tma_prefetch(&P.mapA);
-      tma_prefetch(&P.mapB);
+      tma_prefetch(isA ? &P.mapA : &P.mapB);
       const uint64_t keep = l2_evict_last();   // every operand tile is read by several tiles
-      int it = 0;
+      // both CTAs' halves are counted on the even CTA's barrier, which the
+      // even CTA alone arms with the whole slot's bytes (blocks past K
+      // arrive zero-filled and count in full)
+      const uint32_t cbar0 = cluster_addr(full0, even), ring = smem_u32(opnd);
+      int it = 0, s = 0;
+      uint32_t ph = 0;   // ring position and phase parity
       bool ok = true;
-      for (int x = cl; x < nitems && ok; x += ncl) {
-        const GemmItem w = gemm_item(P, x, nslots);
+      for (int x = S.x0; x < S.end && ok; x += S.step) {
+        const GemmItem w = gemm_item(P, S, cl, x, nslots);
         int m0, n0;
         tile_of(w.unit, m0, n0);
-        const int nb = n0 + (int)rank * kBCols;
-        for (int sl = w.sl0; sl < w.sl1; ++sl, ++it) {
-          const int s = it % NS;
-          if (it >= NS && !gemm_wait(empty0 + 8 * s, ((it / NS) & 1) ^ 1, limit, &abort_flag)) {
+        const int nb = n0 + h * kBCols;
+        for (int sl = w.sl0; sl < w.sl1; ++sl) {
+          if (it >= NS && !gemm_wait(empty0 + 8 * s, ph ^ 1, limit, &abort_flag)) {
             ok = false;
             break;
           }
-          const uint32_t a = smem_u32(opnd + s * kStageBytes), b = a + kHalfA;
-          const int k0 = sl * kGemmKB * kGemmK;
-          // both CTAs' halves are counted on the even CTA's barrier, which
-          // the even CTA alone arms with the whole slot's bytes (blocks past
-          // K arrive zero-filled and count in full)
-          const uint32_t cbar = cluster_addr(full0 + 8 * s, 0);
-          if (leader) mbar_expect_tx(full0 + 8 * s, CL * kStageBytes);
-          if (P.a_mn) {
-            if (P.a_3d) {
-              tma_load_3d_pair(a, &P.mapA, 0, k0, m0 / 64, cbar, keep);
-            } else {
-#pragma unroll
-              for (int g = 0; g < 2; ++g)
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-                  tma_load_2d_pair(a + g * 16384 + j * 8192, &P.mapA, m0 + 64 * g, k0 + 64 * j, cbar, keep);
-            }
-          } else if (P.a_3d) {
-            tma_load_3d_pair(a, &P.mapA, 0, m0, k0 / 64, cbar, keep);
-          } else {
-#pragma unroll
-            for (int j = 0; j < kGemmKB; ++j) tma_load_2d_pair(a + j * 16384, &P.mapA, k0 + 64 * j, m0, cbar, keep);
+          const uint32_t a = ring + s * kStageBytes, b = a + kHalfA, cbar = cbar0 + 8 * s, fbar = full0 + 8 * s;
+          const int k0 = sl * KB * kGemmK;
+          ++it;
+          if (++s == NS) {
+            s = 0;
+            ph ^= 1;
           }
-          if (P.b_mn) {
-            if (P.b_3d) {
-              tma_load_3d_pair(b, &P.mapB, 0, k0, nb / 64, cbar, keep);
+          if (!isA) {
+            gemm_load_half<KB>(b, &P.mapB, P.b_mn, P.b_3d, nb, k0, cbar, keep);
+            continue;
+          }
+          if (leader) mbar_expect_tx(fbar, 2 * kStageBytes);
+          if constexpr (CL == 4) {
+            // A rows h are shared by CTAs h and h + 2: pair pr fetches half of
+            // them for both (2-D boxes): K block pr of two, or with one K
+            // block its 64-wide group pr (MN-major) or rows 64 pr.. (K-major)
+            const uint16_t mc = (uint16_t)((1u << h) | (1u << (h + 2)));
+            if constexpr (KB == 2) {
+              if (P.a_mn) {
+#pragma unroll
+                for (int g = 0; g < 2; ++g)
+                  tma_load_2d_pair_mc(a + g * 16384 + pr * 8192, &P.mapA, m0 + 64 * g, k0 + 64 * pr, cbar, mc, keep);
+              } else {
+                tma_load_2d_pair_mc(a + pr * 16384, &P.mapA, k0 + 64 * pr, m0, cbar, mc, keep);
+              }
+            } else if (P.a_mn) {
+              tma_load_2d_pair_mc(a + pr * 8192, &P.mapA, m0 + 64 * pr, k0, cbar, mc, keep);
             } else {
-#pragma unroll
-              for (int g = 0; g < 2; ++g)
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-                  tma_load_2d_pair(b + g * 16384 + j * 8192, &P.mapB, nb + 64 * g, k0 + 64 * j, cbar, keep);
+              tma_load_2d_pair_mc(a + pr * 8192, &P.mapA, k0, m0 + 64 * pr, cbar, mc, keep);
             }
-          } else if (P.b_3d) {
-            tma_load_3d_pair(b, &P.mapB, 0, nb, k0 / 64, cbar, keep);
           } else {
-#pragma unroll
-            for (int j = 0; j < kGemmKB; ++j) tma_load_2d_pair(b + j * 16384, &P.mapB, k0 + 64 * j, nb, cbar, keep);
+            gemm_load_half<KB>(a, &P.mapA, P.a_mn, P.a_3d, m0, k0, cbar, keep);
           }
         }
       }
+      issued[isA ? 0 : 1] = it;
       if (!ok) {
         abort_flag = 1;
         set_error(P.err, DEVERR_TIMEOUT);
-        // loads in flight complete on the even CTA's barriers: that CTA
-        // drains them (the odd CTA stays resident until then, at the final
-        // cluster barrier)
-        if (leader)
-          for (int k = it - NS < 0 ? 0 : it - NS; k < it; ++k) mbar_wait(full0 + 8 * (k % NS), (k / NS) & 1, drain);
       }
     }
   } else if (warp == 1) {
     // ---- MMA issuer (the even CTA of a pair) ----
     if (lane == 0 && leader) {
-      const uint32_t idesc = idesc_bf16_f32(CL * kGemmM, kGemmN, P.a_mn, P.b_mn);
+      const uint32_t idesc = idesc_bf16_f32(2 * kGemmM, kGemmN, P.a_mn, P.b_mn);
       // MN-major: atoms of 64 (M or N) x 8 K rows, 64-wide groups 16 KB
       // apart; K-major: atoms of 8 rows x 64 K, K blocks 16 KB apart
-      const uint32_t a_lbo = P.a_mn ? 16384 : 16, b_lbo = P.b_mn ? 16384 : 16;
+      const uint32_t a_lbo = P.a_mn ? KB * 8192 : 16, b_lbo = P.b_mn ? KB * 8192 : 16;
       const uint32_t a_blk = P.a_mn ? 8192 : 16384, b_blk = P.b_mn ? 8192 : 16384;   // next K block
       const uint32_t a_step = P.a_mn ? 2048 : 32, b_step = P.b_mn ? 2048 : 32;         // next 16 of K
-      int it = 0, i = 0;
+      // a descriptor's start-address field holds address >> 4 in 14 bits and
+      // the ring lies below 2^18 bytes, so descriptors advance by adding
+      // offset >> 4: built once here, not per MMA
+      const uint32_t ring = smem_u32(opnd);
+      const uint64_t ad0 = smem_desc_sw128(ring, a_lbo, 1024), bd0 = smem_desc_sw128(ring + kHalfA, b_lbo, 1024);
+      uint32_t aoff[KB * 4], boff[KB * 4];
+#pragma unroll
+      for (int j = 0; j < KB; ++j)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          aoff[j * 4 + kk] = (j * a_blk + kk * a_step) >> 4;
+          boff[j * 4 + kk] = (j * b_blk + kk * b_step) >> 4;
+        }
+      int s = 0, i = 0;
+      uint32_t ph = 0;   // ring position and phase parity
       bool ok = true;
-      for (int x = cl; x < nitems && ok; x += ncl, ++i) {
-        const GemmItem w = gemm_item(P, x, nslots);
+      for (int x = S.x0; x < S.end && ok; x += S.step, ++i) {
+        const GemmItem w = gemm_item(P, S, cl, x, nslots);
         const int b = i & 1;
         if (i >= 2) {
           // both CTAs' epilogues have drained this accumulator buffer
@@ -337,36 +438,37 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         }
         tc_fence_after();
         const uint32_t d = tmem + b * kGemmN;
-        for (int sl = w.sl0; sl < w.sl1; ++sl, ++it) {
-          const int s = it % NS;
-          if (!gemm_wait(full0 + 8 * s, (it / NS) & 1, limit, &abort_flag)) {
+        for (int sl = w.sl0; sl < w.sl1; ++sl) {
+          if (!gemm_wait(full0 + 8 * s, ph, limit, &abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a = smem_u32(opnd + s * kStageBytes), bb = a + kHalfA;
+          const uint32_t so = (uint32_t)(s * kStageBytes) >> 4;
+          const int nk = P.nkb - sl * KB;   // K blocks left (the last slot may hold fewer than KB)
 #pragma unroll
-          for (int j = 0; j < kGemmKB; ++j) {
-            const int kb = sl * kGemmKB + j;
-            if (kb >= P.nkb) break;
+          for (int j = 0; j < KB; ++j) {
+            if (j >= nk) break;
 #pragma unroll
-            for (int kk = 0; kk < kGemmK / 16; ++kk) {
-              const uint64_t ad = smem_desc_sw128(a + j * a_blk + kk * a_step, a_lbo, 1024);
-              const uint64_t bd = smem_desc_sw128(bb + j * b_blk + kk * b_step, b_lbo, 1024);
-              tc_mma_bf16<CL>(d, ad, bd, idesc, (kb != w.sl0 * kGemmKB) || kk != 0);
-            }
+            for (int kk = 0; kk < kGemmK / 16; ++kk)
+              tc_mma_bf16<2>(d, ad0 + so + aoff[j * 4 + kk], bd0 + so + boff[j * 4 + kk], idesc,
+                             sl != w.sl0 || j != 0 || kk != 0);
           }
-          tc_commit<CL>(empty0 + 8 * s);   // both CTAs may refill the slot
+          tc_commit_mask(empty0 + 8 * s, slot_mask);   // every producer writing the slot may refill it
+          if (++s == NS) {
+            s = 0;
+            ph ^= 1;
+          }
         }
         if (!ok) break;
-        tc_commit<CL>(tfull0 + 8 * b);
+        tc_commit_mask(tfull0 + 8 * b, pair_mask);
       }
       if (!ok) {
         abort_flag = 1;
         set_error(P.err, DEVERR_TIMEOUT);
       }
       // every MMA issued has completed before either CTA may free TMEM
-      tc_commit<CL>(done_bar);
+      tc_commit_mask(done_bar, pair_mask);
       mbar_wait(done_bar, 0, drain);
     }
   } else if (warp == 2) {
@@ -375,9 +477,9 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       Epi::prefetch(P);
       int g = 0;
       bool ok = true;
-      for (int x = cl; x < nitems && ok; x += ncl) {
+      for (int x = S.x0; x < S.end && ok; x += S.step) {
         int m0, n0;
-        tile_of(gemm_item(P, x, nslots).unit, m0, n0);
+        tile_of(gemm_item(P, S, cl, x, nslots).unit, m0, n0);
         for (int j = 0; j < kGemmChunks; ++j, ++g) {
           const int e = g % NE;
           if (g >= NE && !gemm_wait(eempty0 + 8 * e, ((g / NE) & 1) ^ 1, limit, &abort_flag)) {
@@ -403,8 +505,8 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
 
     int g = 0, i = 0;
     bool dead = false;
-    for (int x = cl; x < nitems; x += ncl, ++i) {
-      const GemmItem w = gemm_item(P, x, nslots);
+    for (int x = S.x0; x < S.end; x += S.step, ++i) {
+      const GemmItem w = gemm_item(P, S, cl, x, nslots);
       int m0, n0;
       tile_of(w.unit, m0, n0);
       const int b = i & 1;
@@ -412,32 +514,75 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       tc_fence_after();
       got = __all_sync(0xffffffffu, got);
       const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + b * kGemmN;
-      // a piece: its partial accumulator goes to the workspace; the warp that
-      // completes a row block's second piece adds the other and finishes it
+      // a piece of a unit cut in two: the piece that runs first puts its
+      // partial accumulator (this warp's 32 rows) in the workspace and raises
+      // the rows' ready flag; the other waits for the flag, adds the partial
+      // and runs the epilogue
       bool finish = true;
       if (w.piece >= 0 && got) {
-        // layout [64 column quads][128 rows][4]: a warp's 16-byte accesses
-        // cover 512 contiguous bytes
-        float4* wq = reinterpret_cast<float4*>(P.ws) + (size_t)(w.q * CL + rank) * (kGemmM * kGemmN / 4) + rr;
+        int32_t* flag = P.ws_cnt + (w.key * CL + rank) * 4 + q;
+        if (!w.fin) {
+          // layout [64 column quads][128 rows][4]: a warp's 16-byte accesses
+          // cover 512 contiguous bytes
+          float4* wq = reinterpret_cast<float4*>(P.ws) + (size_t)(w.q * CL + rank) * (kGemmM * kGemmN / 4) + rr;
 #pragma unroll 1
-        for (int j = 0; j < kGemmChunks; ++j) {
-          float acc[32];
-          tmem_ld32(tacc + j * kGemmChunk, acc);
+          for (int j = 0; j < kGemmChunks; ++j) {
+            float acc[32];
+            tmem_ld32(tacc + j * kGemmChunk, acc);
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            wq[(size_t)(j * 8 + c) * kGemmM] = make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
-        }
-        __threadfence();
-        __syncwarp();
-        int32_t* cnt = P.ws_cnt + ((w.unit - P.nfull) * CL + rank) * 4 + q;
-        int last = 0;
-        if (lane == 0) last = atomicAdd(cnt, 1) == P.split - 1;
-        finish = __shfl_sync(0xffffffffu, last, 0) != 0;
-        if (finish) {
+            for (int c = 0; c < 8; ++c)
+              wq[(size_t)(j * 8 + c) * kGemmM] = make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+          }
           __threadfence();
-          if (lane == 0) *cnt = 0;   // every piece has arrived: ready for the next launch
+          __syncwarp();
+          if (lane == 0) st_release_gpu(flag, 1);
+          finish = false;
+        } else {
+          // the other piece runs on another cluster and never waits for this
+          // one: a bounded wait
+          int ready = 0;
+          if (lane == 0) {
+            const uint64_t t0 = global_ns();
+            while (!(ready = ld_acquire_gpu(flag) == 1))
+              if (abort_flag || (int64_t)(global_ns() - t0) > limit) break;
+            if (ready) *flag = 0;   // consumed: clear for the next launch
+          }
+          got = __shfl_sync(0xffffffffu, ready, 0) != 0;
+          __syncwarp();   // orders the other lanes' partial loads after lane 0's acquire
         }
       }
+      // The CTA's last item: every MMA has completed, so the operand ring is
+      // idle; each warp takes 32 KB of it (at least 128 KB in all) for the
+      // other piece's partial and the result chunks, so that no chunk waits
+      // for a store buffer.
+      const bool last = x + S.step >= S.end;
+      uint8_t* wring = opnd + q * 32768;
+      if (last && inplace && lane == 0 && prev_e >= 0) {
+        bulk_wait_read<0>();
+        mbar_arrive(eempty0 + 8 * prev_e);
+        prev_e = -1;
+      }
+      const float4* oq = nullptr;   // the other piece's partial (finishing a piece)
+      bool part_smem = false;
+      float4 nxt[8];
+      if (w.piece >= 0 && finish && got) {
+        oq = reinterpret_cast<const float4*>(P.ws) + (size_t)((w.q ^ 1) * CL + rank) * (kGemmM * kGemmN / 4) + rr;
+        if (last) {
+          // this warp's rows of the partial, [64 column quads][32 rows][16 B]:
+          // two column quads per lane, one bulk copy each
+          const uint32_t lbar = last0 + 8 * q;
+          if (lane == 0) mbar_expect_tx(lbar, 32 * 1024);
+          __syncwarp();
+          for (int c = lane; c < 64; c += 32)
+            bulk_load(smem_u32(wring) + c * 512, oq - lane + (size_t)c * kGemmM, 512, lbar);
+          got = __all_sync(0xffffffffu, gemm_wait(lbar, 0, limit, &abort_flag));
+          part_smem = true;
+        } else {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) nxt[c] = __ldcg(oq + (size_t)c * kGemmM);
+        }
+      }
+      const bool inpl = inplace && !last;   // results in place in the leaf chunk
       for (int j = 0; j < kGemmChunks; ++j, ++g) {
         const int e = g % NE;
         if (got && staged) got = gemm_wait(efull0 + 8 * e, (g / NE) & 1, limit, &abort_flag);
@@ -450,7 +595,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         if (!finish) {
           // another piece finishes this row block: only release the leaves
           if (lane == 0 && staged) {
-            if (inplace) {
+            if (inpl) {
               bulk_wait_read<0>();
               if (prev_e >= 0) mbar_arrive(eempty0 + 8 * prev_e);
               prev_e = -1;
@@ -462,18 +607,25 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         }
         float acc[32], o[32];
         tmem_ld32(tacc + j * kGemmChunk, acc);
-        if (w.piece >= 0) {
+        if (oq) {
           // the other piece's partial: two pieces, one addition, the same
-          // result whichever finished last
-          const float4* oq = reinterpret_cast<const float4*>(P.ws) +
-                             (size_t)((w.q ^ 1) * CL + rank) * (kGemmM * kGemmN / 4) + rr;
+          // result whichever finished last; from the ring, or with the next
+          // chunk's loads issued before this chunk is used (each is an L2
+          // round trip)
+          float4 cur[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            cur[c] = part_smem ? *reinterpret_cast<const float4*>(wring + (j * 8 + c) * 512 + lane * 16) : nxt[c];
+          if (!part_smem && j + 1 < kGemmChunks) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) nxt[c] = __ldcg(oq + (size_t)((j + 1) * 8 + c) * kGemmM);
+          }
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            const float4 t = __ldcg(oq + (size_t)(j * 8 + c) * kGemmM);
-            acc[4 * c] = __fadd_rn(acc[4 * c], t.x);
-            acc[4 * c + 1] = __fadd_rn(acc[4 * c + 1], t.y);
-            acc[4 * c + 2] = __fadd_rn(acc[4 * c + 2], t.z);
-            acc[4 * c + 3] = __fadd_rn(acc[4 * c + 3], t.w);
+            acc[4 * c] = __fadd_rn(acc[4 * c], cur[c].x);
+            acc[4 * c + 1] = __fadd_rn(acc[4 * c + 1], cur[c].y);
+            acc[4 * c + 2] = __fadd_rn(acc[4 * c + 2], cur[c].z);
+            acc[4 * c + 3] = __fadd_rn(acc[4 * c + 3], cur[c].w);
           }
         }
         const uint8_t* st = ebuf + e * P.epi_stage_bytes;
@@ -490,10 +642,13 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         // this warp's 32 rows x 32 columns go out through its own TMA store:
         // no barrier across the epilogue warps
         // the result goes to this warp's rows of the IDENT leaf's chunk (read
-        // above, no longer needed) or to a separate double buffer
-        uint8_t* ob = inplace ? ebuf + e * P.epi_stage_bytes + P.inplace_off + q * (32 * 128)
-                              : obuf + (j & 1) * kGemmOutBytes + q * (32 * 128);
-        if (!inplace && lane == 0) bulk_wait_read<1>();   // this buffer's previous store has read it
+        // above, no longer needed), to a separate double buffer, or in the
+        // last item to the chunk's 4 KB of the ring (whose partial has been
+        // read: all lanes read before any writes, below)
+        uint8_t* ob = last   ? wring + j * 4096
+                      : inpl ? ebuf + e * P.epi_stage_bytes + P.inplace_off + q * (32 * 128)
+                             : obuf + (j & 1) * kGemmOutBytes + q * (32 * 128);
+        if (!inpl && !last && lane == 0) bulk_wait_read<1>();   // this buffer's previous store has read it
         __syncwarp();
 #pragma unroll
         for (int c = 0; c < 8; ++c)
@@ -502,12 +657,12 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          if (staged && !inplace) mbar_arrive(eempty0 + 8 * e);
+          if (staged && !inpl) mbar_arrive(eempty0 + 8 * e);
           if (n0 + j * kGemmChunk < P.N && m0 + q * 32 < P.M) {
             tma_store_2d_hint(&P.maps[kMaxStaged], n0 + j * kGemmChunk, m0 + q * 32, smem_u32(ob), l2_evict_first());
           }
           bulk_commit();
-          if (inplace) {
+          if (inpl) {
             // the previous chunk's buffer is free once its store has read it
             bulk_wait_read<1>();
             if (prev_e >= 0) mbar_arrive(eempty0 + 8 * prev_e);
@@ -520,7 +675,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_cluster(cluster_addr(tempty0 + 8 * b, 0));
+        mbar_arrive_cluster(cluster_addr(tempty0 + 8 * b, even));
       }
     }
     if (dead) {
@@ -531,11 +686,18 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   }
   tc_fence_before();
   __syncthreads();
+  if (abort_flag && leader && threadIdx.x == 0) {
+    // loads in flight complete on the even CTA's barriers: that CTA drains
+    // the slots either producer may still be filling (the odd CTA stays
+    // resident until then, at the cluster barrier below)
+    const int last = issued[0] > issued[1] ? issued[0] : issued[1];
+    for (int k = last - NS < 0 ? 0 : last - NS; k < last; ++k) mbar_wait(full0 + 8 * (k % NS), (k / NS) & 1, drain);
+  }
   // no CTA leaves while its peer may still write to its shared memory or
   // issue MMAs into its TMEM
   cluster_sync();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc<CL>(tmem, 512);
+  if (warp == 1) tmem_dealloc<2>(tmem, 512);
 }
 
 }  // namespace fg

@@ -91,11 +91,6 @@ constexpr int64_t kUnpackWaitNs = 100000000LL;          // 100 ms: a chunk load 
 // Stages of the load ring: bf16 chunks are 16 KB, f32 chunks 32 KB.
 __host__ __device__ constexpr int unpack_stages(int bf16) { return bf16 ? 4 : 3; }
 
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-               : "memory");
-}
 __device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
                "r"(src), "r"(bytes)

@@ -104,8 +104,13 @@ typedef struct tf_layout tf_layout;
  * flag and the kernel returns.  flags tune the kernels without changing
  * results: bits 8-15 = height in tiles of the bands the tile walk sweeps
  * column by column (0 = row-major walk), and for GEMM-epilogue groups the
- * most CTA pairs to launch (0 = one pair per two SMs); bits 16-23 = tiles per reduce work
- * unit (0 = chosen from the frame and the SM count); bits 24-25 = how an
+ * most clusters to launch (0 = as many as the device runs at once); bits
+ * 16-23 = tiles per reduce work unit (0 = chosen from the frame and the SM
+ * count), and for GEMM-epilogue groups bits 16-17 the cluster shape (0 =
+ * chosen, 1 = CTA pairs, 2 = 4-CTA clusters whose two pairs share their A
+ * rows), bits 18-19 the K blocks of 64 per operand ring slot (0 = chosen,
+ * 1, 2), bits 20-21 the schedule (0 = chosen, 1 = round robin with the last
+ * round split along K, 2 = equal shares of all tiles' K steps); bits 24-25 = how an
  * elementwise group writes its output: 0 default (= 2), 1 the CTA's tile
  * staged in shared memory and stored by one TMA store, 2 each warp's slice
  * stored by its own TMA store, 3 direct 16-byte stores from registers;

@@ -53,3 +53,18 @@ def test_tuple_programs_compile():
         plan = graph_from_spec(g).build()
         assert plan.n_groups == 1
         _compile(plan.source(0))
+
+
+@pytest.mark.parametrize("shape,cl,kb", [(0, 2, 2), (1 << 16, 2, 2), (2 << 16, 4, 2), (1 << 18, 2, 1),
+                                         ((2 << 16) | (1 << 18), 4, 1)])
+def test_gemm_cluster_shapes_compile(shape, cl, kb):
+    """The GEMM-epilogue program in CTA pairs and in 4-CTA clusters whose two
+    pairs share their A rows (multicast), with one or two K blocks per ring
+    slot."""
+    spec = W.sf_update(256, 256, 512)
+    plan = graph_from_spec(spec).build(flags=shape)
+    assert plan.groups[0].kind == "gemm"
+    src = plan.source(0)
+    assert f"__cluster_dims__({cl}, 1, 1)" in src
+    assert f"gemm_body<fg::JitEpi, {cl}, {kb}>" in src
+    _compile(src)

@@ -13,6 +13,9 @@ from group_execution_gb300 import _lib
 
 pytestmark = pytest.mark.gpu
 MODES = [0, _lib.FG_FLAG_INTERPRET]
+PAIRS, CLUSTER4 = 1 << 16, 2 << 16     # GEMM cluster shape: CTA pairs only / two pairs sharing A
+KB1, KB2 = 1 << 18, 2 << 18            # K blocks per operand ring slot
+SHAPES = [CLUSTER4 | KB2, CLUSTER4 | KB1, PAIRS | KB1]
 
 
 def _matmul_graph(K, M, N, ta, tb, epi=None):
@@ -104,13 +107,14 @@ def test_sf_update_full():
 
 @pytest.mark.parametrize("K,M,N,cap", [(1024, 1024, 1024, 5), (1024, 1024, 1024, 7), (2048, 1024, 1024, 5),
                                        (1088, 768, 1280, 7)])
-def test_split_tail(K, M, N, cap):
+@pytest.mark.parametrize("kb", [KB2, KB1])
+def test_split_tail(K, M, N, cap, kb):
     """The last round's tiles split along K (CTA pairs capped so that a tail
     exists): the partial accumulators meet in the workspace and the last
     piece finishes the epilogue; run twice, so the arrival counters are seen
     to reset."""
     spec = W.sf_update(K, M, N)
-    g, plan, inputs, dev = prepare(spec, flags=cap << 8)
+    g, plan, inputs, dev = prepare(spec, flags=(cap << 8) | PAIRS | kb)
     ref = OE.run_unfused(spec, inputs)[spec.outputs[0]]
     w = inputs[2]
     for _ in range(2):
@@ -125,7 +129,7 @@ def test_split_tail(K, M, N, cap):
 def test_split_tail_plain_layouts(ta, tb):
     K, M, N = 1024, 1024, 768
     spec = _matmul_graph(K, M, N, ta, tb)
-    g, plan, inputs, dev = prepare(spec, flags=5 << 8)
+    g, plan, inputs, dev = prepare(spec, flags=(5 << 8) | PAIRS)
     env = run_fused(plan, spec, dev)
     plan.sync()
     A = inputs[0].T if ta else inputs[0]
@@ -136,3 +140,74 @@ def test_split_tail_plain_layouts(ta, tb):
 def test_split_tail_full_size():
     # 256 pair tiles on 76 pairs: the last 28 run as K halves
     _sf_update(1024, 4096, 4096, 0)
+
+
+# ---- 4-CTA clusters: two pairs on side-by-side tiles share their A rows ----
+
+@pytest.mark.parametrize("ta,tb", [(1, 0), (0, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("kmn", [(1024, 512, 1024), (1096, 392, 1288), (200, 264, 600), (64, 128, 512)])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_cluster_shapes_layouts(ta, tb, kmn, shape):
+    """4-CTA clusters (two pairs sharing A rows) and one-K-block ring slots,
+    every operand layout; ragged M, N and K (with clusters the second pair's
+    tile lies past N when the tile columns are odd: N = 600), K shorter than
+    one ring slot."""
+    K, M, N = kmn
+    spec = _matmul_graph(K, M, N, ta, tb)
+    g, plan, inputs, dev = prepare(spec, flags=shape)
+    env = run_fused(plan, spec, dev)
+    plan.sync()
+    A = inputs[0].T if ta else inputs[0]
+    B = inputs[1].T if tb else inputs[1]
+    _check_matmul_bound(env[spec.outputs[0]].cpu().numpy(), A, B)
+
+
+@pytest.mark.parametrize("K,M,N,cap", [(2048, 1024, 2048, 5), (2048, 1024, 2048, 3), (2048, 1024, 2048, 7),
+                                       (1152, 776, 1800, 6), (4096, 512, 1024, 3)])
+@pytest.mark.parametrize("kb", [KB2, KB1])
+def test_cluster4_stream_k(K, M, N, cap, kb):
+    """Clusters capped so that the units do not divide evenly: each cluster
+    runs an equal share of all units' ring slots, a unit cut by a share
+    boundary meets its two partial accumulators in the workspace; run twice,
+    so the arrival counters are seen to reset."""
+    spec = W.sf_update(K, M, N)
+    g, plan, inputs, dev = prepare(spec, flags=(cap << 8) | CLUSTER4 | kb)
+    ref = OE.run_unfused(spec, inputs)[spec.outputs[0]]
+    w = inputs[2]
+    for _ in range(2):
+        env = run_fused(plan, spec, dev)
+        plan.sync()
+        got = env[spec.outputs[0]].cpu().numpy()
+        assert rel_err(got, ref) <= TOL_F32
+        assert rel_err(w - got, w - ref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("ta,tb", [(0, 1), (1, 1)])
+@pytest.mark.parametrize("kb", [KB2, KB1])
+def test_cluster4_stream_k_plain(ta, tb, kb):
+    K, M, N = 2048, 1024, 1536
+    spec = _matmul_graph(K, M, N, ta, tb)
+    g, plan, inputs, dev = prepare(spec, flags=(5 << 8) | CLUSTER4 | kb)
+    env = run_fused(plan, spec, dev)
+    plan.sync()
+    A = inputs[0].T if ta else inputs[0]
+    B = inputs[1].T if tb else inputs[1]
+    _check_matmul_bound(env[spec.outputs[0]].cpu().numpy(), A, B)
+
+
+@pytest.mark.parametrize("epi", ["bias_relu", "trans_leaf"])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_cluster_shapes_epilogues(epi, shape):
+    spec = _matmul_graph(1024, 256, 1024, 1, 0, epi)
+    g, plan, inputs, dev = prepare(spec, flags=shape)
+    assert plan.n_groups == 1 and plan.groups[0].kind == "gemm"
+    env = run_fused(plan, spec, dev)
+    plan.sync()
+    ref = OE.run_unfused(spec, inputs)[spec.outputs[0]]
+    assert rel_err(env[spec.outputs[0]].cpu().numpy(), ref) <= 1e-4
+
+
+def test_sf_update_k4096_full_size():
+    """The compute-bound SF update (B = K = 4096) in the default launch:
+    4-CTA clusters, stream-K shares."""
+    _sf_update(4096, 4096, 4096, 0)
