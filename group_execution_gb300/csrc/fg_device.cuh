@@ -436,9 +436,13 @@ __device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) 
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
   return r;
 }
-// Arrival on an mbarrier that may live in another CTA of the cluster.
+// Arrival on an mbarrier that may live in another CTA of the cluster, as a
+// signal (release at CTA scope: the signalled hazards, such as TMEM reads
+// finished before tcgen05.fence::before_thread_sync, need no wider memory
+// ordering, and a cluster-scope release also waits for this thread's bulk
+// stores still in flight, about a microsecond).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
