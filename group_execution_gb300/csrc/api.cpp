@@ -614,7 +614,7 @@ fg_status alloc_device(fg_plan* p, GroupExec& ge) {
       const size_t keys = mp.sk ? (size_t)(ge.grid / CL - 1) : (size_t)(mp.nunits - mp.nfull);
       cudaError_t e = cudaMalloc(&ge.scratch, sizeof(float) * keys * 2 * CL * kGemmM * kGemmN);
       if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(split-tail workspace)");
-      ge.counter_bytes = sizeof(int32_t) * keys * CL * 4;
+      ge.counter_bytes = sizeof(int32_t) * keys * CL * 8;
       e = cudaMalloc(&ge.counters, ge.counter_bytes);
       if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(split-tail counters)");
       e = cudaMemset(ge.counters, 0, ge.counter_bytes);

@@ -163,7 +163,7 @@ struct GroupParams {
 // of 64, the epilogue in 128 x 32 column chunks.
 constexpr int kGemmM = 128, kGemmN = 256, kGemmK = 64, kGemmChunk = 32;
 constexpr int kGemmKB = 2;             // K blocks per operand ring slot (interpreted kernel; compiled: 1 or 2)
-constexpr int kGemmWarps = 8;          // A loads, MMA, epilogue loads, 4 epilogue warps, B loads
+constexpr int kGemmWarps = 12;         // A loads, MMA, epilogue loads, 4 epilogue warps, B loads, 4 epilogue warps
 constexpr int kGemmCluster = 2;        // CTAs of a pair issuing 2-SM MMAs on one 256-row tile
 constexpr int kGemmCluster4 = 4;       // two pairs on adjacent 256-column tiles sharing their A rows
 
@@ -199,7 +199,7 @@ struct GemmParams {
   // into the two pieces on either side of a share boundary)
   int32_t sk;
   float* ws;                           // [pieces][cluster CTAs][64 column quads][128 rows][4] partial accumulators
-  int32_t* ws_cnt;                     // [split units][cluster CTAs][4 warps] partial-ready flags (cleared by the reader)
+  int32_t* ws_cnt;                     // [split units][cluster CTAs][8 epilogue warps] partial-ready flags (cleared by the reader)
 };
 
 // Loads already issued always land; waiting for them before a CTA exits uses

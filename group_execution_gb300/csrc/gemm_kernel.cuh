@@ -25,7 +25,10 @@
 //           jointly with the peer) and, in the even CTA, issues the MMAs from
 //           one thread,
 //   warp 2  TMA producer of the epilogue leaves, 128 x 32 chunk by chunk,
-//   warps 3-6 epilogue: each thread owns one accumulator row (TMEM lane),
+//   warps 3-6 and 8-11 epilogue, the two sets taking alternate 32-column
+//           chunks (a chunk's TMEM read, leaf reads, epilogue and store are
+//           one warp's serial chain): each thread owns one accumulator row
+//           (TMEM lane),
 //           reads 32 columns per chunk with tcgen05.ld, evaluates the
 //           epilogue program eight values at a time and stages the result
 //           for a TMA store.
@@ -271,7 +274,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   __shared__ uint32_t tmem_slot;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // barriers: full[16] empty[16] tfull[2] tempty[2] efull[8] eempty[8] done
-  // last[4] (one per epilogue warp)
+  // last[8] (one per epilogue warp)
   const uint32_t bars = smem_u32(smem);
   const uint32_t full0 = bars, empty0 = bars + 128, tfull0 = bars + 256, tempty0 = bars + 272;
   const uint32_t efull0 = bars + 288, eempty0 = bars + 352, done_bar = bars + 416, last0 = bars + 424;
@@ -308,14 +311,14 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull0 + 8 * b, 1);
-      mbar_init(tempty0 + 8 * b, 4 * 2);   // every epilogue warp of the pair
+      mbar_init(tempty0 + 8 * b, 8 * 2);   // every epilogue warp of the pair
     }
     for (int e = 0; e < NE; ++e) {
       mbar_init(efull0 + 8 * e, 1);
       mbar_init(eempty0 + 8 * e, 4);
     }
     mbar_init(done_bar, 1);
-    for (int k = 0; k < 4; ++k) mbar_init(last0 + 8 * k, 1);
+    for (int k = 0; k < 8; ++k) mbar_init(last0 + 8 * k, 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc<2>(smem_u32(&tmem_slot), 512);
@@ -499,6 +502,8 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   } else {
     // ---- epilogue ----
     const int q = warp & 3;              // TMEM lane quarter this warp may access
+    const int set = warp >= 8 ? 1 : 0;   // chunks j with j % 2 == set
+    const int ew = set * 4 + q;          // epilogue warp index
     const int rr = q * 32 + lane;        // accumulator row of this thread
     const bool inplace = P.inplace_off >= 0;
     int prev_e = -1;                     // buffer whose release waits for its store (lane 0)
@@ -520,13 +525,13 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       // and runs the epilogue
       bool finish = true;
       if (w.piece >= 0 && got) {
-        int32_t* flag = P.ws_cnt + (w.key * CL + rank) * 4 + q;
+        int32_t* flag = P.ws_cnt + (w.key * CL + rank) * 8 + ew;
         if (!w.fin) {
           // layout [64 column quads][128 rows][4]: a warp's 16-byte accesses
           // cover 512 contiguous bytes
           float4* wq = reinterpret_cast<float4*>(P.ws) + (size_t)(w.q * CL + rank) * (kGemmM * kGemmN / 4) + rr;
 #pragma unroll 1
-          for (int j = 0; j < kGemmChunks; ++j) {
+          for (int j = set; j < kGemmChunks; j += 2) {
             float acc[32];
             tmem_ld32(tacc + j * kGemmChunk, acc);
 #pragma unroll
@@ -552,9 +557,9 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         }
       }
       // The CTA's last item: every MMA has completed, so the operand ring is
-      // idle; each warp takes 32 KB of it (at least 128 KB in all) for the
-      // other piece's partial and the result chunks, so that no chunk waits
-      // for a store buffer.
+      // idle; each TMEM lane quarter takes 32 KB of it (at least 128 KB in
+      // all) for the other piece's partial and the result chunks, so that no
+      // chunk waits for a store buffer.
       const bool last = x + S.step >= S.end;
       uint8_t* wring = opnd + q * 32768;
       if (last && inplace && lane == 0 && prev_e >= 0) {
@@ -568,22 +573,23 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       if (w.piece >= 0 && finish && got) {
         oq = reinterpret_cast<const float4*>(P.ws) + (size_t)((w.q ^ 1) * CL + rank) * (kGemmM * kGemmN / 4) + rr;
         if (last) {
-          // this warp's rows of the partial, [64 column quads][32 rows][16 B]:
-          // two column quads per lane, one bulk copy each
-          const uint32_t lbar = last0 + 8 * q;
-          if (lane == 0) mbar_expect_tx(lbar, 32 * 1024);
+          // this warp's rows of the partial in its chunks, [column quad][32
+          // rows][16 B]: one 512-byte bulk copy per lane
+          const uint32_t lbar = last0 + 8 * ew;
+          if (lane == 0) mbar_expect_tx(lbar, 16 * 1024);
           __syncwarp();
-          for (int c = lane; c < 64; c += 32)
-            bulk_load(smem_u32(wring) + c * 512, oq - lane + (size_t)c * kGemmM, 512, lbar);
+          const int c = ((lane >> 3) * 2 + set) * 8 + (lane & 7);
+          bulk_load(smem_u32(wring) + c * 512, oq - lane + (size_t)c * kGemmM, 512, lbar);
           got = __all_sync(0xffffffffu, gemm_wait(lbar, 0, limit, &abort_flag));
           part_smem = true;
         } else {
 #pragma unroll
-          for (int c = 0; c < 8; ++c) nxt[c] = __ldcg(oq + (size_t)c * kGemmM);
+          for (int c = 0; c < 8; ++c) nxt[c] = __ldcg(oq + (size_t)(set * 8 + c) * kGemmM);
         }
       }
       const bool inpl = inplace && !last;   // results in place in the leaf chunk
       for (int j = 0; j < kGemmChunks; ++j, ++g) {
+        if ((j & 1) != set) continue;   // the other set's chunk
         const int e = g % NE;
         if (got && staged) got = gemm_wait(efull0 + 8 * e, (g / NE) & 1, limit, &abort_flag);
         // tcgen05.ld is warp-collective: decide per warp
@@ -616,9 +622,9 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             cur[c] = part_smem ? *reinterpret_cast<const float4*>(wring + (j * 8 + c) * 512 + lane * 16) : nxt[c];
-          if (!part_smem && j + 1 < kGemmChunks) {
+          if (!part_smem && j + 2 < kGemmChunks) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) nxt[c] = __ldcg(oq + (size_t)((j + 1) * 8 + c) * kGemmM);
+            for (int c = 0; c < 8; ++c) nxt[c] = __ldcg(oq + (size_t)((j + 2) * 8 + c) * kGemmM);
           }
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
@@ -648,7 +654,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         uint8_t* ob = last   ? wring + j * 4096
                       : inpl ? ebuf + e * P.epi_stage_bytes + P.inplace_off + q * (32 * 128)
                              : obuf + (j & 1) * kGemmOutBytes + q * (32 * 128);
-        if (!inpl && !last && lane == 0) bulk_wait_read<1>();   // this buffer's previous store has read it
+        if (!inpl && !last && lane == 0) bulk_wait_read<0>();   // this warp's buffer: its previous store has read it
         __syncwarp();
 #pragma unroll
         for (int c = 0; c < 8; ++c)
@@ -662,11 +668,17 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
             tma_store_2d_hint(&P.maps[kMaxStaged], n0 + j * kGemmChunk, m0 + q * 32, smem_u32(ob), l2_evict_first());
           }
           bulk_commit();
-          if (inpl) {
-            // the previous chunk's buffer is free once its store has read it
+          if (inpl && NE > 2) {
+            // this warp's previous chunk's buffer is free once its store has
+            // read it
             bulk_wait_read<1>();
             if (prev_e >= 0) mbar_arrive(eempty0 + 8 * prev_e);
             prev_e = e;
+          } else if (inpl) {
+            // with two leaf buffers each set's chunks reuse one buffer: free
+            // it now (a deferred release would wait for itself)
+            bulk_wait_read<0>();
+            mbar_arrive(eempty0 + 8 * e);
           }
         }
       }
