@@ -506,19 +506,29 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
   // tile columns; bits 18-19: 1 or 2 K blocks per slot (0 = chosen).
   ge.compiled = !(o.flags & FG_FLAG_INTERPRET);
   const int shape = (o.flags >> 16) & 3, kbf = (o.flags >> 18) & 3, sched = (o.flags >> 20) & 3;
+  const int tnf = (o.flags >> 22) & 3;
   const bool c4 = ge.compiled && p.ntn >= 2 && shape == 2;
   const int KB = ge.compiled && kbf == 1 ? 1 : 2;
   const int CL = c4 ? kGemmCluster4 : kGemmCluster, PR = CL / 2;
   if (c4) p.a_3d = 0;   // each CTA fetches half of an A half: 2-D boxes
+  // Pair tile width (flag bits 22-23: 0 or 1 = 256, 2 = 128 columns; the
+  // interpreter and 4-CTA clusters keep 256).  128-column tiles fill the
+  // rounds of a short-K launch better, but measured slower: each tile's
+  // fixed costs and the doubled A traffic outweigh it.
+  int TN = kGemmN;
+  if (ge.compiled && !c4 && tnf == 2) TN = 128;
+  p.ntn = (int32_t)((cg.N + TN - 1) / TN);
+  p.ntiles = p.ntm * p.ntn;
   cg.gemm_cl = CL;
   cg.gemm_kb = KB;
+  cg.gemm_tn = TN;
   // operand ring and epilogue-leaf ring depths that fit 227 KB, in order of
   // preference: long K needs a deep operand ring (its feed is latency bound),
   // short K a deep leaf ring (the epilogue streams the leaves from HBM).  A
   // ring slot holds KB K blocks of the CTA's 128 rows of A and of its half of
   // B's columns.
   const int limit = 227 * 1024 - 256, fixed = 2048 + (p.inplace_off >= 0 ? 0 : 2 * kGemmM * kGemmChunk * 4);
-  const int stage = KB * (kGemmM + kGemmN / 2) * kGemmK * 2;
+  const int stage = KB * (kGemmM + TN / 2) * kGemmK * 2;
   int ns = 0, ne = 0;
   static const std::vector<std::pair<int, int>> prefs_short = {{2, 6}, {2, 5}, {2, 4}, {2, 3}, {2, 2}};
   static const std::vector<std::pair<int, int>> prefs_long = {{3, 2}, {2, 4}, {2, 3}, {2, 2}};
@@ -612,7 +622,7 @@ fg_status alloc_device(fg_plan* p, GroupExec& ge) {
       // boundary (stream-K); two pieces each
       const int CL = ge.cg.gemm_cl;
       const size_t keys = mp.sk ? (size_t)(ge.grid / CL - 1) : (size_t)(mp.nunits - mp.nfull);
-      cudaError_t e = cudaMalloc(&ge.scratch, sizeof(float) * keys * 2 * CL * kGemmM * kGemmN);
+      cudaError_t e = cudaMalloc(&ge.scratch, sizeof(float) * keys * 2 * CL * kGemmM * ge.cg.gemm_tn);
       if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(split-tail workspace)");
       ge.counter_bytes = sizeof(int32_t) * keys * CL * 8;
       e = cudaMalloc(&ge.counters, ge.counter_bytes);
@@ -715,29 +725,30 @@ fg_status launch_gemm(GroupExec& ge, void* const* ptrs, void* stream) {
       //   K-major  [K/64][rows][64],   box 64 x 128 rows x 2 K blocks.
       // Otherwise 2-D boxes: MN-major 64 x 64, K-major 64 x 128 rows.
       // With KB K blocks per ring slot the 3-D boxes cover KB * 64 K rows
-      // (MN-major) or KB K blocks (K-major).  In 4-CTA clusters with one K
-      // block per slot each CTA fetches 64 of its 128 A rows (K-major box
-      // 64 x 64).
+      // (MN-major) or KB K blocks (K-major), over a half's R rows (A: 128;
+      // B: half the tile's columns).  In 4-CTA clusters with one K block per
+      // slot each CTA fetches 64 of its 128 A rows (K-major box 64 x 64).
       uint64_t dims[3], strides[2];
       uint32_t box[3];
       const int KB = cg.gemm_kb;
-      auto view = [&](bool mn, bool v3, int64_t rows, bool half_rows) {
+      auto view = [&](bool mn, bool v3, int64_t rows, int R, bool half_rows) {
         const int64_t inner = mn ? rows : cg.K, outer = mn ? cg.K : rows;
         if (v3) {
           dims[0] = 64; dims[1] = outer; dims[2] = inner / 64; strides[0] = inner * 2; strides[1] = 128;
-          box[0] = 64; box[1] = mn ? 64 * KB : 128; box[2] = mn ? 2 : KB;
+          box[0] = 64; box[1] = mn ? 64 * KB : R; box[2] = mn ? R / 64 : KB;
           return 3;
         }
-        dims[0] = inner; dims[1] = outer; strides[0] = inner * 2; box[0] = 64; box[1] = mn || half_rows ? 64 : 128;
+        dims[0] = inner; dims[1] = outer; strides[0] = inner * 2; box[0] = 64;
+        box[1] = mn || half_rows ? 64 : R;
         return 2;
       };
-      int rank = view(gp.a_mn, gp.a_3d, cg.M, cg.gemm_cl == kGemmCluster4 && KB == 1);
+      int rank = view(gp.a_mn, gp.a_3d, cg.M, kGemmM, cg.gemm_cl == kGemmCluster4 && KB == 1);
       if (fg_status st = encode(&gp.mapA, ptrs[cg.mm_a], rank, dims, strides, box, true,
                                 CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
         return st;
       // B: [K, N] (N contiguous), or [N, K] when transposed; each CTA of a
       // pair stages its half of the tile's columns
-      rank = view(gp.b_mn, gp.b_3d, cg.N, false);
+      rank = view(gp.b_mn, gp.b_3d, cg.N, cg.gemm_tn / 2, false);
       if (fg_status st = encode(&gp.mapB, ptrs[cg.mm_b], rank, dims, strides, box, true,
                                 CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
         return st;

@@ -43,7 +43,6 @@ namespace fg {
 constexpr int kGemmThreads = kGemmWarps * 32;
 constexpr int kGemmABytes = kGemmM * kGemmK * 2;    // 16 KB: this CTA's 128 rows of one A block
 constexpr int kGemmOutBytes = kGemmM * kGemmChunk * 4;   // 16 KB
-constexpr int kGemmChunks = kGemmN / kGemmChunk;    // 8
 
 // Leaf reads for one epilogue thread: accumulator row rr of the tile, eight
 // columns starting at q8 inside the current 32-column chunk.
@@ -232,10 +231,11 @@ __device__ __forceinline__ GemmItem gemm_item(const GemmParams& P, const GemmSch
   return w;
 }
 
-// One operand half of a ring slot (this CTA's 128 rows of A or columns of
-// B, KB K blocks from k0) into this CTA's shared memory, counted on the pair
-// barrier cbar: one copy through a 3-D view, or 2-D boxes.
-template <int KB>
+// One operand half of a ring slot (this CTA's R rows of A or columns of B,
+// KB K blocks from k0) into this CTA's shared memory, counted on the pair
+// barrier cbar: one copy through a 3-D view, or 2-D boxes.  Layouts:
+// MN-major [R / 64 groups][KB * 64 K rows][64], K-major [KB][R rows][64 K].
+template <int KB, int R>
 __device__ __forceinline__ void gemm_load_half(uint32_t dst, const CUtensorMap* m, int mn, int v3, int r0, int k0,
                                                uint32_t cbar, uint64_t keep) {
   if (mn) {
@@ -243,7 +243,7 @@ __device__ __forceinline__ void gemm_load_half(uint32_t dst, const CUtensorMap* 
       tma_load_3d_pair(dst, m, 0, k0, r0 / 64, cbar, keep);
     } else {
 #pragma unroll
-      for (int g = 0; g < 2; ++g)
+      for (int g = 0; g < R / 64; ++g)
 #pragma unroll
         for (int j = 0; j < KB; ++j)
           tma_load_2d_pair(dst + g * (KB * 8192) + j * 8192, m, r0 + 64 * g, k0 + 64 * j, cbar, keep);
@@ -252,22 +252,26 @@ __device__ __forceinline__ void gemm_load_half(uint32_t dst, const CUtensorMap* 
     tma_load_3d_pair(dst, m, 0, r0, k0 / 64, cbar, keep);
   } else {
 #pragma unroll
-    for (int j = 0; j < KB; ++j) tma_load_2d_pair(dst + j * 16384, m, k0 + 64 * j, r0, cbar, keep);
+    for (int j = 0; j < KB; ++j) tma_load_2d_pair(dst + j * (R * 128), m, k0 + 64 * j, r0, cbar, keep);
   }
 }
 
 // CL = 2: a CTA pair per 256 x 256 tile (cta_group::2), each CTA holding
 // half of A's rows and half of B's columns.  CL = 4: two such pairs on the
 // two 256-column halves of a 256 x 512 unit, sharing their A halves.  KB: K
-// blocks of 64 per operand ring slot (1: 32 KB slots, 2: 64 KB).
-template <class Epi, int CL, int KB>
+// blocks of 64 per operand ring slot (1 or 2).  TN: columns of a pair's tile
+// (256, or 128: half the epilogue per tile, for short K where the epilogue's
+// streams dominate and finer tiles fill the last round).
+template <class Epi, int CL, int KB, int TN>
 __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   static_assert(CL == 2 || CL == 4, "the kernel runs CTA pairs, alone or two by two");
   static_assert(KB == 1 || KB == 2, "one or two K blocks per ring slot");
+  static_assert(TN == 256 || TN == 128, "pair tiles of 256 or 128 columns");
   constexpr int PR = CL / 2;                                       // pairs per cluster
-  constexpr int kBCols = kGemmN / 2;                               // B columns staged per CTA
+  constexpr int kBCols = TN / 2;                                   // B columns staged per CTA
+  constexpr int kGemmChunks = TN / kGemmChunk;                     // epilogue chunks per tile
   constexpr int kHalfA = KB * kGemmABytes;                         // 128 rows x KB K blocks
-  constexpr int kStageBytes = kHalfA + KB * kBCols * kGemmK * 2;   // 32 KB per K block and CTA
+  constexpr int kStageBytes = kHalfA + KB * kBCols * kGemmK * 2;   // 32 (24) KB per K block and CTA
   extern __shared__ uint8_t smem_raw[];
   __shared__ int abort_flag;
   __shared__ int issued[2];            // operand slots issued by the A and B producers
@@ -300,7 +304,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   const int nsn = (P.ntn + PR - 1) / PR;
   auto tile_of = [&](int u, int& m0, int& n0) {
     m0 = ((u / nsn) * 2 + h) * kGemmM;
-    n0 = ((u % nsn) * PR + pr) * kGemmN;
+    n0 = ((u % nsn) * PR + pr) * TN;
   };
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -365,7 +369,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
             ph ^= 1;
           }
           if (!isA) {
-            gemm_load_half<KB>(b, &P.mapB, P.b_mn, P.b_3d, nb, k0, cbar, keep);
+            gemm_load_half<KB, kBCols>(b, &P.mapB, P.b_mn, P.b_3d, nb, k0, cbar, keep);
             continue;
           }
           if (leader) mbar_expect_tx(fbar, 2 * kStageBytes);
@@ -388,7 +392,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
               tma_load_2d_pair_mc(a + pr * 8192, &P.mapA, k0, m0 + 64 * pr, cbar, mc, keep);
             }
           } else {
-            gemm_load_half<KB>(a, &P.mapA, P.a_mn, P.a_3d, m0, k0, cbar, keep);
+            gemm_load_half<KB, kGemmM>(a, &P.mapA, P.a_mn, P.a_3d, m0, k0, cbar, keep);
           }
         }
       }
@@ -401,11 +405,11 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   } else if (warp == 1) {
     // ---- MMA issuer (the even CTA of a pair) ----
     if (lane == 0 && leader) {
-      const uint32_t idesc = idesc_bf16_f32(2 * kGemmM, kGemmN, P.a_mn, P.b_mn);
+      const uint32_t idesc = idesc_bf16_f32(2 * kGemmM, TN, P.a_mn, P.b_mn);
       // MN-major: atoms of 64 (M or N) x 8 K rows, 64-wide groups 16 KB
       // apart; K-major: atoms of 8 rows x 64 K, K blocks 16 KB apart
       const uint32_t a_lbo = P.a_mn ? KB * 8192 : 16, b_lbo = P.b_mn ? KB * 8192 : 16;
-      const uint32_t a_blk = P.a_mn ? 8192 : 16384, b_blk = P.b_mn ? 8192 : 16384;   // next K block
+      const uint32_t a_blk = P.a_mn ? 8192 : 16384, b_blk = P.b_mn ? 8192 : kBCols * 128;   // next K block
       const uint32_t a_step = P.a_mn ? 2048 : 32, b_step = P.b_mn ? 2048 : 32;         // next 16 of K
       // a descriptor's start-address field holds address >> 4 in 14 bits and
       // the ring lies below 2^18 bytes, so descriptors advance by adding
@@ -440,7 +444,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
           }
         }
         tc_fence_after();
-        const uint32_t d = tmem + b * kGemmN;
+        const uint32_t d = tmem + b * TN;
         for (int sl = w.sl0; sl < w.sl1; ++sl) {
           if (!gemm_wait(full0 + 8 * s, ph, limit, &abort_flag)) {
             ok = false;
@@ -518,7 +522,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       bool got = gemm_wait(tfull0 + 8 * b, (i >> 1) & 1, limit, &abort_flag);
       tc_fence_after();
       got = __all_sync(0xffffffffu, got);
-      const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + b * kGemmN;
+      const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + b * TN;
       // a piece of a unit cut in two: the piece that runs first puts its
       // partial accumulator (this warp's 32 rows) in the workspace and raises
       // the rows' ready flag; the other waits for the flag, adds the partial
@@ -529,7 +533,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         if (!w.fin) {
           // layout [64 column quads][128 rows][4]: a warp's 16-byte accesses
           // cover 512 contiguous bytes
-          float4* wq = reinterpret_cast<float4*>(P.ws) + (size_t)(w.q * CL + rank) * (kGemmM * kGemmN / 4) + rr;
+          float4* wq = reinterpret_cast<float4*>(P.ws) + (size_t)(w.q * CL + rank) * (kGemmM * TN / 4) + rr;
 #pragma unroll 1
           for (int j = set; j < kGemmChunks; j += 2) {
             float acc[32];
@@ -557,11 +561,11 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         }
       }
       // The CTA's last item: every MMA has completed, so the operand ring is
-      // idle; each TMEM lane quarter takes 32 KB of it (at least 128 KB in
-      // all) for the other piece's partial and the result chunks, so that no
-      // chunk waits for a store buffer.
+      // idle; each TMEM lane quarter takes TN * 128 bytes of it (the ring is
+      // at least four times that) for the other piece's partial and the
+      // result chunks, so that no chunk waits for a store buffer.
       const bool last = x + S.step >= S.end;
-      uint8_t* wring = opnd + q * 32768;
+      uint8_t* wring = opnd + q * (TN * 128);
       if (last && inplace && lane == 0 && prev_e >= 0) {
         bulk_wait_read<0>();
         mbar_arrive(eempty0 + 8 * prev_e);
@@ -571,15 +575,17 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       bool part_smem = false;
       float4 nxt[8];
       if (w.piece >= 0 && finish && got) {
-        oq = reinterpret_cast<const float4*>(P.ws) + (size_t)((w.q ^ 1) * CL + rank) * (kGemmM * kGemmN / 4) + rr;
+        oq = reinterpret_cast<const float4*>(P.ws) + (size_t)((w.q ^ 1) * CL + rank) * (kGemmM * TN / 4) + rr;
         if (last) {
           // this warp's rows of the partial in its chunks, [column quad][32
-          // rows][16 B]: one 512-byte bulk copy per lane
+          // rows][16 B]: one 512-byte bulk copy per lane and column quad
           const uint32_t lbar = last0 + 8 * ew;
-          if (lane == 0) mbar_expect_tx(lbar, 16 * 1024);
+          if (lane == 0) mbar_expect_tx(lbar, TN / 8 * 512);
           __syncwarp();
-          const int c = ((lane >> 3) * 2 + set) * 8 + (lane & 7);
-          bulk_load(smem_u32(wring) + c * 512, oq - lane + (size_t)c * kGemmM, 512, lbar);
+          if (lane < TN / 8) {
+            const int c = ((lane >> 3) * 2 + set) * 8 + (lane & 7);
+            bulk_load(smem_u32(wring) + c * 512, oq - lane + (size_t)c * kGemmM, 512, lbar);
+          }
           got = __all_sync(0xffffffffu, gemm_wait(lbar, 0, limit, &abort_flag));
           part_smem = true;
         } else {

@@ -105,6 +105,7 @@ struct CompiledGroup {
   int64_t M = 0, N = 0, K = 0;
   int gemm_cl = 2;                    // CTAs per cluster: a pair, or two pairs sharing A rows
   int gemm_kb = 2;                    // K blocks of 64 per operand ring slot
+  int gemm_tn = 256;                  // columns of a pair's tile
   // staging decisions (filled by plan_staging)
   int nstaged = 0, ngathered = 0, stage_bytes = 0, nstages = 0, nsplit = 1;
   int tiles_per_split = 0;

@@ -10,7 +10,7 @@ namespace fg {
 template <int D, int S>
 __global__ void __cluster_dims__(kGemmCluster, 1, 1) __launch_bounds__(kGemmThreads, 1)
     fg_gemm_epi_kernel(const __grid_constant__ GemmParams P) {
-  gemm_body<InterpGemmEpi<D, S>, kGemmCluster, kGemmKB>(P);
+  gemm_body<InterpGemmEpi<D, S>, kGemmCluster, kGemmKB, kGemmN>(P);
 }
 
 cudaError_t launch_gemm_kernel(const GemmParams& p, int big, int grid, int smem, cudaStream_t st) {

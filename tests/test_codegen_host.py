@@ -55,9 +55,10 @@ def test_tuple_programs_compile():
         _compile(plan.source(0))
 
 
-@pytest.mark.parametrize("shape,cl,kb", [(0, 2, 2), (1 << 16, 2, 2), (2 << 16, 4, 2), (1 << 18, 2, 1),
-                                         ((2 << 16) | (1 << 18), 4, 1)])
-def test_gemm_cluster_shapes_compile(shape, cl, kb):
+@pytest.mark.parametrize("shape,cl,kb,tn", [(0, 2, 2, 256), (1 << 16, 2, 2, 256), (2 << 16, 4, 2, 256),
+                                            (1 << 18, 2, 1, 256), ((2 << 16) | (1 << 18), 4, 1, 256),
+                                            (2 << 22, 2, 2, 128), ((2 << 22) | (1 << 18), 2, 1, 128)])
+def test_gemm_cluster_shapes_compile(shape, cl, kb, tn):
     """The GEMM-epilogue program in CTA pairs and in 4-CTA clusters whose two
     pairs share their A rows (multicast), with one or two K blocks per ring
     slot."""
@@ -66,5 +67,5 @@ def test_gemm_cluster_shapes_compile(shape, cl, kb):
     assert plan.groups[0].kind == "gemm"
     src = plan.source(0)
     assert f"__cluster_dims__({cl}, 1, 1)" in src
-    assert f"gemm_body<fg::JitEpi, {cl}, {kb}>" in src
+    assert f"gemm_body<fg::JitEpi, {cl}, {kb}, {tn}>" in src
     _compile(src)

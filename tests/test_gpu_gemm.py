@@ -15,7 +15,8 @@ pytestmark = pytest.mark.gpu
 MODES = [0, _lib.FG_FLAG_INTERPRET]
 PAIRS, CLUSTER4 = 1 << 16, 2 << 16     # GEMM cluster shape: CTA pairs only / two pairs sharing A
 KB1, KB2 = 1 << 18, 2 << 18            # K blocks per operand ring slot
-SHAPES = [CLUSTER4 | KB2, CLUSTER4 | KB1, PAIRS | KB1]
+TN256, TN128 = 1 << 22, 2 << 22        # columns of a pair's tile
+SHAPES = [CLUSTER4 | KB2, CLUSTER4 | KB1, PAIRS | KB1, PAIRS | TN128, PAIRS | KB1 | TN128]
 
 
 def _matmul_graph(K, M, N, ta, tb, epi=None):
@@ -79,6 +80,10 @@ def test_matmul_epilogues(epi, mode):
 
 
 def _sf_update(B, M, N, mode):
+    return _sf_update_flags(B, M, N, mode)
+
+
+def _sf_update_flags(B, M, N, mode):
     spec = W.sf_update(B, M, N)
     g, plan, inputs, dev = prepare(spec, flags=mode)
     assert plan.n_groups == 1 and plan.groups[0].kind == "gemm"
@@ -211,3 +216,24 @@ def test_sf_update_k4096_full_size():
     """The compute-bound SF update (B = K = 4096) in the default launch:
     4-CTA clusters, stream-K shares."""
     _sf_update(4096, 4096, 4096, 0)
+
+
+@pytest.mark.parametrize("K,M,N,cap,kb", [(1024, 1024, 1024, 5, KB2), (1024, 1024, 768, 7, KB1), (1024, 520, 1160, 3, KB2)])
+def test_tn128_split_tail(K, M, N, cap, kb):
+    """128-column pair tiles with the last round split along K (the workspace
+    and flags sized for the narrower tiles); run twice."""
+    spec = W.sf_update(K, M, N)
+    g, plan, inputs, dev = prepare(spec, flags=(cap << 8) | PAIRS | TN128 | kb)
+    ref = OE.run_unfused(spec, inputs)[spec.outputs[0]]
+    w = inputs[2]
+    for _ in range(2):
+        env = run_fused(plan, spec, dev)
+        plan.sync()
+        got = env[spec.outputs[0]].cpu().numpy()
+        assert rel_err(got, ref) <= TOL_F32
+        assert rel_err(w - got, w - ref) <= TOL_BF16
+
+
+def test_sf_update_full_tn128():
+    """The HBM-bound SF update (K = 512) in 128-column pair tiles."""
+    _sf_update_flags(512, 4096, 4096, PAIRS | TN128)
