@@ -464,6 +464,13 @@ __device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* p) {
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+// Counter increment that publishes the caller's earlier writes (release)
+// and, to the thread that reads the last count, everyone's (acquire).
+__device__ __forceinline__ int32_t atom_add_acq_rel_gpu(int32_t* p, int32_t v) {
+  int32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 // L2 eviction policies for TMA copies: operand tiles that other tiles will
 // read again stay (evict_last); data streamed once goes first (evict_first).
 __device__ __forceinline__ uint64_t l2_evict_last() {

@@ -549,20 +549,28 @@ __device__ __forceinline__ void reduce_body(const GroupParams& P) {
       const int r = r0 + lane;
       bool finish = true;
       if (P.nsplit > 1) {
+        // publish this unit's partials with one release increment (the warp
+        // barrier orders the lanes' writes before lane 0's release); the
+        // unit that counts last acquires everyone's and sums them in split
+        // order, its loads issued eight at a time
         if (r < P.FR) P.scratch[(int64_t)sp * P.FR + r] = p;
-        __threadfence();
         __syncwarp();
         int last = 0;
-        if (lane == 0) last = atomicAdd(&P.counters[strip], 1) == P.nsplit - 1;
+        if (lane == 0) last = atom_add_acq_rel_gpu(&P.counters[strip], 1) == P.nsplit - 1;
         last = __shfl_sync(0xffffffffu, last, 0);
+        __syncwarp();
         finish = last != 0;
         if (finish) {
-          __threadfence();
           p = is_sum ? 0.f : neg_inf();
           if (r < P.FR)
-            for (int q = 0; q < P.nsplit; ++q) {
-              const float x = __ldcg(P.scratch + (int64_t)q * P.FR + r);
-              p = is_sum ? __fadd_rn(p, x) : fmaxf(p, x);
+            for (int q0 = 0; q0 < P.nsplit; q0 += 8) {
+              float x[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                x[k] = q0 + k < P.nsplit ? __ldcg(P.scratch + (int64_t)(q0 + k) * P.FR + r) : (is_sum ? 0.f : neg_inf());
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                if (q0 + k < P.nsplit) p = is_sum ? __fadd_rn(p, x[k]) : fmaxf(p, x[k]);
             }
           if (lane == 0) P.counters[strip] = 0;
         }
