@@ -488,7 +488,6 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
   p.a_3d = (a_mn ? cg.M : cg.K) % 64 == 0;
   p.b_3d = (b_mn ? cg.N : cg.K) % 64 == 0;
   p.wait_limit_ns = o.wait_limit_ns;
-  p.epi_stage_bytes = cg.stage_bytes;
   p.epi_tx_bytes = tx;
   p.inject = (o.flags & FG_FLAG_INJECT_NO_LOADS) ? 1 : 0;
   // an IDENT leaf's chunk buffer receives the result in place, so no
@@ -527,24 +526,44 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
   // short K a deep leaf ring (the epilogue streams the leaves from HBM).  A
   // ring slot holds KB K blocks of the CTA's 128 rows of A and of its half of
   // B's columns.
-  const int limit = 227 * 1024 - 256, fixed = 2048 + (p.inplace_off >= 0 ? 0 : 2 * kGemmM * kGemmChunk * 4);
+  // Shared memory: alignment slack, the operand ring, the leaf stages (a
+  // stage of column or row vectors alone needs 128-byte alignment, not the
+  // 1024 of a swizzled box), the output staging and 512 bytes of barriers.
+  int estage = cg.stage_bytes;
+  {
+    bool big = false;
+    int end = 0;
+    for (size_t i = 0; i < cg.leaves.size(); ++i)
+      if (cg.leaves[i].cls != LEAF_GATHER) {
+        big |= gemm_box_bytes(cg.leaves[i].cls) >= 1024;
+        end = std::max(end, cg.leaf_stage_off[i] + (gemm_box_bytes(cg.leaves[i].cls) + 127) / 128 * 128);
+      }
+    if (!big && end > 0) estage = end;
+  }
+  p.epi_stage_bytes = estage;
+  const int limit = 227 * 1024 - 64;   // less the kernel's static shared variables
+  const int fixed = 1024 + 512 + (p.inplace_off >= 0 ? 0 : 2 * kGemmM * kGemmChunk * 4);
+  auto leaf_area = [&](int n) { return (n * estage + 1023) / 1024 * 1024; };
   const int stage = KB * (kGemmM + TN / 2) * kGemmK * 2;
   int ns = 0, ne = 0;
   static const std::vector<std::pair<int, int>> prefs_short = {{2, 6}, {2, 5}, {2, 4}, {2, 3}, {2, 2}};
   static const std::vector<std::pair<int, int>> prefs_long = {{3, 2}, {2, 4}, {2, 3}, {2, 2}};
-  const bool short_k = p.nkb <= 16 && cg.stage_bytes > 0;
+  const bool short_k = p.nkb <= 16 && estage > 0;
   for (const auto& q : short_k ? prefs_short : prefs_long) {
     // the same bytes in flight with one-block slots: twice as many
     const int qs = q.first * (2 / KB);
-    if (!ns && fixed + qs * stage + q.second * cg.stage_bytes <= limit) {
+    if (!ns && fixed + qs * stage + leaf_area(q.second) <= limit) {
       ns = qs;
       ne = q.second;
     }
   }
   if (!ns) throw CompileError{FG_EUNSUPPORTED, "GEMM epilogue stages do not fit in shared memory"};
+  // small leaf chunks (column or row vectors): as many leaf buffers as still
+  // fit, up to the barriers there are (each chunk's load is a round trip)
+  while (estage > 0 && ne < 8 && fixed + ns * stage + leaf_area(ne + 1) <= limit) ++ne;
   p.nstages = ns;
   p.n_epi_bufs = ne;
-  ge.smem = fixed + ns * stage + ne * cg.stage_bytes;
+  ge.smem = fixed + ns * stage + leaf_area(ne);
   // more than half of an SM's shared memory: one CTA per SM, so no two CTAs
   // ever compete for the SM's TMEM
   ge.smem = std::max(ge.smem, 120 * 1024);

@@ -277,15 +277,18 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   __shared__ int issued[2];            // operand slots issued by the A and B producers
   __shared__ uint32_t tmem_slot;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // layout: operand ring | epilogue leaf stages | output staging (per-warp
+  // 4 KB boxes, when the result is not written in place) | barriers; the
+  // ring and the output staging 1024-byte aligned (128-byte swizzle)
+  const int NS = P.nstages, NE = P.n_epi_bufs;
+  uint8_t* opnd = smem;
+  uint8_t* ebuf = opnd + NS * kStageBytes;
+  uint8_t* obuf = ebuf + ((NE * P.epi_stage_bytes + 1023) & ~1023);
   // barriers: full[16] empty[16] tfull[2] tempty[2] efull[8] eempty[8] done
   // last[8] (one per epilogue warp)
-  const uint32_t bars = smem_u32(smem);
+  const uint32_t bars = smem_u32(obuf + (P.inplace_off >= 0 ? 0 : 2 * kGemmOutBytes));
   const uint32_t full0 = bars, empty0 = bars + 128, tfull0 = bars + 256, tempty0 = bars + 272;
   const uint32_t efull0 = bars + 288, eempty0 = bars + 352, done_bar = bars + 416, last0 = bars + 424;
-  uint8_t* opnd = smem + 1024;
-  const int NS = P.nstages, NE = P.n_epi_bufs;
-  uint8_t* ebuf = opnd + NS * kStageBytes;
-  uint8_t* obuf = ebuf + NE * P.epi_stage_bytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool staged = P.epi_tx_bytes > 0;
   const int nslots = (P.nkb + KB - 1) / KB;                       // ring slots per tile
