@@ -430,9 +430,14 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
     rows = {}
     l2 = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
 
-    def timed(fn, reps=10, flush=True, inner=1):
+    def timed(fn, reps=10, flush=True, inner=None):
         """Median and min ms of `inner` back-to-back calls (L2 flushed first
-        when asked), over `reps` repetitions."""
+        when asked), over `reps` repetitions.  Without a flush the calls run
+        ten at a time by default: a single call after a synchronize would also
+        count the host's launch work, during which the device is idle (after
+        a flush, the flush kernel covers it)."""
+        if inner is None:
+            inner = 1 if flush else 10
         fn()
         torch.cuda.synchronize()
         ts = []
