@@ -149,6 +149,50 @@ def cpu_sample(rows=1024, reps=3):
             "sample": f"diamond slab X,Z[{rows},{C}] op by op in float64, best of {reps} ({t:.2f} s each)"}
 
 
+def oracle_samples():
+    """The oracle, as it stands, beside the other configurations' GPU rows:
+    each on a bounded sample, its wall time and the sample's algorithmic
+    throughput (numpy ufuncs run on one core; the float64 matmul of the SF
+    update on every BLAS thread)."""
+    import workloads as W
+    from oracle import execute as OE
+    from oracle import pack as OP
+
+    def best(f, reps=2):
+        ts = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            f()
+            ts.append(time.perf_counter() - t0)
+        return min(ts)
+
+    out = {}
+    sp = W.rnnlm_chain()
+    ins = W.make_inputs(sp, 0)
+    t = best(lambda: OE.run_unfused(sp, ins), 3)
+    out["rnnlm_chain"] = {"ms": t * 1e3, "sample": "the whole chain X, Y [64,1024]", "cores": 1}
+    sp = W.sf_update(512, 256, 4096)
+    ins = W.make_inputs(sp, 0)
+    t = best(lambda: OE.run_unfused(sp, ins))
+    out["sf_update_K512"] = {"ms": t * 1e3, "TFLOPs": 2 * 512 * 256 * 4096 / t / 1e12, "cores": os.cpu_count(),
+                             "sample": "rows 0..255 of W (1/16 of the output): U [512,256], V [512,4096]",
+                             "ms_full_estimate": t * 16e3}
+    sizes = W.tensor_fusion_sizes(0)
+    xs = W.tensor_fusion_inputs(sizes)
+    tp = best(lambda: OP.pack(xs, 0.125))
+    buf = OP.pack(xs, 0.125)
+    tu = best(lambda: OP.unpack(buf, [int(n) for n in sizes], 1.0))
+    out["tensor_fusion"] = {"pack_ms": tp * 1e3, "unpack_ms": tu * 1e3, "cores": 1,
+                            "pack_GBps": int(sizes.sum()) * 6 / tp / 1e9, "sample": "all 161 tensors"}
+    sp = W.random_dag(0, R=512, C=256, nominal_R=8192, nominal_C=4096)
+    ins = W.make_inputs(sp, 0)
+    t = best(lambda: OE.run_unfused(sp, ins), 1)
+    out["random_dag_seed0"] = {"ms": t * 1e3, "cores": 1, "GBps": W.algorithmic_bytes_unfused(sp) / t / 1e9,
+                               "sample": "the same 200-operator graph on [512,256] values (1/256 of the elements)",
+                               "ms_full_estimate": t * 256e3}
+    return out
+
+
 def run_reference(args):
     dist, rank, ws, _ = setup_dist(args)
     if rank != 0:
@@ -330,6 +374,8 @@ def main():
     if rank == 0 and not args.no_rows:
         line["rows"] = secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf16s)
         line["cpu_baseline"] = cpu_sample()
+        for k, v in oracle_samples().items():
+            line["rows"].setdefault(k, {})["oracle"] = v
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
