@@ -475,10 +475,12 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
     """Other hot-path rows, measured outside the headline's timed region."""
     rows = {}
     l2 = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    l2r = torch.zeros(256 << 20, dtype=torch.uint8, device="cuda")
 
     def timed(fn, reps=10, flush=True, inner=None):
         """Median and min ms of `inner` back-to-back calls (L2 flushed first
-        when asked), over `reps` repetitions.  Without a flush the calls run
+        when asked: written, then evicted clean), over `reps` repetitions.
+        Without a flush the calls run
         ten at a time by default: a single call after a synchronize would also
         count the host's launch work, during which the device is idle (after
         a flush, the flush kernel covers it)."""
@@ -489,7 +491,11 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
         ts = []
         for _ in range(reps):
             if flush:
+                # write a buffer twice L2's size, then read another: L2 ends
+                # cold and clean, so the timed launch neither hits its own
+                # data nor writes back the flush's dirty lines
                 l2.fill_(1)
+                l2r.max()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             for _ in range(inner):
