@@ -129,6 +129,7 @@ constexpr int kMaxEpiLeaves = 8;
 constexpr int kTileR = 32;
 constexpr int kTileC = 64;
 constexpr int kConsumerWarps = 8;
+constexpr int kProducerWarps = 2;     // group kernels: TMA producers taking alternate tiles
 constexpr int kMaxStages = 16;
 
 enum RedOp : int { RED_NONE = 0, RED_SUM = 1, RED_MAX = 2 };

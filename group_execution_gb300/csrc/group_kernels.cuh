@@ -22,7 +22,7 @@
 
 namespace fg {
 
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kThreads = (kConsumerWarps + kProducerWarps) * 32;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kOutBufBytes = kTileR * kTileC * 4;   // 8 KB
 constexpr int kXOutSliceBytes = kOutBufBytes;        // per extra output: 8 warps x 32 x 8 floats
@@ -324,17 +324,25 @@ struct RedTiles {   // units (row strip, column split), then the split's tiles
   }
 };
 
-// The producer: one thread issues the TMA loads of every staged leaf for each
-// tile into the ring; on a timeout it waits for its loads still in flight.
+// A producer: one thread issues the TMA loads of every staged leaf for the
+// tiles i = par, par + kProducerWarps, ... into the ring (a thread takes a few
+// hundred ns to wait for a stage, arm it and issue its copies: two producers
+// keep more loads in flight); on a timeout it waits for its loads still in
+// flight.  With at least two stages, each producer's previous wait ensures the
+// parity it waits for belongs to the current use of the stage.
 template <class Prog, class Tiles>
 __device__ __forceinline__ void producer_loop(const GroupParams& P, const typename Prog::Tables& T, const Ring& R,
-                                              Tiles tiles, volatile int* abort_flag) {
+                                              Tiles tiles, volatile int* abort_flag, int par) {
   if (P.inject) return;   // failure injection: consumers wait for loads that never come
   Prog::prefetch(P, T);
   const int NS = P.nstages;
   int i = 0, tr, tc;
   bool ok = true;
   while (tiles.next(tr, tc)) {
+    if (i % kProducerWarps != par) {
+      ++i;
+      continue;
+    }
     const int s = i % NS;
     if (i >= NS && !wait_or_abort(R.empty_s + 8 * s, ((i / NS) & 1) ^ 1, P.wait_limit_ns, abort_flag)) {
       ok = false;
@@ -349,7 +357,8 @@ __device__ __forceinline__ void producer_loop(const GroupParams& P, const typena
     *abort_flag = 1;
     set_error(P.err, DEVERR_TIMEOUT);
     const int64_t drain = P.wait_limit_ns > kDrainLimitNs ? P.wait_limit_ns : kDrainLimitNs;
-    for (int k = i - NS < 0 ? 0 : i - NS; k < i; ++k) mbar_wait(R.full_s + 8 * (k % NS), (k / NS) & 1, drain);
+    for (int k = i - NS < 0 ? 0 : i - NS; k < i; ++k)
+      if (k % kProducerWarps == par) mbar_wait(R.full_s + 8 * (k % NS), (k / NS) & 1, drain);
   }
 }
 
@@ -373,10 +382,10 @@ __device__ __forceinline__ void ew_body(const GroupParams& P) {
   }
   __syncthreads();
 
-  if (warp == kConsumerWarps) {
+  if (warp >= kConsumerWarps) {
     if (lane == 0)
       producer_loop<Prog>(P, T, R, EwTiles{(int)blockIdx.x, (int)gridDim.x, P.ntiles, P.ntr, P.ntc, P.band},
-                          &abort_flag);
+                          &abort_flag, warp - kConsumerWarps);
     return;
   }
 
@@ -491,12 +500,12 @@ __device__ __forceinline__ void reduce_body(const GroupParams& P) {
   }
   __syncthreads();
 
-  if (warp == kConsumerWarps) {
+  if (warp >= kConsumerWarps) {
     if (lane == 0)
       producer_loop<Prog>(P, T, R,
                           RedTiles{(int)blockIdx.x, (int)gridDim.x, P.nunits, P.nsplit, P.tiles_per_split, P.ntc, 0, 0,
                                    0, false},
-                          &abort_flag);
+                          &abort_flag, warp - kConsumerWarps);
     return;
   }
 
