@@ -237,3 +237,23 @@ def test_tn128_split_tail(K, M, N, cap, kb):
 def test_sf_update_full_tn128():
     """The HBM-bound SF update (K = 512) in 128-column pair tiles."""
     _sf_update_flags(512, 4096, 4096, PAIRS | TN128)
+
+
+SK = 2 << 20   # schedule: equal shares of all tiles' K steps
+
+
+@pytest.mark.parametrize("K,M,N,cap,kb", [(2048, 1024, 1024, 5, KB2), (1152, 776, 1800, 7, KB1), (4096, 512, 768, 4, KB2)])
+def test_pairs_stream_k(K, M, N, cap, kb):
+    """CTA pairs walking equal shares of all tiles' K steps: a share boundary
+    cuts a tile into two pieces, the one ending a share finishing it; run
+    twice (the ready flags are cleared by their readers)."""
+    spec = W.sf_update(K, M, N)
+    g, plan, inputs, dev = prepare(spec, flags=(cap << 8) | PAIRS | SK | kb)
+    ref = OE.run_unfused(spec, inputs)[spec.outputs[0]]
+    w = inputs[2]
+    for _ in range(2):
+        env = run_fused(plan, spec, dev)
+        plan.sync()
+        got = env[spec.outputs[0]].cpu().numpy()
+        assert rel_err(got, ref) <= TOL_F32
+        assert rel_err(w - got, w - ref) <= TOL_BF16
