@@ -6,35 +6,35 @@
 // workload).
 //
 // Persistent: CTAs run in pairs on the SMs of one TPC, and a pair walks
-// 256 x 256 output tiles.  Each CTA stages half of the tile's A rows and half
-// of its B columns, two 64-deep K blocks (64 KB) per ring slot, each operand
-// half in one TMA copy where the layout allows; the even CTA issues 2-SM
-// tcgen05.mma instructions (cta_group::2) that read both CTAs' halves and
-// leave each CTA's 128 accumulator rows in its own TMEM.  In a 4-CTA cluster
-// two pairs take side-by-side tiles of the same 256 rows: each A half is
-// fetched once, by the two CTAs that need it taking one K block each and
-// multicasting it to both, so the cluster reads 3/4 of the operand bytes
-// two independent pairs would.  Warp roles, in each CTA:
-//   warp 0  TMA producer of the bf16 A halves, arming the even CTA's slot
-//           barrier; every operand load completes on the even CTA's slot
-//           barrier of each destination's pair,
-//   warp 7  TMA producer of the B halves (a slot's copies issue at a few
-//           hundred ns each from one thread: two producers halve the time
-//           from a slot's release to its refill),
-//   warp 1  allocates TMEM (2 x 256 columns: double-buffered accumulator,
-//           jointly with the peer) and, in the even CTA, issues the MMAs from
-//           one thread,
-//   warp 2  TMA producer of the epilogue leaves, 128 x 32 chunk by chunk,
-//   warps 3-6 and 8-11 epilogue, the two sets taking alternate 32-column
-//           chunks (a chunk's TMEM read, leaf reads, epilogue and store are
-//           one warp's serial chain): each thread owns one accumulator row
-//           (TMEM lane),
-//           reads 32 columns per chunk with tcgen05.ld, evaluates the
-//           epilogue program eight values at a time and stages the result
-//           for a TMA store.
-// The epilogue of tile i overlaps the MMAs of tile i+1.  Every wait is
-// bounded; on expiry the CTA records the error, drains its copies, frees its
-// TMEM and returns.
+// 256 x TN output tiles (TN = 256, or 128 by choice).  Each CTA stages half of
+// the tile's A rows and half of its B columns, KB 64-deep K blocks per ring
+// slot (two by default: 64 KB), each operand half in one TMA copy where the
+// layout allows; the even CTA issues 2-SM tcgen05.mma instructions
+// (cta_group::2) that read both CTAs' halves and leave each CTA's 128
+// accumulator rows in its own TMEM.  In a 4-CTA cluster (by choice) two pairs
+// take side-by-side tiles of the same 256 rows: each A half is fetched once,
+// by the two CTAs that need it taking half of it each and multicasting it to
+// both.  Warp roles, in each CTA:
+//   warp 0     TMA producer of the bf16 A halves, arming the even CTA's slot
+//              barrier; every operand load completes on the even CTA's slot
+//              barrier of each destination's pair,
+//   warp 7     TMA producer of the B halves (a slot's copies issue at a few
+//              hundred ns each from one thread: two producers halve the time
+//              from a slot's release to its refill),
+//   warp 1     allocates TMEM (two accumulator buffers, jointly with the
+//              peer) and, in the even CTA, issues the MMAs from one thread,
+//   warp 2     TMA producer of the epilogue leaves, 128 x 32 chunk by chunk,
+//   warps 3-6  epilogue, and warps 8-11 a second set taking the alternate
+//              32-column chunks (a chunk's TMEM read, leaf reads, epilogue
+//              and store are one warp's serial chain): each thread owns one
+//              accumulator row (TMEM lane), reads 32 columns per chunk with
+//              tcgen05.ld, evaluates the epilogue program eight values at a
+//              time and stages the result for a TMA store.
+// The epilogue of tile i overlaps the MMAs of tile i+1.  A tile cut along K
+// (the last round's, or at a share boundary) meets its two partial
+// accumulators in a workspace; the CTA's last item uses the idle operand ring
+// for its stores.  Every wait is bounded; on expiry the CTA records the
+// error, drains its copies, frees its TMEM and returns.
 #pragma once
 #include "fg_device.cuh"
 
