@@ -77,6 +77,14 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, int32_t x, in
                ::"l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(src)
                : "memory");
 }
+// Programmatic dependent launch: a grid lets the next grid on the stream be
+// placed on the SMs while it drains, and waits, before its own first global
+// memory access, for the previous grid to complete with its writes visible.
+// Both are no-ops for a launch that did not ask for the overlap.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // Contiguous copy global -> shared (both 16-byte aligned, bytes a multiple
 // of 16), counted on an mbarrier.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

@@ -334,6 +334,8 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   cluster_sync();   // the peer's barriers are initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  pdl_launch_dependents();
+  pdl_wait();   // the previous grid's writes are visible from here on
   const int64_t limit = P.wait_limit_ns;
   const int64_t drain = limit > kDrainLimitNs ? limit : kDrainLimitNs;
   const GemmSched S = gemm_sched(P, cl, ncl, nslots);

@@ -381,6 +381,8 @@ __device__ __forceinline__ void ew_body(const GroupParams& P) {
     if (P.out_tma) tma_prefetch(&P.maps[kMaxStaged]);
   }
   __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait();   // the previous grid's writes are visible from here on
 
   if (warp >= kConsumerWarps) {
     if (lane == 0)
@@ -499,6 +501,8 @@ __device__ __forceinline__ void reduce_body(const GroupParams& P) {
     init_barriers(R, P.nstages);
   }
   __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait();   // the previous grid's writes are visible from here on
 
   if (warp >= kConsumerWarps) {
     if (lane == 0)

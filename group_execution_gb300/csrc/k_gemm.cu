@@ -17,7 +17,10 @@ cudaError_t launch_gemm_kernel(const GemmParams& p, int big, int grid, int smem,
   auto k = big ? fg_gemm_epi_kernel<8, 8> : fg_gemm_epi_kernel<4, 4>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, kGemmThreads, smem, st>>>(p);
+  cudaLaunchConfig_t cfg = pdl_config(grid, kGemmThreads, smem, st);
+  cudaLaunchAttribute at[1];
+  pdl_attr(cfg, at);
+  cudaLaunchKernelEx(&cfg, k, p);
   return cudaGetLastError();
 }
 

@@ -23,7 +23,10 @@ template <class K>
 static cudaError_t launch_one(K kernel, const GroupParams& p, int grid, int smem, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, kThreads, smem, st>>>(p);
+  cudaLaunchConfig_t cfg = pdl_config(grid, kThreads, smem, st);
+  cudaLaunchAttribute at[1];
+  pdl_attr(cfg, at);
+  cudaLaunchKernelEx(&cfg, kernel, p);
   return cudaGetLastError();
 }
 

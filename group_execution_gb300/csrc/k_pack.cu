@@ -43,6 +43,8 @@ __device__ __forceinline__ void zero_pad(uint8_t* p, int bytes) {
 
 __global__ void __launch_bounds__(kPackThreads) tf_pack_kernel(const TfChunk* __restrict__ chunks, int nchunks,
                                                                int bf16, float scale, uint8_t* __restrict__ buf) {
+  pdl_launch_dependents();
+  pdl_wait();   // the previous grid's writes are visible from here on
   int ci = blockIdx.x;
   if (ci >= nchunks) return;
   TfChunk c = chunks[ci];
@@ -115,6 +117,8 @@ __global__ void __launch_bounds__(kUnpackThreadsTma, 1)
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait();   // the previous grid's writes are visible from here on
   const int warp = threadIdx.x >> 5;
 
   if (warp == 0) {
@@ -199,7 +203,10 @@ __global__ void __launch_bounds__(kUnpackThreadsTma, 1)
 
 cudaError_t launch_tf_pack(const TfChunk* chunks, int nchunks, int buf_bf16, float scale, void* buf, int grid,
                            cudaStream_t st) {
-  tf_pack_kernel<<<grid, kPackThreads, 0, st>>>(chunks, nchunks, buf_bf16, scale, static_cast<uint8_t*>(buf));
+  cudaLaunchConfig_t cfg = pdl_config(grid, kPackThreads, 0, st);
+  cudaLaunchAttribute at[1];
+  pdl_attr(cfg, at);
+  cudaLaunchKernelEx(&cfg, tf_pack_kernel, chunks, nchunks, buf_bf16, scale, static_cast<uint8_t*>(buf));
   return cudaGetLastError();
 }
 
@@ -223,8 +230,10 @@ cudaError_t launch_tf_unpack(const TfChunk* chunks, int nchunks, int buf_bf16, f
     if (e != cudaSuccess) return e;
     opted.fetch_or(bit, std::memory_order_release);
   }
-  tf_unpack_kernel<<<grid, kUnpackThreadsTma, smem, st>>>(chunks, nchunks, buf_bf16, uscale,
-                                                          static_cast<const uint8_t*>(buf), err);
+  cudaLaunchConfig_t cfg = pdl_config(grid, kUnpackThreadsTma, smem, st);
+  cudaLaunchAttribute at[1];
+  pdl_attr(cfg, at);
+  cudaLaunchKernelEx(&cfg, tf_unpack_kernel, chunks, nchunks, buf_bf16, uscale, static_cast<const uint8_t*>(buf), err);
   return cudaGetLastError();
 }
 

@@ -6,6 +6,24 @@
 
 namespace fg {
 
+// Launch configuration that lets a kernel be placed while the previous grid
+// on the stream drains (programmatic dependent launch); every kernel here
+// waits for that grid before its first global memory access.
+inline cudaLaunchConfig_t pdl_config(int grid, int block, int smem, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  return cfg;
+}
+inline void pdl_attr(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&at)[1]) {
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+}
+
 // exec: 0 = elementwise group (K1), 1 = reduce group (K2).  big selects the
 // 8-register / 8-slot machine (one CTA per SM) over the 4/4 one.
 cudaError_t launch_group_kernel(const GroupParams& p, int exec, int big, int grid, int smem, cudaStream_t st);
