@@ -479,6 +479,15 @@ __device__ __forceinline__ int32_t atom_add_acq_rel_gpu(int32_t* p, int32_t v) {
   asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
 }
+// Counter increment that only publishes the caller's earlier writes: later
+// operations of the thread do not wait for it (its old value arrives in a
+// register whenever the thread reads it).
+__device__ __forceinline__ int32_t atom_add_release_gpu(int32_t* p, int32_t v) {
+  int32_t old;
+  asm volatile("atom.release.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 // L2 eviction policies for TMA copies: operand tiles that other tiles will
 // read again stay (evict_last); data streamed once goes first (evict_first).
 __device__ __forceinline__ uint64_t l2_evict_last() {

@@ -480,6 +480,37 @@ __device__ __forceinline__ void ew_body(const GroupParams& P) {
   if (P.out_tma == 2 && lane == 0) bulk_wait<0>();
 }
 
+// A consumer warp of a reduce CTA, once the count of a split unit of `strip` has
+// arrived (`old`: the counter before its increment, lane 0): the unit that
+// counted last acquires the other
+// units' partials (their release increments precede its own in the counter's
+// order), sums them in split order, loads issued eight at a time, and writes
+// the epilogue's result.
+template <class Prog>
+__device__ __forceinline__ void reduce_finish(const GroupParams& P, const typename Prog::Tables& T, int strip,
+                                              int old, bool is_sum) {
+  const int lane = threadIdx.x & 31;
+  const bool last = __shfl_sync(0xffffffffu, old, 0) == P.nsplit - 1;
+  if (!last) return;
+  fence_acq_rel_gpu();
+  __syncwarp();
+  const int r = strip * kTileR + lane;
+  float p = is_sum ? 0.f : neg_inf();
+  if (r < P.FR) {
+    for (int q0 = 0; q0 < P.nsplit; q0 += 8) {
+      float x[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        x[k] = q0 + k < P.nsplit ? __ldcg(P.scratch + (int64_t)(q0 + k) * P.FR + r) : (is_sum ? 0.f : neg_inf());
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (q0 + k < P.nsplit) p = is_sum ? __fadd_rn(p, x[k]) : fmaxf(p, x[k]);
+    }
+    P.out[r] = Prog::epi(P, T, r, p);
+  }
+  if (lane == 0) P.counters[strip] = 0;
+}
+
 // ---------------------------------------------------------------------------------
 // K2 body: group ending in a row reduction over the frame's last axis, with an
 // optional elementwise epilogue on the reduced vector.  Work units are
@@ -519,6 +550,7 @@ __device__ __forceinline__ void reduce_body(const GroupParams& P) {
   float o[8];
   int i = 0, k_unit = 0;
   bool dead = false;
+  int pend_strip = -1, pend_old = 0;   // this warp's split unit whose count is in flight
   for (int u = blockIdx.x; u < P.nunits; u += gridDim.x, ++k_unit) {
     const int strip = u / P.nsplit, sp = u % P.nsplit;
     const int tcb = sp * P.tiles_per_split;
@@ -556,41 +588,29 @@ __device__ __forceinline__ void reduce_body(const GroupParams& P) {
     float* rb = red + (k_unit & 1) * (kConsumerWarps * 32);
     rb[warp * 32 + lane] = acc;
     if (consumer_bar_or(dead)) break;
-    if (warp == 0) {
+    // the unit's combine falls to the warps in turn: publishing partials
+    // holds the publishing warp until its stores are acknowledged, and one
+    // warp in eight units is a stall the ring absorbs
+    if (warp == k_unit % kConsumerWarps) {
       float p = rb[lane];
       for (int w = 1; w < kConsumerWarps; ++w) p = is_sum ? __fadd_rn(p, rb[w * 32 + lane]) : fmaxf(p, rb[w * 32 + lane]);
       const int r = r0 + lane;
-      bool finish = true;
       if (P.nsplit > 1) {
-        // publish this unit's partials with one release increment (the warp
-        // barrier orders the lanes' writes before lane 0's release); the
-        // unit that counts last acquires everyone's and sums them in split
-        // order, its loads issued eight at a time
+        // this warp's previous split unit's count has arrived by now:
+        // finish its strip if it counted last; then publish this unit's
+        // partials with a release increment whose old value is read only at
+        // this warp's next combine
+        if (pend_strip >= 0) reduce_finish<Prog>(P, T, pend_strip, pend_old, is_sum);
         if (r < P.FR) P.scratch[(int64_t)sp * P.FR + r] = p;
         __syncwarp();
-        int last = 0;
-        if (lane == 0) last = atom_add_acq_rel_gpu(&P.counters[strip], 1) == P.nsplit - 1;
-        last = __shfl_sync(0xffffffffu, last, 0);
-        __syncwarp();
-        finish = last != 0;
-        if (finish) {
-          p = is_sum ? 0.f : neg_inf();
-          if (r < P.FR)
-            for (int q0 = 0; q0 < P.nsplit; q0 += 8) {
-              float x[8];
-#pragma unroll
-              for (int k = 0; k < 8; ++k)
-                x[k] = q0 + k < P.nsplit ? __ldcg(P.scratch + (int64_t)(q0 + k) * P.FR + r) : (is_sum ? 0.f : neg_inf());
-#pragma unroll
-              for (int k = 0; k < 8; ++k)
-                if (q0 + k < P.nsplit) p = is_sum ? __fadd_rn(p, x[k]) : fmaxf(p, x[k]);
-            }
-          if (lane == 0) P.counters[strip] = 0;
-        }
+        if (lane == 0) pend_old = atom_add_release_gpu(&P.counters[strip], 1);   // compared at the next end
+        pend_strip = strip;
+      } else if (r < P.FR) {
+        P.out[r] = Prog::epi(P, T, r, p);
       }
-      if (finish && r < P.FR) P.out[r] = Prog::epi(P, T, r, p);
     }
   }
+  if (pend_strip >= 0 && !dead) reduce_finish<Prog>(P, T, pend_strip, pend_old, is_sum);
 }
 
 }  // namespace fg
