@@ -165,3 +165,26 @@ def test_launch_rejects_bad_pointers():
         plan.launch_group(0, ptrs)
     plan.launch_group(0, {v: dev[v] for v in info.leaves} | {info.out: out})
     plan.sync()
+
+
+@pytest.mark.parametrize("tpu", [1, 2, 5, 16])
+@pytest.mark.parametrize("shape", [(1024, 4096), (700, 1000)])
+def test_row_reductions_forced_splits(tpu, shape):
+    """Rows cut into units of `tpu` column tiles (flag bits 16-23): many split
+    units per CTA, so every consumer warp in turn publishes partials and
+    finishes strips across consecutive units; with an epilogue on the reduced
+    vector; run twice (the strips' counters are cleared by their finishers)."""
+    R, C = shape
+    for op in ("rowsum", "rowmax"):
+        spec = W.GraphSpec()
+        x = spec.input((R, C))
+        v = spec.input((C,))
+        s = spec.op(op, (spec.op("badd_col", (spec.op("relu", (x,)), v)),))
+        spec.mark_output(spec.op("sigmoid", (s,)))
+        g, plan, inputs, dev = prepare(spec, 0, allow_reduce_epilogue=True, flags=tpu << 16)
+        assert plan.n_groups == 1 and plan.groups[0].kind == "reduce"
+        ref = OE.run_unfused(spec, inputs)[spec.outputs[0]]
+        for _ in range(2):
+            env = run_fused(plan, spec, dev)
+            plan.sync()
+            assert rel_err(env[spec.outputs[0]].cpu().numpy(), ref) <= TOL_F32
