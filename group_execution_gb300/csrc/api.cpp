@@ -549,6 +549,16 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
   static const std::vector<std::pair<int, int>> prefs_short = {{2, 6}, {2, 5}, {2, 4}, {2, 3}, {2, 2}};
   static const std::vector<std::pair<int, int>> prefs_long = {{3, 2}, {2, 4}, {2, 3}, {2, 2}};
   const bool short_k = p.nkb <= 16 && estage > 0;
+  // results written in place leave through the epilogue warps' own stores
+  // (short K: the leaf buffers turn over fastest when each warp frees its
+  // rows as soon as its copy has read them) or through the leaf producer,
+  // one copy per chunk before it reloads the buffer (long K: no epilogue
+  // warp waits for a copy); flag bits 24-25: 1 = producer, 2 = warps, 0 =
+  // chosen
+  {
+    const int stf = (o.flags >> 24) & 3;
+    p.wstore = p.inplace_off >= 0 && (stf == 2 || (stf == 0 && short_k)) ? 1 : 0;
+  }
   for (const auto& q : short_k ? prefs_short : prefs_long) {
     // the same bytes in flight with one-block slots: twice as many
     const int qs = q.first * (2 / KB);
@@ -558,6 +568,9 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
     }
   }
   if (!ns) throw CompileError{FG_EUNSUPPORTED, "GEMM epilogue stages do not fit in shared memory"};
+  // the CTA's last item stages each TMEM lane quarter's results (and the
+  // other piece's partial) in TN * 128 bytes of the idle operand ring
+  if (ns * stage < 4 * TN * 128) throw CompileError{FG_EUNSUPPORTED, "internal: GEMM operand ring below the last item's staging"};
   // small leaf chunks (column or row vectors): as many leaf buffers as still
   // fit, up to the barriers there are (each chunk's load is a round trip)
   while (estage > 0 && ne < 8 && fixed + ns * stage + leaf_area(ne + 1) <= limit) ++ne;
@@ -781,8 +794,11 @@ fg_status launch_gemm(GroupExec& ge, void* const* ptrs, void* stream) {
           return st;
     }
     gp.out = static_cast<float*>(ptrs[cg.out_value]);
-    // each epilogue warp stores its own 32 x 32 box
+    // each epilogue warp stores its own 32 x 32 box; results written in
+    // place leave a whole 128 x 32 chunk at a time
     if (fg_status st = leaf_map(&gp.maps[kMaxStaged], ptrs[cg.out_value], LEAF_IDENT, cg.FR, cg.FC, 32, kGemmChunk))
+      return st;
+    if (fg_status st = leaf_map(&gp.maps[kMaxStaged + 1], ptrs[cg.out_value], LEAF_IDENT, cg.FR, cg.FC, kGemmM, kGemmChunk))
       return st;
     ge.last_ptrs = key;
   }

@@ -170,7 +170,8 @@ constexpr int kGemmCluster4 = 4;       // two pairs on adjacent 256-column tiles
 
 struct GemmParams {
   CUtensorMap mapA, mapB;              // bf16 operands (boxes per major-ness)
-  CUtensorMap maps[kMaxStaged + 1];    // epilogue leaves, [kMaxStaged] = output
+  CUtensorMap maps[kMaxStaged + 2];    // epilogue leaves, [kMaxStaged] = output in 32 x 32 boxes,
+                                       // [kMaxStaged + 1] = output in 128 x 32 boxes
   VmInstr prog[kMaxProg];              // epilogue program (interpreted variant)
   LeafDesc leaves[kMaxLeaves];
   float* out;
@@ -186,6 +187,9 @@ struct GemmParams {
   int32_t nstages;                     // operand ring depth
   int32_t epi_stage_bytes, epi_tx_bytes, n_epi_bufs;
   int32_t inplace_off;                 // >= 0: the result overwrites this IDENT leaf's chunk (no out buffers)
+  int32_t wstore;                      // in place: 1 = each epilogue warp stores its rows of the chunk and
+                                       // frees the buffer once the copy has read them; 0 = the leaf producer
+                                       // stores the whole chunk before reloading the buffer
   int32_t inject;                      // failure injection: 1 = the producers issue no loads
   // work units: a cluster's tiles (the pair's 256 x 256 tile, or the two
   // pairs' 256 x 512) in row-major order

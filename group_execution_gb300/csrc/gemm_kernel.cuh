@@ -23,13 +23,17 @@
 //              from a slot's release to its refill),
 //   warp 1     allocates TMEM (two accumulator buffers, jointly with the
 //              peer) and, in the even CTA, issues the MMAs from one thread,
-//   warp 2     TMA producer of the epilogue leaves, 128 x 32 chunk by chunk,
+//   warp 2     TMA producer of the epilogue leaves, 128 x 32 chunk by chunk
+//              (for long K it also stores the results written in place of an
+//              IDENT leaf's chunk, one copy per chunk, before the buffer is
+//              loaded again),
 //   warps 3-6  epilogue, and warps 8-11 a second set taking the alternate
-//              32-column chunks (a chunk's TMEM read, leaf reads, epilogue
-//              and store are one warp's serial chain): each thread owns one
+//              32-column chunks (a chunk's TMEM read, leaf reads and
+//              epilogue are one warp's serial chain): each thread owns one
 //              accumulator row (TMEM lane), reads 32 columns per chunk with
 //              tcgen05.ld, evaluates the epilogue program eight values at a
-//              time and stages the result for a TMA store.
+//              time and stages the result for a TMA store (its own, or, for
+//              results written in place with long K, warp 2's).
 // The epilogue of tile i overlaps the MMAs of tile i+1.  A tile cut along K
 // (the last round's, or at a share boundary) meets its two partial
 // accumulators in a workspace; the CTA's last item uses the idle operand ring
@@ -289,6 +293,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   const uint32_t bars = smem_u32(obuf + (P.inplace_off >= 0 ? 0 : 2 * kGemmOutBytes));
   const uint32_t full0 = bars, empty0 = bars + 128, tfull0 = bars + 256, tempty0 = bars + 272;
   const uint32_t efull0 = bars + 288, eempty0 = bars + 352, done_bar = bars + 416, last0 = bars + 424;
+  const bool inplace = P.inplace_off >= 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool staged = P.epi_tx_bytes > 0;
   const int nslots = (P.nkb + KB - 1) / KB;                       // ring slots per tile
@@ -322,7 +327,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
     }
     for (int e = 0; e < NE; ++e) {
       mbar_init(efull0 + 8 * e, 1);
-      mbar_init(eempty0 + 8 * e, 4);
+      mbar_init(eempty0 + 8 * e, 4);   // the four warps of the chunk's set
     }
     mbar_init(done_bar, 1);
     for (int k = 0; k < 8; ++k) mbar_init(last0 + 8 * k, 1);
@@ -487,6 +492,36 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
     // ---- epilogue leaf producer ----
     if (lane == 0 && staged && !P.inject) {
       Epi::prefetch(P);
+      // the oldest chunk whose buffer has not been taken back: item rx,
+      // column chunk rj; its results leave from the buffer (in place) when
+      // this CTA finishes the unit and it is not the CTA's last item (whose
+      // results go out from the operand ring, warp by warp)
+      int rx = S.x0, rj = 0, rm0 = 0, rn0 = 0;
+      bool rstore = false;
+      auto retire_item = [&]() {
+        if (rx >= S.end) return;
+        const GemmItem w = gemm_item(P, S, cl, rx, nslots);
+        tile_of(w.unit, rm0, rn0);
+        rstore = inplace && !P.wstore && (w.piece < 0 || w.fin) && rx + S.step < S.end;
+      };
+      // wait until chunk h's buffer is released by its four epilogue warps,
+      // store the results they left in it, and move on to the next chunk
+      auto retire = [&](int h) -> bool {
+        const int e = h % NE;
+        if (!gemm_wait(eempty0 + 8 * e, (h / NE) & 1, limit, &abort_flag)) return false;
+        if (rstore && rn0 + rj * kGemmChunk < P.N && rm0 < P.M) {
+          tma_store_2d_hint(&P.maps[kMaxStaged + 1], rn0 + rj * kGemmChunk, rm0,
+                            smem_u32(ebuf + e * P.epi_stage_bytes + P.inplace_off), l2_evict_first());
+          bulk_commit();
+        }
+        if (++rj == kGemmChunks) {
+          rj = 0;
+          rx += S.step;
+          retire_item();
+        }
+        return true;
+      };
+      retire_item();
       int g = 0;
       bool ok = true;
       for (int x = S.x0; x < S.end && ok; x += S.step) {
@@ -494,19 +529,26 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         tile_of(gemm_item(P, S, cl, x, nslots).unit, m0, n0);
         for (int j = 0; j < kGemmChunks; ++j, ++g) {
           const int e = g % NE;
-          if (g >= NE && !gemm_wait(eempty0 + 8 * e, ((g / NE) & 1) ^ 1, limit, &abort_flag)) {
-            ok = false;
-            break;
+          if (g >= NE) {
+            if (!retire(g - NE)) {
+              ok = false;
+              break;
+            }
+            bulk_wait_read<0>();   // a store from this buffer has read it
           }
           mbar_expect_tx(efull0 + 8 * e, P.epi_tx_bytes);
           Epi::issue(P, smem_u32(ebuf + e * P.epi_stage_bytes), efull0 + 8 * e, m0, n0 + j * kGemmChunk);
         }
       }
+      // the last chunks' results (only in place: otherwise nothing waits for
+      // these releases)
+      for (int h = g - NE < 0 ? 0 : g - NE; ok && inplace && !P.wstore && h < g; ++h) ok = retire(h);
       if (!ok) {
         abort_flag = 1;
         set_error(P.err, DEVERR_TIMEOUT);
         for (int k = g - NE < 0 ? 0 : g - NE; k < g; ++k) mbar_wait(efull0 + 8 * (k % NE), (k / NE) & 1, drain);
       }
+      bulk_wait<0>();   // the stores issued here have completed
     }
   } else {
     // ---- epilogue ----
@@ -514,8 +556,6 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
     const int set = warp >= 8 ? 1 : 0;   // chunks j with j % 2 == set
     const int ew = set * 4 + q;          // epilogue warp index
     const int rr = q * 32 + lane;        // accumulator row of this thread
-    const bool inplace = P.inplace_off >= 0;
-    int prev_e = -1;                     // buffer whose release waits for its store (lane 0)
 
     int g = 0, i = 0;
     bool dead = false;
@@ -571,11 +611,6 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       // result chunks, so that no chunk waits for a store buffer.
       const bool last = x + S.step >= S.end;
       uint8_t* wring = opnd + q * (TN * 128);
-      if (last && inplace && lane == 0 && prev_e >= 0) {
-        bulk_wait_read<0>();
-        mbar_arrive(eempty0 + 8 * prev_e);
-        prev_e = -1;
-      }
       const float4* oq = nullptr;   // the other piece's partial (finishing a piece)
       bool part_smem = false;
       float4 nxt[8];
@@ -611,14 +646,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         }
         if (!finish) {
           // another piece finishes this row block: only release the leaves
-          if (lane == 0 && staged) {
-            if (inpl) {
-              bulk_wait_read<0>();
-              if (prev_e >= 0) mbar_arrive(eempty0 + 8 * prev_e);
-              prev_e = -1;
-            }
-            mbar_arrive(eempty0 + 8 * e);
-          }
+          if (lane == 0 && staged) mbar_arrive(eempty0 + 8 * e);
           __syncwarp();
           continue;
         }
@@ -656,12 +684,12 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) o[s8 * 8 + k] = o8[k];
         }
-        // this warp's 32 rows x 32 columns go out through its own TMA store:
-        // no barrier across the epilogue warps
         // the result goes to this warp's rows of the IDENT leaf's chunk (read
-        // above, no longer needed), to a separate double buffer, or in the
-        // last item to the chunk's 4 KB of the ring (whose partial has been
-        // read: all lanes read before any writes, below)
+        // above, no longer needed), to a separate buffer or, in the last
+        // item, to the chunk's 4 KB of the ring (whose partial has been read:
+        // all lanes read before any writes, below); it leaves through this
+        // warp's own TMA store of its 32 rows x 32 columns, or (in place,
+        // long K) through warp 2's store of the whole chunk
         uint8_t* ob = last   ? wring + j * 4096
                       : inpl ? ebuf + e * P.epi_stage_bytes + P.inplace_off + q * (32 * 128)
                              : obuf + (j & 1) * kGemmOutBytes + q * (32 * 128);
@@ -674,21 +702,17 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          if (staged && !inpl) mbar_arrive(eempty0 + 8 * e);
-          if (n0 + j * kGemmChunk < P.N && m0 + q * 32 < P.M) {
-            tma_store_2d_hint(&P.maps[kMaxStaged], n0 + j * kGemmChunk, m0 + q * 32, smem_u32(ob), l2_evict_first());
+          if (staged && !inpl) mbar_arrive(eempty0 + 8 * e);   // the leaf chunk has been read
+          if (!inpl || P.wstore) {
+            if (n0 + j * kGemmChunk < P.N && m0 + q * 32 < P.M) {
+              tma_store_2d_hint(&P.maps[kMaxStaged], n0 + j * kGemmChunk, m0 + q * 32, smem_u32(ob), l2_evict_first());
+            }
+            bulk_commit();
           }
-          bulk_commit();
-          if (inpl && NE > 2) {
-            // this warp's previous chunk's buffer is free once its store has
-            // read it
-            bulk_wait_read<1>();
-            if (prev_e >= 0) mbar_arrive(eempty0 + 8 * prev_e);
-            prev_e = e;
-          } else if (inpl) {
-            // with two leaf buffers each set's chunks reuse one buffer: free
-            // it now (a deferred release would wait for itself)
-            bulk_wait_read<0>();
+          if (inpl) {
+            // the buffer is reloaded once released: after this warp's copy
+            // has read its rows, or (warp 2 storing the chunk) at once
+            if (P.wstore) bulk_wait_read<0>();
             mbar_arrive(eempty0 + 8 * e);
           }
         }

@@ -257,3 +257,35 @@ def test_pairs_stream_k(K, M, N, cap, kb):
         got = env[spec.outputs[0]].cpu().numpy()
         assert rel_err(got, ref) <= TOL_F32
         assert rel_err(w - got, w - ref) <= TOL_BF16
+
+
+ST_PRODUCER, ST_WARPS = 1 << 24, 2 << 24   # in-place results stored by the leaf producer / by the epilogue warps
+
+
+@pytest.mark.parametrize("store", [ST_PRODUCER, ST_WARPS])
+@pytest.mark.parametrize("K,M,N,extra", [
+    (512, 4096, 4096, 0),                                # the HBM-bound update, default launch (six leaf buffers)
+    (4096, 1024, 1024, 0),                               # long K: two leaf buffers
+    (1024, 1024, 1024, (5 << 8) | PAIRS | KB2),          # last round split along K
+    (1024, 520, 1160, (3 << 8) | PAIRS | KB1),           # ragged rows and columns, split tail
+    (1024, 1024, 768, (7 << 8) | PAIRS | TN128 | KB1),   # 128-column pair tiles
+    (4096, 512, 768, (4 << 8) | PAIRS | SK | KB2),       # stream-K shares, two leaf buffers
+    (512, 776, 1000, (2 << 8) | CLUSTER4 | KB2),         # 4-CTA clusters, ragged
+])
+def test_inplace_store_modes(store, K, M, N, extra):
+    """Results written in place of the IDENT leaf's chunk leave either in one
+    copy per 128 x 32 chunk from the leaf producer before it reloads the
+    buffer, or in each epilogue warp's copy of its rows, the warp freeing the
+    buffer once the copy has read them; every schedule and tile shape, run
+    twice (split flags are cleared by readers)."""
+    spec = W.sf_update(K, M, N)
+    g, plan, inputs, dev = prepare(spec, flags=extra | store)
+    assert plan.n_groups == 1 and plan.groups[0].kind == "gemm"
+    ref = OE.run_unfused(spec, inputs)[spec.outputs[0]]
+    w = inputs[2]
+    for _ in range(2):
+        env = run_fused(plan, spec, dev)
+        plan.sync()
+        got = env[spec.outputs[0]].cpu().numpy()
+        assert rel_err(got, ref) <= TOL_F32
+        assert rel_err(w - got, w - ref) <= TOL_BF16
