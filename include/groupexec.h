@@ -114,7 +114,11 @@ typedef struct tf_layout tf_layout;
  * the columns of a CTA pair's tile (0 or 1 = 256, 2 = 128); bits 24-25 = how an
  * elementwise group writes its output: 0 default (= 2), 1 the CTA's tile
  * staged in shared memory and stored by one TMA store, 2 each warp's slice
- * stored by its own TMA store, 3 direct 16-byte stores from registers;
+ * stored by its own TMA store, 3 direct 16-byte stores from registers; and
+ * for GEMM-epilogue groups whose result is written in place of a leaf's
+ * staged chunk, how it leaves (0 = chosen by K, 1 = the leaf producer's copy
+ * of each 128 x 32 chunk before it reloads the buffer, 2 = each epilogue
+ * warp's copy of its 32 rows; 3 = as 1);
  * bit 26 runs the groups' operator programs on the register-stack
  * interpreter instead of compiling each program to straight-line code when
  * the plan is built (default; needs NVRTC, loaded at run time); bit 27 is a
