@@ -550,10 +550,11 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
   static const std::vector<std::pair<int, int>> prefs_long = {{3, 2}, {2, 4}, {2, 3}, {2, 2}};
   const bool short_k = p.nkb <= 16 && estage > 0;
   // results written in place leave through the epilogue warps' own stores
-  // (short K: the leaf buffers turn over fastest when each warp frees its
-  // rows as soon as its copy has read them) or through the leaf producer,
-  // one copy per chunk before it reloads the buffer (long K: no epilogue
-  // warp waits for a copy); flag bits 24-25: 1 = producer, 2 = warps, 0 =
+  // (short K: the leaf stream is the whole load, and one producer thread
+  // issuing a copy and waiting for its read per chunk falls behind) or
+  // through the leaf producer, one copy per chunk before it reloads the
+  // buffer (long K: no epilogue warp waits for a copy, which shortens the
+  // exposed last epilogue); flag bits 24-25: 1 = producer, 2 = warps, 0 =
   // chosen
   {
     const int stf = (o.flags >> 24) & 3;

@@ -188,8 +188,9 @@ struct GemmParams {
   int32_t epi_stage_bytes, epi_tx_bytes, n_epi_bufs;
   int32_t inplace_off;                 // >= 0: the result overwrites this IDENT leaf's chunk (no out buffers)
   int32_t wstore;                      // in place: 1 = each epilogue warp stores its rows of the chunk and
-                                       // frees the buffer once the copy has read them; 0 = the leaf producer
-                                       // stores the whole chunk before reloading the buffer
+                                       // frees the buffer once the copy has read them (checked at its next
+                                       // store); 0 = the leaf producer stores the whole chunk before
+                                       // reloading the buffer
   int32_t inject;                      // failure injection: 1 = the producers issue no loads
   // work units: a cluster's tiles (the pair's 256 x 256 tile, or the two
   // pairs' 256 x 512) in row-major order

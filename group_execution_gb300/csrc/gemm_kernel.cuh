@@ -496,13 +496,14 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       // column chunk rj; its results leave from the buffer (in place) when
       // this CTA finishes the unit and it is not the CTA's last item (whose
       // results go out from the operand ring, warp by warp)
+      const bool pstore = inplace && !P.wstore;   // this thread stores in-place results
       int rx = S.x0, rj = 0, rm0 = 0, rn0 = 0;
       bool rstore = false;
       auto retire_item = [&]() {
         if (rx >= S.end) return;
         const GemmItem w = gemm_item(P, S, cl, rx, nslots);
         tile_of(w.unit, rm0, rn0);
-        rstore = inplace && !P.wstore && (w.piece < 0 || w.fin) && rx + S.step < S.end;
+        rstore = (w.piece < 0 || w.fin) && rx + S.step < S.end;
       };
       // wait until chunk h's buffer is released by its four epilogue warps,
       // store the results they left in it, and move on to the next chunk
@@ -521,7 +522,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         }
         return true;
       };
-      retire_item();
+      if (pstore) retire_item();
       int g = 0;
       bool ok = true;
       for (int x = S.x0; x < S.end && ok; x += S.step) {
@@ -530,11 +531,12 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         for (int j = 0; j < kGemmChunks; ++j, ++g) {
           const int e = g % NE;
           if (g >= NE) {
-            if (!retire(g - NE)) {
+            if (pstore ? !retire(g - NE)
+                       : !gemm_wait(eempty0 + 8 * e, ((g / NE) & 1) ^ 1, limit, &abort_flag)) {
               ok = false;
               break;
             }
-            bulk_wait_read<0>();   // a store from this buffer has read it
+            if (pstore) bulk_wait_read<0>();   // a store from this buffer has read it
           }
           mbar_expect_tx(efull0 + 8 * e, P.epi_tx_bytes);
           Epi::issue(P, smem_u32(ebuf + e * P.epi_stage_bytes), efull0 + 8 * e, m0, n0 + j * kGemmChunk);
@@ -542,7 +544,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       }
       // the last chunks' results (only in place: otherwise nothing waits for
       // these releases)
-      for (int h = g - NE < 0 ? 0 : g - NE; ok && inplace && !P.wstore && h < g; ++h) ok = retire(h);
+      for (int h = g - NE < 0 ? 0 : g - NE; ok && pstore && h < g; ++h) ok = retire(h);
       if (!ok) {
         abort_flag = 1;
         set_error(P.err, DEVERR_TIMEOUT);
@@ -556,6 +558,10 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
     const int set = warp >= 8 ? 1 : 0;   // chunks j with j % 2 == set
     const int ew = set * 4 + q;          // epilogue warp index
     const int rr = q * 32 + lane;        // accumulator row of this thread
+    // in place with per-warp stores: a chunk's buffer is released once this
+    // warp's copy has read it, checked at the warp's next store
+    const bool wdefer = inplace && P.wstore;
+    int prev_e = -1;                     // buffer whose release waits for its store (lane 0)
 
     int g = 0, i = 0;
     bool dead = false;
@@ -611,6 +617,11 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       // result chunks, so that no chunk waits for a store buffer.
       const bool last = x + S.step >= S.end;
       uint8_t* wring = opnd + q * (TN * 128);
+      if (last && wdefer && lane == 0 && prev_e >= 0) {
+        bulk_wait_read<0>();
+        mbar_arrive(eempty0 + 8 * prev_e);
+        prev_e = -1;
+      }
       const float4* oq = nullptr;   // the other piece's partial (finishing a piece)
       bool part_smem = false;
       float4 nxt[8];
@@ -646,7 +657,14 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         }
         if (!finish) {
           // another piece finishes this row block: only release the leaves
-          if (lane == 0 && staged) mbar_arrive(eempty0 + 8 * e);
+          if (lane == 0 && staged) {
+            if (inpl && wdefer && prev_e >= 0) {
+              bulk_wait_read<0>();
+              mbar_arrive(eempty0 + 8 * prev_e);
+              prev_e = -1;
+            }
+            mbar_arrive(eempty0 + 8 * e);
+          }
           __syncwarp();
           continue;
         }
@@ -709,10 +727,18 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
             }
             bulk_commit();
           }
-          if (inpl) {
-            // the buffer is reloaded once released: after this warp's copy
-            // has read its rows, or (warp 2 storing the chunk) at once
-            if (P.wstore) bulk_wait_read<0>();
+          if (inpl && !wdefer) {
+            mbar_arrive(eempty0 + 8 * e);   // warp 2 stores the chunk before reloading the buffer
+          } else if (inpl && NE > 2) {
+            // this warp's previous chunk's buffer is free once its copy has
+            // read it (a wait here would stall the warp for every copy)
+            bulk_wait_read<1>();
+            if (prev_e >= 0) mbar_arrive(eempty0 + 8 * prev_e);
+            prev_e = e;
+          } else if (inpl) {
+            // with two leaf buffers each set's chunks reuse one buffer: free
+            // it now (a deferred release would wait for itself)
+            bulk_wait_read<0>();
             mbar_arrive(eempty0 + 8 * e);
           }
         }
