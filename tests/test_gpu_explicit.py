@@ -138,6 +138,27 @@ def _mlp_spec(M, K, N):
     return g
 
 
+def test_pattern_mlp_full_size():
+    """The MLP layer the benchmark times, relu(X W + b) with X, W [4096, 4096]
+    bf16: the matmul + bias + relu pattern makes it one GEMM-epilogue group,
+    launched as the benchmark launches it, the whole output against the
+    oracle."""
+    spec = W.GraphSpec()
+    x = spec.input((4096, 4096), "bf16")
+    w = spec.input((4096, 4096), "bf16")
+    b = spec.input((4096,))
+    y = spec.op("relu", (spec.op("badd_col", (spec.op("matmul_bf16", (x, w), (0, 0)), b)),))
+    spec.mark_output(y)
+    plan = graph_from_spec(spec).partition(patterns=[("matmul_bias_relu", ["matmul_bf16", "badd_col", "relu"], True)]).build()
+    assert plan.n_groups == 1 and plan.groups[0].kind == "gemm"
+    ins = W.make_inputs(spec, 0)
+    dev = {vid: to_dev(spec, vid, a) for vid, a in ins.items()}
+    env = run_fused(plan, spec, dev)
+    plan.sync()
+    ref = OE.run_unfused(spec, ins)[y]
+    assert rel_err(env[y].cpu().numpy(), ref) <= 1e-4
+
+
 @pytest.mark.parametrize("shape", [(256, 128, 512), (200, 72, 264)])
 def test_pattern_plan_matmul_bias_relu(shape):
     """FuseOpsByPattern with the page's matmul + bias pattern extended by relu:

@@ -149,6 +149,23 @@ def test_random_dag_small(seed):
     _check(spec, seed=seed)
 
 
+def test_random_dag_full_size():
+    """The random DAG at its full size (seed 0: 200 operators over [8192, 4096]
+    and [4096, 8192] values), partitioned and launched as the benchmark runs
+    it: every graph output against the oracle (about a minute of host time)."""
+    spec = W.random_dag(0)
+    g, plan, inputs, dev = prepare(spec, 0)
+    for info in plan.groups:
+        assert info.status == 0, info
+    ref = OE.run_unfused(spec, inputs)
+    env = run_fused(plan, spec, dev)
+    plan.sync()
+    assert len(spec.outputs) > 10
+    for vid in spec.outputs:
+        e = rel_err(env[vid].cpu().numpy(), ref[vid])
+        assert e <= TOL_F32, (vid, spec.values[vid].op, e)
+
+
 def test_launch_rejects_bad_pointers():
     from group_execution_gb300 import FgError
     spec = W.diamond(64, 32)
