@@ -35,7 +35,8 @@ out from the passages they cite:
 
 Parity status: every function here is pinned by tests under ``tests/``
 (``-m "not gpu"``) against brute force, closed forms, worked examples from the
-pages or library routines, except the long random-DAG numerics, which only the
-oracle itself defines ("parity unpinned" beyond per-op pins).
+pages or library routines.  The composition of operators in ``execute`` is
+pinned against an independent element-by-element evaluator on small random
+DAGs; the full-size chains rely on that composition and the per-operator pins.
 """
 from . import kinds, postdom, partition, execute, pack, buckets, explicit, patterns, simulate  # noqa: F401

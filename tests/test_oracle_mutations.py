@@ -12,6 +12,7 @@ from tests import test_oracle_partition as TP
 from tests import test_oracle_postdom as TD
 from tests import test_oracle_pack as TK
 from tests import test_oracle_execute as TE
+from tests import test_oracle_composition as TC
 
 
 def _fails(fn):
@@ -149,3 +150,26 @@ def test_mutation_allreduce_ignores_the_channel(monkeypatch):
         return tot, fin, st, fi
     monkeypatch.setattr(S, "simulate", bad)
     _fails(TS.test_channel_is_used_in_production_order)
+
+
+def _patch_op(monkeypatch, op_name, fn):
+    orig = E.apply_op
+    monkeypatch.setattr(E, "apply_op", lambda op, args, attrs: fn(orig, args, attrs) if op == op_name
+                        else orig(op, args, attrs))
+
+
+def test_mutation_reshape_column_major(monkeypatch):
+    _patch_op(monkeypatch, "reshape", lambda orig, args, attrs: np.ascontiguousarray(
+        np.asarray(args[0]).reshape(int(attrs[0]), int(attrs[1]), order="F")))
+    _fails(TC.test_every_operator_composed)
+
+
+def test_mutation_transpose_as_reshape(monkeypatch):
+    _patch_op(monkeypatch, "transpose", lambda orig, args, attrs: np.ascontiguousarray(
+        np.asarray(args[0]).reshape(args[0].shape[::-1])))
+    _fails(lambda: TC.test_random_dag_composition(0))
+
+
+def test_mutation_operands_reversed(monkeypatch):
+    _patch_op(monkeypatch, "sub", lambda orig, args, attrs: orig("sub", list(reversed(args)), attrs))
+    _fails(TC.test_every_operator_composed)
