@@ -170,6 +170,7 @@ constexpr int kGemmCluster4 = 4;       // two pairs on adjacent 256-column tiles
 
 struct GemmParams {
   CUtensorMap mapA, mapB;              // bf16 operands (boxes per major-ness)
+  CUtensorMap mapB2;                   // B in half-width boxes (units cut into column halves)
   CUtensorMap maps[kMaxStaged + 2];    // epilogue leaves, [kMaxStaged] = output in 32 x 32 boxes,
                                        // [kMaxStaged + 1] = output in 128 x 32 boxes
   VmInstr prog[kMaxProg];              // epilogue program (interpreted variant)
@@ -200,6 +201,9 @@ struct GemmParams {
   // [split_at, nslots); the first publishes its partial accumulator in the
   // workspace, the second adds it and runs the epilogue
   int32_t nfull, split, split_at;
+  // nsplit_n = 1: the split units are cut into their two column halves
+  // instead (each over all of K, on a pair of its own: no partial sums)
+  int32_t nsplit_n;
   // sk = 1: each cluster runs a contiguous 1/ncl share of all units' ring
   // slots instead (at least one whole unit, so a unit is cut at most once,
   // into the two pieces on either side of a share boundary)

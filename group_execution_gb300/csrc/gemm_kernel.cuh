@@ -34,10 +34,12 @@
 //              tcgen05.ld, evaluates the epilogue program eight values at a
 //              time and stages the result for a TMA store (its own, or, for
 //              results written in place with long K, warp 2's).
-// The epilogue of tile i overlaps the MMAs of tile i+1.  A tile cut along K
+// The epilogue of tile i overlaps the MMAs of tile i+1.  The last round's
+// tiles are cut into column halves (a half-width MMA and B box, over all of
+// K, on pairs the round would leave idle), or cut along K: a tile cut along K
 // (the last round's, or at a share boundary) meets its two partial
-// accumulators in a workspace; the CTA's last item uses the idle operand ring
-// for its stores.  Every wait is bounded; on expiry the CTA records the
+// accumulators in a workspace.  The CTA's last item uses the idle operand
+// ring for its stores.  Every wait is bounded; on expiry the CTA records the
 // error, drains its copies, frees its TMEM and returns.
 #pragma once
 #include "fg_device.cuh"
@@ -166,7 +168,8 @@ __device__ __forceinline__ bool gemm_wait(uint32_t bar, uint32_t parity, int64_t
 }
 
 // A cluster's work list: item indices [x0, end) in steps of `step`.  Round
-// robin: items are whole units, then the pieces of the split last round.
+// robin: items are whole units, then the pieces of the split last round (two
+// K pieces, or the two column halves, of each of its units).
 // Stream-K (P.sk): the cluster owns ring slots [b0, b1) of the sequence of
 // all units' slots, and its items are the units that range touches.
 struct GemmSched {
@@ -191,18 +194,20 @@ __device__ __forceinline__ GemmSched gemm_sched(const GemmParams& P, int cl, int
   return S;
 }
 
-// One item: a whole unit, or one K piece (ring slots [sl0, sl1)) of a unit
-// cut in two.  q indexes the piece's workspace (q ^ 1 is the other piece of
-// the same unit) and key its ready flags.  The piece that runs later
-// finishes the unit (fin): the other publishes its partial accumulator.
+// One item: a whole unit, one K piece (ring slots [sl0, sl1)) of a unit cut
+// in two, or one column half of a unit (half = 0 or 1, all of K).  q indexes
+// a K piece's workspace (q ^ 1 is the other piece of the same unit) and key
+// its ready flags.  The piece that runs later finishes the unit (fin): the
+// other publishes its partial accumulator.
 struct GemmItem {
-  int unit, piece, sl0, sl1, q, key;   // piece = -1 for a whole unit
+  int unit, piece, sl0, sl1, q, key;   // piece = -1 for a whole unit or a column half
+  int half;                            // -1, or the column half of the unit
   bool fin;
 };
 __device__ __forceinline__ GemmItem gemm_item(const GemmParams& P, const GemmSched& S, int cl, int idx,
                                               int nslots) {
   GemmItem w;
-  w.piece = w.q = w.key = -1;
+  w.piece = w.q = w.key = w.half = -1;
   w.fin = true;
   if (P.sk) {
     w.unit = idx;
@@ -219,6 +224,12 @@ __device__ __forceinline__ GemmItem gemm_item(const GemmParams& P, const GemmSch
     }
   } else if (idx < P.nfull) {
     w.unit = idx;
+    w.sl0 = 0;
+    w.sl1 = nslots;
+  } else if (P.nsplit_n) {
+    const int q = idx - P.nfull;
+    w.unit = P.nfull + q / 2;
+    w.half = q & 1;
     w.sl0 = 0;
     w.sl1 = nslots;
   } else {
@@ -276,6 +287,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   constexpr int kGemmChunks = TN / kGemmChunk;                     // epilogue chunks per tile
   constexpr int kHalfA = KB * kGemmABytes;                         // 128 rows x KB K blocks
   constexpr int kStageBytes = kHalfA + KB * kBCols * kGemmK * 2;   // 32 (24) KB per K block and CTA
+  constexpr int kStageBytesH = kHalfA + KB * (kBCols / 2) * kGemmK * 2;   // a column half's slot
   extern __shared__ uint8_t smem_raw[];
   __shared__ int abort_flag;
   __shared__ int issued[2];            // operand slots issued by the A and B producers
@@ -314,6 +326,13 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
     m0 = ((u / nsn) * 2 + h) * kGemmM;
     n0 = ((u % nsn) * PR + pr) * TN;
   };
+  // an item's output block: its unit's tile, or the tile's column half; and
+  // its 32-column epilogue chunks
+  auto item_tile = [&](const GemmItem& w, int& m0, int& n0) {
+    tile_of(w.unit, m0, n0);
+    if (w.half > 0) n0 += TN / 2;
+  };
+  auto item_chunks = [&](const GemmItem& w) { return w.half >= 0 ? kGemmChunks / 2 : kGemmChunks; };
   if (threadIdx.x == 0) {
     abort_flag = 0;
     issued[0] = issued[1] = 0;
@@ -353,6 +372,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
     const bool isA = warp == 0;
     if (lane == 0 && !P.inject) {
       tma_prefetch(isA ? &P.mapA : &P.mapB);
+      if (!isA && P.nsplit_n) tma_prefetch(&P.mapB2);
       const uint64_t keep = l2_evict_last();   // every operand tile is read by several tiles
       // both CTAs' halves are counted on the even CTA's barrier, which the
       // even CTA alone arms with the whole slot's bytes (blocks past K
@@ -364,8 +384,9 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       for (int x = S.x0; x < S.end && ok; x += S.step) {
         const GemmItem w = gemm_item(P, S, cl, x, nslots);
         int m0, n0;
-        tile_of(w.unit, m0, n0);
-        const int nb = n0 + h * kBCols;
+        item_tile(w, m0, n0);
+        const bool hb = w.half >= 0;   // a column half: each CTA stages kBCols / 2 columns of B
+        const int nb = n0 + h * (hb ? kBCols / 2 : kBCols);
         for (int sl = w.sl0; sl < w.sl1; ++sl) {
           if (it >= NS && !gemm_wait(empty0 + 8 * s, ph ^ 1, limit, &abort_flag)) {
             ok = false;
@@ -379,10 +400,16 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
             ph ^= 1;
           }
           if (!isA) {
+            if constexpr (TN == kGemmN) {
+              if (hb) {
+                gemm_load_half<KB, kBCols / 2>(b, &P.mapB2, P.b_mn, P.b_3d, nb, k0, cbar, keep);
+                continue;
+              }
+            }
             gemm_load_half<KB, kBCols>(b, &P.mapB, P.b_mn, P.b_3d, nb, k0, cbar, keep);
             continue;
           }
-          if (leader) mbar_expect_tx(fbar, 2 * kStageBytes);
+          if (leader) mbar_expect_tx(fbar, 2 * (hb ? kStageBytesH : kStageBytes));
           if constexpr (CL == 4) {
             // A rows h are shared by CTAs h and h + 2: pair pr fetches half of
             // them for both (2-D boxes): K block pr of two, or with one K
@@ -416,23 +443,26 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
     // ---- MMA issuer (the even CTA of a pair) ----
     if (lane == 0 && leader) {
       const uint32_t idesc = idesc_bf16_f32(2 * kGemmM, TN, P.a_mn, P.b_mn);
+      const uint32_t idesc_h = idesc_bf16_f32(2 * kGemmM, TN / 2, P.a_mn, P.b_mn);   // a column half
       // MN-major: atoms of 64 (M or N) x 8 K rows, 64-wide groups 16 KB
       // apart; K-major: atoms of 8 rows x 64 K, K blocks 16 KB apart
       const uint32_t a_lbo = P.a_mn ? KB * 8192 : 16, b_lbo = P.b_mn ? KB * 8192 : 16;
       const uint32_t a_blk = P.a_mn ? 8192 : 16384, b_blk = P.b_mn ? 8192 : kBCols * 128;   // next K block
+      const uint32_t b_blk_h = P.b_mn ? 8192 : kBCols / 2 * 128;
       const uint32_t a_step = P.a_mn ? 2048 : 32, b_step = P.b_mn ? 2048 : 32;         // next 16 of K
       // a descriptor's start-address field holds address >> 4 in 14 bits and
       // the ring lies below 2^18 bytes, so descriptors advance by adding
       // offset >> 4: built once here, not per MMA
       const uint32_t ring = smem_u32(opnd);
       const uint64_t ad0 = smem_desc_sw128(ring, a_lbo, 1024), bd0 = smem_desc_sw128(ring + kHalfA, b_lbo, 1024);
-      uint32_t aoff[KB * 4], boff[KB * 4];
+      uint32_t aoff[KB * 4], boff[KB * 4], boff_h[KB * 4];
 #pragma unroll
       for (int j = 0; j < KB; ++j)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           aoff[j * 4 + kk] = (j * a_blk + kk * a_step) >> 4;
           boff[j * 4 + kk] = (j * b_blk + kk * b_step) >> 4;
+          boff_h[j * 4 + kk] = (j * b_blk_h + kk * b_step) >> 4;
         }
       int s = 0, i = 0;
       uint32_t ph = 0;   // ring position and phase parity
@@ -455,6 +485,8 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         }
         tc_fence_after();
         const uint32_t d = tmem + b * TN;
+        const bool hb = w.half >= 0;
+        const uint32_t id = hb ? idesc_h : idesc;
         for (int sl = w.sl0; sl < w.sl1; ++sl) {
           if (!gemm_wait(full0 + 8 * s, ph, limit, &abort_flag)) {
             ok = false;
@@ -468,7 +500,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
             if (j >= nk) break;
 #pragma unroll
             for (int kk = 0; kk < kGemmK / 16; ++kk)
-              tc_mma_bf16<2>(d, ad0 + so + aoff[j * 4 + kk], bd0 + so + boff[j * 4 + kk], idesc,
+              tc_mma_bf16<2>(d, ad0 + so + aoff[j * 4 + kk], bd0 + so + (hb ? boff_h : boff)[j * 4 + kk], id,
                              sl != w.sl0 || j != 0 || kk != 0);
           }
           tc_commit_mask(empty0 + 8 * s, slot_mask);   // every producer writing the slot may refill it
@@ -497,12 +529,13 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       // this CTA finishes the unit and it is not the CTA's last item (whose
       // results go out from the operand ring, warp by warp)
       const bool pstore = inplace && !P.wstore;   // this thread stores in-place results
-      int rx = S.x0, rj = 0, rm0 = 0, rn0 = 0;
+      int rx = S.x0, rj = 0, rm0 = 0, rn0 = 0, rnch = kGemmChunks;
       bool rstore = false;
       auto retire_item = [&]() {
         if (rx >= S.end) return;
         const GemmItem w = gemm_item(P, S, cl, rx, nslots);
-        tile_of(w.unit, rm0, rn0);
+        item_tile(w, rm0, rn0);
+        rnch = item_chunks(w);
         rstore = (w.piece < 0 || w.fin) && rx + S.step < S.end;
       };
       // wait until chunk h's buffer is released by its four epilogue warps,
@@ -515,7 +548,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
                             smem_u32(ebuf + e * P.epi_stage_bytes + P.inplace_off), l2_evict_first());
           bulk_commit();
         }
-        if (++rj == kGemmChunks) {
+        if (++rj == rnch) {
           rj = 0;
           rx += S.step;
           retire_item();
@@ -526,9 +559,11 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       int g = 0;
       bool ok = true;
       for (int x = S.x0; x < S.end && ok; x += S.step) {
+        const GemmItem wi = gemm_item(P, S, cl, x, nslots);
         int m0, n0;
-        tile_of(gemm_item(P, S, cl, x, nslots).unit, m0, n0);
-        for (int j = 0; j < kGemmChunks; ++j, ++g) {
+        item_tile(wi, m0, n0);
+        const int nch = item_chunks(wi);
+        for (int j = 0; j < nch; ++j, ++g) {
           const int e = g % NE;
           if (g >= NE) {
             if (pstore ? !retire(g - NE)
@@ -568,7 +603,8 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
     for (int x = S.x0; x < S.end; x += S.step, ++i) {
       const GemmItem w = gemm_item(P, S, cl, x, nslots);
       int m0, n0;
-      tile_of(w.unit, m0, n0);
+      item_tile(w, m0, n0);
+      const int nch = item_chunks(w);
       const int b = i & 1;
       bool got = gemm_wait(tfull0 + 8 * b, (i >> 1) & 1, limit, &abort_flag);
       tc_fence_after();
@@ -645,7 +681,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         }
       }
       const bool inpl = inplace && !last;   // results in place in the leaf chunk
-      for (int j = 0; j < kGemmChunks; ++j, ++g) {
+      for (int j = 0; j < nch; ++j, ++g) {
         if ((j & 1) != set) continue;   // the other set's chunk
         const int e = g % NE;
         if (got && staged) got = gemm_wait(efull0 + 8 * e, (g / NE) & 1, limit, &abort_flag);

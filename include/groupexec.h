@@ -110,7 +110,9 @@ typedef struct tf_layout tf_layout;
  * chosen, 1 = CTA pairs, 2 = 4-CTA clusters whose two pairs share their A
  * rows), bits 18-19 the K blocks of 64 per operand ring slot (0 = chosen,
  * 1, 2), bits 20-21 the schedule (0 = chosen, 1 = round robin with the last
- * round split along K, 2 = equal shares of all tiles' K steps), bits 22-23
+ * round's tiles cut along K into two pieces, 2 = equal shares of all tiles'
+ * K steps, 3 = round robin with the last round's tiles cut into their two
+ * column halves, the choice for CTA pairs with 256-column tiles), bits 22-23
  * the columns of a CTA pair's tile (0 or 1 = 256, 2 = 128); bits 24-25 = how an
  * elementwise group writes its output: 0 default (= 2), 1 the CTA's tile
  * staged in shared memory and stored by one TMA store, 2 each warp's slice

@@ -16,6 +16,7 @@ MODES = [0, _lib.FG_FLAG_INTERPRET]
 PAIRS, CLUSTER4 = 1 << 16, 2 << 16     # GEMM cluster shape: CTA pairs only / two pairs sharing A
 KB1, KB2 = 1 << 18, 2 << 18            # K blocks per operand ring slot
 TN256, TN128 = 1 << 22, 2 << 22        # columns of a pair's tile
+KSPLIT = 1 << 20                       # schedule: round robin, the last round's units cut into K pieces
 SHAPES = [CLUSTER4 | KB2, CLUSTER4 | KB1, PAIRS | KB1, PAIRS | TN128, PAIRS | KB1 | TN128]
 
 
@@ -119,7 +120,7 @@ def test_split_tail(K, M, N, cap, kb):
     piece finishes the epilogue; run twice, so the arrival counters are seen
     to reset."""
     spec = W.sf_update(K, M, N)
-    g, plan, inputs, dev = prepare(spec, flags=(cap << 8) | PAIRS | kb)
+    g, plan, inputs, dev = prepare(spec, flags=(cap << 8) | PAIRS | KSPLIT | kb)
     ref = OE.run_unfused(spec, inputs)[spec.outputs[0]]
     w = inputs[2]
     for _ in range(2):
@@ -134,7 +135,7 @@ def test_split_tail(K, M, N, cap, kb):
 def test_split_tail_plain_layouts(ta, tb):
     K, M, N = 1024, 1024, 768
     spec = _matmul_graph(K, M, N, ta, tb)
-    g, plan, inputs, dev = prepare(spec, flags=(5 << 8) | PAIRS)
+    g, plan, inputs, dev = prepare(spec, flags=(5 << 8) | PAIRS | KSPLIT)
     env = run_fused(plan, spec, dev)
     plan.sync()
     A = inputs[0].T if ta else inputs[0]
@@ -144,6 +145,12 @@ def test_split_tail_plain_layouts(ta, tb):
 
 def test_split_tail_full_size():
     # 256 pair tiles on 76 pairs: the last 28 run as K halves
+    _sf_update(1024, 4096, 4096, KSPLIT)
+
+
+def test_column_half_tail_full_size():
+    # 256 pair tiles on 76 pairs: the last 28 run as 56 column halves (the
+    # default for CTA pairs)
     _sf_update(1024, 4096, 4096, 0)
 
 
@@ -213,8 +220,8 @@ def test_cluster_shapes_epilogues(epi, shape):
 
 
 def test_sf_update_k4096_full_size():
-    """The compute-bound SF update (B = K = 4096) in the default launch:
-    4-CTA clusters, stream-K shares."""
+    """The compute-bound SF update (B = K = 4096) in the default launch: CTA
+    pairs, the last round's units cut into column halves."""
     _sf_update(4096, 4096, 4096, 0)
 
 
@@ -266,8 +273,9 @@ ST_PRODUCER, ST_WARPS = 1 << 24, 2 << 24   # in-place results stored by the leaf
 @pytest.mark.parametrize("K,M,N,extra", [
     (512, 4096, 4096, 0),                                # the HBM-bound update, default launch (six leaf buffers)
     (4096, 1024, 1024, 0),                               # long K: two leaf buffers
-    (1024, 1024, 1024, (5 << 8) | PAIRS | KB2),          # last round split along K
-    (1024, 520, 1160, (3 << 8) | PAIRS | KB1),           # ragged rows and columns, split tail
+    (1024, 1024, 1024, (5 << 8) | PAIRS | KSPLIT | KB2), # last round split along K
+    (1024, 1024, 1024, (5 << 8) | PAIRS | KB2),          # last round cut into column halves
+    (1024, 520, 1160, (3 << 8) | PAIRS | KSPLIT | KB1),  # ragged rows and columns, split tail
     (1024, 1024, 768, (7 << 8) | PAIRS | TN128 | KB1),   # 128-column pair tiles
     (4096, 512, 768, (4 << 8) | PAIRS | SK | KB2),       # stream-K shares, two leaf buffers
     (512, 776, 1000, (2 << 8) | CLUSTER4 | KB2),         # 4-CTA clusters, ragged
@@ -289,3 +297,46 @@ def test_inplace_store_modes(store, K, M, N, extra):
         got = env[spec.outputs[0]].cpu().numpy()
         assert rel_err(got, ref) <= TOL_F32
         assert rel_err(w - got, w - ref) <= TOL_BF16
+
+
+NSPLIT = 3 << 20   # schedule: round robin, the last round's units cut into their column halves
+
+
+@pytest.mark.parametrize("K,M,N,cap", [
+    (512, 1024, 1024, 5),    # one unit cut
+    (1024, 1024, 1024, 7),   # two units cut
+    (1024, 1024, 1160, 9),   # the second half partly past N
+    (1024, 1024, 1088, 9),   # the second half wholly past N
+    (256, 520, 1160, 3),     # ragged rows and columns
+    (4096, 1024, 1024, 5),   # long K
+])
+@pytest.mark.parametrize("kb", [KB2, KB1])
+def test_column_half_tail(K, M, N, cap, kb):
+    """The last round's units cut into their two 128-column halves, each over
+    all of K on a pair of its own (half-width B boxes and MMAs, four epilogue
+    chunks, no partial sums); run twice."""
+    spec = W.sf_update(K, M, N)
+    g, plan, inputs, dev = prepare(spec, flags=(cap << 8) | PAIRS | NSPLIT | kb)
+    ref = OE.run_unfused(spec, inputs)[spec.outputs[0]]
+    w = inputs[2]
+    for _ in range(2):
+        env = run_fused(plan, spec, dev)
+        plan.sync()
+        got = env[spec.outputs[0]].cpu().numpy()
+        assert rel_err(got, ref) <= TOL_F32
+        assert rel_err(w - got, w - ref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("ta,tb", [(1, 0), (0, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("mode", MODES)
+def test_column_half_tail_layouts(ta, tb, mode):
+    """Column-half tail units in every operand layout (K-major B takes the
+    half-width K-block stride), compiled and interpreted epilogues."""
+    K, M, N = 512, 1024, 768
+    spec = _matmul_graph(K, M, N, ta, tb)
+    g, plan, inputs, dev = prepare(spec, flags=(5 << 8) | PAIRS | NSPLIT | mode)
+    env = run_fused(plan, spec, dev)
+    plan.sync()
+    A = inputs[0].T if ta else inputs[0]
+    B = inputs[1].T if tb else inputs[1]
+    _check_matmul_bound(env[spec.outputs[0]].cpu().numpy(), A, B)
