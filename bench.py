@@ -688,13 +688,43 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
     bu, _ = timed(each_bucket(tf.unpack_range, 1.0), flush=False, inner=10)
     gp, _ = timed(graphed(each_bucket(tf.pack_range, 0.125)), flush=False, inner=10)
     gu, _ = timed(graphed(each_bucket(tf.unpack_range, 1.0)), flush=False, inner=10)
+    # all buckets packed in one launch, each marked ready as soon as its bytes
+    # are written: a second stream waits for each bucket in turn and records
+    # an event, timed from an event just before the launch (median of 10).
+    # An L2 flush runs first on the launching stream, so that every wait is
+    # enqueued before the pack starts (the host's enqueueing is not timed)
+    tf.set_buckets(bounds)
+    ob, _ = timed(lambda: tf.pack_buckets(0.125, buf), flush=False, inner=10)
+    s2 = torch.cuda.Stream()
+    ready = [[] for _ in range(nb)]
+    for _ in range(10):
+        torch.cuda.synchronize()
+        l2.fill_(1)
+        l2r.max()
+        st = torch.cuda.Event(enable_timing=True)
+        st.record()
+        tf.pack_buckets(0.125, buf)
+        evs = []
+        for k in range(nb):
+            tf.bucket_wait(k, s2)
+            ev = torch.cuda.Event(enable_timing=True)
+            ev.record(s2)
+            evs.append(ev)
+        torch.cuda.synchronize()
+        for k in range(nb):
+            ready[k].append(st.elapsed_time(evs[k]) * 1e3)
     rows["tensor_fusion_buckets_8MiB"] = {
         "buckets": nb, "launches_each": nb, "pack_us": bp * 1e3, "unpack_us": bu * 1e3,
         "graph_pack_us": gp * 1e3, "graph_pack_GBps": nbytes / (gp * 1e-3) / 1e9,
         "graph_pack_frac": nbytes / (gp * 1e-3) / 1e9 / hbm, "graph_unpack_us": gu * 1e3,
         "graph_unpack_GBps": nbytes / (gu * 1e-3) / 1e9, "graph_unpack_frac": nbytes / (gu * 1e-3) / 1e9 / hbm,
+        "one_launch_pack_us": ob * 1e3, "one_launch_pack_GBps": nbytes / (ob * 1e-3) / 1e9,
+        "one_launch_pack_frac": nbytes / (ob * 1e-3) / 1e9 / hbm,
+        "bucket_ready_us": [statistics.median(r) for r in ready],
         "bucket_bytes": [e - s for s, e in tf.bucket_ranges(bounds)],
-        "note": "pack_us/unpack_us: one host launch per bucket; graph_*: the launches replayed from a CUDA graph"}
+        "note": "pack_us/unpack_us: one host launch per bucket; graph_*: the launches replayed from a CUDA graph; "
+                "one_launch_pack: every bucket in one launch, bucket_ready_us: when a stream waiting on each "
+                "bucket's ready word passes it, from the launch's start"}
 
     # training-step simulator fed by measured group times: a backward pass of
     # 161 gradient computations (g_i = 0.5 * relu(x_i) over the gradient set's

@@ -289,6 +289,31 @@ class TensorFusion:
         _lib.check(self.lib.tf_unpack_range(self.h, first, count, C.c_float(uscale), C.c_void_p(buf.data_ptr()),
                                             _stream_handle(stream)))
 
+    def set_buckets(self, bounds):
+        """Bucket table for one-launch packing: bucket b holds tensors
+        bounds[b] .. bounds[b+1]-1 (as plan_threshold returns them)."""
+        nb = len(bounds) - 1
+        arr = (C.c_int32 * len(bounds))(*[int(x) for x in bounds])
+        _lib.check(self.lib.tf_layout_set_buckets(self.h, nb, arr))
+
+    def pack_buckets(self, scale, buf, stream=None):
+        """Pack every tensor in one launch; each bucket is marked ready as
+        soon as its bytes are written (see bucket_wait)."""
+        _lib.check(self.lib.tf_pack_buckets(self.h, C.c_float(scale), C.c_void_p(buf.data_ptr()),
+                                            _stream_handle(stream)))
+
+    def bucket_wait(self, b, stream=None):
+        """Make `stream` wait until bucket b of the last pack_buckets launch
+        is ready (a stream-ordered wait: no kernel runs for it)."""
+        _lib.check(self.lib.tf_bucket_wait(self.h, b, _stream_handle(stream)))
+
+    def bucket_ready(self, b):
+        """True once bucket b of the last pack_buckets launch is written
+        (a synchronous read of its ready word)."""
+        r = C.c_int32()
+        _lib.check(self.lib.tf_bucket_ready(self.h, b, C.byref(r)))
+        return bool(r.value)
+
     def bucket_ranges(self, bounds):
         """Byte range [start, end) of every bucket in the fusion buffer."""
         starts = [self.offsets[b] if b < len(self.offsets) else self.total_bytes for b in bounds]

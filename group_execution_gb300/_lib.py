@@ -81,6 +81,10 @@ SIGNATURES = {
     "tf_buckets_merge": (_I32, [_P, _P, _I32]),
     "tf_pack_range": (_I32, [_P, _I32, _I32, _F, _P, _P]),
     "tf_unpack_range": (_I32, [_P, _I32, _I32, _F, _P, _P]),
+    "tf_layout_set_buckets": (_I32, [_P, _I32, _P]),
+    "tf_pack_buckets": (_I32, [_P, _F, _P, _P]),
+    "tf_bucket_wait": (_I32, [_P, _I32, _P]),
+    "tf_bucket_ready": (_I32, [_P, _I32, _P]),
     "tf_layout_destroy": (None, [_P]),
 }
 

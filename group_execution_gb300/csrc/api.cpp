@@ -120,7 +120,29 @@ struct tf_layout {
   int32_t* d_err = nullptr;
   int nchunks = 0;
   std::vector<int32_t> chunk_begin;  // first chunk of every tensor, [n + 1]
+  // AllReduce buckets packed in one launch: device block of the chunk ->
+  // bucket map [nchunks], chunks per bucket [nb], counters [nb] and ready
+  // words [nb]; seq = the last bucketed pack enqueued (ready words hold it)
+  int32_t nb = 0;
+  int32_t* d_bucket = nullptr;
+  uint32_t seq = 0;
 };
+
+// cuStreamWaitValue32 through the runtime's driver entry point (no link
+// against the driver library).
+using WaitValueFn = CUresult (*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+WaitValueFn wait_value_fn() {
+  static WaitValueFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuStreamWaitValue32", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<WaitValueFn>(p);
+  });
+  return fn;
+}
 
 // ---------------------------------------------------------------------------
 extern "C" {
@@ -1281,6 +1303,79 @@ fg_status tf_pack(const tf_layout* l, float scale, void* buf, void* stream) {
   return tf_pack_range(l, 0, l->n, scale, buf, stream);
 }
 
+fg_status tf_layout_set_buckets(tf_layout* l, int32_t nb, const int32_t* bounds) {
+  if (!l || !bounds) return err(FG_EINVAL, "null argument");
+  if (nb <= 0 || bounds[0] != 0 || bounds[nb] != l->n) return err(FG_EINVAL, "bucket bounds must run from 0 to n");
+  for (int32_t b = 0; b < nb; ++b)
+    if (bounds[b + 1] <= bounds[b]) return err(FG_EINVAL, "bucket bounds must increase strictly");
+  // chunk -> bucket, then chunks per bucket; counters and ready words zero
+  std::vector<int32_t> host((size_t)l->nchunks + 3 * (size_t)nb, 0);
+  for (int32_t b = 0; b < nb; ++b) {
+    const int c0 = l->chunk_begin[bounds[b]], c1 = l->chunk_begin[bounds[b + 1]];
+    for (int c = c0; c < c1; ++c) host[c] = b;
+    host[(size_t)l->nchunks + b] = c1 - c0;
+  }
+  int32_t* d = nullptr;
+  cudaError_t e = cudaMalloc(&d, sizeof(int32_t) * host.size());
+  if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(bucket table)");
+  e = cudaMemcpy(d, host.data(), sizeof(int32_t) * host.size(), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(d);
+    return cuda_err(e, "cudaMemcpy(bucket table)");
+  }
+  if (l->d_bucket) {
+    // an earlier table may still be read by a launch in flight
+    cudaDeviceSynchronize();
+    cudaFree(l->d_bucket);
+  }
+  l->d_bucket = d;
+  l->nb = nb;
+  l->seq = 0;
+  return FG_OK;
+}
+
+fg_status tf_pack_buckets(tf_layout* l, float scale, void* buf, void* stream) {
+  if (!l || !buf) return err(FG_EINVAL, "null argument");
+  if (!l->nb) return err(FG_EINVAL, "no bucket table (tf_layout_set_buckets)");
+  if (reinterpret_cast<uintptr_t>(buf) % 256) return err(FG_EINVAL, "fusion buffer must be 256-byte aligned");
+  int nsm = 148;
+  device_present(&nsm);
+  TfBuckets bk;
+  bk.chunk_bucket = l->d_bucket;
+  bk.nchunks = l->d_bucket + l->nchunks;
+  bk.count = l->d_bucket + l->nchunks + l->nb;
+  bk.ready = reinterpret_cast<uint32_t*>(l->d_bucket + l->nchunks + 2 * l->nb);
+  bk.seq = l->seq + 1;
+  cudaError_t e = launch_tf_pack(l->d_chunks, l->nchunks, l->buf_bf16, scale, buf, std::min(l->nchunks, nsm * 8),
+                                 static_cast<cudaStream_t>(stream), bk);
+  if (e != cudaSuccess) return cuda_err(e, "tf_pack_buckets launch");
+  l->seq = bk.seq;
+  return FG_OK;
+}
+
+fg_status tf_bucket_wait(const tf_layout* l, int32_t b, void* stream) {
+  if (!l) return err(FG_EINVAL, "null argument");
+  if (!l->nb || !l->seq) return err(FG_EINVAL, "no bucketed pack has been enqueued");
+  if (b < 0 || b >= l->nb) return err(FG_EINVAL, "bucket out of range");
+  WaitValueFn fn = wait_value_fn();
+  if (!fn) return err(FG_EUNSUPPORTED, "cuStreamWaitValue32 is not available");
+  const int32_t* ready = l->d_bucket + l->nchunks + 2 * l->nb + b;
+  CUresult r = fn(static_cast<CUstream>(stream), reinterpret_cast<CUdeviceptr>(ready), l->seq, CU_STREAM_WAIT_VALUE_GEQ);
+  if (r != CUDA_SUCCESS) return err(FG_ECUDA, "cuStreamWaitValue32 failed (" + std::to_string((int)r) + ")");
+  return FG_OK;
+}
+
+fg_status tf_bucket_ready(const tf_layout* l, int32_t b, int32_t* ready) {
+  if (!l || !ready) return err(FG_EINVAL, "null argument");
+  if (!l->nb || !l->seq) return err(FG_EINVAL, "no bucketed pack has been enqueued");
+  if (b < 0 || b >= l->nb) return err(FG_EINVAL, "bucket out of range");
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpy(&v, l->d_bucket + l->nchunks + 2 * l->nb + b, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_err(e, "reading a bucket's ready word");
+  *ready = (int32_t)(v - l->seq) >= 0 ? 1 : 0;
+  return FG_OK;
+}
+
 fg_status tf_unpack(const tf_layout* l, float uscale, const void* buf, void* stream) {
   if (!l) return err(FG_EINVAL, "null argument");
   return tf_unpack_range(l, 0, l->n, uscale, buf, stream);
@@ -1337,6 +1432,7 @@ fg_status tf_sync_status(tf_layout* l, void* stream) {
 void tf_layout_destroy(tf_layout* l) {
   if (!l) return;
   if (l->d_chunks) cudaFree(l->d_chunks);
+  if (l->d_bucket) cudaFree(l->d_bucket);
   delete l;
 }
 

@@ -13,7 +13,11 @@
 // bulk copies (rounded up to 16 bytes, which stays inside the tensor's
 // padding), four warps widen and scale them into a staging buffer, and each
 // chunk leaves as one bulk store of its 16-byte multiple plus at most three
-// plain stores.
+// plain stores.  A pack of several AllReduce buckets in one launch counts
+// every chunk for its bucket; the CTA that counts a bucket's last chunk
+// publishes the bucket as ready (a release store of the launch's sequence
+// number), so that a stream-ordered wait can start that bucket's AllReduce
+// while the rest is still being packed.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -42,7 +46,8 @@ __device__ __forceinline__ void zero_pad(uint8_t* p, int bytes) {
 }
 
 __global__ void __launch_bounds__(kPackThreads) tf_pack_kernel(const TfChunk* __restrict__ chunks, int nchunks,
-                                                               int bf16, float scale, uint8_t* __restrict__ buf) {
+                                                               int bf16, float scale, uint8_t* __restrict__ buf,
+                                                               const TfBuckets bk) {
   pdl_launch_dependents();
   pdl_wait();   // the previous grid's writes are visible from here on
   int ci = blockIdx.x;
@@ -80,6 +85,20 @@ __global__ void __launch_bounds__(kPackThreads) tf_pack_kernel(const TfChunk* __
       }
     }
     if (c.pad_bytes) zero_pad(dst + (size_t)c.count * (bf16 ? 2 : 4), c.pad_bytes);
+    if (bk.ready) {
+      // count the chunk for its bucket: the barrier orders every thread's
+      // stores before thread 0's release (cumulative); the count that
+      // completes the bucket acquires the other CTAs' chunks and publishes
+      // the bucket
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const int b = bk.chunk_bucket[ci];
+        if (atom_add_acq_rel_gpu(&bk.count[b], 1) == bk.nchunks[b] - 1) {
+          bk.count[b] = 0;   // every chunk of this launch has counted: ready for the next
+          st_release_gpu(reinterpret_cast<int32_t*>(bk.ready + b), (int32_t)bk.seq);
+        }
+      }
+    }
     c = cn;
   }
 }
@@ -202,11 +221,11 @@ __global__ void __launch_bounds__(kUnpackThreadsTma, 1)
 }  // namespace
 
 cudaError_t launch_tf_pack(const TfChunk* chunks, int nchunks, int buf_bf16, float scale, void* buf, int grid,
-                           cudaStream_t st) {
+                           cudaStream_t st, const TfBuckets& bk) {
   cudaLaunchConfig_t cfg = pdl_config(grid, kPackThreads, 0, st);
   cudaLaunchAttribute at[1];
   pdl_attr(cfg, at);
-  cudaLaunchKernelEx(&cfg, tf_pack_kernel, chunks, nchunks, buf_bf16, scale, static_cast<uint8_t*>(buf));
+  cudaLaunchKernelEx(&cfg, tf_pack_kernel, chunks, nchunks, buf_bf16, scale, static_cast<uint8_t*>(buf), bk);
   return cudaGetLastError();
 }
 

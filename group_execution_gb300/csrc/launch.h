@@ -47,8 +47,18 @@ struct TfChunk {
   int32_t count;        // elements in the chunk
   int32_t pad_bytes;    // bytes to zero after the chunk (last chunk of a tensor)
 };
+// Per-bucket readiness for a one-launch pack of several AllReduce buckets
+// (all null otherwise): the CTA that counts a bucket's last chunk resets its
+// counter and stores seq in its ready word with release semantics.
+struct TfBuckets {
+  const int32_t* chunk_bucket = nullptr;   // bucket of every chunk of the launch
+  const int32_t* nchunks = nullptr;        // chunks per bucket
+  int32_t* count = nullptr;                // chunks of the bucket written in this launch
+  uint32_t* ready = nullptr;               // last launch whose chunks of the bucket are all written
+  uint32_t seq = 0;
+};
 cudaError_t launch_tf_pack(const TfChunk* chunks, int nchunks, int buf_bf16, float scale, void* buf, int grid,
-                           cudaStream_t st);
+                           cudaStream_t st, const TfBuckets& bk = TfBuckets());
 // Unpack runs one CTA per SM (grid = SM count); err receives DEVERR_TIMEOUT
 // if a wait for a chunk load expires.
 cudaError_t launch_tf_unpack(const TfChunk* chunks, int nchunks, int buf_bf16, float uscale, const void* buf,

@@ -417,6 +417,37 @@ fg_status tf_pack_range(const tf_layout* l, int32_t first, int32_t count, float 
 fg_status tf_unpack_range(const tf_layout* l, int32_t first, int32_t count, float uscale,
                           const void* fusion_buf, void* cuda_stream);
 
+/* One-launch packing of AllReduce buckets (DisCo, Introduction: each fused
+ * buffer's AllReduce starts once its tensors are in it).
+ *
+ * tf_layout_set_buckets: the bucket table, bounds[0 .. n_buckets] as
+ * tf_plan_threshold writes it (bounds[0] = 0, strictly increasing,
+ * bounds[n_buckets] = the layout's tensor count; host, caller-owned, copied).
+ * Replaces an earlier table; allocates the per-bucket device words (chunk
+ * counters and ready words).  FG_EINVAL for a malformed table.
+ *
+ * tf_pack_buckets: packs every tensor in one launch, with tf_pack's result,
+ * and marks each bucket ready the moment its last chunk has been written:
+ * the bucket's ready word receives this launch's sequence number (release
+ * at GPU scope, after the bucket's bytes).  FG_EINVAL without a bucket table.
+ *
+ * tf_bucket_wait: makes cuda_stream wait, in the GPU's front end (no kernel,
+ * no SM), until bucket b of the most recently enqueued tf_pack_buckets launch
+ * is ready; work enqueued on that stream afterwards (the bucket's AllReduce)
+ * reads its bytes.  The pack launch must already be enqueued (on any stream
+ * that does not itself wait for cuda_stream): FG_EINVAL if none is, or if b
+ * is out of range.
+ *
+ * tf_bucket_ready: *ready = 1 if bucket b of the most recently enqueued
+ * tf_pack_buckets launch has been marked ready, else 0 (a synchronous read
+ * of the bucket's ready word; host-side polling).  FG_EINVAL as for
+ * tf_bucket_wait.  Launches of one layout must be ordered (one stream, or
+ * streams that wait for each other): they share the bucket counters. */
+fg_status tf_layout_set_buckets(tf_layout* l, int32_t n_buckets, const int32_t* bounds);
+fg_status tf_pack_buckets(tf_layout* l, float scale, void* fusion_buf, void* cuda_stream);
+fg_status tf_bucket_wait(const tf_layout* l, int32_t bucket, void* cuda_stream);
+fg_status tf_bucket_ready(const tf_layout* l, int32_t bucket, int32_t* ready);
+
 void tf_layout_destroy(tf_layout* l);
 
 #ifdef __cplusplus

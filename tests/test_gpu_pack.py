@@ -138,3 +138,65 @@ def test_range_edge_cases():
     got = buf.cpu().numpy()
     np.testing.assert_array_equal(got[s:e], ref[s:e])
     assert (got[:s] == 0xAB).all() and (got[e:] == 0xAB).all()
+
+
+def _bucketed(sizes, threshold, seed=0):
+    from group_execution_gb300 import plan_threshold
+    xs = W.tensor_fusion_inputs(sizes, seed)
+    dev = [torch.from_numpy(x).cuda() for x in xs]
+    tf = TensorFusion(dev)
+    bounds = plan_threshold(sizes, threshold)
+    tf.set_buckets(bounds)
+    return tf, bounds, PK.pack(xs, 0.125)
+
+
+def test_pack_buckets_one_launch():
+    """Every AllReduce bucket packed in one launch: the buffer equals the
+    oracle's bytes, and after each of three launches every bucket reads as
+    ready (its counter was reset by the bucket's last chunk each time)."""
+    sizes = W.tensor_fusion_sizes(0)
+    tf, bounds, ref = _bucketed(sizes, 8 << 20)
+    nb = len(bounds) - 1
+    assert nb > 3
+    for _ in range(3):
+        buf = torch.full((tf.total_bytes,), 0xAB, dtype=torch.uint8, device="cuda")
+        tf.pack_buckets(0.125, buf)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(buf.cpu().numpy(), ref)
+        assert all(tf.bucket_ready(b) for b in range(nb))
+
+
+def test_pack_buckets_small_and_single():
+    """Buckets of one tensor each (empty and ragged tensors included), and a
+    single bucket of everything."""
+    sizes = [5, 0, 8192, 0, 3, 8192 * 2 + 1, 1]
+    for threshold in (0, 1 << 30):
+        tf, bounds, ref = _bucketed(sizes, threshold, seed=2)
+        assert len(bounds) - 1 == (len(sizes) if threshold == 0 else 1)
+        buf = torch.full((tf.total_bytes,), 0xAB, dtype=torch.uint8, device="cuda")
+        tf.pack_buckets(0.125, buf)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(buf.cpu().numpy(), ref)
+        assert all(tf.bucket_ready(b) for b in range(len(bounds) - 1))
+
+
+def test_bucket_wait_orders_each_bucket():
+    """A second stream waits for each bucket in turn (a stream-ordered wait
+    on its ready word) and copies that bucket's bytes out while the one pack
+    launch may still be running: every copy equals the oracle's bytes."""
+    sizes = W.tensor_fusion_sizes(0)
+    tf, bounds, ref = _bucketed(sizes, 8 << 20)
+    ranges = tf.bucket_ranges(bounds)
+    s2 = torch.cuda.Stream()
+    for _ in range(2):
+        buf = torch.full((tf.total_bytes,), 0xAB, dtype=torch.uint8, device="cuda")
+        torch.cuda.synchronize()
+        tf.pack_buckets(0.125, buf)
+        outs = []
+        for b, (lo, hi) in enumerate(ranges):
+            tf.bucket_wait(b, s2)
+            with torch.cuda.stream(s2):
+                outs.append(buf[lo:hi].clone())
+        torch.cuda.synchronize()
+        for (lo, hi), o in zip(ranges, outs):
+            np.testing.assert_array_equal(o.cpu().numpy(), ref[lo:hi])
