@@ -440,8 +440,11 @@ fg_status tf_unpack_range(const tf_layout* l, int32_t first, int32_t count, floa
  *
  * tf_bucket_ready: *ready = 1 if bucket b of the most recently enqueued
  * tf_pack_buckets launch has been marked ready, else 0 (a synchronous read
- * of the bucket's ready word; host-side polling).  FG_EINVAL as for
- * tf_bucket_wait.  Launches of one layout must be ordered (one stream, or
+ * of the bucket's ready word; host-side polling).  The read is a cudaMemcpy
+ * on the legacy default stream, so it also waits for work on that stream
+ * and on every blocking stream: to watch a pack while it runs, enqueue the
+ * pack on a non-blocking stream (PyTorch's side streams are).  FG_EINVAL as
+ * for tf_bucket_wait.  Launches of one layout must be ordered (one stream, or
  * streams that wait for each other): they share the bucket counters. */
 fg_status tf_layout_set_buckets(tf_layout* l, int32_t n_buckets, const int32_t* bounds);
 fg_status tf_pack_buckets(tf_layout* l, float scale, void* fusion_buf, void* cuda_stream);
