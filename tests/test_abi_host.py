@@ -361,3 +361,35 @@ def test_page_pattern_matmul_bias():
 def test_partition_with_tuples_matches_oracle(seed):
     from tests._helpers import tuple_dag
     _parity(tuple_dag(seed))
+
+
+def test_launches_fail_loudly_without_a_device():
+    """With no CUDA device every entry point that would run a kernel returns
+    FG_ECUDA (there is no CPU fallback), while graph building and grouping
+    still work; the tensor-fusion calls refuse a null layout with FG_EINVAL.
+    Pointers here are never dereferenced: each call fails before any launch."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    lib = _lib.load()
+    spec = W.diamond(200, 132)
+    plan = graph_from_spec(spec).build()
+    info = plan.groups[0]
+    ptrs = plan._ptrs({v: 0x100000 * (i + 1) for i, v in enumerate(info.leaves + info.outs)})
+    assert lib.fg_launch_group(plan.h, 0, ptrs, None) == _lib.FG_ECUDA
+    assert lib.fg_launch_unfused(plan.h, 0, ptrs, None) == _lib.FG_ECUDA
+    assert lib.fg_sync_status(plan.h, None) == _lib.FG_ECUDA
+    numel = (C.c_int64 * 2)(10, 20)
+    grads = (C.c_void_p * 2)(0x100000, 0x200000)
+    h, offs, total = C.c_void_p(), (C.c_int64 * 2)(), C.c_int64()
+    assert lib.tf_layout_create(2, numel, grads, _lib.FG_BF16, 256, C.byref(h), offs, C.byref(total)) == _lib.FG_ECUDA
+    assert h.value is None
+    rowsum = _lib.OPCODES["rowsum"]
+    assert lib.fg_row_reduce_noalloc(rowsum, C.c_void_p(0x100000), 4, 8, C.c_void_p(0x200000), None) == _lib.FG_ECUDA
+    buf, ready = C.c_void_p(0x100000), C.c_int32()
+    assert lib.tf_pack(None, C.c_float(1.0), buf, None) == _lib.FG_EINVAL
+    assert lib.tf_unpack(None, C.c_float(1.0), buf, None) == _lib.FG_EINVAL
+    assert lib.tf_layout_set_buckets(None, 1, (C.c_int32 * 2)(0, 2)) == _lib.FG_EINVAL
+    assert lib.tf_pack_buckets(None, C.c_float(1.0), buf, None) == _lib.FG_EINVAL
+    assert lib.tf_bucket_wait(None, 0, None) == _lib.FG_EINVAL
+    assert lib.tf_bucket_ready(None, 0, C.byref(ready)) == _lib.FG_EINVAL
