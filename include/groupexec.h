@@ -172,7 +172,11 @@ void fg_graph_destroy(fg_graph* g);
  * one-operator program per node for fg_launch_unfused.  Allocates the plan's
  * device error flag and reduce scratch when a CUDA device is present; without
  * one the plan is host-only (queries work, launches fail).  opts may be NULL
- * for the defaults. */
+ * for the defaults.  A group the kernels cannot run (say a matmul operand
+ * whose contiguous extent is not a multiple of 8) does not fail the build:
+ * the plan keeps the grouping, and that group's queries (which still fill
+ * their outputs) and launches return its status, FG_EUNSUPPORTED, with the
+ * reason in fg_last_error. */
 fg_status fg_build_groups(const fg_graph* g, const fg_build_opts* opts, fg_plan** plan);
 
 /* Node and group counts; group_of[node] = the node id of its group's sink
