@@ -48,7 +48,7 @@ typedef enum {
   FG_OK = 0,
   FG_EINVAL = 1,        /* bad argument: null pointer, unknown id, bad opcode */
   FG_ESHAPE = 2,        /* operand shapes do not fit the operator */
-  FG_EUNSUPPORTED = 3,  /* valid graph this build cannot execute (reason in fg_last_error) */
+  FG_EUNSUPPORTED = 3,  /* valid graph the kernels cannot execute (reason in fg_last_error) */
   FG_ENOMEM = 4,        /* host or device allocation failed */
   FG_ECUDA = 5,         /* CUDA runtime/driver error, or no CUDA device */
   FG_ETIMEOUT = 6,      /* a device-side bounded wait expired */
