@@ -427,8 +427,11 @@ fg_status tf_unpack_range(const tf_layout* l, int32_t first, int32_t count, floa
  * tf_layout_set_buckets: the bucket table, bounds[0 .. n_buckets] as
  * tf_plan_threshold writes it (bounds[0] = 0, strictly increasing,
  * bounds[n_buckets] = the layout's tensor count; host, caller-owned, copied).
- * Replaces an earlier table; allocates the per-bucket device words (chunk
- * counters and ready words).  FG_EINVAL for a malformed table.
+ * Replaces an earlier table (after a device-wide synchronize, since a launch
+ * in flight may still read it); allocates the per-bucket device words (chunk
+ * counters and ready words) and restarts the sequence numbers, so call it
+ * between steps, not while a bucket wait is pending.  FG_EINVAL for a
+ * malformed table.
  *
  * tf_pack_buckets: packs every tensor in one launch, with tf_pack's result,
  * and marks each bucket ready the moment its last chunk has been written:
