@@ -520,27 +520,23 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
       p.inplace_off = cg.leaf_stage_off[i];
       break;
     }
-  // Cluster shape and ring granularity.  Two pairs on side-by-side tiles may
-  // share their A rows (4-CTA clusters), and a ring slot holds one or two K
-  // blocks; the interpreter keeps pairs and two-block slots.  Flag bits
-  // 16-17: 1 = pairs only, 2 = 4-CTA clusters whenever the output has two
-  // tile columns; bits 18-19: 1 or 2 K blocks per slot (0 = chosen).
+  // Ring granularity: a ring slot holds one or two K blocks (flag bits
+  // 18-19: 1 or 2, 0 = chosen); the interpreter keeps two-block slots.  The
+  // kernel always runs CTA pairs (2-CTA clusters), whose operand copies land
+  // only in the CTA that issues them.
   ge.compiled = !(o.flags & FG_FLAG_INTERPRET);
-  const int shape = (o.flags >> 16) & 3, kbf = (o.flags >> 18) & 3, sched = (o.flags >> 20) & 3;
+  const int kbf = (o.flags >> 18) & 3, sched = (o.flags >> 20) & 3;
   const int tnf = (o.flags >> 22) & 3;
-  const bool c4 = ge.compiled && p.ntn >= 2 && shape == 2;
   const int KB = ge.compiled && kbf == 1 ? 1 : 2;
-  const int CL = c4 ? kGemmCluster4 : kGemmCluster, PR = CL / 2;
-  if (c4) p.a_3d = 0;   // each CTA fetches half of an A half: 2-D boxes
+  constexpr int CL = kGemmCluster;
   // Pair tile width (flag bits 22-23: 0 or 1 = 256, 2 = 128 columns; the
-  // interpreter and 4-CTA clusters keep 256).  128-column tiles fill the
-  // rounds of a short-K launch better, but measured slower: each tile's
-  // fixed costs and the doubled A traffic outweigh it.
+  // interpreter keeps 256).  128-column tiles fill the rounds of a short-K
+  // launch better, but measured slower: each tile's fixed costs and the
+  // doubled A traffic outweigh it.
   int TN = kGemmN;
-  if (ge.compiled && !c4 && tnf == 2) TN = 128;
+  if (ge.compiled && tnf == 2) TN = 128;
   p.ntn = (int32_t)((cg.N + TN - 1) / TN);
   p.ntiles = p.ntm * p.ntn;
-  cg.gemm_cl = CL;
   cg.gemm_kb = KB;
   cg.gemm_tn = TN;
   // operand ring and epilogue-leaf ring depths that fit 227 KB, in order of
@@ -606,13 +602,13 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
   cg.nstages = ns;
   ge.big = cg.depth > 4 || cg.slots > 4;
   ge.min_blocks = 1;
-  // units of the cluster's 256 rows x PR 256-column tiles; one CTA per SM,
-  // as many clusters as run at once (flag bits 8-15, when set, cap them: a
-  // test hook for the split schedules)
+  // units: the pair's 256 rows x TN columns; one CTA per SM, as many pairs
+  // as run at once (flag bits 8-15, when set, cap them: a test hook for the
+  // split schedules)
   const int nslots = (p.nkb + KB - 1) / KB;
-  const int units = ((p.ntm + 1) / 2) * ((p.ntn + PR - 1) / PR);
+  const int units = ((p.ntm + 1) / 2) * p.ntn;
   p.nunits = units;
-  int avail = gemm_max_clusters(CL, ge.smem);
+  int avail = gemm_max_clusters(ge.smem);
   if (avail <= 0) avail = nsm / CL;
   int ncl = std::max(1, std::min(units, avail));
   const int cap = (o.flags >> 8) & 0xff;
@@ -623,15 +619,14 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
   p.sk = 0;
   p.nsplit_n = 0;
   const int tail = units % ncl;
-  if (sched == 2 || (sched == 0 && c4)) {
+  if (sched == 2) {
     // every cluster takes an equal share of all units' ring slots; a share
     // spans at least one unit, so a unit is cut at most once
     if (units > ncl && tail > 0) {
       p.sk = 1;
       p.split = 2;
     }
-  } else if (units > ncl && tail > 0 && 2 * tail <= ncl && CL == kGemmCluster && TN == kGemmN &&
-             (sched == 3 || sched == 0)) {
+  } else if (units > ncl && tail > 0 && 2 * tail <= ncl && TN == kGemmN && (sched == 3 || sched == 0)) {
     // cut the last round's units into their two column halves over the
     // pairs it would leave idle: each half runs all of K and its own
     // epilogue, with no partial sums to exchange (measured against K pieces:
@@ -687,7 +682,7 @@ fg_status alloc_device(fg_plan* p, GroupExec& ge) {
     if (mp.split > 1 && !mp.nsplit_n) {
       // split units: the last round's (round robin), or one per share
       // boundary (stream-K); two pieces each
-      const int CL = ge.cg.gemm_cl;
+      constexpr int CL = kGemmCluster;
       const size_t keys = mp.sk ? (size_t)(ge.grid / CL - 1) : (size_t)(mp.nunits - mp.nfull);
       cudaError_t e = cudaMalloc(&ge.scratch, sizeof(float) * keys * 2 * CL * kGemmM * ge.cg.gemm_tn);
       if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(split-tail workspace)");
@@ -793,12 +788,11 @@ fg_status launch_gemm(GroupExec& ge, void* const* ptrs, void* stream) {
       // Otherwise 2-D boxes: MN-major 64 x 64, K-major 64 x 128 rows.
       // With KB K blocks per ring slot the 3-D boxes cover KB * 64 K rows
       // (MN-major) or KB K blocks (K-major), over a half's R rows (A: 128;
-      // B: half the tile's columns).  In 4-CTA clusters with one K block per
-      // slot each CTA fetches 64 of its 128 A rows (K-major box 64 x 64).
+      // B: half the tile's columns).
       uint64_t dims[3], strides[2];
       uint32_t box[3];
       const int KB = cg.gemm_kb;
-      auto view = [&](bool mn, bool v3, int64_t rows, int R, bool half_rows) {
+      auto view = [&](bool mn, bool v3, int64_t rows, int R) {
         const int64_t inner = mn ? rows : cg.K, outer = mn ? cg.K : rows;
         if (v3) {
           dims[0] = 64; dims[1] = outer; dims[2] = inner / 64; strides[0] = inner * 2; strides[1] = 128;
@@ -806,22 +800,22 @@ fg_status launch_gemm(GroupExec& ge, void* const* ptrs, void* stream) {
           return 3;
         }
         dims[0] = inner; dims[1] = outer; strides[0] = inner * 2; box[0] = 64;
-        box[1] = mn || half_rows ? 64 : R;
+        box[1] = mn ? 64 : R;
         return 2;
       };
-      int rank = view(gp.a_mn, gp.a_3d, cg.M, kGemmM, cg.gemm_cl == kGemmCluster4 && KB == 1);
+      int rank = view(gp.a_mn, gp.a_3d, cg.M, kGemmM);
       if (fg_status st = encode(&gp.mapA, ptrs[cg.mm_a], rank, dims, strides, box, true,
                                 CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
         return st;
       // B: [K, N] (N contiguous), or [N, K] when transposed; each CTA of a
       // pair stages its half of the tile's columns
-      rank = view(gp.b_mn, gp.b_3d, cg.N, cg.gemm_tn / 2, false);
+      rank = view(gp.b_mn, gp.b_3d, cg.N, cg.gemm_tn / 2);
       if (fg_status st = encode(&gp.mapB, ptrs[cg.mm_b], rank, dims, strides, box, true,
                                 CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
         return st;
       if (gp.nsplit_n) {
         // a unit's column half: each CTA stages a quarter of the tile's columns
-        rank = view(gp.b_mn, gp.b_3d, cg.N, cg.gemm_tn / 4, false);
+        rank = view(gp.b_mn, gp.b_3d, cg.N, cg.gemm_tn / 4);
         if (fg_status st = encode(&gp.mapB2, ptrs[cg.mm_b], rank, dims, strides, box, true,
                                   CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
           return st;

@@ -166,7 +166,6 @@ constexpr int kGemmM = 128, kGemmN = 256, kGemmK = 64, kGemmChunk = 32;
 constexpr int kGemmKB = 2;             // K blocks per operand ring slot (interpreted kernel; compiled: 1 or 2)
 constexpr int kGemmWarps = 12;         // A loads, MMA, epilogue loads, 4 epilogue warps, B loads, 4 epilogue warps
 constexpr int kGemmCluster = 2;        // CTAs of a pair issuing 2-SM MMAs on one 256-row tile
-constexpr int kGemmCluster4 = 4;       // two pairs on adjacent 256-column tiles sharing their A rows
 
 struct GemmParams {
   CUtensorMap mapA, mapB;              // bf16 operands (boxes per major-ness)

@@ -520,17 +520,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(cbar), "l"(policy)
       : "memory");
 }
-// The same tile delivered to the same offset in every CTA of `mask`; each
-// destination's bytes are counted on the barrier at cbar's offset in the CTA
-// of the destination's pair that cbar names (cbar's peer bit).
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* m, int32_t x, int32_t y,
-                                                    uint32_t cbar, uint16_t mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(cbar), "h"(mask), "l"(policy)
-      : "memory");
-}
 // Hinted single-CTA loads and stores (GEMM epilogue streams).
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* m, int32_t x, int32_t y,
                                                  uint32_t bar, uint64_t policy) {

@@ -11,13 +11,11 @@
 // slot (two by default: 64 KB), each operand half in one TMA copy where the
 // layout allows; the even CTA issues 2-SM tcgen05.mma instructions
 // (cta_group::2) that read both CTAs' halves and leave each CTA's 128
-// accumulator rows in its own TMEM.  In a 4-CTA cluster (by choice) two pairs
-// take side-by-side tiles of the same 256 rows: each A half is fetched once,
-// by the two CTAs that need it taking half of it each and multicasting it to
-// both.  Warp roles, in each CTA:
+// accumulator rows in its own TMEM.  Every operand copy lands in the CTA
+// that issued it; no copy is multicast.  Warp roles, in each CTA:
 //   warp 0     TMA producer of the bf16 A halves, arming the even CTA's slot
-//              barrier; every operand load completes on the even CTA's slot
-//              barrier of each destination's pair,
+//              barrier; every operand load of both CTAs completes on that
+//              barrier,
 //   warp 7     TMA producer of the B halves (a slot's copies issue at a few
 //              hundred ns each from one thread: two producers halve the time
 //              from a slot's release to its refill),
@@ -271,18 +269,16 @@ __device__ __forceinline__ void gemm_load_half(uint32_t dst, const CUtensorMap* 
   }
 }
 
-// CL = 2: a CTA pair per 256 x 256 tile (cta_group::2), each CTA holding
-// half of A's rows and half of B's columns.  CL = 4: two such pairs on the
-// two 256-column halves of a 256 x 512 unit, sharing their A halves.  KB: K
-// blocks of 64 per operand ring slot (1 or 2).  TN: columns of a pair's tile
-// (256, or 128: half the epilogue per tile, for short K where the epilogue's
-// streams dominate and finer tiles fill the last round).
-template <class Epi, int CL, int KB, int TN>
+// A CTA pair (a 2-CTA cluster) per 256 x TN tile (cta_group::2), each CTA
+// holding half of A's rows and half of B's columns.  KB: K blocks of 64 per
+// operand ring slot (1 or 2).  TN: columns of a pair's tile (256, or 128:
+// half the epilogue per tile, for short K where the epilogue's streams
+// dominate and finer tiles fill the last round).
+template <class Epi, int KB, int TN>
 __device__ __forceinline__ void gemm_body(const GemmParams& P) {
-  static_assert(CL == 2 || CL == 4, "the kernel runs CTA pairs, alone or two by two");
   static_assert(KB == 1 || KB == 2, "one or two K blocks per ring slot");
   static_assert(TN == 256 || TN == 128, "pair tiles of 256 or 128 columns");
-  constexpr int PR = CL / 2;                                       // pairs per cluster
+  constexpr int CL = kGemmCluster;                                 // CTAs per cluster: one pair
   constexpr int kBCols = TN / 2;                                   // B columns staged per CTA
   constexpr int kGemmChunks = TN / kGemmChunk;                     // epilogue chunks per tile
   constexpr int kHalfA = KB * kGemmABytes;                         // 128 rows x KB K blocks
@@ -311,20 +307,19 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   const int nslots = (P.nkb + KB - 1) / KB;                       // ring slots per tile
 
   const uint32_t rank = cluster_ctarank();
-  const int h = (int)(rank & 1), pr = (int)(rank >> 1);   // CTA within its pair, pair within the cluster
+  const int h = (int)(rank & 1);   // CTA within its pair
   const bool leader = h == 0;
-  const uint32_t even = rank & ~1u;                       // the pair's MMA-issuing CTA
-  const uint16_t pair_mask = (uint16_t)(3u << (2 * pr));
-  // ring slots are released to every producer that writes into them: the
-  // pair's own, and with CL = 4 the other pair's (A multicast)
-  const uint16_t slot_mask = (uint16_t)((1u << CL) - 1);
-  // unit u: 256 rows of block u / nsn and PR tiles of 256 columns; this CTA
-  // works on rows h, pair pr's columns
+  const uint32_t even = 0;         // the pair's MMA-issuing CTA
+  // MMA completions arrive at both CTAs of the pair: ring slots are released
+  // to both producers, accumulators to both epilogues
+  const uint16_t pair_mask = 3u;
+  // unit u: the tile of 256 rows in row block u / ntn and TN columns in
+  // column block u % ntn; this CTA works on its half h of the rows
   const int ncl = gridDim.x / CL, cl = blockIdx.x / CL;
-  const int nsn = (P.ntn + PR - 1) / PR;
+  const int nsn = P.ntn;
   auto tile_of = [&](int u, int& m0, int& n0) {
     m0 = ((u / nsn) * 2 + h) * kGemmM;
-    n0 = ((u % nsn) * PR + pr) * TN;
+    n0 = (u % nsn) * TN;
   };
   // an item's output block: its unit's tile, or the tile's column half; and
   // its 32-column epilogue chunks
@@ -338,7 +333,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
     issued[0] = issued[1] = 0;
     for (int s = 0; s < NS; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, PR);   // one commit from each pair's MMA issuer
+      mbar_init(empty0 + 8 * s, 1);   // one commit from the pair's MMA issuer
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull0 + 8 * b, 1);
@@ -410,27 +405,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
             continue;
           }
           if (leader) mbar_expect_tx(fbar, 2 * (hb ? kStageBytesH : kStageBytes));
-          if constexpr (CL == 4) {
-            // A rows h are shared by CTAs h and h + 2: pair pr fetches half of
-            // them for both (2-D boxes): K block pr of two, or with one K
-            // block its 64-wide group pr (MN-major) or rows 64 pr.. (K-major)
-            const uint16_t mc = (uint16_t)((1u << h) | (1u << (h + 2)));
-            if constexpr (KB == 2) {
-              if (P.a_mn) {
-#pragma unroll
-                for (int g = 0; g < 2; ++g)
-                  tma_load_2d_pair_mc(a + g * 16384 + pr * 8192, &P.mapA, m0 + 64 * g, k0 + 64 * pr, cbar, mc, keep);
-              } else {
-                tma_load_2d_pair_mc(a + pr * 16384, &P.mapA, k0 + 64 * pr, m0, cbar, mc, keep);
-              }
-            } else if (P.a_mn) {
-              tma_load_2d_pair_mc(a + pr * 8192, &P.mapA, m0 + 64 * pr, k0, cbar, mc, keep);
-            } else {
-              tma_load_2d_pair_mc(a + pr * 8192, &P.mapA, k0, m0 + 64 * pr, cbar, mc, keep);
-            }
-          } else {
-            gemm_load_half<KB, kGemmM>(a, &P.mapA, P.a_mn, P.a_3d, m0, k0, cbar, keep);
-          }
+          gemm_load_half<KB, kGemmM>(a, &P.mapA, P.a_mn, P.a_3d, m0, k0, cbar, keep);
         }
       }
       issued[isA ? 0 : 1] = it;
@@ -503,7 +478,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
               tc_mma_bf16<2>(d, ad0 + so + aoff[j * 4 + kk], bd0 + so + (hb ? boff_h : boff)[j * 4 + kk], id,
                              sl != w.sl0 || j != 0 || kk != 0);
           }
-          tc_commit_mask(empty0 + 8 * s, slot_mask);   // every producer writing the slot may refill it
+          tc_commit_mask(empty0 + 8 * s, pair_mask);   // both producers may refill the slot
           if (++s == NS) {
             s = 0;
             ph ^= 1;

@@ -103,7 +103,6 @@ struct CompiledGroup {
   // gemm
   int32_t mm_a = -1, mm_b = -1, mm_ta = 0, mm_tb = 0;
   int64_t M = 0, N = 0, K = 0;
-  int gemm_cl = 2;                    // CTAs per cluster: a pair, or two pairs sharing A rows
   int gemm_kb = 2;                    // K blocks of 64 per operand ring slot
   int gemm_tn = 256;                  // columns of a pair's tile
   // staging decisions (filled by plan_staging)

@@ -10,7 +10,7 @@ namespace fg {
 template <int D, int S>
 __global__ void __cluster_dims__(kGemmCluster, 1, 1) __launch_bounds__(kGemmThreads, 1)
     fg_gemm_epi_kernel(const __grid_constant__ GemmParams P) {
-  gemm_body<InterpGemmEpi<D, S>, kGemmCluster, kGemmKB, kGemmN>(P);
+  gemm_body<InterpGemmEpi<D, S>, kGemmKB, kGemmN>(P);
 }
 
 cudaError_t launch_gemm_kernel(const GemmParams& p, int big, int grid, int smem, cudaStream_t st) {
@@ -25,25 +25,25 @@ cudaError_t launch_gemm_kernel(const GemmParams& p, int big, int grid, int smem,
 }
 
 // Stands in for the GEMM kernel in the occupancy query: residency is set by
-// the shared memory (more than half an SM's) and the cluster shape.
+// the shared memory (more than half an SM's) and the pair clusters.
 __global__ void __launch_bounds__(kGemmThreads, 1) fg_gemm_residency_probe(int) {}
 
-int gemm_max_clusters(int cl, int smem) {
-  static int cached[2][256] = {};   // [cl == 4][smem / 1 KB]: clusters + 1
-  const int ci = cl == 4 ? 1 : 0, si = (smem >> 10) & 255;
-  if (cached[ci][si]) return cached[ci][si] - 1;
+int gemm_max_clusters(int smem) {
+  static int cached[256] = {};   // [smem / 1 KB]: pairs + 1
+  const int si = (smem >> 10) & 255;
+  if (cached[si]) return cached[si] - 1;
   if (cudaFuncSetAttribute(fg_gemm_residency_probe, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cl);
+  cfg.gridDim = dim3(kGemmCluster);
   cfg.blockDim = dim3(kGemmThreads);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = cl;
+  at[0].val.clusterDim.x = kGemmCluster;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
@@ -53,7 +53,7 @@ int gemm_max_clusters(int cl, int smem) {
     cudaGetLastError();
     return 0;
   }
-  cached[ci][si] = n + 1;
+  cached[si] = n + 1;
   return n;
 }
 

@@ -32,9 +32,9 @@ int group_kernel_threads();
 int set_last_error(int status, const char* msg);
 
 cudaError_t launch_gemm_kernel(const GemmParams& p, int big, int grid, int smem, cudaStream_t st);
-// Clusters of `cl` CTAs of the GEMM kernel's shape (one CTA per SM, `smem`
+// CTA pairs (2-CTA clusters) of the GEMM kernel's shape (one CTA per SM, `smem`
 // bytes of shared memory) that the device runs at once; 0 if unknown.
-int gemm_max_clusters(int cl, int smem);
+int gemm_max_clusters(int smem);
 int gemm_smem_bytes(const GemmParams& p);
 
 // Tensor fusion.  One chunk = up to kTfChunk consecutive elements of one

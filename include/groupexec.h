@@ -106,9 +106,8 @@ typedef struct tf_layout tf_layout;
  * column by column (0 = row-major walk), and for GEMM-epilogue groups the
  * most clusters to launch (0 = as many as the device runs at once); bits
  * 16-23 = tiles per reduce work unit (0 = chosen from the frame and the SM
- * count), and for GEMM-epilogue groups bits 16-17 the cluster shape (0 =
- * chosen, 1 = CTA pairs, 2 = 4-CTA clusters whose two pairs share their A
- * rows), bits 18-19 the K blocks of 64 per operand ring slot (0 = chosen,
+ * count), and for GEMM-epilogue groups (which always run as CTA pairs;
+ * bits 16-17 are ignored) bits 18-19 the K blocks of 64 per operand ring slot (0 = chosen,
  * 1, 2), bits 20-21 the schedule (0 = chosen, 1 = round robin with the last
  * round's tiles cut along K into two pieces, 2 = equal shares of all tiles'
  * K steps, 3 = round robin with the last round's tiles cut into their two

@@ -55,17 +55,17 @@ def test_tuple_programs_compile():
         _compile(plan.source(0))
 
 
-@pytest.mark.parametrize("shape,cl,kb,tn", [(0, 2, 2, 256), (1 << 16, 2, 2, 256), (2 << 16, 4, 2, 256),
-                                            (1 << 18, 2, 1, 256), ((2 << 16) | (1 << 18), 4, 1, 256),
-                                            (2 << 22, 2, 2, 128), ((2 << 22) | (1 << 18), 2, 1, 128)])
-def test_gemm_cluster_shapes_compile(shape, cl, kb, tn):
-    """The GEMM-epilogue program in CTA pairs and in 4-CTA clusters whose two
-    pairs share their A rows (multicast), with one or two K blocks per ring
-    slot."""
+@pytest.mark.parametrize("shape,kb,tn", [(0, 2, 256), (1 << 16, 2, 256), (2 << 16, 2, 256), (1 << 18, 1, 256),
+                                         ((2 << 16) | (1 << 18), 1, 256), (2 << 22, 2, 128),
+                                         ((2 << 22) | (1 << 18), 1, 128)])
+def test_gemm_cluster_shapes_compile(shape, kb, tn):
+    """The GEMM-epilogue program always runs CTA pairs (bits 16-17 of the
+    flags are ignored), with one or two K blocks per ring slot and 256- or
+    128-column pair tiles; no operand copy is multicast."""
     spec = W.sf_update(256, 256, 512)
     plan = graph_from_spec(spec).build(flags=shape)
     assert plan.groups[0].kind == "gemm"
     src = plan.source(0)
-    assert f"__cluster_dims__({cl}, 1, 1)" in src
-    assert f"gemm_body<fg::JitEpi, {cl}, {kb}, {tn}>" in src
+    assert "__cluster_dims__(fg::kGemmCluster, 1, 1)" in src
+    assert f"gemm_body<fg::JitEpi, {kb}, {tn}>" in src
     _compile(src)

@@ -13,11 +13,11 @@ from group_execution_gb300 import _lib
 
 pytestmark = pytest.mark.gpu
 MODES = [0, _lib.FG_FLAG_INTERPRET]
-PAIRS, CLUSTER4 = 1 << 16, 2 << 16     # GEMM cluster shape: CTA pairs only / two pairs sharing A
+PAIRS = 1 << 16                        # GEMM cluster shape: CTA pairs (ignored: the only shape)
 KB1, KB2 = 1 << 18, 2 << 18            # K blocks per operand ring slot
 TN256, TN128 = 1 << 22, 2 << 22        # columns of a pair's tile
 KSPLIT = 1 << 20                       # schedule: round robin, the last round's units cut into K pieces
-SHAPES = [CLUSTER4 | KB2, CLUSTER4 | KB1, PAIRS | KB1, PAIRS | TN128, PAIRS | KB1 | TN128]
+SHAPES = [PAIRS | KB2, PAIRS | KB1, PAIRS | TN128, PAIRS | KB1 | TN128]
 
 
 def _matmul_graph(K, M, N, ta, tb, epi=None):
@@ -154,16 +154,14 @@ def test_column_half_tail_full_size():
     _sf_update(1024, 4096, 4096, 0)
 
 
-# ---- 4-CTA clusters: two pairs on side-by-side tiles share their A rows ----
+# ---- ring granularity and tile widths ----
 
 @pytest.mark.parametrize("ta,tb", [(1, 0), (0, 0), (0, 1), (1, 1)])
 @pytest.mark.parametrize("kmn", [(1024, 512, 1024), (1096, 392, 1288), (200, 264, 600), (64, 128, 512)])
 @pytest.mark.parametrize("shape", SHAPES)
 def test_cluster_shapes_layouts(ta, tb, kmn, shape):
-    """4-CTA clusters (two pairs sharing A rows) and one-K-block ring slots,
-    every operand layout; ragged M, N and K (with clusters the second pair's
-    tile lies past N when the tile columns are odd: N = 600), K shorter than
-    one ring slot."""
+    """One- and two-K-block ring slots and 128-column pair tiles, every
+    operand layout; ragged M, N and K, K shorter than one ring slot."""
     K, M, N = kmn
     spec = _matmul_graph(K, M, N, ta, tb)
     g, plan, inputs, dev = prepare(spec, flags=shape)
@@ -174,32 +172,14 @@ def test_cluster_shapes_layouts(ta, tb, kmn, shape):
     _check_matmul_bound(env[spec.outputs[0]].cpu().numpy(), A, B)
 
 
-@pytest.mark.parametrize("K,M,N,cap", [(2048, 1024, 2048, 5), (2048, 1024, 2048, 3), (2048, 1024, 2048, 7),
-                                       (1152, 776, 1800, 6), (4096, 512, 1024, 3)])
-@pytest.mark.parametrize("kb", [KB2, KB1])
-def test_cluster4_stream_k(K, M, N, cap, kb):
-    """Clusters capped so that the units do not divide evenly: each cluster
-    runs an equal share of all units' ring slots, a unit cut by a share
-    boundary meets its two partial accumulators in the workspace; run twice,
-    so the arrival counters are seen to reset."""
-    spec = W.sf_update(K, M, N)
-    g, plan, inputs, dev = prepare(spec, flags=(cap << 8) | CLUSTER4 | kb)
-    ref = OE.run_unfused(spec, inputs)[spec.outputs[0]]
-    w = inputs[2]
-    for _ in range(2):
-        env = run_fused(plan, spec, dev)
-        plan.sync()
-        got = env[spec.outputs[0]].cpu().numpy()
-        assert rel_err(got, ref) <= TOL_F32
-        assert rel_err(w - got, w - ref) <= TOL_BF16
-
-
 @pytest.mark.parametrize("ta,tb", [(0, 1), (1, 1)])
 @pytest.mark.parametrize("kb", [KB2, KB1])
-def test_cluster4_stream_k_plain(ta, tb, kb):
+def test_pairs_stream_k_plain(ta, tb, kb):
+    """A plain matmul with pairs capped so that each runs an equal share of
+    all units' ring slots (stream-K)."""
     K, M, N = 2048, 1024, 1536
     spec = _matmul_graph(K, M, N, ta, tb)
-    g, plan, inputs, dev = prepare(spec, flags=(5 << 8) | CLUSTER4 | kb)
+    g, plan, inputs, dev = prepare(spec, flags=(5 << 8) | PAIRS | (2 << 20) | kb)
     env = run_fused(plan, spec, dev)
     plan.sync()
     A = inputs[0].T if ta else inputs[0]
@@ -249,7 +229,9 @@ def test_sf_update_full_tn128():
 SK = 2 << 20   # schedule: equal shares of all tiles' K steps
 
 
-@pytest.mark.parametrize("K,M,N,cap,kb", [(2048, 1024, 1024, 5, KB2), (1152, 776, 1800, 7, KB1), (4096, 512, 768, 4, KB2)])
+@pytest.mark.parametrize("K,M,N,cap,kb", [(2048, 1024, 1024, 5, KB2), (1152, 776, 1800, 7, KB1), (4096, 512, 768, 4, KB2),
+                                          (2048, 1024, 2048, 3, KB1), (2048, 1024, 2048, 7, KB2),
+                                          (1152, 776, 1800, 6, KB2), (4096, 512, 1024, 3, KB1)])
 def test_pairs_stream_k(K, M, N, cap, kb):
     """CTA pairs walking equal shares of all tiles' K steps: a share boundary
     cuts a tile into two pieces, the one ending a share finishing it; run
@@ -278,7 +260,7 @@ ST_PRODUCER, ST_WARPS = 1 << 24, 2 << 24   # in-place results stored by the leaf
     (1024, 520, 1160, (3 << 8) | PAIRS | KSPLIT | KB1),  # ragged rows and columns, split tail
     (1024, 1024, 768, (7 << 8) | PAIRS | TN128 | KB1),   # 128-column pair tiles
     (4096, 512, 768, (4 << 8) | PAIRS | SK | KB2),       # stream-K shares, two leaf buffers
-    (512, 776, 1000, (2 << 8) | CLUSTER4 | KB2),         # 4-CTA clusters, ragged
+    (512, 776, 1000, (3 << 8) | PAIRS | SK | KB2),       # stream-K shares, ragged
 ])
 def test_inplace_store_modes(store, K, M, N, extra):
     """Results written in place of the IDENT leaf's chunk leave either in one
