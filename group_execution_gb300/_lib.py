@@ -65,6 +65,7 @@ SIGNATURES = {
     "fg_plan_destroy": (None, [_P]),
     "fg_last_error": (C.c_char_p, []),
     "fg_row_reduce_noalloc": (_I32, [_I32, _P, _I64, _I64, _P, _P]),
+    "fg_row_reduce_noalloc_status": (_I32, [_P]),
     "tf_layout_create": (_I32, [_I32, _PI64, C.POINTER(_P), _I32, _I64, C.POINTER(_P), _PI64, _PI64]),
     "tf_pack": (_I32, [_P, _F, _P, _P]),
     "tf_unpack": (_I32, [_P, _F, _P, _P]),

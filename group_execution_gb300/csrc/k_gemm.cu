@@ -20,8 +20,7 @@ cudaError_t launch_gemm_kernel(const GemmParams& p, int big, int grid, int smem,
   cudaLaunchConfig_t cfg = pdl_config(grid, kGemmThreads, smem, st);
   cudaLaunchAttribute at[1];
   pdl_attr(cfg, at);
-  cudaLaunchKernelEx(&cfg, k, p);
-  return cudaGetLastError();
+  return cudaLaunchKernelEx(&cfg, k, p);
 }
 
 // Stands in for the GEMM kernel in the occupancy query: residency is set by

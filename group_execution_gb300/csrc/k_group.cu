@@ -26,8 +26,7 @@ static cudaError_t launch_one(K kernel, const GroupParams& p, int grid, int smem
   cudaLaunchConfig_t cfg = pdl_config(grid, kThreads, smem, st);
   cudaLaunchAttribute at[1];
   pdl_attr(cfg, at);
-  cudaLaunchKernelEx(&cfg, kernel, p);
-  return cudaGetLastError();
+  return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 cudaError_t launch_group_kernel(const GroupParams& p, int exec, int big, int grid, int smem, cudaStream_t st) {

@@ -225,8 +225,7 @@ cudaError_t launch_tf_pack(const TfChunk* chunks, int nchunks, int buf_bf16, flo
   cudaLaunchConfig_t cfg = pdl_config(grid, kPackThreads, 0, st);
   cudaLaunchAttribute at[1];
   pdl_attr(cfg, at);
-  cudaLaunchKernelEx(&cfg, tf_pack_kernel, chunks, nchunks, buf_bf16, scale, static_cast<uint8_t*>(buf), bk);
-  return cudaGetLastError();
+  return cudaLaunchKernelEx(&cfg, tf_pack_kernel, chunks, nchunks, buf_bf16, scale, static_cast<uint8_t*>(buf), bk);
 }
 
 int tf_unpack_smem(int buf_bf16) {
@@ -252,8 +251,7 @@ cudaError_t launch_tf_unpack(const TfChunk* chunks, int nchunks, int buf_bf16, f
   cudaLaunchConfig_t cfg = pdl_config(grid, kUnpackThreadsTma, smem, st);
   cudaLaunchAttribute at[1];
   pdl_attr(cfg, at);
-  cudaLaunchKernelEx(&cfg, tf_unpack_kernel, chunks, nchunks, buf_bf16, uscale, static_cast<const uint8_t*>(buf), err);
-  return cudaGetLastError();
+  return cudaLaunchKernelEx(&cfg, tf_unpack_kernel, chunks, nchunks, buf_bf16, uscale, static_cast<const uint8_t*>(buf), err);
 }
 
 }  // namespace fg

@@ -13,6 +13,7 @@
 
 #include <cstring>
 #include <mutex>
+#include <string>
 
 #include "groupexec.h"
 #include "launch.h"
@@ -25,15 +26,30 @@ constexpr int64_t kMaxRows = 65536;
 constexpr int kMaxSplits = 16;
 constexpr size_t kPartialBytes = size_t(kMaxRows) * kMaxSplits * sizeof(float);   // 4 MiB
 constexpr size_t kCounterBytes = size_t(kMaxRows / kTileR) * sizeof(int32_t);     // 8 KiB
+constexpr size_t kErrOffset = kPartialBytes + kCounterBytes;                          // the error word
+constexpr size_t kScratchBytes = kErrOffset + 256;
 
 // Held by every GPU that loads the library until the process exits.  All
 // calls share it: calls that overlap on the GPU (different streams, or
-// different host threads without ordering) race on it.
-static __device__ __align__(256) unsigned char g_noalloc_scratch[kPartialBytes + kCounterBytes];
+// different host threads without ordering) race on it.  Layout: partial row
+// values | arrival counters | one error word that a kernel giving up on a
+// bounded wait latches, read and cleared by fg_row_reduce_noalloc_status.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_mu;
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
+// The array's device address per device, and the context it was looked up
+// in: a context that is destroyed and created again (cudaDeviceReset) loads
+// the module again, possibly at another address, so the lookup is redone
+// when the current context's id changes.
+struct ScratchAddr {
+  unsigned long long ctx_id;
+  void* addr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -53,18 +69,49 @@ EncodeFn encoder() {
   return fn;
 }
 
-// Device address of the scratch array on the current device, looked up once
-// per device (the first call on a device does this).
+template <class Fn>
+Fn driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<Fn>(p);
+  return nullptr;
+}
+
+// Id of the calling thread's current context (0 if there is none yet or it
+// cannot be read: the lookup below then runs, and makes the device's primary
+// context current).
+unsigned long long current_ctx_id() {
+  static CtxGetCurrentFn get_ctx = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    get_ctx = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  });
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (!get_ctx || !get_id || get_ctx(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch array on the current device.  The first call
+// on a device (per host thread that has no current context yet), and the
+// first after the device's context was created again, looks it up.
 void* scratch_address(int dev, cudaError_t* e) {
+  const unsigned long long id = current_ctx_id();
   std::lock_guard<std::mutex> g(g_mu);
-  if (!g_scratch_addr[dev]) {
+  ScratchAddr& a = g_scratch_addr[dev];
+  if (!a.addr || id == 0 || a.ctx_id != id) {
     void* p = nullptr;
     *e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (*e != cudaSuccess) return nullptr;
-    g_scratch_addr[dev] = p;
+    a.addr = p;
+    a.ctx_id = id;
   }
   *e = cudaSuccess;
-  return g_scratch_addr[dev];
+  return a.addr;
 }
 
 }  // namespace
@@ -147,7 +194,7 @@ extern "C" fg_status fg_row_reduce_noalloc(int32_t opcode, const float* x, int64
   p.nunits = p.ntr * nsplit;
   p.scratch = reinterpret_cast<float*>(scratch);
   p.counters = reinterpret_cast<int32_t*>(scratch + kPartialBytes);
-  p.err = nullptr;
+  p.err = reinterpret_cast<int32_t*>(scratch + kErrOffset);
   // the arrival counters must start at zero (a call cut short by a device
   // timeout could leave them set); partial values are written before read
   if (nsplit > 1) {
@@ -160,4 +207,27 @@ extern "C" fg_status fg_row_reduce_noalloc(int32_t opcode, const float* x, int64
   e = launch_group_kernel(p, 1, 0, grid, smem, st);
   if (e != cudaSuccess) return (fg_status)set_last_error(FG_ECUDA, cudaGetErrorString(e));
   return FG_OK;
+}
+
+extern "C" fg_status fg_row_reduce_noalloc_status(void* cuda_stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev >= kMaxDevices)
+    return (fg_status)set_last_error(FG_ECUDA, "no usable CUDA device");
+  uint8_t* scratch = static_cast<uint8_t*>(scratch_address(dev, &e));
+  if (!scratch) return (fg_status)set_last_error(FG_ECUDA, cudaGetErrorString(e));
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return (fg_status)set_last_error(FG_ECUDA, cudaGetErrorString(e));
+  int32_t word = 0;
+  e = cudaMemcpyAsync(&word, scratch + kErrOffset, sizeof(word), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return (fg_status)set_last_error(FG_ECUDA, cudaGetErrorString(e));
+  if (word == 0) return FG_OK;
+  e = cudaMemsetAsync(scratch + kErrOffset, 0, sizeof(word), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return (fg_status)set_last_error(FG_ECUDA, cudaGetErrorString(e));
+  if (word == DEVERR_TIMEOUT)
+    return (fg_status)set_last_error(FG_ETIMEOUT, "a device-side wait of fg_row_reduce_noalloc exceeded 2 s");
+  return (fg_status)set_last_error(FG_EDEVICE, ("device error word " + std::to_string(word)).c_str());
 }

@@ -250,12 +250,23 @@ const char* fg_last_error(void);
  * Limits: rows <= 65536 (else FG_EINVAL) and rows*cols < 2^31 (else
  * FG_ESHAPE).  x (16-byte aligned) and y (4-byte aligned) are device
  * pointers owned by the caller.  Asynchronous on cuda_stream.  The first
- * call on a device looks up the array's device address; make that call
- * before any stream capture.  All calls share the array, so calls that
- * overlap on the GPU (other streams, or host threads without ordering) race.
- * Device-side timeouts are not reported by this entry point. */
+ * call on a device (and on each host thread with no current context, and
+ * the first after the device's context was created again) looks up the
+ * array's device address; make that call before any stream capture.  All
+ * calls share the array, so calls that overlap on the GPU (other streams,
+ * or host threads without ordering) race.  A bounded device-side wait (2 s)
+ * that expires latches an error word in the same array and leaves y
+ * incomplete; the call itself cannot see it (it returns before the kernel
+ * runs): fg_row_reduce_noalloc_status reports it. */
 fg_status fg_row_reduce_noalloc(int32_t opcode, const float* x, int64_t rows, int64_t cols, float* y,
                                 void* cuda_stream);
+
+/* Synchronizes cuda_stream, then reads and clears the error word that
+ * fg_row_reduce_noalloc's kernels latch on the current device: FG_OK if no
+ * call since the last read gave up, FG_ETIMEOUT if a bounded wait expired
+ * (that call's y is incomplete), FG_ECUDA for a CUDA error.  Allocates
+ * nothing.  No counterpart on the pages either. */
+fg_status fg_row_reduce_noalloc_status(void* cuda_stream);
 
 /* ---- explicit fusion --------------------------------------------------------
  * DisCo, Introduction and Strategy Maker, optimisation methods (i) and (ii):

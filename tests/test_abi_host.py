@@ -386,6 +386,7 @@ def test_launches_fail_loudly_without_a_device():
     assert h.value is None
     rowsum = _lib.OPCODES["rowsum"]
     assert lib.fg_row_reduce_noalloc(rowsum, C.c_void_p(0x100000), 4, 8, C.c_void_p(0x200000), None) == _lib.FG_ECUDA
+    assert lib.fg_row_reduce_noalloc_status(None) == _lib.FG_ECUDA
     buf, ready = C.c_void_p(0x100000), C.c_int32()
     assert lib.tf_pack(None, C.c_float(1.0), buf, None) == _lib.FG_EINVAL
     assert lib.tf_unpack(None, C.c_float(1.0), buf, None) == _lib.FG_EINVAL
