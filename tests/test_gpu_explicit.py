@@ -10,7 +10,7 @@ torch = pytest.importorskip("torch")
 import workloads as W
 from oracle import explicit as OX
 from oracle import execute as OE
-from tests._helpers import rel_err, TOL_F32, small_dags, dag_to_spec
+from tests._helpers import rel_err, check_parity, TOL_F32, small_dags, dag_to_spec
 from tests._gpu import to_dev, run_fused
 from group_execution_gb300 import graph_from_spec, _lib, FgError
 
@@ -35,8 +35,7 @@ def _run_moves(spec, moves, from_fuseops=False, seed=0, expect_outs=None):
     ref = OE.run_unfused(spec, ins, keep=[v.vid for v in spec.ops])
     written = [o for gi in plan.groups for o in gi.outs]
     for o in written:
-        e = rel_err(env[o].cpu().numpy(), ref[o])
-        assert e <= TOL_F32, (o, spec.values[o].op, e)
+        check_parity(spec, o, env[o].cpu().numpy(), ref[o])
     if expect_outs is not None:
         assert [gi.outs for gi in plan.groups] == expect_outs
     return plan

@@ -10,7 +10,7 @@ torch = pytest.importorskip("torch")
 import workloads as W
 from oracle import execute as OE
 from oracle import partition as OP
-from tests._helpers import rel_err, TOL_F32, tuple_dag
+from tests._helpers import check_parity, exact_value, tuple_dag
 from tests._gpu import prepare, run_fused, run_unfused
 
 pytestmark = pytest.mark.gpu
@@ -26,12 +26,12 @@ def _check(spec, seed=0, unfused=True):
     plan.sync()
     for info in plan.groups:
         for o in info.outs:
-            assert rel_err(env[o].cpu().numpy(), ref[o]) <= TOL_F32, (o, spec.values[o].op)
+            check_parity(spec, o, env[o].cpu().numpy(), ref[o])
     if unfused:
         envu = run_unfused(plan, spec, dev)
         plan.sync()
         for o in spec.outputs:
-            assert rel_err(envu[o].cpu().numpy(), ref[o]) <= TOL_F32
+            check_parity(spec, o, envu[o].cpu().numpy(), ref[o])
     return plan
 
 
@@ -47,6 +47,21 @@ def _inception(r1, r2, C, transpose=False, three=False):
         c = g.op("transpose", (c,))
     g.mark_output(g.op("scale", (c,), (0.5,)))
     return g
+
+
+@pytest.mark.parametrize("r1,r2,C", [(64, 32, 64), (40, 24, 32), (37, 29, 20), (300, 212, 96)])
+@pytest.mark.parametrize("transpose", [False, True])
+def test_concat_only_bit_exact(r1, r2, C, transpose):
+    """A tuple of inputs concatenated (and transposed): an injective-only
+    group, equal to the oracle bit for bit."""
+    g = W.GraphSpec()
+    c = g.op("concat", (g.op("tuple", (g.input((r1, C)), g.input((r2, C)))),))
+    if transpose:
+        c = g.op("transpose", (c,))
+    g.mark_output(c)
+    assert exact_value(g, c)
+    plan = _check(g)
+    assert plan.n_groups == 1
 
 
 @pytest.mark.parametrize("r1,r2,C", [(64, 32, 64), (40, 24, 32), (37, 29, 20), (300, 212, 96)])
