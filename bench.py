@@ -7,12 +7,18 @@ group, so a step is one kernel launch.  The headline is that group's HBM
 throughput counted in algorithmic bytes (each leaf read once, the output
 written once) per second, whole job over all ranks.
 
-Printed as one JSON line (rank 0).  Beside the headline the line carries:
-the roofline of the dominant kernel, the end-to-end number through the C ABI
-with host buffers, the CPU oracle's throughput on a bounded sample, the
-unfused one-kernel-per-operator time of the same plan, and the other hot-path
-rows measured in the same process (the RNNLM chain, tensor-fusion pack and
-unpack, the random DAG, and the GEMM-epilogue group when it is available).
+Printed as one JSON line (rank 0), kept under 3 KB.  Beside the headline the
+line carries: the roofline of the dominant kernel, the end-to-end number
+through the C ABI with host buffers, the CPU oracle's throughput on a bounded
+sample, and `rows`: every other hot-path row measured in the same process,
+three significant digits each (us = median microseconds per run, x = speed-up
+over one kernel per operator, frac = fraction of the measured HBM copy peak,
+frac_bf16 = of the measured bf16 peak): the diamond fused and unfused, the
+RNNLM chain (1 and 2 groups; as is and scaled to [65536, 1024]), row sums,
+the diamond with P returned under the three explicit-fusion plans, the tuple
+concatenation, the MLP pattern group, pack and unpack, the AllReduce buckets,
+the training-step simulator, the sufficient-factor update at K = 512 and
+4096, the random DAG, and the oracle's own times.
 
 Inputs (256 MiB) and the output (128 MiB) together exceed the 129 MB L2, so
 the timed loop needs no L2 flush; the smaller rows flush L2 between reps.
@@ -146,7 +152,7 @@ def cpu_sample(rows=1024, reps=3):
         times.append(time.perf_counter() - t0)
     t = min(times)
     return {"value": alg / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"diamond slab X,Z[{rows},{C}] op by op in float64, best of {reps} ({t:.2f} s each)"}
+            "sample": f"diamond X,Z[{rows},{C}] slab, best of {reps} ({t:.2f} s)"}
 
 
 def oracle_samples():
@@ -169,27 +175,20 @@ def oracle_samples():
     out = {}
     sp = W.rnnlm_chain()
     ins = W.make_inputs(sp, 0)
-    t = best(lambda: OE.run_unfused(sp, ins), 3)
-    out["rnnlm_chain"] = {"ms": t * 1e3, "sample": "the whole chain X, Y [64,1024]", "cores": 1}
+    out["rnnlm_ms"] = best(lambda: OE.run_unfused(sp, ins), 3) * 1e3          # the whole chain, 1 core
+    # SF update on rows 0..255 of W (1/16 of the output; BLAS on every core),
+    # scaled to the full output
     sp = W.sf_update(512, 256, 4096)
     ins = W.make_inputs(sp, 0)
-    t = best(lambda: OE.run_unfused(sp, ins))
-    out["sf_update_K512"] = {"ms": t * 1e3, "TFLOPs": 2 * 512 * 256 * 4096 / t / 1e12, "cores": os.cpu_count(),
-                             "sample": "rows 0..255 of W (1/16 of the output): U [512,256], V [512,4096]",
-                             "ms_full_estimate": t * 16e3}
+    out["sf_k512_ms_est"] = best(lambda: OE.run_unfused(sp, ins)) * 16e3
+    out["sf_cores"] = os.cpu_count()
     sizes = W.tensor_fusion_sizes(0)
     xs = W.tensor_fusion_inputs(sizes)
-    tp = best(lambda: OP.pack(xs, 0.125))
-    buf = OP.pack(xs, 0.125)
-    tu = best(lambda: OP.unpack(buf, [int(n) for n in sizes], 1.0))
-    out["tensor_fusion"] = {"pack_ms": tp * 1e3, "unpack_ms": tu * 1e3, "cores": 1,
-                            "pack_GBps": int(sizes.sum()) * 6 / tp / 1e9, "sample": "all 161 tensors"}
+    out["pack_GBps"] = int(sizes.sum()) * 6 / best(lambda: OP.pack(xs, 0.125)) / 1e9    # all 161 tensors
+    # the 200-operator graph on [512,256] values (1/256 of the elements), scaled
     sp = W.random_dag(0, R=512, C=256, nominal_R=8192, nominal_C=4096)
     ins = W.make_inputs(sp, 0)
-    t = best(lambda: OE.run_unfused(sp, ins), 1)
-    out["random_dag_seed0"] = {"ms": t * 1e3, "cores": 1, "GBps": W.algorithmic_bytes_unfused(sp) / t / 1e9,
-                               "sample": "the same 200-operator graph on [512,256] values (1/256 of the elements)",
-                               "ms_full_estimate": t * 256e3}
+    out["dag200_ms_est"] = best(lambda: OE.run_unfused(sp, ins), 1) * 256e3
     return out
 
 
@@ -365,18 +364,19 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": dict(WORKLOAD, parallelism=f"replicas x{ws}", plan=plan.exec_info(0)),
+            "config": dict(WORKLOAD, parallelism=f"replicas x{ws}"),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "traffic": traffic_for("fg_jit_ew_group", "diamond"),
-                         "kernel": "fg_jit_ew_group (compiled group program)", "peak_source": peak_kind,
+                         "kernel": "fg_jit_ew_group", "peak_source": peak_kind,
                          "alg_bytes_per_launch": info.alg_bytes},
             "e2e": e2e, "gpu_launches": args.steps, "clocks": clk.summary()}
     if rank == 0 and not args.no_rows:
         line["rows"] = secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf16s)
         line["cpu_baseline"] = cpu_sample()
-        for k, v in oracle_samples().items():
-            line["rows"].setdefault(k, {})["oracle"] = v
+        line["rows"]["oracle"] = _round(oracle_samples())
     if rank == 0:
+        for k in [k for k in ("roofline", "e2e", "cpu_baseline") if k in line]:
+            line[k] = {a: (float(f"{b:.5g}") if isinstance(b, float) else b) for a, b in line[k].items()}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -539,11 +539,11 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
     env[spec.outputs[0]] = out
     med_f, _ = timed(run_plan(plan, spec, env, True), flush=False)
     med_u, _ = timed(run_plan(plan, spec, env, False), flush=False)
-    rows["diamond"] = {"fused_us": med_f * 1e3, "unfused_us": med_u * 1e3, "speedup_vs_unfused": med_u / med_f,
-                       "fused_launches": 1, "unfused_launches": len(spec.ops),
-                       "unfused_bytes": W.algorithmic_bytes_unfused(spec)}
+    rows["diamond"] = {"us": med_f * 1e3, "unf_us": med_u * 1e3, "x": med_u / med_f,
+                       "frac": plan.groups[0].alg_bytes / (med_f * 1e-3) / 1e9 / hbm}
 
-    # RNNLM chain, both partitions (launch-bound by construction)
+    # RNNLM chain, both partitions (launch-bound by construction): L2 flushed
+    # before each launch, and replayed from a CUDA graph (no host work)
     for epi in (False, True):
         sp = W.rnnlm_chain()
         p = graph_from_spec(sp).build(allow_reduce_epilogue=epi)
@@ -554,14 +554,10 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
             e.setdefault(v.vid, torch.empty(v.shape, device="cuda"))
         med, mn = timed(run_plan(p, sp, e, True))
         medu, _ = timed(run_plan(p, sp, e, False))
-        gmed, gmn = timed(graphed(run_plan(p, sp, e, True)))
-        gmedu, _ = timed(graphed(run_plan(p, sp, e, False)))
-        alg = sum(gi.alg_bytes for gi in p.groups)
-        rows["rnnlm_chain" + ("_1group" if epi else "_2groups")] = {
-            "fused_us": med * 1e3, "fused_min_us": mn * 1e3, "groups": p.n_groups, "unfused_us": medu * 1e3,
-            "graph_fused_us": gmed * 1e3, "graph_fused_min_us": gmn * 1e3, "graph_unfused_us": gmedu * 1e3,
-            "GBps": alg / (gmed * 1e-3) / 1e9,
-            "note": "launch-latency bound (0.53 MB); L2 flushed; graph_* = CUDA-graph replay"}
+        gmed, _ = timed(graphed(run_plan(p, sp, e, True)), flush=False)
+        gmedu, _ = timed(graphed(run_plan(p, sp, e, False)), flush=False)
+        rows["rnnlm_" + ("1g" if epi else "2g")] = {
+            "us": med * 1e3, "unf_us": medu * 1e3, "graph_us": gmed * 1e3, "graph_unf_us": gmedu * 1e3}
 
     # the same chain scaled to X, Y [65536, 1024] (512 MiB): bandwidth-bound,
     # so its roofline fraction means something; inputs exceed L2, no flush
@@ -576,10 +572,22 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
         med, mn = timed(run_plan(p, sp, e, True), flush=False)
         medu, _ = timed(run_plan(p, sp, e, False), flush=False)
         alg = sum(gi.alg_bytes for gi in p.groups)
-        rows["rnnlm_chain_65536x1024" + ("_1group" if epi else "_2groups")] = {
-            "fused_us": med * 1e3, "fused_min_us": mn * 1e3, "groups": p.n_groups, "unfused_us": medu * 1e3,
-            "speedup_vs_unfused": medu / med, "alg_bytes": alg, "GBps": alg / (med * 1e-3) / 1e9,
-            "frac_of_hbm": alg / (med * 1e-3) / 1e9 / hbm}
+        rows["rnnlm65536_" + ("1g" if epi else "2g")] = {
+            "us": med * 1e3, "x": medu / med, "frac": alg / (med * 1e-3) / 1e9 / hbm}
+        del e
+
+    # row sums over [8192, 4096] and [4096, 8192] (134 MB each, above L2)
+    for shp in ((8192, 4096), (4096, 8192)):
+        sp = W.GraphSpec("rowsum")
+        x = sp.input(shp)
+        sp.mark_output(sp.op("rowsum", (x,)))
+        p = graph_from_spec(sp).build()
+        gen = torch.Generator(device="cuda").manual_seed(3)
+        e = {x: torch.empty(shp, device="cuda").uniform_(-1, 1, generator=gen),
+             sp.outputs[0]: torch.empty((shp[0],), device="cuda")}
+        med, _ = timed(run_plan(p, sp, e, True), flush=False)
+        rows[f"rowsum{shp[0]}x{shp[1]}"] = {"us": med * 1e3,
+                                            "frac": p.groups[0].alg_bytes / (med * 1e-3) / 1e9 / hbm}
         del e
 
     # explicit fusion moves on the diamond when P = X + bias is also a result
@@ -596,11 +604,11 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
     plans = {"fuseops": gsp.build()}
     pn = gsp.partition(from_fuseops=True)
     pn.fuse(1, 0, False)
-    plans["non_duplicate"] = pn.build()
+    plans["nondup"] = pn.build()
     pd = gsp.partition(from_fuseops=True)
     for reader in (1, 2, 4):
         pd.fuse(reader, 0, True)
-    plans["duplicate"] = pd.build()
+    plans["dup"] = pd.build()
     row = {}
     for k, pl in plans.items():
         def f(pl=pl):
@@ -608,9 +616,9 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
                 pl.launch_group(gid, {v: e[v] for v in gi.leaves + gi.outs})
         med, _ = timed(f, flush=False)
         alg = sum(gi.alg_bytes for gi in pl.groups)
-        row[k] = {"groups": pl.n_groups, "us": med * 1e3, "alg_bytes": alg, "GBps": alg / (med * 1e-3) / 1e9,
-                  "frac_of_hbm": alg / (med * 1e-3) / 1e9 / hbm}
-    rows["diamond_with_P_output"] = row
+        row[k + "_us"] = med * 1e3
+        row[k + "_frac"] = alg / (med * 1e-3) / 1e9 / hbm
+    rows["diamond_P"] = row
     del e
 
     # two branches joined by a tuple and a concatenation (FuseOps phases 1 and
@@ -628,14 +636,12 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
     med, _ = timed(run_plan(tplan, tsp, te, True), flush=False)
     medu, _ = timed(run_plan(tplan, tsp, te, False), flush=False)
     alg = sum(gi.alg_bytes for gi in tplan.groups)
-    rows["tuple_concat_2x4096x4096"] = {
-        "groups": tplan.n_groups, "fused_us": med * 1e3, "unfused_us": medu * 1e3, "speedup_vs_unfused": medu / med,
-        "alg_bytes": alg, "GBps": alg / (med * 1e-3) / 1e9, "frac_of_hbm": alg / (med * 1e-3) / 1e9 / hbm}
+    rows["tuple"] = {"us": med * 1e3, "x": medu / med, "frac": alg / (med * 1e-3) / 1e9 / hbm}
     del te
 
     # an MLP layer grouped by pattern (FuseOpsByPattern with the page's matmul +
     # bias pattern extended by relu): Y = relu(X W + b), X [4096, 4096],
-    # W [4096, 4096] bf16, one GEMM-epilogue group
+    # W [4096, 4096] bf16, one GEMM-epilogue group; L2 flushed between runs
     msp = W.GraphSpec("mlp")
     mx = msp.input((4096, 4096), "bf16")
     mw = msp.input((4096, 4096), "bf16")
@@ -651,10 +657,8 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
           my: torch.empty((4096, 4096), device="cuda")}
     mgi = mplan.groups[0]
     med, _ = timed(lambda: mplan.launch_group(0, {v: me[v] for v in mgi.leaves + mgi.outs}))
-    rows["mlp_layer_pattern_4096"] = {
-        "groups": mplan.n_groups, "match_of": mpart.match_of, "us": med * 1e3,
-        "TFLOPs": mgi.alg_flops / (med * 1e-3) / 1e12, "frac_of_bf16_peak": mgi.alg_flops / (med * 1e-3) / 1e12 / bf16,
-        "note": "L2 flushed between runs"}
+    tf_ = mgi.alg_flops / (med * 1e-3) / 1e12
+    rows["mlp"] = {"us": med * 1e3, "TFLOPs": tf_, "frac": tf_ / bf16}
     del me
 
     # tensor-fusion pack / unpack
@@ -667,16 +671,15 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
     # 153.6 MB per call exceeds L2: back-to-back calls, no flush
     mp, _ = timed(lambda: tf.pack(0.125, buf), flush=False, inner=10)
     mu, _ = timed(lambda: tf.unpack(1.0, buf), flush=False, inner=10)
-    rows["tensor_fusion"] = {"tensors": len(sizes), "elements": int(sizes.sum()),
-                             "pack_us": mp * 1e3, "pack_GBps": nbytes / (mp * 1e-3) / 1e9,
-                             "pack_frac": nbytes / (mp * 1e-3) / 1e9 / hbm,
-                             "unpack_us": mu * 1e3, "unpack_GBps": nbytes / (mu * 1e-3) / 1e9,
-                             "unpack_frac": nbytes / (mu * 1e-3) / 1e9 / hbm, "launches_each": 1,
-                             "per_tensor_unfused_launches": 2 * len(sizes)}
+    rows["pack"] = {"us": mp * 1e3, "frac": nbytes / (mp * 1e-3) / 1e9 / hbm}
+    rows["unpack"] = {"us": mu * 1e3, "frac": nbytes / (mu * 1e-3) / 1e9 / hbm}
 
     # the same gradients cut into AllReduce buckets by an 8 MiB fusion
-    # threshold, packed and unpacked one launch per bucket (what an overlapped
-    # exchange issues as each bucket's gradients become ready)
+    # threshold: packed one launch per bucket (replayed from a CUDA graph),
+    # and every bucket in one launch with per-bucket ready words; ready_us:
+    # when a second stream waiting on each bucket's word passes it, from the
+    # launch's start (an L2 flush runs first on the launching stream, so that
+    # every wait is enqueued before the pack starts)
     from group_execution_gb300 import plan_threshold
     bounds = plan_threshold(list(sizes), 8 << 20)
     nb = len(bounds) - 1
@@ -684,15 +687,8 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
     def each_bucket(fn, s):
         return lambda: [fn(bounds[k], bounds[k + 1] - bounds[k], s, buf) for k in range(nb)]
 
-    bp, _ = timed(each_bucket(tf.pack_range, 0.125), flush=False, inner=10)
-    bu, _ = timed(each_bucket(tf.unpack_range, 1.0), flush=False, inner=10)
     gp, _ = timed(graphed(each_bucket(tf.pack_range, 0.125)), flush=False, inner=10)
     gu, _ = timed(graphed(each_bucket(tf.unpack_range, 1.0)), flush=False, inner=10)
-    # all buckets packed in one launch, each marked ready as soon as its bytes
-    # are written: a second stream waits for each bucket in turn and records
-    # an event, timed from an event just before the launch (median of 10).
-    # An L2 flush runs first on the launching stream, so that every wait is
-    # enqueued before the pack starts (the host's enqueueing is not timed)
     tf.set_buckets(bounds)
     ob, _ = timed(lambda: tf.pack_buckets(0.125, buf), flush=False, inner=10)
     s2 = torch.cuda.Stream()
@@ -713,26 +709,18 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
         torch.cuda.synchronize()
         for k in range(nb):
             ready[k].append(st.elapsed_time(evs[k]) * 1e3)
-    rows["tensor_fusion_buckets_8MiB"] = {
-        "buckets": nb, "launches_each": nb, "pack_us": bp * 1e3, "unpack_us": bu * 1e3,
-        "graph_pack_us": gp * 1e3, "graph_pack_GBps": nbytes / (gp * 1e-3) / 1e9,
-        "graph_pack_frac": nbytes / (gp * 1e-3) / 1e9 / hbm, "graph_unpack_us": gu * 1e3,
-        "graph_unpack_GBps": nbytes / (gu * 1e-3) / 1e9, "graph_unpack_frac": nbytes / (gu * 1e-3) / 1e9 / hbm,
-        "one_launch_pack_us": ob * 1e3, "one_launch_pack_GBps": nbytes / (ob * 1e-3) / 1e9,
-        "one_launch_pack_frac": nbytes / (ob * 1e-3) / 1e9 / hbm,
-        "bucket_ready_us": [statistics.median(r) for r in ready],
-        "bucket_bytes": [e - s for s, e in tf.bucket_ranges(bounds)],
-        "note": "pack_us/unpack_us: one host launch per bucket; graph_*: the launches replayed from a CUDA graph; "
-                "one_launch_pack: every bucket in one launch, bucket_ready_us: when a stream waiting on each "
-                "bucket's ready word passes it, from the launch's start"}
+    rows["buckets8MiB"] = {"n": nb, "graph_pack_us": gp * 1e3, "graph_unpack_us": gu * 1e3,
+                           "one_launch_us": ob * 1e3, "one_launch_frac": nbytes / (ob * 1e-3) / 1e9 / hbm,
+                           "ready_us": [round(statistics.median(r), 1) for r in ready]}
 
     # training-step simulator fed by measured group times: a backward pass of
     # 161 gradient computations (g_i = 0.5 * relu(x_i) over the gradient set's
     # sizes, one group each, run in production order), every group timed on
-    # this GPU, then the step simulated with AllReduce buckets of the bf16
-    # gradients for several fusion thresholds on an 8-GPU ring (900 GB/s per
-    # link direction; 20 us of per-AllReduce overhead: assumed, the pages
-    # give none)
+    # this GPU (device time per launch: 20 launches replayed from a CUDA
+    # graph), then the step simulated with AllReduce buckets of the bf16
+    # gradients for several fusion thresholds on an 8-GPU ring
+    # T = 2(N-1)x/(B N) + D with B = 900 GB/s per link direction and
+    # D = 20 us per AllReduce (assumed: the pages give none)
     from group_execution_gb300 import simulate
     bsp = W.GraphSpec("backward")
     grads = []
@@ -746,8 +734,6 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
         be[v.vid] = torch.empty(v.shape, device="cuda").uniform_(-1, 1) if v.is_input else torch.empty(v.shape, device="cuda")
     op_time = []
     for gid, gi in enumerate(bplan.groups):
-        # device time per launch: 20 launches of the group replayed from one
-        # CUDA graph (no host work between them)
         ptrs = {v: be[v] for v in gi.leaves + gi.outs}
         rep = graphed(lambda gid=gid, ptrs=ptrs: [bplan.launch_group(gid, ptrs) for _ in range(20)])
         med, _ = timed(rep, reps=3, flush=False)
@@ -756,25 +742,17 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
     gbytes = [int(n_i) * 2 for n_i in sizes]
     c_ring = 2.0 * 7 / (900e9 * 8)
     sim = {}
-    t0 = time.perf_counter()
-    nsim = 0
     for thr in (0, 1 << 20, 4 << 20, 16 << 20, 1 << 40):
         bb = plan_threshold(list(sizes), thr)
         buckets = [list(range(bb[k], bb[k + 1])) for k in range(len(bb) - 1)]
         tot, *_ = simulate(op_time, edges, list(range(len(sizes))), gbytes, buckets, c_ring, 20e-6)
-        nsim += 1
-        sim["threshold_" + ("inf" if thr >= 1 << 40 else str(thr))] = {"buckets": len(buckets), "step_us": tot * 1e6}
-    host_us = (time.perf_counter() - t0) / nsim * 1e6
-    rows["simulated_step_backward161"] = {
-        "compute_us": sum(op_time) * 1e6, "groups": len(op_time), "strategies": sim,
-        "best": min(sim, key=lambda k: sim[k]["step_us"]), "host_us_per_simulation": host_us,
-        "note": "op times: device time per launch of each group on this GPU (CUDA graph of 20 launches, CUDA "
-                "events); AllReduce model T = 2(N-1)x/(B N) + D, "
-                "N = 8, B = 900 GB/s, D = 20 us (assumed)"}
+        sim["one" if thr >= 1 << 40 else "per_tensor" if thr == 0 else str(thr >> 20) + "MiB"] = tot * 1e6
+    rows["sim161"] = {"compute_us": sum(op_time) * 1e6, "step_us": sim}
     del be
 
-    # sufficient-factor gradient + update: one tcgen05 GEMM-epilogue group
-    for B, label in ((512, "sf_update_K512"), (4096, "sf_update_K4096_compute_bound_variant")):
+    # sufficient-factor gradient + update: one tcgen05 GEMM-epilogue group,
+    # L2 flushed before each launch
+    for B, label in ((512, "sf_k512"), (4096, "sf_k4096")):
         sp = W.sf_update(B, 4096, 4096)
         p = graph_from_spec(sp).build()
         e = {}
@@ -788,14 +766,8 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
         medu, _ = timed(run_plan(p, sp, e, False))
         tflops = gi.alg_flops / (med * 1e-3) / 1e12
         gbps = gi.alg_bytes / (med * 1e-3) / 1e9
-        t_mem = gi.alg_bytes / (hbm * 1e9)
-        t_mma = gi.alg_flops / (bf16 * 1e12)
-        rows[label] = {"fused_us": med * 1e3, "unfused_us": medu * 1e3, "speedup_vs_unfused": medu / med,
-                       "TFLOPs": tflops, "frac_of_bf16_peak": tflops / bf16, "GBps": gbps, "frac_of_hbm": gbps / hbm,
-                       "roofline_floor_us": max(t_mem, t_mma) * 1e6,
-                       "frac_of_roofline": max(t_mem, t_mma) / (med * 1e-3),
-                       "bound": "hbm" if t_mem > t_mma else "tensor", "alg_flops": gi.alg_flops,
-                       "alg_bytes": gi.alg_bytes, "kernel": "fg_jit_gemm_group (tcgen05 cta_group::2, 256x256 tiles per CTA pair)"}
+        rows[label] = {"us": med * 1e3, "x": medu / med, "TFLOPs": tflops, "frac_bf16": tflops / bf16,
+                       "frac_hbm": gbps / hbm}
         del e
     torch.cuda.empty_cache()
 
@@ -808,13 +780,22 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
     medf, _ = timed(run_plan(p, sp, e, True), reps=3, flush=False)
     medu, _ = timed(run_plan(p, sp, e, False), reps=3, flush=False)
     alg = sum(gi.alg_bytes for gi in p.groups)
-    rows["random_dag_seed0"] = {"ops": len(sp.ops), "groups": p.n_groups, "fused_ms": medf,
-                                "unfused_ms": medu, "speedup_vs_unfused": medu / medf,
-                                "fused_alg_GBps": alg / (medf * 1e-3) / 1e9,
-                                "fused_alg_bytes": alg, "unfused_bytes": W.algorithmic_bytes_unfused(sp)}
+    rows["dag200"] = {"groups": p.n_groups, "ms": medf, "unf_ms": medu, "x": medu / medf,
+                      "frac": alg / (medf * 1e-3) / 1e9 / hbm}
     del e
     torch.cuda.empty_cache()
-    return rows
+    return {k: _round(v) for k, v in rows.items()}
+
+
+def _round(v):
+    """Three significant digits: the line stays short."""
+    if isinstance(v, dict):
+        return {k: _round(x) for k, x in v.items()}
+    if isinstance(v, list):
+        return [_round(x) for x in v]
+    if isinstance(v, float):
+        return float(f"{v:.3g}")
+    return v
 
 
 if __name__ == "__main__":
