@@ -84,6 +84,7 @@ struct GroupExec {
   int grid = 1, smem = 0;
   float* scratch = nullptr;
   int32_t* counters = nullptr;        // split arrival counters (zero between launches)
+  unsigned long long* sched = nullptr;   // K1 tile claim counter (see the kernel)
   size_t counter_bytes = 0;
   std::string compile_error;          // non-empty: cannot launch
   fg_status compile_status = FG_OK;
@@ -698,6 +699,14 @@ fg_status alloc_device(fg_plan* p, GroupExec& ge) {
   if (ge.compile_status != FG_OK || !ge.gp) return FG_OK;
   GroupParams& gp = *ge.gp;
   gp.err = p->d_err;
+  if (ge.cg.exec == FG_EXEC_ELEMWISE) {
+    // the claim counter of the tiles' dynamic distribution
+    cudaError_t e = cudaMalloc(&ge.sched, sizeof(unsigned long long));
+    if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(work counter)");
+    e = cudaMemset(ge.sched, 0, sizeof(unsigned long long));
+    if (e != cudaSuccess) return cuda_err(e, "cudaMemset(work counter)");
+    gp.sched = ge.sched;
+  }
   if (ge.cg.exec == FG_EXEC_REDUCE && gp.nsplit > 1) {
     cudaError_t e = cudaMalloc(&ge.scratch, sizeof(float) * (size_t)gp.nsplit * gp.FR);
     if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(reduce scratch)");
@@ -715,8 +724,10 @@ fg_status alloc_device(fg_plan* p, GroupExec& ge) {
 void free_exec(GroupExec& ge) {
   if (ge.scratch) cudaFree(ge.scratch);
   if (ge.counters) cudaFree(ge.counters);
+  if (ge.sched) cudaFree(ge.sched);
   ge.scratch = nullptr;
   ge.counters = nullptr;
+  ge.sched = nullptr;
 }
 
 // ---- tensor maps -----------------------------------------------------------
@@ -1189,10 +1200,13 @@ fg_status fg_sync_status(fg_plan* p, void* stream) {
   if (e != cudaSuccess) return cuda_err(e, "reading the device error flag");
   if (flag == 0) return FG_OK;
   cudaMemset(p->d_err, 0, sizeof(int32_t));
-  // a kernel that gave up may have left split arrival counters mid-count
+  // a kernel that gave up may have left split arrival counters mid-count and
+  // its claim counter off the launches' count
   for (auto* v : {&p->groups, &p->singles})
-    for (auto& ge : *v)
+    for (auto& ge : *v) {
       if (ge.counters) cudaMemset(ge.counters, 0, ge.counter_bytes);
+      if (ge.sched) cudaMemset(ge.sched, 0, sizeof(unsigned long long));
+    }
   if (flag == DEVERR_TIMEOUT) return err(FG_ETIMEOUT, "a device-side wait exceeded wait_limit_ns");
   return err(FG_EDEVICE, "device error flag " + std::to_string(flag));
 }

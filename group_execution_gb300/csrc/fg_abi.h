@@ -143,6 +143,8 @@ struct GroupParams {
   float* out;                          // output base (direct stores / reduce output)
   float* scratch;                      // reduce split partials [nsplit][FR]
   int32_t* counters;                   // reduce split arrival counters [ntr]
+  unsigned long long* sched;           // elementwise groups: tiles claimed by all launches (claim c: tile
+                                       // first + c mod ntiles)
   int32_t* err;                        // device error flag
   int64_t wait_limit_ns;
   int32_t nprog, nepi, nleaves, nstaged;

@@ -295,16 +295,6 @@ __device__ __forceinline__ void tile_coords(int t, int ntr, int ntc, int band, i
   tc = local / rows;
 }
 
-struct EwTiles {
-  int t, step, ntiles, ntr, ntc, band;
-  __device__ __forceinline__ bool next(int& tr, int& tc) {
-    if (t >= ntiles) return false;
-    tile_coords(t, ntr, ntc, band, tr, tc);
-    t += step;
-    return true;
-  }
-};
-
 struct RedTiles {   // units (row strip, column split), then the split's tiles
   int u, step, nunits, nsplit, tps, ntc;
   int tc, tc_end, strip;
@@ -324,8 +314,89 @@ struct RedTiles {   // units (row strip, column split), then the split's tiles
   }
 };
 
-// A producer: one thread issues the TMA loads of every staged leaf for the
-// tiles i = par, par + kProducerWarps, ... into the ring (a thread takes a few
+// Elementwise groups claim their tiles dynamically from the group's claim
+// counter (P.sched, 64 bits) with atomic adds.  SMs do not stream at the same
+// rate (with a fixed split of the tiles the slowest CTAs finished several
+// microseconds after the rest, the memory system half idle meanwhile);
+// claiming keeps every CTA busy until the tiles run out.  Each producer's
+// first tile is fixed (no launch-time rush on the counter); later tiles are
+// claimed, one claim ahead.  A launch makes exactly as many claims as it has
+// tiles (each producer with a valid first tile claims until one claim fails),
+// so the counter never needs resetting: claim c is tile first + c mod ntiles
+// of its launch.  (A launch that gave up on a bounded wait leaves the count
+// off; the host clears the counter when it reports the timeout.)  Producer p
+// fills the stages i with i % 2 == p (the ring depth is even, so each owns
+// half of the slots); each stage carries its tile row and column (-1: the
+// producer has no more tiles).
+__device__ __forceinline__ int claim_unit(unsigned long long* ctr, int first, int nunits) {
+  const unsigned long long c = atomicAdd(ctr, 1ull);
+  return first + (int)(c % (unsigned long long)nunits);
+}
+
+struct EwUnits {   // one tile per unit, in the tile walk's order
+  int nunits, ntr, ntc, band;
+  __device__ __forceinline__ int tiles(int) const { return 1; }
+  __device__ __forceinline__ void tile(int u, int, int& tr, int& tc) const { tile_coords(u, ntr, ntc, band, tr, tc); }
+};
+
+// An elementwise producer (one thread): claims tiles until they run out,
+// issues the TMA loads of every staged leaf of each into its stages (a thread
+// takes a few hundred ns to wait for a stage, arm it and issue its copies:
+// two producers keep more loads in flight), then marks its last stage.  The
+// next claim is in flight while the current tile is issued.  On a timeout it
+// waits for its loads still in flight.
+template <class Prog, class Units>
+__device__ __forceinline__ void ew_producer(const GroupParams& P, const typename Prog::Tables& T, const Ring& R,
+                                            int2* info, const Units U, volatile int* abort_flag, int par) {
+  if (P.inject) return;   // failure injection: consumers wait for loads that never come
+  Prog::prefetch(P, T);
+  const int NS = P.nstages;
+  int i = par;
+  bool ok = true;
+  // the first tile of each producer is fixed (no launch-time rush on the
+  // counter); claims number the tiles after those
+  const int first = 2 * (int)gridDim.x;
+  int next = 2 * (int)blockIdx.x + par;
+  for (;;) {
+    const int u = next;
+    if (u >= U.nunits) break;
+    next = claim_unit(P.sched, first, U.nunits);
+    const int nt = U.tiles(u);
+    for (int k = 0; k < nt && ok; ++k, i += kProducerWarps) {
+      const int s = i % NS;
+      if (i >= NS && !wait_or_abort(R.empty_s + 8 * s, ((i / NS) & 1) ^ 1, P.wait_limit_ns, abort_flag)) {
+        ok = false;
+        break;
+      }
+      int tr, tc;
+      U.tile(u, k, tr, tc);
+      info[s] = make_int2(tr, tc);
+      const uint32_t bar = R.full_s + 8 * s;
+      mbar_expect_tx(bar, P.tx_bytes);
+      Prog::issue(P, T, R.base_s + s * P.stage_bytes, bar, tr * kTileR, tc * kTileC);
+    }
+    if (!ok) break;
+  }
+  if (ok) {
+    const int s = i % NS;
+    if (i >= NS && !wait_or_abort(R.empty_s + 8 * s, ((i / NS) & 1) ^ 1, P.wait_limit_ns, abort_flag)) {
+      ok = false;
+    } else {
+      info[s] = make_int2(-1, 0);
+      mbar_arrive(R.full_s + 8 * s);
+    }
+  }
+  if (!ok) {
+    *abort_flag = 1;
+    set_error(P.err, DEVERR_TIMEOUT);
+    const int64_t drain = P.wait_limit_ns > kDrainLimitNs ? P.wait_limit_ns : kDrainLimitNs;
+    for (int k = i - NS < 0 ? 0 : i - NS; k < i; ++k)
+      if (k % kProducerWarps == par) mbar_wait(R.full_s + 8 * (k % NS), (k / NS) & 1, drain);
+  }
+}
+
+// A reduce producer: one thread issues the TMA loads of every staged leaf for
+// the tiles i = par, par + kProducerWarps, ... into the ring (a thread takes a few
 // hundred ns to wait for a stage, arm it and issue its copies: two producers
 // keep more loads in flight); on a timeout it waits for its loads still in
 // flight.  With at least two stages, each producer's previous wait ensures the
@@ -369,6 +440,7 @@ __device__ __forceinline__ void ew_body(const GroupParams& P) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ int abort_flag;
   __shared__ typename Prog::Tables T;
+  __shared__ int2 info[kMaxStages];
   uint8_t* smem = align1024(smem_raw);
   const Ring R = setup_ring(smem);
   uint8_t* outbuf = R.base + P.nstages * P.stage_bytes;
@@ -386,98 +458,110 @@ __device__ __forceinline__ void ew_body(const GroupParams& P) {
 
   if (warp >= kConsumerWarps) {
     if (lane == 0)
-      producer_loop<Prog>(P, T, R, EwTiles{(int)blockIdx.x, (int)gridDim.x, P.ntiles, P.ntr, P.ntc, P.band},
-                          &abort_flag, warp - kConsumerWarps);
-    return;
-  }
-
-  const int NS = P.nstages;
-  const int lr = lane, lc0 = warp * 8;
-  const bool vec_store = (P.FC & 3) == 0 && (reinterpret_cast<uintptr_t>(P.out) & 15) == 0;
-  float o[8];
-  int i = 0;
-  for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x, ++i) {
-    const int s = i % NS;
-    int tr, tc;
-    tile_coords(t, P.ntr, P.ntc, P.band, tr, tc);
-    const int r0 = tr * kTileR, c0 = tc * kTileC;
-    const bool got = wait_or_abort(R.full_s + 8 * s, (i / NS) & 1, P.wait_limit_ns, &abort_flag);
-    uint8_t* ob = outbuf + (i % 3) * kOutBufBytes;
-    if (got) {
-      const TileEnv te{P, R.base + s * P.stage_bytes, lr, lc0, r0, c0,
-                       P.xout_tma ? xbuf + ((i % 3) * P.nxout * 8 + warp) * (kTileR * 32) : nullptr};
-      Prog::run(te, T, P, o);
-      if (P.out_tma == 1) {
-        uint8_t* b = ob + (lc0 >> 5) * (kTileR * 128);
-        const int j0 = (lc0 & 31) >> 2;
-        *reinterpret_cast<float4*>(b + swz(lr, j0)) = make_float4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<float4*>(b + swz(lr, j0 + 1)) = make_float4(o[4], o[5], o[6], o[7]);
-      } else if (P.out_tma == 2) {
-        // this warp's 32 x 8 slice, row-major, stored by its own lane 0
-        float4* b = reinterpret_cast<float4*>(ob + warp * (kTileR * 32) + lr * 32);
-        b[0] = make_float4(o[0], o[1], o[2], o[3]);
-        b[1] = make_float4(o[4], o[5], o[6], o[7]);
-      } else {
-        // each lane writes 32 contiguous bytes of its row: whole sectors
-        const int r = r0 + lr, c = c0 + lc0;
-        if (r < P.FR) {
-          float* op = P.out + (int64_t)r * P.FC + c;
-          if (vec_store && c + 8 <= P.FC) {
-            reinterpret_cast<float4*>(op)[0] = make_float4(o[0], o[1], o[2], o[3]);
-            reinterpret_cast<float4*>(op)[1] = make_float4(o[4], o[5], o[6], o[7]);
-          } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              if (c + k < P.FC) op[k] = o[k];
-          }
-        }
+      ew_producer<Prog>(P, T, R, info, EwUnits{P.ntiles, P.ntr, P.ntc, P.band}, &abort_flag,
+                          warp - kConsumerWarps);
+  } else {
+    const int NS = P.nstages;
+    const int lr = lane, lc0 = warp * 8;
+    const bool vec_store = (P.FC & 3) == 0 && (reinterpret_cast<uintptr_t>(P.out) & 15) == 0;
+    float o[8];
+    static_assert(kProducerWarps == 2, "two producers, owning the even and the odd stages");
+    bool fin0 = false, fin1 = false;   // producers whose last stage has been seen
+    for (int i = 0; !(fin0 && fin1); ++i) {
+      if (i & 1 ? fin1 : fin0) continue;
+      const int s = i % NS;
+      const bool got = wait_or_abort(R.full_s + 8 * s, (i / NS) & 1, P.wait_limit_ns, &abort_flag);
+      const int2 inf = got ? info[s] : make_int2(0, 0);
+      if (inf.x < 0) {
+        // that producer has no more tiles (every warp that waited reads the
+        // same stage).  With the CTA-wide store every warp takes exactly one
+        // barrier per stage it waits for, this one included, so that a warp
+        // that gave up on it meets the others there
+        if (P.out_tma == 1 && consumer_bar_or(false)) break;
+        if (i & 1) fin1 = true;
+        else fin0 = true;
+        continue;
       }
-    } else {
-      abort_flag = 1;
-      set_error(P.err, DEVERR_TIMEOUT);
-    }
-    if (P.out_tma == 2) {
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(R.empty_s + 8 * s);
-        if (got && c0 + lc0 < P.FC) {
-          tma_store_2d(&P.maps[kMaxStaged], c0 + lc0, r0, smem_u32(ob + warp * (kTileR * 32)));
-          if (P.xout_tma) {
-            const uint8_t* xw = xbuf + ((i % 3) * P.nxout * 8 + warp) * (kTileR * 32);
-            for (int j = 0; j < P.nxout; ++j) {
-              if (P.xout[j].cls == LEAF_IDENT)
-                tma_store_2d(&P.xmaps[j], c0 + lc0, r0, smem_u32(xw + j * kXOutSliceBytes));
-              else
-                tma_store_2d(&P.xmaps[j], r0, c0 + lc0, smem_u32(xw + j * kXOutSliceBytes));
+      const int r0 = inf.x * kTileR, c0 = inf.y * kTileC;   // the tile's row and column tiles
+      uint8_t* ob = outbuf + (i % 3) * kOutBufBytes;
+      if (got) {
+        const TileEnv te{P, R.base + s * P.stage_bytes, lr, lc0, r0, c0,
+                         P.xout_tma ? xbuf + ((i % 3) * P.nxout * 8 + warp) * (kTileR * 32) : nullptr};
+        Prog::run(te, T, P, o);
+        if (P.out_tma == 1) {
+          uint8_t* b = ob + (lc0 >> 5) * (kTileR * 128);
+          const int j0 = (lc0 & 31) >> 2;
+          *reinterpret_cast<float4*>(b + swz(lr, j0)) = make_float4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<float4*>(b + swz(lr, j0 + 1)) = make_float4(o[4], o[5], o[6], o[7]);
+        } else if (P.out_tma == 2) {
+          // this warp's 32 x 8 slice, row-major, stored by its own lane 0
+          float4* b = reinterpret_cast<float4*>(ob + warp * (kTileR * 32) + lr * 32);
+          b[0] = make_float4(o[0], o[1], o[2], o[3]);
+          b[1] = make_float4(o[4], o[5], o[6], o[7]);
+        } else {
+          // each lane writes 32 contiguous bytes of its row: whole sectors
+          const int r = r0 + lr, c = c0 + lc0;
+          if (r < P.FR) {
+            float* op = P.out + (int64_t)r * P.FC + c;
+            if (vec_store && c + 8 <= P.FC) {
+              reinterpret_cast<float4*>(op)[0] = make_float4(o[0], o[1], o[2], o[3]);
+              reinterpret_cast<float4*>(op)[1] = make_float4(o[4], o[5], o[6], o[7]);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                if (c + k < P.FC) op[k] = o[k];
             }
           }
+        }
+      } else {
+        abort_flag = 1;
+        set_error(P.err, DEVERR_TIMEOUT);
+      }
+      if (P.out_tma == 2) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(R.empty_s + 8 * s);
+          if (got && c0 + lc0 < P.FC) {
+            tma_store_2d(&P.maps[kMaxStaged], c0 + lc0, r0, smem_u32(ob + warp * (kTileR * 32)));
+            if (P.xout_tma) {
+              const uint8_t* xw = xbuf + ((i % 3) * P.nxout * 8 + warp) * (kTileR * 32);
+              for (int j = 0; j < P.nxout; ++j) {
+                if (P.xout[j].cls == LEAF_IDENT)
+                  tma_store_2d(&P.xmaps[j], c0 + lc0, r0, smem_u32(xw + j * kXOutSliceBytes));
+                else
+                  tma_store_2d(&P.xmaps[j], r0, c0 + lc0, smem_u32(xw + j * kXOutSliceBytes));
+              }
+            }
+            bulk_commit();
+            bulk_wait_read<1>();
+          }
+        }
+        __syncwarp();
+        if (!got) break;
+        continue;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(R.empty_s + 8 * s);
+      if (P.out_tma == 1) {
+        // every consumer warp reaches this barrier once per tile it waited
+        // for: one that gave up leaves together with the others
+        fence_proxy_async_smem();
+        if (consumer_bar_or(!got)) break;
+        if (threadIdx.x == 0) {
+          const uint32_t src = smem_u32(ob);
+          tma_store_2d(&P.maps[kMaxStaged], c0, r0, src);
+          if (c0 + 32 < P.FC) tma_store_2d(&P.maps[kMaxStaged], c0 + 32, r0, src + kTileR * 128);
           bulk_commit();
           bulk_wait_read<1>();
         }
+      } else if (!got) {
+        break;
       }
-      __syncwarp();
-      if (!got) break;
-      continue;
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(R.empty_s + 8 * s);
-    if (P.out_tma == 1) {
-      fence_proxy_async_smem();
-      if (consumer_bar_or(!got)) break;
-      if (threadIdx.x == 0) {
-        const uint32_t src = smem_u32(ob);
-        tma_store_2d(&P.maps[kMaxStaged], c0, r0, src);
-        if (c0 + 32 < P.FC) tma_store_2d(&P.maps[kMaxStaged], c0 + 32, r0, src + kTileR * 128);
-        bulk_commit();
-        bulk_wait_read<1>();
-      }
-    } else if (!got) {
-      break;
-    }
+    if (P.out_tma == 1 && threadIdx.x == 0) bulk_wait<0>();
+    if (P.out_tma == 2 && lane == 0) bulk_wait<0>();
   }
-  if (P.out_tma == 1 && threadIdx.x == 0) bulk_wait<0>();
-  if (P.out_tma == 2 && lane == 0) bulk_wait<0>();
 }
 
 // A consumer warp of a reduce CTA, once the count of a split unit of `strip` has

@@ -744,7 +744,8 @@ void plan_staging(const Graph& g, CompiledGroup& cg, const BuildOpts& o) {
   }
   if (!gemm) {
     int ns = cg.stage_bytes ? (budget - fixed) / cg.stage_bytes : 4;
-    cg.nstages = std::max(2, std::min(ns, kMaxStages));
+    // an even depth: each of the two producers owns every other ring slot
+    cg.nstages = std::max(2, std::min(ns, kMaxStages)) & ~1;
     cg.smem_bytes = fixed + cg.nstages * cg.stage_bytes;
     cg.ctas_per_sm = budget == budget_two ? 2 : 1;
   }

@@ -245,7 +245,8 @@ const char* fg_last_error(void);
  * may imply -- and so cannot build a plan either.  The pages have no
  * counterpart of this entry point.  It runs the reduce-group kernel on a
  * one-operator program with its scratch (per-split partial row values and
- * arrival counters) in a 4 MiB + 8 KiB file-scope device array that every
+ * arrival counters, and an error word) in a file-scope device array of
+ * 4 MiB + 8 KiB + 256 bytes that every
  * GPU which loads the library holds until the process exits.
  * Limits: rows <= 65536 (else FG_EINVAL) and rows*cols < 2^31 (else
  * FG_ESHAPE).  x (16-byte aligned) and y (4-byte aligned) are device
