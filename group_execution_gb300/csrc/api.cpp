@@ -127,7 +127,52 @@ struct tf_layout {
   int32_t nb = 0;
   int32_t* d_bucket = nullptr;
   uint32_t seq = 0;
+  // the table's users: per stream, an event recorded after the last pack or
+  // stream wait enqueued there that reads the table
+  std::vector<std::pair<cudaStream_t, cudaEvent_t>> users;
+  // tables replaced while a launch or wait might still read them, freed once
+  // their users' events have completed
+  struct Retired {
+    int32_t* table;
+    std::vector<std::pair<cudaStream_t, cudaEvent_t>> users;
+  };
+  std::vector<Retired> retired;
 };
+
+namespace {
+// Records on `st` that the current bucket table is read by work enqueued
+// there (one event per stream, re-recorded).
+cudaError_t note_table_use(tf_layout* l, cudaStream_t st) {
+  for (auto& u : l->users)
+    if (u.first == st) return cudaEventRecord(u.second, st);
+  cudaEvent_t ev;
+  cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+  if (e != cudaSuccess) return e;
+  l->users.emplace_back(st, ev);
+  return cudaEventRecord(ev, st);
+}
+
+// Frees the replaced tables whose users have all finished (wait = block
+// until they have).
+void free_retired(tf_layout* l, bool wait) {
+  std::vector<tf_layout::Retired> keep;
+  for (auto& r : l->retired) {
+    bool done = true;
+    for (auto& u : r.users) {
+      const cudaError_t q = wait ? cudaEventSynchronize(u.second) : cudaEventQuery(u.second);
+      if (q == cudaErrorNotReady) done = false;
+    }
+    if (!done) {
+      keep.push_back(std::move(r));
+      continue;
+    }
+    for (auto& u : r.users) cudaEventDestroy(u.second);
+    cudaFree(r.table);
+  }
+  l->retired.swap(keep);
+  cudaGetLastError();   // a not-ready query is not an error of the caller's
+}
+}  // namespace
 
 // cuStreamWaitValue32 through the runtime's driver entry point (no link
 // against the driver library).
@@ -1332,10 +1377,12 @@ fg_status tf_layout_set_buckets(tf_layout* l, int32_t nb, const int32_t* bounds)
     return cuda_err(e, "cudaMemcpy(bucket table)");
   }
   if (l->d_bucket) {
-    // an earlier table may still be read by a launch in flight
-    cudaDeviceSynchronize();
-    cudaFree(l->d_bucket);
+    // an earlier table may still be read by a pack or a stream wait in
+    // flight: it is freed once the events recorded after them have completed
+    l->retired.push_back(tf_layout::Retired{l->d_bucket, std::move(l->users)});
+    l->users.clear();
   }
+  free_retired(l, false);
   l->d_bucket = d;
   l->nb = nb;
   l->seq = 0;
@@ -1358,10 +1405,12 @@ fg_status tf_pack_buckets(tf_layout* l, float scale, void* buf, void* stream) {
                                  static_cast<cudaStream_t>(stream), bk);
   if (e != cudaSuccess) return cuda_err(e, "tf_pack_buckets launch");
   l->seq = bk.seq;
+  e = note_table_use(l, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_err(e, "cudaEventRecord(bucket table use)");
   return FG_OK;
 }
 
-fg_status tf_bucket_wait(const tf_layout* l, int32_t b, void* stream) {
+fg_status tf_bucket_wait(tf_layout* l, int32_t b, void* stream) {
   if (!l) return err(FG_EINVAL, "null argument");
   if (!l->nb || !l->seq) return err(FG_EINVAL, "no bucketed pack has been enqueued");
   if (b < 0 || b >= l->nb) return err(FG_EINVAL, "bucket out of range");
@@ -1370,6 +1419,8 @@ fg_status tf_bucket_wait(const tf_layout* l, int32_t b, void* stream) {
   const int32_t* ready = l->d_bucket + l->nchunks + 2 * l->nb + b;
   CUresult r = fn(static_cast<CUstream>(stream), reinterpret_cast<CUdeviceptr>(ready), l->seq, CU_STREAM_WAIT_VALUE_GEQ);
   if (r != CUDA_SUCCESS) return err(FG_ECUDA, "cuStreamWaitValue32 failed (" + std::to_string((int)r) + ")");
+  const cudaError_t e = note_table_use(l, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_err(e, "cudaEventRecord(bucket table use)");
   return FG_OK;
 }
 
@@ -1439,8 +1490,9 @@ fg_status tf_sync_status(tf_layout* l, void* stream) {
 
 void tf_layout_destroy(tf_layout* l) {
   if (!l) return;
+  if (l->d_bucket) l->retired.push_back(tf_layout::Retired{l->d_bucket, std::move(l->users)});
+  free_retired(l, true);
   if (l->d_chunks) cudaFree(l->d_chunks);
-  if (l->d_bucket) cudaFree(l->d_bucket);
   delete l;
 }
 

@@ -28,9 +28,13 @@
  *     fusion buffer 256-byte aligned).  CUDA launch errors map to FG_ECUDA.
  *     Errors found on the device (a bounded wait that expired) are latched in
  *     the plan's device flag and reported by fg_sync_status.
- *   - A plan is immutable after build.  Launches of one plan must be ordered
- *     on one stream (reduce groups use plan-owned scratch); use one plan per
- *     stream for concurrency.
+ *   - A plan is immutable after build.  Launches of one plan must be ordered:
+ *     on one stream, or on streams ordered by events (each group owns small
+ *     device state that a launch uses from start to end: the tile claim
+ *     counter of an elementwise group, the split partials and arrival
+ *     counters of a reduce group, the split workspace of a GEMM group).
+ *     Plans are independent of each other: for concurrent launches, build one
+ *     plan per stream (the compiled kernels are shared).
  *   - No CPU fallback exists: without a CUDA device every launch returns
  *     FG_ECUDA.  Graph building and grouping are host-only and work without a
  *     device.
@@ -438,10 +442,12 @@ fg_status tf_unpack_range(const tf_layout* l, int32_t first, int32_t count, floa
  * tf_layout_set_buckets: the bucket table, bounds[0 .. n_buckets] as
  * tf_plan_threshold writes it (bounds[0] = 0, strictly increasing,
  * bounds[n_buckets] = the layout's tensor count; host, caller-owned, copied).
- * Replaces an earlier table (after a device-wide synchronize, since a launch
- * in flight may still read it); allocates the per-bucket device words (chunk
- * counters and ready words) and restarts the sequence numbers, so call it
- * between steps, not while a bucket wait is pending.  FG_EINVAL for a
+ * Replaces an earlier table without synchronizing: the old table stays
+ * allocated until the events recorded after every pack and stream wait that
+ * read it have completed (checked at the next replacement, waited for by
+ * tf_layout_destroy).  Allocates the per-bucket device words (chunk counters
+ * and ready words) and restarts the sequence numbers, so call it between
+ * steps: a wait enqueued afterwards refers to the new table.  FG_EINVAL for a
  * malformed table.
  *
  * tf_pack_buckets: packs every tensor in one launch, with tf_pack's result,
@@ -466,7 +472,7 @@ fg_status tf_unpack_range(const tf_layout* l, int32_t first, int32_t count, floa
  * streams that wait for each other): they share the bucket counters. */
 fg_status tf_layout_set_buckets(tf_layout* l, int32_t n_buckets, const int32_t* bounds);
 fg_status tf_pack_buckets(tf_layout* l, float scale, void* fusion_buf, void* cuda_stream);
-fg_status tf_bucket_wait(const tf_layout* l, int32_t bucket, void* cuda_stream);
+fg_status tf_bucket_wait(tf_layout* l, int32_t bucket, void* cuda_stream);
 fg_status tf_bucket_ready(const tf_layout* l, int32_t bucket, int32_t* ready);
 
 void tf_layout_destroy(tf_layout* l);
