@@ -511,9 +511,9 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
             ts.append(a.elapsed_time(b) / inner)
         return statistics.median(ts), min(ts)
 
-    def graphed(fn):
-        """The launches of fn captured once into a CUDA graph and replayed:
-        device time without per-launch host work."""
+    def graphed(fn, n=1):
+        """n runs of fn's launches captured once into a CUDA graph and
+        replayed: device time without per-launch host work."""
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
@@ -522,7 +522,8 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            fn()
+            for _ in range(n):
+                fn()
         return g.replay
 
     def run_plan(p, sp, env, fused=True):
@@ -558,8 +559,9 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
     rows["diamond"] = {"us": med_f * 1e3, "unf_us": med_u * 1e3, "x": med_u / med_f,
                        "frac": plan.groups[0].alg_bytes / (med_f * 1e-3) / 1e9 / hbm}
 
-    # RNNLM chain, both partitions (launch-bound by construction): L2 flushed
-    # before each launch, and replayed from a CUDA graph (no host work)
+    # RNNLM chain, both partitions (launch-bound by construction): one run
+    # after an L2 flush (us), and 20 runs back to back replayed from a CUDA
+    # graph, per run (graph_us: no host work between launches)
     for epi in (False, True):
         sp = W.rnnlm_chain()
         p = graph_from_spec(sp).build(allow_reduce_epilogue=epi)
@@ -570,8 +572,9 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
             e.setdefault(v.vid, torch.empty(v.shape, device="cuda"))
         med, mn = timed(run_plan(p, sp, e, True))
         medu, _ = timed(run_plan(p, sp, e, False))
-        gmed, _ = timed(graphed(run_plan(p, sp, e, True)), flush=False)
-        gmedu, _ = timed(graphed(run_plan(p, sp, e, False)), flush=False)
+        gmed, _ = timed(graphed(run_plan(p, sp, e, True), 20), flush=False, inner=1)
+        gmedu, _ = timed(graphed(run_plan(p, sp, e, False), 20), flush=False, inner=1)
+        gmed, gmedu = gmed / 20, gmedu / 20
         rows["rnnlm_" + ("1g" if epi else "2g")] = {
             "us": med * 1e3, "unf_us": medu * 1e3, "graph_us": gmed * 1e3, "graph_unf_us": gmedu * 1e3}
 

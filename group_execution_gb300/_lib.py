@@ -20,6 +20,7 @@ FG_OK, FG_EINVAL, FG_ESHAPE, FG_EUNSUPPORTED, FG_ENOMEM, FG_ECUDA, FG_ETIMEOUT, 
 FG_F32, FG_BF16 = 0, 1
 FG_FLAG_INTERPRET = 1 << 26
 FG_FLAG_INJECT_NO_LOADS = 1 << 27
+FG_FLAG_NO_SMALL = 1 << 28          # small groups too run the pipelined kernels
 STATUS_NAMES = ["FG_OK", "FG_EINVAL", "FG_ESHAPE", "FG_EUNSUPPORTED", "FG_ENOMEM", "FG_ECUDA",
                 "FG_ETIMEOUT", "FG_EDEVICE"]
 

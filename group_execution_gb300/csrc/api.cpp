@@ -91,6 +91,9 @@ struct GroupExec {
   bool compiled = false;              // run the compiled program (else the interpreter)
   int min_blocks = 2;                 // CTAs per SM the kernel is built for
   void* fn = nullptr;                 // compiled kernel
+  bool small = false;                 // run the small-group kernel instead (direct reads, no ring)
+  int grid_small = 1;
+  void* fn_small = nullptr;
   std::vector<const void*> last_ptrs; // tensor-map cache key
 };
 }  // namespace
@@ -501,6 +504,16 @@ void prepare_group(GroupExec& ge, const BuildOpts& o, int nsm) {
   } else {
     ge.grid = std::max(1, std::min(p.ntiles, ctas * nsm));
   }
+  // Small groups run a kernel without the shared-memory pipeline: one warp
+  // per frame row reading its leaves straight from global memory (compiled
+  // programs without extra outputs or shifted tuple fields; not with the
+  // failure-injection hook, whose point is the pipeline's bounded waits).
+  // Flag bit 28 turns it off.
+  bool shifted = false;
+  for (const LeafUse& l : cg.leaves) shifted |= l.map.shift != 0;
+  ge.small = ge.compiled && cg.alg_bytes <= kSmallGroupBytes && cg.xout_values.empty() && !shifted &&
+             !(o.flags & FG_FLAG_INJECT_NO_LOADS) && !(o.flags & FG_FLAG_NO_SMALL);
+  ge.grid_small = (int)std::max<int64_t>(1, (cg.FR + kSmallThreads / 32 - 1) / (kSmallThreads / 32));
 }
 
 int gemm_box_bytes(int cls) {
@@ -959,7 +972,9 @@ fg_status launch_exec(fg_plan* p, GroupExec& ge, void* const* ptrs, void* stream
     }
     ge.last_ptrs = key;
   }
-  cudaError_t e = ge.fn ? jit_launch(ge.fn, gp, ge.grid, ge.smem, static_cast<cudaStream_t>(stream))
+  cudaError_t e = ge.small && ge.fn_small
+                      ? jit_launch_any(ge.fn_small, &gp, ge.grid_small, kSmallThreads, 0, static_cast<cudaStream_t>(stream))
+                  : ge.fn ? jit_launch(ge.fn, gp, ge.grid, ge.smem, static_cast<cudaStream_t>(stream))
                         : launch_group_kernel(gp, cg.exec == FG_EXEC_REDUCE ? 1 : 0, ge.big ? 1 : 0, ge.grid,
                                               ge.smem, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
@@ -1010,13 +1025,16 @@ fg_status build_plan(const Graph& g, const BuildOpts& o, const std::vector<std::
       for (auto& ge : *v)
         if (ge.compile_status == FG_OK && (ge.gp || ge.mp) && ge.compiled) {
           todo.push_back(&ge);
-          srcs.push_back(jit_source(ge.cg, ge.min_blocks));
+          srcs.push_back(jit_source(ge.cg, ge.min_blocks, ge.small));
         }
     if (!todo.empty()) {
-      std::vector<void*> fns;
-      std::string msg = jit_compile(srcs, fns);
+      std::vector<void*> fns, smalls;
+      std::string msg = jit_compile(srcs, fns, &smalls);
       if (!msg.empty()) return err(FG_ECUDA, msg);
-      for (size_t i = 0; i < todo.size(); ++i) todo[i]->fn = fns[i];
+      for (size_t i = 0; i < todo.size(); ++i) {
+        todo[i]->fn = fns[i];
+        todo[i]->fn_small = smalls[i];
+      }
     }
   }
   *out = p.release();
@@ -1213,7 +1231,7 @@ fg_status fg_plan_group_source(const fg_plan* p, int32_t gid, char* buf, int64_t
   const GroupExec& ge = p->groups[gid];
   if (ge.compile_status != FG_OK) return err(ge.compile_status, ge.compile_error);
   if (!ge.gp && !ge.mp) return err(FG_EUNSUPPORTED, "no compiled program for this group kind");
-  const std::string src = jit_source(ge.cg, ge.min_blocks);
+  const std::string src = jit_source(ge.cg, ge.min_blocks, ge.small);
   if (len_out) *len_out = (int64_t)src.size();
   if (buf && cap > 0) {
     const size_t n = std::min<size_t>(src.size(), (size_t)cap - 1);

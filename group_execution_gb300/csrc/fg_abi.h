@@ -131,6 +131,8 @@ constexpr int kTileC = 64;
 constexpr int kConsumerWarps = 8;
 constexpr int kProducerWarps = 2;     // group kernels: TMA producers taking alternate tiles
 constexpr int kMaxStages = 16;
+constexpr int kSmallThreads = 128;     // small-group kernel: four warps, one frame row each
+constexpr int64_t kSmallGroupBytes = 2 << 20;   // groups of at most this many algorithmic bytes run it
 
 enum RedOp : int { RED_NONE = 0, RED_SUM = 1, RED_MAX = 2 };
 

@@ -158,6 +158,58 @@ struct TileEnv {
   }
 };
 
+// ---- small groups: leaf reads straight from global memory -----------------------
+// One thread's eight frame points (r0, c0 .. c0+7); lr = lc0 = 0 keep the
+// select expressions of compiled programs valid (they test te.r0 + te.lr and
+// te.c0 + te.lc0 + k).
+struct DirectEnv {
+  const GroupParams& P;
+  int r0, lr, c0, lc0;
+
+  __device__ __forceinline__ void ident_l(int l, float (&t)[8]) const {
+    const float* p = P.leaves[l].ptr + (int64_t)r0 * P.FC + c0;
+    if (c0 + 8 <= P.FC && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+      const float4 a = __ldg(reinterpret_cast<const float4*>(p)), c = __ldg(reinterpret_cast<const float4*>(p) + 1);
+      t[0] = a.x; t[1] = a.y; t[2] = a.z; t[3] = a.w;
+      t[4] = c.x; t[5] = c.y; t[6] = c.z; t[7] = c.w;
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) t[k] = c0 + k < P.FC ? __ldg(p + k) : 0.f;
+    }
+  }
+  // the leaf is the transposed value, [FC, FR]
+  __device__ __forceinline__ void trans_l(int l, float (&t)[8]) const {
+    const float* p = P.leaves[l].ptr + r0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t[k] = c0 + k < P.FC ? __ldg(p + (int64_t)(c0 + k) * P.FR) : 0.f;
+  }
+  __device__ __forceinline__ void col_l(int l, float (&t)[8]) const {
+    const float* p = P.leaves[l].ptr + c0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t[k] = c0 + k < P.FC ? __ldg(p + k) : 0.f;
+  }
+  __device__ __forceinline__ void row_l(int l, float (&t)[8]) const {
+    const float v = __ldg(P.leaves[l].ptr + r0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t[k] = v;
+  }
+  // f = sum_k ((g / d_k) % m_k) * s_k over g = r*FC + c (small frames)
+  __device__ __forceinline__ void gather(int leaf, float (&t)[8]) const {
+    const LeafDesc& G = P.leaves[leaf];
+#pragma unroll 1
+    for (int k = 0; k < 8; ++k) {
+      float v = 0.f;
+      if (c0 + k < P.FC) {
+        const uint32_t g = (uint32_t)r0 * (uint32_t)P.FC + (uint32_t)(c0 + k);
+        uint32_t f = 0;
+        for (int q = 0; q < G.nterms; ++q) f += ((g / (uint32_t)G.d[q]) % (uint32_t)G.m[q]) * (uint32_t)G.s[q];
+        v = __ldg(G.ptr + f);
+      }
+      t[k] = v;
+    }
+  }
+};
+
 // Issues the TMA loads of one staged leaf for the tile at (r0, c0).
 __device__ __forceinline__ void issue_leaf(const CUtensorMap* m, int cls, uint32_t dst, uint32_t bar, int r0, int c0) {
   if (cls == LEAF_IDENT) {
@@ -695,6 +747,64 @@ __device__ __forceinline__ void reduce_body(const GroupParams& P) {
     }
   }
   if (pend_strip >= 0 && !dead) reduce_finish<Prog>(P, T, pend_strip, pend_old, is_sum);
+}
+
+// ---------------------------------------------------------------------------------
+// Small groups (a couple of MB of leaves and output at most), elementwise or
+// ending in a row reduction: one warp per frame row, eight consecutive frame
+// columns per lane and pass, leaves read straight from global memory.  No
+// shared-memory ring, no split of a row across CTAs, no barrier: a launch
+// costs little more than one round trip to memory, where the pipelined
+// kernels' set-up (barriers, descriptor fetches, split combines) is several.
+// A reduction folds each lane's values in order, then the lanes in a fixed
+// butterfly; lane 0 applies the epilogue.
+template <class Prog>
+__device__ __forceinline__ void small_body(const GroupParams& P) {
+  pdl_launch_dependents();
+  pdl_wait();   // the previous grid's writes are visible from here on
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * (int)(blockDim.x >> 5) + (int)(threadIdx.x >> 5);
+  if (r >= P.FR) return;
+  const bool red = P.red_op != RED_NONE, is_sum = P.red_op == RED_SUM;
+  const float init = is_sum ? 0.f : neg_inf();
+  float acc = init;
+#pragma unroll 2
+  for (int c = lane * 8; c < P.FC; c += 32 * 8) {
+    const DirectEnv te{P, r, 0, c, 0};
+    float o[8];
+    Prog::run_direct(te, o);
+    if (red) {
+      float v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = c + k < P.FC ? o[k] : init;
+      if (is_sum) {
+        acc = __fadd_rn(acc, __fadd_rn(__fadd_rn(__fadd_rn(v[0], v[1]), __fadd_rn(v[2], v[3])),
+                                       __fadd_rn(__fadd_rn(v[4], v[5]), __fadd_rn(v[6], v[7]))));
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc = fmaxf(acc, v[k]);
+      }
+    } else {
+      float* op = P.out + (int64_t)r * P.FC + c;
+      if (c + 8 <= P.FC && (reinterpret_cast<uintptr_t>(op) & 15) == 0) {
+        reinterpret_cast<float4*>(op)[0] = make_float4(o[0], o[1], o[2], o[3]);
+        reinterpret_cast<float4*>(op)[1] = make_float4(o[4], o[5], o[6], o[7]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (c + k < P.FC) op[k] = o[k];
+      }
+    }
+  }
+  if (red) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+      const float x = __shfl_xor_sync(0xffffffffu, acc, d);
+      acc = is_sum ? __fadd_rn(acc, x) : fmaxf(acc, x);
+    }
+    const typename Prog::Tables T{};
+    if (lane == 0) P.out[r] = Prog::epi(P, T, r, acc);
+  }
 }
 
 }  // namespace fg

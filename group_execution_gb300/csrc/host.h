@@ -115,6 +115,7 @@ struct CompiledGroup {
 
 constexpr int FG_FLAG_INTERPRET = 1 << 26;   // run group programs on the interpreter
 constexpr int FG_FLAG_INJECT_NO_LOADS = 1 << 27;   // failure injection for tests
+constexpr int FG_FLAG_NO_SMALL = 1 << 28;          // small groups too run the pipelined kernels
 
 struct BuildOpts {
   int max_fused_ops = 256, max_args = 64, allow_reduce_epilogue = 0;

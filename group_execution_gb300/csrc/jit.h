@@ -12,10 +12,14 @@ namespace fg {
 
 bool jit_available();
 // CUDA source of a group's kernel; min_blocks is the kernel's CTAs-per-SM bound.
-std::string jit_source(const CompiledGroup& cg, int min_blocks);
+// small = also the small-group kernel (direct leaf reads), fg_jit_small_group
+std::string jit_source(const CompiledGroup& cg, int min_blocks, bool small = false);
 // Compiles (once per process per distinct source) and loads; returns "" or an
 // error message.  funcs[i] is the loaded kernel of sources[i].
-std::string jit_compile(const std::vector<std::string>& sources, std::vector<void*>& funcs);
+std::string jit_compile(const std::vector<std::string>& sources, std::vector<void*>& funcs,
+                        std::vector<void*>* small_funcs = nullptr);
+// One launch of a compiled kernel with `params` as its only argument.
+cudaError_t jit_launch_any(void* func, void* params, int grid, int threads, int smem, cudaStream_t st);
 cudaError_t jit_launch(void* func, const GroupParams& p, int grid, int smem, cudaStream_t st);
 cudaError_t jit_launch_gemm(void* func, const GemmParams& p, int grid, int smem, cudaStream_t st);
 

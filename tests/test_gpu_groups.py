@@ -9,12 +9,14 @@ import workloads as W
 from oracle import execute as OE
 from tests._helpers import rel_err, check_parity, exact_value, TOL_F32
 from tests._gpu import prepare, run_fused, run_unfused
-from group_execution_gb300 import _lib
+from group_execution_gb300 import _lib, graph_from_spec
 
 pytestmark = pytest.mark.gpu
 
 
-MODES = [0, _lib.FG_FLAG_INTERPRET]
+# compiled programs (the small-group kernel for small groups), the
+# interpreter, and compiled programs in the pipelined kernels only
+MODES = [0, _lib.FG_FLAG_INTERPRET, _lib.FG_FLAG_NO_SMALL]
 
 
 def _check(spec, seed=0, unfused=True, **kw):
@@ -231,3 +233,29 @@ def test_row_reductions_forced_splits(tpu, shape):
                 env = run_fused(plan, spec, dev)
                 plan.sync()
                 check_parity(spec, out, env[out].cpu().numpy(), ref)
+
+
+def test_small_groups_get_the_direct_kernel():
+    """Groups of at most 2 MiB carry the small-group kernel; larger ones,
+    groups built with flag bit 28 and interpreted groups do not."""
+    small = graph_from_spec(W.rnnlm_chain()).build(allow_reduce_epilogue=True)
+    assert "fg_jit_small_group" in small.source(0)
+    big = graph_from_spec(W.diamond(1024, 1024)).build()
+    assert "fg_jit_small_group" not in big.source(0)
+    off = graph_from_spec(W.rnnlm_chain()).build(allow_reduce_epilogue=True, flags=_lib.FG_FLAG_NO_SMALL)
+    assert "fg_jit_small_group" not in off.source(0)
+
+
+@pytest.mark.parametrize("shape", [(64, 1024), (37, 30), (1, 4), (300, 1000), (5, 2100)])
+@pytest.mark.parametrize("op", ["rowsum", "rowmax"])
+def test_small_kernel_reductions_both_paths(shape, op):
+    """A reduce group with a broadcast prologue and an epilogue, small enough
+    for the direct kernel, against the oracle on both paths."""
+    R, C = shape
+    spec = W.GraphSpec()
+    x = spec.input((R, C))
+    v = spec.input((C,))
+    s = spec.op(op, (spec.op("badd_col", (spec.op("relu", (x,)), v)),))
+    spec.mark_output(spec.op("sigmoid", (s,)))
+    for fl in (0, _lib.FG_FLAG_NO_SMALL):
+        _check(spec, allow_reduce_epilogue=True, flags=fl)
