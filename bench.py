@@ -725,9 +725,21 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
         torch.cuda.synchronize()
         for k in range(nb):
             ready[k].append(st.elapsed_time(evs[k]) * 1e3)
+    # the same launch with one more CTA consuming the ready words on the
+    # device: how long before the last packing CTA finished each bucket was
+    # seen ready (median of 10)
+    tms = torch.zeros(nb + 1, dtype=torch.int64, device="cuda")
+    lead = [[] for _ in range(nb)]
+    for _ in range(10):
+        tf.pack_buckets_observed(0.125, buf, tms)
+        tf.sync()
+        t = tms.cpu().numpy()
+        for k in range(nb):
+            lead[k].append((int(t[nb]) - int(t[k])) / 1e3)
     rows["buckets8MiB"] = {"n": nb, "graph_pack_us": gp * 1e3, "graph_unpack_us": gu * 1e3,
                            "one_launch_us": ob * 1e3, "one_launch_frac": nbytes / (ob * 1e-3) / 1e9 / hbm,
-                           "ready_us": [round(statistics.median(r), 1) for r in ready]}
+                           "ready_us": [round(statistics.median(r), 1) for r in ready],
+                           "dev_lead_us": [round(statistics.median(r), 1) for r in lead]}
 
     # training-step simulator fed by measured group times: a backward pass of
     # 161 gradient computations (g_i = 0.5 * relu(x_i) over the gradient set's

@@ -302,6 +302,15 @@ class TensorFusion:
         _lib.check(self.lib.tf_pack_buckets(self.h, C.c_float(scale), C.c_void_p(buf.data_ptr()),
                                             _stream_handle(stream)))
 
+    def pack_buckets_observed(self, scale, buf, times, seq_offset=0, wait_limit_ns=100_000_000, stream=None):
+        """pack_buckets with one more CTA in the launch that watches the
+        buckets' ready words: times (int64 device tensor, n_buckets + 1)
+        receives when each bucket was seen ready (device global timer, ns)
+        and, last, when the packing CTAs finished."""
+        _lib.check(self.lib.tf_pack_buckets_observed(self.h, C.c_float(scale), C.c_void_p(buf.data_ptr()),
+                                                     C.c_void_p(times.data_ptr()), seq_offset, wait_limit_ns,
+                                                     _stream_handle(stream)))
+
     def bucket_wait(self, b, stream=None):
         """Make `stream` wait until bucket b of the last pack_buckets launch
         is ready (a stream-ordered wait: no kernel runs for it)."""

@@ -85,6 +85,7 @@ SIGNATURES = {
     "tf_unpack_range": (_I32, [_P, _I32, _I32, _F, _P, _P]),
     "tf_layout_set_buckets": (_I32, [_P, _I32, _P]),
     "tf_pack_buckets": (_I32, [_P, _F, _P, _P]),
+    "tf_pack_buckets_observed": (_I32, [_P, _F, _P, _P, C.c_uint32, _I64, _P]),
     "tf_bucket_wait": (_I32, [_P, _I32, _P]),
     "tf_bucket_ready": (_I32, [_P, _I32, _P]),
     "tf_layout_destroy": (None, [_P]),

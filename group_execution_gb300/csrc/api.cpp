@@ -1407,7 +1407,9 @@ fg_status tf_layout_set_buckets(tf_layout* l, int32_t nb, const int32_t* bounds)
   return FG_OK;
 }
 
-fg_status tf_pack_buckets(tf_layout* l, float scale, void* buf, void* stream) {
+namespace {
+fg_status pack_buckets(tf_layout* l, float scale, void* buf, void* stream, uint64_t* times, uint32_t seq_offset,
+                       int64_t limit_ns) {
   if (!l || !buf) return err(FG_EINVAL, "null argument");
   if (!l->nb) return err(FG_EINVAL, "no bucket table (tf_layout_set_buckets)");
   if (reinterpret_cast<uintptr_t>(buf) % 256) return err(FG_EINVAL, "fusion buffer must be 256-byte aligned");
@@ -1419,13 +1421,41 @@ fg_status tf_pack_buckets(tf_layout* l, float scale, void* buf, void* stream) {
   bk.count = l->d_bucket + l->nchunks + l->nb;
   bk.ready = reinterpret_cast<uint32_t*>(l->d_bucket + l->nchunks + 2 * l->nb);
   bk.seq = l->seq + 1;
-  cudaError_t e = launch_tf_pack(l->d_chunks, l->nchunks, l->buf_bf16, scale, buf, std::min(l->nchunks, nsm * 8),
+  int grid = std::min(l->nchunks, nsm * 8);
+  if (times) {
+    // one more CTA, the observer
+    bk.observe = reinterpret_cast<unsigned long long*>(times);
+    bk.nb = l->nb;
+    bk.seq_offset = seq_offset;
+    bk.limit_ns = limit_ns;
+    bk.err = l->d_err;
+    grid += 1;
+  }
+  cudaError_t e = launch_tf_pack(l->d_chunks, l->nchunks, l->buf_bf16, scale, buf, grid,
                                  static_cast<cudaStream_t>(stream), bk);
   if (e != cudaSuccess) return cuda_err(e, "tf_pack_buckets launch");
   l->seq = bk.seq;
   e = note_table_use(l, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_err(e, "cudaEventRecord(bucket table use)");
   return FG_OK;
+}
+}  // namespace
+
+fg_status tf_pack_buckets(tf_layout* l, float scale, void* buf, void* stream) {
+  return pack_buckets(l, scale, buf, stream, nullptr, 0, 0);
+}
+
+fg_status tf_pack_buckets_observed(tf_layout* l, float scale, void* buf, uint64_t* times, uint32_t seq_offset,
+                                   int64_t wait_limit_ns, void* stream) {
+  if (!times) return err(FG_EINVAL, "null argument");
+  if (reinterpret_cast<uintptr_t>(times) % 8) return err(FG_EINVAL, "times must be 8-byte aligned");
+  if (wait_limit_ns <= 0) return err(FG_EINVAL, "wait_limit_ns must be positive");
+  if (l && l->nb) {
+    // the packing CTAs' finishing time is a maximum: it starts from zero
+    cudaError_t e = cudaMemsetAsync(times + l->nb, 0, sizeof(uint64_t), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_err(e, "cudaMemsetAsync(observed times)");
+  }
+  return pack_buckets(l, scale, buf, stream, times, seq_offset, wait_limit_ns);
 }
 
 fg_status tf_bucket_wait(tf_layout* l, int32_t b, void* stream) {

@@ -45,16 +45,52 @@ __device__ __forceinline__ void zero_pad(uint8_t* p, int bytes) {
   for (int i = threadIdx.x * 2; i < bytes; i += kPackThreads * 2) *reinterpret_cast<uint16_t*>(p + i) = 0;
 }
 
+// The observer of an observed launch (one thread): each bucket's ready word,
+// in bucket order, read with acquire until it holds the watched sequence
+// number, each wait bounded.
+__device__ void observe_buckets(const TfBuckets& bk) {
+  const uint32_t want = bk.seq + bk.seq_offset;
+  bool dead = false;
+  for (int b = 0; b < bk.nb; ++b) {
+    unsigned long long t = 0;
+    if (!dead) {
+      const uint64_t t0 = global_ns();
+      for (;;) {
+        const uint32_t v = (uint32_t)ld_acquire_gpu(reinterpret_cast<const int32_t*>(bk.ready + b));
+        const uint64_t now = global_ns();
+        if ((int32_t)(v - want) >= 0) {
+          t = now;
+          break;
+        }
+        if ((int64_t)(now - t0) > bk.limit_ns) {
+          dead = true;
+          set_error(bk.err, DEVERR_TIMEOUT);
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    bk.observe[b] = t;
+  }
+}
+
 __global__ void __launch_bounds__(kPackThreads) tf_pack_kernel(const TfChunk* __restrict__ chunks, int nchunks,
                                                                int bf16, float scale, uint8_t* __restrict__ buf,
                                                                const TfBuckets bk) {
   pdl_launch_dependents();
   pdl_wait();   // the previous grid's writes are visible from here on
-  int ci = blockIdx.x;
+  // an observed launch: CTA 0 watches the buckets, the others pack
+  const int obs = bk.observe ? 1 : 0;
+  if (obs && blockIdx.x == 0) {
+    if (threadIdx.x == 0) observe_buckets(bk);
+    return;
+  }
+  const int cta = (int)blockIdx.x - obs, ncta = (int)gridDim.x - obs;
+  int ci = cta;
   if (ci >= nchunks) return;
   TfChunk c = chunks[ci];
-  for (; ci < nchunks; ci += gridDim.x) {
-    const int nx = ci + gridDim.x;
+  for (; ci < nchunks; ci += ncta) {
+    const int nx = ci + ncta;
     TfChunk cn;
     if (nx < nchunks) cn = chunks[nx];
     const float* src = c.tensor + c.start;
@@ -101,6 +137,7 @@ __global__ void __launch_bounds__(kPackThreads) tf_pack_kernel(const TfChunk* __
     }
     c = cn;
   }
+  if (obs && threadIdx.x == 0) atomicMax(bk.observe + bk.nb, (unsigned long long)global_ns());
 }
 
 constexpr int kUnpackConsumers = 128;                  // four warps

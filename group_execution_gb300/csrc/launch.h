@@ -56,6 +56,16 @@ struct TfBuckets {
   int32_t* count = nullptr;                // chunks of the bucket written in this launch
   uint32_t* ready = nullptr;               // last launch whose chunks of the bucket are all written
   uint32_t seq = 0;
+  // observed launch: CTA 0 does not pack but watches the ready words, in
+  // bucket order, and writes to observe[b] the global timer when it saw
+  // bucket b reach sequence seq + seq_offset (0 if it gave up after
+  // limit_ns, with DEVERR_TIMEOUT in err); the packing CTAs write their
+  // latest finishing time to observe[nb]
+  unsigned long long* observe = nullptr;
+  int32_t nb = 0;
+  uint32_t seq_offset = 0;
+  int64_t limit_ns = 0;
+  int32_t* err = nullptr;
 };
 cudaError_t launch_tf_pack(const TfChunk* chunks, int nchunks, int buf_bf16, float scale, void* buf, int grid,
                            cudaStream_t st, const TfBuckets& bk = TfBuckets());

@@ -478,6 +478,24 @@ fg_status tf_pack_buckets(tf_layout* l, float scale, void* fusion_buf, void* cud
 fg_status tf_bucket_wait(tf_layout* l, int32_t bucket, void* cuda_stream);
 fg_status tf_bucket_ready(const tf_layout* l, int32_t bucket, int32_t* ready);
 
+/* tf_pack_buckets with a device-side consumer of the ready words inside the
+ * same launch (DisCo, Introduction: a bucket's AllReduce can start as soon
+ * as its tensors are in the fusion buffer; a collective's own kernel would
+ * watch the words this way).  One extra CTA of the launch packs nothing: it
+ * reads each bucket's ready word in bucket order (acquire, polled) until it
+ * holds this launch's sequence number plus seq_offset, and writes the
+ * device's global timer (ns) at that moment to times[b]; the packing CTAs
+ * write the latest time any of them finished to times[n_buckets].  times:
+ * device, 8-byte aligned, n_buckets + 1 entries, caller-owned.  Each wait is
+ * bounded by wait_limit_ns: a wait that expires leaves times[b] = 0 for that
+ * bucket and the rest, and latches FG_ETIMEOUT for tf_sync_status (a test
+ * passes seq_offset = 1, a launch that never comes, to see that happen; use
+ * 0 otherwise).  The fusion buffer receives exactly tf_pack_buckets' bytes.
+ * One CTA watching and the others packing are one launch, so the watcher
+ * never waits for work that cannot be scheduled. */
+fg_status tf_pack_buckets_observed(tf_layout* l, float scale, void* fusion_buf, uint64_t* times,
+                                   uint32_t seq_offset, int64_t wait_limit_ns, void* cuda_stream);
+
 void tf_layout_destroy(tf_layout* l);
 
 #ifdef __cplusplus

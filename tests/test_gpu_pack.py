@@ -200,3 +200,56 @@ def test_bucket_wait_orders_each_bucket():
         torch.cuda.synchronize()
         for (lo, hi), o in zip(ranges, outs):
             np.testing.assert_array_equal(o.cpu().numpy(), ref[lo:hi])
+
+
+def test_bucket_ready_words_seen_by_a_device_consumer_during_the_launch():
+    """A device-side consumer of the ready words (one CTA of the pack launch,
+    polling each bucket's word in order) sees the first buckets ready while
+    other CTAs are still packing: the first bucket well before the launch's
+    last packing CTA finishes.  The buffer still holds tf_pack's bytes."""
+    from group_execution_gb300 import plan_threshold
+    sizes = W.tensor_fusion_sizes(0)
+    xs = W.tensor_fusion_inputs(sizes)
+    dev = [torch.from_numpy(x).cuda() for x in xs]
+    tf = TensorFusion(dev)
+    bounds = plan_threshold(list(sizes), 8 << 20)
+    nb = len(bounds) - 1
+    tf.set_buckets(bounds)
+    buf = torch.empty((tf.total_bytes,), dtype=torch.uint8, device="cuda")
+    times = torch.zeros(nb + 1, dtype=torch.int64, device="cuda")
+    expect = PK.pack(xs, 0.125)
+    for _ in range(3):
+        times.zero_()
+        tf.pack_buckets_observed(0.125, buf, times)
+        tf.sync()
+        t = times.cpu().numpy()
+        assert (t[:nb] > 0).all(), t
+        end = t[nb]
+        # the first bucket (8 MiB of a 51 MB buffer) is seen ready at least
+        # 5 us before the last packing CTA is done
+        assert end - t[0] >= 5000, (t - t[0]).tolist()
+        assert np.array_equal(buf.cpu().numpy(), expect)
+
+
+def test_device_consumer_wait_is_bounded_and_reported():
+    """Watching for a launch that never comes: every wait of the consumer
+    expires after 1 ms, FG_ETIMEOUT is reported once, and the layout then
+    packs and reports normally."""
+    from group_execution_gb300 import FgError, _lib
+    sizes = [5000, 100000, 3000, 70000]
+    xs = W.tensor_fusion_inputs(sizes)
+    dev = [torch.from_numpy(x).cuda() for x in xs]
+    tf = TensorFusion(dev)
+    tf.set_buckets([0, 2, 4])
+    buf = torch.empty((tf.total_bytes,), dtype=torch.uint8, device="cuda")
+    times = torch.zeros(3, dtype=torch.int64, device="cuda")
+    tf.pack_buckets_observed(1.0, buf, times, seq_offset=1, wait_limit_ns=1_000_000)
+    with pytest.raises(FgError) as e:
+        tf.sync()
+    assert e.value.status == _lib.FG_ETIMEOUT
+    assert times.cpu().numpy()[:2].tolist() == [0, 0]
+    tf.sync()                                   # the word was cleared
+    tf.pack_buckets_observed(1.0, buf, times)
+    tf.sync()
+    assert (times.cpu().numpy()[:2] > 0).all()
+    assert np.array_equal(buf.cpu().numpy(), PK.pack(xs, 1.0))
