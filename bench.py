@@ -23,8 +23,11 @@ the training-step simulator, the sufficient-factor update at K = 512 and
 Inputs (256 MiB) and the output (128 MiB) together exceed the 129 MB L2, so
 the timed loop needs no L2 flush; the smaller rows flush L2 between reps.
 
-Multi-GPU: replicas only -- every rank runs the same plan on its own data
-(data-parallel replicas, weak scaling); there is no collective in the path.
+Multi-GPU: the fused groups run as replicas -- every rank runs the same plan
+on its own data (data-parallel replicas, weak scaling; the headline needs no
+collective).  The one exchange step of the path, the AllReduce of the packed
+gradient buckets, is the `exchange` row: NCCL over the ranks' bucket byte
+ranges, each started as soon as its bucket's ready word is set.
 `--impl reference` times the CPU oracle on a bounded sample instead.
 """
 from __future__ import annotations
@@ -370,8 +373,11 @@ def main():
                          "kernel": "fg_jit_ew_group", "peak_source": peak_kind,
                          "alg_bytes_per_launch": info.alg_bytes},
             "e2e": e2e, "gpu_launches": args.steps, "clocks": clk.summary()}
+    if not args.no_rows:
+        xrow = exchange_row(torch, dist, ws, rank, hbm)   # every rank takes part
     if rank == 0 and not args.no_rows:
         line["rows"] = secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf16s)
+        line["rows"]["exchange"] = _round(xrow)
         line["cpu_baseline"] = cpu_sample()
         line["rows"]["oracle"] = _round(oracle_samples())
     if rank == 0:
@@ -380,6 +386,62 @@ def main():
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def exchange_row(torch, dist, ws, rank, hbm):
+    """The data-parallel gradient exchange around tensor fusion (DisCo,
+    Background and Introduction; ring AllReduce in DisCo, Simulator), on every
+    rank: the 161 gradients packed into AllReduce buckets (8 MiB threshold) in
+    one launch, scaled by 1/N; a second stream waits for each bucket's ready
+    word and all-reduces the bucket's byte range over NCCL (bf16 sum of the
+    scaled gradients = their mean); every gradient unpacked after the last
+    bucket.  One rank has nothing to exchange: the same pipeline without the
+    collective.  Time per step: max over ranks of 20 steps after 3."""
+    import workloads as W
+    from group_execution_gb300 import TensorFusion, plan_threshold
+    sizes = W.tensor_fusion_sizes(0)
+    xs = [torch.from_numpy(x).cuda() for x in W.tensor_fusion_inputs(sizes, rank)]
+    tf = TensorFusion(xs)
+    bounds = plan_threshold(list(sizes), 8 << 20)
+    tf.set_buckets(bounds)
+    buf = torch.empty((tf.total_bytes,), dtype=torch.uint8, device="cuda")
+    views = [buf[a:b].view(torch.bfloat16) for a, b in tf.bucket_ranges(bounds)]
+    main, comm = torch.cuda.current_stream(), torch.cuda.Stream()
+
+    def step():
+        tf.pack_buckets(1.0 / ws, buf, stream=main)
+        for k, v in enumerate(views):
+            tf.bucket_wait(k, stream=comm)
+            if ws > 1:
+                with torch.cuda.stream(comm):
+                    dist.all_reduce(v)
+        main.wait_stream(comm)
+        tf.unpack(1.0, buf, stream=main)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(main)
+    for _ in range(20):
+        step()
+    b.record(main)
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) / 20 * 1e3
+    if dist:
+        t = torch.tensor([us], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        us = float(t.item())
+    nbytes = sum(b - a for a, b in tf.bucket_ranges(bounds))
+    row = {"n": ws, "buckets": len(views), "us": us, "bf16_MB": nbytes / 1e6}
+    if ws > 1:
+        row["busbw_GBps"] = 2 * (ws - 1) / ws * nbytes / (us * 1e-6) / 1e9
+    else:
+        row["allreduce"] = "none (1 rank)"
+    del xs, buf
+    return row
 
 
 def run_single(args):

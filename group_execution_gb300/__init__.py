@@ -329,6 +329,19 @@ class TensorFusion:
         return [(starts[k], starts[k + 1]) for k in range(len(bounds) - 1)]
 
 
+def layout_offsets(numels, buf_dtype="bf16", align=256):
+    """Byte offsets of the tensors in the fusion buffer and its total size,
+    computed on the host (no device): as TensorFusion lays them out."""
+    lib = _lib.load()
+    n = len(numels)
+    arr = (C.c_int64 * max(n, 1))(*[int(x) for x in numels])
+    offs = (C.c_int64 * max(n, 1))()
+    total = C.c_int64()
+    _lib.check(lib.tf_layout_offsets(n, arr, FG_BF16 if buf_dtype == "bf16" else FG_F32, align, offs,
+                                     C.byref(total)))
+    return list(offs[:n]), total.value
+
+
 def plan_threshold(numels, threshold_bytes, buf_dtype="bf16", align=256):
     """Threshold fusion of gradient tensors (in production order) into
     AllReduce buckets; returns the boundaries: bucket b holds tensors

@@ -69,6 +69,7 @@ SIGNATURES = {
     "fg_row_reduce_noalloc_status": (_I32, [_P]),
     "tf_layout_create": (_I32, [_I32, _PI64, C.POINTER(_P), _I32, _I64, C.POINTER(_P), _PI64, _PI64]),
     "tf_pack": (_I32, [_P, _F, _P, _P]),
+    "tf_layout_offsets": (_I32, [_I32, _PI64, _I32, _I64, _PI64, _PI64]),
     "tf_unpack": (_I32, [_P, _F, _P, _P]),
     "tf_sync_status": (_I32, [_P, _P]),
     "fg_plan_group_outputs": (_I32, [_P, _I32, _P, _P]),

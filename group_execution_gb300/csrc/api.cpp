@@ -1276,6 +1276,23 @@ fg_status fg_sync_status(fg_plan* p, void* stream) {
 
 // ---------------------------------------------------------------------------
 // tensor fusion
+fg_status tf_layout_offsets(int32_t n, const int64_t* numel, fg_dtype buf_dtype, int64_t align,
+                            int64_t* offsets_out, int64_t* total_out) {
+  if (n > 0 && !numel) return err(FG_EINVAL, "null argument");
+  if (n <= 0) return err(FG_EINVAL, "no tensors");
+  if (buf_dtype != FG_BF16 && buf_dtype != FG_F32) return err(FG_EINVAL, "unknown buffer dtype");
+  if (align < 16 || (align & (align - 1))) return err(FG_EINVAL, "align_bytes must be a power of two >= 16");
+  const int64_t eb = buf_dtype == FG_BF16 ? 2 : 4;
+  int64_t cur = 0;
+  for (int i = 0; i < n; ++i) {
+    if (numel[i] < 0) return err(FG_ESHAPE, "negative element count");
+    if (offsets_out) offsets_out[i] = cur;
+    cur = round_up(cur + numel[i] * eb, align);
+  }
+  if (total_out) *total_out = cur;
+  return FG_OK;
+}
+
 fg_status tf_layout_create(int32_t n, const int64_t* numel, float* const* grads, fg_dtype buf_dtype,
                            int64_t align, tf_layout** out, int64_t* offsets_out, int64_t* total_out) {
   if (!out || (n > 0 && (!numel || !grads))) return err(FG_EINVAL, "null argument");

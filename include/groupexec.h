@@ -383,6 +383,14 @@ fg_status fg_simulate(const fg_sim_problem* p, double* total, double* op_finish,
 
 /* ---- tensor fusion ------------------------------------------------------- */
 
+/* The layout of tf_layout_create computed on the host alone (no device, no
+ * allocation): offsets_out[i] (n entries, or NULL) and total_bytes_out (or
+ * NULL).  For allocating the fusion buffer before the layout exists, or for
+ * a peer that only needs the byte ranges.  FG_EINVAL / FG_ESHAPE as
+ * tf_layout_create. */
+fg_status tf_layout_offsets(int32_t n, const int64_t* numel, fg_dtype buf_dtype, int64_t align_bytes,
+                            int64_t* offsets_out, int64_t* total_bytes_out);
+
 /* Layout of n float32 gradient tensors (device pointers grads[i], numel[i]
  * elements, 16-byte aligned) in one fusion buffer of buf_dtype (FG_BF16 or
  * FG_F32): tensor i starts at byte offset offsets_out[i], a multiple of

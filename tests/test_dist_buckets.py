@@ -2,9 +2,11 @@
 ranks (DisCo, Background: gradients from every device are aggregated with an
 AllReduce; Introduction: small tensors are fused before it; Related Work:
 Horovod's threshold buckets).  Each rank plans its buckets with the library's
-host planner, packs its own gradients (oracle: no GPU here) with scale 1/N
-into an f32 fusion buffer, all-reduces every bucket's byte range on its own,
-unpacks, and must hold the exact mean of both ranks' gradients."""
+host planner and lays the fusion buffer out with the library's host layout
+(the byte ranges the device path all-reduces), packs its own gradients into
+it with scale 1/N (the oracle's arithmetic: no GPU here) in f32, all-reduces
+every bucket's byte range on its own, unpacks, and must hold the exact mean
+of both ranks' gradients."""
 import os
 import socket
 
@@ -30,7 +32,7 @@ def _worker(rank, port, q):
         dist.init_process_group("gloo", rank=rank, world_size=WORLD)
         import workloads as W
         from oracle import pack as PK
-        from group_execution_gb300 import plan_threshold
+        from group_execution_gb300 import plan_threshold, layout_offsets
 
         sizes = [int(x) for x in W.tensor_fusion_sizes(0)[:48]]
         xs = W.tensor_fusion_inputs(sizes, 100 + rank)
@@ -42,8 +44,12 @@ def _worker(rank, port, q):
         assert len(bounds) - 1 >= 3
 
         scale = 1.0 / WORLD
+        offs, total = layout_offsets(sizes, "f32")
+        # the library's layout is the one the oracle's pack writes
+        ref_offs, ref_total = PK.layout(sizes, 4)
+        assert list(offs) == list(ref_offs) and total == ref_total
         buf = torch.from_numpy(PK.pack(xs, scale, "f32"))
-        offs, total = PK.layout(sizes, 4)
+        assert buf.numel() == total
         starts = [offs[b] if b < len(sizes) else total for b in bounds]
         for k in range(len(bounds) - 1):
             view = buf[starts[k]:starts[k + 1]].view(torch.float32)
