@@ -588,12 +588,22 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
   const int tnf = (o.flags >> 22) & 3;
   const int KB = ge.compiled && kbf == 1 ? 1 : 2;
   constexpr int CL = kGemmCluster;
-  // Pair tile width (flag bits 22-23: 0 or 1 = 256, 2 = 128 columns; the
-  // interpreter keeps 256).  128-column tiles fill the rounds of a short-K
-  // launch better, but measured slower: each tile's fixed costs and the
-  // doubled A traffic outweigh it.
+  // Pair tile width (flag bits 22-23: 0 or 1 = 256, 2 = 128, 3 = 224
+  // columns; the interpreter keeps 256).  128-column tiles fill the rounds of
+  // a short-K launch better, but measured slower: each tile's fixed costs and
+  // the doubled A traffic outweigh it.  224-column tiles make the rounds of a
+  // 4096 x 4096 output come out even (304 tiles, 4 rounds on 76 pairs, where
+  // 256 leaves 28 tiles for a last round run in column halves) but measured
+  // slower too (K = 4096: 94.2 against 90.1 us with L2 flushed): the main
+  // loop is close to its operand feed, and 224-column tiles load about 14 %
+  // more operand bytes per flop.
   int TN = kGemmN;
   if (ge.compiled && tnf == 2) TN = 128;
+  if (ge.compiled && tnf == 3) TN = 224;
+  // a 224-column tile's CTA halves start at multiples of 16 columns, not of
+  // 64: an N-contiguous B is read in 2-D boxes (the 3-D view addresses whole
+  // 64-column groups)
+  if (TN == 224 && b_mn) p.b_3d = 0;
   p.ntn = (int32_t)((cg.N + TN - 1) / TN);
   p.ntiles = p.ntm * p.ntn;
   cg.gemm_kb = KB;
@@ -621,7 +631,7 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
   const int limit = 227 * 1024 - 64;   // less the kernel's static shared variables
   const int fixed = 1024 + 512 + (p.inplace_off >= 0 ? 0 : 2 * kGemmM * kGemmChunk * 4);
   auto leaf_area = [&](int n) { return (n * estage + 1023) / 1024 * 1024; };
-  const int stage = KB * (kGemmM + TN / 2) * kGemmK * 2;
+  const int stage = KB * (kGemmM + (TN == 224 ? 128 : TN / 2)) * kGemmK * 2;   // as the kernel's kBStage
   int ns = 0, ne = 0;
   static const std::vector<std::pair<int, int>> prefs_short = {{2, 6}, {2, 5}, {2, 4}, {2, 3}, {2, 2}};
   static const std::vector<std::pair<int, int>> prefs_long = {{3, 2}, {2, 4}, {2, 3}, {2, 2}};
@@ -678,7 +688,10 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
   p.sk = 0;
   p.nsplit_n = 0;
   const int tail = units % ncl;
-  if (sched == 2) {
+  if (TN == 224) {
+    // plain round robin: 224-column tiles are chosen for rounds that come out
+    // even (the split tails' chunk bookkeeping assumes an even chunk count)
+  } else if (sched == 2) {
     // every cluster takes an equal share of all units' ring slots; a share
     // spans at least one unit, so a unit is cut at most once
     if (units > ncl && tail > 0) {
@@ -878,7 +891,7 @@ fg_status launch_gemm(GroupExec& ge, void* const* ptrs, void* stream) {
         return st;
       // B: [K, N] (N contiguous), or [N, K] when transposed; each CTA of a
       // pair stages its half of the tile's columns
-      rank = view(gp.b_mn, gp.b_3d, cg.N, cg.gemm_tn / 2);
+      rank = view(gp.b_mn, gp.b_3d, cg.N, cg.gemm_tn == 224 ? 128 : cg.gemm_tn / 2);
       if (fg_status st = encode(&gp.mapB, ptrs[cg.mm_b], rank, dims, strides, box, true,
                                 CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
         return st;

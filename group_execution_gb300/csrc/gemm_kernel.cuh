@@ -6,7 +6,7 @@
 // workload).
 //
 // Persistent: CTAs run in pairs on the SMs of one TPC, and a pair walks
-// 256 x TN output tiles (TN = 256, or 128 by choice).  Each CTA stages half of
+// 256 x TN output tiles (TN = 256, 224 or 128).  Each CTA stages half of
 // the tile's A rows and half of its B columns, KB 64-deep K blocks per ring
 // slot (two by default: 64 KB), each operand half in one TMA copy where the
 // layout allows; the even CTA issues 2-SM tcgen05.mma instructions
@@ -271,18 +271,23 @@ __device__ __forceinline__ void gemm_load_half(uint32_t dst, const CUtensorMap* 
 
 // A CTA pair (a 2-CTA cluster) per 256 x TN tile (cta_group::2), each CTA
 // holding half of A's rows and half of B's columns.  KB: K blocks of 64 per
-// operand ring slot (1 or 2).  TN: columns of a pair's tile (256, or 128:
+// operand ring slot (1 or 2).  TN: columns of a pair's tile (256; 224, whose
+// rounds come out even where 256 leaves a partial last round; or 128:
 // half the epilogue per tile, for short K where the epilogue's streams
 // dominate and finer tiles fill the last round).
 template <class Epi, int KB, int TN>
 __device__ __forceinline__ void gemm_body(const GemmParams& P) {
   static_assert(KB == 1 || KB == 2, "one or two K blocks per ring slot");
-  static_assert(TN == 256 || TN == 128, "pair tiles of 256 or 128 columns");
+  static_assert(TN == 256 || TN == 224 || TN == 128, "pair tiles of 256, 224 or 128 columns");
   constexpr int CL = kGemmCluster;                                 // CTAs per cluster: one pair
-  constexpr int kBCols = TN / 2;                                   // B columns staged per CTA
+  constexpr int kBCols = TN / 2;                                   // B columns of the tile per CTA
+  // B columns staged per CTA: 224-column tiles stage 128 (whole 64-wide
+  // swizzle groups, the ring laid out as for 256) and their MMAs read the
+  // first 112
+  constexpr int kBStage = TN == 224 ? 128 : kBCols;
   constexpr int kGemmChunks = TN / kGemmChunk;                     // epilogue chunks per tile
   constexpr int kHalfA = KB * kGemmABytes;                         // 128 rows x KB K blocks
-  constexpr int kStageBytes = kHalfA + KB * kBCols * kGemmK * 2;   // 32 (24) KB per K block and CTA
+  constexpr int kStageBytes = kHalfA + KB * kBStage * kGemmK * 2;  // 32 (24) KB per K block and CTA
   constexpr int kStageBytesH = kHalfA + KB * (kBCols / 2) * kGemmK * 2;   // a column half's slot
   extern __shared__ uint8_t smem_raw[];
   __shared__ int abort_flag;
@@ -401,7 +406,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
                 continue;
               }
             }
-            gemm_load_half<KB, kBCols>(b, &P.mapB, P.b_mn, P.b_3d, nb, k0, cbar, keep);
+            gemm_load_half<KB, kBStage>(b, &P.mapB, P.b_mn, P.b_3d, nb, k0, cbar, keep);
             continue;
           }
           if (leader) mbar_expect_tx(fbar, 2 * (hb ? kStageBytesH : kStageBytes));
@@ -422,7 +427,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       // MN-major: atoms of 64 (M or N) x 8 K rows, 64-wide groups 16 KB
       // apart; K-major: atoms of 8 rows x 64 K, K blocks 16 KB apart
       const uint32_t a_lbo = P.a_mn ? KB * 8192 : 16, b_lbo = P.b_mn ? KB * 8192 : 16;
-      const uint32_t a_blk = P.a_mn ? 8192 : 16384, b_blk = P.b_mn ? 8192 : kBCols * 128;   // next K block
+      const uint32_t a_blk = P.a_mn ? 8192 : 16384, b_blk = P.b_mn ? 8192 : kBStage * 128;   // next K block
       const uint32_t b_blk_h = P.b_mn ? 8192 : kBCols / 2 * 128;
       const uint32_t a_step = P.a_mn ? 2048 : 32, b_step = P.b_mn ? 2048 : 32;         // next 16 of K
       // a descriptor's start-address field holds address >> 4 in 14 bits and

@@ -116,7 +116,7 @@ typedef struct tf_layout tf_layout;
  * round's tiles cut along K into two pieces, 2 = equal shares of all tiles'
  * K steps, 3 = round robin with the last round's tiles cut into their two
  * column halves, the choice for CTA pairs with 256-column tiles), bits 22-23
- * the columns of a CTA pair's tile (0 or 1 = 256, 2 = 128); bits 24-25 = how an
+ * the columns of a CTA pair's tile (0 or 1 = 256, 2 = 128, 3 = 224); bits 24-25 = how an
  * elementwise group writes its output: 0 default (= 2), 1 the CTA's tile
  * staged in shared memory and stored by one TMA store, 2 each warp's slice
  * stored by its own TMA store, 3 direct 16-byte stores from registers; and

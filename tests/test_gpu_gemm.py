@@ -322,3 +322,52 @@ def test_column_half_tail_layouts(ta, tb, mode):
     A = inputs[0].T if ta else inputs[0]
     B = inputs[1].T if tb else inputs[1]
     _check_matmul_bound(env[spec.outputs[0]].cpu().numpy(), A, B)
+
+
+TN224 = 3 << 22   # 224-column pair tiles (the choice where their rounds come out even)
+
+
+@pytest.mark.parametrize("ta,tb", [(1, 0), (0, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("kmn", [(1024, 512, 1024), (1096, 392, 1288), (200, 264, 600), (64, 128, 512),
+                                 (512, 256, 4096)])
+@pytest.mark.parametrize("kb", [KB2, KB1])
+def test_tn224_layouts(ta, tb, kmn, kb):
+    """224-column pair tiles: each CTA's B half starts at a multiple of 16
+    columns (2-D boxes for an N-contiguous B), the MMAs read 112 of the 128
+    staged columns; ragged M, N and K, every operand layout."""
+    K, M, N = kmn
+    spec = _matmul_graph(K, M, N, ta, tb)
+    g, plan, inputs, dev = prepare(spec, flags=TN224 | kb)
+    assert "gemm_body<fg::JitEpi, %d, 224>" % (1 if kb == KB1 else 2) in plan.source(0)
+    env = run_fused(plan, spec, dev)
+    plan.sync()
+    A = inputs[0].T if ta else inputs[0]
+    B = inputs[1].T if tb else inputs[1]
+    _check_matmul_bound(env[spec.outputs[0]].cpu().numpy(), A, B)
+
+
+@pytest.mark.parametrize("epi", ["bias_relu", "trans_leaf"])
+def test_tn224_epilogues(epi):
+    spec = _matmul_graph(1024, 512, 1344, 1, 0, epi)
+    g, plan, inputs, dev = prepare(spec, flags=TN224)
+    env = run_fused(plan, spec, dev)
+    plan.sync()
+    ref = OE.run_unfused(spec, inputs)[spec.outputs[0]]
+    assert rel_err(env[spec.outputs[0]].cpu().numpy(), ref) <= TOL_F32
+
+
+@pytest.mark.parametrize("store", [ST_PRODUCER, ST_WARPS])
+@pytest.mark.parametrize("K", [512, 4096])
+def test_tn224_sf_update_full_size(store, K):
+    """The sufficient-factor update at full size in 224-column tiles (304
+    tiles, four rounds on 76 pairs), both in-place store modes, run twice."""
+    spec = W.sf_update(K, 4096, 4096)
+    g, plan, inputs, dev = prepare(spec, flags=TN224 | store)
+    ref = OE.run_unfused(spec, inputs)[spec.outputs[0]]
+    w = inputs[2]
+    for _ in range(2):
+        env = run_fused(plan, spec, dev)
+        plan.sync()
+        got = env[spec.outputs[0]].cpu().numpy()
+        assert rel_err(got, ref) <= TOL_F32
+        assert rel_err(w - got, w - ref) <= TOL_BF16
