@@ -122,6 +122,9 @@ struct tf_layout {
   std::vector<float*> grads;
   TfChunk* d_chunks = nullptr;       // chunk table, followed by the device error word
   int32_t* d_err = nullptr;
+  // chunk claim counter of packs over the whole layout (each launch
+  // advances it by the chunk count)
+  unsigned long long* d_claim = nullptr;
   int nchunks = 0;
   std::vector<int32_t> chunk_begin;  // first chunk of every tensor, [n + 1]
   // AllReduce buckets packed in one launch: device block of the chunk ->
@@ -1352,8 +1355,9 @@ fg_status tf_layout_create(int32_t n, const int64_t* numel, float* const* grads,
   cudaError_t e = cudaMalloc(&l->d_chunks, table + 256);
   if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(chunk table)");
   l->d_err = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(l->d_chunks) + table);
+  l->d_claim = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(l->d_chunks) + table + 64);
   e = cudaMemcpy(l->d_chunks, ch.data(), sizeof(TfChunk) * ch.size(), cudaMemcpyHostToDevice);
-  if (e == cudaSuccess) e = cudaMemset(l->d_err, 0, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemset(l->d_err, 0, 256);   // the error word and the claim counters
   if (e != cudaSuccess) {
     cudaFree(l->d_chunks);
     return cuda_err(e, "cudaMemcpy(chunk table)");
@@ -1380,8 +1384,10 @@ fg_status tf_pack_range(const tf_layout* l, int32_t first, int32_t count, float 
   if (c1 == c0) return FG_OK;
   int nsm = 148;
   device_present(&nsm);
+  // launches over the whole layout claim their chunks dynamically
+  const bool all = c0 == 0 && c1 == l->nchunks;
   cudaError_t e = launch_tf_pack(l->d_chunks + c0, c1 - c0, l->buf_bf16, scale, buf, std::min(c1 - c0, nsm * 8),
-                                 static_cast<cudaStream_t>(stream));
+                                 static_cast<cudaStream_t>(stream), TfBuckets(), all ? l->d_claim : nullptr);
   return e == cudaSuccess ? FG_OK : cuda_err(e, "tf_pack launch");
 }
 
@@ -1462,7 +1468,7 @@ fg_status pack_buckets(tf_layout* l, float scale, void* buf, void* stream, uint6
     grid += 1;
   }
   cudaError_t e = launch_tf_pack(l->d_chunks, l->nchunks, l->buf_bf16, scale, buf, grid,
-                                 static_cast<cudaStream_t>(stream), bk);
+                                 static_cast<cudaStream_t>(stream), bk, l->d_claim);
   if (e != cudaSuccess) return cuda_err(e, "tf_pack_buckets launch");
   l->seq = bk.seq;
   e = note_table_use(l, static_cast<cudaStream_t>(stream));
@@ -1562,7 +1568,7 @@ fg_status tf_sync_status(tf_layout* l, void* stream) {
   if (e != cudaSuccess) return cuda_err(e, "reading the device error flag");
   if (flag == 0) return FG_OK;
   cudaMemset(l->d_err, 0, sizeof(int32_t));
-  if (flag == DEVERR_TIMEOUT) return err(FG_ETIMEOUT, "a device-side wait for a chunk load expired");
+  if (flag == DEVERR_TIMEOUT) return err(FG_ETIMEOUT, "a device-side wait expired (a chunk load or a watched bucket)");
   return err(FG_EDEVICE, "device error flag " + std::to_string(flag));
 }
 

@@ -74,9 +74,17 @@ __device__ void observe_buckets(const TfBuckets& bk) {
   }
 }
 
+// claim: null = CTAs stride over the chunks; else each CTA's first chunk is
+// fixed and the next ones are claimed from this counter, which a launch
+// advances by exactly nchunks (each CTA with a first chunk claims until one
+// claim fails), so that claim c is chunk ncta + c mod nchunks.  SMs do not
+// stream at the same rate: claiming keeps every CTA busy until the chunks run
+// out.
 __global__ void __launch_bounds__(kPackThreads) tf_pack_kernel(const TfChunk* __restrict__ chunks, int nchunks,
                                                                int bf16, float scale, uint8_t* __restrict__ buf,
-                                                               const TfBuckets bk) {
+                                                               const TfBuckets bk, unsigned long long* claim) {
+  __shared__ int s_nx[2];
+  __shared__ TfChunk s_cn[2];
   pdl_launch_dependents();
   pdl_wait();   // the previous grid's writes are visible from here on
   // an observed launch: CTA 0 watches the buckets, the others pack
@@ -89,10 +97,15 @@ __global__ void __launch_bounds__(kPackThreads) tf_pack_kernel(const TfChunk* __
   int ci = cta;
   if (ci >= nchunks) return;
   TfChunk c = chunks[ci];
-  for (; ci < nchunks; ci += ncta) {
-    const int nx = ci + ncta;
+  for (int it = 0;; ++it) {
+    int nx = ci + ncta;
     TfChunk cn;
-    if (nx < nchunks) cn = chunks[nx];
+    unsigned long long cl = 0;
+    if (claim) {
+      if (threadIdx.x == 0) cl = atomicAdd(claim, 1ull);   // the next chunk, in flight meanwhile
+    } else if (nx < nchunks) {
+      cn = chunks[nx];
+    }
     const float* src = c.tensor + c.start;
     uint8_t* dst = buf + c.buf_off;
     if (c.count == kTfChunk) {
@@ -121,12 +134,24 @@ __global__ void __launch_bounds__(kPackThreads) tf_pack_kernel(const TfChunk* __
       }
     }
     if (c.pad_bytes) zero_pad(dst + (size_t)c.count * (bf16 ? 2 : 4), c.pad_bytes);
+    if (claim) {
+      // thread 0 shares the claimed chunk (buffers alternate, so a thread
+      // still reading the last one is never overwritten)
+      if (threadIdx.x == 0) {
+        const int n2 = ncta + (int)(cl % (unsigned long long)nchunks);
+        s_nx[it & 1] = n2;
+        if (n2 < nchunks) s_cn[it & 1] = chunks[n2];
+      }
+      __syncthreads();
+      nx = s_nx[it & 1];
+      if (nx < nchunks) cn = s_cn[it & 1];
+    }
     if (bk.ready) {
       // count the chunk for its bucket: the barrier orders every thread's
       // stores before thread 0's release (cumulative); the count that
       // completes the bucket acquires the other CTAs' chunks and publishes
       // the bucket
-      __syncthreads();
+      if (!claim) __syncthreads();
       if (threadIdx.x == 0) {
         const int b = bk.chunk_bucket[ci];
         if (atom_add_acq_rel_gpu(&bk.count[b], 1) == bk.nchunks[b] - 1) {
@@ -135,6 +160,8 @@ __global__ void __launch_bounds__(kPackThreads) tf_pack_kernel(const TfChunk* __
         }
       }
     }
+    if (nx >= nchunks) break;
+    ci = nx;
     c = cn;
   }
   if (obs && threadIdx.x == 0) atomicMax(bk.observe + bk.nb, (unsigned long long)global_ns());
@@ -258,11 +285,12 @@ __global__ void __launch_bounds__(kUnpackThreadsTma, 1)
 }  // namespace
 
 cudaError_t launch_tf_pack(const TfChunk* chunks, int nchunks, int buf_bf16, float scale, void* buf, int grid,
-                           cudaStream_t st, const TfBuckets& bk) {
+                           cudaStream_t st, const TfBuckets& bk, unsigned long long* claim) {
   cudaLaunchConfig_t cfg = pdl_config(grid, kPackThreads, 0, st);
   cudaLaunchAttribute at[1];
   pdl_attr(cfg, at);
-  return cudaLaunchKernelEx(&cfg, tf_pack_kernel, chunks, nchunks, buf_bf16, scale, static_cast<uint8_t*>(buf), bk);
+  return cudaLaunchKernelEx(&cfg, tf_pack_kernel, chunks, nchunks, buf_bf16, scale, static_cast<uint8_t*>(buf), bk,
+                            claim);
 }
 
 int tf_unpack_smem(int buf_bf16) {

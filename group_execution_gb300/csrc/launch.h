@@ -67,8 +67,10 @@ struct TfBuckets {
   int64_t limit_ns = 0;
   int32_t* err = nullptr;
 };
+// claim: null = CTAs stride over the chunks; else the launch covers all of
+// the layout's chunks and CTAs claim them from this counter (see the kernel)
 cudaError_t launch_tf_pack(const TfChunk* chunks, int nchunks, int buf_bf16, float scale, void* buf, int grid,
-                           cudaStream_t st, const TfBuckets& bk = TfBuckets());
+                           cudaStream_t st, const TfBuckets& bk = TfBuckets(), unsigned long long* claim = nullptr);
 // Unpack runs one CTA per SM (grid = SM count); err receives DEVERR_TIMEOUT
 // if a wait for a chunk load expires.
 cudaError_t launch_tf_unpack(const TfChunk* chunks, int nchunks, int buf_bf16, float uscale, const void* buf,
