@@ -489,6 +489,8 @@ def run_single(args):
         flops = sum(gi.alg_flops for gi in plan.groups)
         kernel = {"elementwise": "fg_jit_ew_group", "reduce": "fg_jit_reduce_group",
                   "gemm": "fg_jit_gemm_group"}[plan.groups[-1].kind]
+        if "fg_jit_small_group" in plan.source(len(plan.groups) - 1):
+            kernel = "fg_jit_small_group"   # small groups run the direct-read kernel
         wl = spec.name
     for _ in range(max(3, args.warmup)):
         fn()
@@ -507,7 +509,8 @@ def run_single(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": wl}, "gpu_launches": args.steps,
             "roofline": {"bound": "hbm", "achieved": gbps, "peak": hbm, "unit": "GB/s", "frac": gbps / hbm,
-                         "traffic": None, "kernel": kernel, "peak_source": peak_kind},
+                         "traffic": traffic_for(kernel, {"sf_update": "sfk512", "sf_update_k4096": "sfk4096"}.get(
+                             args.workload, args.workload)), "kernel": kernel, "peak_source": peak_kind},
             "clocks": clk.summary()}
     if flops:
         line["TFLOPs"] = flops / (ms * 1e-3) / 1e12
@@ -515,24 +518,37 @@ def run_single(args):
     print(json.dumps(line), flush=True)
 
 
+# The sources that define each kernel: its device code, its generated program
+# and its launch configuration.  A committed capture counts only while these
+# hash to the value recorded with it.
+_GROUP = ("fg_abi.h", "fg_device.cuh", "group_kernels.cuh", "jit.cpp", "host_compile.cpp", "api.cpp")
+KERNEL_SOURCES = {
+    "fg_jit_ew_group": _GROUP, "fg_jit_reduce_group": _GROUP, "fg_jit_small_group": _GROUP,
+    "fg_jit_gemm_group": ("fg_abi.h", "fg_device.cuh", "gemm_kernel.cuh", "jit.cpp", "host_compile.cpp", "api.cpp"),
+    "tf_pack_kernel": ("fg_abi.h", "fg_device.cuh", "k_pack.cu", "launch.h", "api.cpp"),
+    "tf_unpack_kernel": ("fg_abi.h", "fg_device.cuh", "k_pack.cu", "launch.h", "api.cpp"),
+}
+
+
 def traffic_for(kernel, workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current sources."""
+    on the kernel's current sources."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         d = json.load(open(p))[workload]
     except Exception:
         return None
-    if d.get("kernel") != kernel or d.get("sources") != sources_hash():
+    if d.get("kernel") != kernel or d.get("sources") != sources_hash(kernel):
         return None
     return d.get("dram_bytes_per_launch")
 
 
-def sources_hash():
+def sources_hash(kernel):
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "group_execution_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES[kernel]:
+        h.update(f.encode())
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
