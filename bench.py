@@ -608,7 +608,6 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
         """Every group (or every operator) of the plan in order, with the
         pointer arrays marshalled once: the host's per-launch work stays
         below the kernels' time."""
-        sh = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
         if fused:
             launches = [(p.lib.fg_launch_group, gid, p._ptrs({v: env[v] for v in gi.leaves + gi.outs}))
                         for gid, gi in enumerate(p.groups)]
@@ -621,6 +620,8 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
                     node += 1
 
         def f():
+            # the stream current at the call (a CUDA-graph capture's, too)
+            sh = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
             for fn, k, ptrs in launches:
                 st = fn(p.h, k, ptrs, sh)
                 if st:

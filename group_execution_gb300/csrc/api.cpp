@@ -514,8 +514,10 @@ void prepare_group(GroupExec& ge, const BuildOpts& o, int nsm) {
   // Flag bit 28 turns it off.
   bool shifted = false;
   for (const LeafUse& l : cg.leaves) shifted |= l.map.shift != 0;
-  ge.small = ge.compiled && cg.alg_bytes <= kSmallGroupBytes && cg.xout_values.empty() && !shifted &&
-             !(o.flags & FG_FLAG_INJECT_NO_LOADS) && !(o.flags & FG_FLAG_NO_SMALL);
+  // (one warp per row: rows of at most 1024 columns, four passes of a warp's
+  // 256 columns, so that a wide single-row frame does not fall to one warp)
+  ge.small = ge.compiled && cg.alg_bytes <= kSmallGroupBytes && cg.FC <= 4 * 32 * 8 && cg.xout_values.empty() &&
+             !shifted && !(o.flags & FG_FLAG_INJECT_NO_LOADS) && !(o.flags & FG_FLAG_NO_SMALL);
   ge.grid_small = (int)std::max<int64_t>(1, (cg.FR + kSmallThreads / 32 - 1) / (kSmallThreads / 32));
 }
 
@@ -1386,7 +1388,8 @@ fg_status tf_pack_range(const tf_layout* l, int32_t first, int32_t count, float 
   device_present(&nsm);
   // launches over the whole layout claim their chunks dynamically
   const bool all = c0 == 0 && c1 == l->nchunks;
-  cudaError_t e = launch_tf_pack(l->d_chunks + c0, c1 - c0, l->buf_bf16, scale, buf, std::min(c1 - c0, nsm * 8),
+  cudaError_t e = launch_tf_pack(l->d_chunks + c0, c1 - c0, l->buf_bf16, scale, buf,
+                                 std::min(c1 - c0, tf_pack_resident(nsm)),
                                  static_cast<cudaStream_t>(stream), TfBuckets(), all ? l->d_claim : nullptr);
   return e == cudaSuccess ? FG_OK : cuda_err(e, "tf_pack launch");
 }
@@ -1457,7 +1460,9 @@ fg_status pack_buckets(tf_layout* l, float scale, void* buf, void* stream, uint6
   bk.count = l->d_bucket + l->nchunks + l->nb;
   bk.ready = reinterpret_cast<uint32_t*>(l->d_bucket + l->nchunks + 2 * l->nb);
   bk.seq = l->seq + 1;
-  int grid = std::min(l->nchunks, nsm * 8);
+  // every CTA resident at once, the observer's included
+  const int resident = tf_pack_resident(nsm);
+  int grid = std::min(l->nchunks, std::max(1, resident - (times ? 1 : 0)));
   if (times) {
     // one more CTA, the observer
     bk.observe = reinterpret_cast<unsigned long long*>(times);

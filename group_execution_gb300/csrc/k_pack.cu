@@ -293,6 +293,22 @@ cudaError_t launch_tf_pack(const TfChunk* chunks, int nchunks, int buf_bf16, flo
                             claim);
 }
 
+int tf_pack_resident(int nsm) {
+  // A claimed launch fixes each CTA's first chunk, so every CTA of its grid
+  // must be resident from the start: one that waits for a slot would only
+  // start once the others run out of chunks, with its first chunk last.
+  static std::atomic<int> per_sm{0};
+  int k = per_sm.load(std::memory_order_relaxed);
+  if (!k) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k, tf_pack_kernel, kPackThreads, 0) != cudaSuccess || k < 1) {
+      (void)cudaGetLastError();
+      return nsm;
+    }
+    per_sm.store(k, std::memory_order_relaxed);
+  }
+  return k * nsm;
+}
+
 int tf_unpack_smem(int buf_bf16) {
   return 128 + 128 + unpack_stages(buf_bf16) * kTfChunk * (buf_bf16 ? 2 : 4) + kUnpackOutBufs * kUnpackOutBytes;
 }

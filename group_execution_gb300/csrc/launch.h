@@ -69,6 +69,8 @@ struct TfBuckets {
 };
 // claim: null = CTAs stride over the chunks; else the launch covers all of
 // the layout's chunks and CTAs claim them from this counter (see the kernel)
+// The pack CTAs that fit on nsm SMs at once (the grid of a claimed launch).
+int tf_pack_resident(int nsm);
 cudaError_t launch_tf_pack(const TfChunk* chunks, int nchunks, int buf_bf16, float scale, void* buf, int grid,
                            cudaStream_t st, const TfBuckets& bk = TfBuckets(), unsigned long long* claim = nullptr);
 // Unpack runs one CTA per SM (grid = SM count); err receives DEVERR_TIMEOUT

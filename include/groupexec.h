@@ -125,8 +125,9 @@ typedef struct tf_layout tf_layout;
  * of each 128 x 32 chunk before it reloads the buffer, 2 = each epilogue
  * warp's copy of its 32 rows; 3 = as 1);
  * bit 28 turns off the small-group kernel (groups of at most 2 MiB of leaves
- * and output otherwise run one warp per frame row, reading the leaves
- * straight from global memory, instead of the shared-memory pipeline);
+ * and output whose frame rows hold at most 1024 elements otherwise run one
+ * warp per frame row, reading the leaves straight from global memory,
+ * instead of the shared-memory pipeline);
  * bit 26 runs the groups' operator programs on the register-stack
  * interpreter instead of compiling each program to straight-line code when
  * the plan is built (default; needs NVRTC, loaded at run time); bit 27 is a
