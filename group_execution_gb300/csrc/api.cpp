@@ -10,6 +10,7 @@
 #include <mutex>
 #include <new>
 #include <string>
+#include <unordered_map>
 #include <vector>
 
 #include "host.h"
@@ -91,7 +92,8 @@ struct GroupExec {
   bool compiled = false;              // run the compiled program (else the interpreter)
   int min_blocks = 2;                 // CTAs per SM the kernel is built for
   void* fn = nullptr;                 // compiled kernel
-  bool small = false;                 // run the small-group kernel instead (direct reads, no ring)
+  bool small = false;                 // run the direct kernel instead (direct reads, no ring)
+  bool small_pdl = true;              // ... launched early behind the stream's previous kernel
   int grid_small = 1;
   void* fn_small = nullptr;
   std::vector<const void*> last_ptrs; // tensor-map cache key
@@ -507,18 +509,37 @@ void prepare_group(GroupExec& ge, const BuildOpts& o, int nsm) {
   } else {
     ge.grid = std::max(1, std::min(p.ntiles, ctas * nsm));
   }
-  // Small groups run a kernel without the shared-memory pipeline: one warp
-  // per frame row reading its leaves straight from global memory (compiled
-  // programs without extra outputs or shifted tuple fields; not with the
-  // failure-injection hook, whose point is the pipeline's bounded waits).
-  // Flag bit 28 turns it off.
-  bool shifted = false;
-  for (const LeafUse& l : cg.leaves) shifted |= l.map.shift != 0;
-  // (one warp per row: rows of at most 1024 columns, four passes of a warp's
-  // 256 columns, so that a wide single-row frame does not fall to one warp)
-  ge.small = ge.compiled && cg.alg_bytes <= kSmallGroupBytes && cg.FC <= 4 * 32 * 8 && cg.xout_values.empty() &&
-             !shifted && !(o.flags & FG_FLAG_INJECT_NO_LOADS) && !(o.flags & FG_FLAG_NO_SMALL);
-  ge.grid_small = (int)std::max<int64_t>(1, (cg.FR + kSmallThreads / 32 - 1) / (kSmallThreads / 32));
+  // The direct kernel reads the leaves straight from global memory, one warp
+  // per frame row segment, without the shared-memory pipeline: for small
+  // groups (rows of at most 1024 columns, so that a wide single-row frame
+  // does not fall to one warp), and for row reductions of at least 8192 row
+  // segments whose leaves are all read row by row (each warp's contiguous
+  // run of a row keeps DRAM pages busier than the pipeline's 32-row tiles
+  // do).  Compiled programs without extra outputs or shifted tuple fields
+  // only; not with the failure-injection hook, whose point is the pipeline's
+  // bounded waits.  Flag bit 28 turns it off.
+  bool shifted = false, rowwise = true;
+  for (const LeafUse& l : cg.leaves) {
+    shifted |= l.map.shift != 0;
+    rowwise &= l.cls == LEAF_IDENT || l.cls == LEAF_COL || l.cls == LEAF_ROW;
+  }
+  // warps per row: rows of 2048 columns or more split into segments of at
+  // least 1024 (a warp's run of 4 KB), up to four per row (one CTA)
+  p.seg = cg.exec == FG_EXEC_REDUCE ? (cg.FC >= 4096 ? 4 : cg.FC >= 2048 ? 2 : 1) : 1;
+  const bool small = cg.alg_bytes <= kSmallGroupBytes && cg.FC <= 4 * 32 * 8;
+  const bool rows = cg.exec == FG_EXEC_REDUCE && rowwise && cg.FR * p.seg >= kDirectMinWarps && cg.FC >= 4 * 32 * 8;
+  ge.small = ge.compiled && (small || rows) && cg.xout_values.empty() && !shifted &&
+             !(o.flags & FG_FLAG_INJECT_NO_LOADS) && !(o.flags & FG_FLAG_NO_SMALL);
+  // A large direct launch waits for the previous kernel to end instead,
+  // unless that was a direct launch too: placed early behind a pipelined
+  // kernel, its CTAs land on SMs whose on-chip memory is split for that
+  // kernel's shared-memory ring, and an SM that keeps taking new CTAs never
+  // drains to change the split (the scaled RNNLM chain, row sum then sigmoid
+  // group, launched back to back: 100 us with early launch, 85 without).
+  ge.small_pdl = small;
+  p.seg_cols = p.seg == 1 ? (int32_t)cg.FC : (int32_t)((cg.FC + 256 * p.seg - 1) / (256 * p.seg) * 256);
+  const int64_t warps = cg.FR * p.seg;
+  ge.grid_small = (int)std::max<int64_t>(1, (warps + kSmallThreads / 32 - 1) / (kSmallThreads / 32));
 }
 
 int gemm_box_bytes(int cls) {
@@ -934,6 +955,21 @@ fg_status launch_gemm(GroupExec& ge, void* const* ptrs, void* stream) {
   return FG_OK;
 }
 
+// Whether the last kernel this library launched on a stream was the direct
+// kernel; returns that and records the new launch's kind.  A large direct
+// launch starts early only behind another direct launch (any other of this
+// library's kernels uses a shared-memory ring).  Only speed depends on it:
+// a kernel launched early waits for its predecessor all the same.
+bool swap_last_direct(void* stream, bool direct) {
+  static std::mutex mu;
+  static std::unordered_map<void*, bool> last;
+  std::lock_guard<std::mutex> g(mu);
+  bool& v = last[stream];
+  const bool prev = v;
+  v = direct;
+  return prev;
+}
+
 fg_status launch_exec(fg_plan* p, GroupExec& ge, void* const* ptrs, void* stream) {
   if (ge.compile_status != FG_OK) return err(ge.compile_status, ge.compile_error);
   if (!p->has_device) return err(FG_ECUDA, "no CUDA device: the plan is host-only");
@@ -942,6 +978,7 @@ fg_status launch_exec(fg_plan* p, GroupExec& ge, void* const* ptrs, void* stream
     if (!ptrs[ge.cg.mm_a] || !ptrs[ge.cg.mm_b]) return err(FG_EINVAL, "null matmul operand");
     if (reinterpret_cast<uintptr_t>(ptrs[ge.cg.mm_a]) % 16 || reinterpret_cast<uintptr_t>(ptrs[ge.cg.mm_b]) % 16)
       return err(FG_EINVAL, "matmul operands must be 16-byte aligned");
+    swap_last_direct(stream, false);
     return launch_gemm(ge, ptrs, stream);
   }
   const CompiledGroup& cg = ge.cg;
@@ -990,8 +1027,11 @@ fg_status launch_exec(fg_plan* p, GroupExec& ge, void* const* ptrs, void* stream
     }
     ge.last_ptrs = key;
   }
-  cudaError_t e = ge.small && ge.fn_small
-                      ? jit_launch_any(ge.fn_small, &gp, ge.grid_small, kSmallThreads, 0, static_cast<cudaStream_t>(stream))
+  const bool direct = ge.small && ge.fn_small;
+  const bool after_direct = swap_last_direct(stream, direct);
+  cudaError_t e = direct
+                      ? jit_launch_any(ge.fn_small, &gp, ge.grid_small, kSmallThreads, 0, static_cast<cudaStream_t>(stream),
+                                       ge.small_pdl || after_direct)
                   : ge.fn ? jit_launch(ge.fn, gp, ge.grid, ge.smem, static_cast<cudaStream_t>(stream))
                         : launch_group_kernel(gp, cg.exec == FG_EXEC_REDUCE ? 1 : 0, ge.big ? 1 : 0, ge.grid,
                                               ge.smem, static_cast<cudaStream_t>(stream));
@@ -1388,6 +1428,7 @@ fg_status tf_pack_range(const tf_layout* l, int32_t first, int32_t count, float 
   device_present(&nsm);
   // launches over the whole layout claim their chunks dynamically
   const bool all = c0 == 0 && c1 == l->nchunks;
+  swap_last_direct(stream, false);
   cudaError_t e = launch_tf_pack(l->d_chunks + c0, c1 - c0, l->buf_bf16, scale, buf,
                                  std::min(c1 - c0, tf_pack_resident(nsm)),
                                  static_cast<cudaStream_t>(stream), TfBuckets(), all ? l->d_claim : nullptr);
@@ -1403,6 +1444,7 @@ fg_status tf_unpack_range(const tf_layout* l, int32_t first, int32_t count, floa
   if (c1 == c0) return FG_OK;
   int nsm = 148;
   device_present(&nsm);
+  swap_last_direct(stream, false);
   cudaError_t e = launch_tf_unpack(l->d_chunks + c0, c1 - c0, l->buf_bf16, uscale, buf, std::min(c1 - c0, nsm),
                                    l->d_err, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FG_OK : cuda_err(e, "tf_unpack launch");
@@ -1472,6 +1514,7 @@ fg_status pack_buckets(tf_layout* l, float scale, void* buf, void* stream, uint6
     bk.err = l->d_err;
     grid += 1;
   }
+  swap_last_direct(stream, false);
   cudaError_t e = launch_tf_pack(l->d_chunks, l->nchunks, l->buf_bf16, scale, buf, grid,
                                  static_cast<cudaStream_t>(stream), bk, l->d_claim);
   if (e != cudaSuccess) return cuda_err(e, "tf_pack_buckets launch");

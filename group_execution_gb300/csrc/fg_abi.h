@@ -131,8 +131,9 @@ constexpr int kTileC = 64;
 constexpr int kConsumerWarps = 8;
 constexpr int kProducerWarps = 2;     // group kernels: TMA producers taking alternate tiles
 constexpr int kMaxStages = 16;
-constexpr int kSmallThreads = 128;     // small-group kernel: four warps, one frame row each
+constexpr int kSmallThreads = 128;     // direct kernel: four warps, one frame row segment each
 constexpr int64_t kSmallGroupBytes = 2 << 20;   // groups of at most this many algorithmic bytes run it
+constexpr int kDirectMinWarps = 8192;  // larger row reductions run it from this many row segments
 
 enum RedOp : int { RED_NONE = 0, RED_SUM = 1, RED_MAX = 2 };
 
@@ -160,6 +161,8 @@ struct GroupParams {
   int32_t nxout;                       // extra outputs (compiled programs only)
   int32_t xout_tma;                    // 1: each warp stages its slice of every extra output
                                        //    in shared memory and stores it with TMA (xmaps)
+  int32_t seg, seg_cols;               // direct kernel: warps per frame row (1, 2 or 4), columns per
+                                       //    warp's segment (a multiple of 256 unless one segment)
   XOutDesc xout[kMaxXOut];
   CUtensorMap xmaps[kMaxXOut];
 };

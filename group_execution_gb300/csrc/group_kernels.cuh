@@ -185,8 +185,14 @@ struct DirectEnv {
   }
   __device__ __forceinline__ void col_l(int l, float (&t)[8]) const {
     const float* p = P.leaves[l].ptr + c0;
+    if (c0 + 8 <= P.FC && (reinterpret_cast<uintptr_t>(p) & 15) == 0) {
+      const float4 a = __ldg(reinterpret_cast<const float4*>(p)), c = __ldg(reinterpret_cast<const float4*>(p) + 1);
+      t[0] = a.x; t[1] = a.y; t[2] = a.z; t[3] = a.w;
+      t[4] = c.x; t[5] = c.y; t[6] = c.z; t[7] = c.w;
+    } else {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) t[k] = c0 + k < P.FC ? __ldg(p + k) : 0.f;
+      for (int k = 0; k < 8; ++k) t[k] = c0 + k < P.FC ? __ldg(p + k) : 0.f;
+    }
   }
   __device__ __forceinline__ void row_l(int l, float (&t)[8]) const {
     const float v = __ldg(P.leaves[l].ptr + r0);
@@ -750,61 +756,78 @@ __device__ __forceinline__ void reduce_body(const GroupParams& P) {
 }
 
 // ---------------------------------------------------------------------------------
-// Small groups (a couple of MB of leaves and output at most), elementwise or
-// ending in a row reduction: one warp per frame row, eight consecutive frame
-// columns per lane and pass, leaves read straight from global memory.  No
-// shared-memory ring, no split of a row across CTAs, no barrier: a launch
-// costs little more than one round trip to memory, where the pipelined
-// kernels' set-up (barriers, descriptor fetches, split combines) is several.
+// The direct kernel: no shared-memory ring, leaves read straight from global
+// memory.  It runs small groups (a couple of MB of leaves and output at most,
+// rows of at most 1024 columns), elementwise or ending in a row reduction,
+// where the pipelined kernels' set-up (barriers, descriptor fetches, split
+// combines) would cost several round trips to memory; and larger row
+// reductions whose leaves are all read row by row (the frame's own layout,
+// vectors over its rows or columns), where each warp's contiguous run of a
+// row keeps the memory system's pages busier than the pipeline's 32-row
+// tiles (the CTA scheduler also spreads the short CTAs over the SMs as they
+// free up).  One warp per frame row segment (P.seg warps per row, each
+// P.seg_cols columns), eight consecutive frame columns per lane and pass.
 // A reduction folds each lane's values in order, then the lanes in a fixed
-// butterfly; lane 0 applies the epilogue.
+// butterfly, then the row's segments in order; one lane applies the
+// epilogue.
 template <class Prog>
 __device__ __forceinline__ void small_body(const GroupParams& P) {
+  __shared__ float part[kSmallThreads / 32];
   pdl_launch_dependents();
   pdl_wait();   // the previous grid's writes are visible from here on
-  const int lane = threadIdx.x & 31;
-  const int r = blockIdx.x * (int)(blockDim.x >> 5) + (int)(threadIdx.x >> 5);
-  if (r >= P.FR) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int S = P.seg;   // a power of two dividing the CTA's warps: a row's segments share a CTA
+  const int wid = blockIdx.x * (kSmallThreads / 32) + warp;
+  const int r = wid / S, sg = wid - r * S;
   const bool red = P.red_op != RED_NONE, is_sum = P.red_op == RED_SUM;
   const float init = is_sum ? 0.f : neg_inf();
   float acc = init;
+  if (r < P.FR) {
+    const int c_end = min(P.FC, (sg + 1) * P.seg_cols);
 #pragma unroll 2
-  for (int c = lane * 8; c < P.FC; c += 32 * 8) {
-    const DirectEnv te{P, r, 0, c, 0};
-    float o[8];
-    Prog::run_direct(te, o);
-    if (red) {
-      float v[8];
+    for (int c = sg * P.seg_cols + lane * 8; c < c_end; c += 32 * 8) {
+      const DirectEnv te{P, r, 0, c, 0};
+      float o[8];
+      Prog::run_direct(te, o);
+      if (red) {
+        float v[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = c + k < P.FC ? o[k] : init;
-      if (is_sum) {
-        acc = __fadd_rn(acc, __fadd_rn(__fadd_rn(__fadd_rn(v[0], v[1]), __fadd_rn(v[2], v[3])),
-                                       __fadd_rn(__fadd_rn(v[4], v[5]), __fadd_rn(v[6], v[7]))));
+        for (int k = 0; k < 8; ++k) v[k] = c + k < P.FC ? o[k] : init;
+        if (is_sum) {
+          acc = __fadd_rn(acc, __fadd_rn(__fadd_rn(__fadd_rn(v[0], v[1]), __fadd_rn(v[2], v[3])),
+                                         __fadd_rn(__fadd_rn(v[4], v[5]), __fadd_rn(v[6], v[7]))));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) acc = fmaxf(acc, v[k]);
+        }
       } else {
+        float* op = P.out + (int64_t)r * P.FC + c;
+        if (c + 8 <= P.FC && (reinterpret_cast<uintptr_t>(op) & 15) == 0) {
+          reinterpret_cast<float4*>(op)[0] = make_float4(o[0], o[1], o[2], o[3]);
+          reinterpret_cast<float4*>(op)[1] = make_float4(o[4], o[5], o[6], o[7]);
+        } else {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) acc = fmaxf(acc, v[k]);
-      }
-    } else {
-      float* op = P.out + (int64_t)r * P.FC + c;
-      if (c + 8 <= P.FC && (reinterpret_cast<uintptr_t>(op) & 15) == 0) {
-        reinterpret_cast<float4*>(op)[0] = make_float4(o[0], o[1], o[2], o[3]);
-        reinterpret_cast<float4*>(op)[1] = make_float4(o[4], o[5], o[6], o[7]);
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (c + k < P.FC) op[k] = o[k];
+          for (int k = 0; k < 8; ++k)
+            if (c + k < P.FC) op[k] = o[k];
+        }
       }
     }
   }
-  if (red) {
+  if (!red) return;
 #pragma unroll
-    for (int d = 16; d > 0; d >>= 1) {
-      const float x = __shfl_xor_sync(0xffffffffu, acc, d);
-      acc = is_sum ? __fadd_rn(acc, x) : fmaxf(acc, x);
-    }
-    const typename Prog::Tables T{};
-    if (lane == 0) P.out[r] = Prog::epi(P, T, r, acc);
+  for (int d = 16; d > 0; d >>= 1) {
+    const float x = __shfl_xor_sync(0xffffffffu, acc, d);
+    acc = is_sum ? __fadd_rn(acc, x) : fmaxf(acc, x);
   }
+  if (S > 1) {
+    // every warp of the CTA reaches this barrier (S is the launch's)
+    if (lane == 0) part[warp] = acc;
+    __syncthreads();
+    if (sg != 0) return;
+    for (int k = 1; k < S; ++k) acc = is_sum ? __fadd_rn(acc, part[warp + k]) : fmaxf(acc, part[warp + k]);
+  }
+  const typename Prog::Tables T{};
+  if (lane == 0 && r < P.FR) P.out[r] = Prog::epi(P, T, r, acc);
 }
 
 }  // namespace fg

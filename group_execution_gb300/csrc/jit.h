@@ -18,8 +18,11 @@ std::string jit_source(const CompiledGroup& cg, int min_blocks, bool small = fal
 // error message.  funcs[i] is the loaded kernel of sources[i].
 std::string jit_compile(const std::vector<std::string>& sources, std::vector<void*>& funcs,
                         std::vector<void*>* small_funcs = nullptr);
-// One launch of a compiled kernel with `params` as its only argument.
-cudaError_t jit_launch_any(void* func, void* params, int grid, int threads, int smem, cudaStream_t st);
+// One launch of a compiled kernel with `params` as its only argument; pdl:
+// the launch may begin while the stream's previous kernel finishes (the
+// kernel waits for it with griddepcontrol.wait).
+cudaError_t jit_launch_any(void* func, void* params, int grid, int threads, int smem, cudaStream_t st,
+                           bool pdl = true);
 cudaError_t jit_launch(void* func, const GroupParams& p, int grid, int smem, cudaStream_t st);
 cudaError_t jit_launch_gemm(void* func, const GemmParams& p, int grid, int smem, cudaStream_t st);
 
