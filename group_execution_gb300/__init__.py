@@ -215,6 +215,13 @@ class Plan:
         return dict(zip(("tile_rows", "tile_cols", "stages", "n_staged", "n_gathered", "prog_len"),
                         [x.value for x in v]))
 
+    def direct_info(self, gid):
+        """Whether group gid runs on the direct kernel, its warps per frame
+        row, and whether its launch always may begin early."""
+        v = [C.c_int32() for _ in range(3)]
+        _lib.check(self.lib.fg_plan_group_direct_info(self.h, gid, *[C.byref(x) for x in v]))
+        return dict(zip(("direct", "segments", "early_launch"), [x.value for x in v]))
+
     def source(self, gid):
         """CUDA source the plan compiles for group gid."""
         n = C.c_int64()

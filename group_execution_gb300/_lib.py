@@ -62,6 +62,7 @@ SIGNATURES = {
     "fg_launch_unfused": (_I32, [_P, _I32, C.POINTER(_P), _P]),
     "fg_sync_status": (_I32, [_P, _P]),
     "fg_plan_group_exec_info": (_I32, [_P, _I32, _PI32, _PI32, _PI32, _PI32, _PI32, _PI32]),
+    "fg_plan_group_direct_info": (_I32, [_P, _I32, _PI32, _PI32, _PI32]),
     "fg_plan_group_source": (_I32, [_P, _I32, C.c_char_p, _I64, _PI64]),
     "fg_plan_destroy": (None, [_P]),
     "fg_last_error": (C.c_char_p, []),

@@ -1283,6 +1283,18 @@ fg_status fg_plan_group_exec_info(const fg_plan* p, int32_t gid, int32_t* tile_r
   return FG_OK;
 }
 
+fg_status fg_plan_group_direct_info(const fg_plan* p, int32_t gid, int32_t* direct, int32_t* segments,
+                                    int32_t* early_launch) {
+  if (!p) return err(FG_EINVAL, "null plan");
+  if (gid < 0 || gid >= (int32_t)p->groups.size()) return err(FG_EINVAL, "unknown group id");
+  const GroupExec& ge = p->groups[gid];
+  const bool d = ge.small && ge.gp;
+  if (direct) *direct = d ? 1 : 0;
+  if (segments) *segments = d ? ge.gp->seg : 1;
+  if (early_launch) *early_launch = d ? (ge.small_pdl ? 1 : 0) : 1;
+  return FG_OK;
+}
+
 fg_status fg_plan_group_source(const fg_plan* p, int32_t gid, char* buf, int64_t cap, int64_t* len_out) {
   if (!p) return err(FG_EINVAL, "null plan");
   if (gid < 0 || gid >= (int32_t)p->groups.size()) return err(FG_EINVAL, "unknown group id");

@@ -234,6 +234,17 @@ fg_status fg_plan_group_exec_info(const fg_plan* p, int32_t gid, int32_t* tile_r
                                   int32_t* tile_cols, int32_t* stages, int32_t* n_staged,
                                   int32_t* n_gathered, int32_t* prog_len);
 
+/* Diagnostics: whether fg_launch_group runs gid on the direct kernel (leaves
+ * read straight from global memory, one warp per frame row segment, no
+ * shared-memory ring: small groups, and row reductions of at least 8192 row
+ * segments whose leaves are all read row by row), the warps per frame row
+ * (1 unless direct), and whether its launch always may begin while the
+ * stream's previous kernel finishes (a large direct launch does so only
+ * behind another direct launch).  Any output pointer may be NULL.  Host
+ * only; FG_EINVAL for a null plan or an unknown group. */
+fg_status fg_plan_group_direct_info(const fg_plan* p, int32_t gid, int32_t* direct, int32_t* segments,
+                                    int32_t* early_launch);
+
 /* The CUDA source the plan compiles for group gid (the group's operator
  * program written out as straight-line code inside the shared pipeline).
  * Writes at most cap bytes including the terminating NUL to buf (buf may be
