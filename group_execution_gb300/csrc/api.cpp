@@ -673,6 +673,17 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
     const int stf = (o.flags >> 24) & 3;
     p.wstore = p.inplace_off >= 0 && (stf == 2 || (stf == 0 && short_k)) ? 1 : 0;
   }
+  // flag bits 29-30: the operand ring's bytes (1 = 64 KB, 2 = 96 KB, 3 =
+  // 128 KB; 0 = chosen), the leaf ring taking what is left
+  const int ringf = (o.flags >> 29) & 3;
+  if (ringf) {
+    const int qs = (ringf + 1) * 32 * 1024 / stage;
+    for (int q = 8; q >= 2 && !ns; --q)
+      if (qs >= 1 && fixed + qs * stage + leaf_area(q) <= limit) {
+        ns = qs;
+        ne = q;
+      }
+  }
   for (const auto& q : short_k ? prefs_short : prefs_long) {
     // the same bytes in flight with one-block slots: twice as many
     const int qs = q.first * (2 / KB);
@@ -683,8 +694,9 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
   }
   if (!ns) throw CompileError{FG_EUNSUPPORTED, "GEMM epilogue stages do not fit in shared memory"};
   // the CTA's last item stages each TMEM lane quarter's results (and the
-  // other piece's partial) in TN * 128 bytes of the idle operand ring
-  if (ns * stage < 4 * TN * 128) throw CompileError{FG_EUNSUPPORTED, "internal: GEMM operand ring below the last item's staging"};
+  // other piece's partial) in TN * 128 bytes of the idle operand ring, when
+  // the ring holds that much
+  p.last_ring = ns * stage >= 4 * TN * 128 ? 1 : 0;
   // small leaf chunks (column or row vectors): as many leaf buffers as still
   // fit, up to the barriers there are (each chunk's load is a round trip)
   while (estage > 0 && ne < 8 && fixed + ns * stage + leaf_area(ne + 1) <= limit) ++ne;

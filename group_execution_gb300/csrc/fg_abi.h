@@ -199,6 +199,8 @@ struct GemmParams {
                                        // store); 0 = the leaf producer stores the whole chunk before
                                        // reloading the buffer
   int32_t inject;                      // failure injection: 1 = the producers issue no loads
+  int32_t last_ring;                   // 1: the CTA's last item stages its results in the idle operand
+                                       // ring (which holds 4 x TN x 128 bytes); 0: as every other item
   // work units: a cluster's tiles (the pair's 256 x 256 tile, or the two
   // pairs' 256 x 512) in row-major order
   int32_t nunits;

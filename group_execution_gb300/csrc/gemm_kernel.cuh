@@ -516,7 +516,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         const GemmItem w = gemm_item(P, S, cl, rx, nslots);
         item_tile(w, rm0, rn0);
         rnch = item_chunks(w);
-        rstore = (w.piece < 0 || w.fin) && rx + S.step < S.end;
+        rstore = (w.piece < 0 || w.fin) && (rx + S.step < S.end || !P.last_ring);
       };
       // wait until chunk h's buffer is released by its four epilogue warps,
       // store the results they left in it, and move on to the next chunk
@@ -628,10 +628,10 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
         }
       }
       // The CTA's last item: every MMA has completed, so the operand ring is
-      // idle; each TMEM lane quarter takes TN * 128 bytes of it (the ring is
-      // at least four times that) for the other piece's partial and the
-      // result chunks, so that no chunk waits for a store buffer.
-      const bool last = x + S.step >= S.end;
+      // idle; each TMEM lane quarter takes TN * 128 bytes of it (when the
+      // ring is at least four times that) for the other piece's partial and
+      // the result chunks, so that no chunk waits for a store buffer.
+      const bool last = P.last_ring && x + S.step >= S.end;
       uint8_t* wring = opnd + q * (TN * 128);
       if (last && wdefer && lane == 0 && prev_e >= 0) {
         bulk_wait_read<0>();

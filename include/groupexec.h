@@ -123,11 +123,14 @@ typedef struct tf_layout tf_layout;
  * for GEMM-epilogue groups whose result is written in place of a leaf's
  * staged chunk, how it leaves (0 = chosen by K, 1 = the leaf producer's copy
  * of each 128 x 32 chunk before it reloads the buffer, 2 = each epilogue
- * warp's copy of its 32 rows; 3 = as 1);
- * bit 28 turns off the small-group kernel (groups of at most 2 MiB of leaves
- * and output whose frame rows hold at most 1024 elements otherwise run one
- * warp per frame row, reading the leaves straight from global memory,
- * instead of the shared-memory pipeline);
+ * warp's copy of its 32 rows; 3 = as 1); bits 29-30 the GEMM operand
+ * ring's size (0 = chosen by K, 1 = 64 KB, 2 = 96 KB, 3 = 128 KB; the
+ * epilogue's leaf buffers take the shared memory left, up to eight);
+ * bit 28 turns off the direct kernel (groups of at most 2 MiB of leaves and
+ * output whose frame rows hold at most 1024 elements, and row reductions of
+ * at least 8192 row segments whose leaves are all read row by row,
+ * otherwise run one warp per frame row segment, reading the leaves straight
+ * from global memory, instead of the shared-memory pipeline);
  * bit 26 runs the groups' operator programs on the register-stack
  * interpreter instead of compiling each program to straight-line code when
  * the plan is built (default; needs NVRTC, loaded at run time); bit 27 is a
