@@ -371,3 +371,60 @@ def test_tn224_sf_update_full_size(store, K):
         got = env[spec.outputs[0]].cpu().numpy()
         assert rel_err(got, ref) <= TOL_F32
         assert rel_err(w - got, w - ref) <= TOL_BF16
+
+
+RING64, RING96 = 1 << 29, 2 << 29   # operand ring of 64 or 96 KB, the leaf buffers taking the rest
+
+
+@pytest.mark.parametrize("K,M,N,extra", [
+    (512, 1024, 1024, RING96 | KB1),                       # eight leaf buffers; the last item as any other
+    (512, 1024, 1024, RING64 | KB2),                       # a single operand slot
+    (4096, 1024, 1024, RING96 | KB1),                      # long K: the leaf producer stores in place
+    (1024, 1024, 1024, (5 << 8) | KSPLIT | KB1 | RING64),  # split along K: the partial read from global
+    (1024, 1024, 1024, (5 << 8) | NSPLIT | KB1 | RING96),  # column halves
+    (512, 776, 1000, (3 << 8) | SK | KB2 | RING64),        # stream-K shares, ragged
+])
+def test_operand_ring_sizes(K, M, N, extra):
+    """Operand rings below the size the CTA's last item stages its results in
+    (the last item then writes through the leaf buffers like the others);
+    every schedule, run twice."""
+    spec = W.sf_update(K, M, N)
+    g, plan, inputs, dev = prepare(spec, flags=extra)
+    assert plan.n_groups == 1 and plan.groups[0].kind == "gemm"
+    ref = OE.run_unfused(spec, inputs)[spec.outputs[0]]
+    w = inputs[2]
+    for _ in range(2):
+        env = run_fused(plan, spec, dev)
+        plan.sync()
+        got = env[spec.outputs[0]].cpu().numpy()
+        assert rel_err(got, ref) <= TOL_F32
+        assert rel_err(w - got, w - ref) <= TOL_BF16
+
+
+RING64, RING96 = 1 << 29, 2 << 29   # operand ring of 64 or 96 KB, the leaf buffers taking the rest
+
+
+@pytest.mark.parametrize("K,M,N,extra", [
+    (512, 1024, 1024, RING96 | KB1),                       # eight leaf buffers; the last item as any other
+    (512, 1024, 1024, RING64 | KB2),                       # a single operand slot
+    (4096, 1024, 1024, RING96 | KB1),                      # long K: the leaf producer stores in place
+    (1024, 1024, 1024, (5 << 8) | KSPLIT | KB1 | RING64),  # split along K: the partial read from global
+    (1024, 1024, 1024, (5 << 8) | NSPLIT | KB1 | RING96),  # column halves
+    (512, 776, 1000, (3 << 8) | SK | KB2 | RING64),        # stream-K shares, ragged
+])
+def test_operand_ring_sizes(K, M, N, extra):
+    """Operand rings below the size the CTA's last item stages its results in
+    (the last item then writes through the leaf buffers like the others);
+    every schedule, run twice."""
+    spec = W.sf_update(K, M, N)
+    g, plan, inputs, dev = prepare(spec, flags=extra)
+    assert plan.n_groups == 1 and plan.groups[0].kind == "gemm"
+    ref = OE.run_unfused(spec, inputs)[spec.outputs[0]]
+    w = inputs[2]
+    for _ in range(2):
+        env = run_fused(plan, spec, dev)
+        plan.sync()
+        got = env[spec.outputs[0]].cpu().numpy()
+        assert rel_err(got, ref) <= TOL_F32
+        assert rel_err(w - got, w - ref) <= TOL_BF16
+
