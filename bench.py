@@ -489,8 +489,8 @@ def run_single(args):
         flops = sum(gi.alg_flops for gi in plan.groups)
         kernel = {"elementwise": "fg_jit_ew_group", "reduce": "fg_jit_reduce_group",
                   "gemm": "fg_jit_gemm_group"}[plan.groups[-1].kind]
-        if "fg_jit_small_group" in plan.source(len(plan.groups) - 1):
-            kernel = "fg_jit_small_group"   # small groups run the direct-read kernel
+        if plan.direct_info(len(plan.groups) - 1)["direct"]:
+            kernel = "fg_jit_small_group"   # the direct kernel (leaves read straight from global memory)
         wl = spec.name
     for _ in range(max(3, args.warmup)):
         fn()

@@ -1042,7 +1042,9 @@ fg_status launch_exec(fg_plan* p, GroupExec& ge, void* const* ptrs, void* stream
   const bool direct = ge.small && ge.fn_small;
   const bool after_direct = swap_last_direct(stream, direct);
   cudaError_t e = direct
-                      ? jit_launch_any(ge.fn_small, &gp, ge.grid_small, kSmallThreads, 0, static_cast<cudaStream_t>(stream),
+                      ? jit_launch_any(ge.fn_small, &gp, ge.grid_small, kSmallThreads,
+                                       gp.seg > 1 ? kSmallThreads / 32 * (int)sizeof(float) : 0,
+                                       static_cast<cudaStream_t>(stream),
                                        ge.small_pdl || after_direct)
                   : ge.fn ? jit_launch(ge.fn, gp, ge.grid, ge.smem, static_cast<cudaStream_t>(stream))
                         : launch_group_kernel(gp, cg.exec == FG_EXEC_REDUCE ? 1 : 0, ge.big ? 1 : 0, ge.grid,
@@ -1095,7 +1097,7 @@ fg_status build_plan(const Graph& g, const BuildOpts& o, const std::vector<std::
       for (auto& ge : *v)
         if (ge.compile_status == FG_OK && (ge.gp || ge.mp) && ge.compiled) {
           todo.push_back(&ge);
-          srcs.push_back(jit_source(ge.cg, ge.min_blocks, ge.small));
+          srcs.push_back(jit_source(ge.cg, ge.min_blocks, ge.small ? ge.gp->seg : 0));
         }
     if (!todo.empty()) {
       std::vector<void*> fns, smalls;
@@ -1313,7 +1315,7 @@ fg_status fg_plan_group_source(const fg_plan* p, int32_t gid, char* buf, int64_t
   const GroupExec& ge = p->groups[gid];
   if (ge.compile_status != FG_OK) return err(ge.compile_status, ge.compile_error);
   if (!ge.gp && !ge.mp) return err(FG_EUNSUPPORTED, "no compiled program for this group kind");
-  const std::string src = jit_source(ge.cg, ge.min_blocks, ge.small);
+  const std::string src = jit_source(ge.cg, ge.min_blocks, ge.small && ge.gp ? ge.gp->seg : 0);
   if (len_out) *len_out = (int64_t)src.size();
   if (buf && cap > 0) {
     const size_t n = std::min<size_t>(src.size(), (size_t)cap - 1);

@@ -770,22 +770,33 @@ __device__ __forceinline__ void reduce_body(const GroupParams& P) {
 // A reduction folds each lane's values in order, then the lanes in a fixed
 // butterfly, then the row's segments in order; one lane applies the
 // epilogue.
-template <class Prog>
+template <class Prog, bool kSeg>
 __device__ __forceinline__ void small_body(const GroupParams& P) {
-  __shared__ float part[kSmallThreads / 32];
+  // the segments' partials (kSeg: launched with this much dynamic shared
+  // memory; a one-segment launch has neither it nor the barrier, and its
+  // warps without a row leave at once: measured 0.6 us less per run on the
+  // two-group RNNLM chain than the segmented body with one segment)
+  extern __shared__ float part[];
   pdl_launch_dependents();
   pdl_wait();   // the previous grid's writes are visible from here on
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int S = P.seg;   // a power of two dividing the CTA's warps: a row's segments share a CTA
   const int wid = blockIdx.x * (kSmallThreads / 32) + warp;
-  const int r = wid / S, sg = wid - r * S;
+  int r = wid, sg = 0, c_begin = 0, c_end = P.FC;
+  if constexpr (kSeg) {
+    const int S = P.seg;   // a power of two dividing the CTA's warps: a row's segments share a CTA
+    r = wid / S;
+    sg = wid - r * S;
+    c_begin = sg * P.seg_cols;
+    c_end = min(P.FC, c_begin + P.seg_cols);
+  } else if (r >= P.FR) {
+    return;
+  }
   const bool red = P.red_op != RED_NONE, is_sum = P.red_op == RED_SUM;
   const float init = is_sum ? 0.f : neg_inf();
   float acc = init;
   if (r < P.FR) {
-    const int c_end = min(P.FC, (sg + 1) * P.seg_cols);
 #pragma unroll 2
-    for (int c = sg * P.seg_cols + lane * 8; c < c_end; c += 32 * 8) {
+    for (int c = c_begin + lane * 8; c < c_end; c += 32 * 8) {
       const DirectEnv te{P, r, 0, c, 0};
       float o[8];
       Prog::run_direct(te, o);
@@ -819,12 +830,12 @@ __device__ __forceinline__ void small_body(const GroupParams& P) {
     const float x = __shfl_xor_sync(0xffffffffu, acc, d);
     acc = is_sum ? __fadd_rn(acc, x) : fmaxf(acc, x);
   }
-  if (S > 1) {
-    // every warp of the CTA reaches this barrier (S is the launch's)
+  if constexpr (kSeg) {
+    // every warp of the CTA reaches this barrier
     if (lane == 0) part[warp] = acc;
     __syncthreads();
     if (sg != 0) return;
-    for (int k = 1; k < S; ++k) acc = is_sum ? __fadd_rn(acc, part[warp + k]) : fmaxf(acc, part[warp + k]);
+    for (int k = 1; k < P.seg; ++k) acc = is_sum ? __fadd_rn(acc, part[warp + k]) : fmaxf(acc, part[warp + k]);
   }
   const typename Prog::Tables T{};
   if (lane == 0 && r < P.FR) P.out[r] = Prog::epi(P, T, r, acc);

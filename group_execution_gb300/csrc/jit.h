@@ -12,8 +12,9 @@ namespace fg {
 
 bool jit_available();
 // CUDA source of a group's kernel; min_blocks is the kernel's CTAs-per-SM bound.
-// small = also the small-group kernel (direct leaf reads), fg_jit_small_group
-std::string jit_source(const CompiledGroup& cg, int min_blocks, bool small = false);
+// small_seg > 0: also the direct kernel (direct leaf reads), fg_jit_small_group,
+// for that many warps per frame row (its segmented body when more than one)
+std::string jit_source(const CompiledGroup& cg, int min_blocks, int small_seg = 0);
 // Compiles (once per process per distinct source) and loads; returns "" or an
 // error message.  funcs[i] is the loaded kernel of sources[i].
 std::string jit_compile(const std::vector<std::string>& sources, std::vector<void*>& funcs,
