@@ -736,27 +736,30 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
       p.sk = 1;
       p.split = 2;
     }
-  } else if (units > ncl && tail > 0 && 2 * tail <= ncl && TN == kGemmN && (sched == 3 || sched == 0)) {
+  } else if (units > ncl && tail > 0 && 2 * tail <= ncl && TN == kGemmN &&
+             (sched == 3 || (sched == 0 && p.nkb < 64))) {
     // cut the last round's units into their two column halves over the
     // pairs it would leave idle: each half runs all of K and its own
-    // epilogue, with no partial sums to exchange (measured against K pieces:
-    // K=512 32.8 -> 30.7 us with L2 flushed, where K pieces do not apply;
-    // K=4096 equal flushed, 90.4 -> 89.3 us back to back)
+    // epilogue, with no partial sums to exchange; a half moves 3/4 of a
+    // tile's operand bytes for half its flops.  Measured against symmetric
+    // K pieces (below): K=1024 38.9 against 43.0 us, K=2048 53.3 against
+    // 59.4 us with L2 flushed; from 64 K blocks the K pieces win (K=4096
+    // 88.1-90.1 against 91.2-92.1 us flushed, 87 against 89 back to back)
     p.nfull = units - tail;
     p.split = 2;
     p.nsplit_n = 1;
     p.split_at = nslots;
-  } else if (units > ncl && tail > 0 && 2 * tail <= ncl && p.nkb >= 16 && sched != 3) {
-    // split the last round's units along K into halves over the pairs it
-    // would leave idle, when K is long enough for the halves to outweigh the
-    // partial sums' traffic (two pieces: their sum does not depend on which
-    // ends last)
+  } else if (units > ncl && tail > 0 && 2 * tail <= ncl && p.nkb >= 16 && (sched == 1 || sched == 0)) {
+    // split the last round's units along K into equal halves over the pairs
+    // it would leave idle, when K is long enough for the halves to outweigh
+    // the partial sums' traffic: both pieces run full-width MMAs, then each
+    // hands the other its partial of the other's column half and finishes
+    // its own half (two pieces: their sum does not depend on which ends
+    // last)
     p.nfull = units - tail;
     p.split = 2;
-    // the first piece also writes its partial (about ten K blocks' worth of
-    // MMA time): it takes that much less of K, so that its partial is ready
-    // when the second piece's MMAs end
-    p.split_at = std::max(1, std::min(nslots / 2, (nslots - 10 / KB) / 2));
+    p.ksym = 1;
+    p.split_at = std::max(1, nslots / 2);
   }
 }
 
@@ -796,7 +799,7 @@ fg_status alloc_device(fg_plan* p, GroupExec& ge) {
       const size_t keys = mp.sk ? (size_t)(ge.grid / CL - 1) : (size_t)(mp.nunits - mp.nfull);
       cudaError_t e = cudaMalloc(&ge.scratch, sizeof(float) * keys * 2 * CL * kGemmM * ge.cg.gemm_tn);
       if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(split-tail workspace)");
-      ge.counter_bytes = sizeof(int32_t) * keys * CL * 8;
+      ge.counter_bytes = sizeof(int32_t) * keys * 2 * CL * 8;   // per piece for symmetric pieces
       e = cudaMalloc(&ge.counters, ge.counter_bytes);
       if (e != cudaSuccess) return cuda_err(e, "cudaMalloc(split-tail counters)");
       e = cudaMemset(ge.counters, 0, ge.counter_bytes);

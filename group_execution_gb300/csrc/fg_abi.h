@@ -216,8 +216,14 @@ struct GemmParams {
   // slots instead (at least one whole unit, so a unit is cut at most once,
   // into the two pieces on either side of a share boundary)
   int32_t sk;
+  // ksym = 1 (round robin with K pieces): the two pieces of a cut unit take
+  // equal halves of K and each finishes one column half of the tile: each
+  // writes its partial of the other's half, raises its flags, then waits for
+  // the other's partial of its own half (neither waits before publishing)
+  int32_t ksym;
   float* ws;                           // [pieces][cluster CTAs][64 column quads][128 rows][4] partial accumulators
-  int32_t* ws_cnt;                     // [split units][cluster CTAs][8 epilogue warps] partial-ready flags (cleared by the reader)
+  int32_t* ws_cnt;                     // [split units][pieces (ksym)][cluster CTAs][8 epilogue warps]
+                                       // partial-ready flags (cleared by the reader)
 };
 
 // Loads already issued always land; waiting for them before a CTA exits uses

@@ -199,13 +199,14 @@ __device__ __forceinline__ GemmSched gemm_sched(const GemmParams& P, int cl, int
 // other publishes its partial accumulator.
 struct GemmItem {
   int unit, piece, sl0, sl1, q, key;   // piece = -1 for a whole unit or a column half
-  int half;                            // -1, or the column half of the unit
+  int half;                            // -1, or the column half of the unit (a half-width MMA)
+  int ehalf;                           // -1, or the column half a symmetric K piece finishes
   bool fin;
 };
 __device__ __forceinline__ GemmItem gemm_item(const GemmParams& P, const GemmSched& S, int cl, int idx,
                                               int nslots) {
   GemmItem w;
-  w.piece = w.q = w.key = w.half = -1;
+  w.piece = w.q = w.key = w.half = w.ehalf = -1;
   w.fin = true;
   if (P.sk) {
     w.unit = idx;
@@ -235,11 +236,13 @@ __device__ __forceinline__ GemmItem gemm_item(const GemmParams& P, const GemmSch
     w.unit = P.nfull + w.q / P.split;
     w.key = w.unit - P.nfull;
     w.piece = w.q & 1;
-    // the first piece is the shorter: it also writes its partial, and is
-    // done when the second's MMAs end
+    // symmetric: equal halves of K, each piece finishing one column half;
+    // otherwise the first piece is the shorter: it also writes its partial,
+    // and is done when the second's MMAs end
     w.sl0 = w.piece ? P.split_at : 0;
     w.sl1 = w.piece ? nslots : P.split_at;
-    w.fin = w.piece == 1;
+    w.fin = P.ksym || w.piece == 1;
+    if (P.ksym) w.ehalf = w.piece;
   }
   return w;
 }
@@ -333,6 +336,13 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
     if (w.half > 0) n0 += TN / 2;
   };
   auto item_chunks = [&](const GemmItem& w) { return w.half >= 0 ? kGemmChunks / 2 : kGemmChunks; };
+  // the epilogue's view: a symmetric K piece finishes one column half of its
+  // (full-width) accumulator
+  auto epi_tile = [&](const GemmItem& w, int& m0, int& n0) {
+    item_tile(w, m0, n0);
+    if (w.ehalf > 0) n0 += TN / 2;
+  };
+  auto epi_chunks = [&](const GemmItem& w) { return w.ehalf >= 0 ? kGemmChunks / 2 : item_chunks(w); };
   if (threadIdx.x == 0) {
     abort_flag = 0;
     issued[0] = issued[1] = 0;
@@ -514,8 +524,8 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       auto retire_item = [&]() {
         if (rx >= S.end) return;
         const GemmItem w = gemm_item(P, S, cl, rx, nslots);
-        item_tile(w, rm0, rn0);
-        rnch = item_chunks(w);
+        epi_tile(w, rm0, rn0);
+        rnch = epi_chunks(w);
         rstore = (w.piece < 0 || w.fin) && (rx + S.step < S.end || !P.last_ring);
       };
       // wait until chunk h's buffer is released by its four epilogue warps,
@@ -541,8 +551,8 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       for (int x = S.x0; x < S.end && ok; x += S.step) {
         const GemmItem wi = gemm_item(P, S, cl, x, nslots);
         int m0, n0;
-        item_tile(wi, m0, n0);
-        const int nch = item_chunks(wi);
+        epi_tile(wi, m0, n0);
+        const int nch = epi_chunks(wi);
         for (int j = 0; j < nch; ++j, ++g) {
           const int e = g % NE;
           if (g >= NE) {
@@ -583,8 +593,9 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
     for (int x = S.x0; x < S.end; x += S.step, ++i) {
       const GemmItem w = gemm_item(P, S, cl, x, nslots);
       int m0, n0;
-      item_tile(w, m0, n0);
-      const int nch = item_chunks(w);
+      epi_tile(w, m0, n0);
+      const int nch = epi_chunks(w);
+      const int tc0 = w.ehalf >= 0 ? w.ehalf * (kGemmChunks / 2) : 0;   // first accumulator chunk of this view
       const int b = i & 1;
       bool got = gemm_wait(tfull0 + 8 * b, (i >> 1) & 1, limit, &abort_flag);
       tc_fence_after();
@@ -595,7 +606,37 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       // the rows' ready flag; the other waits for the flag, adds the partial
       // and runs the epilogue
       bool finish = true;
-      if (w.piece >= 0 && got) {
+      if (w.ehalf >= 0 && got) {
+        // a symmetric K piece: this piece's partial of the other column half
+        // into the workspace ([32 column quads][128 rows][4]: a warp's
+        // 16-byte stores cover 512 contiguous bytes), this warp's flag
+        // raised, then the other piece's partial of this half awaited
+        // (bounded: it runs on another cluster)
+        float4* wq = reinterpret_cast<float4*>(P.ws) + (size_t)(w.q * CL + rank) * (kGemmM * TN / 4) + rr;
+        const int oc0 = (1 - w.ehalf) * (kGemmChunks / 2);
+#pragma unroll 1
+        for (int j = set; j < kGemmChunks / 2; j += 2) {
+          float acc[32];
+          tmem_ld32(tacc + (oc0 + j) * kGemmChunk, acc);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            wq[(size_t)(j * 8 + c) * kGemmM] = make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+        }
+        __threadfence();
+        __syncwarp();
+        int32_t* mine = P.ws_cnt + ((w.key * 2 + w.piece) * CL + rank) * 8 + ew;
+        int32_t* other = P.ws_cnt + ((w.key * 2 + (1 - w.piece)) * CL + rank) * 8 + ew;
+        int ready = 0;
+        if (lane == 0) {
+          st_release_gpu(mine, 1);
+          const uint64_t t0 = global_ns();
+          while (!(ready = ld_acquire_gpu(other) == 1))
+            if (abort_flag || (int64_t)(global_ns() - t0) > limit) break;
+          if (ready) *other = 0;   // consumed: clear for the next launch
+        }
+        got = __shfl_sync(0xffffffffu, ready, 0) != 0;
+        __syncwarp();   // orders the other lanes' partial loads after lane 0's acquire
+      } else if (w.piece >= 0 && got) {
         int32_t* flag = P.ws_cnt + (w.key * CL + rank) * 8 + ew;
         if (!w.fin) {
           // layout [64 column quads][128 rows][4]: a warp's 16-byte accesses
@@ -643,7 +684,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
       float4 nxt[8];
       if (w.piece >= 0 && finish && got) {
         oq = reinterpret_cast<const float4*>(P.ws) + (size_t)((w.q ^ 1) * CL + rank) * (kGemmM * TN / 4) + rr;
-        if (last) {
+        if (last && w.ehalf < 0) {
           // this warp's rows of the partial in its chunks, [column quad][32
           // rows][16 B]: one 512-byte bulk copy per lane and column quad
           const uint32_t lbar = last0 + 8 * ew;
@@ -685,7 +726,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
           continue;
         }
         float acc[32], o[32];
-        tmem_ld32(tacc + j * kGemmChunk, acc);
+        tmem_ld32(tacc + (tc0 + j) * kGemmChunk, acc);
         if (oq) {
           // the other piece's partial: two pieces, one addition, the same
           // result whichever finished last; from the ring, or with the next
@@ -695,7 +736,7 @@ __device__ __forceinline__ void gemm_body(const GemmParams& P) {
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             cur[c] = part_smem ? *reinterpret_cast<const float4*>(wring + (j * 8 + c) * 512 + lane * 16) : nxt[c];
-          if (!part_smem && j + 2 < kGemmChunks) {
+          if (!part_smem && j + 2 < nch) {
 #pragma unroll
             for (int c = 0; c < 8; ++c) nxt[c] = __ldcg(oq + (size_t)((j + 2) * 8 + c) * kGemmM);
           }

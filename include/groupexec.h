@@ -113,9 +113,10 @@ typedef struct tf_layout tf_layout;
  * count), and for GEMM-epilogue groups (which always run as CTA pairs;
  * bits 16-17 are ignored) bits 18-19 the K blocks of 64 per operand ring slot (0 = chosen,
  * 1, 2), bits 20-21 the schedule (0 = chosen, 1 = round robin with the last
- * round's tiles cut along K into two pieces, 2 = equal shares of all tiles'
- * K steps, 3 = round robin with the last round's tiles cut into their two
- * column halves, the choice for CTA pairs with 256-column tiles), bits 22-23
+ * round's tiles cut along K into two equal pieces, each finishing one column
+ * half with the other's partial sums, the choice from 64 K blocks, 2 = equal
+ * shares of all tiles' K steps, 3 = round robin with the last round's tiles
+ * cut into their two column halves, the choice below 64 K blocks), bits 22-23
  * the columns of a CTA pair's tile (0 or 1 = 256, 2 = 128, 3 = 224); bits 24-25 = how an
  * elementwise group writes its output: 0 default (= 2), 1 the CTA's tile
  * staged in shared memory and stored by one TMA store, 2 each warp's slice
