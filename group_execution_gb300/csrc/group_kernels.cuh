@@ -552,10 +552,14 @@ __device__ __forceinline__ void ew_body(const GroupParams& P) {
           *reinterpret_cast<float4*>(b + swz(lr, j0)) = make_float4(o[0], o[1], o[2], o[3]);
           *reinterpret_cast<float4*>(b + swz(lr, j0 + 1)) = make_float4(o[4], o[5], o[6], o[7]);
         } else if (P.out_tma == 2) {
-          // this warp's 32 x 8 slice, row-major, stored by its own lane 0
+          // this warp's 32 x 8 slice, row-major, stored by its own lane 0;
+          // lanes 4-7 of every eight write their rows' halves in the other
+          // order, so that each eight lanes' 16-byte stores cover all banks
           float4* b = reinterpret_cast<float4*>(ob + warp * (kTileR * 32) + lr * 32);
-          b[0] = make_float4(o[0], o[1], o[2], o[3]);
-          b[1] = make_float4(o[4], o[5], o[6], o[7]);
+          const float4 lo = make_float4(o[0], o[1], o[2], o[3]), hi = make_float4(o[4], o[5], o[6], o[7]);
+          const int h = (lr >> 2) & 1;
+          b[h] = h ? hi : lo;
+          b[h ^ 1] = h ? lo : hi;
         } else {
           // each lane writes 32 contiguous bytes of its row: whole sectors
           const int r = r0 + lr, c = c0 + lc0;
