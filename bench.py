@@ -27,7 +27,7 @@ Multi-GPU: the fused groups run as replicas -- every rank runs the same plan
 on its own data (data-parallel replicas, weak scaling; the headline needs no
 collective).  The one exchange step of the path, the AllReduce of the packed
 gradient buckets, is the `exchange` row: NCCL over the ranks' bucket byte
-ranges, each started as soon as its bucket's ready word is set.
+ranges, each started as soon as its bucket's count says it is complete.
 `--impl reference` times the CPU oracle on a bounded sample instead.
 """
 from __future__ import annotations
@@ -771,7 +771,7 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
 
     # the same gradients cut into AllReduce buckets by an 8 MiB fusion
     # threshold: packed one launch per bucket (replayed from a CUDA graph),
-    # and every bucket in one launch with per-bucket ready words; ready_us:
+    # and every bucket in one launch with per-bucket chunk counts; ready_us:
     # when a second stream waiting on each bucket's word passes it, from the
     # launch's start (an L2 flush runs first on the launching stream, so that
     # every wait is enqueued before the pack starts)
@@ -804,7 +804,7 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
         torch.cuda.synchronize()
         for k in range(nb):
             ready[k].append(st.elapsed_time(evs[k]) * 1e3)
-    # the same launch with one more CTA consuming the ready words on the
+    # the same launch with one more CTA consuming the bucket counts on the
     # device: how long before the last packing CTA finished each bucket was
     # seen ready (median of 10)
     tms = torch.zeros(nb + 1, dtype=torch.int64, device="cuda")

@@ -311,7 +311,7 @@ class TensorFusion:
 
     def pack_buckets_observed(self, scale, buf, times, seq_offset=0, wait_limit_ns=100_000_000, stream=None):
         """pack_buckets with one more CTA in the launch that watches the
-        buckets' ready words: times (int64 device tensor, n_buckets + 1)
+        buckets' counts: times (int64 device tensor, n_buckets + 1)
         receives when each bucket was seen ready (device global timer, ns)
         and, last, when the packing CTAs finished."""
         _lib.check(self.lib.tf_pack_buckets_observed(self.h, C.c_float(scale), C.c_void_p(buf.data_ptr()),
@@ -325,7 +325,7 @@ class TensorFusion:
 
     def bucket_ready(self, b):
         """True once bucket b of the last pack_buckets launch is written
-        (a synchronous read of its ready word)."""
+        (a synchronous read of its count)."""
         r = C.c_int32()
         _lib.check(self.lib.tf_bucket_ready(self.h, b, C.byref(r)))
         return bool(r.value)

@@ -130,11 +130,14 @@ struct tf_layout {
   int nchunks = 0;
   std::vector<int32_t> chunk_begin;  // first chunk of every tensor, [n + 1]
   // AllReduce buckets packed in one launch: device block of the chunk ->
-  // bucket map [nchunks], chunks per bucket [nb], counters [nb] and ready
-  // words [nb]; seq = the last bucketed pack enqueued (ready words hold it)
+  // bucket map [nchunks], chunks per bucket [nb] and counts [nb] (chunks
+  // written by every bucketed pack so far, never reset); seq = the number of
+  // bucketed packs enqueued with this table: bucket b of the last one is
+  // complete once its count reaches seq * bucket_chunks[b]
   int32_t nb = 0;
   int32_t* d_bucket = nullptr;
   uint32_t seq = 0;
+  std::vector<uint32_t> bucket_chunks;
   // the table's users: per stream, an event recorded after the last pack or
   // stream wait enqueued there that reads the table
   std::vector<std::pair<cudaStream_t, cudaEvent_t>> users;
@@ -1489,12 +1492,14 @@ fg_status tf_layout_set_buckets(tf_layout* l, int32_t nb, const int32_t* bounds)
   if (nb <= 0 || bounds[0] != 0 || bounds[nb] != l->n) return err(FG_EINVAL, "bucket bounds must run from 0 to n");
   for (int32_t b = 0; b < nb; ++b)
     if (bounds[b + 1] <= bounds[b]) return err(FG_EINVAL, "bucket bounds must increase strictly");
-  // chunk -> bucket, then chunks per bucket; counters and ready words zero
-  std::vector<int32_t> host((size_t)l->nchunks + 3 * (size_t)nb, 0);
+  // chunk -> bucket, then chunks per bucket; counts zero
+  std::vector<int32_t> host((size_t)l->nchunks + 2 * (size_t)nb, 0);
+  std::vector<uint32_t> per(nb);
   for (int32_t b = 0; b < nb; ++b) {
     const int c0 = l->chunk_begin[bounds[b]], c1 = l->chunk_begin[bounds[b + 1]];
     for (int c = c0; c < c1; ++c) host[c] = b;
     host[(size_t)l->nchunks + b] = c1 - c0;
+    per[b] = (uint32_t)(c1 - c0);
   }
   int32_t* d = nullptr;
   cudaError_t e = cudaMalloc(&d, sizeof(int32_t) * host.size());
@@ -1514,6 +1519,7 @@ fg_status tf_layout_set_buckets(tf_layout* l, int32_t nb, const int32_t* bounds)
   l->d_bucket = d;
   l->nb = nb;
   l->seq = 0;
+  l->bucket_chunks = std::move(per);
   return FG_OK;
 }
 
@@ -1528,8 +1534,7 @@ fg_status pack_buckets(tf_layout* l, float scale, void* buf, void* stream, uint6
   TfBuckets bk;
   bk.chunk_bucket = l->d_bucket;
   bk.nchunks = l->d_bucket + l->nchunks;
-  bk.count = l->d_bucket + l->nchunks + l->nb;
-  bk.ready = reinterpret_cast<uint32_t*>(l->d_bucket + l->nchunks + 2 * l->nb);
+  bk.count = reinterpret_cast<uint32_t*>(l->d_bucket + l->nchunks + l->nb);
   bk.seq = l->seq + 1;
   // every CTA resident at once, the observer's included
   const int resident = tf_pack_resident(nsm);
@@ -1577,8 +1582,11 @@ fg_status tf_bucket_wait(tf_layout* l, int32_t b, void* stream) {
   if (b < 0 || b >= l->nb) return err(FG_EINVAL, "bucket out of range");
   WaitValueFn fn = wait_value_fn();
   if (!fn) return err(FG_EUNSUPPORTED, "cuStreamWaitValue32 is not available");
-  const int32_t* ready = l->d_bucket + l->nchunks + 2 * l->nb + b;
-  CUresult r = fn(static_cast<CUstream>(stream), reinterpret_cast<CUdeviceptr>(ready), l->seq, CU_STREAM_WAIT_VALUE_GEQ);
+  // the count reaches this pack's total (a cyclic comparison, as the count
+  // wraps modulo 2^32)
+  const int32_t* count = l->d_bucket + l->nchunks + l->nb + b;
+  const uint32_t target = l->seq * l->bucket_chunks[b];
+  CUresult r = fn(static_cast<CUstream>(stream), reinterpret_cast<CUdeviceptr>(count), target, CU_STREAM_WAIT_VALUE_GEQ);
   if (r != CUDA_SUCCESS) return err(FG_ECUDA, "cuStreamWaitValue32 failed (" + std::to_string((int)r) + ")");
   const cudaError_t e = note_table_use(l, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_err(e, "cudaEventRecord(bucket table use)");
@@ -1590,9 +1598,9 @@ fg_status tf_bucket_ready(const tf_layout* l, int32_t b, int32_t* ready) {
   if (!l->nb || !l->seq) return err(FG_EINVAL, "no bucketed pack has been enqueued");
   if (b < 0 || b >= l->nb) return err(FG_EINVAL, "bucket out of range");
   uint32_t v = 0;
-  cudaError_t e = cudaMemcpy(&v, l->d_bucket + l->nchunks + 2 * l->nb + b, sizeof(v), cudaMemcpyDeviceToHost);
-  if (e != cudaSuccess) return cuda_err(e, "reading a bucket's ready word");
-  *ready = (int32_t)(v - l->seq) >= 0 ? 1 : 0;
+  cudaError_t e = cudaMemcpy(&v, l->d_bucket + l->nchunks + l->nb + b, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_err(e, "reading a bucket's count");
+  *ready = (int32_t)(v - l->seq * l->bucket_chunks[b]) >= 0 ? 1 : 0;
   return FG_OK;
 }
 

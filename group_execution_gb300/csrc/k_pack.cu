@@ -45,18 +45,18 @@ __device__ __forceinline__ void zero_pad(uint8_t* p, int bytes) {
   for (int i = threadIdx.x * 2; i < bytes; i += kPackThreads * 2) *reinterpret_cast<uint16_t*>(p + i) = 0;
 }
 
-// The observer of an observed launch (one thread): each bucket's ready word,
-// in bucket order, read with acquire until it holds the watched sequence
-// number, each wait bounded.
+// The observer of an observed launch (one thread): each bucket's count, in
+// bucket order, read with acquire until it reaches the watched launch's
+// total, each wait bounded.
 __device__ void observe_buckets(const TfBuckets& bk) {
-  const uint32_t want = bk.seq + bk.seq_offset;
   bool dead = false;
   for (int b = 0; b < bk.nb; ++b) {
+    const uint32_t want = (bk.seq + bk.seq_offset) * (uint32_t)bk.nchunks[b];
     unsigned long long t = 0;
     if (!dead) {
       const uint64_t t0 = global_ns();
       for (;;) {
-        const uint32_t v = (uint32_t)ld_acquire_gpu(reinterpret_cast<const int32_t*>(bk.ready + b));
+        const uint32_t v = (uint32_t)ld_acquire_gpu(reinterpret_cast<const int32_t*>(bk.count + b));
         const uint64_t now = global_ns();
         if ((int32_t)(v - want) >= 0) {
           t = now;
@@ -146,19 +146,13 @@ __global__ void __launch_bounds__(kPackThreads) tf_pack_kernel(const TfChunk* __
       nx = s_nx[it & 1];
       if (nx < nchunks) cn = s_cn[it & 1];
     }
-    if (bk.ready) {
+    if (bk.count) {
       // count the chunk for its bucket: the barrier orders every thread's
-      // stores before thread 0's release (cumulative); the count that
-      // completes the bucket acquires the other CTAs' chunks and publishes
-      // the bucket
+      // stores before thread 0's release reduction (cumulative), which
+      // returns nothing, so thread 0 does not wait for it; a reader that
+      // sees the bucket's total with acquire sees every chunk counted
       if (!claim) __syncthreads();
-      if (threadIdx.x == 0) {
-        const int b = bk.chunk_bucket[ci];
-        if (atom_add_acq_rel_gpu(&bk.count[b], 1) == bk.nchunks[b] - 1) {
-          bk.count[b] = 0;   // every chunk of this launch has counted: ready for the next
-          st_release_gpu(reinterpret_cast<int32_t*>(bk.ready + b), (int32_t)bk.seq);
-        }
-      }
+      if (threadIdx.x == 0) red_add_release_gpu(bk.count + bk.chunk_bucket[ci], 1u);
     }
     if (nx >= nchunks) break;
     ci = nx;

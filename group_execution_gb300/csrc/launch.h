@@ -48,19 +48,20 @@ struct TfChunk {
   int32_t pad_bytes;    // bytes to zero after the chunk (last chunk of a tensor)
 };
 // Per-bucket readiness for a one-launch pack of several AllReduce buckets
-// (all null otherwise): the CTA that counts a bucket's last chunk resets its
-// counter and stores seq in its ready word with release semantics.
+// (all null otherwise): every chunk adds one to its bucket's count with a
+// release reduction; the count is never reset.
 struct TfBuckets {
   const int32_t* chunk_bucket = nullptr;   // bucket of every chunk of the launch
   const int32_t* nchunks = nullptr;        // chunks per bucket
-  int32_t* count = nullptr;                // chunks of the bucket written in this launch
-  uint32_t* ready = nullptr;               // last launch whose chunks of the bucket are all written
-  uint32_t seq = 0;
-  // observed launch: CTA 0 does not pack but watches the ready words, in
-  // bucket order, and writes to observe[b] the global timer when it saw
-  // bucket b reach sequence seq + seq_offset (0 if it gave up after
-  // limit_ns, with DEVERR_TIMEOUT in err); the packing CTAs write their
-  // latest finishing time to observe[nb]
+  uint32_t* count = nullptr;               // chunks of the bucket written by every bucketed launch so far
+                                           // (never reset; wraps modulo 2^32)
+  uint32_t seq = 0;                        // this launch's number: bucket b is complete once count[b]
+                                           // reaches seq * nchunks[b] (cyclic comparison)
+  // observed launch: CTA 0 does not pack but watches the counts, in bucket
+  // order, and writes to observe[b] the global timer when it saw bucket b
+  // complete for launch seq + seq_offset (0 if it gave up after limit_ns,
+  // with DEVERR_TIMEOUT in err); the packing CTAs write their latest
+  // finishing time to observe[nb]
   unsigned long long* observe = nullptr;
   int32_t nb = 0;
   uint32_t seq_offset = 0;

@@ -472,15 +472,18 @@ fg_status tf_unpack_range(const tf_layout* l, int32_t first, int32_t count, floa
  * Replaces an earlier table without synchronizing: the old table stays
  * allocated until the events recorded after every pack and stream wait that
  * read it have completed (checked at the next replacement, waited for by
- * tf_layout_destroy).  Allocates the per-bucket device words (chunk counters
- * and ready words) and restarts the sequence numbers, so call it between
- * steps: a wait enqueued afterwards refers to the new table.  FG_EINVAL for a
+ * tf_layout_destroy).  Allocates the per-bucket device counts of written
+ * chunks (zero) and restarts the launch numbering, so call it between steps:
+ * a wait enqueued afterwards refers to the new table.  FG_EINVAL for a
  * malformed table.
  *
  * tf_pack_buckets: packs every tensor in one launch, with tf_pack's result,
- * and marks each bucket ready the moment its last chunk has been written:
- * the bucket's ready word receives this launch's sequence number (release
- * at GPU scope, after the bucket's bytes).  FG_EINVAL without a bucket table.
+ * and counts every chunk written for its bucket (a release reduction at GPU
+ * scope, after the chunk's bytes, into a count that is never reset): bucket
+ * b of the k-th launch since the table was set is complete, all its bytes
+ * visible, once its count reaches k times its chunk count (compared
+ * cyclically: the count wraps modulo 2^32).  FG_EINVAL without a bucket
+ * table.
  *
  * tf_bucket_wait: makes cuda_stream wait, in the GPU's front end (no kernel,
  * no SM), until bucket b of the most recently enqueued tf_pack_buckets launch
@@ -490,24 +493,25 @@ fg_status tf_unpack_range(const tf_layout* l, int32_t first, int32_t count, floa
  * is out of range.
  *
  * tf_bucket_ready: *ready = 1 if bucket b of the most recently enqueued
- * tf_pack_buckets launch has been marked ready, else 0 (a synchronous read
- * of the bucket's ready word; host-side polling).  The read is a cudaMemcpy
+ * tf_pack_buckets launch is complete, else 0 (a synchronous read of the
+ * bucket's count; host-side polling).  The read is a cudaMemcpy
  * on the legacy default stream, so it also waits for work on that stream
  * and on every blocking stream: to watch a pack while it runs, enqueue the
  * pack on a non-blocking stream (PyTorch's side streams are).  FG_EINVAL as
  * for tf_bucket_wait.  Launches of one layout must be ordered (one stream, or
- * streams that wait for each other): they share the bucket counters. */
+ * streams that wait for each other): they share the bucket counts. */
 fg_status tf_layout_set_buckets(tf_layout* l, int32_t n_buckets, const int32_t* bounds);
 fg_status tf_pack_buckets(tf_layout* l, float scale, void* fusion_buf, void* cuda_stream);
 fg_status tf_bucket_wait(tf_layout* l, int32_t bucket, void* cuda_stream);
 fg_status tf_bucket_ready(const tf_layout* l, int32_t bucket, int32_t* ready);
 
-/* tf_pack_buckets with a device-side consumer of the ready words inside the
- * same launch (DisCo, Introduction: a bucket's AllReduce can start as soon
- * as its tensors are in the fusion buffer; a collective's own kernel would
- * watch the words this way).  One extra CTA of the launch packs nothing: it
- * reads each bucket's ready word in bucket order (acquire, polled) until it
- * holds this launch's sequence number plus seq_offset, and writes the
+/* tf_pack_buckets with a device-side consumer of the bucket counts inside
+ * the same launch (DisCo, Introduction: a bucket's AllReduce can start as
+ * soon as its tensors are in the fusion buffer; a collective's own kernel
+ * would watch the counts this way).  One extra CTA of the launch packs
+ * nothing: it reads each bucket's count in bucket order (acquire, polled)
+ * until it reaches the total of the launch seq_offset launches after this
+ * one (0: this one), and writes the
  * device's global timer (ns) at that moment to times[b]; the packing CTAs
  * write the latest time any of them finished to times[n_buckets].  times:
  * device, 8-byte aligned, n_buckets + 1 entries, caller-owned.  Each wait is

@@ -153,7 +153,7 @@ def _bucketed(sizes, threshold, seed=0):
 def test_pack_buckets_one_launch():
     """Every AllReduce bucket packed in one launch: the buffer equals the
     oracle's bytes, and after each of three launches every bucket reads as
-    ready (its counter was reset by the bucket's last chunk each time)."""
+    ready (its count reached that launch's total each time)."""
     sizes = W.tensor_fusion_sizes(0)
     tf, bounds, ref = _bucketed(sizes, 8 << 20)
     nb = len(bounds) - 1
@@ -182,7 +182,7 @@ def test_pack_buckets_small_and_single():
 
 def test_bucket_wait_orders_each_bucket():
     """A second stream waits for each bucket in turn (a stream-ordered wait
-    on its ready word) and copies that bucket's bytes out while the one pack
+    on its count) and copies that bucket's bytes out while the one pack
     launch may still be running: every copy equals the oracle's bytes."""
     sizes = W.tensor_fusion_sizes(0)
     tf, bounds, ref = _bucketed(sizes, 8 << 20)
@@ -203,8 +203,8 @@ def test_bucket_wait_orders_each_bucket():
 
 
 def test_bucket_ready_words_seen_by_a_device_consumer_during_the_launch():
-    """A device-side consumer of the ready words (one CTA of the pack launch,
-    polling each bucket's word in order) sees the first buckets ready while
+    """A device-side consumer of the bucket counts (one CTA of the pack
+    launch, polling each bucket's count in order) sees the first buckets ready while
     other CTAs are still packing: the first bucket well before the launch's
     last packing CTA finishes.  The buffer still holds tf_pack's bytes."""
     from group_execution_gb300 import plan_threshold
