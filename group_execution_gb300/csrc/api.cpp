@@ -406,6 +406,8 @@ void fill_leaf_desc(LeafDesc& d, const LeafUse& l, int stage_off, int map_idx, i
     d.d[k] = l.map.d[k];
     d.m[k] = l.map.m[k];
     d.s[k] = l.map.s[k];
+    d.dd[k] = fast_div(l.map.d[k]);
+    d.dm[k] = fast_div(l.map.m[k]);
   }
 }
 
@@ -449,6 +451,8 @@ void prepare_group(GroupExec& ge, const BuildOpts& o, int nsm) {
       x.d[k] = mp.d[k];
       x.m[k] = mp.m[k];
       x.s[k] = mp.s[k];
+      x.dd[k] = fast_div(mp.d[k]);
+      x.dm[k] = fast_div(mp.m[k]);
     }
   }
   std::copy(cg.epi.begin(), cg.epi.end(), p.epi);

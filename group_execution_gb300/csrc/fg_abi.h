@@ -94,6 +94,29 @@ enum LeafClass : int {
 
 constexpr int kMaxTerms = 4;
 
+// Division by an invariant divisor d of dividends x < 2^31 (Granlund and
+// Montgomery, "Division by Invariant Integers using Multiplication"):
+// floor(x / d) = floor(x * mul / 2^sh) with l = ceil(log2 d),
+// mul = ceil(2^(31 + l) / d) < 2^32 and sh = 31 + l.  With x < 2^31,
+// x * mul / 2^sh exceeds x / d by less than 2^-l <= 1/d, which never
+// reaches the next integer.  A divisor above 2^31 gives mul = 0 (quotient 0).
+struct FastDiv {
+  uint32_t mul;
+  int32_t sh;
+};
+#ifndef __CUDACC_RTC__
+inline FastDiv fast_div(int64_t d) {
+  FastDiv f{0u, 32};
+  if (d <= 0 || d > (int64_t(1) << 31)) return f;
+  int l = 0;
+  while ((int64_t(1) << l) < d) ++l;
+  const uint64_t num = uint64_t(1) << (31 + l);
+  f.mul = (uint32_t)((num + (uint64_t)d - 1) / (uint64_t)d);
+  f.sh = 31 + l;
+  return f;
+}
+#endif
+
 struct LeafDesc {
   int32_t cls;
   int32_t stage_off;     // byte offset of this leaf's boxes inside a stage
@@ -101,6 +124,7 @@ struct LeafDesc {
   int32_t nterms;        // gather
   const float* ptr;      // gather base pointer (filled at launch)
   int64_t d[kMaxTerms], m[kMaxTerms], s[kMaxTerms];
+  FastDiv dd[kMaxTerms], dm[kMaxTerms];   // the divisions by d[k] and m[k]
   // a tuple's field is read at g - shift (staged boxes move by shift_r rows
   // and shift_c columns); gathers skip indices outside [0, numel)
   int64_t shift, numel;
@@ -116,6 +140,7 @@ struct XOutDesc {
   float* ptr;            // filled at launch
   int32_t cls, nterms;
   int64_t d[kMaxTerms], m[kMaxTerms], s[kMaxTerms];
+  FastDiv dd[kMaxTerms], dm[kMaxTerms];
 };
 
 // ---- kernel parameter blocks -------------------------------------------------

@@ -467,6 +467,21 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 __device__ __forceinline__ void st_release_gpu(int32_t* p, int32_t v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+// floor(x / d) for x < 2^31 by d's multiplier (FastDiv).
+__device__ __forceinline__ uint32_t div_inv(uint32_t x, FastDiv f) {
+  return (uint32_t)(((uint64_t)x * f.mul) >> f.sh);
+}
+// A gather's source offset, sum_k ((g / d_k) % m_k) * s_k, for g < 2^31.
+template <class Desc>
+__device__ __forceinline__ uint32_t digit_offset(const Desc& G, uint32_t g) {
+  uint32_t f = 0;
+  for (int q = 0; q < G.nterms; ++q) {
+    const uint32_t a = div_inv(g, G.dd[q]);
+    f += (a - div_inv(a, G.dm[q]) * (uint32_t)G.m[q]) * (uint32_t)G.s[q];
+  }
+  return f;
+}
+
 // A reduction with release semantics at GPU scope and no result: the thread
 // does not wait for it.
 __device__ __forceinline__ void red_add_release_gpu(uint32_t* p, uint32_t v) {

@@ -84,17 +84,16 @@ struct GemmEnv {
   __device__ __forceinline__ void gather(int leaf, float (&t)[8]) const {
     const LeafDesc& G = P.leaves[leaf];
     const int r = r0 + rr;
-#pragma unroll 1
+    uint32_t f[8];
+#pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int c = cc0 + q8 + k;
-      float v = 0.f;
-      if (r < P.M && c < P.N) {
-        const uint32_t g = (uint32_t)r * (uint32_t)P.N + (uint32_t)c;
-        uint32_t f = 0;
-        for (int q = 0; q < G.nterms; ++q) f += ((g / (uint32_t)G.d[q]) % (uint32_t)G.m[q]) * (uint32_t)G.s[q];
-        v = __ldg(G.ptr + f);
-      }
-      t[k] = v;
+      f[k] = r < P.M && c < P.N ? digit_offset(G, (uint32_t)r * (uint32_t)P.N + (uint32_t)c) : 0u;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int c = cc0 + q8 + k;
+      t[k] = r < P.M && c < P.N ? __ldg(G.ptr + f[k]) : 0.f;
     }
   }
 };

@@ -89,24 +89,25 @@ struct TileEnv {
   __device__ __forceinline__ void gather(int leaf, float (&t)[8]) const {
     const LeafDesc& G = P.leaves[leaf];
     const int r = r0 + lr;
-#pragma unroll 1
+    // every offset first, then the eight loads together (one memory latency,
+    // not eight)
+    uint32_t f[8];
+    bool ok[8];
+#pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int c = c0 + lc0 + k;
-      float v = 0.f;
-      if (r < P.FR && c < P.FC) {
-        uint32_t g = (uint32_t)r * (uint32_t)P.FC + (uint32_t)c;
-        bool in = true;
-        if (G.shift) {
-          // a tuple's field: other fields' points map outside it
-          in = (int64_t)g >= G.shift;
-          g = (uint32_t)((int64_t)g - G.shift);
-        }
-        uint32_t f = 0;
-        for (int q = 0; q < G.nterms; ++q) f += ((g / (uint32_t)G.d[q]) % (uint32_t)G.m[q]) * (uint32_t)G.s[q];
-        if (in && (!G.shift || (int64_t)f < G.numel)) v = __ldg(G.ptr + f);
+      ok[k] = r < P.FR && c < P.FC;
+      uint32_t g = (uint32_t)r * (uint32_t)P.FC + (uint32_t)c;
+      if (G.shift) {
+        // a tuple's field: other fields' points map outside it
+        ok[k] = ok[k] && (int64_t)g >= G.shift;
+        g = (uint32_t)((int64_t)g - G.shift);
       }
-      t[k] = v;
+      f[k] = ok[k] ? digit_offset(G, g) : 0u;
+      if (G.shift) ok[k] = ok[k] && (int64_t)f[k] < G.numel;
     }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t[k] = ok[k] ? __ldg(G.ptr + f[k]) : 0.f;
   }
   // Extra output j: this thread's eight frame points, written where the
   // output's map sends them: rows of 32 contiguous bytes for the identity; a
@@ -150,9 +151,7 @@ struct TileEnv {
       for (int k = 0; k < 8; ++k) {
         if (c + k >= P.FC) break;
         const uint32_t g = (uint32_t)r * (uint32_t)P.FC + (uint32_t)(c + k);
-        uint32_t f = 0;
-        for (int q = 0; q < X.nterms; ++q) f += ((g / (uint32_t)X.d[q]) % (uint32_t)X.m[q]) * (uint32_t)X.s[q];
-        X.ptr[f] = v[k];
+        X.ptr[digit_offset(X, g)] = v[k];
       }
     }
   }
@@ -202,17 +201,12 @@ struct DirectEnv {
   // f = sum_k ((g / d_k) % m_k) * s_k over g = r*FC + c (small frames)
   __device__ __forceinline__ void gather(int leaf, float (&t)[8]) const {
     const LeafDesc& G = P.leaves[leaf];
-#pragma unroll 1
-    for (int k = 0; k < 8; ++k) {
-      float v = 0.f;
-      if (c0 + k < P.FC) {
-        const uint32_t g = (uint32_t)r0 * (uint32_t)P.FC + (uint32_t)(c0 + k);
-        uint32_t f = 0;
-        for (int q = 0; q < G.nterms; ++q) f += ((g / (uint32_t)G.d[q]) % (uint32_t)G.m[q]) * (uint32_t)G.s[q];
-        v = __ldg(G.ptr + f);
-      }
-      t[k] = v;
-    }
+    uint32_t f[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      f[k] = c0 + k < P.FC ? digit_offset(G, (uint32_t)r0 * (uint32_t)P.FC + (uint32_t)(c0 + k)) : 0u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t[k] = c0 + k < P.FC ? __ldg(G.ptr + f[k]) : 0.f;
   }
 };
 

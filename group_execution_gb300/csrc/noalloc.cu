@@ -177,6 +177,8 @@ extern "C" fg_status fg_row_reduce_noalloc(int32_t opcode, const float* x, int64
     L.d[0] = 1;
     L.m[0] = rows * cols;
     L.s[0] = 1;
+    L.dd[0] = fast_div(1);
+    L.dm[0] = fast_div(rows * cols);
     p.stage_bytes = p.tx_bytes = 0;
     p.nstages = 4;
   }
