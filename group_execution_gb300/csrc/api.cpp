@@ -986,6 +986,8 @@ bool swap_last_direct(void* stream, bool direct) {
   static std::mutex mu;
   static std::unordered_map<void*, bool> last;
   std::lock_guard<std::mutex> g(mu);
+  // bounded: forgetting the streams costs at most one early start each
+  if (last.size() >= 1024 && !last.count(stream)) last.clear();
   bool& v = last[stream];
   const bool prev = v;
   v = direct;
