@@ -562,14 +562,19 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
     l2r = torch.zeros(256 << 20, dtype=torch.uint8, device="cuda")
 
     def timed(fn, reps=10, flush=True, inner=None):
-        """Median and min ms of `inner` back-to-back calls (L2 flushed first
+        """Typical and min ms of `inner` back-to-back calls (L2 flushed first
         when asked: written, then evicted clean), over `reps` repetitions.
-        Without a flush the calls run
-        ten at a time by default: a single call after a synchronize would also
-        count the host's launch work, during which the device is idle (after
-        a flush, the flush kernel covers it)."""
+        Without a flush the calls run ten at a time by default: a single call
+        after a synchronize would also count the host's launch work, during
+        which the device is idle (after a flush, the flush kernel covers it);
+        the typical value is the median.  A flushed single call is timed 20
+        times and the typical value is the mean of the middle half: event
+        times move in steps of about 1 us on this GPU, and the median of such
+        samples lands on one step or the next from run to run."""
         if inner is None:
             inner = 1 if flush else 10
+        if flush and inner == 1:
+            reps = max(reps, 20)
         fn()
         torch.cuda.synchronize()
         ts = []
@@ -587,6 +592,9 @@ def secondary_rows(torch, W, graph_from_spec, plan, spec, dv, out, hbm, bf16, bf
             b.record()
             torch.cuda.synchronize()
             ts.append(a.elapsed_time(b) / inner)
+        if flush and inner == 1:
+            mid = sorted(ts)[len(ts) // 4: len(ts) - len(ts) // 4]
+            return sum(mid) / len(mid), min(ts)
         return statistics.median(ts), min(ts)
 
     def graphed(fn, n=1):
