@@ -253,3 +253,58 @@ def test_device_consumer_wait_is_bounded_and_reported():
     tf.sync()
     assert (times.cpu().numpy()[:2] > 0).all()
     assert np.array_equal(buf.cpu().numpy(), PK.pack(xs, 1.0))
+
+
+def test_pack_of_unpack_reproduces_the_buffer():
+    """Unpack then pack with scale 1 gives back the bf16 buffer byte for byte
+    (data bytes: bf16 -> fp32 -> bf16 is exact; padding: zero), over ragged
+    tensors; with an fp32 buffer, pack then unpack with scale 1 is the
+    identity on the tensors."""
+    sizes = [1, 7, 8192, 8193, 3 * 8192 - 5, 0, 65536 + 17]
+    xs = W.tensor_fusion_inputs(sizes, 4)
+    dev = [torch.from_numpy(x).cuda() for x in xs]
+    tf = TensorFusion(dev)
+    buf = torch.empty((tf.total_bytes,), dtype=torch.uint8, device="cuda")
+    tf.pack(0.125, buf)
+    tf.unpack(1.0, buf)
+    buf2 = torch.full((tf.total_bytes,), 0xAB, dtype=torch.uint8, device="cuda")
+    tf.pack(1.0, buf2)
+    tf.sync()
+    np.testing.assert_array_equal(buf2.cpu().numpy(), buf.cpu().numpy())
+    dev32 = [torch.from_numpy(x).cuda() for x in xs]
+    tf32 = TensorFusion(dev32, "f32")
+    b32 = torch.empty((tf32.total_bytes,), dtype=torch.uint8, device="cuda")
+    tf32.pack(1.0, b32)
+    for d in dev32:
+        d.fill_(float("nan"))
+    tf32.unpack(1.0, b32)
+    tf32.sync()
+    for d, x in zip(dev32, xs):
+        np.testing.assert_array_equal(d.cpu().numpy(), x)
+
+
+def test_bucket_counts_over_many_launches_and_a_new_table():
+    """The bucket counts are never reset: after each of 12 bucketed launches
+    every bucket reads complete, a stream waiting on the last launch's
+    totals passes, and a new bucket table starts the counting over (its
+    buckets read complete after its first launch)."""
+    from group_execution_gb300 import plan_threshold
+    sizes = W.tensor_fusion_sizes(0)[:60]
+    tf, bounds, ref = _bucketed(sizes, 2 << 20)
+    nb = len(bounds) - 1
+    buf = torch.empty((tf.total_bytes,), dtype=torch.uint8, device="cuda")
+    s2 = torch.cuda.Stream()
+    for _ in range(12):
+        tf.pack_buckets(0.125, buf)
+        torch.cuda.synchronize()
+        assert all(tf.bucket_ready(b) for b in range(nb))
+    for b in range(nb):
+        tf.bucket_wait(b, s2)
+    s2.synchronize()
+    np.testing.assert_array_equal(buf.cpu().numpy(), ref)
+    bounds2 = plan_threshold(list(sizes), 8 << 20)
+    tf.set_buckets(bounds2)
+    tf.pack_buckets(0.125, buf)
+    torch.cuda.synchronize()
+    assert all(tf.bucket_ready(b) for b in range(len(bounds2) - 1))
+    np.testing.assert_array_equal(buf.cpu().numpy(), ref)
