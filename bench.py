@@ -13,9 +13,9 @@ through the C ABI with host buffers, the CPU oracle's throughput on a bounded
 sample, and `rows`: every other hot-path row measured in the same process,
 three significant digits each (us = microseconds per run: the median of
 back-to-back runs, or for a flushed single launch the mean of the middle
-half of 20 samples; x = speed-up
-over one kernel per operator, frac = fraction of the measured HBM copy peak,
-frac_bf16 = of the measured bf16 peak): the diamond fused and unfused, the
+half of 20 samples; x = speed-up over one kernel per operator, frac =
+fraction of the measured HBM copy peak, frac_bf16 = of the measured bf16
+peak): the diamond fused and unfused, the
 RNNLM chain (1 and 2 groups; as is and scaled to [65536, 1024]), row sums,
 the diamond with P returned under the three explicit-fusion plans, the tuple
 concatenation, the MLP pattern group, pack and unpack, the AllReduce buckets,
