@@ -226,13 +226,13 @@ struct GemmParams {
   int32_t inject;                      // failure injection: 1 = the producers issue no loads
   int32_t last_ring;                   // 1: the CTA's last item stages its results in the idle operand
                                        // ring (which holds 4 x TN x 128 bytes); 0: as every other item
-  // work units: a cluster's tiles (the pair's 256 x 256 tile, or the two
-  // pairs' 256 x 512) in row-major order
+  // work units: the pairs' 256-row x TN-column tiles in row-major order
   int32_t nunits;
   // round-robin schedule: units [0, nfull) run whole; each later unit runs
   // as split = 2 pieces along K, ring slots [0, split_at) and
-  // [split_at, nslots); the first publishes its partial accumulator in the
-  // workspace, the second adds it and runs the epilogue
+  // [split_at, nslots); without ksym the first publishes its partial
+  // accumulator in the workspace and the second adds it and runs the
+  // epilogue
   int32_t nfull, split, split_at;
   // nsplit_n = 1: the split units are cut into their two column halves
   // instead (each over all of K, on a pair of its own: no partial sums)

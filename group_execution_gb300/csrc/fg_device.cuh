@@ -400,8 +400,8 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uin
 }
 // Arrives once on the mbarrier at `bar` in every CTA of the cluster whose bit
 // is set in `mask` when every 2-SM MMA issued so far by this thread has
-// completed (the pair's two CTAs; a 4-CTA cluster also releases a ring slot
-// to the other pair's producers this way).
+// completed (the pair's two CTAs: both producers get the ring slot back, both
+// epilogues the accumulator).
 __device__ __forceinline__ void tc_commit_mask(uint32_t bar, uint16_t mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(

@@ -194,8 +194,10 @@ __device__ __forceinline__ GemmSched gemm_sched(const GemmParams& P, int cl, int
 // One item: a whole unit, one K piece (ring slots [sl0, sl1)) of a unit cut
 // in two, or one column half of a unit (half = 0 or 1, all of K).  q indexes
 // a K piece's workspace (q ^ 1 is the other piece of the same unit) and key
-// its ready flags.  The piece that runs later finishes the unit (fin): the
-// other publishes its partial accumulator.
+// its ready flags.  Of two unequal pieces (a stream-K share boundary, or the
+// round-robin tail without ksym) one finishes the unit (fin) and the other
+// publishes its partial accumulator; two symmetric pieces both publish and
+// each finishes one column half (ehalf).
 struct GemmItem {
   int unit, piece, sl0, sl1, q, key;   // piece = -1 for a whole unit or a column half
   int half;                            // -1, or the column half of the unit (a half-width MMA)

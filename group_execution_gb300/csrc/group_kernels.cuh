@@ -4,14 +4,18 @@
 // interpreter (InterpProg) or a straight-line program generated from the
 // group and compiled at plan-build time.
 //
-// One persistent CTA per SM slot walks 32x64 tiles of the group's frame.  A
-// producer warp streams every staged leaf's tile into a ring of shared-memory
-// stages with TMA (transposed leaves arrive as transposed boxes, so the
-// transposition costs no extra global traffic); eight consumer warps evaluate
-// the program on the tile from shared memory, eight values per thread, in
-// registers.  K1 writes the result with TMA stores; K2 folds it into per-row
-// partial sums or maxima.  No intermediate of the group ever reaches global
-// memory (TVM "Operator Fusion", FuseTIR; DisCo, Introduction, on op fusion).
+// Persistent CTAs (one per SM slot) walk 32x64 tiles of the group's frame.
+// Two producer warps, taking alternate ring stages, stream every staged
+// leaf's tile into a ring of shared-memory stages with TMA (transposed leaves
+// arrive as transposed boxes, so the transposition costs no extra global
+// traffic); eight consumer warps evaluate the program on the tile from
+// shared memory, eight values per thread, in registers.  K1 writes the
+// result with TMA stores and claims its tiles from a per-group counter; K2
+// folds it into per-row partial sums or maxima.  No intermediate of the
+// group ever reaches global memory (TVM "Operator Fusion", FuseTIR; DisCo,
+// Introduction, on op fusion).  Small groups and row reductions over
+// row-contiguous leaves run the direct kernel at the end of this file
+// instead.
 //
 // Thread layout inside a tile: lane = tile row (0..31), consumer warp w owns
 // tile columns 8w..8w+7.  Staged 2-D boxes are 128-byte swizzled so that the

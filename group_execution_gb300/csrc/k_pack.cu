@@ -4,20 +4,24 @@
 // size is the sum of theirs).
 //
 // The host splits every tensor into chunks of up to 8192 elements and uploads
-// the chunk table once.  Pack: CTAs stride over chunks; each thread issues all
-// of its loads for a full chunk (32 elements, 128 bytes) before any
-// conversion, and the next chunk's descriptor is fetched while the current
-// chunk is in flight.  A tensor's last chunk also zeroes the padding up to the
-// next aligned offset, so the buffer is fully defined.  Unpack: one CTA per SM;
-// a producer warp brings chunks of the buffer into a shared-memory ring with
-// bulk copies (rounded up to 16 bytes, which stays inside the tensor's
-// padding), four warps widen and scale them into a staging buffer, and each
-// chunk leaves as one bulk store of its 16-byte multiple plus at most three
-// plain stores.  A pack of several AllReduce buckets in one launch counts
-// every chunk for its bucket; the CTA that counts a bucket's last chunk
-// publishes the bucket as ready (a release store of the launch's sequence
-// number), so that a stream-ordered wait can start that bucket's AllReduce
-// while the rest is still being packed.
+// the chunk table once.  Pack: each CTA starts on a fixed chunk and then
+// either strides over the chunks (range packs) or claims the next one from a
+// layout counter (packs of the whole layout, bucketed or not); each thread
+// issues all of its loads for a full chunk (32 elements, 128 bytes) before
+// any conversion, and the next chunk's descriptor is fetched while the
+// current chunk is in flight.  A tensor's last chunk also zeroes the padding
+// up to the next aligned offset, so the buffer is fully defined.  Unpack: one
+// CTA per SM; a producer warp brings chunks of the buffer into a
+// shared-memory ring with bulk copies (rounded up to 16 bytes, which stays
+// inside the tensor's padding), four warps widen and scale them into a
+// staging buffer, and each chunk leaves as one bulk store of its 16-byte
+// multiple plus at most three plain stores.
+//
+// A pack of several AllReduce buckets in one launch counts every chunk it
+// writes into its bucket's count with a release reduction.  The counts are
+// never reset: the k-th launch has completed bucket b once b's count reaches
+// k times b's chunk count, so a stream-ordered wait can start that bucket's
+// AllReduce while the rest is still being packed.
 #include <cuda_bf16.h>
 
 #include <algorithm>
