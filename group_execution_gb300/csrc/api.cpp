@@ -626,10 +626,10 @@ void prepare_gemm(GroupExec& ge, const BuildOpts& o, int nsm, const Graph& g) {
   // a short-K launch better, but measured slower: each tile's fixed costs and
   // the doubled A traffic outweigh it.  224-column tiles make the rounds of a
   // 4096 x 4096 output come out even (304 tiles, 4 rounds on 76 pairs, where
-  // 256 leaves 28 tiles for a last round run in column halves) but measured
-  // slower too (K = 4096: 94.2 against 90.1 us with L2 flushed): the main
-  // loop is close to its operand feed, and 224-column tiles load about 14 %
-  // more operand bytes per flop.
+  // 256 leaves 28 tiles for a last round cut in two) but measured slower too
+  // (K = 4096: 94.2 against 90.1 us with L2 flushed, when that last round ran
+  // in column halves): the main loop is close to its operand feed, and
+  // 224-column tiles load about 14 % more operand bytes per flop.
   int TN = kGemmN;
   if (ge.compiled && tnf == 2) TN = 128;
   if (ge.compiled && tnf == 3) TN = 224;
