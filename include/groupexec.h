@@ -184,10 +184,12 @@ void fg_graph_destroy(fg_graph* g);
  * device error flag and reduce scratch when a CUDA device is present; without
  * one the plan is host-only (queries work, launches fail).  opts may be NULL
  * for the defaults.  A group the kernels cannot run (say a matmul operand
- * whose contiguous extent is not a multiple of 8) does not fail the build:
- * the plan keeps the grouping, and that group's queries (which still fill
- * their outputs) and launches return its status, FG_EUNSUPPORTED, with the
- * reason in fg_last_error. */
+ * whose contiguous extent is not a multiple of 8, or a leaf that would be
+ * gathered from a frame of 2^31 or more elements) does not fail the build:
+ * the plan keeps the grouping, and that group's fg_plan_group_info (which
+ * still fills its outputs), fg_plan_group_source and launches return its
+ * status, FG_EUNSUPPORTED, with the reason in fg_last_error; the other
+ * per-group diagnostics fill what they can and return FG_OK. */
 fg_status fg_build_groups(const fg_graph* g, const fg_build_opts* opts, fg_plan** plan);
 
 /* Node and group counts; group_of[node] = the node id of its group's sink
