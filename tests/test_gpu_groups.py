@@ -259,3 +259,24 @@ def test_small_kernel_reductions_both_paths(shape, op):
     spec.mark_output(spec.op("sigmoid", (s,)))
     for fl in (0, _lib.FG_FLAG_NO_SMALL):
         _check(spec, allow_reduce_epilogue=True, flags=fl)
+
+
+@pytest.mark.parametrize("shape", [(1, 1), (1, 3), (5, 1), (2, 1), (4096, 1), (1, 1025), (3, 2)])
+def test_degenerate_frames(shape):
+    """Single-element, single-row and single-column frames: the diamond
+    group (its transposed output of a single column is a reinterpretation,
+    so the leaves are read in place) and a row reduction with a broadcast
+    prologue and an epilogue, each through the direct kernel, the pipeline
+    and the interpreter, fused and unfused; maxima bit for bit."""
+    _check(W.diamond(*shape))
+    R, C = shape
+    for op in ("rowsum", "rowmax"):
+        spec = W.GraphSpec()
+        x = spec.input((R, C))
+        v = spec.input((C,))
+        s = spec.op(op, (spec.op("badd_col", (spec.op("relu", (x,)), v)),))
+        spec.mark_output(s)
+        plan, env, ref, _ = _check(spec)
+        if op == "rowmax":
+            assert exact_value(spec, s)
+            np.testing.assert_array_equal(env[s].cpu().numpy(), ref[s])
